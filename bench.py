@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Throughput of the tensor-parallel MLP forward + backward on GB300.
+
+One step = tp_mlp_fwd + tp_mlp_bwd of the GPT-style workload
+(X [S=2048, B=4, H=4096] bf16, W1 [16384, 4096] column-split over T=8,
+W2 [4096, 16384] row-split, GeLU-tanh, bias, residual) on seeded synthetic
+inputs.  The metric is algorithmic TFLOP/s (12*M*H*F per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the step on
+its own GPU (the library's shards all live on one GPU); the reported value is
+the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "TP-sharded MLP fwd+bwd TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas only; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value, device="cpu"):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU step
+# ---------------------------------------------------------------------------
+def kernel_flops(w):
+    """Algorithmic FLOP of one launch of each GEMM kernel for workload w."""
+    M, H, F, g = w.M, w.H, w.F, w.g
+    return {"col_fwd": 2.0 * M * H * F * g, "row_fwd": 2.0 * M * F * H, "row_dgrad_act": 2.0 * M * H * F,
+            "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H}
+
+
+def run_gpu(args, w, dist, rank, local, ws):
+    import torch
+
+    import tensor_transformer_mlp_shard_gb300 as tp
+    from tensor_transformer_mlp_shard_gb300 import build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bf = torch.bfloat16
+    T, M, H, F, g = w.T, w.M, w.H, w.F, w.g
+    Fs = F // T
+    lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
+                   residual=w.residual, seq_parallel=w.seq_parallel)
+    full = synth.mlp_tensors(w)
+    td = bf if w.dtype == "bf16" else torch.float32
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=td)
+
+    # shards: W1 rows (gate/up stacked per shard for SwiGLU), W2 columns
+    if w.act == "swiglu":
+        W1 = [up(np.concatenate([full["W1"][i * Fs:(i + 1) * Fs], full["W1"][F + i * Fs:F + (i + 1) * Fs]]))
+              for i in range(T)]
+    else:
+        W1 = [up(full["W1"][i * Fs:(i + 1) * Fs]) for i in range(T)]
+    W2 = [up(full["W2"][:, i * Fs:(i + 1) * Fs]) for i in range(T)]
+    if not w.has_bias:
+        b1 = None
+    elif w.act == "swiglu":
+        b1 = [up(np.concatenate([full["b1"][i * Fs:(i + 1) * Fs], full["b1"][F + i * Fs:F + (i + 1) * Fs]]))
+              for i in range(T)]
+    else:
+        b1 = [up(full["b1"][i * Fs:(i + 1) * Fs]) for i in range(T)]
+    b2 = up(full["b2"]) if w.has_bias else None
+    rows = lay.xrows
+    X = [up(full["X"][j * rows:(j + 1) * rows]) for j in range(lay.nx)]
+    dY = [up(full["dY"][j * rows:(j + 1) * rows]) for j in range(lay.nx)]
+    Y = [torch.empty(rows, H, dtype=td, device=dev) for _ in range(lay.nx)]
+    dX = [torch.empty(rows, H, dtype=td, device=dev) for _ in range(lay.nx)]
+    pre = [torch.empty(M, g * Fs, dtype=td, device=dev) for _ in range(T)]
+    A = [torch.empty(M, Fs, dtype=td, device=dev) for _ in range(T)]
+    f32 = torch.float32
+    dW1 = [torch.empty(g * Fs, H, dtype=f32, device=dev) for _ in range(T)]
+    dW2 = [torch.empty(H, Fs, dtype=f32, device=dev) for _ in range(T)]
+    db1 = [torch.empty(g * Fs, dtype=f32, device=dev) for _ in range(T)] if w.has_bias else None
+    db2 = torch.empty(H, dtype=f32, device=dev) if w.has_bias else None
+    wsp = tp.alloc_workspace(lay.workspace_bytes(), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream)
+        lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
+
+    # ---- device-resident timing --------------------------------------------
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if tp.sync_status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    tp.prof_enable(True)
+    tp.prof_collect()  # drop warm-up records
+    n0 = tp.launch_count()
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    ms = e0.elapsed_time(e1)
+    launches = tp.launch_count() - n0
+    kernels = tp.prof_collect()
+    tp.prof_enable(False)
+    clk = clocks.stop()
+    status = tp.sync_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {tp.status_str(status)} in timed region")
+    ms_max = max_over_ranks(dist, ms, dev)
+    flops_step = w.flops()
+    value = ws * flops_step * args.steps / (ms_max * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers ---------------------
+    hX = [x.cpu().pin_memory() for x in X]
+    hdY = [d.cpu().pin_memory() for d in dY]
+    hY = [torch.empty(rows, H, dtype=td).pin_memory() for _ in range(lay.nx)]
+    h2d = sum(t.numel() * t.element_size() for t in hX + hdY)
+    d2h = sum(t.numel() * t.element_size() for t in hY)
+
+    def e2e_step():
+        for d, h in zip(X, hX):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(dY, hdY):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(hY, Y):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(dist, e2.elapsed_time(e3), dev)
+    e2e_value = ws * flops_step * args.steps / (ms_e2e * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel -----------------------------------
+    peaks = load_peaks()
+    kf = kernel_flops(w)
+    per_kernel = {}
+    for name, (n, tot) in kernels.items():
+        avg = tot / max(1, n)
+        ent = {"launches": n, "avg_ms": round(avg, 4), "share": None}
+        if name in kf and avg > 0:
+            ent["tflops"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+        per_kernel[name] = ent
+    tot_all = sum(t for _, t in kernels.values()) or 1.0
+    for name, (n, tot) in kernels.items():
+        per_kernel[name]["share"] = round(tot / tot_all, 4)
+    gemms = {k: v for k, v in kernels.items() if k in kf}
+    dom = max(gemms, key=lambda k: gemms[k][1]) if gemms else None
+    roofline = None
+    if dom:
+        n, tot = kernels[dom]
+        achieved = kf[dom] / ((tot / n) * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak_kind": f"bf16 sustained ({peaks['source']})",
+                    "algorithmic_flop_per_launch": kf[dom]}
+    step_frac = value / ws / peaks["bf16_tflops_sustained"]
+    return {
+        "value": round(value, 2), "ms_per_step": round(ms_max / args.steps, 4),
+        "pct_of_dense_bf16_peak": round(100 * step_frac, 2),
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches, "roofline": roofline, "kernels": per_kernel, "clocks": clk,
+        "peaks": peaks,
+    }
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, tokens, full=None):
+    """Time the fp64 oracle's fwd+bwd on the first `tokens` tokens of the
+    workload with the full weights; returns (seconds, algorithmic FLOP)."""
+    import oracle
+    if full is None:
+        full = synth.mlp_tensors(w, M=tokens)
+    W1s = oracle.shard_column_weight(full["W1"], w.T, w.act)
+    b1s = oracle.shard_column_bias(full["b1"], w.T, w.act) if w.has_bias else None
+    W2s = oracle.shard_row_weight(full["W2"], w.T)
+    X, dY = full["X"][:tokens], full["dY"][:tokens]
+    t0 = time.perf_counter()
+    pre, A, _ = oracle.mlp_fwd(X, W1s, b1s, W2s, full["b2"], w.act, w.residual)
+    oracle.mlp_bwd(dY, X, W1s, W2s, pre, A, w.act, w.residual)
+    dt = time.perf_counter() - t0
+    flops = 3.0 * (2.0 * tokens * w.H * w.F * w.g + 2.0 * tokens * w.F * w.H)
+    return dt, flops
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w, rank):
+    # per-step sample sized so that warm-up + timed steps take ~2 minutes
+    probe_tokens = 64
+    full = synth.mlp_tensors(w, M=2048)
+    dt, fl = oracle_sample(w, probe_tokens, full)
+    rate = fl / dt
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_token = 3.0 * (2.0 * w.H * w.F * w.g + 2.0 * w.F * w.H)
+    tokens = int(max(64, min(2048, budget * rate / per_token)))
+    for _ in range(args.warmup):
+        oracle_sample(w, tokens, full)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(w, tokens, full)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = f"first {tokens} of {w.M} tokens per step, full weights, fp64 numpy"
+    return {"value": round(value, 5), "ms_per_step": round(1e3 * tot_t / args.steps, 2),
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def cpu_baseline(w):
+    tokens = 1024
+    full = synth.mlp_tensors(w, M=tokens)
+    dt, fl = oracle_sample(w, tokens, full)
+    return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle fwd+bwd on the first {tokens} of {w.M} tokens with the full weights "
+                      f"({fl / 1e9:.0f} GFLOP, {dt:.1f} s)"}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    if w.kind != "mlp":
+        raise SystemExit("bench.py times the MLP workloads (gpt, swiglu, sp, tiny)")
+    ws, rank, local = dist_env()
+    config = {"workload": f"{w.name}: X [S={w.S},B={w.B},H={w.H}] {w.dtype}, F={w.F}, T={w.T}, {w.act}"
+                          f"{', bias' if w.has_bias else ''}{', residual' if w.residual else ''}"
+                          f"{', sequence-parallel' if w.seq_parallel else ''}",
+              "S": w.S, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "act": w.act, "global_batch": w.B * ws,
+              "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
+              "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)"}
+    base = {"metric": METRIC, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded SplitMix64 + Box-Muller), random-init weights", "config": config}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        out = dict(base)
+        out["impl"] = "reference"
+        out["n_gpus"] = 1
+        out["dtype"] = "f64"
+        out.update(run_reference(args, w, rank))
+        print(json.dumps(out))
+        return
+
+    import torch
+    dist = dist_init(ws, "nccl" if torch.cuda.is_available() else "gloo")
+    res = run_gpu(args, w, dist, rank, local, ws)
+    if rank == 0:
+        out = dict(base)
+        out.update(res)
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * tp_mlp.h -- C ABI of the single-GPU tensor-parallel MLP library (libtpmlp.so).
+ *
+ * What it computes.  The Megatron tensor-parallel MLP: a ColumnParallelLinear,
+ * an activation, then a RowParallelLinear ("Megatron-LM 源码精读", s3.1-s3.3
+ * and the s3.3 figure; the gitcode.csdn.net walk-through, s02).  All T shards
+ * live in one GPU's memory, each shard in its own buffer.  The two all-reduces
+ * of the multi-GPU layer become fp32 sums over shards inside one kernel:
+ *   forward  (row layer):    Y  = sum_i A_i W2_i^T + b2 [+ X]
+ *   backward (column layer): dX = sum_i dPre_i W1_i     [+ dY]
+ * The sequence-parallel variant ("Megatron-LM 源码精读" s3.5; walk-through s06)
+ * stores X, Y, dY and dX as T token shards of [S/T, B, H]; the all-gather and
+ * reduce-scatter become shard-indexed loads and stores.
+ *
+ * Conventions used by every entry point.
+ *   Tokens.  M = S*B tokens; activations are row-major [S, B, width], i.e. a
+ *     [M, width] matrix with token m = s*B + b.
+ *   Weights.  PyTorch [out, in] layout; a linear layer computes X W^T
+ *     ("Megatron-LM 源码精读" s3.1: weight shape [out_per_part, in]).
+ *   Shards.  g = 2 for SwiGLU, else 1; Fs = F/T.
+ *     W1_i : [g*Fs, H]   column shard i (SwiGLU: Fs gate rows, then Fs up rows)
+ *     b1_i : [g*Fs]      sharded with W1 (same stacking)
+ *     W2_i : [H, Fs]     row shard i = columns [i*Fs, (i+1)*Fs) of W2
+ *     b2   : [H]         replicated, added once after the shard sum
+ *     pre_i: [M, g*Fs]   pre-activation of shard i (kept for the backward)
+ *     A_i  : [M, Fs]     activation of shard i (input of row shard i)
+ *   Pointer arrays.  Arguments typed `const void* const*` are host arrays of
+ *     device pointers, one per shard (T entries) or, for activations under
+ *     sequence parallelism, one per token shard (T entries of [M/T, width]);
+ *     without sequence parallelism activations take a 1-entry array.
+ *   Element types.  dtype TP_DT_BF16: every activation, weight, bias and
+ *     activation gradient is bf16; weight and bias gradients (dW*, db*) are
+ *     fp32.  dtype TP_DT_F32: everything is fp32.  Products accumulate in fp32.
+ *   Alignment.  Every device pointer is 16-byte aligned; H, F/T and (for the
+ *     row layer input) the shard width are multiples of 8.
+ *   Ownership.  The caller owns every device buffer, including the workspace.
+ *     The library keeps host state only (the handle); it allocates no device
+ *     memory in any entry point below.
+ *   Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *     Every compute entry point only enqueues work: no host synchronisation.
+ *   Errors.  Argument and shape errors return before anything is enqueued.
+ *     Launch failures return TP_ERR_CUDA.  A kernel whose internal wait
+ *     exceeds the wait limit records TP_ERR_TIMEOUT in a device status word
+ *     and returns early; tp_sync_status() reports (and clears) it.
+ *     tp_last_error() gives a message for the last failing call of the
+ *     calling thread.
+ */
+#ifndef TP_MLP_H
+#define TP_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#define TP_MLP_ABI_VERSION 1
+#define TP_MAX_SHARDS 16
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_ARG = 1,          /* null/misaligned pointer, bad enum, bad workspace */
+    TP_ERR_SHAPE = 2,        /* F % T, S % T under SP, width % 8, T range, ... */
+    TP_ERR_UNSUPPORTED = 3,  /* valid request this library does not implement */
+    TP_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    TP_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (device status) */
+} tp_status;
+
+typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act;
+typedef enum { TP_DT_F32 = 0, TP_DT_BF16 = 1 } tp_dtype;
+
+/* Problem description shared by the MLP and the single-layer entry points.
+ * For the single layers, H is the replicated width (column input, row output)
+ * and F the split width (column output, row input) before sharding. */
+typedef struct {
+    int S, B;              /* sequence length and micro-batch: M = S*B tokens */
+    int H;                 /* hidden (replicated) width */
+    int F;                 /* FFN (split) width, divisible by T */
+    int T;                 /* tensor-parallel size, 1..TP_MAX_SHARDS */
+    int act;               /* tp_act (column layer) */
+    int dtype;             /* tp_dtype */
+    int has_bias;          /* b1/b2 present (column/row bias) */
+    int residual;          /* row output adds a residual: MLP Y = X + MLP(X) */
+    int seq_parallel;      /* activations stored as T token shards */
+    int wgrad_accumulate;  /* dW += instead of dW = (gradient-accumulation fusion) */
+} tp_mlp_desc;
+
+typedef struct tp_mlp tp_mlp; /* opaque handle: validated descriptor */
+
+/* ---- handle ------------------------------------------------------------ */
+
+/* Validate `desc` and create a handle.  Host only: no CUDA call.
+ * Returns TP_ERR_SHAPE for F % T != 0, T outside 1..TP_MAX_SHARDS, widths not
+ * multiples of 8, S % T != 0 under sequence parallelism (bf16 additionally
+ * needs M/T % 128 == 0 under sequence parallelism); TP_ERR_ARG for bad
+ * enums, flags other than 0/1 or a null pointer. */
+TP_API tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out);
+TP_API void tp_mlp_destroy(tp_mlp *h);
+
+/* Bytes of device workspace tp_mlp_bwd needs (256-byte aligned start).  It
+ * holds dPre_i (M x g*Fs per shard, in dtype) and fp32 partial column sums for
+ * the bias gradients. */
+TP_API size_t tp_mlp_workspace_bytes(const tp_mlp *h);
+
+/* ---- MLP forward ("Megatron-LM 源码精读" s3.3 figure) ------------------------
+ * X   : 1 pointer [M, H], or T token shards [M/T, H] under seq_parallel
+ * W1  : T pointers [g*Fs, H];  b1: T pointers [g*Fs] or NULL (has_bias = 0)
+ * W2  : T pointers [H, Fs];    b2: [H] or NULL
+ * Y   : 1 pointer [M, H], or T token shards [M/T, H] under seq_parallel
+ * pre : T pointers [M, g*Fs]; may be NULL when act = TP_ACT_NONE
+ * A   : T pointers [M, Fs]
+ * Computes pre_i = X W1_i^T + b1_i, A_i = act(pre_i) (no reduction), then
+ * Y = sum_{i=0}^{T-1} A_i W2_i^T + b2 (+ X if residual) with the sum in fp32
+ * inside one kernel, in shard order. */
+TP_API tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1,
+                     const void *const *b1, const void *const *W2, const void *b2,
+                     void *const *Y, void *const *pre, void *const *A, void *stream);
+
+/* ---- MLP backward ------------------------------------------------------------
+ * dY  : like Y;  X, W1, W2, pre, A: as passed to / produced by tp_mlp_fwd
+ * dX  : like X (bf16/f32 per dtype)
+ * dW1 : T pointers [g*Fs, H] fp32;  db1: T pointers [g*Fs] fp32 or NULL
+ * dW2 : T pointers [H, Fs] fp32;    db2: [H] fp32 or NULL
+ * workspace: >= tp_mlp_workspace_bytes(h) bytes of device memory, 256-byte
+ *   aligned; contents on entry are ignored and on return are undefined.
+ * Computes dA_i = dY W2_i and dPre_i = dA_i (.) act'(pre_i) (no reduction:
+ * the row layer's backward has no communication, s3.2), dW2_i = dY^T A_i,
+ * db2 = sum_m dY, dW1_i = dPre_i^T X, db1_i = sum_m dPre_i and
+ * dX = sum_i dPre_i W1_i (+ dY if residual) in fp32 inside one kernel.
+ * With wgrad_accumulate the weight gradients are added to dW1/dW2 (bias
+ * gradients are always overwritten). */
+TP_API tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X,
+                     const void *const *W1, const void *const *W2,
+                     const void *const *pre, const void *const *A,
+                     void *const *dX, void *const *dW1, void *const *db1,
+                     void *const *dW2, void *db2, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* ---- single layers ("Megatron-LM 源码精读" s3.1, s3.2; walk-through s02) ------
+ * tp_linear_col: out_i = act(X W_i^T + b_i) for every shard, no reduction.
+ *   X: like tp_mlp_fwd's X; W: T x [g*Fs, H]; b: T x [g*Fs] or NULL;
+ *   out: T x [M, Fs]; pre: T x [M, g*Fs] or NULL (not stored). */
+TP_API tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X,
+                        const void *const *W, const void *const *b,
+                        void *const *out, void *const *pre, void *stream);
+
+/* tp_linear_row: Y = sum_i X_i W_i^T + b (+ R), the sum over shards in fp32
+ *   inside one kernel.  X: T x [M, Fs]; W: T x [H, Fs]; b: [H] or NULL;
+ *   R: like Y, or NULL (required iff desc->residual); Y: 1 x [M, H] or T token
+ *   shards under seq_parallel.  desc->act is ignored. */
+TP_API tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X,
+                        const void *const *W, const void *b,
+                        const void *const *R, void *const *Y, void *stream);
+
+/* Workspace bytes for tp_linear_col_bwd / tp_linear_row_bwd (bias partials). */
+TP_API size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc);
+
+/* tp_linear_col_bwd: gradients of tp_linear_col with act = TP_ACT_NONE
+ *   (TP_ERR_UNSUPPORTED otherwise; the fused activation backward belongs to
+ *   tp_mlp_bwd).  dOut: T x [M, Fs]; X, W as in the forward;
+ *   dX = sum_i dOut_i W_i (fp32 sum over shards in one kernel), stored like X;
+ *   dW_i = dOut_i^T X (fp32, T x [Fs, H]); db_i = sum_m dOut_i (fp32) or NULL. */
+TP_API tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut,
+                            const void *const *X, const void *const *W,
+                            void *const *dX, void *const *dW, void *const *db,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* tp_linear_row_bwd: gradients of tp_linear_row (no reduction over shards).
+ *   dY: like Y; X, W as in the forward; dX_i = dY W_i (T x [M, Fs]);
+ *   dW_i = dY^T X_i (fp32, T x [H, Fs]); db = sum_m dY (fp32 [H]) or NULL.
+ *   The residual's gradient is dY itself and is not materialised. */
+TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY,
+                            const void *const *X, const void *const *W,
+                            void *const *dX, void *const *dW, void *db,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---- status, limits, diagnostics ---------------------------------------- */
+
+/* Synchronise `stream`, then read and clear the device status word.  Returns
+ * TP_OK, TP_ERR_TIMEOUT (a bounded wait ran out) or TP_ERR_CUDA. */
+TP_API tp_status tp_sync_status(void *stream);
+
+/* Wall-clock bound of every in-kernel wait, in nanoseconds (default 4e9).
+ * Applies to launches made after the call. */
+TP_API void tp_set_wait_limit_ns(uint64_t ns);
+
+/* Launch a kernel that waits for a device flag nothing ever sets, bounded by
+ * limit_ns; it records TP_ERR_TIMEOUT in the status word and returns.  Used
+ * to test the failure path without faulting or hanging the GPU. */
+TP_API tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Number of kernels this library has launched since load. */
+TP_API uint64_t tp_launch_count(void);
+
+/* Per-kernel timing ("timers"): when enabled, every launch is bracketed by
+ * CUDA events recorded on its own stream.  tp_prof_collect synchronises the
+ * recorded events and returns, per kernel name, launches and total device
+ * milliseconds; it then clears the records.  Returns the number of entries
+ * written (<= max_entries) or -1 on error. */
+typedef struct {
+    char name[48];
+    int launches;
+    double total_ms;
+} tp_prof_entry;
+TP_API void tp_prof_enable(int on);
+TP_API int tp_prof_collect(tp_prof_entry *entries, int max_entries);
+
+TP_API const char *tp_status_str(tp_status s);
+TP_API const char *tp_last_error(void);
+TP_API int tp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TP_MLP_H */

@@ -1,0 +1,11 @@
+"""Single-GPU tensor-parallel MLP for GB300 (sm_103a).
+
+The Megatron ColumnParallelLinear -> activation -> RowParallelLinear block with
+all T shards in one GPU's memory; the cross-shard all-reduces are fp32 sums
+inside the tcgen05 GEMM kernels of ``libtpmlp.so`` (C ABI in
+``include/tp_mlp.h``).  This package is the thin Python binding.
+"""
+from .binding import (ACT, DTYPE, Layout, TPMLP, TpError, alloc_workspace, debug_wait_timeout,  # noqa: F401
+                      launch_count, lib, library_path, linear_col, linear_col_bwd, linear_row, linear_row_bwd,
+                      linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_wait_limit_ns, status_str,
+                      sync_status)

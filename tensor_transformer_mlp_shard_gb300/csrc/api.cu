@@ -1,0 +1,649 @@
+// C-ABI of libtpmlp: argument validation, the GEMM plans of every
+// tensor-parallel product, dispatch to the bf16 (tcgen05) or fp32 (SIMT)
+// engine, device status, launch accounting and per-kernel timing.
+//
+// Mapping from the multi-GPU layers to single-GPU plans ("Megatron-LM 源码精读"
+// s3.1-s3.5):
+//   ColumnParallelLinear forward: T independent problems (no communication);
+//   RowParallelLinear forward:    one problem whose K loop runs over the T
+//                                 shards (the all-reduce as an fp32 sum);
+//   ColumnParallelLinear dgrad:   the same K loop over shards (the backward
+//                                 all-reduce);
+//   RowParallelLinear dgrad:      T independent problems;
+//   sequence parallelism:         token-sharded buffers selected per row
+//                                 (all-gather / reduce-scatter as addressing).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+struct tp_mlp {
+    tp_mlp_desc d;
+};
+
+namespace tpmlp {
+
+tp_status read_and_clear_status(cudaStream_t st, int *out);
+tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+static thread_local char g_err[512] = "";
+
+tp_status set_error(tp_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+tp_status cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return TP_OK;
+    return set_error(TP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------
+// runtime state
+// ---------------------------------------------------------------------------
+static std::atomic<uint64_t> g_launches{0};
+static std::atomic<unsigned> g_launch_id{0};
+static std::atomic<uint64_t> g_wait_limit{4000000000ull};
+
+uint64_t wait_limit_ns() { return g_wait_limit.load(); }
+
+unsigned next_launch_id() {
+    unsigned id = ++g_launch_id;
+    if (id == 0) id = ++g_launch_id;  // 0 never names a launch
+    return id;
+}
+
+int num_sms() {
+    static int cache[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int &c = cache[dev % 64];
+    if (c == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        c = n;
+    }
+    return c;
+}
+
+// per-kernel timing
+struct ProfRec {
+    std::string name;
+    cudaEvent_t a, b;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRec> g_prof_recs;
+static std::vector<cudaEvent_t> g_event_pool;
+static thread_local cudaEvent_t g_pending = nullptr;
+
+static cudaEvent_t get_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void launch_begin(const char *name, cudaStream_t st) {
+    (void)name;
+    g_launches.fetch_add(1);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_pending = nullptr;
+    if (!g_prof_on) return;
+    cudaEvent_t e = get_event();
+    if (e && cudaEventRecord(e, st) == cudaSuccess) g_pending = e;
+}
+
+void launch_end(const char *name, cudaStream_t st) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof_on || !g_pending) return;
+    cudaEvent_t e = get_event();
+    if (e && cudaEventRecord(e, st) == cudaSuccess) g_prof_recs.push_back({name, g_pending, e});
+    g_pending = nullptr;
+}
+
+// ---------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static tp_status check_array(const void *const *arr, int n, const char *name) {
+    if (!arr) return set_error(TP_ERR_ARG, "%s: pointer array is NULL", name);
+    for (int i = 0; i < n; ++i) {
+        if (!arr[i]) return set_error(TP_ERR_ARG, "%s[%d] is NULL", name, i);
+        if (!aligned16(arr[i])) return set_error(TP_ERR_ARG, "%s[%d] is not 16-byte aligned", name, i);
+    }
+    return TP_OK;
+}
+
+static tp_status check_one(const void *p, const char *name) {
+    if (!p) return set_error(TP_ERR_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return set_error(TP_ERR_ARG, "%s is not 16-byte aligned", name);
+    return TP_OK;
+}
+
+#define TRY(x)                        \
+    do {                              \
+        tp_status _s = (x);           \
+        if (_s != TP_OK) return _s;   \
+    } while (0)
+
+static tp_status validate_desc(const tp_mlp_desc *d) {
+    if (!d) return set_error(TP_ERR_ARG, "descriptor is NULL");
+    if (d->act < TP_ACT_NONE || d->act > TP_ACT_SWIGLU) return set_error(TP_ERR_ARG, "bad act %d", d->act);
+    if (d->dtype != TP_DT_F32 && d->dtype != TP_DT_BF16) return set_error(TP_ERR_ARG, "bad dtype %d", d->dtype);
+    const int flags[4] = {d->has_bias, d->residual, d->seq_parallel, d->wgrad_accumulate};
+    for (int f : flags)
+        if (f != 0 && f != 1) return set_error(TP_ERR_ARG, "boolean flags must be 0 or 1");
+    if (d->T < 1 || d->T > TP_MAX_SHARDS)
+        return set_error(TP_ERR_SHAPE, "T=%d outside 1..%d", d->T, TP_MAX_SHARDS);
+    if (d->S < 0 || d->B < 0) return set_error(TP_ERR_SHAPE, "negative S or B");
+    const long long M = static_cast<long long>(d->S) * d->B;
+    if (M > (1ll << 24)) return set_error(TP_ERR_SHAPE, "M = S*B = %lld exceeds 2^24 tokens", M);
+    if (d->H < 8 || d->H % 8) return set_error(TP_ERR_SHAPE, "H=%d must be a positive multiple of 8", d->H);
+    if (d->F < 1 || d->F % d->T)
+        return set_error(TP_ERR_SHAPE, "F=%d is not divisible by T=%d (divide(output_size, world_size))", d->F,
+                         d->T);
+    const int Fs = d->F / d->T;
+    if (Fs % 8) return set_error(TP_ERR_SHAPE, "F/T=%d must be a multiple of 8", Fs);
+    if (d->H > (1 << 20) || Fs > (1 << 20)) return set_error(TP_ERR_SHAPE, "width above 2^20");
+    if (d->seq_parallel) {
+        if (d->S % d->T) return set_error(TP_ERR_SHAPE, "sequence parallel needs S %% T == 0 (S=%d, T=%d)", d->S, d->T);
+        if (d->dtype == TP_DT_BF16 && M > 0 && (M / d->T) % 128)
+            return set_error(TP_ERR_SHAPE, "bf16 sequence parallel needs M/T %% 128 == 0 (M/T=%lld)", M / d->T);
+    }
+    return TP_OK;
+}
+
+struct Dims {
+    int M, H, Fs, T, g, nx, rs;
+    size_t es;
+};
+
+static Dims dims_of(const tp_mlp_desc *d) {
+    Dims x;
+    x.M = d->S * d->B;
+    x.H = d->H;
+    x.T = d->T;
+    x.Fs = d->F / d->T;
+    x.g = d->act == TP_ACT_SWIGLU ? 2 : 1;
+    x.nx = d->seq_parallel ? d->T : 1;
+    x.rs = d->seq_parallel ? x.M / d->T : 0;
+    x.es = d->dtype == TP_DT_BF16 ? 2 : 4;
+    return x;
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static tp_status run_gemm(const GemmPlan &g, int dtype, cudaStream_t st) {
+    return dtype == TP_DT_BF16 ? launch_tc_gemm(g, st) : launch_simt_gemm(g, st);
+}
+
+// plan helpers --------------------------------------------------------------
+static void set_operand(OperandPlan &o, const void *const *ptrs, int n, int rows, int cols, bool mn, int p_stride,
+                        int s_stride, int rows_split) {
+    for (int i = 0; i < kMaxShards; ++i) o.ptr[i] = i < n ? ptrs[i] : nullptr;
+    o.n = n;
+    o.rows = rows;
+    o.cols = cols;
+    o.mn_major = mn;
+    o.p_stride = p_stride;
+    o.s_stride = s_stride;
+    o.rows_split = rows_split;
+}
+
+static void set_out(OutPlan &o, const void *const *ptrs, int n, int p_stride, int rows_split, long long ld) {
+    for (int i = 0; i < kMaxShards; ++i) o.ptr[i] = i < n ? const_cast<void *>(ptrs[i]) : nullptr;
+    o.n = n;
+    o.p_stride = p_stride;
+    o.rows_split = rows_split;
+    o.ld = ld;
+}
+
+static void set_bias(GemmPlan &g, const void *const *b, int n, int p_stride) {
+    g.has_bias = b != nullptr;
+    for (int i = 0; i < kMaxShards; ++i) g.bias[i] = (b && i < n) ? b[i] : nullptr;
+    g.bias_p_stride = p_stride;
+}
+
+// Column forward: out_i = act(X W_i^T + b_i), i < T (no reduction).
+static tp_status column_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W,
+                            const void *const *b, void *const *out, void *const *pre, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    GemmPlan g;
+    g.name = "col_fwd";
+    g.kind = EPI_COL;
+    g.act = d->act;
+    g.M = x.M;
+    g.N = x.Fs;
+    g.P = x.T;
+    g.S = 1;
+    g.Kseg = x.H;
+    set_operand(g.A, X, x.nx, x.rs ? x.rs : x.M, x.H, false, 0, 0, x.rs);
+    set_operand(g.B, W, x.T, x.g * x.Fs, x.H, false, 1, 0, 0);
+    g.b_dual_off = d->act == TP_ACT_SWIGLU ? x.Fs : 0;
+    set_out(g.out, reinterpret_cast<const void *const *>(out), x.T, 1, 0, x.Fs);
+    if (pre) set_out(g.out2, reinterpret_cast<const void *const *>(pre), x.T, 1, 0, (long long)x.g * x.Fs);
+    set_bias(g, d->has_bias ? b : nullptr, x.T, 1);
+    return run_gemm(g, d->dtype, st);
+}
+
+// Row forward: Y = sum_i X_i W_i^T + b (+R); the K loop runs over shards.
+static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void *const *W, const void *b,
+                         const void *const *R, void *const *Y, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    GemmPlan g;
+    g.name = "row_fwd";
+    g.kind = EPI_PLAIN;
+    g.M = x.M;
+    g.N = x.H;
+    g.P = 1;
+    g.S = x.T;
+    g.Kseg = x.Fs;
+    set_operand(g.A, Xs, x.T, x.M, x.Fs, false, 0, 1, 0);
+    set_operand(g.B, W, x.T, x.H, x.Fs, false, 0, 1, 0);
+    set_out(g.out, reinterpret_cast<const void *const *>(Y), x.nx, 0, x.rs, x.H);
+    if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
+    const void *bb[1] = {b};
+    set_bias(g, (d->has_bias && b) ? bb : nullptr, 1, 0);
+    return run_gemm(g, d->dtype, st);
+}
+
+// Row-layer dgrad: dOut_i = (dY W_i) [* act'(pre_i)], i < T (no reduction).
+static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY, const void *const *W,
+                           const void *const *pre, void *const *dOut, long long ld_out, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    GemmPlan g;
+    g.name = act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
+    g.kind = act == TP_ACT_NONE ? EPI_PLAIN : EPI_DACT;
+    g.act = act;
+    g.M = x.M;
+    g.N = x.Fs;
+    g.P = x.T;
+    g.S = 1;
+    g.Kseg = x.H;
+    set_operand(g.A, dY, x.nx, x.rs ? x.rs : x.M, x.H, false, 0, 0, x.rs);
+    set_operand(g.B, W, x.T, x.H, x.Fs, true, 1, 0, 0);
+    set_out(g.out, reinterpret_cast<const void *const *>(dOut), x.T, 1, 0, ld_out);
+    if (act != TP_ACT_NONE) set_out(g.aux, pre, x.T, 1, 0, ld_out);
+    return run_gemm(g, d->dtype, st);
+}
+
+// Weight gradient dW_i = G_i^T Act_i over all tokens (fp32).  G has width
+// gw (the output side of the layer), Act width aw; either may be token-sharded
+// (1 buffer or nx buffers) or per shard (T buffers).
+static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const *G, int g_per_shard, int gw,
+                       const void *const *Act, int a_per_shard, int aw, void *const *dW, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    GemmPlan g;
+    g.name = name;
+    g.kind = EPI_F32;
+    g.M = gw;
+    g.N = aw;
+    g.P = x.T;
+    g.S = 1;
+    g.Kseg = x.M;
+    if (g_per_shard)
+        set_operand(g.A, G, x.T, x.M, gw, true, 1, 0, 0);
+    else
+        set_operand(g.A, G, x.nx, x.rs ? x.rs : x.M, gw, true, 0, 0, x.rs);
+    if (a_per_shard)
+        set_operand(g.B, Act, x.T, x.M, aw, true, 1, 0, 0);
+    else
+        set_operand(g.B, Act, x.nx, x.rs ? x.rs : x.M, aw, true, 0, 0, x.rs);
+    set_out(g.out, reinterpret_cast<const void *const *>(dW), x.T, 1, 0, aw);
+    g.accumulate = d->wgrad_accumulate != 0;
+    return run_gemm(g, d->dtype, st);
+}
+
+// Column-layer dgrad: dX = sum_i dOut_i W_i (+R); the K loop runs over shards.
+static tp_status column_dgrad(const tp_mlp_desc *d, const void *const *dOut, int kw, const void *const *W,
+                              const void *const *R, void *const *dX, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    GemmPlan g;
+    g.name = "col_dgrad";
+    g.kind = EPI_PLAIN;
+    g.M = x.M;
+    g.N = x.H;
+    g.P = 1;
+    g.S = x.T;
+    g.Kseg = kw;
+    set_operand(g.A, dOut, x.T, x.M, kw, false, 0, 1, 0);
+    set_operand(g.B, W, x.T, kw, x.H, true, 0, 1, 0);
+    set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
+    if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
+    set_bias(g, nullptr, 0, 0);
+    return run_gemm(g, d->dtype, st);
+}
+
+static tp_status colsum(const tp_mlp_desc *d, const char *name, const void *const *in, int n_in, int p_stride,
+                        int rows_split, int P, int N, void *const *out, float *partials, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    ColsumPlan c;
+    c.name = name;
+    set_out(c.in, in, n_in, p_stride, rows_split, N);
+    c.P = P;
+    c.M = x.M;
+    c.N = N;
+    for (int i = 0; i < kMaxShards; ++i) c.out[i] = i < P ? static_cast<float *>(out[i]) : nullptr;
+    c.partials = partials;
+    return launch_colsum(c, d->dtype, st);
+}
+
+static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
+    const Dims x = dims_of(d);
+    return align256(sizeof(float) * static_cast<size_t>(P) * colsum_chunks(x.M) * N);
+}
+
+static size_t mlp_ws_layout(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
+    const Dims x = dims_of(d);
+    const size_t shard = align256(static_cast<size_t>(x.M) * x.g * x.Fs * x.es);
+    if (dpre_shard_bytes) *dpre_shard_bytes = shard;
+    size_t part = 0;
+    if (d->has_bias) {
+        size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
+        part = a > b ? a : b;
+    }
+    return shard * x.T + part;
+}
+
+static tp_status zero_grads(const tp_mlp_desc *d, void *const *dW, int nW, size_t wbytes, void *const *db, int ndb,
+                            size_t dbbytes, cudaStream_t st) {
+    if (!d->wgrad_accumulate)
+        for (int i = 0; i < nW; ++i) TRY(cuda_check(cudaMemsetAsync(dW[i], 0, wbytes, st), "cudaMemsetAsync(dW)"));
+    if (db)
+        for (int i = 0; i < ndb; ++i) TRY(cuda_check(cudaMemsetAsync(db[i], 0, dbbytes, st), "cudaMemsetAsync(db)"));
+    return TP_OK;
+}
+
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+// ---------------------------------------------------------------------------
+// exported C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int tp_abi_version(void) { return TP_MLP_ABI_VERSION; }
+
+const char *tp_status_str(tp_status s) {
+    switch (s) {
+        case TP_OK: return "TP_OK";
+        case TP_ERR_ARG: return "TP_ERR_ARG";
+        case TP_ERR_SHAPE: return "TP_ERR_SHAPE";
+        case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+        case TP_ERR_CUDA: return "TP_ERR_CUDA";
+        case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    }
+    return "TP_ERR_UNKNOWN";
+}
+
+const char *tp_last_error(void) { return g_err; }
+
+tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out) {
+    if (!out) return set_error(TP_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    TRY(validate_desc(desc));
+    tp_mlp *h = new (std::nothrow) tp_mlp;
+    if (!h) return set_error(TP_ERR_ARG, "out of host memory");
+    h->d = *desc;
+    *out = h;
+    return TP_OK;
+}
+
+void tp_mlp_destroy(tp_mlp *h) { delete h; }
+
+size_t tp_mlp_workspace_bytes(const tp_mlp *h) { return h ? mlp_ws_layout(&h->d, nullptr) : 0; }
+
+tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                     const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                     void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->d;
+    const Dims x = dims_of(d);
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (d->has_bias) {
+        TRY(check_array(b1, x.T, "b1"));
+        TRY(check_one(b2, "b2"));
+    }
+    if (x.M == 0) return TP_OK;  // no tokens: activation buffers may be empty (NULL)
+    TRY(check_array(X, x.nx, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
+    TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
+    if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));
+    return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr,
+                   d->residual ? X : nullptr, Y, st);
+}
+
+tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, const void *const *W1,
+                     const void *const *W2, const void *const *pre, const void *const *A, void *const *dX,
+                     void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->d;
+    const Dims x = dims_of(d);
+    const int gw = x.g * x.Fs;
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (x.M > 0) {  // no tokens: activation buffers may be empty (NULL)
+        TRY(check_array(dY, x.nx, "dY"));
+        TRY(check_array(X, x.nx, "X"));
+        if (d->act != TP_ACT_NONE) TRY(check_array(pre, x.T, "pre"));
+        TRY(check_array(A, x.T, "A"));
+        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.nx, "dX"));
+    }
+    TRY(check_array(reinterpret_cast<const void *const *>(dW1), x.T, "dW1"));
+    TRY(check_array(reinterpret_cast<const void *const *>(dW2), x.T, "dW2"));
+    if (d->has_bias) {
+        TRY(check_array(reinterpret_cast<const void *const *>(db1), x.T, "db1"));
+        TRY(check_one(db2, "db2"));
+    }
+    size_t shard_bytes = 0;
+    const size_t need = mlp_ws_layout(d, &shard_bytes);
+    if (workspace_bytes < need)
+        return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *const *db2a = reinterpret_cast<void *const *>(&db2);
+    if (x.M == 0) {
+        TRY(zero_grads(d, dW1, x.T, sizeof(float) * gw * x.H, d->has_bias ? db1 : nullptr, x.T, sizeof(float) * gw, st));
+        return zero_grads(d, dW2, x.T, sizeof(float) * x.H * x.Fs, d->has_bias ? db2a : nullptr, 1,
+                          sizeof(float) * x.H, st);
+    }
+    void *dpre[kMaxShards];
+    for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
+    float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
+    // row layer: dPre_i = (dY W2_i) * act'(pre_i), dW2_i = dY^T A_i
+    TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st));
+    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st));
+    // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY)
+    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st));
+    TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st));
+    if (d->has_bias) {
+        TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
+        TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+    }
+    return TP_OK;
+}
+
+tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
+                        void *const *out, void *const *pre, void *stream) {
+    TRY(validate_desc(desc));
+    const Dims x = dims_of(desc);
+    TRY(check_array(W, x.T, "W"));
+    if (desc->has_bias) TRY(check_array(b, x.T, "b"));
+    if (x.M == 0) return TP_OK;
+    TRY(check_array(X, x.nx, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(out), x.T, "out"));
+    if (pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
+    return column_fwd(desc, X, W, desc->has_bias ? b : nullptr, out, pre, static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
+                        const void *const *R, void *const *Y, void *stream) {
+    TRY(validate_desc(desc));
+    const Dims x = dims_of(desc);
+    TRY(check_array(W, x.T, "W"));
+    if (desc->has_bias) TRY(check_one(b, "b"));
+    if (!desc->residual && R) return set_error(TP_ERR_ARG, "R given but desc->residual is 0");
+    if (x.M == 0) return TP_OK;
+    TRY(check_array(X, x.T, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
+    if (desc->residual) TRY(check_array(R, x.nx, "R"));
+    return row_fwd(desc, X, W, desc->has_bias ? b : nullptr, desc->residual ? R : nullptr, Y,
+                   static_cast<cudaStream_t>(stream));
+}
+
+size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
+    if (validate_desc(desc) != TP_OK || !desc->has_bias) return 0;
+    const Dims x = dims_of(desc);
+    size_t a = partials_bytes(desc, x.T, x.g * x.Fs), b = partials_bytes(desc, 1, x.H);
+    return a > b ? a : b;
+}
+
+static tp_status check_ws(const tp_mlp_desc *d, void *ws, size_t bytes) {
+    const size_t need = tp_linear_workspace_bytes(d);
+    if (bytes < need) return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", bytes, need);
+    if (need && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    return TP_OK;
+}
+
+tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, const void *const *X,
+                            const void *const *W, void *const *dX, void *const *dW, void *const *db, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    TRY(validate_desc(desc));
+    if (desc->act != TP_ACT_NONE)
+        return set_error(TP_ERR_UNSUPPORTED, "tp_linear_col_bwd takes act = TP_ACT_NONE (use tp_mlp_bwd)");
+    const Dims x = dims_of(desc);
+    if (x.M > 0) {
+        TRY(check_array(dOut, x.T, "dOut"));
+        TRY(check_array(X, x.nx, "X"));
+        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.nx, "dX"));
+    }
+    TRY(check_array(W, x.T, "W"));
+    TRY(check_array(reinterpret_cast<const void *const *>(dW), x.T, "dW"));
+    if (desc->has_bias) TRY(check_array(reinterpret_cast<const void *const *>(db), x.T, "db"));
+    TRY(check_ws(desc, workspace, workspace_bytes));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (x.M == 0)
+        return zero_grads(desc, dW, x.T, sizeof(float) * x.Fs * x.H, desc->has_bias ? db : nullptr, x.T,
+                          sizeof(float) * x.Fs, st);
+    TRY(column_dgrad(desc, dOut, x.Fs, W, nullptr, dX, st));
+    TRY(wgrad(desc, "wgrad_col", dOut, 1, x.Fs, X, 0, x.H, dW, st));
+    if (desc->has_bias)
+        TRY(colsum(desc, "bias_grad_col", dOut, x.T, 1, 0, x.T, x.Fs, db, static_cast<float *>(workspace), st));
+    return TP_OK;
+}
+
+tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
+                            const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    TRY(validate_desc(desc));
+    const Dims x = dims_of(desc);
+    if (x.M > 0) {
+        TRY(check_array(dY, x.nx, "dY"));
+        TRY(check_array(X, x.T, "X"));
+        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.T, "dX"));
+    }
+    TRY(check_array(W, x.T, "W"));
+    TRY(check_array(reinterpret_cast<const void *const *>(dW), x.T, "dW"));
+    if (desc->has_bias) TRY(check_one(db, "db"));
+    TRY(check_ws(desc, workspace, workspace_bytes));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *const *dba = reinterpret_cast<void *const *>(&db);
+    if (x.M == 0)
+        return zero_grads(desc, dW, x.T, sizeof(float) * x.H * x.Fs, desc->has_bias ? dba : nullptr, 1,
+                          sizeof(float) * x.H, st);
+    TRY(row_dgrad(desc, TP_ACT_NONE, dY, W, nullptr, dX, x.Fs, st));
+    TRY(wgrad(desc, "wgrad_row", dY, 0, x.H, X, 1, x.Fs, dW, st));
+    if (desc->has_bias)
+        TRY(colsum(desc, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
+    return TP_OK;
+}
+
+tp_status tp_sync_status(void *stream) {
+    int v = 0;
+    TRY(read_and_clear_status(static_cast<cudaStream_t>(stream), &v));
+    if (v == TP_OK) return TP_OK;
+    return set_error(static_cast<tp_status>(v), "device reported %s", tp_status_str(static_cast<tp_status>(v)));
+}
+
+void tp_set_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns ? ns : 1); }
+
+tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
+    return launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+void tp_prof_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_on = on != 0;
+}
+
+int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
+    std::vector<ProfRec> recs;
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        recs.swap(g_prof_recs);
+    }
+    std::map<std::string, std::pair<int, double>> agg;
+    std::vector<std::string> order;
+    int rc = 0;
+    for (auto &r : recs) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) rc = -1;
+        if (!agg.count(r.name)) order.push_back(r.name);
+        auto &e = agg[r.name];
+        e.first += 1;
+        e.second += ms;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        for (auto &r : recs) {
+            g_event_pool.push_back(r.a);
+            g_event_pool.push_back(r.b);
+        }
+    }
+    if (rc) {
+        set_error(TP_ERR_CUDA, "event timing failed");
+        return -1;
+    }
+    int n = 0;
+    for (auto &name : order) {
+        if (!entries || n >= max_entries) break;
+        tp_prof_entry &e = entries[n++];
+        memset(&e, 0, sizeof(e));
+        snprintf(e.name, sizeof(e.name), "%s", name.c_str());
+        e.launches = agg[name].first;
+        e.total_ms = agg[name].second;
+    }
+    return n;
+}
+
+}  // extern "C"

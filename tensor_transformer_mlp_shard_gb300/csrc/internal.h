@@ -1,0 +1,99 @@
+// Host-side internal interfaces of libtpmlp: the GEMM plan that the C-ABI
+// layer builds for every product in the tensor-parallel MLP, and the launchers
+// that execute a plan on the tcgen05 (bf16) or SIMT (fp32) kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tp_mlp.h"
+
+namespace tpmlp {
+
+constexpr int kMaxShards = TP_MAX_SHARDS;
+
+// Epilogue kinds shared by both GEMM engines.
+enum EpiKind : int {
+    EPI_COL = 0,    // + bias, store pre, store act(pre)          (column forward)
+    EPI_PLAIN = 1,  // + bias, + residual, store                   (row forward, dgrads)
+    EPI_DACT = 2,   // * act'(pre) (SwiGLU: writes dG and dU)      (row-layer dgrad)
+    EPI_F32 = 3     // store or accumulate fp32                    (weight gradients)
+};
+
+// One GEMM operand: a set of row-major buffers [rows, cols] with leading
+// dimension `cols`.  K-major operands have the output's M (or N) dimension as
+// rows and K as cols; MN-major operands have K as rows.  For problem p, K
+// segment s and buffer row r the buffer used is
+//   p * p_stride + s * s_stride + (rows_split ? r / rows_split : 0)
+// at local row r % rows_split (token shards under sequence parallelism).
+struct OperandPlan {
+    const void *ptr[kMaxShards];
+    int n = 0;
+    int rows = 0, cols = 0;
+    bool mn_major = false;
+    int p_stride = 0, s_stride = 0, rows_split = 0;
+};
+
+// An output (or auxiliary input) addressed by problem and token row.
+struct OutPlan {
+    void *ptr[kMaxShards];
+    int n = 0;
+    int p_stride = 0, rows_split = 0;
+    long long ld = 0;  // elements
+};
+
+// D_p[M, N] = sum_{s < S} A_{p,s}[M, Kseg] * B_{p,s}[N, Kseg]^T for p < P, then
+// the epilogue.  For SwiGLU (act == TP_ACT_SWIGLU) N counts hidden units and
+// the gate/up halves sit `N` columns apart in pre / dPre / bias.
+struct GemmPlan {
+    const char *name = "";
+    int kind = EPI_PLAIN;
+    int act = TP_ACT_NONE;
+    int M = 0, N = 0, P = 1, S = 1, Kseg = 0;
+    OperandPlan A, B;
+    int b_dual_off = 0;   // column forward with SwiGLU: up rows start here in W1_i
+    OutPlan out;          // main output
+    OutPlan out2;         // pre (EPI_COL); n == 0 -> not stored
+    OutPlan aux;          // residual (EPI_PLAIN) or pre (EPI_DACT); n == 0 -> none
+    const void *bias[kMaxShards];
+    int bias_p_stride = 0;
+    bool has_bias = false;
+    bool accumulate = false;  // EPI_F32
+};
+
+// Column sums over token rows: out_p[c] = sum_m in_p[m, c] for c < N, fp32.
+struct ColsumPlan {
+    const char *name = "";
+    OutPlan in;      // P problems, token rows (may be token-sharded)
+    int P = 1, M = 0, N = 0;
+    float *out[kMaxShards];
+    float *partials = nullptr;  // workspace: P * chunks * N floats
+};
+
+int colsum_chunks(int M);
+
+// Launchers (return a tp_status).  They only enqueue work on `st`.
+tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
+tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
+tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
+
+// Device status words (per device), the wait limit and the launch counter.
+struct DeviceWords {
+    int *status = nullptr;
+    unsigned *abort_word = nullptr;
+};
+tp_status device_words(DeviceWords *w);
+uint64_t wait_limit_ns();
+unsigned next_launch_id();
+int num_sms();
+
+// Profiling + launch accounting around every kernel launch.
+void launch_begin(const char *name, cudaStream_t st);
+void launch_end(const char *name, cudaStream_t st);
+
+// Error message of the calling thread.
+tp_status set_error(tp_status s, const char *fmt, ...);
+tp_status cuda_check(cudaError_t e, const char *what);
+
+}  // namespace tpmlp

@@ -1,0 +1,209 @@
+// Token-dimension column sums (the bias gradients db = sum_m dOut[m, :]),
+// the device status words and the bounded-wait self-test kernel.
+//
+// The column sum is HBM-bound: one pass over the input with 16-byte
+// coalesced loads.  Pass 1 sums fixed chunks of token rows per column strip
+// into fp32 partials (workspace); pass 2 adds the partials of each column in
+// chunk order.  Both passes use a fixed order, so results are run-to-run
+// deterministic (no atomics).
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace tpmlp {
+
+// ---------------------------------------------------------------------------
+// status words
+// ---------------------------------------------------------------------------
+__device__ int g_tp_status = 0;
+__device__ unsigned g_tp_abort = 0;
+__device__ unsigned g_tp_never_set = 0;
+
+tp_status device_words(DeviceWords *w) {
+    static int cached_dev = -1;
+    static DeviceWords cached[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+    (void)cached_dev;
+    if (dev < 64 && have[dev]) {
+        *w = cached[dev];
+        return TP_OK;
+    }
+    void *ps = nullptr, *pa = nullptr;
+    e = cudaGetSymbolAddress(&ps, g_tp_status);
+    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(status)");
+    e = cudaGetSymbolAddress(&pa, g_tp_abort);
+    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(abort)");
+    w->status = static_cast<int *>(ps);
+    w->abort_word = static_cast<unsigned *>(pa);
+    if (dev < 64) {
+        cached[dev] = *w;
+        have[dev] = true;
+    }
+    return TP_OK;
+}
+
+tp_status read_and_clear_status(cudaStream_t st, int *out) {
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_check(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_tp_status, sizeof(int));
+    if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyFromSymbol(status)");
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_tp_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyToSymbol(status)");
+    *out = v;
+    return TP_OK;
+}
+
+// Waits for a flag that nothing sets; the wall-clock bound ends the wait and
+// the kernel records TP_ERR_TIMEOUT, like any of the GEMM kernels' waits.
+__global__ void wait_timeout_kernel(unsigned long long limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (*reinterpret_cast<volatile unsigned *>(&g_tp_never_set) == 0) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicCAS(&g_tp_status, 0, TP_ERR_TIMEOUT);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+
+tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st) {
+    launch_begin("wait_timeout", st);
+    wait_timeout_kernel<<<1, 1, 0, st>>>(limit_ns);
+    cudaError_t e = cudaGetLastError();
+    launch_end("wait_timeout", st);
+    return cuda_check(e, "wait_timeout_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// column sums
+// ---------------------------------------------------------------------------
+constexpr int kChunkRows = 256;
+constexpr int kWarps = 8;
+
+int colsum_chunks(int M) { return M <= 0 ? 1 : (M + kChunkRows - 1) / kChunkRows; }
+
+struct ColsumParams {
+    const void *ptr[kMaxShards];
+    int p_stride, rows_split;
+    long long ld;
+    int M, N, chunks;
+    float *partials;
+    float *out[kMaxShards];
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T *src, float *dst);
+
+template <>
+__device__ __forceinline__ void load_vec<__nv_bfloat16>(const __nv_bfloat16 *src, float *dst) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(src);
+    dst[0] = bf16_lo(w.x); dst[1] = bf16_hi(w.x);
+    dst[2] = bf16_lo(w.y); dst[3] = bf16_hi(w.y);
+    dst[4] = bf16_lo(w.z); dst[5] = bf16_hi(w.z);
+    dst[6] = bf16_lo(w.w); dst[7] = bf16_hi(w.w);
+}
+
+template <>
+__device__ __forceinline__ void load_vec<float>(const float *src, float *dst) {
+    const float4 w = *reinterpret_cast<const float4 *>(src);
+    dst[0] = w.x; dst[1] = w.y; dst[2] = w.z; dst[3] = w.w;
+}
+
+// grid: x = column strips of 32*VEC columns, y = row chunks, z = problems
+template <typename T, int VEC>
+__global__ void __launch_bounds__(32 * kWarps) colsum_partial_kernel(const __grid_constant__ ColsumParams p) {
+    __shared__ float red[kWarps][32 * VEC];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int z = blockIdx.z;
+    const int col = blockIdx.x * 32 * VEC + lane * VEC;
+    const int r0 = blockIdx.y * kChunkRows;
+    const int r1 = min(p.M, r0 + kChunkRows);
+    float acc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.0f;
+    if (col < p.N) {
+        for (int r = r0 + warp; r < r1; r += kWarps) {
+            int idx = z * p.p_stride, lr = r;
+            if (p.rows_split) {
+                idx += r / p.rows_split;
+                lr = r % p.rows_split;
+            }
+            const T *src = static_cast<const T *>(p.ptr[idx]) + static_cast<long long>(lr) * p.ld + col;
+            float v[VEC];
+            load_vec<T>(src, v);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] += v[j];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) red[warp][lane * VEC + j] = acc[j];
+    __syncthreads();
+    for (int c = threadIdx.x; c < 32 * VEC; c += blockDim.x) {
+        const int gc = blockIdx.x * 32 * VEC + c;
+        if (gc >= p.N) continue;
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[w][c];
+        p.partials[(static_cast<long long>(z) * p.chunks + blockIdx.y) * p.N + gc] = s;
+    }
+}
+
+__global__ void colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
+    const int z = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= p.N) return;
+    const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
+    float s = 0.0f;
+    for (int k = 0; k < p.chunks; ++k) s += src[static_cast<long long>(k) * p.N];
+    p.out[z][c] = s;
+}
+
+tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st) {
+    ColsumParams prm;
+    memset(&prm, 0, sizeof(prm));
+    for (int i = 0; i < kMaxShards; ++i) {
+        prm.ptr[i] = i < c.in.n ? c.in.ptr[i] : nullptr;
+        prm.out[i] = i < c.P ? c.out[i] : nullptr;
+    }
+    prm.p_stride = c.in.p_stride;
+    prm.rows_split = c.in.rows_split;
+    prm.ld = c.in.ld;
+    prm.M = c.M;
+    prm.N = c.N;
+    prm.chunks = colsum_chunks(c.M);
+    prm.partials = c.partials;
+    if (c.N == 0 || c.P == 0) return TP_OK;
+    if (c.M == 0) {
+        for (int z = 0; z < c.P; ++z) {
+            cudaError_t e = cudaMemsetAsync(c.out[z], 0, sizeof(float) * c.N, st);
+            if (e != cudaSuccess) return cuda_check(e, "cudaMemsetAsync(colsum)");
+        }
+        return TP_OK;
+    }
+    const int vec = dtype == TP_DT_BF16 ? 8 : 4;
+    dim3 g1((c.N + 32 * vec - 1) / (32 * vec), prm.chunks, c.P);
+    launch_begin(c.name, st);
+    if (dtype == TP_DT_BF16)
+        colsum_partial_kernel<__nv_bfloat16, 8><<<g1, 32 * kWarps, 0, st>>>(prm);
+    else
+        colsum_partial_kernel<float, 4><<<g1, 32 * kWarps, 0, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end(c.name, st);
+    if (e != cudaSuccess) return cuda_check(e, c.name);
+    dim3 g2((c.N + 255) / 256, c.P);
+    launch_begin("colsum_finalize", st);
+    colsum_finalize_kernel<<<g2, 256, 0, st>>>(prm);
+    e = cudaGetLastError();
+    launch_end("colsum_finalize", st);
+    return cuda_check(e, "colsum_finalize");
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol include/tp_mlp.h declares, and rejects bad descriptors and pointers
+before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp_mlp.h")
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from tensor_transformer_mlp_shard_gb300 import build
+    build.build()
+    import tensor_transformer_mlp_shard_gb300 as tp
+    return tp
+
+
+def declared_symbols():
+    names = []
+    for path in (HEADER,):
+        with open(path) as f:
+            for line in f:
+                m = re.match(r"^TP_API\s+[\w\s\*]+?\b(tp_\w+)\(", line)
+                if m:
+                    names.append(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(tp):
+    names = declared_symbols()
+    assert len(names) >= 19
+    L = ctypes.CDLL(tp.library_path())
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding knows every one of them
+    from tensor_transformer_mlp_shard_gb300.binding import SIGNATURES
+    assert set(names) == set(SIGNATURES)
+
+
+def test_abi_version_and_status_strings(tp):
+    L = tp.lib()
+    assert L.tp_abi_version() == 1
+    assert L.tp_status_str(0) == b"TP_OK"
+    assert L.tp_status_str(2) == b"TP_ERR_SHAPE"
+    assert L.tp_status_str(5) == b"TP_ERR_TIMEOUT"
+
+
+def _create(tp, **kw):
+    base = dict(S=128, B=2, H=256, F=1024, T=2, act="gelu_tanh", dtype="bf16")
+    base.update(kw)
+    d = tp.make_desc(**base)
+    h = ctypes.c_void_p()
+    s = tp.lib().tp_mlp_create(ctypes.byref(d), ctypes.byref(h))
+    if s == 0:
+        tp.lib().tp_mlp_destroy(h)
+    return s
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, 0),
+    ({"F": 1000, "T": 3}, 2),           # divide(): F % T != 0
+    ({"T": 0}, 2),
+    ({"T": 17}, 2),
+    ({"H": 260}, 2),                    # H % 8
+    ({"F": 1028, "T": 2}, 2),           # F/T = 514, not a multiple of 8
+    ({"S": 100, "T": 8, "F": 1024, "seq_parallel": True}, 2),   # S % T
+    ({"S": 8 * 100, "B": 1, "T": 8, "F": 1024, "seq_parallel": True}, 2),  # bf16 SP: M/T % 128
+    ({"S": 8 * 100, "B": 1, "T": 8, "F": 1024, "seq_parallel": True, "dtype": "f32"}, 0),
+    ({"S": 0}, 0),                      # empty problem is valid
+    ({"act": "swiglu"}, 0),
+])
+def test_create_validation(tp, kw, expect):
+    assert _create(tp, **kw) == expect
+
+
+def test_bad_enum_and_flags(tp):
+    d = tp.make_desc(128, 2, 256, 1024, 2)
+    d.act = 7
+    h = ctypes.c_void_p()
+    assert tp.lib().tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 1
+    d = tp.make_desc(128, 2, 256, 1024, 2)
+    d.residual = 2
+    assert tp.lib().tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 1
+    assert tp.lib().tp_mlp_create(None, ctypes.byref(h)) == 1
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch(tp):
+    L = tp.lib()
+    d = tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh", dtype="bf16")
+    h = ctypes.c_void_p()
+    assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    from tensor_transformer_mlp_shard_gb300.binding import _arr
+    good = [0x10000 * (i + 1) for i in range(2)]
+    # X array missing
+    assert L.tp_mlp_fwd(h, None, _arr(good), None, _arr(good), None, _arr(good[:1]), _arr(good), _arr(good),
+                        None) == 1
+    # misaligned W1[1]
+    bad = [0x10000, 0x20008]
+    assert L.tp_mlp_fwd(h, _arr(good[:1]), _arr(bad), None, _arr(good), None, _arr(good[:1]), _arr(good),
+                        _arr(good), None) == 1
+    assert b"W1[1]" in L.tp_last_error()
+    # workspace too small
+    ws_need = L.tp_mlp_workspace_bytes(h)
+    assert ws_need >= 2 * 256 * 512 * 2
+    assert L.tp_mlp_bwd(h, _arr(good[:1]), _arr(good[:1]), _arr(good), _arr(good), _arr(good), _arr(good),
+                        _arr(good[:1]), _arr(good), None, _arr(good), None, ctypes.c_void_p(0x100000), 16,
+                        None) == 1
+    assert b"workspace" in L.tp_last_error()
+    L.tp_mlp_destroy(h)
+
+
+def test_linear_col_bwd_rejects_activation(tp):
+    from tensor_transformer_mlp_shard_gb300.binding import _arr
+    L = tp.lib()
+    d = tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh")
+    p = [0x10000, 0x20000]
+    assert L.tp_linear_col_bwd(ctypes.byref(d), _arr(p), _arr(p[:1]), _arr(p), _arr(p[:1]), _arr(p), None,
+                               None, 0, None) == 3
+
+
+def test_workspace_sizes(tp):
+    # dPre (T * M * g*Fs * 2 bytes, each shard 256-aligned) + bias partials
+    lay = tp.Layout(S=2048, B=4, H=4096, F=16384, T=8, act="gelu_tanh", dtype="bf16", has_bias=True)
+    d = lay.desc()
+    h = ctypes.c_void_p()
+    L = tp.lib()
+    assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    ws = L.tp_mlp_workspace_bytes(h)
+    dpre = 8 * 8192 * 2048 * 2
+    chunks = 8192 // 256
+    partials = 4 * 8 * chunks * 2048
+    assert ws == dpre + partials
+    L.tp_mlp_destroy(h)
+    lay2 = tp.Layout(S=2048, B=4, H=4096, F=16384, T=8, act="none", has_bias=False)
+    assert tp.linear_workspace_bytes(lay2) == 0

@@ -1,0 +1,200 @@
+"""GPU parity of the tensor-parallel MLP against the fp64 oracle, through the
+C ABI.  Sizes span several 128 x 256 tiles with ragged tails in M, N and K;
+tolerances are max|gpu - ref| <= tol * max|ref| with tol = 1e-5 (fp32) and
+1e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import TOL, MlpRun, host, mlp_inputs, oracle_full, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import tensor_transformer_mlp_shard_gb300 as tp
+    from tensor_transformer_mlp_shard_gb300 import build
+    build.build()
+    return tp
+
+
+def _check_all(run, ref, lay, tol):
+    T = lay.T
+    errs = {}
+    errs["Y"] = rel_err(run.gathered(run.Y), ref["Y"])
+    for i in range(T):
+        errs[f"A{i}"] = rel_err(host(run.A[i]), ref["A"][i])
+        errs[f"pre{i}"] = rel_err(host(run.pre[i]), ref["pre"][i])
+        errs[f"dW1_{i}"] = rel_err(host(run.dW1[i]), ref["dW1"][i])
+        errs[f"dW2_{i}"] = rel_err(host(run.dW2[i]), ref["dW2"][i])
+        if lay.has_bias:
+            errs[f"db1_{i}"] = rel_err(host(run.db1[i]), ref["db1"][i])
+    errs["dX"] = rel_err(run.gathered(run.dX), ref["dX"])
+    if lay.has_bias:
+        errs["db2"] = rel_err(host(run.db2), ref["db2"])
+    bad = {k: v for k, v in errs.items() if not (v <= tol)}
+    assert not bad, bad
+    return errs
+
+
+CASES = [
+    # M, H, F, T, act, dtype, bias, residual, sp
+    (300, 264, 800, 4, "gelu_tanh", "bf16", True, True, False),
+    (300, 264, 800, 4, "swiglu", "bf16", True, False, False),
+    (300, 264, 800, 2, "none", "bf16", False, True, False),
+    (200, 136, 64, 1, "gelu_tanh", "bf16", True, False, False),
+    (1024, 264, 1600, 8, "gelu_tanh", "bf16", False, False, True),
+    (512, 200, 1024, 4, "swiglu", "bf16", False, True, True),
+    (2048, 1024, 8192, 8, "gelu_tanh", "bf16", True, True, False),
+    (256, 256, 1024, 2, "gelu_tanh", "f32", True, False, False),
+    (300, 264, 800, 4, "swiglu", "f32", True, True, False),
+    (120, 72, 240, 3, "gelu_tanh", "f32", True, True, True),
+]
+
+
+@pytest.mark.parametrize("M,H,F,T,act,dtype,bias,residual,sp", CASES)
+def test_mlp_matches_oracle(tp, M, H, F, T, act, dtype, bias, residual, sp):
+    S, B = M // 2, 2
+    lay = tp.TPMLP(S=S, B=B, H=H, F=F, T=T, act=act, dtype=dtype, has_bias=bias, residual=residual,
+                   seq_parallel=sp)
+    t = mlp_inputs(M, H, F, T, act, dtype, has_bias=bias)
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    assert tp.sync_status() == 0
+    ref = oracle_full(lay, t)
+    _check_all(run, ref, lay, TOL[dtype])
+
+
+def test_tiny_workload_full(tp):
+    """The Tiny problem: X [128,2,256] fp32, W1 [1024,256], W2 [256,1024],
+    T=2, GeLU-tanh, biases present and zero; checked in full at 1e-5."""
+    import synth
+    w = synth.WORKLOADS["tiny"]
+    lay = tp.TPMLP(S=w.S, B=w.B, H=w.H, F=w.F, T=w.T, act=w.act, dtype=w.dtype, has_bias=True)
+    full = synth.mlp_tensors(w)
+    t = dict(full)
+    t["W1s"] = oracle.shard_column_weight(full["W1"], w.T, w.act)
+    t["b1s"] = oracle.shard_column_bias(full["b1"], w.T, w.act)
+    t["W2s"] = oracle.shard_row_weight(full["W2"], w.T)
+    t = {k: (np.ascontiguousarray(v) if isinstance(v, np.ndarray) else
+             [np.ascontiguousarray(x) for x in v] if isinstance(v, list) else v) for k, v in t.items()}
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    assert tp.sync_status() == 0
+    _check_all(run, oracle_full(lay, t), lay, 1e-5)
+
+
+def test_column_shards_are_independent_bitwise(tp):
+    """Changing W1_j / b1_j leaves pre_i and A_i (i != j) bitwise unchanged."""
+    lay = tp.TPMLP(S=150, B=2, H=264, F=800, T=4, act="gelu_tanh", dtype="bf16", has_bias=True)
+    t = mlp_inputs(300, 264, 800, 4, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    run.fwd()
+    pre0 = [p.clone() for p in run.pre]
+    A0 = [a.clone() for a in run.A]
+    run.W1[2].mul_(-1.5)
+    run.b1[2].add_(1.0)
+    run.fwd()
+    assert tp.sync_status() == 0
+    for i in range(4):
+        same = torch.equal(run.pre[i], pre0[i]) and torch.equal(run.A[i], A0[i])
+        assert same == (i != 2)
+
+
+def test_row_backward_needs_no_reduction_bitwise(tp):
+    """Changing W2_j leaves dW2_i bitwise unchanged for every i and dW1_i for
+    i != j: the row layer's backward has no cross-shard sum."""
+    lay = tp.TPMLP(S=150, B=2, H=264, F=800, T=4, act="swiglu", dtype="bf16")
+    t = mlp_inputs(300, 264, 800, 4, "swiglu", "bf16", has_bias=False)
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    dW2 = [d.clone() for d in run.dW2]
+    dW1 = [d.clone() for d in run.dW1]
+    run.W2[1].mul_(0.5)
+    run.bwd()
+    assert tp.sync_status() == 0
+    for i in range(4):
+        assert torch.equal(run.dW2[i], dW2[i])
+        assert torch.equal(run.dW1[i], dW1[i]) == (i != 1)
+
+
+def test_sharded_equals_unsharded_on_gpu(tp):
+    """The library at T = 1, 2, 4, 8 on the same full weights gives the same Y
+    and dX within tolerance."""
+    M, H, F = 256, 256, 1024
+    outs = {}
+    for T in (1, 2, 4, 8):
+        lay = tp.TPMLP(S=128, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+        t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16")
+        run = MlpRun(lay, t)
+        run.fwd()
+        run.bwd()
+        assert tp.sync_status() == 0
+        outs[T] = (run.gathered(run.Y), run.gathered(run.dX),
+                   oracle.unshard_column([host(d) for d in run.dW1]))
+    for T in (2, 4, 8):
+        for a, b in zip(outs[T], outs[1]):
+            assert rel_err(a, b) < 1e-2
+
+
+def test_deterministic_and_accumulate(tp):
+    lay = tp.TPMLP(S=150, B=2, H=264, F=800, T=4, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(300, 264, 800, 4, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    Y0, dX0 = [y.clone() for y in run.Y], [d.clone() for d in run.dX]
+    dW10 = [d.clone() for d in run.dW1]
+    db10 = [d.clone() for d in run.db1]
+    run.fwd()
+    run.bwd()
+    for a, b in zip(Y0 + dX0 + dW10 + db10, run.Y + run.dX + run.dW1 + run.db1):
+        assert torch.equal(a, b)
+    acc = tp.TPMLP(S=150, B=2, H=264, F=800, T=4, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True,
+                   wgrad_accumulate=True)
+    acc.bwd(run.dY, run.X, run.W1, run.W2, run.pre, run.A, run.dX, run.dW1, run.db1, run.dW2, run.db2, run.ws)
+    assert tp.sync_status() == 0
+    for a, b in zip(dW10, run.dW1):
+        assert torch.equal(2 * a, b)
+
+
+def test_empty_tokens(tp):
+    lay = tp.TPMLP(S=0, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    t = mlp_inputs(0, 64, 256, 2, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    assert tp.sync_status() == 0
+    for d in run.dW1 + run.dW2 + run.db1 + [run.db2]:
+        assert torch.count_nonzero(d).item() == 0
+
+
+def test_bounded_wait_reports_timeout(tp):
+    """A kernel waiting on a flag that nothing sets gives up after its limit
+    and records TP_ERR_TIMEOUT; the context stays usable."""
+    assert tp.sync_status() == 0
+    tp.debug_wait_timeout(2_000_000)  # 2 ms
+    assert tp.sync_status() == 5
+    assert tp.sync_status() == 0
+    # the library still computes correctly afterwards
+    lay = tp.TPMLP(S=64, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    t = mlp_inputs(128, 64, 256, 2, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    run.fwd()
+    assert tp.sync_status() == 0
+    assert rel_err(run.gathered(run.Y), oracle_full(lay, t)["Y"]) < 1e-2
+
+
+def test_binding_rejects_wrong_shapes(tp):
+    lay = tp.TPMLP(S=64, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    t = mlp_inputs(128, 64, 256, 2, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    with pytest.raises(ValueError):
+        lay.fwd(run.X, run.W1[:1], run.b1, run.W2, run.b2, run.Y, run.pre, run.A)
+    with pytest.raises(ValueError):
+        lay.fwd([run.X[0][:100]], run.W1, run.b1, run.W2, run.b2, run.Y, run.pre, run.A)
