@@ -181,6 +181,28 @@ TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *d
                             void *const *dX, void *const *dW, void *db,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/* tp_linear_row_bwd_noalloc: tp_linear_row_bwd without a caller workspace.
+ *   The pages have no counterpart: this entry point exists for callers that
+ *   cannot allocate device memory when they call -- a plugin that is handed
+ *   only the op's tensors and has no allocator of its own, a process whose
+ *   device memory is fully reserved by another (caching) allocator, or a
+ *   latency-critical loop that cannot take cudaMalloc's implicit device
+ *   synchronisation.  It computes exactly what tp_linear_row_bwd computes and
+ *   allocates nothing: the bias-gradient partial sums go to a 4 MiB array
+ *   compiled into the library (held on every GPU that loads the library until
+ *   the process exits).  Arguments are those of tp_linear_row_bwd minus the
+ *   workspace.  A problem whose partials exceed 4 MiB (4 * ceil(M/256) * H
+ *   bytes, rounded up to 256, when has_bias) returns TP_ERR_UNSUPPORTED.
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   All calls share the one array and each call overwrites the part it reads
+ *   (nothing needs to start at zero), so calls that overlap on the GPU -- on
+ *   different streams, or from several host threads -- race. */
+TP_API tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *const *dY,
+                                           const void *const *X, const void *const *W,
+                                           void *const *dX, void *const *dW, void *db,
+                                           void *stream);
+
 /* ---- status, limits, diagnostics ---------------------------------------- */
 
 /* Synchronise `stream`, then read and clear the device status word.  Returns

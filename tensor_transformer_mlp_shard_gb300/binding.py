@@ -60,6 +60,7 @@ SIGNATURES = {
     "tp_linear_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Desc)]),
     "tp_linear_col_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
+    "tp_linear_row_bwd_noalloc": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP]),
     "tp_sync_status": (ctypes.c_int, [VP]),
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
@@ -305,6 +306,24 @@ def linear_row_bwd(layout: Layout, dY, X, W, dX, dW, db, workspace=None, stream=
     ws, nws = _workspace(workspace, linear_workspace_bytes(layout))
     _check(lib().tp_linear_row_bwd(ctypes.byref(d), _arr(pdy), _arr(px), _arr(pw), _arr(pdx), _arr(pdw), pdb,
                                    ws, nws, _stream(stream)))
+
+
+def linear_row_bwd_noalloc(layout: Layout, dY, X, W, dX, dW, db, stream=None):
+    """tp_linear_row_bwd for callers that cannot allocate device memory: the
+    bias-gradient scratch comes from a fixed 4 MiB array inside the library
+    instead of a caller workspace (see include/tp_mlp.h for the limits and
+    for why overlapping calls race)."""
+    c, T, H, Fs = _Checker(layout.dtype), layout.T, layout.H, layout.Fs
+    f32 = torch.float32
+    d = layout.desc()
+    pdy = c.tensors("dY", dY, layout.nx, (layout.xrows, H))
+    px = c.tensors("X", X, T, (layout.M, Fs))
+    pw = c.tensors("W", W, T, (H, Fs))
+    pdx = c.tensors("dX", dX, T, (layout.M, Fs))
+    pdw = c.tensors("dW", dW, T, (H, Fs), f32)
+    pdb = c.tensors("db", db, 1, (H,), f32)[0] if layout.has_bias else None
+    _check(lib().tp_linear_row_bwd_noalloc(ctypes.byref(d), _arr(pdy), _arr(px), _arr(pw), _arr(pdx), _arr(pdw),
+                                           pdb, _stream(stream)))
 
 
 # ---------------------------------------------------------------------------
