@@ -150,6 +150,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     from tensor_transformer_mlp_shard_gb300 import build
     build.build()
     torch.cuda.set_device(local)
+    tp.set_tile_mode(args.tile_mode)
     dev = torch.device("cuda", local)
     bf = torch.bfloat16
     T, M, H, F, g = w.T, w.M, w.H, w.F, w.g
@@ -361,6 +362,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
+                    help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -373,7 +376,8 @@ def main():
                           f"{', sequence-parallel' if w.seq_parallel else ''}",
               "S": w.S, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "act": w.act, "global_batch": w.B * ws,
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
-              "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)"}
+              "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
+              "tile_mode": args.tile_mode}
     base = {"metric": METRIC, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded SplitMix64 + Box-Muller), random-init weights", "config": config}

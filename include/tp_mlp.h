@@ -218,6 +218,15 @@ TP_API void tp_set_wait_limit_ns(uint64_t ns);
  * to test the failure path without faulting or hanging the GPU. */
 TP_API tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream);
 
+/* GEMM tiling of the bf16 engine, for all launches made after the call:
+ * TP_TILE_AUTO (default) uses 256-row tiles computed by a pair of CTAs on two
+ * SMs (tcgen05 cta_group::2) whenever M > 128, else 128-row single-CTA tiles;
+ * TP_TILE_SINGLE / TP_TILE_PAIR force one or the other.  Both accumulate every
+ * output element over K in the same order.  Returns TP_ERR_ARG for an unknown
+ * mode. */
+typedef enum { TP_TILE_AUTO = 0, TP_TILE_SINGLE = 1, TP_TILE_PAIR = 2 } tp_tile_mode;
+TP_API tp_status tp_set_tile_mode(int mode);
+
 /* Number of kernels this library has launched since load. */
 TP_API uint64_t tp_launch_count(void);
 

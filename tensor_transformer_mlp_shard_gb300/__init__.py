@@ -8,5 +8,6 @@ inside the tcgen05 GEMM kernels of ``libtpmlp.so`` (C ABI in
 from .binding import (ACT, DTYPE, Layout, TPMLP, TpError, alloc_workspace, debug_wait_timeout,  # noqa: F401
                       launch_count, lib, library_path, linear_col, linear_col_bwd, linear_row, linear_row_bwd,
                       linear_row_bwd_noalloc,
-                      linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_wait_limit_ns, status_str,
+                      linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_tile_mode, set_wait_limit_ns,
+                      status_str,
                       sync_status)

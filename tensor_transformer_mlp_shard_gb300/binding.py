@@ -65,6 +65,7 @@ SIGNATURES = {
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
     "tp_launch_count": (ctypes.c_uint64, []),
+    "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
     "tp_prof_collect": (ctypes.c_int, [ctypes.POINTER(ProfEntry), ctypes.c_int]),
 }
@@ -340,6 +341,15 @@ def set_wait_limit_ns(ns: int):
 
 def debug_wait_timeout(limit_ns: int, stream=None):
     _check(lib().tp_debug_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+TILE_MODES = {"auto": 0, "single": 1, "pair": 2}
+
+
+def set_tile_mode(mode: str):
+    """GEMM tiling of the bf16 engine: "auto", "single" (128-row tiles, one
+    CTA) or "pair" (256-row tiles on a CTA pair)."""
+    _check(lib().tp_set_tile_mode(TILE_MODES[mode]))
 
 
 def launch_count() -> int:

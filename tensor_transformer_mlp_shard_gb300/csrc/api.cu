@@ -601,6 +601,13 @@ tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
 
 uint64_t tp_launch_count(void) { return g_launches.load(); }
 
+tp_status tp_set_tile_mode(int mode) {
+    if (mode != TP_TILE_AUTO && mode != TP_TILE_SINGLE && mode != TP_TILE_PAIR)
+        return set_error(TP_ERR_ARG, "unknown tile mode %d", mode);
+    set_tile_mode(mode);
+    return TP_OK;
+}
+
 void tp_prof_enable(int on) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     g_prof_on = on != 0;

@@ -75,6 +75,7 @@ int colsum_chunks(int M);
 
 // Launchers (return a tp_status).  They only enqueue work on `st`.
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
+void set_tile_mode(int mode);  // TP_TILE_*
 tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
 

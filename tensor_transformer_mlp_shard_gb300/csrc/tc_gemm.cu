@@ -12,12 +12,14 @@
 //
 // Tile: 128 x 256 (tcgen05 M=128, N=256, K=16 per instruction, cta_group::1),
 // BK = 64 bf16 = one 128-byte swizzle row.  Warp 0 issues TMA, warp 1 issues
-// MMAs, warps 2-5 run the epilogue out of one of two TMEM accumulators while
+// MMAs, warps 2-9 run the epilogue out of one of two TMEM accumulators while
 // the next tile accumulates into the other.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -31,14 +33,15 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int MN_BOX = 64;         // MN-major operands: 64 elements (128 B) per box row
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 
 struct Sel {
-    int p_stride, s_stride, rows_split;
+    int p_stride, s_stride, rows_split, nsplit;  // nsplit: token shards (when rows_split > 0)
 };
 struct Out {
     void *ptr[kMaxShards];
@@ -204,12 +207,16 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &pi, int
     nt = n - pi * p.n_tiles;
 }
 
+// Tensor map and local row for buffer row `row`.  A row past the last token
+// shard (the second half of a CTA-pair tile beyond M) stays on the last shard's
+// map at a row past its end, where the TMA load reads zero fill.
 __device__ __forceinline__ void select(const Sel &s, int pi, int seg, int row, int &idx, int &lrow) {
     idx = pi * s.p_stride + seg * s.s_stride;
     lrow = row;
     if (s.rows_split) {
-        idx += row / s.rows_split;
-        lrow = row % s.rows_split;
+        const int j = min(row / s.rows_split, s.nsplit - 1);
+        idx += j;
+        lrow = row - j * s.rows_split;
     }
 }
 
@@ -243,11 +250,30 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float *v)
 
 // ---------------------------------------------------------------------------
 // epilogues: thread (warp q, lane l) owns output row m0 + 32q + l and walks
-// the accumulator in 32-column chunks.  Columns come in groups of 8 that are
-// either all inside N or all outside (N % 8 == 0).
+// its half of the accumulator (`half` selects 128 of the 256 columns; for
+// SwiGLU 64 gate + the matching 64 up columns) in 32-column chunks.  Columns
+// come in groups of 8 that are either all inside N or all outside (N % 8 == 0).
 // ---------------------------------------------------------------------------
+// Activations of the bf16 epilogues use the SFU's tanh.approx.f32 (maximum
+// relative error about 2^-11, far below the 2^-8 resolution of the bf16
+// results they produce).  sigmoid(x) = (1 + tanh(x/2)) / 2.
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_tanh_fast(float x) {
+    const float t = tanh_fast(kGeluK0 * fmaf(kGeluK1 * x * x, x, x));
+    return 0.5f * x * (1.0f + t);
+}
+__device__ __forceinline__ float gelu_tanh_grad_fast(float x) {
+    const float t = tanh_fast(kGeluK0 * fmaf(kGeluK1 * x * x, x, x));
+    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * kGeluK0 * fmaf(3.0f * kGeluK1, x * x, 1.0f);
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+
 template <int EPI>
-__device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, int nt, uint32_t taddr) {
+__device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, int nt, uint32_t taddr, int half) {
     const bool row_ok = row < p.M;
     if (EPI == EPI_COL && p.act == TP_ACT_SWIGLU) {
         // accumulator columns [0,128) = gate units, [128,256) = up units
@@ -255,7 +281,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
         const __nv_bfloat16 *bias =
             p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
             uint32_t rg[32], ru[32];
             __syncwarp();
             tmem_ld32(taddr + c * 32, rg);
@@ -290,7 +316,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
                     store_bf16x8(pre + p.N + u, U);
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) A[j] = G[j] * sigmoid_f(G[j]) * U[j];
+                for (int j = 0; j < 8; ++j) A[j] = G[j] * sigmoid_fast(G[j]) * U[j];
                 store_bf16x8(act + u, A);
             }
         }
@@ -298,7 +324,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
     }
     const int n0 = nt * BN;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
@@ -341,7 +367,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
                 if (pre) store_bf16x8(pre + col, x);
                 if (p.act == TP_ACT_GELU_TANH) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) x[j] = gelu_tanh_f(x[j]);
+                    for (int j = 0; j < 8; ++j) x[j] = gelu_tanh_fast(x[j]);
                 }
                 store_bf16x8(act + col, x);
             }
@@ -381,7 +407,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
                     float x[8];
                     load_bf16x8(pre + u, x);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) d[j] *= gelu_tanh_grad_f(x[j]);
+                    for (int j = 0; j < 8; ++j) d[j] *= gelu_tanh_grad_fast(x[j]);
                     store_bf16x8(o + u, d);
                 } else if (p.act == TP_ACT_SWIGLU) {
                     float G[8], U[8], dG[8], dU[8];
@@ -389,7 +415,7 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
                     load_bf16x8(pre + p.N + u, U);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float s = sigmoid_f(G[j]);
+                        const float s = sigmoid_fast(G[j]);
                         dG[j] = d[j] * U[j] * s * (1.0f + G[j] * (1.0f - s));
                         dU[j] = d[j] * G[j] * s;
                     }
@@ -429,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull0 + 8 * i, 1);
-            mbar_init(tempty0 + 8 * i, 128);
+            mbar_init(tempty0 + 8 * i, 32 * EPI_WARPS);
         }
         mbar_init(drain, 1);
         fence_mbar_init();
@@ -555,8 +581,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue (warps 2..9) ----------------
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;   // which 128 accumulator columns it drains
         int it = 0;
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -568,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             tile_coords(p, t, pi, mt, nt);
             const int row = mt * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            run_epilogue<EPI>(p, pi, row, nt, taddr);
+            run_epilogue<EPI>(p, pi, row, nt, taddr, half);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
         }
@@ -578,6 +605,271 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant: a cluster of two CTAs on two SMs computes one 256 x 256
+// tile with tcgen05.mma.cta_group::2 (M = 256).  CTA r of the pair loads rows
+// [128r, 128r + 128) of the A tile and rows [128r, 128r + 128) of the B tile
+// (for SwiGLU: CTA 0 the gate rows, CTA 1 the up rows) into its own shared
+// memory; the MMA, issued by CTA 0, reads both CTAs' halves and leaves rows
+// [128r, 128r + 128) of the accumulator in CTA r's TMEM.  Each SM thus reads
+// half of the B tile it would read alone, and a stage is 32 KB, so the ring
+// is 6 stages deep.
+//
+// Barriers: every load of both CTAs completes on CTA 0's full[s] (CTA 0 arms
+// it for both); the MMA commit multicasts to empty[s] and tfull[a] of both
+// CTAs; both CTAs' epilogue threads arrive on CTA 0's tempty[a].
+// ---------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+constexpr int P_TILE_M = 256;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// arrive on the barrier at this shared-memory offset in both CTAs of the pair
+// once all previously issued MMAs of this thread have completed
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+template <bool A_MN, bool B_MN>
+__device__ constexpr uint32_t make_idesc_pair() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(P_TILE_M >> 4) << 24);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_STAGES * P_STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * P_STAGES + 5);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * P_STAGES;
+    const uint32_t tfull0 = empty0 + 8 * P_STAGES;
+    const uint32_t tempty0 = tfull0 + 16;
+    const uint32_t drain = tempty0 + 16;
+    const uint32_t smem_base = smem_u32(smem);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P_STAGES; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull0 + 8 * i, 1);
+            mbar_init(tempty0 + 8 * i, 2 * 32 * EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = pair_id; ok && t < p.total_tiles; t += npairs) {
+                int pi, mt, nt;
+                tile_coords(p, t, pi, mt, nt);
+                const int m0 = mt * P_TILE_M + 128 * rank;
+                // B rows of this CTA: its half of the 256 tile columns, or for
+                // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
+                const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
+                for (int s = 0; ok && s < p.S; ++s) {
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb_local = full0 + 8 * stage;
+                        const uint32_t fb = map_to_cta(fb_local, 0);
+                        if (rank == 0) {
+                            mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                            armed |= 1u << stage;
+                            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                        }
+                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
+                        const uint32_t sb = sa + P_A_BYTES;
+                        const int k0 = kb * BK;
+                        int idx, lrow;
+                        if (!A_MN) {
+                            select(p.selA, pi, s, m0, idx, lrow);
+                            tma_load_2d_pair(sa, &p.mapA[idx], fb, k0, lrow);
+                        } else {
+                            select(p.selA, pi, s, k0, idx, lrow);
+                            tma_load_2d_pair(sa, &p.mapA[idx], fb, m0, lrow);
+                            tma_load_2d_pair(sa + MN_BOX_BYTES, &p.mapA[idx], fb, m0 + MN_BOX, lrow);
+                        }
+                        if (!B_MN) {
+                            select(p.selB, pi, s, n0, idx, lrow);
+                            tma_load_2d_pair(sb, &p.mapB[idx], fb, k0, lrow);
+                        } else {
+                            select(p.selB, pi, s, k0, idx, lrow);
+                            tma_load_2d_pair(sb, &p.mapB[idx], fb, n0, lrow);
+                            tma_load_2d_pair(sb + MN_BOX_BYTES, &p.mapB[idx], fb, n0 + MN_BOX, lrow);
+                        }
+                        if (++stage == P_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // CTA 0's full barriers count both CTAs' bytes: wait until every
+            // copy it armed has landed before the pair can exit.
+            for (int i = 0; i < P_STAGES; ++i)
+                if (armed & (1u << i)) mbar_wait_drain(full0 + 8 * i, (armed_par >> i) & 1u, p.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (CTA 0 only) ----------------
+            constexpr uint32_t idesc = make_idesc_pair<A_MN, B_MN>();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = pair_id; ok && t < p.total_tiles; t += npairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_par = (it >> 1) & 1;
+                if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1u, p)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                uint32_t accumulate = 0;
+                for (int s = 0; ok && s < p.S; ++s) {
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        if (!mbar_wait(full0 + 8 * stage, phase, p)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
+                        const uint32_t sb = sa + P_A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, MN_BOX_BYTES, 1024)
+                                                     : smem_desc(sa + kk * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, MN_BOX_BYTES, 1024)
+                                                     : smem_desc(sb + kk * 32, 16, 1024);
+                            umma_bf16_pair(d, ad, bd, idesc, accumulate);
+                            accumulate = 1;
+                        }
+                        umma_commit_pair_mc(empty0 + 8 * stage);
+                        if (++stage == P_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(tfull0 + 8 * acc);
+            }
+            umma_commit_pair(drain);
+            mbar_wait_drain(drain, 0, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 2..9 of both CTAs) ----------------
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t tempty_leader = map_to_cta(tempty0, 0);
+        int it = 0;
+        for (int t = pair_id; t < p.total_tiles; t += npairs, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_par = (it >> 1) & 1;
+            const bool ok = mbar_wait(tfull0 + 8 * acc, acc_par, p);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            int pi, mt, nt;
+            tile_coords(p, t, pi, mt, nt);
+            const int row = mt * P_TILE_M + 128 * rank + q * 32 + lane;
+            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            run_epilogue<EPI>(p, pi, row, nt, taddr, half);
+            tc_fence_before();
+            mbar_arrive_cluster(tempty_leader + 8 * acc);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -596,13 +888,13 @@ static int kernel_index(int kind, bool amn, bool bmn) {
     return -1;
 }
 
-static KernelFn kernel_at(int i) {
+static KernelFn kernel_at(int i, bool pair) {
     switch (i) {
-        case 0: return tc_gemm_kernel<EPI_COL, false, false>;
-        case 1: return tc_gemm_kernel<EPI_PLAIN, false, false>;
-        case 2: return tc_gemm_kernel<EPI_PLAIN, false, true>;
-        case 3: return tc_gemm_kernel<EPI_DACT, false, true>;
-        case 4: return tc_gemm_kernel<EPI_F32, true, true>;
+        case 0: return pair ? tc_gemm_pair_kernel<EPI_COL, false, false> : tc_gemm_kernel<EPI_COL, false, false>;
+        case 1: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, false> : tc_gemm_kernel<EPI_PLAIN, false, false>;
+        case 2: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, true> : tc_gemm_kernel<EPI_PLAIN, false, true>;
+        case 3: return pair ? tc_gemm_pair_kernel<EPI_DACT, false, true> : tc_gemm_kernel<EPI_DACT, false, true>;
+        case 4: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true> : tc_gemm_kernel<EPI_F32, true, true>;
     }
     return nullptr;
 }
@@ -644,7 +936,11 @@ static void copy_out(Out &o, const OutPlan &src) {
     o.ld = src.ld;
 }
 
+static std::atomic<int> g_tile_mode{0};
+
 }  // namespace tc
+
+void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
 
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     using namespace tc;
@@ -652,7 +948,14 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     if (ki < 0)
         return set_error(TP_ERR_UNSUPPORTED, "no tcgen05 kernel for epilogue %d / majors %d%d", g.kind,
                          int(g.A.mn_major), int(g.B.mn_major));
-    KernelFn fn = kernel_at(ki);
+    // CTA pairs (256-row tiles) unless single-CTA tiles are requested or the
+    // problem has a single 128-row tile.
+    const int mode = g_tile_mode.load();
+    const bool use_pair = mode == TP_TILE_PAIR || (mode == TP_TILE_AUTO && g.M > BM);
+    KernelFn fn = kernel_at(ki, use_pair);
+    const int tile_m = use_pair ? P_TILE_M : BM;
+    // rows of the B tile that one CTA loads per box
+    const int b_box_rows = (use_pair || g.b_dual_off) ? BN / 2 : BN;
     Params prm;
     memset(&prm, 0, sizeof(prm));
     for (int i = 0; i < g.A.n; ++i) {
@@ -661,15 +964,12 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
         if (s != TP_OK) return s;
     }
     for (int i = 0; i < g.B.n; ++i) {
-        tp_status s;
-        if (g.B.mn_major)
-            s = encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, MN_BOX, BK);
-        else
-            s = encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, BK, g.b_dual_off ? BN / 2 : BN);
+        tp_status s = g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, MN_BOX, BK)
+                                   : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, BK, b_box_rows);
         if (s != TP_OK) return s;
     }
-    prm.selA = {g.A.p_stride, g.A.s_stride, g.A.rows_split};
-    prm.selB = {g.B.p_stride, g.B.s_stride, g.B.rows_split};
+    prm.selA = {g.A.p_stride, g.A.s_stride, g.A.rows_split, g.A.n};
+    prm.selB = {g.B.p_stride, g.B.s_stride, g.B.rows_split, g.B.n};
     copy_out(prm.out, g.out);
     copy_out(prm.out2, g.out2);
     copy_out(prm.aux, g.aux);
@@ -684,11 +984,11 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.S = g.S;
     prm.Kseg = g.Kseg;
     prm.num_kb = (g.Kseg + BK - 1) / BK;
-    prm.m_tiles = (g.M + BM - 1) / BM;
+    prm.m_tiles = (g.M + tile_m - 1) / tile_m;
     const int n_per_tile = g.b_dual_off ? BN / 2 : BN;
     prm.n_tiles = (g.N + n_per_tile - 1) / n_per_tile;
     prm.total_tiles = prm.m_tiles * prm.n_tiles * g.P;
-    prm.group_m = 16;
+    prm.group_m = use_pair ? 8 : 16;
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
     prm.accumulate = g.accumulate ? 1 : 0;
@@ -701,23 +1001,66 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.wait_limit_ns = wait_limit_ns();
     if (prm.total_tiles == 0 || prm.num_kb == 0) return TP_OK;
 
-    // opt in to > 48 KB of dynamic shared memory, once per kernel and device
+    // opt in to > 48 KB of dynamic shared memory and size the persistent
+    // grid, once per kernel and device
     static std::mutex mu;
-    static bool attr_set[64][kNumKernels] = {};
+    static bool attr_set[64][2][kNumKernels] = {};
+    static int max_pairs[64][kNumKernels] = {};
     int dev = 0;
     cudaGetDevice(&dev);
+    const int smem_bytes = use_pair ? P_SMEM_BYTES : SMEM_BYTES;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev % 64][ki]) {
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (!attr_set[dev % 64][use_pair][ki]) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
             if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");
-            attr_set[dev % 64][ki] = true;
+            if (use_pair) {
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+                (void)e;
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+                cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+                cfg.dynamicSmemBytes = smem_bytes;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+                if (e != cudaSuccess || n <= 0) {
+                    cudaGetLastError();
+                    n = num_sms() / 2;
+                }
+                max_pairs[dev % 64][ki] = n;
+            }
+            attr_set[dev % 64][use_pair][ki] = true;
         }
     }
-    const int grid = prm.total_tiles < num_sms() ? prm.total_tiles : num_sms();
+    cudaError_t e;
     launch_begin(g.name, st);
-    fn<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    if (use_pair) {
+        const int pairs = std::min(prm.total_tiles, max_pairs[dev % 64][ki]);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fn, prm);
+    } else {
+        const int grid = prm.total_tiles < num_sms() ? prm.total_tiles : num_sms();
+        fn<<<grid, NUM_THREADS, smem_bytes, st>>>(prm);
+        e = cudaGetLastError();
+    }
     launch_end(g.name, st);
     return cuda_check(e, g.name);
 }
