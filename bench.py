@@ -143,6 +143,24 @@ def kernel_flops(w):
             "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H}
 
 
+def recorded_traffic(w, tile_mode, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none for this workload and tiling or the kernel source has
+    changed since it was captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{w.name}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["kernel_source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    if digest != rec.get("sha256") or rec.get("tile_mode") not in (tile_mode, "pair" if tile_mode == "auto" else None):
+        return None
+    return rec.get("bytes_per_launch", {}).get(kernel)
+
+
 def run_gpu(args, w, dist, rank, local, ws):
     import torch
 
@@ -282,6 +300,8 @@ def run_gpu(args, w, dist, rank, local, ws):
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                     "peak_kind": f"bf16 sustained ({peaks['source']})",
                     "algorithmic_flop_per_launch": kf[dom]}
+    if roofline is not None:
+        roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
     step_frac = value / ws / peaks["bf16_tflops_sustained"]
     return {
         "value": round(value, 2), "ms_per_step": round(ms_max / args.steps, 4),
