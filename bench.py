@@ -82,6 +82,12 @@ def max_over_ranks(dist, value, device="cpu"):
     return float(t.item())
 
 
+def job_throughput(world_size, flops_per_step, steps, ms_slowest):
+    """Whole-job TFLOP/s: every rank runs `steps` steps of its own replica; the
+    job takes as long as the slowest rank."""
+    return world_size * flops_per_step * steps / (ms_slowest * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -245,7 +251,7 @@ def run_gpu(args, w, dist, rank, local, ws):
         raise RuntimeError(f"device status {tp.status_str(status)} in timed region")
     ms_max = max_over_ranks(dist, ms, dev)
     flops_step = w.flops()
-    value = ws * flops_step * args.steps / (ms_max * 1e-3) / 1e12
+    value = job_throughput(ws, flops_step, args.steps, ms_max)
 
     # ---- end to end through the C ABI with host buffers ---------------------
     hX = [x.cpu().pin_memory() for x in X]
@@ -274,7 +280,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     e3.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(dist, e2.elapsed_time(e3), dev)
-    e2e_value = ws * flops_step * args.steps / (ms_e2e * 1e-3) / 1e12
+    e2e_value = job_throughput(ws, flops_step, args.steps, ms_e2e)
 
     # ---- roofline of the dominant kernel -----------------------------------
     peaks = load_peaks()
