@@ -1,0 +1,148 @@
+"""FP8 variant of the tensor-parallel MLP -- oracle, TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/`` and ``bench.py``'s CPU legs import this module; it shares no
+code with the CUDA path.
+
+Source: "Megatron-LM 源码精读——大模型并行训练全景" (roger-lv.github.io), s8.2
+(mixed precision / FP8): E4M3 in the forward, E5M2 in the backward, per-tensor
+scaling from the tensor's amax, with the amax reduced across the tensor- and
+data-parallel group.  Readings (also in the design doc):
+  F1 one scale per logical tensor: the amax is the maximum over all T shards
+     (the cross-shard amax all-reduce), scale = fmax / amax computed in fp32
+     (1 when amax is 0), fmax = 448 (E4M3) or 57344 (E5M2);
+  F2 quantisation q = fp8(x * scale): the product is rounded to fp32, then to
+     the FP8 format with round-to-nearest-even, saturating to +-fmax;
+  F3 a GEMM of quantised operands is dequantised by 1 / (scale_a * scale_b)
+     (fp32), applied to the fp32/fp64 sum before bias, activation or residual;
+  F4 the forward quantises X, W1, W2 (E4M3) and the stored bf16 activation A
+     (E4M3); the backward quantises dY (E5M2) and the stored bf16 dPre (E5M2);
+     pre, A, dPre, Y and dX are stored in bf16 (round-to-nearest-even), as in
+     the bf16 variant, and act' uses the stored bf16 pre;
+  F5 bias gradients sum the unquantised bf16 dPre and dY.
+
+FP8 formats (OCP 8-bit floating point): E4M3 -- 1 sign, 4 exponent bits
+(bias 7), 3 mantissa bits, largest finite 448, smallest normal 2^-6, smallest
+subnormal 2^-9, no infinities; E5M2 -- 1 sign, 5 exponent bits (bias 15),
+2 mantissa bits, largest finite 57344, smallest normal 2^-14, smallest
+subnormal 2^-16.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import mlp as _mlp
+
+FORMATS = {
+    # name: (mantissa bits, minimum normal exponent, largest finite)
+    "e4m3": (3, -6, 448.0),
+    "e5m2": (2, -14, 57344.0),
+}
+
+
+def fmax(fmt: str) -> float:
+    return FORMATS[fmt][2]
+
+
+def round_fp8(v, fmt: str):
+    """Round values (exact in fp64) to the FP8 format: nearest, ties to even,
+    saturating to the largest finite value (F2).  Returns fp64 values."""
+    mbits, emin, top = FORMATS[fmt]
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))   # a = m * 2^ex with m in [0.5, 1)
+    e = (ex - 1).astype(np.float64)
+    e = np.maximum(e, emin)               # subnormals share the minimum exponent's quantum
+    quantum = np.exp2(e - mbits)
+    q = np.rint(a / quantum) * quantum    # np.rint: round half to even
+    q = np.minimum(q, top)
+    return np.copysign(q, v) * (a > 0)
+
+
+def round_bf16(x):
+    """Round to bf16 (nearest, ties to even) through the fp32 bit pattern."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def scale_of(amax, fmt: str) -> np.float32:
+    """Per-tensor scale fmax / amax in fp32 (F1); 1 when amax is 0."""
+    amax = np.float32(amax)
+    if amax == 0 or not np.isfinite(amax):
+        return np.float32(1.0)
+    return np.float32(np.float32(fmax(fmt)) / amax)
+
+
+def amax_of(parts) -> np.float32:
+    """Maximum |x| over all shards of one logical tensor (F1)."""
+    return np.float32(max(float(np.max(np.abs(np.asarray(p, np.float64)))) if np.size(p) else 0.0
+                          for p in parts))
+
+
+def quantize(parts, fmt: str):
+    """Quantise every shard of one tensor with the tensor's scale.  Returns
+    (list of quantised values as fp64, scale)."""
+    s = scale_of(amax_of(parts), fmt)
+    out = [round_fp8((np.asarray(p, np.float32) * s).astype(np.float32), fmt) for p in parts]
+    return out, s
+
+
+def dequant(sa, sb) -> float:
+    """Dequantisation factor of a product of two quantised operands (F3)."""
+    return float(np.float32(1.0) / np.float32(np.float32(sa) * np.float32(sb)))
+
+
+def mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act: str, residual: bool):
+    """Forward of the FP8 variant.  X is the full [M, H] input (bf16 values).
+    Returns a dict with pre, A (bf16-rounded, per shard), Y (fp64, before the
+    bf16 store), and the quantised operands and scales the backward reuses."""
+    T = len(W1s)
+    (Xq,), sx = quantize([X], "e4m3")
+    W1q, sw1 = quantize(W1s, "e4m3")
+    W2q, sw2 = quantize(W2s, "e4m3")
+    d1 = dequant(sx, sw1)
+    pre, A = [], []
+    for i in range(T):
+        p = (Xq @ W1q[i].T) * d1
+        if b1s is not None and b1s[i] is not None:
+            p = p + np.asarray(b1s[i], np.float64)
+        pre.append(round_bf16(p))
+        A.append(round_bf16(_mlp.act_fwd(p, act)))
+    Aq, sa = quantize(A, "e4m3")
+    d2 = dequant(sa, sw2)
+    Y = None
+    for i in range(T):
+        part = Aq[i] @ W2q[i].T
+        Y = part if Y is None else Y + part
+    Y = Y * d2
+    if b2 is not None:
+        Y = Y + np.asarray(b2, np.float64)
+    if residual:
+        Y = Y + np.asarray(X, np.float64)
+    return {"pre": pre, "A": A, "Y": Y, "Xq": Xq, "W1q": W1q, "W2q": W2q, "Aq": Aq,
+            "sx": sx, "sw1": sw1, "sw2": sw2, "sa": sa}
+
+
+def mlp_bwd_fp8(dY, f, act: str, residual: bool):
+    """Backward of the FP8 variant given the forward's dict ``f``."""
+    T = len(f["W1q"])
+    (dYq,), sdy = quantize([dY], "e5m2")
+    d = dequant(sdy, f["sw2"])
+    dPre = []
+    for i in range(T):
+        dA = (dYq @ f["W2q"][i]) * d
+        dPre.append(round_bf16(_mlp.act_bwd(f["pre"][i], dA, act)))
+    dPq, sdp = quantize(dPre, "e5m2")
+    dW2 = [(dYq.T @ f["Aq"][i]) * dequant(sdy, f["sa"]) for i in range(T)]
+    dW1 = [(dPq[i].T @ f["Xq"]) * dequant(sdp, f["sx"]) for i in range(T)]
+    dX = None
+    for i in range(T):
+        part = dPq[i] @ f["W1q"][i]
+        dX = part if dX is None else dX + part
+    dX = dX * dequant(sdp, f["sw1"])
+    if residual:
+        dX = dX + np.asarray(dY, np.float64)
+    db1 = [p.sum(axis=0) for p in dPre]
+    db2 = np.asarray(dY, np.float64).sum(axis=0)
+    return {"dPre": dPre, "dX": dX, "dW1": dW1, "dW2": dW2, "db1": db1, "db2": db2, "sdy": sdy, "sdp": sdp}

@@ -1,0 +1,94 @@
+"""Pins of the FP8 oracle (oracle/fp8.py) against torch's float8/bfloat16
+casts (library routines), the formats' definitions and the plain fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8
+
+
+def _torch_round(x, fmt):
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.tensor(x, dtype=torch.float32).to(dt).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_round_fp8_matches_torch_in_range(fmt):
+    rng = np.random.default_rng(0)
+    top = fp8.fmax(fmt)
+    # log-uniform magnitudes over the whole range incl. subnormals, both signs
+    mags = np.exp2(rng.uniform(np.log2(top) - 30, np.log2(top) + 0.0, 200000)).astype(np.float32)
+    x = (mags * rng.choice([-1, 1], mags.size)).astype(np.float32)
+    x = x[np.abs(x) <= top]
+    assert np.array_equal(fp8.round_fp8(x, fmt), _torch_round(x, fmt))
+    # every representable value and every midpoint between neighbours (ties)
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    vals = np.unique(codes.view(dt).to(torch.float64).numpy())
+    vals = vals[np.isfinite(vals)]
+    assert np.array_equal(fp8.round_fp8(vals, fmt), vals)
+    pos = vals[vals >= 0]
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    assert np.array_equal(fp8.round_fp8(mids, fmt), _torch_round(mids, fmt))
+
+
+def test_format_definitions():
+    assert fp8.round_fp8(np.array([1e6, -1e6]), "e4m3").tolist() == [448.0, -448.0]   # saturates
+    assert fp8.round_fp8(np.array([460.0, 470.0]), "e4m3").tolist() == [448.0, 448.0]
+    assert fp8.round_fp8(np.array([1e9]), "e5m2").tolist() == [57344.0]
+    assert fp8.round_fp8(np.array([2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11]), "e4m3").tolist() == \
+        [2.0 ** -9, 0.0, 2.0 ** -9]
+    assert fp8.round_fp8(np.array([2.0 ** -16, 2.0 ** -17]), "e5m2").tolist() == [2.0 ** -16, 0.0]
+    assert fp8.round_fp8(np.array([1.0 + 2 ** -4, 1.0 + 3 * 2 ** -4]), "e4m3").tolist() == [1.0, 1.25]
+
+
+def test_round_bf16_matches_torch():
+    x = np.random.default_rng(1).standard_normal(100000).astype(np.float32) * 10
+    assert np.array_equal(fp8.round_bf16(x), torch.tensor(x).to(torch.bfloat16).double().numpy())
+
+
+def test_scale_maps_amax_to_fmax():
+    x = np.random.default_rng(2).standard_normal((7, 9)).astype(np.float32)
+    (q,), s = fp8.quantize([x], "e4m3")
+    assert np.max(np.abs(q)) == 448.0
+    assert s == np.float32(np.float32(448.0) / np.float32(np.max(np.abs(x))))
+    (q0,), s0 = fp8.quantize([np.zeros((2, 2), np.float32)], "e5m2")
+    assert s0 == 1.0 and not q0.any()
+    # one scale across shards: the shard holding the amax reaches fmax, the other does not
+    parts, s = fp8.quantize([x, x / 4], "e4m3")
+    assert np.max(np.abs(parts[0])) == 448.0 and np.max(np.abs(parts[1])) <= 112.0
+
+
+@pytest.mark.parametrize("act", ["gelu_tanh", "swiglu"])
+def test_fp8_pipeline_close_to_exact_mlp(act):
+    """The FP8 variant approximates the exact MLP within the formats' relative
+    precision (E4M3 2^-4, E5M2 2^-3 per element); a transposed operand, an
+    inverted scale or a missing term would be off by orders of magnitude."""
+    rng = np.random.default_rng(3)
+    M, H, F, T = 64, 96, 128, 4
+    g = 2 if act == "swiglu" else 1
+    X = fp8.round_bf16(rng.standard_normal((M, H)))
+    W1 = fp8.round_bf16(rng.standard_normal((g * F, H)) * 0.1)
+    W2 = fp8.round_bf16(rng.standard_normal((H, F)) * 0.1)
+    b1 = fp8.round_bf16(rng.standard_normal(g * F) * 0.1)
+    b2 = fp8.round_bf16(rng.standard_normal(H) * 0.1)
+    dY = fp8.round_bf16(rng.standard_normal((M, H)))
+    W1s = oracle.shard_column_weight(W1, T, act)
+    b1s = oracle.shard_column_bias(b1, T, act)
+    W2s = oracle.shard_row_weight(W2, T)
+    f = fp8.mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act, True)
+    g8 = fp8.mlp_bwd_fp8(dY, f, act, True)
+    pre, A, Y = oracle.mlp_fwd(X, W1s, b1s, W2s, b2, act, True)
+    g64 = oracle.mlp_bwd(dY, X, W1s, W2s, pre, A, act, True)
+
+    def rel(a, b):
+        return np.max(np.abs(np.asarray(a) - np.asarray(b))) / np.max(np.abs(b))
+
+    assert rel(f["Y"], Y) < 0.05
+    assert rel(g8["dX"], g64["dX"]) < 0.1
+    for i in range(T):
+        assert rel(g8["dW1"][i], g64["dW1"][i]) < 0.15
+        assert rel(g8["dW2"][i], g64["dW2"][i]) < 0.15
+        assert rel(g8["db1"][i], g64["db1"][i]) < 0.1
+    assert rel(g8["db2"], g64["db2"]) == 0.0
