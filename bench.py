@@ -182,7 +182,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
                    residual=w.residual, seq_parallel=w.seq_parallel)
     full = synth.mlp_tensors(w)
-    td = bf if w.dtype == "bf16" else torch.float32
+    td = torch.float32 if w.dtype == "f32" else bf
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=td)
@@ -218,7 +218,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream)
+        lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp if w.dtype == "fp8" else None)
         lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
 
     # ---- device-resident timing --------------------------------------------
@@ -302,13 +302,16 @@ def run_gpu(args, w, dist, rank, local, ws):
         n, tot = kernels[dom]
         achieved = kf[dom] / ((tot / n) * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
+        peak_kind = f"bf16 sustained ({peaks['source']})"
+        if w.dtype == "fp8":
+            # dense fp8 : bf16 tensor rate is 4.5 : 2.25 PFLOP/s nominal
+            peak, peak_kind = 2.0 * peak, f"fp8 = 2 x bf16 sustained ({peaks['source']}) x nominal ratio"
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                    "peak_kind": f"bf16 sustained ({peaks['source']})",
-                    "algorithmic_flop_per_launch": kf[dom]}
-    if roofline is not None:
+                    "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
+    if roofline is not None and w.dtype == "bf16":
         roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
-    step_frac = value / ws / peaks["bf16_tflops_sustained"]
+    step_frac = value / ws / (peaks["bf16_tflops_sustained"] * (2.0 if w.dtype == "fp8" else 1.0))
     return {
         "value": round(value, 2), "ms_per_step": round(ms_max / args.steps, 4),
         "pct_of_dense_bf16_peak": round(100 * step_frac, 2),
@@ -388,12 +391,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", default="workload", choices=["workload", "fp8"],
+                    help="fp8: the FP8 variant (E4M3 forward, E5M2 backward, bf16 buffers) of the workload")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = synth.WORKLOADS[args.workload]
+    if args.dtype == "fp8":
+        import dataclasses
+        w = dataclasses.replace(w, dtype="fp8")
     if w.kind != "mlp":
         raise SystemExit("bench.py times the MLP workloads (gpt, swiglu, sp, tiny)")
     ws, rank, local = dist_env()

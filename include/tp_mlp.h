@@ -30,7 +30,9 @@
  *     without sequence parallelism activations take a 1-entry array.
  *   Element types.  dtype TP_DT_BF16: every activation, weight, bias and
  *     activation gradient is bf16; weight and bias gradients (dW*, db*) are
- *     fp32.  dtype TP_DT_F32: everything is fp32.  Products accumulate in fp32.
+ *     fp32.  dtype TP_DT_F32: everything is fp32.  TP_DT_FP8: the buffers of
+ *     TP_DT_BF16, FP8 products inside (see tp_dtype).  Products accumulate in
+ *     fp32.
  *   Alignment.  Every device pointer is 16-byte aligned; H, F/T and (for the
  *     row layer input) the shard width are multiples of 8.
  *   Ownership.  The caller owns every device buffer, including the workspace.
@@ -74,7 +76,17 @@ typedef enum {
 } tp_status;
 
 typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act;
-typedef enum { TP_DT_F32 = 0, TP_DT_BF16 = 1 } tp_dtype;
+/* TP_DT_FP8: bf16 buffers at the interface (exactly as TP_DT_BF16), FP8 GEMMs
+ * inside ("Megatron-LM 源码精读" s8.2): every GEMM operand is quantised per
+ * tensor with scale = fmax / amax, the amax taken over all shards of the
+ * tensor -- E4M3 (fmax 448) for X, W1, W2 and the activation A in the forward,
+ * E5M2 (fmax 57344) for dY and dPre in the backward -- the products run on
+ * tcgen05 kind::f8f6f4 in fp32 and are dequantised by 1/(scale_a*scale_b)
+ * before the epilogue.  pre, A, dPre, Y, dX stay bf16; bias gradients sum the
+ * unquantised bf16 dPre and dY.  Needs H and F/T multiples of 16, the forward
+ * through tp_mlp_fwd_ws, and the same workspace for the following backward
+ * (it carries the quantised forward operands).  MLP entry points only. */
+typedef enum { TP_DT_F32 = 0, TP_DT_BF16 = 1, TP_DT_FP8 = 2 } tp_dtype;
 
 /* Problem description shared by the MLP and the single-layer entry points.
  * For the single layers, H is the replicated width (column input, row output)
@@ -104,9 +116,10 @@ typedef struct tp_mlp tp_mlp; /* opaque handle: validated descriptor */
 TP_API tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out);
 TP_API void tp_mlp_destroy(tp_mlp *h);
 
-/* Bytes of device workspace tp_mlp_bwd needs (256-byte aligned start).  It
- * holds dPre_i (M x g*Fs per shard, in dtype) and fp32 partial column sums for
- * the bias gradients. */
+/* Bytes of device workspace tp_mlp_bwd (and, for TP_DT_FP8, tp_mlp_fwd_ws)
+ * needs (256-byte aligned start).  It holds dPre_i (M x g*Fs per shard, bf16
+ * or fp32), fp32 partial column sums for the bias gradients and, for FP8, the
+ * per-tensor amax values and the quantised operands. */
 TP_API size_t tp_mlp_workspace_bytes(const tp_mlp *h);
 
 /* ---- MLP forward ("Megatron-LM 源码精读" s3.3 figure) ------------------------
@@ -122,6 +135,16 @@ TP_API size_t tp_mlp_workspace_bytes(const tp_mlp *h);
 TP_API tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1,
                      const void *const *b1, const void *const *W2, const void *b2,
                      void *const *Y, void *const *pre, void *const *A, void *stream);
+
+/* tp_mlp_fwd with a workspace (>= tp_mlp_workspace_bytes, 256-byte aligned).
+ * Required for TP_DT_FP8, where the forward quantises X, W1, W2 and A into the
+ * workspace and tp_mlp_bwd must then be given the same workspace, unchanged in
+ * between; for the other dtypes the workspace is not touched.  TP_DT_FP8
+ * through tp_mlp_fwd returns TP_ERR_ARG. */
+TP_API tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *const *W1,
+                               const void *const *b1, const void *const *W2, const void *b2,
+                               void *const *Y, void *const *pre, void *const *A, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /* ---- MLP backward ------------------------------------------------------------
  * dY  : like Y;  X, W1, W2, pre, A: as passed to / produced by tp_mlp_fwd
@@ -202,6 +225,17 @@ TP_API tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *
                                            const void *const *X, const void *const *W,
                                            void *const *dX, void *const *dW, void *db,
                                            void *stream);
+
+/* Per-tensor FP8 quantisation of one logical tensor split over `nbuf` bf16
+ * buffers (its shards): amax = max |x| over all buffers (the cross-shard amax
+ * reduction), scale = fmax / amax in fp32 (1 if amax is 0), then
+ * out_k = fp8(in_k * scale) with round-to-nearest-even, saturating to +-fmax
+ * ("Megatron-LM 源码精读" s8.2).  fmt: 0 = E4M3 (fmax 448), 1 = E5M2 (57344).
+ * in/out: nbuf (<= 40) pointers, buffer k holding n[k] elements (n[k] % 8 == 0;
+ * out one byte per element).  amax: one device float, overwritten.  This is
+ * the quantiser the TP_DT_FP8 path uses for every operand. */
+TP_API tp_status tp_fp8_quantize(const void *const *in, void *const *out, const int64_t *n, int nbuf,
+                                 int fmt, float *amax, void *stream);
 
 /* ---- status, limits, diagnostics ---------------------------------------- */
 

@@ -146,3 +146,51 @@ def mlp_bwd_fp8(dY, f, act: str, residual: bool):
     db1 = [p.sum(axis=0) for p in dPre]
     db2 = np.asarray(dY, np.float64).sum(axis=0)
     return {"dPre": dPre, "dX": dX, "dW1": dW1, "dW2": dW2, "db1": db1, "db2": db2, "sdy": sdy, "sdp": sdp}
+
+
+def mlp_sampled_fp8(rows, units, X, W1s, b1s, W2s, b2, dY, act: str, residual: bool):
+    """The FP8 variant's Y and dX at the given token rows and its dW1 rows,
+    dW2 columns and db1 entries at the given hidden units of every shard
+    (``units[i]`` indexes [0, F/T) of shard i; for SwiGLU both the gate and the
+    up row of a unit), plus db2 in full.
+
+    The per-tensor scales of A and dPre depend on every token, so A and dPre
+    are formed in full (two GEMMs); every other product is evaluated only where
+    sampled.  Same arithmetic as mlp_fwd_fp8 / mlp_bwd_fp8."""
+    rows = np.asarray(rows)
+    T = len(W1s)
+    fs = np.asarray(W2s[0]).shape[1]
+    (Xq,), sx = quantize([X], "e4m3")
+    W1q, sw1 = quantize(W1s, "e4m3")
+    W2q, sw2 = quantize(W2s, "e4m3")
+    d1 = dequant(sx, sw1)
+    pre, A = [], []
+    for i in range(T):
+        p = (Xq @ W1q[i].T) * d1
+        if b1s is not None and b1s[i] is not None:
+            p = p + np.asarray(b1s[i], np.float64)
+        pre.append(round_bf16(p))
+        A.append(round_bf16(_mlp.act_fwd(p, act)))
+        del p
+    Aq, sa = quantize(A, "e4m3")
+    Y = sum(Aq[i][rows] @ W2q[i].T for i in range(T)) * dequant(sa, sw2)
+    if b2 is not None:
+        Y = Y + np.asarray(b2, np.float64)
+    if residual:
+        Y = Y + np.asarray(X, np.float64)[rows]
+    (dYq,), sdy = quantize([dY], "e5m2")
+    d = dequant(sdy, sw2)
+    dPre = [round_bf16(_mlp.act_bwd(pre[i], (dYq @ W2q[i]) * d, act)) for i in range(T)]
+    dPq, sdp = quantize(dPre, "e5m2")
+    dX = sum(dPq[i][rows] @ W1q[i] for i in range(T)) * dequant(sdp, sw1)
+    if residual:
+        dX = dX + np.asarray(dY, np.float64)[rows]
+    out = {"Y": Y, "dX": dX, "dW1": [], "dW2": [], "db1": [],
+           "db2": np.asarray(dY, np.float64).sum(axis=0)}
+    for i in range(T):
+        u = np.asarray(units[i])
+        sel = np.concatenate([u, fs + u]) if act == "swiglu" else u
+        out["dW1"].append((dPq[i][:, sel].T @ Xq) * dequant(sdp, sx))
+        out["dW2"].append((dYq.T @ Aq[i][:, u]) * dequant(sdy, sa))
+        out["db1"].append(dPre[i][:, sel].sum(axis=0))
+    return out

@@ -116,7 +116,7 @@ class Workload:
     F: int
     T: int
     act: str          # "gelu_tanh" | "swiglu" | "none"
-    dtype: str        # "f32" | "bf16"
+    dtype: str        # "f32" | "bf16" | "fp8" (bf16 buffers, FP8 products)
     has_bias: bool
     bias_std: float
     residual: bool
@@ -170,7 +170,7 @@ def mlp_tensors(w: Workload, M: int | None = None):
     rows), W2 is [H, F], X and dY are [M, H].  Biases are None when absent."""
     M = w.M if M is None else M
     g = w.g
-    rnd = round_bf16 if w.dtype == "bf16" else (lambda a: a)
+    rnd = (lambda a: a) if w.dtype == "f32" else round_bf16
     t = {
         "X": rnd(normal(SEED_BASE + TID_X, (M, w.H), w.x_std)),
         "W1": rnd(normal(SEED_BASE + TID_W1, (g * w.F, w.H), w.w_std)),

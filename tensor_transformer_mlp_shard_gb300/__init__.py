@@ -6,6 +6,7 @@ inside the tcgen05 GEMM kernels of ``libtpmlp.so`` (C ABI in
 ``include/tp_mlp.h``).  This package is the thin Python binding.
 """
 from .binding import (ACT, DTYPE, Layout, TPMLP, TpError, alloc_workspace, debug_wait_timeout,  # noqa: F401
+                      fp8_quantize,
                       launch_count, lib, library_path, linear_col, linear_col_bwd, linear_row, linear_row_bwd,
                       linear_row_bwd_noalloc,
                       linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_tile_mode, set_wait_limit_ns,

@@ -18,8 +18,8 @@ import torch
 from . import build as _build
 
 ACT = {"none": 0, "gelu_tanh": 1, "swiglu": 2}
-DTYPE = {"f32": 0, "bf16": 1}
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}  # fp8: bf16 buffers
 STATUS = {0: "TP_OK", 1: "TP_ERR_ARG", 2: "TP_ERR_SHAPE", 3: "TP_ERR_UNSUPPORTED", 4: "TP_ERR_CUDA",
           5: "TP_ERR_TIMEOUT"}
 MAX_SHARDS = 16
@@ -54,6 +54,7 @@ SIGNATURES = {
     "tp_mlp_destroy": (None, [VP]),
     "tp_mlp_workspace_bytes": (ctypes.c_size_t, [VP]),
     "tp_mlp_fwd": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP]),
+    "tp_mlp_fwd_ws": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_mlp_bwd": (ctypes.c_int, [VP, PP, PP, PP, PP, PP, PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_col": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP]),
     "tp_linear_row": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP]),
@@ -61,6 +62,7 @@ SIGNATURES = {
     "tp_linear_col_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd_noalloc": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP]),
+    "tp_fp8_quantize": (ctypes.c_int, [PP, PP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int, VP, VP]),
     "tp_sync_status": (ctypes.c_int, [VP]),
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
@@ -196,7 +198,9 @@ class TPMLP(Layout):
     def workspace_bytes(self) -> int:
         return int(lib().tp_mlp_workspace_bytes(self._h))
 
-    def fwd(self, X, W1, b1, W2, b2, Y, pre, A, stream=None):
+    def fwd(self, X, W1, b1, W2, b2, Y, pre, A, stream=None, workspace=None):
+        """Forward; `workspace` (required for dtype "fp8") must then be passed,
+        unchanged, to the following bwd."""
         c, T, H, Fs, g = self._c, self.T, self.H, self.Fs, self.g
         px = c.tensors("X", X, self.nx, (self.xrows, H))
         pw1 = c.tensors("W1", W1, T, (g * Fs, H))
@@ -206,8 +210,13 @@ class TPMLP(Layout):
         py = c.tensors("Y", Y, self.nx, (self.xrows, H))
         pp = c.optional("pre", pre, T, (self.M, g * Fs))
         pa = c.tensors("A", A, T, (self.M, Fs))
-        _check(lib().tp_mlp_fwd(self._h, _arr(px), _arr(pw1), _arr(pb1), _arr(pw2), pb2, _arr(py), _arr(pp),
-                                _arr(pa), _stream(stream)))
+        if workspace is None:
+            _check(lib().tp_mlp_fwd(self._h, _arr(px), _arr(pw1), _arr(pb1), _arr(pw2), pb2, _arr(py), _arr(pp),
+                                    _arr(pa), _stream(stream)))
+        else:
+            ws_ptr, ws_bytes = _workspace(workspace, self.workspace_bytes())
+            _check(lib().tp_mlp_fwd_ws(self._h, _arr(px), _arr(pw1), _arr(pb1), _arr(pw2), pb2, _arr(py),
+                                       _arr(pp), _arr(pa), ws_ptr, ws_bytes, _stream(stream)))
 
     def bwd(self, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace, stream=None):
         c, T, H, Fs, g = self._c, self.T, self.H, self.Fs, self.g
@@ -325,6 +334,28 @@ def linear_row_bwd_noalloc(layout: Layout, dY, X, W, dX, dW, db, stream=None):
     pdb = c.tensors("db", db, 1, (H,), f32)[0] if layout.has_bias else None
     _check(lib().tp_linear_row_bwd_noalloc(ctypes.byref(d), _arr(pdy), _arr(px), _arr(pw), _arr(pdx), _arr(pdw),
                                            pdb, _stream(stream)))
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def fp8_quantize(inputs, outputs, fmt: str, amax, stream=None):
+    """Quantise one tensor split over bf16 buffers `inputs` into uint8 buffers
+    `outputs` (same element counts) with one per-tensor scale; the amax lands
+    in the one-element fp32 CUDA tensor `amax`."""
+    inputs, outputs = list(inputs), list(outputs)
+    if len(inputs) != len(outputs):
+        raise ValueError("inputs and outputs differ in length")
+    for a, b in zip(inputs, outputs):
+        if not (a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous()):
+            raise ValueError("contiguous CUDA tensors required")
+        if a.dtype != torch.bfloat16 or b.dtype != torch.uint8 or a.numel() != b.numel():
+            raise ValueError("bf16 inputs and uint8 outputs of equal sizes required")
+    if not (amax.is_cuda and amax.dtype == torch.float32 and amax.numel() >= 1):
+        raise ValueError("amax must be a CUDA float32 tensor")
+    n = (ctypes.c_int64 * len(inputs))(*[t.numel() for t in inputs])
+    _check(lib().tp_fp8_quantize(_arr([t.data_ptr() for t in inputs]), _arr([t.data_ptr() for t in outputs]), n,
+                                 len(inputs), FP8_FORMATS[fmt], amax.data_ptr(), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

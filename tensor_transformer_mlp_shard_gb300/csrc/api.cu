@@ -150,7 +150,8 @@ static tp_status check_one(const void *p, const char *name) {
 static tp_status validate_desc(const tp_mlp_desc *d) {
     if (!d) return set_error(TP_ERR_ARG, "descriptor is NULL");
     if (d->act < TP_ACT_NONE || d->act > TP_ACT_SWIGLU) return set_error(TP_ERR_ARG, "bad act %d", d->act);
-    if (d->dtype != TP_DT_F32 && d->dtype != TP_DT_BF16) return set_error(TP_ERR_ARG, "bad dtype %d", d->dtype);
+    if (d->dtype != TP_DT_F32 && d->dtype != TP_DT_BF16 && d->dtype != TP_DT_FP8)
+        return set_error(TP_ERR_ARG, "bad dtype %d", d->dtype);
     const int flags[4] = {d->has_bias, d->residual, d->seq_parallel, d->wgrad_accumulate};
     for (int f : flags)
         if (f != 0 && f != 1) return set_error(TP_ERR_ARG, "boolean flags must be 0 or 1");
@@ -166,6 +167,8 @@ static tp_status validate_desc(const tp_mlp_desc *d) {
     const int Fs = d->F / d->T;
     if (Fs % 8) return set_error(TP_ERR_SHAPE, "F/T=%d must be a multiple of 8", Fs);
     if (d->H > (1 << 20) || Fs > (1 << 20)) return set_error(TP_ERR_SHAPE, "width above 2^20");
+    if (d->dtype == TP_DT_FP8 && (d->H % 16 || Fs % 16))
+        return set_error(TP_ERR_SHAPE, "FP8 needs H and F/T to be multiples of 16 (H=%d, F/T=%d)", d->H, Fs);
     if (d->seq_parallel) {
         if (d->S % d->T) return set_error(TP_ERR_SHAPE, "sequence parallel needs S %% T == 0 (S=%d, T=%d)", d->S, d->T);
         if (d->dtype == TP_DT_BF16 && M > 0 && (M / d->T) % 128)
@@ -188,14 +191,14 @@ static Dims dims_of(const tp_mlp_desc *d) {
     x.g = d->act == TP_ACT_SWIGLU ? 2 : 1;
     x.nx = d->seq_parallel ? d->T : 1;
     x.rs = d->seq_parallel ? x.M / d->T : 0;
-    x.es = d->dtype == TP_DT_BF16 ? 2 : 4;
+    x.es = d->dtype == TP_DT_F32 ? 4 : 2;  // FP8 keeps bf16 buffers at the interface
     return x;
 }
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 static tp_status run_gemm(const GemmPlan &g, int dtype, cudaStream_t st) {
-    return dtype == TP_DT_BF16 ? launch_tc_gemm(g, st) : launch_simt_gemm(g, st);
+    return dtype == TP_DT_F32 ? launch_simt_gemm(g, st) : launch_tc_gemm(g, st);
 }
 
 // plan helpers --------------------------------------------------------------
@@ -346,7 +349,7 @@ static tp_status colsum(const tp_mlp_desc *d, const char *name, const void *cons
     c.N = N;
     for (int i = 0; i < kMaxShards; ++i) c.out[i] = i < P ? static_cast<float *>(out[i]) : nullptr;
     c.partials = partials;
-    return launch_colsum(c, d->dtype, st);
+    return launch_colsum(c, d->dtype == TP_DT_F32 ? TP_DT_F32 : TP_DT_BF16, st);
 }
 
 static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
@@ -354,7 +357,8 @@ static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
     return align256(sizeof(float) * static_cast<size_t>(P) * colsum_chunks(x.M) * N);
 }
 
-static size_t mlp_ws_layout(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
+// Workspace of the backward: dPre_i (bf16/fp32) then the bias partials.
+static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
     const Dims x = dims_of(d);
     const size_t shard = align256(static_cast<size_t>(x.M) * x.g * x.Fs * x.es);
     if (dpre_shard_bytes) *dpre_shard_bytes = shard;
@@ -366,12 +370,243 @@ static size_t mlp_ws_layout(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
     return shard * x.T + part;
 }
 
+// FP8 region (after the backward region): amax slots, then the quantised
+// operands.  The forward fills Xq, W1q, W2q, Aq and their amax slots; the
+// backward reads them and fills dYq, dPq.
+enum { AMAX_X = 0, AMAX_W1, AMAX_W2, AMAX_A, AMAX_DY, AMAX_DP, AMAX_SLOTS = 8 };
+struct Fp8Layout {
+    size_t amax, xq, w1q, w1q_shard, w2q, w2q_shard, aq, aq_shard, dyq, dpq, dpq_shard, end;
+};
+
+static Fp8Layout fp8_layout(const tp_mlp_desc *d) {
+    const Dims x = dims_of(d);
+    Fp8Layout L;
+    size_t o = align256(bwd_ws_bytes(d, nullptr));
+    L.amax = o;
+    o += 256;
+    L.xq = o;
+    o += align256(size_t(x.M) * x.H);
+    L.w1q_shard = align256(size_t(x.g) * x.Fs * x.H);
+    L.w1q = o;
+    o += L.w1q_shard * x.T;
+    L.w2q_shard = align256(size_t(x.H) * x.Fs);
+    L.w2q = o;
+    o += L.w2q_shard * x.T;
+    L.aq_shard = align256(size_t(x.M) * x.Fs);
+    L.aq = o;
+    o += L.aq_shard * x.T;
+    L.dyq = o;
+    o += align256(size_t(x.M) * x.H);
+    L.dpq_shard = align256(size_t(x.M) * x.g * x.Fs);
+    L.dpq = o;
+    o += L.dpq_shard * x.T;
+    L.end = o;
+    return L;
+}
+
+static size_t mlp_ws_layout(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
+    const size_t b = bwd_ws_bytes(d, dpre_shard_bytes);
+    return d->dtype == TP_DT_FP8 ? fp8_layout(d).end : b;
+}
+
 static tp_status zero_grads(const tp_mlp_desc *d, void *const *dW, int nW, size_t wbytes, void *const *db, int ndb,
                             size_t dbbytes, cudaStream_t st) {
     if (!d->wgrad_accumulate)
         for (int i = 0; i < nW; ++i) TRY(cuda_check(cudaMemsetAsync(dW[i], 0, wbytes, st), "cudaMemsetAsync(dW)"));
     if (db)
         for (int i = 0; i < ndb; ++i) TRY(cuda_check(cudaMemsetAsync(db[i], 0, dbbytes, st), "cudaMemsetAsync(db)"));
+    return TP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 variant ("Megatron-LM 源码精读" s8.2): every GEMM operand is quantised
+// per tensor -- E4M3 for X, W1, W2 and A in the forward, E5M2 for dY and
+// dPre in the backward -- with one scale per tensor over all its shards; the
+// GEMMs run on tcgen05 kind::f8f6f4 and dequantise in the epilogue.  pre, A,
+// dPre, Y and dX stay bf16; bias gradients sum the unquantised bf16 tensors.
+// ---------------------------------------------------------------------------
+static void set_fp8(GemmPlan &g, int fa, int fb, const float *amax, int slot_a, int slot_b) {
+    g.fp8 = true;
+    g.fmt_a = fa;
+    g.fmt_b = fb;
+    g.amax_a = amax + slot_a;
+    g.amax_b = amax + slot_b;
+}
+
+static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W1, const void *const *b1,
+                         const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                         void *ws, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    const int gw = x.g * x.Fs;
+    const Fp8Layout L = fp8_layout(d);
+    char *base = static_cast<char *>(ws);
+    float *amax = reinterpret_cast<float *>(base + L.amax);
+    void *xq = base + L.xq;
+    void *w1q[kMaxShards], *w2q[kMaxShards], *aq[kMaxShards];
+    for (int i = 0; i < x.T; ++i) {
+        w1q[i] = base + L.w1q + i * L.w1q_shard;
+        w2q[i] = base + L.w2q + i * L.w2q_shard;
+        aq[i] = base + L.aq + i * L.aq_shard;
+    }
+    // quantise X (E4M3; sequence shards are gathered into one buffer), W1, W2
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    const size_t rows = x.rs ? x.rs : x.M;
+    for (int j = 0; j < x.nx; ++j)
+        segs[n++] = {X[j], static_cast<char *>(xq) + j * rows * x.H, (long long)(rows * x.H), AMAX_X, FP8_E4M3};
+    for (int i = 0; i < x.T; ++i) segs[n++] = {W1[i], w1q[i], (long long)gw * x.H, AMAX_W1, FP8_E4M3};
+    for (int i = 0; i < x.T; ++i) segs[n++] = {W2[i], w2q[i], (long long)x.H * x.Fs, AMAX_W2, FP8_E4M3};
+    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    // column GEMM: pre_i = Xq W1q_i^T / (s_x s_w1) + b1_i, A_i = act(pre_i)
+    {
+        GemmPlan g;
+        g.name = "col_fwd";
+        g.kind = EPI_COL;
+        g.act = d->act;
+        g.M = x.M;
+        g.N = x.Fs;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.H;
+        const void *xa[1] = {xq};
+        set_operand(g.A, xa, 1, x.M, x.H, false, 0, 0, 0);
+        set_operand(g.B, w1q, x.T, gw, x.H, false, 1, 0, 0);
+        g.b_dual_off = d->act == TP_ACT_SWIGLU ? x.Fs : 0;
+        set_out(g.out, reinterpret_cast<const void *const *>(A), x.T, 1, 0, x.Fs);
+        if (pre) set_out(g.out2, reinterpret_cast<const void *const *>(pre), x.T, 1, 0, gw);
+        set_bias(g, d->has_bias ? b1 : nullptr, x.T, 1);
+        set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_X, AMAX_W1);
+        TRY(launch_tc_gemm(g, st));
+    }
+    // quantise A (E4M3, one scale over all shards)
+    n = 0;
+    for (int i = 0; i < x.T; ++i) segs[n++] = {A[i], aq[i], (long long)x.M * x.Fs, AMAX_A, FP8_E4M3};
+    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    // row GEMM: Y = sum_i Aq_i W2q_i^T / (s_a s_w2) + b2 (+ X)
+    GemmPlan g;
+    g.name = "row_fwd";
+    g.kind = EPI_PLAIN;
+    g.M = x.M;
+    g.N = x.H;
+    g.P = 1;
+    g.S = x.T;
+    g.Kseg = x.Fs;
+    set_operand(g.A, aq, x.T, x.M, x.Fs, false, 0, 1, 0);
+    set_operand(g.B, w2q, x.T, x.H, x.Fs, false, 0, 1, 0);
+    set_out(g.out, reinterpret_cast<const void *const *>(Y), x.nx, 0, x.rs, x.H);
+    if (d->residual) set_out(g.aux, X, x.nx, 0, x.rs, x.H);
+    const void *bb[1] = {b2};
+    set_bias(g, d->has_bias ? bb : nullptr, 1, 0);
+    set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_A, AMAX_W2);
+    return launch_tc_gemm(g, st);
+}
+
+static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void *const *pre, void *const *dX,
+                         void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *ws, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    const int gw = x.g * x.Fs;
+    const Fp8Layout L = fp8_layout(d);
+    size_t shard_bytes = 0;
+    bwd_ws_bytes(d, &shard_bytes);
+    char *base = static_cast<char *>(ws);
+    float *amax = reinterpret_cast<float *>(base + L.amax);
+    float *partials = reinterpret_cast<float *>(base + x.T * shard_bytes);
+    void *xq = base + L.xq, *dyq = base + L.dyq;
+    void *w1q[kMaxShards], *w2q[kMaxShards], *aq[kMaxShards], *dpq[kMaxShards], *dpre[kMaxShards];
+    for (int i = 0; i < x.T; ++i) {
+        w1q[i] = base + L.w1q + i * L.w1q_shard;
+        w2q[i] = base + L.w2q + i * L.w2q_shard;
+        aq[i] = base + L.aq + i * L.aq_shard;
+        dpq[i] = base + L.dpq + i * L.dpq_shard;
+        dpre[i] = base + i * shard_bytes;
+    }
+    // quantise dY (E5M2; sequence shards gathered)
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    const size_t rows = x.rs ? x.rs : x.M;
+    for (int j = 0; j < x.nx; ++j)
+        segs[n++] = {dY[j], static_cast<char *>(dyq) + j * rows * x.H, (long long)(rows * x.H), AMAX_DY, FP8_E5M2};
+    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    const void *dya[1] = {dyq};
+    const void *xa[1] = {xq};
+    // row layer dgrad: dPre_i = (dYq W2q_i) / (s_dy s_w2) * act'(pre_i)
+    {
+        GemmPlan g;
+        g.name = d->act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
+        g.kind = d->act == TP_ACT_NONE ? EPI_PLAIN : EPI_DACT;
+        g.act = d->act;
+        g.M = x.M;
+        g.N = x.Fs;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.H;
+        set_operand(g.A, dya, 1, x.M, x.H, false, 0, 0, 0);
+        set_operand(g.B, w2q, x.T, x.H, x.Fs, true, 1, 0, 0);
+        set_out(g.out, dpre, x.T, 1, 0, gw);
+        if (d->act != TP_ACT_NONE) set_out(g.aux, pre, x.T, 1, 0, gw);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_W2);
+        TRY(launch_tc_gemm(g, st));
+    }
+    // quantise dPre (E5M2, one scale over all shards)
+    n = 0;
+    for (int i = 0; i < x.T; ++i) segs[n++] = {dpre[i], dpq[i], (long long)x.M * gw, AMAX_DP, FP8_E5M2};
+    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    // weight gradients (both operands MN-major over the tokens)
+    {
+        GemmPlan g;
+        g.name = "wgrad_row";
+        g.kind = EPI_F32;
+        g.M = x.H;
+        g.N = x.Fs;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.M;
+        set_operand(g.A, dya, 1, x.M, x.H, true, 0, 0, 0);
+        set_operand(g.B, aq, x.T, x.M, x.Fs, true, 1, 0, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dW2), x.T, 1, 0, x.Fs);
+        g.accumulate = d->wgrad_accumulate != 0;
+        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_A);
+        TRY(launch_tc_gemm(g, st));
+    }
+    {
+        GemmPlan g;
+        g.name = "wgrad_col";
+        g.kind = EPI_F32;
+        g.M = gw;
+        g.N = x.H;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.M;
+        set_operand(g.A, dpq, x.T, x.M, gw, true, 1, 0, 0);
+        set_operand(g.B, xa, 1, x.M, x.H, true, 0, 0, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dW1), x.T, 1, 0, x.H);
+        g.accumulate = d->wgrad_accumulate != 0;
+        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DP, AMAX_X);
+        TRY(launch_tc_gemm(g, st));
+    }
+    // column layer dgrad: dX = sum_i dPq_i W1q_i / (s_dp s_w1) (+ dY)
+    {
+        GemmPlan g;
+        g.name = "col_dgrad";
+        g.kind = EPI_PLAIN;
+        g.M = x.M;
+        g.N = x.H;
+        g.P = 1;
+        g.S = x.T;
+        g.Kseg = gw;
+        set_operand(g.A, dpq, x.T, x.M, gw, false, 0, 1, 0);
+        set_operand(g.B, w1q, x.T, gw, x.H, true, 0, 1, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
+        if (d->residual) set_out(g.aux, dY, x.nx, 0, x.rs, x.H);
+        set_bias(g, nullptr, 0, 0);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DP, AMAX_W1);
+        TRY(launch_tc_gemm(g, st));
+    }
+    if (d->has_bias) {
+        void *const *db2a = reinterpret_cast<void *const *>(&db2);
+        TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
+        TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+    }
     return TP_OK;
 }
 
@@ -415,9 +650,9 @@ void tp_mlp_destroy(tp_mlp *h) { delete h; }
 
 size_t tp_mlp_workspace_bytes(const tp_mlp *h) { return h ? mlp_ws_layout(&h->d, nullptr) : 0; }
 
-tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
-                     const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
-                     void *stream) {
+static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                              const void *const *W2, const void *b2, void *const *Y, void *const *pre,
+                              void *const *A, void *workspace, size_t workspace_bytes, bool has_ws, void *stream) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
     const tp_mlp_desc *d = &h->d;
     const Dims x = dims_of(d);
@@ -427,15 +662,36 @@ tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, con
         TRY(check_array(b1, x.T, "b1"));
         TRY(check_one(b2, "b2"));
     }
+    if (d->dtype == TP_DT_FP8) {
+        if (!has_ws) return set_error(TP_ERR_ARG, "the FP8 forward needs a workspace: call tp_mlp_fwd_ws");
+        const size_t need = mlp_ws_layout(d, nullptr);
+        if (workspace_bytes < need)
+            return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    }
     if (x.M == 0) return TP_OK;  // no tokens: activation buffers may be empty (NULL)
     TRY(check_array(X, x.nx, "X"));
     TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
     TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
     if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d->dtype == TP_DT_FP8) return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, Y, pre, A, workspace, st);
     TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));
     return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr,
                    d->residual ? X : nullptr, Y, st);
+}
+
+tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                     const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                     void *stream) {
+    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, nullptr, 0, false, stream);
+}
+
+tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                        const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, workspace, workspace_bytes, true, stream);
 }
 
 tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, const void *const *W1,
@@ -474,6 +730,9 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
         return zero_grads(d, dW2, x.T, sizeof(float) * x.H * x.Fs, d->has_bias ? db2a : nullptr, 1,
                           sizeof(float) * x.H, st);
     }
+    if (d->dtype == TP_DT_FP8)
+        return fp8_bwd(d, dY, pre, dX, dW1, d->has_bias ? db1 : nullptr, dW2, d->has_bias ? db2 : nullptr,
+                       workspace, st);
     void *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
@@ -493,6 +752,7 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
 tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
                         void *const *out, void *const *pre, void *stream) {
     TRY(validate_desc(desc));
+    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     const Dims x = dims_of(desc);
     TRY(check_array(W, x.T, "W"));
     if (desc->has_bias) TRY(check_array(b, x.T, "b"));
@@ -506,6 +766,7 @@ tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const voi
 tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
                         const void *const *R, void *const *Y, void *stream) {
     TRY(validate_desc(desc));
+    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     const Dims x = dims_of(desc);
     TRY(check_array(W, x.T, "W"));
     if (desc->has_bias) TRY(check_one(b, "b"));
@@ -537,6 +798,7 @@ tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, co
                             const void *const *W, void *const *dX, void *const *dW, void *const *db, void *workspace,
                             size_t workspace_bytes, void *stream) {
     TRY(validate_desc(desc));
+    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     if (desc->act != TP_ACT_NONE)
         return set_error(TP_ERR_UNSUPPORTED, "tp_linear_col_bwd takes act = TP_ACT_NONE (use tp_mlp_bwd)");
     const Dims x = dims_of(desc);
@@ -564,6 +826,7 @@ tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, cons
                             const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
                             size_t workspace_bytes, void *stream) {
     TRY(validate_desc(desc));
+    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     const Dims x = dims_of(desc);
     if (x.M > 0) {
         TRY(check_array(dY, x.nx, "dY"));
@@ -584,6 +847,21 @@ tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, cons
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
     return TP_OK;
+}
+
+tp_status tp_fp8_quantize(const void *const *in, void *const *out, const int64_t *n, int nbuf, int fmt, float *amax,
+                          void *stream) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return set_error(TP_ERR_ARG, "bad FP8 format %d", fmt);
+    if (nbuf < 1 || nbuf > kMaxQuantSegs) return set_error(TP_ERR_ARG, "nbuf=%d outside 1..%d", nbuf, kMaxQuantSegs);
+    if (!n || !amax) return set_error(TP_ERR_ARG, "n or amax is NULL");
+    TRY(check_array(in, nbuf, "in"));
+    TRY(check_array(reinterpret_cast<const void *const *>(out), nbuf, "out"));
+    QuantSeg segs[kMaxQuantSegs];
+    for (int i = 0; i < nbuf; ++i) {
+        if (n[i] < 0 || n[i] % 8) return set_error(TP_ERR_SHAPE, "n[%d]=%lld is not a non-negative multiple of 8", i, (long long)n[i]);
+        segs[i] = {in[i], out[i], (long long)n[i], 0, fmt};
+    }
+    return launch_fp8_quantize(segs, nbuf, amax, true, static_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_sync_status(void *stream) {

@@ -26,6 +26,12 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float x) {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// FP8 per-tensor scale: fmax / amax in fp32 (IEEE division), 1 when amax is
+// 0 or not finite.  The quantiser and the GEMM epilogues share it.
+__device__ __forceinline__ float fp8_scale(float amax, float fmax) {
+    return (amax > 0.0f && amax <= 3.0e38f) ? fmax / amax : 1.0f;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -1,0 +1,112 @@
+// Per-tensor FP8 quantisation of bf16 tensors ("Megatron-LM 源码精读", s8.2:
+// per-tensor scaling from the amax; E4M3 forward, E5M2 backward).
+//
+// A logical tensor may be split over several buffers (its shards); its amax is
+// the maximum over all of them -- the cross-shard amax all-reduce done as a
+// device-wide max.  Pass 1 (amax_kernel) reduces |x| into one fp32 slot per
+// tensor with an integer atomicMax on the bit pattern (valid for non-negative
+// floats).  Pass 2 (quant_kernel) computes scale = fmax / amax and writes
+// fp8(x * scale) with round-to-nearest-even, saturating to +-fmax.  Both passes
+// are HBM bound: 16-byte loads of 8 bf16, 8-byte stores of 8 fp8 codes.
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace tpmlp {
+
+struct QuantParams {
+    QuantSeg seg[kMaxQuantSegs];
+    float *amax;
+};
+
+__global__ void __launch_bounds__(256) amax_kernel(const __grid_constant__ QuantParams p) {
+    const QuantSeg &sg = p.seg[blockIdx.y];
+    const uint4 *in = static_cast<const uint4 *>(sg.in);
+    const long long nv = sg.n / 8;
+    float m = 0.0f;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
+        const uint4 w = in[i];
+        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))));
+        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y))));
+        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))));
+        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+        atomicMax(reinterpret_cast<unsigned *>(p.amax + sg.slot), __float_as_uint(m));
+    }
+}
+
+__device__ __forceinline__ uint16_t to_fp8x2(float a, float b, int fmt) {
+    const float2 v = make_float2(a, b);
+    return fmt == FP8_E5M2 ? __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E5M2)
+                           : __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(256) quant_kernel(const __grid_constant__ QuantParams p) {
+    const QuantSeg &sg = p.seg[blockIdx.y];
+    const float s = fp8_scale(p.amax[sg.slot], sg.fmt == FP8_E5M2 ? 57344.0f : 448.0f);
+    const uint4 *in = static_cast<const uint4 *>(sg.in);
+    uint2 *out = static_cast<uint2 *>(sg.out);
+    const long long nv = sg.n / 8;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
+        const uint4 w = in[i];
+        // x * scale is rounded to fp32 first, then to FP8
+        const float x0 = bf16_lo(w.x) * s, x1 = bf16_hi(w.x) * s, x2 = bf16_lo(w.y) * s, x3 = bf16_hi(w.y) * s;
+        const float x4 = bf16_lo(w.z) * s, x5 = bf16_hi(w.z) * s, x6 = bf16_lo(w.w) * s, x7 = bf16_hi(w.w) * s;
+        uint2 o;
+        o.x = uint32_t(to_fp8x2(x0, x1, sg.fmt)) | (uint32_t(to_fp8x2(x2, x3, sg.fmt)) << 16);
+        o.y = uint32_t(to_fp8x2(x4, x5, sg.fmt)) | (uint32_t(to_fp8x2(x6, x7, sg.fmt)) << 16);
+        out[i] = o;
+    }
+}
+
+static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, float *amax, cudaStream_t st) {
+    if (nseg <= 0) return TP_OK;
+    if (nseg > kMaxQuantSegs) return set_error(TP_ERR_UNSUPPORTED, "too many quantisation segments (%d)", nseg);
+    QuantParams prm;
+    memset(&prm, 0, sizeof(prm));
+    long long maxn = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (segs[i].n % 8) return set_error(TP_ERR_SHAPE, "quantised buffer length %lld not a multiple of 8", segs[i].n);
+        prm.seg[i] = segs[i];
+        maxn = segs[i].n > maxn ? segs[i].n : maxn;
+    }
+    prm.amax = amax;
+    if (maxn == 0) return TP_OK;
+    const long long blocks = (maxn / 8 + 255) / 256;
+    const int gx = static_cast<int>(blocks < 1024 ? blocks : 1024);
+    dim3 grid(gx, nseg);
+    const char *name = amax_pass ? "fp8_amax" : "fp8_quant";
+    launch_begin(name, st);
+    if (amax_pass)
+        amax_kernel<<<grid, 256, 0, st>>>(prm);
+    else
+        quant_kernel<<<grid, 256, 0, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end(name, st);
+    return cuda_check(e, name);
+}
+
+tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st) {
+    if (zero_slots) {
+        for (int i = 0; i < nseg; ++i) {
+            cudaError_t e = cudaMemsetAsync(amax + segs[i].slot, 0, sizeof(float), st);
+            if (e != cudaSuccess) return cuda_check(e, "cudaMemsetAsync(amax)");
+        }
+    }
+    tp_status s = launch_pass(true, segs, nseg, amax, st);
+    if (s != TP_OK) return s;
+    return launch_pass(false, segs, nseg, amax, st);
+}
+
+}  // namespace tpmlp

@@ -13,6 +13,8 @@ namespace tpmlp {
 
 constexpr int kMaxShards = TP_MAX_SHARDS;
 
+enum Fp8Format : int { FP8_E4M3 = 0, FP8_E5M2 = 1 };
+
 // Epilogue kinds shared by both GEMM engines.
 enum EpiKind : int {
     EPI_COL = 0,    // + bias, store pre, store act(pre)          (column forward)
@@ -60,6 +62,11 @@ struct GemmPlan {
     int bias_p_stride = 0;
     bool has_bias = false;
     bool accumulate = false;  // EPI_F32
+    // FP8 operands (1-byte elements): formats and per-tensor amax of A and B;
+    // the epilogue scales the sum by 1 / (scale_a * scale_b)
+    bool fp8 = false;
+    int fmt_a = 0, fmt_b = 0;  // FP8_E4M3 / FP8_E5M2
+    const float *amax_a = nullptr, *amax_b = nullptr;
 };
 
 // Column sums over token rows: out_p[c] = sum_m in_p[m, c] for c < N, fp32.
@@ -72,6 +79,21 @@ struct ColsumPlan {
 };
 
 int colsum_chunks(int M);
+
+// One buffer of a tensor to quantise to FP8: n bf16 elements (n % 8 == 0) at
+// `in`, n codes written at `out`; `slot` indexes the tensor's amax in the
+// amax array (all buffers of one tensor share a slot and hence a scale).
+struct QuantSeg {
+    const void *in = nullptr;
+    void *out = nullptr;
+    long long n = 0;
+    int slot = 0;
+    int fmt = 0;  // FP8_E4M3 / FP8_E5M2
+};
+constexpr int kMaxQuantSegs = 40;
+
+// amax pass (slots optionally zeroed first) then quantise pass.
+tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st);
 
 // Launchers (return a tp_status).  They only enqueue work on `st`.
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);

@@ -1,6 +1,7 @@
-// bf16 GEMM engine for sm_103a: TMA -> shared-memory ring -> tcgen05.mma ->
-// TMEM accumulators -> fused epilogue, in one persistent, warp-specialised
-// kernel.  Every product of the tensor-parallel MLP runs on it:
+// GEMM engine for sm_103a, host side: tensor maps, tiling choice, launch.
+// The kernels live in tc_gemm_kernels.cuh; this unit instantiates the bf16
+// ones and tc_gemm_fp8.cu the FP8 ones.  Every product of the tensor-parallel
+// MLP runs on them:
 //   column forward   pre_p = X W1_p^T (+b1_p), A_p = act(pre_p)      EPI_COL
 //   row forward      Y = sum_s A_s W2_s^T (+b2) (+X)                EPI_PLAIN, S = T
 //   row dgrad        dPre_p = (dY W2_p) * act'(pre_p)               EPI_DACT
@@ -9,11 +10,6 @@
 // The cross-shard sums (the forward and backward all-reduces of the
 // multi-GPU layer) are the K loop over segments s: every shard's K range is
 // accumulated into the same fp32 TMEM accumulator in shard order.
-//
-// Tile: 128 x 256 (tcgen05 M=128, N=256, K=16 per instruction, cta_group::1),
-// BK = 64 bf16 = one 128-byte swizzle row.  Warp 0 issues TMA, warp 1 issues
-// MMAs, warps 2-9 run the epilogue out of one of two TMEM accumulators while
-// the next tile accumulates into the other.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -25,858 +21,14 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tc_gemm_kernels.cuh"
 
 namespace tpmlp {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators of 128 lanes x 256 columns
-constexpr int MN_BOX = 64;         // MN-major operands: 64 elements (128 B) per box row
-constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;  // 8 KB
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-
-struct Sel {
-    int p_stride, s_stride, rows_split, nsplit;  // nsplit: token shards (when rows_split > 0)
-};
-struct Out {
-    void *ptr[kMaxShards];
-    int p_stride, rows_split;
-    long long ld;
-};
-
-struct Params {
-    CUtensorMap mapA[kMaxShards];
-    CUtensorMap mapB[kMaxShards];
-    Sel selA, selB;
-    Out out, out2, aux;
-    const void *bias[kMaxShards];
-    int bias_p_stride, has_bias, has_out2, has_aux;
-    int M, N, P, S, Kseg, num_kb;
-    int m_tiles, n_tiles, total_tiles, group_m;
-    int act, b_dual_off, accumulate;
-    int *status;
-    unsigned *abort_word;
-    unsigned launch_id;
-    unsigned long long wait_limit_ns;
-};
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with parity `parity` to complete.  Gives up when
-// another thread of this launch aborted, or after the wall-clock limit (then
-// it records TP_ERR_TIMEOUT and aborts the launch).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Params &p) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63u) == 0) {
-            if (*reinterpret_cast<volatile unsigned *>(p.abort_word) == p.launch_id) return false;
-            if (global_timer_ns() - t0 > p.wait_limit_ns) {
-                raise_device_error(p.status, p.abort_word, p.launch_id, TP_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-// Wait used only while draining on the way out: bounded, ignores the abort word.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) return;
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading and
-// stride byte offsets (16-byte units), descriptor version 1 at bit 46 and the
-// 128-byte swizzle layout (value 2 at bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bit 4),
-// bf16 A and B (bits 7, 10), A/B major-ness (bits 15, 16), N/8 at bit 17,
-// M/16 at bit 24.
-template <bool A_MN, bool B_MN>
-__device__ constexpr uint32_t make_idesc() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-}
-
-// ---------------------------------------------------------------------------
-// tile schedule: tiles are grouped in bands of `group_m` row tiles; within a
-// band the row tile varies fastest.  Column tiles of all problems are laid
-// side by side (problem p owns column tiles [p*n_tiles, (p+1)*n_tiles)).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tile_coords(const Params &p, int t, int &pi, int &mt, int &nt) {
-    const int n_tot = p.P * p.n_tiles;
-    const int per_group = p.group_m * n_tot;
-    const int g = t / per_group;
-    const int first_m = g * p.group_m;
-    const int gm = min(p.m_tiles - first_m, p.group_m);
-    const int r = t - g * per_group;
-    mt = first_m + r % gm;
-    const int n = r / gm;
-    pi = n / p.n_tiles;
-    nt = n - pi * p.n_tiles;
-}
-
-// Tensor map and local row for buffer row `row`.  A row past the last token
-// shard (the second half of a CTA-pair tile beyond M) stays on the last shard's
-// map at a row past its end, where the TMA load reads zero fill.
-__device__ __forceinline__ void select(const Sel &s, int pi, int seg, int row, int &idx, int &lrow) {
-    idx = pi * s.p_stride + seg * s.s_stride;
-    lrow = row;
-    if (s.rows_split) {
-        const int j = min(row / s.rows_split, s.nsplit - 1);
-        idx += j;
-        lrow = row - j * s.rows_split;
-    }
-}
-
-template <typename T>
-__device__ __forceinline__ T *row_ptr(const Out &o, int pi, int row) {
-    int idx = pi * o.p_stride;
-    int lrow = row;
-    if (o.rows_split) {
-        idx += row / o.rows_split;
-        lrow = row % o.rows_split;
-    }
-    return reinterpret_cast<T *>(o.ptr[idx]) + static_cast<long long>(lrow) * o.ld;
-}
-
-__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *src, float *dst) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(src);
-    dst[0] = bf16_lo(w.x); dst[1] = bf16_hi(w.x);
-    dst[2] = bf16_lo(w.y); dst[3] = bf16_hi(w.y);
-    dst[4] = bf16_lo(w.z); dst[5] = bf16_hi(w.z);
-    dst[6] = bf16_lo(w.w); dst[7] = bf16_hi(w.w);
-}
-
-__device__ __forceinline__ void store_bf16x8(__nv_bfloat16 *dst, const float *v) {
-    uint4 w;
-    w.x = pack_bf16x2(v[0], v[1]);
-    w.y = pack_bf16x2(v[2], v[3]);
-    w.z = pack_bf16x2(v[4], v[5]);
-    w.w = pack_bf16x2(v[6], v[7]);
-    *reinterpret_cast<uint4 *>(dst) = w;
-}
-
-// ---------------------------------------------------------------------------
-// epilogues: thread (warp q, lane l) owns output row m0 + 32q + l and walks
-// its half of the accumulator (`half` selects 128 of the 256 columns; for
-// SwiGLU 64 gate + the matching 64 up columns) in 32-column chunks.  Columns
-// come in groups of 8 that are either all inside N or all outside (N % 8 == 0).
-// ---------------------------------------------------------------------------
-// Activations of the bf16 epilogues use the SFU's tanh.approx.f32 (maximum
-// relative error about 2^-11, far below the 2^-8 resolution of the bf16
-// results they produce).  sigmoid(x) = (1 + tanh(x/2)) / 2.
-__device__ __forceinline__ float tanh_fast(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float gelu_tanh_fast(float x) {
-    const float t = tanh_fast(kGeluK0 * fmaf(kGeluK1 * x * x, x, x));
-    return 0.5f * x * (1.0f + t);
-}
-__device__ __forceinline__ float gelu_tanh_grad_fast(float x) {
-    const float t = tanh_fast(kGeluK0 * fmaf(kGeluK1 * x * x, x, x));
-    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * kGeluK0 * fmaf(3.0f * kGeluK1, x * x, 1.0f);
-}
-__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
-
-template <int EPI>
-__device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, int nt, uint32_t taddr, int half) {
-    const bool row_ok = row < p.M;
-    if (EPI == EPI_COL && p.act == TP_ACT_SWIGLU) {
-        // accumulator columns [0,128) = gate units, [128,256) = up units
-        const int ubase = nt * (BN / 2);
-        const __nv_bfloat16 *bias =
-            p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
-#pragma unroll 1
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            uint32_t rg[32], ru[32];
-            __syncwarp();
-            tmem_ld32(taddr + c * 32, rg);
-            tmem_ld32(taddr + BN / 2 + c * 32, ru);
-            tmem_ld_wait();
-            const int u0 = ubase + c * 32;
-            if (!row_ok) continue;
-            __nv_bfloat16 *pre = p.has_out2 ? row_ptr<__nv_bfloat16>(p.out2, pi, row) : nullptr;
-            __nv_bfloat16 *act = row_ptr<__nv_bfloat16>(p.out, pi, row);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int u = u0 + g8 * 8;
-                if (u >= p.N) break;
-                float G[8], U[8], A[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    G[j] = __uint_as_float(rg[g8 * 8 + j]);
-                    U[j] = __uint_as_float(ru[g8 * 8 + j]);
-                }
-                if (bias) {
-                    float bg[8], bu[8];
-                    load_bf16x8(bias + u, bg);
-                    load_bf16x8(bias + p.N + u, bu);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        G[j] += bg[j];
-                        U[j] += bu[j];
-                    }
-                }
-                if (pre) {
-                    store_bf16x8(pre + u, G);
-                    store_bf16x8(pre + p.N + u, U);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) A[j] = G[j] * sigmoid_fast(G[j]) * U[j];
-                store_bf16x8(act + u, A);
-            }
-        }
-        return;
-    }
-    const int n0 = nt * BN;
-#pragma unroll 1
-    for (int c = 4 * half; c < 4 * half + 4; ++c) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-        const int col0 = n0 + c * 32;
-        if (!row_ok || col0 >= p.N) continue;
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        if (EPI == EPI_F32) {
-            float *o = row_ptr<float>(p.out, pi, row) + col0;
-#pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4) {
-                if (col0 + g4 * 4 >= p.N) break;
-                float4 w = make_float4(v[g4 * 4], v[g4 * 4 + 1], v[g4 * 4 + 2], v[g4 * 4 + 3]);
-                if (p.accumulate) {
-                    const float4 old = *reinterpret_cast<const float4 *>(o + g4 * 4);
-                    w.x += old.x; w.y += old.y; w.z += old.z; w.w += old.w;
-                }
-                *reinterpret_cast<float4 *>(o + g4 * 4) = w;
-            }
-            continue;
-        }
-        if (EPI == EPI_COL) {
-            const __nv_bfloat16 *bias =
-                p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
-            __nv_bfloat16 *pre = p.has_out2 ? row_ptr<__nv_bfloat16>(p.out2, pi, row) : nullptr;
-            __nv_bfloat16 *act = row_ptr<__nv_bfloat16>(p.out, pi, row);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int col = col0 + g8 * 8;
-                if (col >= p.N) break;
-                float *x = v + g8 * 8;
-                if (bias) {
-                    float b[8];
-                    load_bf16x8(bias + col, b);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) x[j] += b[j];
-                }
-                if (pre) store_bf16x8(pre + col, x);
-                if (p.act == TP_ACT_GELU_TANH) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) x[j] = gelu_tanh_fast(x[j]);
-                }
-                store_bf16x8(act + col, x);
-            }
-        } else if (EPI == EPI_PLAIN) {
-            const __nv_bfloat16 *bias =
-                p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
-            const __nv_bfloat16 *res = p.has_aux ? row_ptr<const __nv_bfloat16>(p.aux, pi, row) : nullptr;
-            __nv_bfloat16 *o = row_ptr<__nv_bfloat16>(p.out, pi, row);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int col = col0 + g8 * 8;
-                if (col >= p.N) break;
-                float *x = v + g8 * 8;
-                if (bias) {
-                    float b[8];
-                    load_bf16x8(bias + col, b);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) x[j] += b[j];
-                }
-                if (res) {
-                    float rr[8];
-                    load_bf16x8(res + col, rr);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) x[j] += rr[j];
-                }
-                store_bf16x8(o + col, x);
-            }
-        } else if (EPI == EPI_DACT) {
-            const __nv_bfloat16 *pre = row_ptr<const __nv_bfloat16>(p.aux, pi, row);
-            __nv_bfloat16 *o = row_ptr<__nv_bfloat16>(p.out, pi, row);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int u = col0 + g8 * 8;
-                if (u >= p.N) break;
-                float *d = v + g8 * 8;
-                if (p.act == TP_ACT_GELU_TANH) {
-                    float x[8];
-                    load_bf16x8(pre + u, x);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) d[j] *= gelu_tanh_grad_fast(x[j]);
-                    store_bf16x8(o + u, d);
-                } else if (p.act == TP_ACT_SWIGLU) {
-                    float G[8], U[8], dG[8], dU[8];
-                    load_bf16x8(pre + u, G);
-                    load_bf16x8(pre + p.N + u, U);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float s = sigmoid_fast(G[j]);
-                        dG[j] = d[j] * U[j] * s * (1.0f + G[j] * (1.0f - s));
-                        dU[j] = d[j] * G[j] * s;
-                    }
-                    store_bf16x8(o + u, dG);
-                    store_bf16x8(o + p.N + u, dU);
-                } else {
-                    store_bf16x8(o + u, d);
-                }
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// the kernel
-// ---------------------------------------------------------------------------
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = full0 + 8 * STAGES;
-    const uint32_t tfull0 = empty0 + 8 * STAGES;
-    const uint32_t tempty0 = tfull0 + 16;
-    const uint32_t drain = tempty0 + 16;
-    const uint32_t smem_base = smem_u32(smem);
-
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(tfull0 + 8 * i, 1);
-            mbar_init(tempty0 + 8 * i, 32 * EPI_WARPS);
-        }
-        mbar_init(drain, 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t armed = 0, armed_par = 0;  // per stage: armed phase not yet known consumed
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
-                int pi, mt, nt;
-                tile_coords(p, t, pi, mt, nt);
-                const int m0 = mt * BM;
-                const int n0 = p.b_dual_off ? nt * (BN / 2) : nt * BN;
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
-                        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t fb = full0 + 8 * stage;
-                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                        armed |= 1u << stage;
-                        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-                        const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                        const uint32_t sb = sa + A_BYTES;
-                        const int k0 = kb * BK;
-                        int idx, lrow;
-                        if (!A_MN) {
-                            select(p.selA, pi, s, m0, idx, lrow);
-                            tma_load_2d(sa, &p.mapA[idx], fb, k0, lrow);
-                        } else {
-                            select(p.selA, pi, s, k0, idx, lrow);
-#pragma unroll
-                            for (int j = 0; j < BM / MN_BOX; ++j)
-                                tma_load_2d(sa + j * MN_BOX_BYTES, &p.mapA[idx], fb, m0 + j * MN_BOX, lrow);
-                        }
-                        if (!B_MN) {
-                            select(p.selB, pi, s, n0, idx, lrow);
-                            if (p.b_dual_off) {
-                                tma_load_2d(sb, &p.mapB[idx], fb, k0, lrow);
-                                tma_load_2d(sb + B_BYTES / 2, &p.mapB[idx], fb, k0, lrow + p.b_dual_off);
-                            } else {
-                                tma_load_2d(sb, &p.mapB[idx], fb, k0, lrow);
-                            }
-                        } else {
-                            select(p.selB, pi, s, k0, idx, lrow);
-#pragma unroll
-                            for (int j = 0; j < BN / MN_BOX; ++j)
-                                tma_load_2d(sb + j * MN_BOX_BYTES, &p.mapB[idx], fb, n0 + j * MN_BOX, lrow);
-                        }
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-            }
-            // Make sure no bulk copy is still landing in shared memory when the
-            // CTA exits (only matters on the abort path).
-            for (int i = 0; i < STAGES; ++i)
-                if (armed & (1u << i)) mbar_wait_drain(full0 + 8 * i, (armed_par >> i) & 1u, p.wait_limit_ns);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = make_idesc<A_MN, B_MN>();
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            int it = 0;
-            for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
-                const int acc = it & 1;
-                const uint32_t acc_par = (it >> 1) & 1;
-                if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1u, p)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + acc * BN;
-                uint32_t accumulate = 0;
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
-                        if (!mbar_wait(full0 + 8 * stage, phase, p)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                        const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            // K-major: advance 16 elements = 32 B inside the swizzle row.
-                            // MN-major: advance 16 K rows = 2 swizzle atoms of 1 KB.
-                            const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, MN_BOX_BYTES, 1024)
-                                                     : smem_desc(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, MN_BOX_BYTES, 1024)
-                                                     : smem_desc(sb + kk * 32, 16, 1024);
-                            umma_bf16(d, ad, bd, idesc, accumulate);
-                            accumulate = 1;
-                        }
-                        umma_commit(empty0 + 8 * stage);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-                if (!ok) break;
-                umma_commit(tfull0 + 8 * acc);
-            }
-            // all issued MMAs complete before TMEM is released
-            umma_commit(drain);
-            mbar_wait_drain(drain, 0, p.wait_limit_ns);
-        }
-        __syncwarp();
-    } else {
-        // ---------------- epilogue (warps 2..9) ----------------
-        const int q = warp & 3;             // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;   // which 128 accumulator columns it drains
-        int it = 0;
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t acc_par = (it >> 1) & 1;
-            const bool ok = mbar_wait(tfull0 + 8 * acc, acc_par, p);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            int pi, mt, nt;
-            tile_coords(p, t, pi, mt, nt);
-            const int row = mt * BM + q * 32 + lane;
-            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            run_epilogue<EPI>(p, pi, row, nt, taddr, half);
-            tc_fence_before();
-            mbar_arrive(tempty0 + 8 * acc);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
-// ---------------------------------------------------------------------------
-// CTA-pair variant: a cluster of two CTAs on two SMs computes one 256 x 256
-// tile with tcgen05.mma.cta_group::2 (M = 256).  CTA r of the pair loads rows
-// [128r, 128r + 128) of the A tile and rows [128r, 128r + 128) of the B tile
-// (for SwiGLU: CTA 0 the gate rows, CTA 1 the up rows) into its own shared
-// memory; the MMA, issued by CTA 0, reads both CTAs' halves and leaves rows
-// [128r, 128r + 128) of the accumulator in CTA r's TMEM.  Each SM thus reads
-// half of the B tile it would read alone, and a stage is 32 KB, so the ring
-// is 6 stages deep.
-//
-// Barriers: every load of both CTAs completes on CTA 0's full[s] (CTA 0 arms
-// it for both); the MMA commit multicasts to empty[s] and tfull[a] of both
-// CTAs; both CTAs' epilogue threads arrive on CTA 0's tempty[a].
-// ---------------------------------------------------------------------------
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of A
-constexpr int P_B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows of B
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
-constexpr int P_TILE_M = 256;
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of the same shared-memory offset in CTA `rank`
-__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// TMA load into this CTA's shared memory whose completion is signalled on an
-// mbarrier of either CTA of the pair (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int c0,
-                                                 int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// arrive on the barrier at this shared-memory offset in both CTAs of the pair
-// once all previously issued MMAs of this thread have completed
-__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar) {
-    const uint16_t mask = 0x3;
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-template <bool A_MN, bool B_MN>
-__device__ constexpr uint32_t make_idesc_pair() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(P_TILE_M >> 4) << 24);
-}
-
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_STAGES * P_STAGE_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * P_STAGES + 5);
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = full0 + 8 * P_STAGES;
-    const uint32_t tfull0 = empty0 + 8 * P_STAGES;
-    const uint32_t tempty0 = tfull0 + 16;
-    const uint32_t drain = tempty0 + 16;
-    const uint32_t smem_base = smem_u32(smem);
-
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
-    const int pair_id = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < P_STAGES; ++i) {
-            mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(tfull0 + 8 * i, 1);
-            mbar_init(tempty0 + 8 * i, 2 * 32 * EPI_WARPS);
-        }
-        mbar_init(drain, 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    cluster_sync();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer (both CTAs) ----------------
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t armed = 0, armed_par = 0;
-            bool ok = true;
-            for (int t = pair_id; ok && t < p.total_tiles; t += npairs) {
-                int pi, mt, nt;
-                tile_coords(p, t, pi, mt, nt);
-                const int m0 = mt * P_TILE_M + 128 * rank;
-                // B rows of this CTA: its half of the 256 tile columns, or for
-                // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
-                const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
-                        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t fb_local = full0 + 8 * stage;
-                        const uint32_t fb = map_to_cta(fb_local, 0);
-                        if (rank == 0) {
-                            mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
-                            armed |= 1u << stage;
-                            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-                        }
-                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                        const uint32_t sb = sa + P_A_BYTES;
-                        const int k0 = kb * BK;
-                        int idx, lrow;
-                        if (!A_MN) {
-                            select(p.selA, pi, s, m0, idx, lrow);
-                            tma_load_2d_pair(sa, &p.mapA[idx], fb, k0, lrow);
-                        } else {
-                            select(p.selA, pi, s, k0, idx, lrow);
-                            tma_load_2d_pair(sa, &p.mapA[idx], fb, m0, lrow);
-                            tma_load_2d_pair(sa + MN_BOX_BYTES, &p.mapA[idx], fb, m0 + MN_BOX, lrow);
-                        }
-                        if (!B_MN) {
-                            select(p.selB, pi, s, n0, idx, lrow);
-                            tma_load_2d_pair(sb, &p.mapB[idx], fb, k0, lrow);
-                        } else {
-                            select(p.selB, pi, s, k0, idx, lrow);
-                            tma_load_2d_pair(sb, &p.mapB[idx], fb, n0, lrow);
-                            tma_load_2d_pair(sb + MN_BOX_BYTES, &p.mapB[idx], fb, n0 + MN_BOX, lrow);
-                        }
-                        if (++stage == P_STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-            }
-            // CTA 0's full barriers count both CTAs' bytes: wait until every
-            // copy it armed has landed before the pair can exit.
-            for (int i = 0; i < P_STAGES; ++i)
-                if (armed & (1u << i)) mbar_wait_drain(full0 + 8 * i, (armed_par >> i) & 1u, p.wait_limit_ns);
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ---------------- MMA issuer (CTA 0 only) ----------------
-            constexpr uint32_t idesc = make_idesc_pair<A_MN, B_MN>();
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            int it = 0;
-            for (int t = pair_id; ok && t < p.total_tiles; t += npairs, ++it) {
-                const int acc = it & 1;
-                const uint32_t acc_par = (it >> 1) & 1;
-                if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1u, p)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + acc * BN;
-                uint32_t accumulate = 0;
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
-                        if (!mbar_wait(full0 + 8 * stage, phase, p)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                        const uint32_t sb = sa + P_A_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, MN_BOX_BYTES, 1024)
-                                                     : smem_desc(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, MN_BOX_BYTES, 1024)
-                                                     : smem_desc(sb + kk * 32, 16, 1024);
-                            umma_bf16_pair(d, ad, bd, idesc, accumulate);
-                            accumulate = 1;
-                        }
-                        umma_commit_pair_mc(empty0 + 8 * stage);
-                        if (++stage == P_STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-                if (!ok) break;
-                umma_commit_pair_mc(tfull0 + 8 * acc);
-            }
-            umma_commit_pair(drain);
-            mbar_wait_drain(drain, 0, p.wait_limit_ns);
-        }
-        __syncwarp();
-    } else {
-        // ---------------- epilogue (warps 2..9 of both CTAs) ----------------
-        const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const uint32_t tempty_leader = map_to_cta(tempty0, 0);
-        int it = 0;
-        for (int t = pair_id; t < p.total_tiles; t += npairs, ++it) {
-            const int acc = it & 1;
-            const uint32_t acc_par = (it >> 1) & 1;
-            const bool ok = mbar_wait(tfull0 + 8 * acc, acc_par, p);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            int pi, mt, nt;
-            tile_coords(p, t, pi, mt, nt);
-            const int row = mt * P_TILE_M + 128 * rank + q * 32 + lane;
-            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            run_epilogue<EPI>(p, pi, row, nt, taddr, half);
-            tc_fence_before();
-            mbar_arrive_cluster(tempty_leader + 8 * acc);
-        }
-    }
-
-    tc_fence_before();
-    cluster_sync();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
-}
-
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
 typedef void (*KernelFn)(Params);
 constexpr int kNumKernels = 5;
+KernelFn fp8_kernel_at(int i, bool pair);  // tc_gemm_fp8.cu
 
 // The five (epilogue, A major, B major) combinations the MLP uses.
 static int kernel_index(int kind, bool amn, bool bmn) {
@@ -888,13 +40,14 @@ static int kernel_index(int kind, bool amn, bool bmn) {
     return -1;
 }
 
-static KernelFn kernel_at(int i, bool pair) {
+static KernelFn kernel_at(int i, bool pair, bool fp8) {
+    if (fp8) return fp8_kernel_at(i, pair);
     switch (i) {
-        case 0: return pair ? tc_gemm_pair_kernel<EPI_COL, false, false> : tc_gemm_kernel<EPI_COL, false, false>;
-        case 1: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, false> : tc_gemm_kernel<EPI_PLAIN, false, false>;
-        case 2: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, true> : tc_gemm_kernel<EPI_PLAIN, false, true>;
-        case 3: return pair ? tc_gemm_pair_kernel<EPI_DACT, false, true> : tc_gemm_kernel<EPI_DACT, false, true>;
-        case 4: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true> : tc_gemm_kernel<EPI_F32, true, true>;
+        case 0: return pair ? tc_gemm_pair_kernel<EPI_COL, false, false, false> : tc_gemm_kernel<EPI_COL, false, false, false>;
+        case 1: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, false, false> : tc_gemm_kernel<EPI_PLAIN, false, false, false>;
+        case 2: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, true, false> : tc_gemm_kernel<EPI_PLAIN, false, true, false>;
+        case 3: return pair ? tc_gemm_pair_kernel<EPI_DACT, false, true, false> : tc_gemm_kernel<EPI_DACT, false, true, false>;
+        case 4: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true, false> : tc_gemm_kernel<EPI_F32, true, true, false>;
     }
     return nullptr;
 }
@@ -913,14 +66,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-static tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows) {
+// 2D tensor map of a row-major [rows, cols] buffer of 1-byte (FP8) or
+// 2-byte (bf16) elements, 128-byte swizzle.
+static tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows,
+                            bool fp8) {
     auto fn = encode_fn();
     if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (fp8 ? 1 : 2)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -952,20 +108,23 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     // problem has a single 128-row tile.
     const int mode = g_tile_mode.load();
     const bool use_pair = mode == TP_TILE_PAIR || (mode == TP_TILE_AUTO && g.M > BM);
-    KernelFn fn = kernel_at(ki, use_pair);
+    const bool fp8 = g.fp8;
+    KernelFn fn = kernel_at(ki, use_pair, fp8);
+    const int bke = fp8 ? Elem<true>::BKE : Elem<false>::BKE;  // K elements per stage
+    const int mnb = fp8 ? Elem<true>::MNB : Elem<false>::MNB;  // MN elements per MN-major box
     const int tile_m = use_pair ? P_TILE_M : BM;
     // rows of the B tile that one CTA loads per box
     const int b_box_rows = (use_pair || g.b_dual_off) ? BN / 2 : BN;
     Params prm;
     memset(&prm, 0, sizeof(prm));
     for (int i = 0; i < g.A.n; ++i) {
-        tp_status s = g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, MN_BOX, BK)
-                                   : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, BK, BM);
+        tp_status s = g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, mnb, bke, fp8)
+                                   : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke, BM, fp8);
         if (s != TP_OK) return s;
     }
     for (int i = 0; i < g.B.n; ++i) {
-        tp_status s = g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, MN_BOX, BK)
-                                   : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, BK, b_box_rows);
+        tp_status s = g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
+                                   : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke, b_box_rows, fp8);
         if (s != TP_OK) return s;
     }
     prm.selA = {g.A.p_stride, g.A.s_stride, g.A.rows_split, g.A.n};
@@ -983,7 +142,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.P = g.P;
     prm.S = g.S;
     prm.Kseg = g.Kseg;
-    prm.num_kb = (g.Kseg + BK - 1) / BK;
+    prm.num_kb = (g.Kseg + bke - 1) / bke;
     prm.m_tiles = (g.M + tile_m - 1) / tile_m;
     const int n_per_tile = g.b_dual_off ? BN / 2 : BN;
     prm.n_tiles = (g.N + n_per_tile - 1) / n_per_tile;
@@ -992,6 +151,16 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
     prm.accumulate = g.accumulate ? 1 : 0;
+    // instruction descriptor: fp32 accumulator (bit 4), A/B formats (bits 7-9,
+    // 10-12: bf16 = 1 for kind::f16; E4M3 = 0, E5M2 = 1 for kind::f8f6f4),
+    // A/B MN-major (bits 15, 16), N/8 at bit 17, M/16 at bit 24
+    const uint32_t fa = fp8 ? uint32_t(g.fmt_a) : 1u, fb = fp8 ? uint32_t(g.fmt_b) : 1u;
+    prm.idesc = (1u << 4) | (fa << 7) | (fb << 10) | (uint32_t(g.A.mn_major) << 15) |
+                (uint32_t(g.B.mn_major) << 16) | (uint32_t(BN >> 3) << 17) | (uint32_t(tile_m >> 4) << 24);
+    prm.amax_a = fp8 ? g.amax_a : nullptr;
+    prm.amax_b = fp8 ? g.amax_b : nullptr;
+    prm.fmax_a = g.fmt_a == FP8_E5M2 ? 57344.0f : 448.0f;
+    prm.fmax_b = g.fmt_b == FP8_E5M2 ? 57344.0f : 448.0f;
     DeviceWords w;
     tp_status s = device_words(&w);
     if (s != TP_OK) return s;
@@ -1004,14 +173,14 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     // opt in to > 48 KB of dynamic shared memory and size the persistent
     // grid, once per kernel and device
     static std::mutex mu;
-    static bool attr_set[64][2][kNumKernels] = {};
-    static int max_pairs[64][kNumKernels] = {};
+    static bool attr_set[64][2][2][kNumKernels] = {};
+    static int max_pairs[64][2][kNumKernels] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     const int smem_bytes = use_pair ? P_SMEM_BYTES : SMEM_BYTES;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev % 64][use_pair][ki]) {
+        if (!attr_set[dev % 64][fp8][use_pair][ki]) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
             if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute");
             if (use_pair) {
@@ -1034,15 +203,15 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
                     cudaGetLastError();
                     n = num_sms() / 2;
                 }
-                max_pairs[dev % 64][ki] = n;
+                max_pairs[dev % 64][fp8][ki] = n;
             }
-            attr_set[dev % 64][use_pair][ki] = true;
+            attr_set[dev % 64][fp8][use_pair][ki] = true;
         }
     }
     cudaError_t e;
     launch_begin(g.name, st);
     if (use_pair) {
-        const int pairs = std::min(prm.total_tiles, max_pairs[dev % 64][ki]);
+        const int pairs = std::min(prm.total_tiles, max_pairs[dev % 64][fp8][ki]);
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -28,14 +28,14 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 
 def dev(a, dtype: str, device="cuda"):
-    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    td = torch.float32 if dtype == "f32" else torch.bfloat16
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device=device, dtype=td)
 
 
 def mlp_inputs(M, H, F, T, act, dtype, has_bias=True, bias_std=0.02, seed_off=0, x_std=1.0, w_std=0.02):
     """Seeded full tensors (synth) and their shards (oracle layout)."""
     g = 2 if act == "swiglu" else 1
-    rnd = synth.round_bf16 if dtype == "bf16" else (lambda a: a)
+    rnd = (lambda a: a) if dtype == "f32" else synth.round_bf16
     base = synth.SEED_BASE + 1000 * seed_off
     t = {
         "X": rnd(synth.normal(base + synth.TID_X, (M, H), x_std)),
@@ -70,7 +70,7 @@ class MlpRun:
         self.W2 = [dev(w, dt) for w in t["W2s"]]
         self.b1 = [dev(b, dt) for b in t["b1s"]] if lay.has_bias else None
         self.b2 = dev(t["b2"], dt) if lay.has_bias else None
-        td = torch.bfloat16 if dt == "bf16" else torch.float32
+        td = torch.float32 if dt == "f32" else torch.bfloat16
         rows = lay.xrows
         self.Y = [torch.full((rows, H), float("nan"), dtype=td, device=device) for _ in range(lay.nx)]
         self.dX = [torch.full((rows, H), float("nan"), dtype=td, device=device) for _ in range(lay.nx)]
@@ -85,7 +85,8 @@ class MlpRun:
         self.ws = tp.alloc_workspace(lay.workspace_bytes()) if isinstance(lay, tp.TPMLP) else None
 
     def fwd(self):
-        self.lay.fwd(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.pre, self.A)
+        ws = self.ws if self.lay.dtype == "fp8" else None
+        self.lay.fwd(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.pre, self.A, workspace=ws)
 
     def bwd(self):
         self.lay.bwd(self.dY, self.X, self.W1, self.W2, self.pre, self.A, self.dX, self.dW1, self.db1,

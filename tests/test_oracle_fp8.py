@@ -92,3 +92,30 @@ def test_fp8_pipeline_close_to_exact_mlp(act):
         assert rel(g8["dW2"][i], g64["dW2"][i]) < 0.15
         assert rel(g8["db1"][i], g64["db1"][i]) < 0.1
     assert rel(g8["db2"], g64["db2"]) == 0.0
+
+
+@pytest.mark.parametrize("act", ["gelu_tanh", "swiglu"])
+def test_sampled_fp8_agrees_with_full(act):
+    rng = np.random.default_rng(9)
+    M, H, F, T = 40, 32, 64, 2
+    g = 2 if act == "swiglu" else 1
+    X = fp8.round_bf16(rng.standard_normal((M, H)))
+    W1s = oracle.shard_column_weight(fp8.round_bf16(rng.standard_normal((g * F, H)) * 0.1), T, act)
+    b1s = oracle.shard_column_bias(fp8.round_bf16(rng.standard_normal(g * F) * 0.1), T, act)
+    W2s = oracle.shard_row_weight(fp8.round_bf16(rng.standard_normal((H, F)) * 0.1), T)
+    b2 = fp8.round_bf16(rng.standard_normal(H) * 0.1)
+    dY = fp8.round_bf16(rng.standard_normal((M, H)))
+    f = fp8.mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act, True)
+    gr = fp8.mlp_bwd_fp8(dY, f, act, True)
+    rows = np.array([0, 5, 39])
+    units = [np.array([0, 31]), np.array([7])]
+    s = fp8.mlp_sampled_fp8(rows, units, X, W1s, b1s, W2s, b2, dY, act, True)
+    assert np.allclose(s["Y"], f["Y"][rows], rtol=0, atol=1e-12)
+    assert np.allclose(s["dX"], gr["dX"][rows], rtol=0, atol=1e-12)
+    assert np.array_equal(s["db2"], gr["db2"])
+    fs = F // T
+    for i in range(T):
+        sel = np.concatenate([units[i], fs + units[i]]) if act == "swiglu" else units[i]
+        assert np.allclose(s["dW1"][i], gr["dW1"][i][sel], rtol=0, atol=1e-12)
+        assert np.allclose(s["dW2"][i], gr["dW2"][i][:, units[i]], rtol=0, atol=1e-12)
+        assert np.allclose(s["db1"][i], gr["db1"][i][sel], rtol=0, atol=1e-12)
