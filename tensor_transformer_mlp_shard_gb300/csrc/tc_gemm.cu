@@ -66,22 +66,41 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D tensor map of a row-major [rows, cols] buffer of 1-byte (FP8) or
-// 2-byte (bf16) elements, 128-byte swizzle.
-static tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows,
-                            bool fp8) {
+// 2D tensor map of a row-major [rows, cols] buffer with leading dimension
+// `ld` elements.
+static tp_status encode_map_ex(CUtensorMap *m, const void *ptr, int rows, int cols, long long ld, int box_inner,
+                               int box_rows, CUtensorMapDataType type, int esize, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
     if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (fp8 ? 1 : 2)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, type, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%d x %d] box [%d x %d]", int(r),
                          rows, cols, box_rows, box_inner);
+    return TP_OK;
+}
+
+// operand map: 1-byte (FP8) or 2-byte (bf16) elements, 128-byte swizzle
+static tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows,
+                            bool fp8) {
+    return encode_map_ex(m, ptr, rows, cols, cols, box_inner, box_rows,
+                         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, fp8 ? 1 : 2,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// bulk-store map of an epilogue output: boxes of 32 rows x 64 bytes
+// (32 bf16 or 16 fp32), 64-byte swizzle, matching the staging layout
+static tp_status encode_out_maps(CUtensorMap *maps, const OutPlan &o, int rows, int cols, bool f32) {
+    for (int i = 0; i < o.n; ++i) {
+        tp_status s = encode_map_ex(&maps[i], o.ptr[i], rows, cols, o.ld, f32 ? 16 : 32, 32,
+                                    f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    f32 ? 4 : 2, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (s != TP_OK) return s;
+    }
     return TP_OK;
 }
 
@@ -89,6 +108,7 @@ static void copy_out(Out &o, const OutPlan &src) {
     for (int i = 0; i < kMaxShards; ++i) o.ptr[i] = i < src.n ? src.ptr[i] : nullptr;
     o.p_stride = src.p_stride;
     o.rows_split = src.rows_split;
+    o.nsplit = src.n;
     o.ld = src.ld;
 }
 
@@ -157,6 +177,25 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     const uint32_t fa = fp8 ? uint32_t(g.fmt_a) : 1u, fb = fp8 ? uint32_t(g.fmt_b) : 1u;
     prm.idesc = (1u << 4) | (fa << 7) | (fb << 10) | (uint32_t(g.A.mn_major) << 15) |
                 (uint32_t(g.B.mn_major) << 16) | (uint32_t(BN >> 3) << 17) | (uint32_t(tile_m >> 4) << 24);
+    // Epilogue outputs go through shared memory and bulk tensor stores, except
+    // when accumulating into dW (read-modify-write) or for SwiGLU with a unit
+    // count that is not a multiple of 32 (a 32-column gate block would reach
+    // into the up half of pre / dPre, which a store clipped at the buffer's
+    // width cannot prevent).
+    prm.out_tma = !g.accumulate && !(g.act == TP_ACT_SWIGLU && g.N % 32) ? 1 : 0;
+    if (prm.out_tma) {
+        const bool f32 = g.kind == EPI_F32;
+        // columns of a whole output row: pre / dPre hold both SwiGLU halves
+        const int ocols = static_cast<int>(g.out.ld);
+        const int orows = g.out.rows_split ? g.out.rows_split : g.M;
+        tp_status s = encode_out_maps(prm.mapO, g.out, orows, ocols, f32);
+        if (s != TP_OK) return s;
+        if (g.out2.n) {
+            s = encode_out_maps(prm.mapO2, g.out2, g.out2.rows_split ? g.out2.rows_split : g.M,
+                                static_cast<int>(g.out2.ld), false);
+            if (s != TP_OK) return s;
+        }
+    }
     prm.amax_a = fp8 ? g.amax_a : nullptr;
     prm.amax_b = fp8 ? g.amax_b : nullptr;
     prm.fmax_a = g.fmt_a == FP8_E5M2 ? 57344.0f : 448.0f;

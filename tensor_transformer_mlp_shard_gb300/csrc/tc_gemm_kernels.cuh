@@ -45,20 +45,28 @@ struct Elem {
     static constexpr uint32_t MNB_BYTES = ROW_BYTES * BKE;      // 16 KB fp8, 8 KB bf16
     static constexpr uint32_t KADV_MN = ROW_BYTES * (F8 ? 32 : 16);
 };
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+// Epilogue staging: each epilogue warp owns two 2 KB buffers of 32 rows x
+// 64 bytes (64-byte swizzle) that feed bulk tensor stores.
+constexpr int EPI_STAGE_BYTES = 4096;
+constexpr int EPI_SMEM = EPI_WARPS * EPI_STAGE_BYTES;  // 32 KB
+constexpr int BAR_BYTES = 1024;                          // barriers + TMEM slot
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES + EPI_SMEM;
 
 struct Sel {
     int p_stride, s_stride, rows_split, nsplit;  // nsplit: token shards (when rows_split > 0)
 };
 struct Out {
     void *ptr[kMaxShards];
-    int p_stride, rows_split;
+    int p_stride, rows_split, nsplit;
     long long ld;
 };
 
 struct Params {
     CUtensorMap mapA[kMaxShards];
     CUtensorMap mapB[kMaxShards];
+    CUtensorMap mapO[kMaxShards];    // bulk-store maps of `out` (when out_tma)
+    CUtensorMap mapO2[kMaxShards];   // ... and of `out2`
+    int out_tma;                     // epilogue writes through shared memory + bulk tensor stores
     Sel selA, selB;
     Out out, out2, aux;
     const void *bias[kMaxShards];
@@ -297,6 +305,245 @@ __device__ __forceinline__ float gelu_tanh_grad_fast(float x) {
     return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * kGeluK0 * fmaf(3.0f * kGeluK1, x * x, 1.0f);
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+
+// ---------------------------------------------------------------------------
+// epilogue through shared memory: every epilogue warp stages a 32-row x
+// 64-byte block (lane = row, 4 x 16 bytes, 64-byte swizzle) in one of its two
+// buffers and writes it with one bulk tensor store, which clips rows and
+// columns outside the output.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t a, const uint4 &v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+struct Stager {
+    uint32_t base;    // this warp's 4 KB
+    uint32_t toggle;  // which 2 KB half is next
+};
+
+__device__ __forceinline__ void stage_store(Stager &st, const CUtensorMap *map, int x, int y, const uint4 (&w)[4],
+                                            int lane) {
+    const uint32_t buf = st.base + st.toggle * 2048u;
+    st.toggle ^= 1u;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last used this half has read it
+    __syncwarp();
+    const uint32_t rowa = buf + static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) st_shared_v4(rowa + ((static_cast<uint32_t>(j) ^ sw) << 4), w[j]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, buf, x, y);
+        bulk_commit();
+    }
+}
+
+__device__ __forceinline__ void pack_bf16x32(const float *v, uint4 (&w)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j].x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        w[j].y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        w[j].z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        w[j].w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+    }
+}
+
+__device__ __forceinline__ void pack_f32x16(const float *v, uint4 (&w)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                          __float_as_uint(v[4 * j + 3]));
+}
+
+// output map index and local row of the 32-row block starting at row0
+__device__ __forceinline__ void out_index(const Out &o, int pi, int row0, int &idx, int &lrow) {
+    idx = pi * o.p_stride;
+    lrow = row0;
+    if (o.rows_split) {
+        const int j = min(row0 / o.rows_split, o.nsplit - 1);
+        idx += j;
+        lrow = row0 - j * o.rows_split;
+    }
+}
+
+// 8 bf16 from global, or zeros when the group lies outside [0, limit)
+__device__ __forceinline__ void load_bf16x8_guarded(const __nv_bfloat16 *src, bool ok, float *dst) {
+    if (ok) {
+        load_bf16x8(src, dst);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = 0.0f;
+    }
+}
+
+template <int EPI>
+__device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int row, int nt, uint32_t taddr, int half,
+                                                 float dq, Stager &stg, int lane) {
+    const int row0 = row - lane;             // first row of this warp's block
+    const bool block_ok = row0 < p.M;        // warp-uniform
+    const bool row_ok = row < p.M;
+    int oi, oy, oi2 = 0, oy2 = 0;
+    out_index(p.out, pi, row0, oi, oy);
+    if (p.has_out2) out_index(p.out2, pi, row0, oi2, oy2);
+    const __nv_bfloat16 *bias =
+        p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
+    uint4 w[4];
+    if (EPI == EPI_COL && p.act == TP_ACT_SWIGLU) {
+        // accumulator columns [0,128) = gate units, [128,256) = up units (N % 32 == 0 here)
+        const int ubase = nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+            uint32_t rg[32], ru[32];
+            __syncwarp();
+            tmem_ld32(taddr + c * 32, rg);
+            tmem_ld32(taddr + BN / 2 + c * 32, ru);
+            tmem_ld_wait();
+            const int u0 = ubase + c * 32;
+            if (!block_ok || u0 >= p.N) continue;
+            float G[32], U[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                G[j] = __uint_as_float(rg[j]) * dq;
+                U[j] = __uint_as_float(ru[j]) * dq;
+            }
+            if (bias) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float bg[8], bu[8];
+                    load_bf16x8(bias + u0 + 8 * g8, bg);
+                    load_bf16x8(bias + p.N + u0 + 8 * g8, bu);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        G[8 * g8 + j] += bg[j];
+                        U[8 * g8 + j] += bu[j];
+                    }
+                }
+            }
+            if (p.has_out2) {
+                pack_bf16x32(G, w);
+                stage_store(stg, &p.mapO2[oi2], u0, oy2, w, lane);
+                pack_bf16x32(U, w);
+                stage_store(stg, &p.mapO2[oi2], p.N + u0, oy2, w, lane);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) G[j] = G[j] * sigmoid_fast(G[j]) * U[j];
+            pack_bf16x32(G, w);
+            stage_store(stg, &p.mapO[oi], u0, oy, w, lane);
+        }
+        return;
+    }
+    const int n0 = nt * BN;
+#pragma unroll 1
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int col0 = n0 + c * 32;
+        if (!block_ok || col0 >= p.N) continue;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * dq;
+        if (EPI == EPI_F32) {
+            pack_f32x16(v, w);
+            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+            if (col0 + 16 < p.N) {
+                pack_f32x16(v + 16, w);
+                stage_store(stg, &p.mapO[oi], col0 + 16, oy, w, lane);
+            }
+            continue;
+        }
+        if (EPI == EPI_COL || EPI == EPI_PLAIN) {
+            if (bias) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float b[8];
+                    load_bf16x8_guarded(bias + col0 + 8 * g8, col0 + 8 * g8 < p.N, b);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[8 * g8 + j] += b[j];
+                }
+            }
+        }
+        if (EPI == EPI_COL) {
+            if (p.has_out2) {
+                pack_bf16x32(v, w);
+                stage_store(stg, &p.mapO2[oi2], col0, oy2, w, lane);
+            }
+            if (p.act == TP_ACT_GELU_TANH) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
+            }
+            pack_bf16x32(v, w);
+            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+        } else if (EPI == EPI_PLAIN) {
+            if (p.has_aux) {
+                const __nv_bfloat16 *res = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float rr[8];
+                    load_bf16x8_guarded(res + col0 + 8 * g8, row_ok && col0 + 8 * g8 < p.N, rr);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[8 * g8 + j] += rr[j];
+                }
+            }
+            pack_bf16x32(v, w);
+            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+        } else if (EPI == EPI_DACT) {
+            const __nv_bfloat16 *pre = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
+            if (p.act == TP_ACT_SWIGLU) {
+                float dU[32];
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float G[8], U[8];
+                    const bool ok = row_ok && col0 + 8 * g8 < p.N;
+                    load_bf16x8_guarded(pre + col0 + 8 * g8, ok, G);
+                    load_bf16x8_guarded(pre + p.N + col0 + 8 * g8, ok, U);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float s = sigmoid_fast(G[j]);
+                        const float d = v[8 * g8 + j];
+                        v[8 * g8 + j] = d * U[j] * s * (1.0f + G[j] * (1.0f - s));
+                        dU[8 * g8 + j] = d * G[j] * s;
+                    }
+                }
+                pack_bf16x32(v, w);
+                stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+                pack_bf16x32(dU, w);
+                stage_store(stg, &p.mapO[oi], p.N + col0, oy, w, lane);
+            } else {
+                if (p.act == TP_ACT_GELU_TANH) {
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        float x[8];
+                        load_bf16x8_guarded(pre + col0 + 8 * g8, row_ok && col0 + 8 * g8 < p.N, x);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] *= gelu_tanh_grad_fast(x[j]);
+                    }
+                }
+                pack_bf16x32(v, w);
+                stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+            }
+        }
+    }
+}
 
 template <int EPI>
 __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, int nt, uint32_t taddr, int half,
@@ -613,6 +860,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;   // which 128 accumulator columns it drains
         const float dq = dequant_factor(p);
+        Stager stg{smem_base + STAGES * STAGE_BYTES + BAR_BYTES + (warp - 2) * EPI_STAGE_BYTES, 0u};
         int it = 0;
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -624,10 +872,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             tile_coords(p, t, pi, mt, nt);
             const int row = mt * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
+            if (p.out_tma)
+                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane);
+            else
+                run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
         }
+        if (lane == 0) bulk_wait<0>();  // bulk stores done before the CTA leaves
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -654,7 +907,7 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * ROW_BYTES;  // 16 KB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = 128 * ROW_BYTES;  // 16 KB: this CTA's 128 rows of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + BAR_BYTES + EPI_SMEM;
 constexpr int P_TILE_M = 256;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -893,6 +1146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         const float dq = dequant_factor(p);
+        Stager stg{smem_base + P_STAGES * P_STAGE_BYTES + BAR_BYTES + (warp - 2) * EPI_STAGE_BYTES, 0u};
         const uint32_t tempty_leader = map_to_cta(tempty0, 0);
         int it = 0;
         for (int t = pair_id; t < p.total_tiles; t += npairs, ++it) {
@@ -905,10 +1159,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             tile_coords(p, t, pi, mt, nt);
             const int row = mt * P_TILE_M + 128 * rank + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
+            if (p.out_tma)
+                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane);
+            else
+                run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
             tc_fence_before();
             mbar_arrive_cluster(tempty_leader + 8 * acc);
         }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     }
 
     tc_fence_before();
