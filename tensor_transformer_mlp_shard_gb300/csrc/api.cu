@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <algorithm>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -273,7 +274,8 @@ static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void
 
 // Row-layer dgrad: dOut_i = (dY W_i) [* act'(pre_i)], i < T (no reduction).
 static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY, const void *const *W,
-                           const void *const *pre, void *const *dOut, long long ld_out, cudaStream_t st) {
+                           const void *const *pre, void *const *dOut, long long ld_out, cudaStream_t st,
+                           float *col_partials = nullptr, bool *fused = nullptr) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
@@ -288,6 +290,10 @@ static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY,
     set_operand(g.B, W, x.T, x.H, x.Fs, true, 1, 0, 0);
     set_out(g.out, reinterpret_cast<const void *const *>(dOut), x.T, 1, 0, ld_out);
     if (act != TP_ACT_NONE) set_out(g.aux, pre, x.T, 1, 0, ld_out);
+    // db1 column sums fused into the bf16 epilogue when it can take them
+    const bool fuse = col_partials && act != TP_ACT_NONE && d->dtype != TP_DT_F32 && tc_fused_epilogue(g);
+    if (fuse) g.col_partials = col_partials;
+    if (fused) *fused = fuse;
     return run_gemm(g, d->dtype, st);
 }
 
@@ -352,6 +358,19 @@ static tp_status colsum(const tp_mlp_desc *d, const char *name, const void *cons
     return launch_colsum(c, d->dtype == TP_DT_F32 ? TP_DT_F32 : TP_DT_BF16, st);
 }
 
+// db1 from the fused epilogue's per-32-row-block column sums
+static tp_status db1_finalize(const tp_mlp_desc *d, int gw, void *const *db1, float *partials, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    ColsumPlan c;
+    c.name = "bias_grad_col";
+    c.P = x.T;
+    c.M = x.M;
+    c.N = gw;
+    for (int i = 0; i < kMaxShards; ++i) c.out[i] = i < x.T ? static_cast<float *>(db1[i]) : nullptr;
+    c.partials = partials;
+    return launch_colsum_finalize(c, (x.M + 31) / 32, st);
+}
+
 static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
     const Dims x = dims_of(d);
     return align256(sizeof(float) * static_cast<size_t>(P) * colsum_chunks(x.M) * N);
@@ -364,8 +383,10 @@ static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
     if (dpre_shard_bytes) *dpre_shard_bytes = shard;
     size_t part = 0;
     if (d->has_bias) {
-        size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
-        part = a > b ? a : b;
+        // db1: colsum partials, or the fused epilogue's per-32-row-block sums
+        const size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
+        const size_t c = align256(sizeof(float) * size_t(x.T) * ((x.M + 31) / 32) * x.g * x.Fs);
+        part = std::max(a, std::max(b, c));
     }
     return shard * x.T + part;
 }
@@ -458,6 +479,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     for (int i = 0; i < x.T; ++i) segs[n++] = {W2[i], w2q[i], (long long)x.H * x.Fs, AMAX_W2, FP8_E4M3};
     TRY(launch_fp8_quantize(segs, n, amax, true, st));
     // column GEMM: pre_i = Xq W1q_i^T / (s_x s_w1) + b1_i, A_i = act(pre_i)
+    bool a_fused = false;
     {
         GemmPlan g;
         g.name = "col_fwd";
@@ -476,12 +498,17 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
         if (pre) set_out(g.out2, reinterpret_cast<const void *const *>(pre), x.T, 1, 0, gw);
         set_bias(g, d->has_bias ? b1 : nullptr, x.T, 1);
         set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_X, AMAX_W1);
+        a_fused = tc_fused_epilogue(g);
+        if (a_fused) {  // the epilogue reduces amax(A) as it stores A
+            TRY(cuda_check(cudaMemsetAsync(amax + AMAX_A, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
+            g.amax_out = amax + AMAX_A;
+        }
         TRY(launch_tc_gemm(g, st));
     }
     // quantise A (E4M3, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {A[i], aq[i], (long long)x.M * x.Fs, AMAX_A, FP8_E4M3};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    TRY(launch_fp8_quantize(segs, n, amax, true, st, a_fused));
     // row GEMM: Y = sum_i Aq_i W2q_i^T / (s_a s_w2) + b2 (+ X)
     GemmPlan g;
     g.name = "row_fwd";
@@ -530,6 +557,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
     const void *dya[1] = {dyq};
     const void *xa[1] = {xq};
     // row layer dgrad: dPre_i = (dYq W2q_i) / (s_dy s_w2) * act'(pre_i)
+    bool dp_fused = false;
     {
         GemmPlan g;
         g.name = d->act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
@@ -545,12 +573,18 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_out(g.out, dpre, x.T, 1, 0, gw);
         if (d->act != TP_ACT_NONE) set_out(g.aux, pre, x.T, 1, 0, gw);
         set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_W2);
+        dp_fused = d->act != TP_ACT_NONE && tc_fused_epilogue(g);
+        if (dp_fused) {  // the epilogue reduces amax(dPre) and the db1 partials
+            TRY(cuda_check(cudaMemsetAsync(amax + AMAX_DP, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
+            g.amax_out = amax + AMAX_DP;
+            if (d->has_bias) g.col_partials = partials;
+        }
         TRY(launch_tc_gemm(g, st));
     }
     // quantise dPre (E5M2, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {dpre[i], dpq[i], (long long)x.M * gw, AMAX_DP, FP8_E5M2};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    TRY(launch_fp8_quantize(segs, n, amax, true, st, dp_fused));
     // weight gradients (both operands MN-major over the tokens)
     {
         GemmPlan g;
@@ -604,7 +638,10 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
     }
     if (d->has_bias) {
         void *const *db2a = reinterpret_cast<void *const *>(&db2);
-        TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
+        if (dp_fused)
+            TRY(db1_finalize(d, gw, db1, partials, st));
+        else
+            TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
         TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
@@ -737,13 +774,17 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
     // row layer: dPre_i = (dY W2_i) * act'(pre_i), dW2_i = dY^T A_i
-    TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st));
+    bool db1_fused = false;
+    TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st, d->has_bias ? partials : nullptr, &db1_fused));
     TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st));
     // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY)
     TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st));
     TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st));
     if (d->has_bias) {
-        TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
+        if (db1_fused)
+            TRY(db1_finalize(d, gw, db1, partials, st));
+        else
+            TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
         TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;

@@ -97,7 +97,9 @@ static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, flo
     return cuda_check(e, name);
 }
 
-tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st) {
+tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st,
+                              bool amax_known) {
+    if (amax_known) return launch_pass(false, segs, nseg, amax, st);  // amax already reduced by the producer
     if (zero_slots) {
         for (int i = 0; i < nseg; ++i) {
             cudaError_t e = cudaMemsetAsync(amax + segs[i].slot, 0, sizeof(float), st);

@@ -67,6 +67,12 @@ struct GemmPlan {
     bool fp8 = false;
     int fmt_a = 0, fmt_b = 0;  // FP8_E4M3 / FP8_E5M2
     const float *amax_a = nullptr, *amax_b = nullptr;
+    // Reductions fused into the bulk-store epilogue (tc_fused_epilogue(g)):
+    // atomic max of |out| as bf16 (the FP8 amax of A / dPre; zero it first) and,
+    // for EPI_DACT, column sums of out per 32-row block into
+    // col_partials[P][ceil(M/32)][out.ld] (the db1 partials).
+    float *amax_out = nullptr;
+    float *col_partials = nullptr;
 };
 
 // Column sums over token rows: out_p[c] = sum_m in_p[m, c] for c < N, fp32.
@@ -93,13 +99,17 @@ struct QuantSeg {
 constexpr int kMaxQuantSegs = 40;
 
 // amax pass (slots optionally zeroed first) then quantise pass.
-tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st);
+tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st,
+                              bool amax_known = false);
 
 // Launchers (return a tp_status).  They only enqueue work on `st`.
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
+bool tc_fused_epilogue(const GemmPlan &g);  // true when amax_out / col_partials are honoured
 void set_tile_mode(int mode);  // TP_TILE_*
 tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
+// second pass only: out_p[c] = sum_{k < chunks} partials[p][k][c]
+tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st);
 
 // Device status words (per device), the wait limit and the launch counter.
 struct DeviceWords {

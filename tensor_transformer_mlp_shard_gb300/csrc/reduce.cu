@@ -18,18 +18,16 @@ namespace tpmlp {
 // ---------------------------------------------------------------------------
 // status words
 // ---------------------------------------------------------------------------
-__device__ int g_tp_status = 0;
+__device__ int g_tp_status = 0;  // first device-side error of any launch
 __device__ unsigned g_tp_abort = 0;
 __device__ unsigned g_tp_never_set = 0;
 
 tp_status device_words(DeviceWords *w) {
-    static int cached_dev = -1;
     static DeviceWords cached[64];
     static bool have[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
-    (void)cached_dev;
     if (dev < 64 && have[dev]) {
         *w = cached[dev];
         return TP_OK;
@@ -164,6 +162,23 @@ __global__ void colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
     float s = 0.0f;
     for (int k = 0; k < p.chunks; ++k) s += src[static_cast<long long>(k) * p.N];
     p.out[z][c] = s;
+}
+
+tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st) {
+    ColsumParams prm;
+    memset(&prm, 0, sizeof(prm));
+    for (int i = 0; i < kMaxShards; ++i) prm.out[i] = i < c.P ? c.out[i] : nullptr;
+    prm.M = c.M;
+    prm.N = c.N;
+    prm.chunks = chunks;
+    prm.partials = c.partials;
+    if (c.N == 0 || c.P == 0) return TP_OK;
+    dim3 g2((c.N + 255) / 256, c.P);
+    launch_begin("colsum_finalize", st);
+    colsum_finalize_kernel<<<g2, 256, 0, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end("colsum_finalize", st);
+    return cuda_check(e, "colsum_finalize");
 }
 
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st) {

@@ -118,6 +118,8 @@ static std::atomic<int> g_tile_mode{0};
 
 void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
 
+bool tc_fused_epilogue(const GemmPlan &g) { return !g.accumulate && !(g.act == TP_ACT_SWIGLU && g.N % 32); }
+
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     using namespace tc;
     const int ki = kernel_index(g.kind, g.A.mn_major, g.B.mn_major);
@@ -182,7 +184,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     // count that is not a multiple of 32 (a 32-column gate block would reach
     // into the up half of pre / dPre, which a store clipped at the buffer's
     // width cannot prevent).
-    prm.out_tma = !g.accumulate && !(g.act == TP_ACT_SWIGLU && g.N % 32) ? 1 : 0;
+    prm.out_tma = tc_fused_epilogue(g) ? 1 : 0;
     if (prm.out_tma) {
         const bool f32 = g.kind == EPI_F32;
         // columns of a whole output row: pre / dPre hold both SwiGLU halves
@@ -196,6 +198,9 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
             if (s != TP_OK) return s;
         }
     }
+    prm.amax_out = prm.out_tma ? g.amax_out : nullptr;
+    prm.col_partials = prm.out_tma && g.kind == EPI_DACT ? g.col_partials : nullptr;
+    prm.partial_ld = static_cast<int>(g.out.ld);
     prm.amax_a = fp8 ? g.amax_a : nullptr;
     prm.amax_b = fp8 ? g.amax_b : nullptr;
     prm.fmax_a = g.fmt_a == FP8_E5M2 ? 57344.0f : 448.0f;

@@ -75,6 +75,9 @@ struct Params {
     int m_tiles, n_tiles, total_tiles, group_m;
     int act, b_dual_off, accumulate;
     uint32_t idesc;                  // tcgen05 instruction descriptor (formats, majors, M, N)
+    float *amax_out;                 // bulk-store epilogue: atomic max |bf16 output| (A / dPre), or null
+    float *col_partials;             // DACT bulk-store epilogue: per-32-row-block column sums, or null
+    int partial_ld;                  //   [P][ceil(M/32)][partial_ld] floats
     const float *amax_a, *amax_b;    // FP8: per-tensor amax of the two operands, else null
     float fmax_a, fmax_b;            // FP8: largest finite value of each operand's format
     int *status;
@@ -394,6 +397,58 @@ __device__ __forceinline__ void load_bf16x8_guarded(const __nv_bfloat16 *src, bo
     }
 }
 
+// Column sums of a 32 x 32 block held one row per lane (v[j] = column j of
+// this lane's row): a recursive-halving exchange leaves the sum of column
+// `lane` in v[0] after 31 shuffles.
+__device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float send = upper ? v[j] : v[j + o];
+            const float keep = upper ? v[j + o] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// db1 partials and amax of one 32-column block of outputs: rows past M and
+// columns past N contribute nothing.  The partial sums add the fp32 values the
+// epilogue rounds to bf16; the amax is rounded once when flushed (rounding is
+// monotone, so max |bf16(v)| = bf16(max |v|)).
+__device__ __forceinline__ void fused_reductions(const Params &p, int pi, int row0, int col0, const float *vals,
+                                                 bool row_ok, int lane, float &amx, int part_off = 0) {
+    float v[32];
+    if (row_ok && col0 + 32 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = vals[j];
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (row_ok && col0 + j < p.N) ? vals[j] : 0.0f;
+    }
+    if (p.amax_out) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amx = fmaxf(amx, fabsf(v[j]));
+    }
+    if (p.col_partials) {
+        const float sum = warp_column_sum32(v, lane);
+        if (col0 + lane < p.N)
+            p.col_partials[(static_cast<long long>(pi) * ((p.M + 31) / 32) + row0 / 32) * p.partial_ld + part_off + col0 +
+                           lane] = sum;
+    }
+}
+
+__device__ __forceinline__ void flush_amax(const Params &p, float amx) {
+    if (!p.amax_out) return;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amx = fmaxf(amx, __shfl_xor_sync(0xffffffffu, amx, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned *>(p.amax_out), __float_as_uint(bf16_round(amx)));
+}
+
 template <int EPI>
 __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int row, int nt, uint32_t taddr, int half,
                                                  float dq, Stager &stg, int lane) {
@@ -405,6 +460,8 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
     if (p.has_out2) out_index(p.out2, pi, row0, oi2, oy2);
     const __nv_bfloat16 *bias =
         p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
+    const bool fuse = p.amax_out != nullptr || p.col_partials != nullptr;
+    float amx = 0.0f;  // max |bf16 output| of this thread (FP8 scale of A / dPre)
     uint4 w[4];
     if (EPI == EPI_COL && p.act == TP_ACT_SWIGLU) {
         // accumulator columns [0,128) = gate units, [128,256) = up units (N % 32 == 0 here)
@@ -445,9 +502,57 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) G[j] = G[j] * sigmoid_fast(G[j]) * U[j];
+            if (fuse) fused_reductions(p, pi, row0, u0, G, row_ok, lane, amx);
             pack_bf16x32(G, w);
             stage_store(stg, &p.mapO[oi], u0, oy, w, lane);
         }
+        if (fuse) flush_amax(p, amx);
+        return;
+    }
+    const int n0 = nt * BN;
+        const bool gelu = p.act == TP_ACT_GELU_TANH;
+        const __nv_bfloat16 *pre = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
+        uint4 nxt[4];
+        auto fetch = [&](int c, uint4(&dst)[4]) {
+            const int col0 = n0 + c * 32;
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8)
+                dst[g8] = (gelu && row_ok && col0 + 8 * g8 < p.N)
+                              ? *reinterpret_cast<const uint4 *>(pre + col0 + 8 * g8)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        };
+        fetch(4 * half, nxt);
+#pragma unroll 1
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
+            uint4 cur[4];
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) cur[g8] = nxt[g8];
+            if (c + 1 < 4 * half + 4) fetch(c + 1, nxt);
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+            const int col0 = n0 + c * 32;
+            if (!block_ok || col0 >= p.N) continue;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * dq;
+            if (gelu) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const uint32_t q4[4] = {cur[g8].x, cur[g8].y, cur[g8].z, cur[g8].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        v[8 * g8 + 2 * k] *= gelu_tanh_grad_fast(bf16_lo(q4[k]));
+                        v[8 * g8 + 2 * k + 1] *= gelu_tanh_grad_fast(bf16_hi(q4[k]));
+                    }
+                }
+            }
+            if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
+            pack_bf16x32(v, w);
+            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+        }
+        if (fuse) flush_amax(p, amx);
         return;
     }
     const int n0 = nt * BN;
@@ -491,6 +596,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
             }
+            if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
             pack_bf16x32(v, w);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
         } else if (EPI == EPI_PLAIN) {
@@ -524,6 +630,11 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                         dU[8 * g8 + j] = d * G[j] * s;
                     }
                 }
+                if (fuse) {
+                    // dG feeds db1 columns [0, N), dU columns [N, 2N)
+                    fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
+                    fused_reductions(p, pi, row0, col0, dU, row_ok, lane, amx, p.N);
+                }
                 pack_bf16x32(v, w);
                 stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
                 pack_bf16x32(dU, w);
@@ -538,11 +649,13 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                         for (int j = 0; j < 8; ++j) v[8 * g8 + j] *= gelu_tanh_grad_fast(x[j]);
                     }
                 }
+                if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
                 pack_bf16x32(v, w);
                 stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
             }
         }
     }
+    if (fuse) flush_amax(p, amx);
 }
 
 template <int EPI>

@@ -131,8 +131,8 @@ def test_workspace_sizes(tp):
     assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
     ws = L.tp_mlp_workspace_bytes(h)
     dpre = 8 * 8192 * 2048 * 2
-    chunks = 8192 // 256
-    partials = 4 * 8 * chunks * 2048
+    # db1 partials: one fp32 row of column sums per 32-token block and shard
+    partials = 4 * 8 * (8192 // 32) * 2048
     assert ws == dpre + partials
     L.tp_mlp_destroy(h)
     lay2 = tp.Layout(S=2048, B=4, H=4096, F=16384, T=8, act="none", has_bias=False)

@@ -75,6 +75,7 @@ CASES = [
     (300, 272, 832, 4, "gelu_tanh", True, True, False),
     (300, 272, 832, 4, "swiglu", False, False, False),
     (512, 256, 1024, 4, "gelu_tanh", False, False, True),
+    (256, 256, 1024, 4, "swiglu", True, True, False),
     (2048, 1024, 8192, 8, "gelu_tanh", True, True, False),
 ]
 

@@ -48,6 +48,7 @@ CASES = [
     (1024, 264, 1600, 8, "gelu_tanh", "bf16", False, False, True),
     (512, 200, 1024, 4, "swiglu", "bf16", False, True, True),
     (384, 136, 384, 3, "gelu_tanh", "bf16", True, True, True),
+    (256, 264, 1024, 4, "swiglu", "bf16", True, False, False),
     (2048, 1024, 8192, 8, "gelu_tanh", "bf16", True, True, False),
     (256, 256, 1024, 2, "gelu_tanh", "f32", True, False, False),
     (300, 264, 800, 4, "swiglu", "f32", True, True, False),
