@@ -510,52 +510,6 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
         return;
     }
     const int n0 = nt * BN;
-        const bool gelu = p.act == TP_ACT_GELU_TANH;
-        const __nv_bfloat16 *pre = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
-        uint4 nxt[4];
-        auto fetch = [&](int c, uint4(&dst)[4]) {
-            const int col0 = n0 + c * 32;
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8)
-                dst[g8] = (gelu && row_ok && col0 + 8 * g8 < p.N)
-                              ? *reinterpret_cast<const uint4 *>(pre + col0 + 8 * g8)
-                              : make_uint4(0u, 0u, 0u, 0u);
-        };
-        fetch(4 * half, nxt);
-#pragma unroll 1
-        for (int c = 4 * half; c < 4 * half + 4; ++c) {
-            uint4 cur[4];
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) cur[g8] = nxt[g8];
-            if (c + 1 < 4 * half + 4) fetch(c + 1, nxt);
-            uint32_t r[32];
-            __syncwarp();
-            tmem_ld32(taddr + c * 32, r);
-            tmem_ld_wait();
-            const int col0 = n0 + c * 32;
-            if (!block_ok || col0 >= p.N) continue;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * dq;
-            if (gelu) {
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    const uint32_t q4[4] = {cur[g8].x, cur[g8].y, cur[g8].z, cur[g8].w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        v[8 * g8 + 2 * k] *= gelu_tanh_grad_fast(bf16_lo(q4[k]));
-                        v[8 * g8 + 2 * k + 1] *= gelu_tanh_grad_fast(bf16_hi(q4[k]));
-                    }
-                }
-            }
-            if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
-            pack_bf16x32(v, w);
-            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
-        }
-        if (fuse) flush_amax(p, amx);
-        return;
-    }
-    const int n0 = nt * BN;
 #pragma unroll 1
     for (int c = 4 * half; c < 4 * half + 4; ++c) {
         uint32_t r[32];
