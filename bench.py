@@ -158,8 +158,11 @@ def recorded_traffic(w, tile_mode, kernel):
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, rec["kernel_source"]), "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
+        h = hashlib.sha256()
+        for src in rec["kernel_sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        digest = h.hexdigest()
     except (OSError, KeyError, ValueError):
         return None
     if digest != rec.get("sha256") or rec.get("tile_mode") not in (tile_mode, "pair" if tile_mode == "auto" else None):
