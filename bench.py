@@ -8,6 +8,8 @@ inputs.  The metric is algorithmic TFLOP/s (12*M*H*F per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+  python bench.py --block layer ...      # the TransformerLayer MLP sub-block:
+                                         # LayerNorm -> MLP -> dropout + residual
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (the library's shards all live on one GPU); the reported value is
@@ -149,6 +151,20 @@ def kernel_flops(w):
             "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H}
 
 
+LAYER_DROPOUT_P = 0.1  # Megatron's default hidden dropout
+LAYER_SEED = 0x5EED_0000_0001
+
+
+def hbm_kernel_bytes(w):
+    """Algorithmic HBM bytes of one launch of the sub-block's memory-bound
+    kernels (each operand read or written once)."""
+    M, H = w.M, w.H
+    es = 4 if w.dtype == "f32" else 2
+    return {"layernorm_fwd": 2 * M * H * es + 2 * H * es + 8 * M,
+            "layernorm_bwd": 4 * M * H * es + H * es + 8 * M,
+            "dropout_bwd": 2 * M * H * es}
+
+
 def recorded_traffic(w, tile_mode, kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
     when there is none for this workload and tiling or the kernel source has
@@ -182,8 +198,13 @@ def run_gpu(args, w, dist, rank, local, ws):
     bf = torch.bfloat16
     T, M, H, F, g = w.T, w.M, w.H, w.F, w.g
     Fs = F // T
-    lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
-                   residual=w.residual, seq_parallel=w.seq_parallel)
+    layer = args.block == "layer"
+    if layer:
+        lay = tp.TPLayer(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
+                         seq_parallel=w.seq_parallel, dropout_p=LAYER_DROPOUT_P)
+    else:
+        lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
+                       residual=w.residual, seq_parallel=w.seq_parallel)
     full = synth.mlp_tensors(w)
     td = torch.float32 if w.dtype == "f32" else bf
 
@@ -219,10 +240,24 @@ def run_gpu(args, w, dist, rank, local, ws):
     db2 = torch.empty(H, dtype=f32, device=dev) if w.has_bias else None
     wsp = tp.alloc_workspace(lay.workspace_bytes(), device=dev)
     stream = torch.cuda.current_stream(dev)
+    if layer:
+        lnp = synth.layer_tensors(1, H, w.dtype)
+        gamma, beta = up(lnp["gamma"]), up(lnp["beta"])
+        Xn = torch.empty(M, H, dtype=td, device=dev)
+        mean = torch.empty(M, dtype=f32, device=dev)
+        rstd = torch.empty(M, dtype=f32, device=dev)
+        dgamma = torch.empty(H, dtype=f32, device=dev)
+        dbeta = torch.empty(H, dtype=f32, device=dev)
 
-    def step():
-        lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp if w.dtype == "fp8" else None)
-        lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
+        def step():
+            lay.fwd(X, gamma, beta, W1, b1, W2, b2, LAYER_SEED, Y, Xn, mean, rstd, pre, A, workspace=wsp,
+                    stream=stream)
+            lay.bwd(dY, X, gamma, Xn, mean, rstd, W1, W2, pre, A, LAYER_SEED, dX, dgamma, dbeta, dW1, db1, dW2,
+                    db2, wsp, stream=stream)
+    else:
+        def step():
+            lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp if w.dtype == "fp8" else None)
+            lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
 
     # ---- device-resident timing --------------------------------------------
     for _ in range(args.warmup):
@@ -288,12 +323,17 @@ def run_gpu(args, w, dist, rank, local, ws):
     # ---- roofline of the dominant kernel -----------------------------------
     peaks = load_peaks()
     kf = kernel_flops(w)
+    kb = hbm_kernel_bytes(w)
     per_kernel = {}
     for name, (n, tot) in kernels.items():
         avg = tot / max(1, n)
         ent = {"launches": n, "avg_ms": round(avg, 4), "share": None}
         if name in kf and avg > 0:
             ent["tflops"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+        if name in kb and avg > 0:
+            gbs = kb[name] / (avg * 1e-3) / 1e9
+            ent["gbs"] = round(gbs, 1)
+            ent["hbm_frac"] = round(gbs / peaks["hbm_gbs"], 4)
         per_kernel[name] = ent
     tot_all = sum(t for _, t in kernels.values()) or 1.0
     for name, (n, tot) in kernels.items():
@@ -312,7 +352,7 @@ def run_gpu(args, w, dist, rank, local, ws):
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                     "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
-    if roofline is not None and w.dtype == "bf16":
+    if roofline is not None and w.dtype == "bf16" and not layer:
         roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
     step_frac = value / ws / (peaks["bf16_tflops_sustained"] * (2.0 if w.dtype == "fp8" else 1.0))
     return {
@@ -327,10 +367,12 @@ def run_gpu(args, w, dist, rank, local, ws):
 # ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_sample(w, tokens, full=None):
-    """Time the fp64 oracle's fwd+bwd on the first `tokens` tokens of the
-    workload with the full weights; returns (seconds, algorithmic FLOP)."""
+def oracle_sample(w, tokens, full=None, block="mlp"):
+    """Time the fp64 oracle's fwd+bwd (of the MLP, or of the sub-block) on the
+    first `tokens` tokens of the workload with the full weights; returns
+    (seconds, algorithmic FLOP)."""
     import oracle
+    from oracle import layer as olayer
     if full is None:
         full = synth.mlp_tensors(w, M=tokens)
     W1s = oracle.shard_column_weight(full["W1"], w.T, w.act)
@@ -338,8 +380,14 @@ def oracle_sample(w, tokens, full=None):
     W2s = oracle.shard_row_weight(full["W2"], w.T)
     X, dY = full["X"][:tokens], full["dY"][:tokens]
     t0 = time.perf_counter()
-    pre, A, _ = oracle.mlp_fwd(X, W1s, b1s, W2s, full["b2"], w.act, w.residual)
-    oracle.mlp_bwd(dY, X, W1s, W2s, pre, A, w.act, w.residual)
+    if block == "layer":
+        lnp = synth.layer_tensors(1, w.H, w.dtype)
+        f = olayer.layer_fwd(X, lnp["gamma"], lnp["beta"], W1s, b1s, W2s, full["b2"], w.act, LAYER_DROPOUT_P,
+                             LAYER_SEED)
+        olayer.layer_bwd(dY, X, lnp["gamma"], W1s, W2s, f, w.act, LAYER_DROPOUT_P)
+    else:
+        pre, A, _ = oracle.mlp_fwd(X, W1s, b1s, W2s, full["b2"], w.act, w.residual)
+        oracle.mlp_bwd(dY, X, W1s, W2s, pre, A, w.act, w.residual)
     dt = time.perf_counter() - t0
     flops = 3.0 * (2.0 * tokens * w.H * w.F * w.g + 2.0 * tokens * w.F * w.H)
     return dt, flops
@@ -352,20 +400,20 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def run_reference(args, w, rank):
+def run_reference(args, w, rank, block="mlp"):
     # per-step sample sized so that warm-up + timed steps take ~2 minutes
     probe_tokens = 64
     full = synth.mlp_tensors(w, M=2048)
-    dt, fl = oracle_sample(w, probe_tokens, full)
+    dt, fl = oracle_sample(w, probe_tokens, full, block)
     rate = fl / dt
     budget = 120.0 / max(1, args.steps + args.warmup)
     per_token = 3.0 * (2.0 * w.H * w.F * w.g + 2.0 * w.F * w.H)
     tokens = int(max(64, min(2048, budget * rate / per_token)))
     for _ in range(args.warmup):
-        oracle_sample(w, tokens, full)
+        oracle_sample(w, tokens, full, block)
     tot_t, tot_f = 0.0, 0.0
     for _ in range(args.steps):
-        dt, fl = oracle_sample(w, tokens, full)
+        dt, fl = oracle_sample(w, tokens, full, block)
         tot_t += dt
         tot_f += fl
     value = tot_f / tot_t / 1e12
@@ -376,10 +424,10 @@ def run_reference(args, w, rank):
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def cpu_baseline(w):
+def cpu_baseline(w, block="mlp"):
     tokens = 1024
     full = synth.mlp_tensors(w, M=tokens)
-    dt, fl = oracle_sample(w, tokens, full)
+    dt, fl = oracle_sample(w, tokens, full, block)
     return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"fp64 numpy oracle fwd+bwd on the first {tokens} of {w.M} tokens with the full weights "
                       f"({fl / 1e9:.0f} GFLOP, {dt:.1f} s)"}
@@ -396,6 +444,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", default="workload", choices=["workload", "fp8"],
                     help="fp8: the FP8 variant (E4M3 forward, E5M2 backward, bf16 buffers) of the workload")
+    ap.add_argument("--block", default="mlp", choices=["mlp", "layer"],
+                    help="layer: the TransformerLayer MLP sub-block, Y = X + dropout(MLP(LayerNorm(X))), "
+                         f"p = {LAYER_DROPOUT_P}")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
     args = ap.parse_args()
@@ -415,6 +466,10 @@ def main():
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
               "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
               "tile_mode": args.tile_mode}
+    if args.block == "layer":
+        config["workload"] += f"; TransformerLayer MLP sub-block: LayerNorm -> MLP -> dropout(p={LAYER_DROPOUT_P})" \
+                              " + residual"
+        config["block"] = "layer"
     base = {"metric": METRIC, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded SplitMix64 + Box-Muller), random-init weights", "config": config}
@@ -426,7 +481,7 @@ def main():
         out["impl"] = "reference"
         out["n_gpus"] = 1
         out["dtype"] = "f64"
-        out.update(run_reference(args, w, rank))
+        out.update(run_reference(args, w, rank, args.block))
         print(json.dumps(out))
         return
 
@@ -437,7 +492,7 @@ def main():
         out = dict(base)
         out.update(res)
         if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(w)
+            out["cpu_baseline"] = cpu_baseline(w, args.block)
         print(json.dumps(out))
     if dist is not None:
         dist.destroy_process_group()

@@ -226,6 +226,71 @@ TP_API tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *
                                            void *const *dX, void *const *dW, void *db,
                                            void *stream);
 
+/* ---- TransformerLayer MLP sub-block (walk-through s03; "Megatron-LM 源码精读"
+ * s3.5) ---------------------------------------------------------------------
+ * The MLP half of a transformer layer, on the tensor-parallel MLP above:
+ *   Xn = LayerNorm(X; gamma, beta)  per token over H: (x - mean) * rstd *
+ *                                   gamma + beta, population variance,
+ *                                   rstd = 1 / sqrt(var + ln_eps)
+ *   Z  = MLP(Xn)                    as tp_mlp_fwd (b2 included), no residual
+ *   Y  = X + dropout_p(Z)           bias-dropout-add; the residual is X
+ * Dropout: element (m, h) of Z, m the global token index (sequence sharding
+ * does not change it), uses word e mod 4 of Philox4x32-10 (Salmon et al.,
+ * SC 2011) with counter (q mod 2^32, q div 2^32, 0, 0), q = e div 4,
+ * e = m*H + h, and key (seed mod 2^32, seed div 2^32); it is kept iff the
+ * word's top 24 bits are >= floor(p * 2^24) and kept values are scaled by
+ * 1/(1-p).  The backward redraws the flags from the same seed.  p = 0 skips
+ * the dropout.  Under sequence parallelism X, Y, dY and dX are T token shards
+ * as in the MLP; Xn is one contiguous [M, H] buffer (the gathered LayerNorm
+ * output the column layer reads). */
+typedef struct {
+    tp_mlp_desc mlp;  /* the MLP; mlp.residual must be 0 (the block adds X) */
+    float dropout_p;  /* in [0, 1) */
+    float ln_eps;     /* > 0 (1e-5 in Megatron) */
+} tp_layer_desc;
+
+typedef struct tp_layer tp_layer;
+
+/* Validate and create (host only).  Besides tp_mlp_create's checks: TP_ERR_ARG
+ * for mlp.residual != 0, p outside [0, 1) or ln_eps <= 0; TP_ERR_UNSUPPORTED
+ * for H above 8192 (bf16, FP8) or 4096 (fp32), the LayerNorm kernels' row
+ * capacity. */
+TP_API tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out);
+TP_API void tp_layer_destroy(tp_layer *h);
+
+/* Bytes of device workspace for tp_layer_bwd (and, for TP_DT_FP8,
+ * tp_layer_fwd, whose quantised operands the backward reads from it): the
+ * MLP's workspace, dZ and dXn ([M, H] each). */
+TP_API size_t tp_layer_workspace_bytes(const tp_layer *h);
+
+/* Forward.  X, Y: like tp_mlp_fwd's X and Y; gamma, beta: [H] (bf16, fp32 for
+ * TP_DT_F32); W1, b1, W2, b2, pre, A: as in tp_mlp_fwd; seed: dropout key.
+ * Outputs kept for the backward: Xn [M, H] (activation dtype), mean and rstd
+ * [M] fp32, pre, A.  workspace: required (>= tp_layer_workspace_bytes,
+ * 256-byte aligned) for TP_DT_FP8 and then passed unchanged to tp_layer_bwd;
+ * ignored otherwise (may be NULL). */
+TP_API tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, const void *beta,
+                              const void *const *W1, const void *const *b1, const void *const *W2,
+                              const void *b2, uint64_t seed, void *const *Y, void *Xn, float *mean,
+                              float *rstd, void *const *pre, void *const *A, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* Backward.  dY, dX: like Y and X; X, gamma, Xn, mean, rstd, W1, W2, pre, A
+ * and seed: as given to / produced by tp_layer_fwd.  Computes
+ *   dZ  = dY * keep / (1 - p),
+ *   the MLP backward on (dZ, Xn): dW1, db1, dW2, db2 exactly as tp_mlp_bwd
+ *     (fp32, wgrad_accumulate honoured) and dXn,
+ *   dX  = dY + rstd * (g - mean_h(g) - xhat * mean_h(g * xhat)) with
+ *         g = dXn * gamma, xhat = (X - mean) * rstd,
+ *   dgamma = sum_m dXn * xhat, dbeta = sum_m dXn ([H] fp32, overwritten).
+ * workspace: >= tp_layer_workspace_bytes, 256-byte aligned. */
+TP_API tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X, const void *gamma,
+                              const void *Xn, const float *mean, const float *rstd,
+                              const void *const *W1, const void *const *W2, const void *const *pre,
+                              const void *const *A, uint64_t seed, void *const *dX, float *dgamma,
+                              float *dbeta, void *const *dW1, void *const *db1, void *const *dW2,
+                              void *db2, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Per-tensor FP8 quantisation of one logical tensor split over `nbuf` bf16
  * buffers (its shards): amax = max |x| over all buffers (the cross-shard amax
  * reduction), scale = fmax / amax in fp32 (1 if amax is 0), then

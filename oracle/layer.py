@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from . import fp8 as _fp8
 from . import mlp as _mlp
 
 LN_EPS = 1e-5
@@ -121,4 +122,30 @@ def layer_bwd(dY, X, gamma, W1s, W2s, f, act: str, p: float):
     g = _mlp.mlp_bwd(dZ, f["Xn"], W1s, W2s, f["pre"], f["A"], act, False)
     dXln, dgamma, dbeta = layernorm_bwd(g["dX"], X, gamma, f["mean"], f["rstd"])
     g.update(dZ=dZ, dXn=g["dX"], dX=dY + dXln, dgamma=dgamma, dbeta=dbeta)
+    return g
+
+
+def layer_fwd_fp8(X, gamma, beta, W1s, b1s, W2s, b2, act: str, p: float, seed: int, eps: float = LN_EPS):
+    """The sub-block with the MLP in the FP8 variant (fp8.py): the LayerNorm
+    output is stored in bf16 and that bf16 tensor is the MLP's input (reading
+    F4 of fp8.py applied to Xn)."""
+    Xn, mean, rstd = layernorm_fwd(X, gamma, beta, eps)
+    Xn_b = _fp8.round_bf16(Xn)
+    f = _fp8.mlp_fwd_fp8(Xn_b, W1s, b1s, W2s, b2, act, False)
+    Z = f["Y"]
+    keep = dropout_keep(seed, np.arange(Z.shape[0]), Z.shape[1], p)
+    Y = np.asarray(X, np.float64) + np.where(keep, Z / (1.0 - p), 0.0)
+    return {"Xn": Xn_b, "mean": mean, "rstd": rstd, "pre": f["pre"], "A": f["A"], "Z": Z, "keep": keep, "Y": Y,
+            "mlp": f}
+
+
+def layer_bwd_fp8(dY, X, gamma, act: str, p: float, f):
+    """Backward of layer_fwd_fp8: dZ and dXn are stored in bf16 (F4), the MLP
+    backward is fp8.mlp_bwd_fp8 on dZ."""
+    dY = np.asarray(dY, np.float64)
+    dZ = _fp8.round_bf16(np.where(f["keep"], dY / (1.0 - p), 0.0))
+    g = _fp8.mlp_bwd_fp8(dZ, f["mlp"], act, False)
+    dXn = _fp8.round_bf16(g["dX"])
+    dXln, dgamma, dbeta = layernorm_bwd(dXn, X, gamma, f["mean"], f["rstd"])
+    g.update(dZ=dZ, dXn=dXn, dX=dY + dXln, dgamma=dgamma, dbeta=dbeta)
     return g

@@ -30,6 +30,7 @@ SEED_BASE = 20261202
 # tensor ids (seed = SEED_BASE + id)
 TID_X, TID_W1, TID_B1, TID_W2, TID_B2, TID_DY = 1, 2, 3, 4, 5, 6
 TID_Z, TID_DY_QKV, TID_DY_O, TID_WQKV, TID_WO = 7, 8, 9, 10, 11
+TID_GAMMA, TID_BETA, TID_ROW_SHIFT, TID_ROW_SCALE = 12, 13, 14, 15
 
 
 def build(force: bool = False) -> str:
@@ -198,4 +199,22 @@ def attn_tensors(w: Workload, M: int | None = None):
         "Wo": rnd(normal(SEED_BASE + TID_WO, (w.H, w.F_o), w.w_std)),
         "dYqkv": rnd(normal(SEED_BASE + TID_DY_QKV, (M, w.F), w.dy_std)),
         "dYo": rnd(normal(SEED_BASE + TID_DY_O, (M, w.H), w.dy_std)),
+    }
+
+
+def layer_tensors(M: int, H: int, dtype: str, seed_off: int = 0):
+    """LayerNorm parameters and a residual-stream-like input for the
+    TransformerLayer MLP sub-block: gamma ~ 1 + 0.1 N(0,1), beta ~ 0.05 N(0,1)
+    ([H]), and X [M, H] whose rows have their own offset (N(0,1)) and scale
+    (0.5 + |N(0,1)|) around a N(0,1) body, so that the LayerNorm's mean and
+    variance differ per token.  Rounded to bf16 unless dtype is "f32"."""
+    rnd = (lambda a: a) if dtype == "f32" else round_bf16
+    base = SEED_BASE + 1000 * seed_off
+    shift = normal(base + TID_ROW_SHIFT, (M, 1), 1.0)
+    scale = 0.5 + np.abs(normal(base + TID_ROW_SCALE, (M, 1), 1.0))
+    X = normal(base + TID_X, (M, H), 1.0) * scale + shift
+    return {
+        "X": rnd(X.astype(np.float32)),
+        "gamma": rnd(normal(base + TID_GAMMA, (H,), 0.1, mean=1.0)),
+        "beta": rnd(normal(base + TID_BETA, (H,), 0.05)),
     }

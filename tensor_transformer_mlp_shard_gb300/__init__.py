@@ -5,7 +5,7 @@ all T shards in one GPU's memory; the cross-shard all-reduces are fp32 sums
 inside the tcgen05 GEMM kernels of ``libtpmlp.so`` (C ABI in
 ``include/tp_mlp.h``).  This package is the thin Python binding.
 """
-from .binding import (ACT, DTYPE, Layout, TPMLP, TpError, alloc_workspace, debug_wait_timeout,  # noqa: F401
+from .binding import (ACT, DTYPE, Layout, TPLayer, TPMLP, TpError, alloc_workspace, debug_wait_timeout,  # noqa: F401
                       fp8_quantize,
                       launch_count, lib, library_path, linear_col, linear_col_bwd, linear_row, linear_row_bwd,
                       linear_row_bwd_noalloc,

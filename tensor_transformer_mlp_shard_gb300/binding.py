@@ -37,6 +37,10 @@ class Desc(ctypes.Structure):
                 ("residual", ctypes.c_int), ("seq_parallel", ctypes.c_int), ("wgrad_accumulate", ctypes.c_int)]
 
 
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("mlp", Desc), ("dropout_p", ctypes.c_float), ("ln_eps", ctypes.c_float)]
+
+
 class ProfEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
@@ -62,6 +66,13 @@ SIGNATURES = {
     "tp_linear_col_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd_noalloc": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP]),
+    "tp_layer_create": (ctypes.c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(VP)]),
+    "tp_layer_destroy": (None, [VP]),
+    "tp_layer_workspace_bytes": (ctypes.c_size_t, [VP]),
+    "tp_layer_fwd": (ctypes.c_int, [VP, PP, VP, VP, PP, PP, PP, VP, ctypes.c_uint64, PP, VP, VP, VP, PP, PP, VP,
+                                    ctypes.c_size_t, VP]),
+    "tp_layer_bwd": (ctypes.c_int, [VP, PP, PP, VP, VP, VP, VP, PP, PP, PP, PP, ctypes.c_uint64, PP, VP, VP, PP,
+                                    PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_fp8_quantize": (ctypes.c_int, [PP, PP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int, VP, VP]),
     "tp_sync_status": (ctypes.c_int, [VP]),
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
@@ -237,6 +248,77 @@ class TPMLP(Layout):
         _check(lib().tp_mlp_bwd(self._h, _arr(pdy), _arr(px), _arr(pw1), _arr(pw2), _arr(pp), _arr(pa),
                                 _arr(pdx), _arr(pdw1), _arr(pdb1), _arr(pdw2), pdb2, ws_ptr, ws_bytes,
                                 _stream(stream)))
+
+
+class TPLayer(Layout):
+    """Handle for the TransformerLayer MLP sub-block
+    Y = X + dropout_p(MLP(LayerNorm(X))) (tp_layer_create).  The MLP keyword
+    arguments are those of TPMLP (residual must stay False)."""
+
+    def __init__(self, *args, dropout_p: float = 0.0, ln_eps: float = 1e-5, **kw):
+        super().__init__(*args, **kw)
+        self.dropout_p, self.ln_eps = float(dropout_p), float(ln_eps)
+        self._d = LayerDesc(self.desc(), self.dropout_p, self.ln_eps)
+        h = VP()
+        _check(lib().tp_layer_create(ctypes.byref(self._d), ctypes.byref(h)))
+        self._h = h
+        self._c = _Checker(self.dtype)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.tp_layer_destroy(h)
+            self._h = None
+
+    def workspace_bytes(self) -> int:
+        return int(lib().tp_layer_workspace_bytes(self._h))
+
+    def fwd(self, X, gamma, beta, W1, b1, W2, b2, seed, Y, Xn, mean, rstd, pre, A, workspace=None, stream=None):
+        c, T, H, Fs, g, M = self._c, self.T, self.H, self.Fs, self.g, self.M
+        f32 = torch.float32
+        px = c.tensors("X", X, self.nx, (self.xrows, H))
+        pg = c.tensors("gamma", gamma, 1, (H,))[0]
+        pbt = c.tensors("beta", beta, 1, (H,))[0]
+        pw1 = c.tensors("W1", W1, T, (g * Fs, H))
+        pw2 = c.tensors("W2", W2, T, (H, Fs))
+        pb1 = c.tensors("b1", b1, T, (g * Fs,)) if self.has_bias else None
+        pb2 = c.tensors("b2", b2, 1, (H,))[0] if self.has_bias else None
+        py = c.tensors("Y", Y, self.nx, (self.xrows, H))
+        pxn = c.tensors("Xn", Xn, 1, (M, H))[0]
+        pm = c.tensors("mean", mean, 1, (M,), f32)[0]
+        pr = c.tensors("rstd", rstd, 1, (M,), f32)[0]
+        pp = c.optional("pre", pre, T, (M, g * Fs))
+        pa = c.tensors("A", A, T, (M, Fs))
+        ws_ptr, ws_bytes = (None, 0) if workspace is None else _workspace(workspace, self.workspace_bytes())
+        _check(lib().tp_layer_fwd(self._h, _arr(px), pg, pbt, _arr(pw1), _arr(pb1), _arr(pw2), pb2,
+                                  int(seed) & (2 ** 64 - 1), _arr(py), pxn, pm, pr, _arr(pp), _arr(pa), ws_ptr,
+                                  ws_bytes, _stream(stream)))
+
+    def bwd(self, dY, X, gamma, Xn, mean, rstd, W1, W2, pre, A, seed, dX, dgamma, dbeta, dW1, db1, dW2, db2,
+            workspace, stream=None):
+        c, T, H, Fs, g, M = self._c, self.T, self.H, self.Fs, self.g, self.M
+        f32 = torch.float32
+        pdy = c.tensors("dY", dY, self.nx, (self.xrows, H))
+        px = c.tensors("X", X, self.nx, (self.xrows, H))
+        pg = c.tensors("gamma", gamma, 1, (H,))[0]
+        pxn = c.tensors("Xn", Xn, 1, (M, H))[0]
+        pm = c.tensors("mean", mean, 1, (M,), f32)[0]
+        pr = c.tensors("rstd", rstd, 1, (M,), f32)[0]
+        pw1 = c.tensors("W1", W1, T, (g * Fs, H))
+        pw2 = c.tensors("W2", W2, T, (H, Fs))
+        pp = c.optional("pre", pre, T, (M, g * Fs))
+        pa = c.tensors("A", A, T, (M, Fs))
+        pdx = c.tensors("dX", dX, self.nx, (self.xrows, H))
+        pdg = c.tensors("dgamma", dgamma, 1, (H,), f32)[0]
+        pdb = c.tensors("dbeta", dbeta, 1, (H,), f32)[0]
+        pdw1 = c.tensors("dW1", dW1, T, (g * Fs, H), f32)
+        pdw2 = c.tensors("dW2", dW2, T, (H, Fs), f32)
+        pdb1 = c.tensors("db1", db1, T, (g * Fs,), f32) if self.has_bias else None
+        pdb2 = c.tensors("db2", db2, 1, (H,), f32)[0] if self.has_bias else None
+        ws_ptr, ws_bytes = _workspace(workspace, self.workspace_bytes())
+        _check(lib().tp_layer_bwd(self._h, _arr(pdy), _arr(px), pg, pxn, pm, pr, _arr(pw1), _arr(pw2), _arr(pp),
+                                  _arr(pa), int(seed) & (2 ** 64 - 1), _arr(pdx), pdg, pdb, _arr(pdw1), _arr(pdb1),
+                                  _arr(pdw2), pdb2, ws_ptr, ws_bytes, _stream(stream)))
 
 
 def _workspace(workspace, need):

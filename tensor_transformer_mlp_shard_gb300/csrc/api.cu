@@ -31,6 +31,13 @@ struct tp_mlp {
     tp_mlp_desc d;
 };
 
+struct tp_layer {
+    tp_layer_desc d;
+    tp_mlp_desc inner;  // the MLP inside the sub-block: d.mlp with the residual handled by the block
+    uint32_t drop_threshold;
+    float drop_scale;
+};
+
 namespace tpmlp {
 
 tp_status read_and_clear_status(cudaStream_t st, int *out);
@@ -251,9 +258,26 @@ static tp_status column_fwd(const tp_mlp_desc *d, const void *const *X, const vo
     return run_gemm(g, d->dtype, st);
 }
 
+// Dropout of the row forward's output (TransformerLayer bias-dropout-add):
+// Y = R + dropout(sum + b), element m*H + h drawn from Philox4x32-10 under `seed`.
+struct DropCfg {
+    bool on = false;
+    uint32_t threshold = 0;  // floor(p * 2^24)
+    float scale = 1.0f;      // 1 / (1 - p)
+    uint64_t seed = 0;
+};
+
+static void set_drop(GemmPlan &g, const DropCfg *dc) {
+    if (!dc || !dc->on) return;
+    g.dropout = true;
+    g.drop_threshold = dc->threshold;
+    g.drop_scale = dc->scale;
+    g.drop_seed = dc->seed;
+}
+
 // Row forward: Y = sum_i X_i W_i^T + b (+R); the K loop runs over shards.
 static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void *const *W, const void *b,
-                         const void *const *R, void *const *Y, cudaStream_t st) {
+                         const void *const *R, void *const *Y, cudaStream_t st, const DropCfg *drop = nullptr) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = "row_fwd";
@@ -269,6 +293,7 @@ static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void
     if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
     const void *bb[1] = {b};
     set_bias(g, (d->has_bias && b) ? bb : nullptr, 1, 0);
+    set_drop(g, drop);
     return run_gemm(g, d->dtype, st);
 }
 
@@ -455,8 +480,8 @@ static void set_fp8(GemmPlan &g, int fa, int fb, const float *amax, int slot_a, 
 }
 
 static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W1, const void *const *b1,
-                         const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
-                         void *ws, cudaStream_t st) {
+                         const void *const *W2, const void *b2, const void *const *R, void *const *Y,
+                         void *const *pre, void *const *A, void *ws, cudaStream_t st, const DropCfg *drop) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
@@ -509,7 +534,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {A[i], aq[i], (long long)x.M * x.Fs, AMAX_A, FP8_E4M3};
     TRY(launch_fp8_quantize(segs, n, amax, true, st, a_fused));
-    // row GEMM: Y = sum_i Aq_i W2q_i^T / (s_a s_w2) + b2 (+ X)
+    // row GEMM: Y = sum_i Aq_i W2q_i^T / (s_a s_w2) + b2 (+ R), optionally through dropout
     GemmPlan g;
     g.name = "row_fwd";
     g.kind = EPI_PLAIN;
@@ -521,10 +546,11 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     set_operand(g.A, aq, x.T, x.M, x.Fs, false, 0, 1, 0);
     set_operand(g.B, w2q, x.T, x.H, x.Fs, false, 0, 1, 0);
     set_out(g.out, reinterpret_cast<const void *const *>(Y), x.nx, 0, x.rs, x.H);
-    if (d->residual) set_out(g.aux, X, x.nx, 0, x.rs, x.H);
+    if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
     const void *bb[1] = {b2};
     set_bias(g, d->has_bias ? bb : nullptr, 1, 0);
     set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_A, AMAX_W2);
+    set_drop(g, drop);
     return launch_tc_gemm(g, st);
 }
 
@@ -687,80 +713,27 @@ void tp_mlp_destroy(tp_mlp *h) { delete h; }
 
 size_t tp_mlp_workspace_bytes(const tp_mlp *h) { return h ? mlp_ws_layout(&h->d, nullptr) : 0; }
 
-static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
-                              const void *const *W2, const void *b2, void *const *Y, void *const *pre,
-                              void *const *A, void *workspace, size_t workspace_bytes, bool has_ws, void *stream) {
-    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
-    const tp_mlp_desc *d = &h->d;
-    const Dims x = dims_of(d);
-    TRY(check_array(W1, x.T, "W1"));
-    TRY(check_array(W2, x.T, "W2"));
-    if (d->has_bias) {
-        TRY(check_array(b1, x.T, "b1"));
-        TRY(check_one(b2, "b2"));
-    }
-    if (d->dtype == TP_DT_FP8) {
-        if (!has_ws) return set_error(TP_ERR_ARG, "the FP8 forward needs a workspace: call tp_mlp_fwd_ws");
-        const size_t need = mlp_ws_layout(d, nullptr);
-        if (workspace_bytes < need)
-            return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
-        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
-    }
-    if (x.M == 0) return TP_OK;  // no tokens: activation buffers may be empty (NULL)
-    TRY(check_array(X, x.nx, "X"));
-    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
-    TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
-    if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (d->dtype == TP_DT_FP8) return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, Y, pre, A, workspace, st);
+// MLP forward on validated arguments: Y = R + dropout(MLP(X)) with R and the
+// dropout optional (the plain MLP passes R = X iff residual, no dropout).
+static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const void *const *W1,
+                              const void *const *b1, const void *const *W2, const void *b2, const void *const *R,
+                              void *const *Y, void *const *pre, void *const *A, void *workspace, const DropCfg *drop,
+                              cudaStream_t st) {
+    if (d->dtype == TP_DT_FP8)
+        return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop);
     TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));
-    return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr,
-                   d->residual ? X : nullptr, Y, st);
+    return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr, R, Y, st, drop);
 }
 
-tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
-                     const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
-                     void *stream) {
-    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, nullptr, 0, false, stream);
-}
-
-tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
-                        const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
-                        void *workspace, size_t workspace_bytes, void *stream) {
-    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, workspace, workspace_bytes, true, stream);
-}
-
-tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, const void *const *W1,
-                     const void *const *W2, const void *const *pre, const void *const *A, void *const *dX,
-                     void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *workspace,
-                     size_t workspace_bytes, void *stream) {
-    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
-    const tp_mlp_desc *d = &h->d;
+// MLP backward on validated arguments (workspace checked by the caller).
+static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const void *const *X,
+                              const void *const *W1, const void *const *W2, const void *const *pre,
+                              const void *const *A, void *const *dX, void *const *dW1, void *const *db1,
+                              void *const *dW2, void *db2, void *workspace, cudaStream_t st) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
-    TRY(check_array(W1, x.T, "W1"));
-    TRY(check_array(W2, x.T, "W2"));
-    if (x.M > 0) {  // no tokens: activation buffers may be empty (NULL)
-        TRY(check_array(dY, x.nx, "dY"));
-        TRY(check_array(X, x.nx, "X"));
-        if (d->act != TP_ACT_NONE) TRY(check_array(pre, x.T, "pre"));
-        TRY(check_array(A, x.T, "A"));
-        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.nx, "dX"));
-    }
-    TRY(check_array(reinterpret_cast<const void *const *>(dW1), x.T, "dW1"));
-    TRY(check_array(reinterpret_cast<const void *const *>(dW2), x.T, "dW2"));
-    if (d->has_bias) {
-        TRY(check_array(reinterpret_cast<const void *const *>(db1), x.T, "db1"));
-        TRY(check_one(db2, "db2"));
-    }
     size_t shard_bytes = 0;
-    const size_t need = mlp_ws_layout(d, &shard_bytes);
-    if (workspace_bytes < need)
-        return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
-    if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
-        return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mlp_ws_layout(d, &shard_bytes);
     void *const *db2a = reinterpret_cast<void *const *>(&db2);
     if (x.M == 0) {
         TRY(zero_grads(d, dW1, x.T, sizeof(float) * gw * x.H, d->has_bias ? db1 : nullptr, x.T, sizeof(float) * gw, st));
@@ -788,6 +761,78 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
         TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
+}
+
+static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                              const void *const *W2, const void *b2, void *const *Y, void *const *pre,
+                              void *const *A, void *workspace, size_t workspace_bytes, bool has_ws, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->d;
+    const Dims x = dims_of(d);
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (d->has_bias) {
+        TRY(check_array(b1, x.T, "b1"));
+        TRY(check_one(b2, "b2"));
+    }
+    if (d->dtype == TP_DT_FP8) {
+        if (!has_ws) return set_error(TP_ERR_ARG, "the FP8 forward needs a workspace: call tp_mlp_fwd_ws");
+        const size_t need = mlp_ws_layout(d, nullptr);
+        if (workspace_bytes < need)
+            return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    }
+    if (x.M == 0) return TP_OK;  // no tokens: activation buffers may be empty (NULL)
+    TRY(check_array(X, x.nx, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
+    TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
+    if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
+    return mlp_fwd_core(d, X, W1, b1, W2, b2, d->residual ? X : nullptr, Y, pre, A, workspace, nullptr,
+                        static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                     const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                     void *stream) {
+    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, nullptr, 0, false, stream);
+}
+
+tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
+                        const void *const *W2, const void *b2, void *const *Y, void *const *pre, void *const *A,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    return mlp_fwd_impl(h, X, W1, b1, W2, b2, Y, pre, A, workspace, workspace_bytes, true, stream);
+}
+
+tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, const void *const *W1,
+                     const void *const *W2, const void *const *pre, const void *const *A, void *const *dX,
+                     void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->d;
+    const Dims x = dims_of(d);
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (x.M > 0) {  // no tokens: activation buffers may be empty (NULL)
+        TRY(check_array(dY, x.nx, "dY"));
+        TRY(check_array(X, x.nx, "X"));
+        if (d->act != TP_ACT_NONE) TRY(check_array(pre, x.T, "pre"));
+        TRY(check_array(A, x.T, "A"));
+        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.nx, "dX"));
+    }
+    TRY(check_array(reinterpret_cast<const void *const *>(dW1), x.T, "dW1"));
+    TRY(check_array(reinterpret_cast<const void *const *>(dW2), x.T, "dW2"));
+    if (d->has_bias) {
+        TRY(check_array(reinterpret_cast<const void *const *>(db1), x.T, "db1"));
+        TRY(check_one(db2, "db2"));
+    }
+    const size_t need = mlp_ws_layout(d, nullptr);
+    if (workspace_bytes < need)
+        return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    return mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace,
+                        static_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
@@ -888,6 +933,200 @@ tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, cons
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
     return TP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TransformerLayer MLP sub-block: Y = X + dropout(MLP(LayerNorm(X)))
+// ---------------------------------------------------------------------------
+tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out) {
+    if (!out) return set_error(TP_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (!desc) return set_error(TP_ERR_ARG, "descriptor is NULL");
+    TRY(validate_desc(&desc->mlp));
+    if (desc->mlp.residual)
+        return set_error(TP_ERR_ARG, "mlp.residual must be 0: the sub-block adds X after the dropout");
+    const double p = desc->dropout_p;
+    if (!(p >= 0.0 && p < 1.0)) return set_error(TP_ERR_ARG, "dropout_p=%g outside [0, 1)", p);
+    if (!(desc->ln_eps > 0.0f && desc->ln_eps < 1.0e30f)) return set_error(TP_ERR_ARG, "ln_eps must be positive");
+    const int ln_dtype = desc->mlp.dtype == TP_DT_F32 ? TP_DT_F32 : TP_DT_BF16;
+    if (!ln_supported(desc->mlp.H, ln_dtype))
+        return set_error(TP_ERR_UNSUPPORTED, "LayerNorm width H=%d above %d", desc->mlp.H,
+                         ln_dtype == TP_DT_F32 ? 4096 : 8192);
+    tp_layer *h = new (std::nothrow) tp_layer;
+    if (!h) return set_error(TP_ERR_ARG, "out of host memory");
+    h->d = *desc;
+    h->inner = desc->mlp;
+    // keep iff the draw's top 24 bits >= floor(p * 2^24); kept values scaled by 1/(1-p)
+    h->drop_threshold = static_cast<uint32_t>(p * 16777216.0);
+    h->drop_scale = static_cast<float>(1.0 / (1.0 - p));
+    *out = h;
+    return TP_OK;
+}
+
+void tp_layer_destroy(tp_layer *h) { delete h; }
+
+// Workspace: [MLP workspace | dZ (or the LayerNorm partials) | dXn]
+struct LayerWs {
+    size_t mlp, dz, dxn, end;
+};
+
+static LayerWs layer_ws(const tp_layer *h) {
+    const Dims x = dims_of(&h->inner);
+    const size_t act = align256(static_cast<size_t>(x.M) * x.H * x.es);
+    const size_t part = align256(sizeof(float) * 2 * static_cast<size_t>(ln_bwd_chunks(x.M)) * x.H);
+    LayerWs L;
+    L.mlp = 0;
+    L.dz = align256(mlp_ws_layout(&h->inner, nullptr));
+    L.dxn = L.dz + std::max(act, part);
+    L.end = L.dxn + act;
+    return L;
+}
+
+size_t tp_layer_workspace_bytes(const tp_layer *h) { return h ? layer_ws(h).end : 0; }
+
+static tp_status check_layer_ws(const tp_layer *h, void *ws, size_t bytes) {
+    const size_t need = layer_ws(h).end;
+    if (bytes < need) return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", bytes, need);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    return TP_OK;
+}
+
+// shard pointers into a contiguous [M, H] buffer (1 entry without sequence parallelism)
+static void split_rows(void *base, const Dims &x, void **out) {
+    const size_t shard = static_cast<size_t>(x.rs) * x.H * x.es;
+    for (int j = 0; j < x.nx; ++j) out[j] = static_cast<char *>(base) + j * shard;
+}
+
+static LnPlan ln_plan(const tp_layer *h) {
+    const Dims x = dims_of(&h->inner);
+    LnPlan lp;
+    memset(lp.x, 0, sizeof(lp.x));
+    memset(lp.dy, 0, sizeof(lp.dy));
+    memset(lp.dx, 0, sizeof(lp.dx));
+    lp.M = x.M;
+    lp.H = x.H;
+    lp.rows_split = x.rs;
+    lp.eps = h->d.ln_eps;
+    lp.drop_threshold = h->drop_threshold;
+    lp.drop_scale = h->drop_scale;
+    return lp;
+}
+
+tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, const void *beta,
+                       const void *const *W1, const void *const *b1, const void *const *W2, const void *b2,
+                       uint64_t seed, void *const *Y, void *Xn, float *mean, float *rstd, void *const *pre,
+                       void *const *A, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->inner;
+    const Dims x = dims_of(d);
+    TRY(check_one(gamma, "gamma"));
+    TRY(check_one(beta, "beta"));
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (d->has_bias) {
+        TRY(check_array(b1, x.T, "b1"));
+        TRY(check_one(b2, "b2"));
+    }
+    if (d->dtype == TP_DT_FP8) TRY(check_layer_ws(h, workspace, workspace_bytes));
+    if (x.M == 0) return TP_OK;
+    TRY(check_array(X, x.nx, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
+    TRY(check_one(Xn, "Xn"));
+    TRY(check_one(mean, "mean"));
+    TRY(check_one(rstd, "rstd"));
+    TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
+    if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int ln_dtype = d->dtype == TP_DT_F32 ? TP_DT_F32 : TP_DT_BF16;
+    LnPlan lp = ln_plan(h);
+    for (int j = 0; j < x.nx; ++j) lp.x[j] = X[j];
+    lp.xn = Xn;
+    lp.gamma = gamma;
+    lp.beta = beta;
+    lp.mean = mean;
+    lp.rstd = rstd;
+    TRY(launch_ln_fwd(lp, ln_dtype, st));
+    void *xn[kMaxShards];
+    split_rows(Xn, x, xn);
+    DropCfg dc;
+    dc.on = h->d.dropout_p > 0.0f;
+    dc.threshold = h->drop_threshold;
+    dc.scale = h->drop_scale;
+    dc.seed = seed;
+    return mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st);
+}
+
+tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X, const void *gamma, const void *Xn,
+                       const float *mean, const float *rstd, const void *const *W1, const void *const *W2,
+                       const void *const *pre, const void *const *A, uint64_t seed, void *const *dX, float *dgamma,
+                       float *dbeta, void *const *dW1, void *const *db1, void *const *dW2, void *db2,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const tp_mlp_desc *d = &h->inner;
+    const Dims x = dims_of(d);
+    TRY(check_one(gamma, "gamma"));
+    TRY(check_one(dgamma, "dgamma"));
+    TRY(check_one(dbeta, "dbeta"));
+    TRY(check_array(W1, x.T, "W1"));
+    TRY(check_array(W2, x.T, "W2"));
+    if (x.M > 0) {
+        TRY(check_array(dY, x.nx, "dY"));
+        TRY(check_array(X, x.nx, "X"));
+        TRY(check_one(Xn, "Xn"));
+        TRY(check_one(mean, "mean"));
+        TRY(check_one(rstd, "rstd"));
+        if (d->act != TP_ACT_NONE) TRY(check_array(pre, x.T, "pre"));
+        TRY(check_array(A, x.T, "A"));
+        TRY(check_array(reinterpret_cast<const void *const *>(dX), x.nx, "dX"));
+    }
+    TRY(check_array(reinterpret_cast<const void *const *>(dW1), x.T, "dW1"));
+    TRY(check_array(reinterpret_cast<const void *const *>(dW2), x.T, "dW2"));
+    if (d->has_bias) {
+        TRY(check_array(reinterpret_cast<const void *const *>(db1), x.T, "db1"));
+        TRY(check_one(db2, "db2"));
+    }
+    TRY(check_layer_ws(h, workspace, workspace_bytes));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int ln_dtype = d->dtype == TP_DT_F32 ? TP_DT_F32 : TP_DT_BF16;
+    const LayerWs L = layer_ws(h);
+    char *base = static_cast<char *>(workspace);
+    LnPlan lp = ln_plan(h);
+    lp.gamma = gamma;
+    lp.dgamma = dgamma;
+    lp.dbeta = dbeta;
+    if (x.M == 0) {
+        TRY(mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, base + L.mlp, st));
+        return launch_ln_bwd(lp, ln_dtype, st);
+    }
+    for (int j = 0; j < x.nx; ++j) {
+        lp.x[j] = X[j];
+        lp.dy[j] = dY[j];
+        lp.dx[j] = dX[j];
+    }
+    // dZ = dY * keep / (1 - p) (without dropout the MLP takes dY itself)
+    void *dzs[kMaxShards];
+    const void *dz[kMaxShards];
+    if (h->d.dropout_p > 0.0f) {
+        lp.dz = base + L.dz;
+        lp.drop_seed = seed;
+        TRY(launch_dropout_bwd(lp, ln_dtype, st));
+        split_rows(lp.dz, x, dzs);
+        for (int j = 0; j < x.nx; ++j) dz[j] = dzs[j];
+    } else {
+        for (int j = 0; j < x.nx; ++j) dz[j] = dY[j];
+    }
+    // MLP backward on (dZ, Xn) into dXn
+    void *xn[kMaxShards], *dxn[kMaxShards];
+    split_rows(const_cast<void *>(Xn), x, xn);
+    split_rows(base + L.dxn, x, dxn);
+    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st));
+    // LayerNorm backward plus the residual branch: dX = dY + LN'(dXn); partials reuse the dZ region
+    lp.dxn = base + L.dxn;
+    lp.mean = const_cast<float *>(mean);
+    lp.rstd = const_cast<float *>(rstd);
+    lp.partials = reinterpret_cast<float *>(base + L.dz);
+    return launch_ln_bwd(lp, ln_dtype, st);
 }
 
 tp_status tp_fp8_quantize(const void *const *in, void *const *out, const int64_t *n, int nbuf, int fmt, float *amax,

@@ -32,6 +32,43 @@ __device__ __forceinline__ float fp8_scale(float amax, float fmax) {
     return (amax > 0.0f && amax <= 3.0e38f) ? fmax / amax : 1.0f;
 }
 
+// Philox4x32-10 (Salmon, Moraes, Dror & Shaw, SC 2011): 10 rounds of
+// (c0..c3) <- (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0)),
+// the key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Dropout draws: element e of a [rows, ld] tensor uses word e mod 4 of
+// Philox4x32-10 at counter (e div 4) with key (seed lo, seed hi); it is kept
+// when the word's top 24 bits reach `threshold` = floor(p * 2^24).
+struct DropoutParams {
+    int on;
+    uint32_t threshold;
+    float scale;  // 1 / (1 - p)
+    uint32_t seed_lo, seed_hi;
+    long long ld;  // columns of the whole tensor (element index = row * ld + col)
+};
+
+// keep flags of the 4 elements starting at e (e % 4 == 0), applied to v[0..3]
+__device__ __forceinline__ void dropout4(const DropoutParams &d, long long e, float *v) {
+    const unsigned long long q = static_cast<unsigned long long>(e) >> 2;
+    const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), 0u, 0u),
+                                  d.seed_lo, d.seed_hi);
+    v[0] = (r.x >> 8) >= d.threshold ? v[0] * d.scale : 0.0f;
+    v[1] = (r.y >> 8) >= d.threshold ? v[1] * d.scale : 0.0f;
+    v[2] = (r.z >> 8) >= d.threshold ? v[2] * d.scale : 0.0f;
+    v[3] = (r.w >> 8) >= d.threshold ? v[3] * d.scale : 0.0f;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -73,6 +73,11 @@ struct GemmPlan {
     // col_partials[P][ceil(M/32)][out.ld] (the db1 partials).
     float *amax_out = nullptr;
     float *col_partials = nullptr;
+    // EPI_PLAIN: out = residual + dropout(acc + bias) (TransformerLayer bias-dropout-add)
+    bool dropout = false;
+    uint32_t drop_threshold = 0;
+    float drop_scale = 1.0f;
+    uint64_t drop_seed = 0;
 };
 
 // Column sums over token rows: out_p[c] = sum_m in_p[m, c] for c < N, fp32.
@@ -110,6 +115,33 @@ tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
 // second pass only: out_p[c] = sum_{k < chunks} partials[p][k][c]
 tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st);
+
+// LayerNorm and dropout-backward operands of the TransformerLayer MLP
+// sub-block.  X, dY and dX are token-row tensors in `rows_split`-row shards
+// (0: one buffer); Xn, dXn and dZ are single contiguous [M, H] buffers.
+struct LnPlan {
+    int M = 0, H = 0, rows_split = 0;
+    float eps = 1e-5f;
+    const void *x[kMaxShards];   // X (forward and backward)
+    const void *dy[kMaxShards];  // dY (LayerNorm backward residual term, dropout backward input)
+    void *dx[kMaxShards];        // LayerNorm backward output dX
+    void *xn = nullptr;          // forward output Xn
+    const void *dxn = nullptr;   // backward input: gradient of Xn
+    void *dz = nullptr;          // dropout backward output
+    const void *gamma = nullptr, *beta = nullptr;  // [H], activation dtype
+    float *mean = nullptr, *rstd = nullptr;        // [M]
+    float *partials = nullptr;   // backward: 2 * ln_bwd_chunks(M) * H floats
+    float *dgamma = nullptr, *dbeta = nullptr;     // [H] fp32
+    uint32_t drop_threshold = 0;
+    float drop_scale = 1.0f;
+    uint64_t drop_seed = 0;
+};
+
+int ln_bwd_chunks(int M);
+bool ln_supported(int H, int dtype);  // H within the LayerNorm kernels' row capacity
+tp_status launch_ln_fwd(const LnPlan &p, int dtype, cudaStream_t st);
+tp_status launch_ln_bwd(const LnPlan &p, int dtype, cudaStream_t st);
+tp_status launch_dropout_bwd(const LnPlan &p, int dtype, cudaStream_t st);
 
 // Device status words (per device), the wait limit and the launch counter.
 struct DeviceWords {

@@ -30,6 +30,7 @@ struct Params {
     const float *bias[kMaxShards];
     int bias_p_stride, has_bias, has_out2, has_aux;
     int M, N, P, S, Kseg, kind, act, b_dual_off, accumulate;
+    DropoutParams drop;
 };
 
 // element (mn, k) of an operand for problem pi and K segment s; zero outside
@@ -131,6 +132,14 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
                 }
             } else if (p.kind == EPI_PLAIN) {
                 if (bias) v += bias[n];
+                if (p.drop.on) {
+                    // draw of element (m, n): word (e mod 4) of the Philox block e div 4
+                    const long long e = static_cast<long long>(m) * p.drop.ld + n;
+                    float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    w4[e & 3] = v;
+                    dropout4(p.drop, e & ~3ll, w4);
+                    v = w4[e & 3];
+                }
                 if (p.has_aux) v += out_at(p.aux, pi, m)[n];
                 out_at(p.out, pi, m)[n] = v;
             } else if (p.kind == EPI_DACT) {
@@ -194,6 +203,12 @@ tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
     prm.accumulate = g.accumulate;
+    prm.drop.on = g.dropout ? 1 : 0;
+    prm.drop.threshold = g.drop_threshold;
+    prm.drop.scale = g.drop_scale;
+    prm.drop.seed_lo = static_cast<uint32_t>(g.drop_seed);
+    prm.drop.seed_hi = static_cast<uint32_t>(g.drop_seed >> 32);
+    prm.drop.ld = g.N;
     if (g.M == 0 || g.N == 0 || g.P == 0) return TP_OK;
     dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, g.P);
     launch_begin(g.name, st);

@@ -198,6 +198,12 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
             if (s != TP_OK) return s;
         }
     }
+    prm.drop.on = g.dropout ? 1 : 0;
+    prm.drop.threshold = g.drop_threshold;
+    prm.drop.scale = g.drop_scale;
+    prm.drop.seed_lo = static_cast<uint32_t>(g.drop_seed);
+    prm.drop.seed_hi = static_cast<uint32_t>(g.drop_seed >> 32);
+    prm.drop.ld = g.N;
     prm.amax_out = prm.out_tma ? g.amax_out : nullptr;
     prm.col_partials = prm.out_tma && g.kind == EPI_DACT ? g.col_partials : nullptr;
     prm.partial_ld = static_cast<int>(g.out.ld);

@@ -75,6 +75,7 @@ struct Params {
     int m_tiles, n_tiles, total_tiles, group_m;
     int act, b_dual_off, accumulate;
     uint32_t idesc;                  // tcgen05 instruction descriptor (formats, majors, M, N)
+    DropoutParams drop;              // EPI_PLAIN: out = residual + dropout(acc + bias)
     float *amax_out;                 // bulk-store epilogue: atomic max |bf16 output| (A / dPre), or null
     float *col_partials;             // DACT bulk-store epilogue: per-32-row-block column sums, or null
     int partial_ld;                  //   [P][ceil(M/32)][partial_ld] floats
@@ -554,6 +555,11 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
             pack_bf16x32(v, w);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
         } else if (EPI == EPI_PLAIN) {
+            if (p.drop.on) {
+                const long long e0 = static_cast<long long>(row) * p.drop.ld + col0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dropout4(p.drop, e0 + 4 * k, v + 4 * k);
+            }
             if (p.has_aux) {
                 const __nv_bfloat16 *res = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
 #pragma unroll
@@ -727,6 +733,11 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
                     load_bf16x8(bias + col, b);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) x[j] += b[j];
+                }
+                if (p.drop.on) {
+                    const long long e0 = static_cast<long long>(row) * p.drop.ld + col;
+                    dropout4(p.drop, e0, x);
+                    dropout4(p.drop, e0 + 4, x + 4);
                 }
                 if (res) {
                     float rr[8];

@@ -137,3 +137,76 @@ def test_workspace_sizes(tp):
     L.tp_mlp_destroy(h)
     lay2 = tp.Layout(S=2048, B=4, H=4096, F=16384, T=8, act="none", has_bias=False)
     assert tp.linear_workspace_bytes(lay2) == 0
+
+
+def _layer_create(tp, p=0.1, eps=1e-5, **kw):
+    from tensor_transformer_mlp_shard_gb300.binding import LayerDesc
+    base = dict(S=128, B=2, H=256, F=1024, T=2, act="gelu_tanh", dtype="bf16")
+    base.update(kw)
+    d = LayerDesc(tp.make_desc(**base), p, eps)
+    h = ctypes.c_void_p()
+    s = tp.lib().tp_layer_create(ctypes.byref(d), ctypes.byref(h))
+    ws = 0
+    if s == 0:
+        ws = tp.lib().tp_layer_workspace_bytes(h)
+        tp.lib().tp_layer_destroy(h)
+    return s, ws
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, 0),
+    ({"p": 0.0}, 0),
+    ({"p": 0.999}, 0),
+    ({"p": 1.0}, 1),                      # dropout probability outside [0, 1)
+    ({"p": -0.1}, 1),
+    ({"p": float("nan")}, 1),
+    ({"eps": 0.0}, 1),
+    ({"residual": True}, 1),              # the block adds X itself
+    ({"H": 8192}, 0),
+    ({"H": 8200}, 3),                     # above the LayerNorm kernels' row capacity (bf16)
+    ({"H": 4096, "dtype": "f32"}, 0),
+    ({"H": 4104, "dtype": "f32"}, 3),
+    ({"F": 1000, "T": 3}, 2),             # the MLP's own shape checks still apply
+    ({"dtype": "fp8"}, 0),
+])
+def test_layer_create_validation(tp, kw, expect):
+    assert _layer_create(tp, **kw)[0] == expect
+
+
+def test_layer_workspace_holds_mlp_workspace_dz_and_dxn(tp):
+    s, ws = _layer_create(tp)
+    assert s == 0
+    d = tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh", dtype="bf16")
+    h = ctypes.c_void_p()
+    assert tp.lib().tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    mlp_ws = tp.lib().tp_mlp_workspace_bytes(h)
+    tp.lib().tp_mlp_destroy(h)
+    M, H = 256, 256
+    assert ws >= mlp_ws + 2 * M * H * 2
+    # M = 0: nothing but alignment padding
+    s0, ws0 = _layer_create(tp, S=0)
+    assert s0 == 0 and ws0 <= 4096
+
+
+def test_layer_null_pointers_rejected_before_launch(tp):
+    from tensor_transformer_mlp_shard_gb300.binding import LayerDesc, _arr
+    L = tp.lib()
+    d = LayerDesc(tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh", dtype="bf16"), 0.1, 1e-5)
+    h = ctypes.c_void_p()
+    assert L.tp_layer_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    good = [0x10000 * (i + 1) for i in range(2)]
+    one = _arr(good[:1])
+    # gamma missing
+    assert L.tp_layer_fwd(h, one, None, 0x10000, _arr(good), None, _arr(good), None, 7, one, 0x10000, 0x10000,
+                          0x10000, _arr(good), _arr(good), None, 0, None) == 1
+    assert b"gamma" in L.tp_last_error()
+    # Xn misaligned
+    assert L.tp_layer_fwd(h, one, 0x10000, 0x10000, _arr(good), None, _arr(good), None, 7, one, 0x10008, 0x10000,
+                          0x10000, _arr(good), _arr(good), None, 0, None) == 1
+    assert b"Xn" in L.tp_last_error()
+    # backward: workspace too small
+    assert L.tp_layer_bwd(h, one, one, 0x10000, 0x10000, 0x10000, 0x10000, _arr(good), _arr(good), _arr(good),
+                          _arr(good), 7, one, 0x10000, 0x10000, _arr(good), None, _arr(good), None,
+                          ctypes.c_void_p(0x100000), 16, None) == 1
+    assert b"workspace" in L.tp_last_error()
+    L.tp_layer_destroy(h)

@@ -93,3 +93,31 @@ def test_sub_block_matches_torch_autograd(act):
     assert rel(np.concatenate(gr["dW2"], axis=1), W2t.grad.numpy()) < 1e-12
     assert rel(gr["db2"], b2t.grad.numpy()) < 1e-12
     assert 0 < f["keep"].mean() < 1
+
+
+def test_fp8_sub_block_stays_within_the_fp8_error_of_the_exact_one():
+    """layer_fwd_fp8 / layer_bwd_fp8 differ from the exact sub-block only by
+    the FP8 rounding of the MLP's operands (a few percent of max |ref|), and
+    share its dropout flags and LayerNorm statistics exactly.  Forward bound:
+    E4M3's relative half-step 2^-4 plus margin; backward bound: E5M2's
+    relative half-step 2^-3 (dZ and dPre are E5M2 operands)."""
+    rng = np.random.default_rng(11)
+    M, H, F, T, p, seed = 64, 64, 256, 2, 0.2, 99
+    X = rng.normal(size=(M, H)) * 2 + 0.5
+    gamma, beta = 1 + 0.1 * rng.normal(size=H), 0.05 * rng.normal(size=H)
+    W1s = [0.1 * rng.normal(size=(F // T, H)) for _ in range(T)]
+    b1s = [0.02 * rng.normal(size=F // T) for _ in range(T)]
+    W2s = [0.1 * rng.normal(size=(H, F // T)) for _ in range(T)]
+    b2 = 0.02 * rng.normal(size=H)
+    dY = rng.normal(size=(M, H))
+    e = layer.layer_fwd(X, gamma, beta, W1s, b1s, W2s, b2, "gelu_tanh", p, seed)
+    q = layer.layer_fwd_fp8(X, gamma, beta, W1s, b1s, W2s, b2, "gelu_tanh", p, seed)
+    assert np.array_equal(e["keep"], q["keep"])
+    assert np.array_equal(e["mean"], q["mean"]) and np.array_equal(e["rstd"], q["rstd"])
+    dz = e["Y"] - X
+    assert 0 < np.max(np.abs((q["Y"] - X) - dz)) / np.max(np.abs(dz)) < 0.08
+    ge = layer.layer_bwd(dY, X, gamma, W1s, W2s, e, "gelu_tanh", p)
+    gq = layer.layer_bwd_fp8(dY, X, gamma, "gelu_tanh", p, q)
+    for k in ("dgamma", "dbeta", "db2"):
+        r = np.max(np.abs(gq[k] - ge[k])) / np.max(np.abs(ge[k]))
+        assert r < 0.125, (k, r)
