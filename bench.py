@@ -148,7 +148,25 @@ def kernel_flops(w):
     """Algorithmic FLOP of one launch of each GEMM kernel for workload w."""
     M, H, F, g = w.M, w.H, w.F, w.g
     return {"col_fwd": 2.0 * M * H * F * g, "row_fwd": 2.0 * M * F * H, "row_dgrad_act": 2.0 * M * H * F,
-            "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H}
+            "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H,
+            "fused_mlp_fwd": 2.0 * M * H * F * g + 2.0 * M * F * H}
+
+
+def gemm_bytes(w):
+    """Algorithmic HBM bytes of one launch of each GEMM kernel (bf16 operands
+    and activations, fp32 weight gradients; every operand read once, every
+    output written once) -- with kernel_flops, the arithmetic intensity that
+    decides which roof bounds the kernel."""
+    M, H, F, g = w.M, w.H, w.F, w.g
+    e = 2
+    res = M * H * e if w.residual else 0
+    return {"col_fwd": e * (M * H + g * F * H + M * g * F + M * F),
+            "row_fwd": e * (M * F + H * F + M * H) + res,
+            "row_dgrad_act": e * (M * H + H * F + 2 * M * g * F),
+            "wgrad_row": e * (M * H + M * F) + 4 * H * F,
+            "wgrad_col": e * (M * g * F + M * H) + 4 * g * F * H,
+            "col_dgrad": e * (M * g * F + g * F * H + M * H) + res,
+            "fused_mlp_fwd": e * (M * H + g * F * H + H * F + M * g * F + M * F + M * H) + res}
 
 
 LAYER_DROPOUT_P = 0.1  # Megatron's default hidden dropout
@@ -194,6 +212,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     build.build()
     torch.cuda.set_device(local)
     tp.set_tile_mode(args.tile_mode)
+    tp.set_fused_fwd(args.fused)
     dev = torch.device("cuda", local)
     bf = torch.bfloat16
     T, M, H, F, g = w.T, w.M, w.H, w.F, w.g
@@ -343,16 +362,26 @@ def run_gpu(args, w, dist, rank, local, ws):
     roofline = None
     if dom:
         n, tot = kernels[dom]
-        achieved = kf[dom] / ((tot / n) * 1e-3) / 1e12
+        avg_s = (tot / n) * 1e-3
         peak = peaks["bf16_tflops_sustained"]
         peak_kind = f"bf16 sustained ({peaks['source']})"
         if w.dtype == "fp8":
             # dense fp8 : bf16 tensor rate is 4.5 : 2.25 PFLOP/s nominal
             peak, peak_kind = 2.0 * peak, f"fp8 = 2 x bf16 sustained ({peaks['source']}) x nominal ratio"
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                    "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
-    if roofline is not None and w.dtype == "bf16" and not layer:
+        gb = gemm_bytes(w)[dom]
+        # below the ridge point (peak FLOP/s / peak B/s) the kernel is bound by HBM
+        if kf[dom] / gb < peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
+            achieved = gb / avg_s / 1e9
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                        "peak_kind": f"HBM copy ({peaks['source']})", "algorithmic_bytes_per_launch": gb,
+                        "tflops": round(kf[dom] / avg_s / 1e12, 1)}
+        else:
+            achieved = kf[dom] / avg_s / 1e12
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                        "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
+    if roofline is not None and w.dtype == "bf16" and not layer and roofline["bound"] == "tensor":
         roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
     step_frac = value / ws / (peaks["bf16_tflops_sustained"] * (2.0 if w.dtype == "fp8" else 1.0))
     return {
@@ -447,6 +476,8 @@ def main():
     ap.add_argument("--block", default="mlp", choices=["mlp", "layer"],
                     help="layer: the TransformerLayer MLP sub-block, Y = X + dropout(MLP(LayerNorm(X))), "
                          f"p = {LAYER_DROPOUT_P}")
+    ap.add_argument("--fused", default="auto", choices=["auto", "on", "off"],
+                    help="forward as one fused kernel for narrow MLPs (H <= 256): auto / on / off")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
     args = ap.parse_args()
@@ -465,7 +496,7 @@ def main():
               "S": w.S, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "act": w.act, "global_batch": w.B * ws,
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
               "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
-              "tile_mode": args.tile_mode}
+              "tile_mode": args.tile_mode, "fused_fwd": args.fused}
     if args.block == "layer":
         config["workload"] += f"; TransformerLayer MLP sub-block: LayerNorm -> MLP -> dropout(p={LAYER_DROPOUT_P})" \
                               " + residual"

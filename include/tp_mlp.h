@@ -326,6 +326,22 @@ TP_API tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream);
 typedef enum { TP_TILE_AUTO = 0, TP_TILE_SINGLE = 1, TP_TILE_PAIR = 2 } tp_tile_mode;
 TP_API tp_status tp_set_tile_mode(int mode);
 
+/* Forward of the MLP (and of the sub-block) as one fused kernel, for all
+ * calls made after this one.  The fused kernel keeps a 128-token tile's
+ * output [128 x H] in tensor memory and streams the F dimension through it
+ * in 64-unit chunks: per chunk the column GEMM, bias and activation (pre and
+ * A are still stored for the backward), then A goes from shared memory
+ * straight into the row GEMM, so A is never read back from HBM.  It takes
+ * bf16 with act = none or GeLU-tanh, H a multiple of 64 up to 256 and F/T a
+ * multiple of 64; other problems always use the two-kernel path.
+ * Its parallelism is the token tiles, so TP_FUSED_AUTO (default) uses it for
+ * those problems when M >= 64 x (SM count) (at least half the SMs get a
+ * tile); TP_FUSED_ON uses it for every problem it takes, TP_FUSED_OFF never.
+ * Both paths accumulate every output in fp32 over the same products; the
+ * order of the additions differs.  Returns TP_ERR_ARG for an unknown mode. */
+typedef enum { TP_FUSED_AUTO = 0, TP_FUSED_OFF = 1, TP_FUSED_ON = 2 } tp_fused_mode;
+TP_API tp_status tp_set_fused_fwd(int mode);
+
 /* Number of kernels this library has launched since load. */
 TP_API uint64_t tp_launch_count(void);
 

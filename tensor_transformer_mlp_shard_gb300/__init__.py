@@ -9,6 +9,7 @@ from .binding import (ACT, DTYPE, Layout, TPLayer, TPMLP, TpError, alloc_workspa
                       fp8_quantize,
                       launch_count, lib, library_path, linear_col, linear_col_bwd, linear_row, linear_row_bwd,
                       linear_row_bwd_noalloc,
-                      linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_tile_mode, set_wait_limit_ns,
+                      linear_workspace_bytes, make_desc, prof_collect, prof_enable, set_fused_fwd, set_tile_mode,
+                      set_wait_limit_ns,
                       status_str,
                       sync_status)

@@ -79,6 +79,7 @@ SIGNATURES = {
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
     "tp_launch_count": (ctypes.c_uint64, []),
     "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
+    "tp_set_fused_fwd": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
     "tp_prof_collect": (ctypes.c_int, [ctypes.POINTER(ProfEntry), ctypes.c_int]),
 }
@@ -463,6 +464,16 @@ def set_tile_mode(mode: str):
     """GEMM tiling of the bf16 engine: "auto", "single" (128-row tiles, one
     CTA) or "pair" (256-row tiles on a CTA pair)."""
     _check(lib().tp_set_tile_mode(TILE_MODES[mode]))
+
+
+FUSED_MODES = {"auto": 0, "off": 1, "on": 2}
+
+
+def set_fused_fwd(mode: str):
+    """Forward as one fused kernel for narrow bf16 MLPs (H <= 256): "auto"
+    (when the token tiles fill at least half the GPU), "on" (whenever the
+    shape allows it) or "off" (always the column and row GEMM kernels)."""
+    _check(lib().tp_set_fused_fwd(FUSED_MODES[mode]))
 
 
 def launch_count() -> int:

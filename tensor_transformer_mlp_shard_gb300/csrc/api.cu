@@ -668,7 +668,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             TRY(db1_finalize(d, gw, db1, partials, st));
         else
             TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
-        TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+        if (db2) TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
 }
@@ -721,15 +721,52 @@ static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const 
                               cudaStream_t st) {
     if (d->dtype == TP_DT_FP8)
         return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop);
+    const Dims x = dims_of(d);
+    const int mode = fused_fwd_mode();
+    if (mode != TP_FUSED_OFF && fused_fwd_supported(x.H, x.Fs, d->act, d->dtype) &&
+        (mode == TP_FUSED_ON || x.M >= 64ll * num_sms())) {
+        FusedPlan f;
+        for (int j = 0; j < kMaxShards; ++j) {
+            f.X[j] = j < x.nx ? X[j] : nullptr;
+            f.R[j] = (R && j < x.nx) ? R[j] : nullptr;
+            f.Y[j] = j < x.nx ? Y[j] : nullptr;
+            f.W1[j] = j < x.T ? W1[j] : nullptr;
+            f.b1[j] = (d->has_bias && j < x.T) ? b1[j] : nullptr;
+            f.W2[j] = j < x.T ? W2[j] : nullptr;
+            f.pre[j] = (pre && j < x.T) ? pre[j] : nullptr;
+            f.A[j] = j < x.T ? A[j] : nullptr;
+        }
+        f.b2 = d->has_bias ? b2 : nullptr;
+        f.n_tok = x.nx;
+        f.rows_split = x.rs;
+        f.M = x.M;
+        f.H = x.H;
+        f.Fs = x.Fs;
+        f.T = x.T;
+        f.act = d->act;
+        f.has_bias = d->has_bias != 0;
+        f.has_res = R != nullptr;
+        f.has_pre = pre != nullptr;
+        if (drop && drop->on) {
+            f.dropout = true;
+            f.drop_threshold = drop->threshold;
+            f.drop_scale = drop->scale;
+            f.drop_seed = drop->seed;
+        }
+        return launch_fused_mlp_fwd(f, st);
+    }
     TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));
     return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr, R, Y, st, drop);
 }
 
 // MLP backward on validated arguments (workspace checked by the caller).
+// db2_done: the caller has produced db2 already (the sub-block's dropout
+// backward sums dZ as it writes it).
 static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const void *const *X,
                               const void *const *W1, const void *const *W2, const void *const *pre,
                               const void *const *A, void *const *dX, void *const *dW1, void *const *db1,
-                              void *const *dW2, void *db2, void *workspace, cudaStream_t st) {
+                              void *const *dW2, void *db2, void *workspace, cudaStream_t st,
+                              bool db2_done = false) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     size_t shard_bytes = 0;
@@ -741,8 +778,8 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
                           sizeof(float) * x.H, st);
     }
     if (d->dtype == TP_DT_FP8)
-        return fp8_bwd(d, dY, pre, dX, dW1, d->has_bias ? db1 : nullptr, dW2, d->has_bias ? db2 : nullptr,
-                       workspace, st);
+        return fp8_bwd(d, dY, pre, dX, dW1, d->has_bias ? db1 : nullptr, dW2,
+                       (d->has_bias && !db2_done) ? db2 : nullptr, workspace, st);
     void *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
@@ -758,7 +795,7 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
             TRY(db1_finalize(d, gw, db1, partials, st));
         else
             TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
-        TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+        if (!db2_done) TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
 }
@@ -965,7 +1002,8 @@ tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out) {
 
 void tp_layer_destroy(tp_layer *h) { delete h; }
 
-// Workspace: [MLP workspace | dZ (or the LayerNorm partials) | dXn]
+// Workspace: [MLP workspace | dZ, later the LayerNorm partials | dXn, before
+// that the db2 partials of the dropout backward]
 struct LayerWs {
     size_t mlp, dz, dxn, end;
 };
@@ -973,12 +1011,13 @@ struct LayerWs {
 static LayerWs layer_ws(const tp_layer *h) {
     const Dims x = dims_of(&h->inner);
     const size_t act = align256(static_cast<size_t>(x.M) * x.H * x.es);
-    const size_t part = align256(sizeof(float) * 2 * static_cast<size_t>(ln_bwd_chunks(x.M)) * x.H);
+    const size_t ln_part = align256(sizeof(float) * 2 * static_cast<size_t>(ln_bwd_chunks(x.M)) * x.H);
+    const size_t drop_part = align256(sizeof(float) * static_cast<size_t>(dropout_bwd_chunks(x.M)) * x.H);
     LayerWs L;
     L.mlp = 0;
     L.dz = align256(mlp_ws_layout(&h->inner, nullptr));
-    L.dxn = L.dz + std::max(act, part);
-    L.end = L.dxn + act;
+    L.dxn = L.dz + std::max(act, ln_part);
+    L.end = L.dxn + std::max(act, drop_part);
     return L;
 }
 
@@ -1104,14 +1143,18 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
         lp.dy[j] = dY[j];
         lp.dx[j] = dX[j];
     }
-    // dZ = dY * keep / (1 - p) (without dropout the MLP takes dY itself)
+    // dZ = dY * keep / (1 - p) and db2 = sum_m dZ (without dropout the MLP takes dY itself)
     void *dzs[kMaxShards];
     const void *dz[kMaxShards];
-    if (h->d.dropout_p > 0.0f) {
-        lp.dz = base + L.dz;
-        lp.drop_seed = seed;
-        TRY(launch_dropout_bwd(lp, ln_dtype, st));
-        split_rows(lp.dz, x, dzs);
+    const bool dropout = h->d.dropout_p > 0.0f;
+    if (dropout) {
+        LnPlan dp = lp;
+        dp.dz = base + L.dz;
+        dp.drop_seed = seed;
+        dp.partials = reinterpret_cast<float *>(base + L.dxn);  // free until the MLP writes dXn
+        dp.db2 = d->has_bias ? static_cast<float *>(db2) : nullptr;
+        TRY(launch_dropout_bwd(dp, ln_dtype, st));
+        split_rows(dp.dz, x, dzs);
         for (int j = 0; j < x.nx; ++j) dz[j] = dzs[j];
     } else {
         for (int j = 0; j < x.nx; ++j) dz[j] = dY[j];
@@ -1120,7 +1163,7 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
     void *xn[kMaxShards], *dxn[kMaxShards];
     split_rows(const_cast<void *>(Xn), x, xn);
     split_rows(base + L.dxn, x, dxn);
-    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st));
+    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st, dropout));
     // LayerNorm backward plus the residual branch: dX = dY + LN'(dXn); partials reuse the dZ region
     lp.dxn = base + L.dxn;
     lp.mean = const_cast<float *>(mean);
@@ -1158,6 +1201,13 @@ tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
 }
 
 uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+tp_status tp_set_fused_fwd(int mode) {
+    if (mode != TP_FUSED_AUTO && mode != TP_FUSED_OFF && mode != TP_FUSED_ON)
+        return set_error(TP_ERR_ARG, "unknown fused-forward mode %d", mode);
+    set_fused_fwd_mode(mode);
+    return TP_OK;
+}
 
 tp_status tp_set_tile_mode(int mode) {
     if (mode != TP_TILE_AUTO && mode != TP_TILE_SINGLE && mode != TP_TILE_PAIR)

@@ -1,0 +1,502 @@
+// Fused MLP forward for narrow layers (the FlashFusedMLP idea of Megatron's
+// fusions/ package, "Megatron-LM 源码精读" s2 code map): one persistent
+// kernel per 128-token tile runs
+//   for every shard i and every 64-unit chunk c of shard i:
+//     acc1  = X_tile W1_i[c]^T                    (tcgen05, TMEM, N = 64)
+//     pre   = acc1 + b1_i[c]  -> HBM (kept for the backward)
+//     A     = act(pre)        -> HBM (kept for the backward)
+//                             -> shared memory, 128-byte swizzled K-major
+//     Y    += A W2_i[:, c]^T                      (tcgen05, TMEM, K = 64)
+//   Y = (X +) dropout(Y + b2) -> HBM   (dropout only in the TransformerLayer)
+// so A never makes the round trip HBM -> row GEMM, and the cross-shard sum of
+// the row layer (the forward all-reduce) is the Y accumulation over (i, c).
+// The output tile [128 x H] lives in TMEM next to two 64-column accumulators
+// of the column GEMM, so H <= 256: at wider layers the output row does not
+// fit on chip and the two-kernel path (tc_gemm) runs instead.
+//
+// Warp roles (320 threads): warp 0 issues TMA (the X tile once per token
+// tile, then W1 and W2 boxes in consumption order through an 8-slot ring),
+// warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of chunk
+// c - 1, so that the tensor core works while the epilogue turns chunk c - 1
+// into A), warps 2-9 run the epilogues.  Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "tc_gemm_kernels.cuh"
+
+namespace tpmlp {
+namespace tc {
+tp_status encode_map_ex(CUtensorMap *m, const void *ptr, int rows, int cols, long long ld, int box_inner,
+                        int box_rows, CUtensorMapDataType type, int esize, CUtensorMapSwizzle swz);
+tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows, bool fp8);
+}  // namespace tc
+
+namespace fm {
+using namespace tc;
+
+constexpr int kRows = 128;      // token rows per tile (tcgen05 M)
+constexpr int kChunk = 64;      // hidden units per chunk: column GEMM N, row GEMM K
+constexpr int kMaxH = 256;      // output tile [128 x H] + 2 x 64 accumulator columns <= 512 TMEM columns
+constexpr int kBox = 64 * 128;  // one [64 rows x 64] bf16 box (128-byte rows): 8 KB
+constexpr int kSlots = 8;
+constexpr int kXBytes = kMaxH / 64 * (kRows * 128);  // X tile: H/64 boxes of [128 x 64]
+constexpr int kABytes = kRows * 128;                 // A chunk [128 x 64] bf16
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kOffX = kSlots * kBox;
+constexpr int kOffA = kOffX + kXBytes;
+constexpr int kOffEpi = kOffA + 2 * kABytes;
+constexpr int kOffBar = kOffEpi + kEpiWarps * EPI_STAGE_BYTES;
+constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment slack
+constexpr int kTmemCols = 512;
+constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 320
+
+struct FusedParams {
+    CUtensorMap mapX[kMaxShards];    // X token shards, boxes [128 rows x 64], 128-byte swizzle
+    CUtensorMap mapW1[kMaxShards];   // W1_i [Fs, H], boxes [64 x 64]
+    CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [64 x 64]
+    CUtensorMap mapPre[kMaxShards];  // pre_i [M, Fs], store boxes [32 x 32], 64-byte swizzle
+    CUtensorMap mapA[kMaxShards];    // A_i [M, Fs]
+    CUtensorMap mapY[kMaxShards];    // Y token shards
+    const __nv_bfloat16 *b1[kMaxShards];
+    const __nv_bfloat16 *b2;
+    const __nv_bfloat16 *res[kMaxShards];
+    DropoutParams drop;        // Y = R + dropout(sum + b2) (TransformerLayer bias-dropout-add)
+    int rows_split, n_tok;
+    int M, H, Fs, T, act, has_bias, has_res, has_pre;
+    int m_tiles, cps, nc, kb;  // chunks per shard, chunks per tile (T * cps), H / 64
+    uint32_t idesc;            // bf16 x bf16 -> fp32, both K-major, M = 128, N = 64
+    int *status;
+    unsigned *abort_word;
+    unsigned launch_id;
+    unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, const FusedParams &p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (*reinterpret_cast<volatile unsigned *>(p.abort_word) == p.launch_id) return false;
+            if (global_timer_ns() - t0 > p.wait_limit_ns) {
+                raise_device_error(p.status, p.abort_word, p.launch_id, TP_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// token shard and local row of global row `row0`
+__device__ __forceinline__ void tok_index(const FusedParams &p, int row0, int &j, int &lrow) {
+    j = 0;
+    lrow = row0;
+    if (p.rows_split) {
+        j = min(row0 / p.rows_split, p.n_tok - 1);
+        lrow = row0 - j * p.rows_split;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid_constant__ FusedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 32);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * kSlots;
+    const uint32_t xfull = empty0 + 8 * kSlots, xempty = xfull + 8;
+    const uint32_t accf0 = xempty + 8, acce0 = accf0 + 16;  // column-GEMM accumulator full / drained
+    const uint32_t af0 = acce0 + 16, ae0 = af0 + 16;        // A buffer written / consumed
+    const uint32_t yfull = ae0 + 16, yempty = yfull + 8, drain = yempty + 8;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr uint32_t kEpiThreads = 32 * kEpiWarps;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        mbar_init(xfull, 1);
+        mbar_init(xempty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, kEpiThreads);
+            mbar_init(af0 + 8 * b, kEpiThreads);
+            mbar_init(ae0 + 8 * b, 1);
+        }
+        mbar_init(yfull, 1);
+        mbar_init(yempty, kEpiThreads);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int slot = 0;
+            uint32_t phase = 0, armed = 0, armed_par = 0;
+            bool x_armed = false, ok = true;
+            uint32_t x_par = 0;
+            auto load_box = [&](const CUtensorMap *map, int c0, int c1) -> bool {
+                if (!fwait(empty0 + 8 * slot, phase ^ 1u, p)) return false;
+                const uint32_t fb = full0 + 8 * slot;
+                mbar_arrive_expect_tx(fb, kBox);
+                armed |= 1u << slot;
+                armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
+                tma_load_2d(sbase + slot * kBox, map, fb, c0, c1);
+                if (++slot == kSlots) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+                return true;
+            };
+            int it = 0;
+            for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it) {
+                int tj, tl;
+                tok_index(p, t * kRows, tj, tl);
+                if (!fwait(xempty, (it & 1) ^ 1u, p)) break;
+                mbar_arrive_expect_tx(xfull, p.kb * kRows * 128);
+                x_armed = true;
+                x_par = it & 1;
+                for (int kb = 0; kb < p.kb; ++kb)
+                    tma_load_2d(sbase + kOffX + kb * kRows * 128, &p.mapX[tj], xfull, kb * 64, tl);
+                // boxes in the order the MMA warp consumes them
+                for (int c = 0; ok && c <= p.nc; ++c) {
+                    if (c < p.nc) {
+                        const int i = c / p.cps, u0 = (c % p.cps) * kChunk;
+                        for (int kb = 0; ok && kb < p.kb; ++kb) ok = load_box(&p.mapW1[i], kb * 64, u0);
+                    }
+                    if (ok && c >= 1) {
+                        const int i = (c - 1) / p.cps, u0 = ((c - 1) % p.cps) * kChunk;
+                        for (int g = 0; ok && g < p.kb; ++g) ok = load_box(&p.mapW2[i], u0, g * 64);
+                    }
+                }
+            }
+            // no bulk copy may still be landing in shared memory when the CTA exits
+            for (int i = 0; i < kSlots; ++i)
+                if (armed & (1u << i)) mbar_wait_drain(full0 + 8 * i, (armed_par >> i) & 1u, p.wait_limit_ns);
+            if (x_armed) mbar_wait_drain(xfull, x_par, p.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int slot = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0, cgb = 0;
+            for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it, cgb += p.nc) {
+                for (int c = 0; ok && c <= p.nc; ++c) {
+                    if (c < p.nc) {
+                        // column GEMM of chunk c: acc1[b] = X_tile W1 chunk^T (K = H)
+                        const int cg = cgb + c, b = cg & 1;
+                        const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                        if (!fwait(acce0 + 8 * b, (use & 1u) ^ 1u, p)) {
+                            ok = false;
+                            break;
+                        }
+                        if (c == 0 && !fwait(xfull, it & 1, p)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + kAccCol + kChunk * b;
+                        for (int kb = 0; kb < p.kb; ++kb) {
+                            if (!fwait(full0 + 8 * slot, phase, p)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sx = sbase + kOffX + kb * kRows * 128, sw = sbase + slot * kBox;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_bf16(d, smem_desc(sx + kk * 32, 16, 1024), smem_desc(sw + kk * 32, 16, 1024),
+                                          p.idesc, (kb | kk) ? 1u : 0u);
+                            umma_commit(empty0 + 8 * slot);
+                            if (++slot == kSlots) {
+                                slot = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        umma_commit(accf0 + 8 * b);
+                        if (c == p.nc - 1) umma_commit(xempty);  // the tile's last read of X
+                    }
+                    if (c >= 1) {
+                        // row GEMM of chunk c - 1: Y[:, 64g..] += A W2 chunk^T (K = 64)
+                        const int cg = cgb + c - 1, b = cg & 1;
+                        const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                        if (!fwait(af0 + 8 * b, use & 1u, p)) {
+                            ok = false;
+                            break;
+                        }
+                        if (c == 1 && !fwait(yempty, (it & 1) ^ 1u, p)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = sbase + kOffA + b * kABytes;
+                        for (int g = 0; g < p.kb; ++g) {
+                            if (!fwait(full0 + 8 * slot, phase, p)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sw = sbase + slot * kBox;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_bf16(tmem_base + 64 * g, smem_desc(sa + kk * 32, 16, 1024),
+                                          smem_desc(sw + kk * 32, 16, 1024), p.idesc, (c > 1 || kk > 0) ? 1u : 0u);
+                            umma_commit(empty0 + 8 * slot);
+                            if (++slot == kSlots) {
+                                slot = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        umma_commit(ae0 + 8 * b);
+                    }
+                }
+                if (!ok) break;
+                umma_commit(yfull);
+            }
+            // all issued MMAs complete before TMEM is released
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogues (warps 2..9) ----------------
+        const int q = warp & 3;            // TMEM lane quarter: rows q*32 .. q*32+31 of the tile
+        const int h = (warp - 2) >> 2;     // column half: chunk columns 32h.., output columns 128h..
+        Stager stg{sbase + kOffEpi + (warp - 2) * EPI_STAGE_BYTES, 0u};
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t r_tile = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
+        int it = 0, cgb = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it, cgb += p.nc) {
+            const int row0 = t * kRows + q * 32;
+            const int row = row0 + lane;
+            const bool block_ok = row0 < p.M;  // warp-uniform
+            const bool row_ok = row < p.M;
+            for (int c = 0; c < p.nc; ++c) {
+                const int cg = cgb + c, b = cg & 1;
+                const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                ok = fwait(accf0 + 8 * b, use & 1u, p);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r[32];
+                tmem_ld32(tmem_base + kAccCol + kChunk * b + h * 32 + lane_off, r);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(acce0 + 8 * b);
+                const int i = c / p.cps, u = (c % p.cps) * kChunk + h * 32;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (p.has_bias) {
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        float bb[8];
+                        load_bf16x8(p.b1[i] + u + 8 * g8, bb);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += bb[j];
+                    }
+                }
+                uint4 w[4];
+                if (p.has_pre) {
+                    pack_bf16x32(v, w);
+                    if (block_ok) stage_store(stg, &p.mapPre[i], u, row0, w, lane);
+                }
+                if (p.act == TP_ACT_GELU_TANH) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
+                }
+                pack_bf16x32(v, w);
+                if (block_ok) stage_store(stg, &p.mapA[i], u, row0, w, lane);
+                // A into the row GEMM's operand buffer: row r_tile, 16-byte chunks
+                // 4h..4h+3 of its 128-byte line, 128-byte swizzle (chunk ^ (row & 7))
+                ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rowa = sbase + kOffA + b * kABytes + r_tile * 128u;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    st_shared_v4(rowa + ((static_cast<uint32_t>(4 * h + jj) ^ (r_tile & 7u)) << 4), w[jj]);
+                fence_async_smem();
+                mbar_arrive(af0 + 8 * b);
+            }
+            if (!ok) break;
+            ok = fwait(yfull, it & 1, p);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            int tj, tl;
+            tok_index(p, row0, tj, tl);
+            for (int cb = 0; cb < 4; ++cb) {
+                const int col = h * 128 + cb * 32;
+                if (col >= p.H) break;
+                uint32_t r[32];
+                tmem_ld32(tmem_base + col + lane_off, r);
+                tmem_ld_wait();
+                if (!block_ok) continue;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (p.has_bias) {
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        float bb[8];
+                        load_bf16x8(p.b2 + col + 8 * g8, bb);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += bb[j];
+                    }
+                }
+                if (p.drop.on) {
+                    const long long e0 = static_cast<long long>(row) * p.H + col;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dropout4(p.drop, e0 + 4 * k, v + 4 * k);
+                }
+                if (p.has_res) {
+                    const __nv_bfloat16 *res =
+                        p.res[tj] + static_cast<long long>(row_ok ? tl + lane : tl) * p.H + col;
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        float rr[8];
+                        load_bf16x8_guarded(res + 8 * g8, row_ok, rr);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += rr[j];
+                    }
+                }
+                uint4 w[4];
+                pack_bf16x32(v, w);
+                stage_store(stg, &p.mapY[tj], col, tl, w, lane);
+            }
+            tc_fence_before();
+            mbar_arrive(yempty);
+        }
+        if (lane == 0) bulk_wait<0>();  // bulk stores done before the CTA leaves
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace fm
+
+static std::atomic<int> g_fused_mode{TP_FUSED_AUTO};
+void set_fused_fwd_mode(int mode) { g_fused_mode.store(mode); }
+int fused_fwd_mode() { return g_fused_mode.load(); }
+
+bool fused_fwd_supported(int H, int Fs, int act, int dtype) {
+    return dtype == TP_DT_BF16 && act != TP_ACT_SWIGLU && H >= 64 && H <= fm::kMaxH && H % 64 == 0 && Fs >= 64 &&
+           Fs % 64 == 0;
+}
+
+tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
+    using namespace fm;
+    if (f.M == 0) return TP_OK;
+    if (f.T < 1 || f.T > kMaxShards || f.n_tok < 1 || f.n_tok > kMaxShards)
+        return set_error(TP_ERR_ARG, "fused forward: bad shard counts");
+    if (!fused_fwd_supported(f.H, f.Fs, f.act, TP_DT_BF16))
+        return set_error(TP_ERR_UNSUPPORTED, "fused forward: H=%d, F/T=%d, act=%d outside its shapes", f.H, f.Fs,
+                         f.act);
+    FusedParams prm;
+    memset(&prm, 0, sizeof(prm));
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int tok_rows = f.rows_split ? f.rows_split : f.M;
+    for (int j = 0; j < f.n_tok; ++j) {
+        tp_status s = tc::encode_map(&prm.mapX[j], f.X[j], tok_rows, f.H, 64, kRows, false);
+        if (s == TP_OK)
+            s = tc::encode_map_ex(&prm.mapY[j], f.Y[j], tok_rows, f.H, f.H, 32, 32, bf, 2, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (s != TP_OK) return s;
+        prm.res[j] = f.has_res ? static_cast<const __nv_bfloat16 *>(f.R[j]) : nullptr;
+    }
+    for (int i = 0; i < f.T; ++i) {
+        tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, 64, false);
+        if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 64, false);
+        if (s == TP_OK)
+            s = tc::encode_map_ex(&prm.mapA[i], f.A[i], f.M, f.Fs, f.Fs, 32, 32, bf, 2, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (s == TP_OK && f.has_pre)
+            s = tc::encode_map_ex(&prm.mapPre[i], f.pre[i], f.M, f.Fs, f.Fs, 32, 32, bf, 2,
+                                  CU_TENSOR_MAP_SWIZZLE_64B);
+        if (s != TP_OK) return s;
+        prm.b1[i] = f.has_bias ? static_cast<const __nv_bfloat16 *>(f.b1[i]) : nullptr;
+    }
+    prm.b2 = f.has_bias ? static_cast<const __nv_bfloat16 *>(f.b2) : nullptr;
+    prm.drop.on = f.dropout ? 1 : 0;
+    prm.drop.threshold = f.drop_threshold;
+    prm.drop.scale = f.drop_scale;
+    prm.drop.seed_lo = static_cast<uint32_t>(f.drop_seed);
+    prm.drop.seed_hi = static_cast<uint32_t>(f.drop_seed >> 32);
+    prm.drop.ld = f.H;
+    prm.rows_split = f.rows_split;
+    prm.n_tok = f.n_tok;
+    prm.M = f.M;
+    prm.H = f.H;
+    prm.Fs = f.Fs;
+    prm.T = f.T;
+    prm.act = f.act;
+    prm.has_bias = f.has_bias ? 1 : 0;
+    prm.has_res = f.has_res ? 1 : 0;
+    prm.has_pre = f.has_pre ? 1 : 0;
+    prm.m_tiles = (f.M + kRows - 1) / kRows;
+    prm.cps = f.Fs / kChunk;
+    prm.nc = f.T * prm.cps;
+    prm.kb = f.H / 64;
+    // fp32 accumulator (bit 4), bf16 A and B (bits 7-9, 10-12), both K-major,
+    // N/8 at bit 17, M/16 at bit 24
+    prm.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kChunk >> 3) << 17) | (uint32_t(kRows >> 4) << 24);
+    DeviceWords w;
+    tp_status s = device_words(&w);
+    if (s != TP_OK) return s;
+    prm.status = w.status;
+    prm.abort_word = w.abort_word;
+    prm.launch_id = next_launch_id();
+    prm.wait_limit_ns = wait_limit_ns();
+
+    // opt in to > 48 KB of dynamic shared memory, once per device
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev % 64]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(fused_mlp_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(fused_mlp_fwd)");
+            attr_set[dev % 64] = true;
+        }
+    }
+    const int grid = prm.m_tiles < num_sms() ? prm.m_tiles : num_sms();
+    launch_begin("fused_mlp_fwd", st);
+    fused_mlp_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end("fused_mlp_fwd", st);
+    return cuda_check(e, "fused_mlp_fwd");
+}
+
+}  // namespace tpmlp

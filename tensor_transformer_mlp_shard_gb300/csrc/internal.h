@@ -116,6 +116,32 @@ tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
 // second pass only: out_p[c] = sum_{k < chunks} partials[p][k][c]
 tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st);
 
+// Fused MLP forward (one kernel for the column GEMM, the activation and the
+// row GEMM; A passes through shared memory on its way to the row GEMM).
+// Pointer arrays as in the MLP entry points: X, R, Y have n_tok token shards
+// of rows_split rows (n_tok = 1, rows_split = 0 without sequence
+// parallelism); W1, b1, W2, pre, A have T entries.
+struct FusedPlan {
+    const void *X[kMaxShards];
+    const void *R[kMaxShards];  // residual (null entries: none)
+    void *Y[kMaxShards];
+    const void *W1[kMaxShards], *b1[kMaxShards], *W2[kMaxShards];
+    const void *b2 = nullptr;
+    void *pre[kMaxShards];      // null entries: not stored (act = none)
+    void *A[kMaxShards];
+    int n_tok = 1, rows_split = 0;
+    int M = 0, H = 0, Fs = 0, T = 1, act = TP_ACT_NONE;
+    bool has_bias = false, has_res = false, has_pre = false;
+    bool dropout = false;  // as GemmPlan's dropout of the row forward
+    uint32_t drop_threshold = 0;
+    float drop_scale = 1.0f;
+    uint64_t drop_seed = 0;
+};
+void set_fused_fwd_mode(int mode);  // TP_FUSED_*
+int fused_fwd_mode();
+bool fused_fwd_supported(int H, int Fs, int act, int dtype);  // shapes the fused kernel takes
+tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st);
+
 // LayerNorm and dropout-backward operands of the TransformerLayer MLP
 // sub-block.  X, dY and dX are token-row tensors in `rows_split`-row shards
 // (0: one buffer); Xn, dXn and dZ are single contiguous [M, H] buffers.
@@ -130,14 +156,17 @@ struct LnPlan {
     void *dz = nullptr;          // dropout backward output
     const void *gamma = nullptr, *beta = nullptr;  // [H], activation dtype
     float *mean = nullptr, *rstd = nullptr;        // [M]
-    float *partials = nullptr;   // backward: 2 * ln_bwd_chunks(M) * H floats
+    float *partials = nullptr;   // LayerNorm backward: 2 * ln_bwd_chunks(M) * H floats (at most);
+                                 // dropout backward: dropout_bwd_chunks(M) * H floats
     float *dgamma = nullptr, *dbeta = nullptr;     // [H] fp32
+    float *db2 = nullptr;        // dropout backward: sum_m dZ ([H] fp32), or null
     uint32_t drop_threshold = 0;
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
 };
 
-int ln_bwd_chunks(int M);
+int ln_bwd_chunks(int M);  // upper bound on the LayerNorm backward's blocks
+int dropout_bwd_chunks(int M);
 bool ln_supported(int H, int dtype);  // H within the LayerNorm kernels' row capacity
 tp_status launch_ln_fwd(const LnPlan &p, int dtype, cudaStream_t st);
 tp_status launch_ln_bwd(const LnPlan &p, int dtype, cudaStream_t st);

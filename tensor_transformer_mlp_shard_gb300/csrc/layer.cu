@@ -2,8 +2,10 @@
 // Core walk-through, s03: LayerNorm -> MLP -> bias/dropout/residual add):
 // LayerNorm forward and backward and the dropout backward.  All three are HBM
 // bound: one pass over their [M, H] operands with 16-byte vector accesses,
-// one token row per block (the forward) or kLnBwdRows rows per block (the
-// backward, which also emits one row of dgamma/dbeta partial sums).
+// one token row per block (the forward), a run of rows per block (the
+// backward, which also emits one row of dgamma/dbeta partial sums) or a
+// kDropRows-row column strip per block (the dropout backward, which emits
+// one row of db2 partial sums).
 // Sequence-parallel tensors (X, dY, dX) are addressed through the token shard
 // holding the row.
 #include <cuda_runtime.h>
@@ -15,18 +17,26 @@ namespace tpmlp {
 
 constexpr int kLnThreads = 256;
 constexpr int kLnMaxVpt = 4;    // 16-byte vectors per thread and row: H <= 8192 (bf16), 4096 (fp32)
-constexpr int kLnBwdRows = 16;  // rows per backward block
+constexpr int kLnBwdMinRows = 8;  // fewest rows per backward block (bounds the partials)
 
 template <typename T>
 struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
-    __device__ static void load(const __nv_bfloat16 *p, float *v) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(p);
+    using Raw = uint4;
+    __device__ static Raw load_raw(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint4 *>(p); }
+    __device__ static void unpack(const Raw &w, float *v) {
         v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
         v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
     }
+    __device__ static Raw pack(const float *v) {
+        Raw w;
+        w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
+        w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
+        return w;
+    }
+    __device__ static float first(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
     __device__ static void store(__nv_bfloat16 *p, const float *v) {
         uint4 w;
         w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
@@ -37,10 +47,11 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
     static constexpr int N = 4;
-    __device__ static void load(const float *p, float *v) {
-        const float4 w = *reinterpret_cast<const float4 *>(p);
-        v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
-    }
+    using Raw = float4;
+    __device__ static Raw load_raw(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    __device__ static void unpack(const Raw &w, float *v) { v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w; }
+    __device__ static Raw pack(const float *v) { return make_float4(v[0], v[1], v[2], v[3]); }
+    __device__ static float first(const float *p) { return *p; }
     __device__ static void store(float *p, const float *v) {
         *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
     }
@@ -78,8 +89,11 @@ __device__ __forceinline__ float2 block_sum2(float a, float b) {
 }
 
 // ---------------------------------------------------------------------------
-// LayerNorm forward, one block per token row: mean and population variance in
-// fp32 from two passes over the row held in registers, rstd = 1/sqrt(var+eps),
+// LayerNorm forward, one block per token row.  The row, gamma and beta are
+// loaded up front; the statistics come from one block reduction of the
+// shifted sums S1 = sum(x - k), S2 = sum((x - k)^2) with k = x[0] (so that a
+// large row mean does not cancel digits): mean = k + S1/H,
+// var = S2/H - (S1/H)^2 (population variance), rstd = 1/sqrt(var + eps),
 // Xn = (x - mean) * rstd * gamma + beta.
 // ---------------------------------------------------------------------------
 template <typename T, int VPT>
@@ -91,41 +105,48 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __grid_constan
     const T *x = static_cast<const T *>(p.x[j0]) + off;
     T *y = static_cast<T *>(p.xn) + static_cast<long long>(row) * p.H;
     const int nv = p.H / V::N;
-    float xv[VPT][V::N];
-    float s = 0.0f;
+    typename V::Raw rx[VPT], rg[VPT], rb[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int i = threadIdx.x + k * kLnThreads;
         if (i < nv) {
-            V::load(x + i * V::N, xv[k]);
-#pragma unroll
-            for (int j = 0; j < V::N; ++j) s += xv[k][j];
+            rx[k] = V::load_raw(x + i * V::N);
+            rg[k] = V::load_raw(static_cast<const T *>(p.gamma) + i * V::N);
+            rb[k] = V::load_raw(static_cast<const T *>(p.beta) + i * V::N);
         }
     }
-    const float mean = block_sum2(s, 0.0f).x / p.H;
-    float q = 0.0f;
+    const float shift = V::first(x);
+    float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int i = threadIdx.x + k * kLnThreads;
         if (i < nv) {
+            float v[V::N];
+            V::unpack(rx[k], v);
 #pragma unroll
             for (int j = 0; j < V::N; ++j) {
-                const float d = xv[k][j] - mean;
-                q += d * d;
+                const float d = v[j] - shift;
+                s1 += d;
+                s2 = fmaf(d, d, s2);
             }
         }
     }
-    const float rstd = 1.0f / sqrtf(block_sum2(q, 0.0f).x / p.H + p.eps);
+    const float2 s = block_sum2(s1, s2);
+    const float m1 = s.x / p.H;
+    const float mean = shift + m1;
+    const float var = fmaxf(s.y / p.H - m1 * m1, 0.0f);
+    const float rstd = 1.0f / sqrtf(var + p.eps);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int i = threadIdx.x + k * kLnThreads;
         if (i < nv) {
-            float g[V::N], b[V::N], o[V::N];
-            V::load(static_cast<const T *>(p.gamma) + i * V::N, g);
-            V::load(static_cast<const T *>(p.beta) + i * V::N, b);
+            float v[V::N], g[V::N], b[V::N];
+            V::unpack(rx[k], v);
+            V::unpack(rg[k], g);
+            V::unpack(rb[k], b);
 #pragma unroll
-            for (int j = 0; j < V::N; ++j) o[j] = (xv[k][j] - mean) * rstd * g[j] + b[j];
-            V::store(y + i * V::N, o);
+            for (int j = 0; j < V::N; ++j) v[j] = (v[j] - mean) * rstd * g[j] + b[j];
+            V::store(y + i * V::N, v);
         }
     }
     if (threadIdx.x == 0) {
@@ -134,70 +155,171 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __grid_constan
     }
 }
 
+// The same LayerNorm forward with one warp per token row (rows of up to
+// 32 * VPW vectors): no block barrier, and a block keeps 8 rows in flight.
+template <typename T, int VPW>
+__global__ void __launch_bounds__(kLnThreads) ln_fwd_warp_kernel(const __grid_constant__ LnPlan p) {
+    using V = Vec<T>;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kLnThreads / 32) + (threadIdx.x >> 5);
+    if (row >= p.M) return;  // whole warps leave; no block barrier follows
+    int j0;
+    const long long off = shard_offset(p.rows_split, row, p.H, &j0);
+    const T *x = static_cast<const T *>(p.x[j0]) + off;
+    T *y = static_cast<T *>(p.xn) + static_cast<long long>(row) * p.H;
+    const int nv = p.H / V::N;
+    typename V::Raw rx[VPW];
+#pragma unroll
+    for (int k = 0; k < VPW; ++k) {
+        const int i = lane + 32 * k;
+        if (i < nv) rx[k] = V::load_raw(x + i * V::N);
+    }
+    const float shift = V::first(x);
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPW; ++k) {
+        const int i = lane + 32 * k;
+        if (i < nv) {
+            float v[V::N];
+            V::unpack(rx[k], v);
+#pragma unroll
+            for (int j = 0; j < V::N; ++j) {
+                const float d = v[j] - shift;
+                s1 += d;
+                s2 = fmaf(d, d, s2);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    const float m1 = s1 / p.H;
+    const float mean = shift + m1;
+    const float var = fmaxf(s2 / p.H - m1 * m1, 0.0f);
+    const float rstd = 1.0f / sqrtf(var + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPW; ++k) {
+        const int i = lane + 32 * k;
+        if (i < nv) {
+            float v[V::N], g[V::N], b[V::N];
+            V::unpack(rx[k], v);
+            V::unpack(V::load_raw(static_cast<const T *>(p.gamma) + i * V::N), g);
+            V::unpack(V::load_raw(static_cast<const T *>(p.beta) + i * V::N), b);
+#pragma unroll
+            for (int j = 0; j < V::N; ++j) v[j] = (v[j] - mean) * rstd * g[j] + b[j];
+            V::store(y + i * V::N, v);
+        }
+    }
+    if (lane == 0) {
+        p.mean[row] = mean;
+        p.rstd[row] = rstd;
+    }
+}
+
 // ---------------------------------------------------------------------------
-// LayerNorm backward over kLnBwdRows token rows per block.  With
+// LayerNorm backward over `rows` token rows per block (chosen so that the
+// grid is one wave of resident blocks).  With
 // g = dXn * gamma and xhat = (x - mean) * rstd:
 //   dX = dY + rstd * (g - mean_h(g) - xhat * mean_h(g * xhat))
 // (dY: the residual branch of the sub-block), and the block's partial column
 // sums of dXn * xhat (dgamma) and dXn (dbeta) into
-// partials[0][blockIdx.x][:] and partials[1][blockIdx.x][:].
+// partials[0][blockIdx.x][:] and partials[1][blockIdx.x][:].  The loads of
+// row r + 1 (x, dXn, dY, kept as raw 16-byte vectors) are issued before row
+// r is reduced, so that every thread has two rows of loads in flight.
 // ---------------------------------------------------------------------------
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(const __grid_constant__ LnPlan p) {
+struct LnRowRaw {
+    typename Vec<T>::Raw x[VPT], d[VPT], r[VPT];
+    float mean, rstd;
+};
+
+template <typename T, int VPT>
+__device__ __forceinline__ void ln_bwd_load(const LnPlan &p, int row, int nv, LnRowRaw<T, VPT> &o) {
+    using V = Vec<T>;
+    int js;
+    const long long off = shard_offset(p.rows_split, row, p.H, &js);
+    const T *x = static_cast<const T *>(p.x[js]) + off;
+    const T *dy = static_cast<const T *>(p.dy[js]) + off;
+    const T *dxn = static_cast<const T *>(p.dxn) + static_cast<long long>(row) * p.H;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int i = threadIdx.x + k * kLnThreads;
+        if (i < nv) {
+            o.x[k] = V::load_raw(x + i * V::N);
+            o.d[k] = V::load_raw(dxn + i * V::N);
+            o.r[k] = V::load_raw(dy + i * V::N);
+        }
+    }
+    o.mean = p.mean[row];
+    o.rstd = p.rstd[row];
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(const __grid_constant__ LnPlan p, int rows) {
     using V = Vec<T>;
     const int nv = p.H / V::N;
-    float gm[VPT][V::N], pg[VPT][V::N], pb[VPT][V::N];
+    typename V::Raw rgm[VPT];
+    float pg[VPT][V::N], pb[VPT][V::N];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int i = threadIdx.x + k * kLnThreads;
 #pragma unroll
-        for (int j = 0; j < V::N; ++j) pg[k][j] = pb[k][j] = gm[k][j] = 0.0f;
-        if (i < nv) V::load(static_cast<const T *>(p.gamma) + i * V::N, gm[k]);
+        for (int j = 0; j < V::N; ++j) pg[k][j] = pb[k][j] = 0.0f;
+        if (i < nv) rgm[k] = V::load_raw(static_cast<const T *>(p.gamma) + i * V::N);
     }
-    const int r0 = blockIdx.x * kLnBwdRows;
-    const int r1 = min(p.M, r0 + kLnBwdRows);
+    const int r0 = blockIdx.x * rows;
+    const int r1 = min(p.M, r0 + rows);
+    LnRowRaw<T, VPT> cur, nxt;
+    ln_bwd_load<T, VPT>(p, r0, nv, cur);
 #pragma unroll 1
     for (int row = r0; row < r1; ++row) {
-        int js;
-        const long long off = shard_offset(p.rows_split, row, p.H, &js);
-        const T *x = static_cast<const T *>(p.x[js]) + off;
-        const T *dy = static_cast<const T *>(p.dy[js]) + off;
-        T *dx = static_cast<T *>(p.dx[js]) + off;
-        const T *dxn = static_cast<const T *>(p.dxn) + static_cast<long long>(row) * p.H;
-        const float mean = p.mean[row], rstd = p.rstd[row];
-        float xh[VPT][V::N], g[VPT][V::N];
+        if (row + 1 < r1) ln_bwd_load<T, VPT>(p, row + 1, nv, nxt);
+        const float mean = cur.mean, rstd = cur.rstd;
         float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int i = threadIdx.x + k * kLnThreads;
             if (i < nv) {
-                float xv[V::N], d[V::N];
-                V::load(x + i * V::N, xv);
-                V::load(dxn + i * V::N, d);
+                float xv[V::N], d[V::N], gm[V::N];
+                V::unpack(cur.x[k], xv);
+                V::unpack(cur.d[k], d);
+                V::unpack(rgm[k], gm);
 #pragma unroll
                 for (int j = 0; j < V::N; ++j) {
-                    xh[k][j] = (xv[j] - mean) * rstd;
-                    g[k][j] = d[j] * gm[k][j];
-                    s1 += g[k][j];
-                    s2 += g[k][j] * xh[k][j];
-                    pg[k][j] += d[j] * xh[k][j];
+                    const float xh = (xv[j] - mean) * rstd;
+                    const float g = d[j] * gm[j];
+                    s1 += g;
+                    s2 = fmaf(g, xh, s2);
+                    pg[k][j] = fmaf(d[j], xh, pg[k][j]);
                     pb[k][j] += d[j];
                 }
             }
         }
         const float2 s = block_sum2(s1, s2);
         const float mg = s.x / p.H, mgx = s.y / p.H;
+        int js;
+        const long long off = shard_offset(p.rows_split, row, p.H, &js);
+        T *dx = static_cast<T *>(p.dx[js]) + off;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int i = threadIdx.x + k * kLnThreads;
             if (i < nv) {
-                float r[V::N], o[V::N];
-                V::load(dy + i * V::N, r);
+                float xv[V::N], d[V::N], gm[V::N], o[V::N];
+                V::unpack(cur.x[k], xv);
+                V::unpack(cur.d[k], d);
+                V::unpack(rgm[k], gm);
+                V::unpack(cur.r[k], o);
 #pragma unroll
-                for (int j = 0; j < V::N; ++j) o[j] = r[j] + rstd * (g[k][j] - mg - xh[k][j] * mgx);
+                for (int j = 0; j < V::N; ++j) {
+                    const float xh = (xv[j] - mean) * rstd;
+                    o[j] += rstd * (d[j] * gm[j] - mg - xh * mgx);
+                }
                 V::store(dx + i * V::N, o);
             }
         }
+        cur = nxt;
     }
     const long long chunks = gridDim.x;
 #pragma unroll
@@ -215,10 +337,22 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(const __grid_constan
     }
 }
 
-// Dropout backward: dZ = dY * keep / (1 - p), the keep flags redrawn from the
-// forward's Philox stream (element m*H + h); dY token-sharded, dZ contiguous.
+// ---------------------------------------------------------------------------
+// Dropout backward fused with the column sums of its output:
+//   dZ = dY * keep / (1 - p)   (keep flags redrawn from the forward's Philox
+//                               stream, element m*H + h),
+//   partials[blockIdx.y][c] = sum over the block's kDropRows rows of dZ[:, c]
+// (db2 = the sum of the partial rows).  A block covers kDropRows token rows
+// and 8 * kDropThreads (bf16) or 4 * kDropThreads (fp32) columns; each thread
+// walks its column vector down the rows with kDropUnroll loads in flight.
+// dY is token-sharded, dZ contiguous.
+// ---------------------------------------------------------------------------
+constexpr int kDropThreads = 128;
+constexpr int kDropRows = 32;
+constexpr int kDropUnroll = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(256) dropout_bwd_kernel(const __grid_constant__ LnPlan p) {
+__global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_constant__ LnPlan p) {
     using V = Vec<T>;
     DropoutParams d;
     d.on = 1;
@@ -227,27 +361,51 @@ __global__ void __launch_bounds__(256) dropout_bwd_kernel(const __grid_constant_
     d.seed_lo = static_cast<uint32_t>(p.drop_seed);
     d.seed_hi = static_cast<uint32_t>(p.drop_seed >> 32);
     d.ld = p.H;
-    const int vpr = p.H / V::N;  // vectors per row
-    const long long nv = static_cast<long long>(p.M) * vpr;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nv;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int row = static_cast<int>(i / vpr);
-        const int col = static_cast<int>(i - static_cast<long long>(row) * vpr) * V::N;
-        int js;
-        const long long off = shard_offset(p.rows_split, row, p.H, &js);
-        float v[V::N];
-        V::load(static_cast<const T *>(p.dy[js]) + off + col, v);
-        const long long e = static_cast<long long>(row) * p.H + col;
+    const int col = (blockIdx.x * kDropThreads + threadIdx.x) * V::N;
+    if (col >= p.H) return;
+    const int r0 = blockIdx.y * kDropRows;
+    const int r1 = min(p.M, r0 + kDropRows);
+    float acc[V::N];
 #pragma unroll
-        for (int j = 0; j < V::N; j += 4) dropout4(d, e + j, v + j);
-        V::store(static_cast<T *>(p.dz) + e, v);
+    for (int j = 0; j < V::N; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+    for (int rb = r0; rb < r1; rb += kDropUnroll) {
+        typename V::Raw raw[kDropUnroll];
+#pragma unroll
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int row = rb + u;
+            if (row < r1) {
+                int js;
+                const long long off = shard_offset(p.rows_split, row, p.H, &js);
+                raw[u] = V::load_raw(static_cast<const T *>(p.dy[js]) + off + col);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int row = rb + u;
+            if (row < r1) {
+                float v[V::N];
+                V::unpack(raw[u], v);
+                const long long e = static_cast<long long>(row) * p.H + col;
+#pragma unroll
+                for (int j = 0; j < V::N; j += 4) dropout4(d, e + j, v + j);
+                V::store(static_cast<T *>(p.dz) + e, v);
+                // the column sums take the stored (rounded) values: db2 = sum_m dZ as the MLP sees it
+                V::unpack(V::pack(v), v);
+#pragma unroll
+                for (int j = 0; j < V::N; ++j) acc[j] += v[j];
+            }
+        }
     }
+    float *out = p.partials + static_cast<long long>(blockIdx.y) * p.H + col;
+#pragma unroll
+    for (int j = 0; j < V::N; j += 4) *reinterpret_cast<float4 *>(out + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-int ln_bwd_chunks(int M) { return M <= 0 ? 1 : (M + kLnBwdRows - 1) / kLnBwdRows; }
+int ln_bwd_chunks(int M) { return M <= 0 ? 1 : (M + kLnBwdMinRows - 1) / kLnBwdMinRows; }
 
 static int ln_vpt(int H, int dtype) {
     const int nv = H / (dtype == TP_DT_F32 ? 4 : 8);
@@ -258,24 +416,55 @@ static int ln_vpt(int H, int dtype) {
 
 bool ln_supported(int H, int dtype) { return H % (dtype == TP_DT_F32 ? 4 : 8) == 0 && ln_vpt(H, dtype) > 0; }
 
+constexpr int kLnWarpMaxVpw = 16;  // warp-per-row forward up to 512 vectors per row
+
 template <typename T>
 static void ln_fwd_dispatch(const LnPlan &p, int vpt, cudaStream_t st) {
-    if (vpt == 1)
-        ln_fwd_kernel<T, 1><<<p.M, kLnThreads, 0, st>>>(p);
-    else if (vpt == 2)
-        ln_fwd_kernel<T, 2><<<p.M, kLnThreads, 0, st>>>(p);
-    else
-        ln_fwd_kernel<T, 4><<<p.M, kLnThreads, 0, st>>>(p);
+    const int nv = p.H / Vec<T>::N;
+    if (nv <= 32 * kLnWarpMaxVpw) {
+        const int grid = (p.M + kLnThreads / 32 - 1) / (kLnThreads / 32);
+        if (nv <= 32)
+            ln_fwd_warp_kernel<T, 1><<<grid, kLnThreads, 0, st>>>(p);
+        else if (nv <= 64)
+            ln_fwd_warp_kernel<T, 2><<<grid, kLnThreads, 0, st>>>(p);
+        else if (nv <= 128)
+            ln_fwd_warp_kernel<T, 4><<<grid, kLnThreads, 0, st>>>(p);
+        else if (nv <= 256)
+            ln_fwd_warp_kernel<T, 8><<<grid, kLnThreads, 0, st>>>(p);
+        else
+            ln_fwd_warp_kernel<T, 16><<<grid, kLnThreads, 0, st>>>(p);
+        return;
+    }
+    (void)vpt;  // rows above the warp kernel's capacity take four vectors per thread
+    ln_fwd_kernel<T, kLnMaxVpt><<<p.M, kLnThreads, 0, st>>>(p);
+}
+
+template <typename T, int VPT>
+static void ln_bwd_launch(const LnPlan &p, int *chunks_out, cudaStream_t st) {
+    // one wave: rows per block = M / (resident blocks), at least kLnBwdMinRows
+    static const int per_sm = [] {  // same value on every device of one architecture
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln_bwd_kernel<T, VPT>, kLnThreads, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        return n;
+    }();
+    const long long slots = static_cast<long long>(per_sm) * num_sms();
+    int rows = static_cast<int>((p.M + slots - 1) / slots);
+    if (rows < kLnBwdMinRows) rows = kLnBwdMinRows;
+    const int chunks = (p.M + rows - 1) / rows;
+    *chunks_out = chunks;
+    ln_bwd_kernel<T, VPT><<<chunks, kLnThreads, 0, st>>>(p, rows);
 }
 
 template <typename T>
-static void ln_bwd_dispatch(const LnPlan &p, int vpt, int chunks, cudaStream_t st) {
+static void ln_bwd_dispatch(const LnPlan &p, int vpt, int *chunks, cudaStream_t st) {
     if (vpt == 1)
-        ln_bwd_kernel<T, 1><<<chunks, kLnThreads, 0, st>>>(p);
+        ln_bwd_launch<T, 1>(p, chunks, st);
     else if (vpt == 2)
-        ln_bwd_kernel<T, 2><<<chunks, kLnThreads, 0, st>>>(p);
+        ln_bwd_launch<T, 2>(p, chunks, st);
     else
-        ln_bwd_kernel<T, 4><<<chunks, kLnThreads, 0, st>>>(p);
+        ln_bwd_launch<T, 4>(p, chunks, st);
 }
 
 tp_status launch_ln_fwd(const LnPlan &p, int dtype, cudaStream_t st) {
@@ -300,12 +489,12 @@ tp_status launch_ln_bwd(const LnPlan &p, int dtype, cudaStream_t st) {
         if (e == cudaSuccess) e = cudaMemsetAsync(p.dbeta, 0, sizeof(float) * p.H, st);
         return cuda_check(e, "cudaMemsetAsync(dgamma, dbeta)");
     }
-    const int chunks = ln_bwd_chunks(p.M);
+    int chunks = 1;
     launch_begin("layernorm_bwd", st);
     if (dtype == TP_DT_F32)
-        ln_bwd_dispatch<float>(p, vpt, chunks, st);
+        ln_bwd_dispatch<float>(p, vpt, &chunks, st);
     else
-        ln_bwd_dispatch<__nv_bfloat16>(p, vpt, chunks, st);
+        ln_bwd_dispatch<__nv_bfloat16>(p, vpt, &chunks, st);
     cudaError_t e = cudaGetLastError();
     launch_end("layernorm_bwd", st);
     if (e != cudaSuccess) return cuda_check(e, "layernorm_bwd");
@@ -321,19 +510,30 @@ tp_status launch_ln_bwd(const LnPlan &p, int dtype, cudaStream_t st) {
     return launch_colsum_finalize(c, chunks, st);
 }
 
+int dropout_bwd_chunks(int M) { return M <= 0 ? 1 : (M + kDropRows - 1) / kDropRows; }
+
 tp_status launch_dropout_bwd(const LnPlan &p, int dtype, cudaStream_t st) {
     if (p.M == 0) return TP_OK;
-    const long long nv = static_cast<long long>(p.M) * p.H / (dtype == TP_DT_F32 ? 4 : 8);
-    const long long want = (nv + 255) / 256, cap = 8ll * num_sms();
-    const int grid = static_cast<int>(want < cap ? want : cap);
+    const int vec = dtype == TP_DT_F32 ? 4 : 8;
+    const int chunks = dropout_bwd_chunks(p.M);
+    const dim3 grid((p.H / vec + kDropThreads - 1) / kDropThreads, chunks);
     launch_begin("dropout_bwd", st);
     if (dtype == TP_DT_F32)
-        dropout_bwd_kernel<float><<<grid, 256, 0, st>>>(p);
+        dropout_bwd_kernel<float><<<grid, kDropThreads, 0, st>>>(p);
     else
-        dropout_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+        dropout_bwd_kernel<__nv_bfloat16><<<grid, kDropThreads, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     launch_end("dropout_bwd", st);
-    return cuda_check(e, "dropout_bwd");
+    if (e != cudaSuccess) return cuda_check(e, "dropout_bwd");
+    if (!p.db2) return TP_OK;  // no bias gradient wanted
+    ColsumPlan c;
+    c.name = "bias_grad_row";
+    c.P = 1;
+    c.M = p.M;
+    c.N = p.H;
+    c.out[0] = p.db2;
+    c.partials = p.partials;
+    return launch_colsum_finalize(c, chunks, st);
 }
 
 }  // namespace tpmlp

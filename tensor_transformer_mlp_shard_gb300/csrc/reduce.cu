@@ -154,14 +154,37 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_partial_kernel(const __gri
     }
 }
 
-__global__ void colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
+// Second pass: out_z[c] = sum_k partials[z][k][c].  A block owns 32 columns;
+// warp w adds the partial rows k = w, w + kWarps, ... in increasing k (four
+// interleaved accumulators for memory-level parallelism, combined in a fixed
+// order), then warp 0 adds the warps' sums in warp order: deterministic.
+__global__ void __launch_bounds__(32 * kWarps) colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
+    __shared__ float red[kWarps][32];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int z = blockIdx.y;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= p.N) return;
-    const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
-    float s = 0.0f;
-    for (int k = 0; k < p.chunks; ++k) s += src[static_cast<long long>(k) * p.N];
-    p.out[z][c] = s;
+    const int c = blockIdx.x * 32 + lane;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    if (c < p.N) {
+        const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
+        const long long step = static_cast<long long>(kWarps) * p.N;
+        int k = warp;
+        for (; k + 3 * kWarps < p.chunks; k += 4 * kWarps) {
+            const float *q = src + static_cast<long long>(k) * p.N;
+            a0 += q[0];
+            a1 += q[step];
+            a2 += q[2 * step];
+            a3 += q[3 * step];
+        }
+        for (; k < p.chunks; k += kWarps) a0 += src[static_cast<long long>(k) * p.N];
+    }
+    red[warp][lane] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (warp == 0 && c < p.N) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[w][lane];
+        p.out[z][c] = s;
+    }
 }
 
 tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st) {
@@ -173,9 +196,9 @@ tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t s
     prm.chunks = chunks;
     prm.partials = c.partials;
     if (c.N == 0 || c.P == 0) return TP_OK;
-    dim3 g2((c.N + 255) / 256, c.P);
+    dim3 g2((c.N + 31) / 32, c.P);
     launch_begin("colsum_finalize", st);
-    colsum_finalize_kernel<<<g2, 256, 0, st>>>(prm);
+    colsum_finalize_kernel<<<g2, 32 * kWarps, 0, st>>>(prm);
     cudaError_t e = cudaGetLastError();
     launch_end("colsum_finalize", st);
     return cuda_check(e, "colsum_finalize");
@@ -213,9 +236,9 @@ tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     launch_end(c.name, st);
     if (e != cudaSuccess) return cuda_check(e, c.name);
-    dim3 g2((c.N + 255) / 256, c.P);
+    dim3 g2((c.N + 31) / 32, c.P);
     launch_begin("colsum_finalize", st);
-    colsum_finalize_kernel<<<g2, 256, 0, st>>>(prm);
+    colsum_finalize_kernel<<<g2, 32 * kWarps, 0, st>>>(prm);
     e = cudaGetLastError();
     launch_end("colsum_finalize", st);
     return cuda_check(e, "colsum_finalize");

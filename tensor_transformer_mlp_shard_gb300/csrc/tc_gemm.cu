@@ -68,8 +68,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2D tensor map of a row-major [rows, cols] buffer with leading dimension
 // `ld` elements.
-static tp_status encode_map_ex(CUtensorMap *m, const void *ptr, int rows, int cols, long long ld, int box_inner,
-                               int box_rows, CUtensorMapDataType type, int esize, CUtensorMapSwizzle swz) {
+tp_status encode_map_ex(CUtensorMap *m, const void *ptr, int rows, int cols, long long ld, int box_inner,
+                        int box_rows, CUtensorMapDataType type, int esize, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
     if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -85,8 +85,7 @@ static tp_status encode_map_ex(CUtensorMap *m, const void *ptr, int rows, int co
 }
 
 // operand map: 1-byte (FP8) or 2-byte (bf16) elements, 128-byte swizzle
-static tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows,
-                            bool fp8) {
+tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int box_inner, int box_rows, bool fp8) {
     return encode_map_ex(m, ptr, rows, cols, cols, box_inner, box_rows,
                          fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, fp8 ? 1 : 2,
                          CU_TENSOR_MAP_SWIZZLE_128B);

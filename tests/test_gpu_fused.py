@@ -1,0 +1,129 @@
+"""GPU parity of the fused MLP forward (one kernel: column GEMM, bias,
+activation, row GEMM with A passed through shared memory; Megatron's
+FlashFusedMLP idea, "Megatron-LM 源码精读" s2 code map) through the C ABI.
+
+* Against the fp64 oracle, element by element, on ragged multi-tile sizes,
+  sequence parallelism, odd T, every H the kernel takes (64..256) and more
+  token tiles than SMs (the persistent loop): tolerance 1e-2 * max|ref|
+  (bf16 storage of pre and A, fp32 sums), the MLP's bf16 bound.
+* Against the two-kernel path on the same inputs: both accumulate the same
+  products in fp32 in 64-element K steps, so pre and A agree bit for bit and
+  Y to within fp32 reassociation of the chunk sums.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import MlpRun, host, mlp_inputs, rel_err
+from oracle import layer as olayer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import tensor_transformer_mlp_shard_gb300 as tp
+    from tensor_transformer_mlp_shard_gb300 import build
+    build.build()
+    yield tp
+    tp.set_fused_fwd("auto")
+
+
+CASES = [
+    # M, H, F, T, act, bias, residual, sp
+    (300, 256, 1024, 2, "gelu_tanh", True, True, False),
+    (300, 64, 512, 4, "none", False, False, False),
+    (517, 128, 768, 3, "gelu_tanh", True, False, False),
+    (1024, 192, 1024, 4, "gelu_tanh", True, True, True),
+    (128, 256, 256, 1, "gelu_tanh", False, True, False),
+    (40000, 256, 1024, 2, "gelu_tanh", True, True, False),
+]
+
+
+def _fwd(tp, lay, t, mode):
+    tp.set_fused_fwd(mode)
+    run = MlpRun(lay, t)
+    n0 = tp.launch_count()
+    run.fwd()
+    launches = tp.launch_count() - n0
+    assert tp.sync_status() == 0
+    return run, launches
+
+
+@pytest.mark.parametrize("M,H,F,T,act,bias,residual,sp", CASES)
+def test_fused_forward_matches_oracle_and_two_kernel_path(tp, M, H, F, T, act, bias, residual, sp):
+    S, B = (M // 2, 2) if M % 2 == 0 else (M, 1)
+    lay = tp.TPMLP(S=S, B=B, H=H, F=F, T=T, act=act, dtype="bf16", has_bias=bias, residual=residual,
+                   seq_parallel=sp)
+    t = mlp_inputs(M, H, F, T, act, "bf16", has_bias=bias)
+    fused, n_fused = _fwd(tp, lay, t, "on")
+    split, n_split = _fwd(tp, lay, t, "off")
+    assert n_fused == 1 and n_split == 2
+    pre, A, Y = oracle.mlp_fwd(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, residual)
+    errs = {"Y": rel_err(fused.gathered(fused.Y), Y)}
+    for i in range(T):
+        errs[f"pre{i}"] = rel_err(host(fused.pre[i]), pre[i])
+        errs[f"A{i}"] = rel_err(host(fused.A[i]), A[i])
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
+    for i in range(T):
+        assert torch.equal(fused.pre[i], split.pre[i]), i
+        assert torch.equal(fused.A[i], split.A[i]), i
+    d = rel_err(fused.gathered(fused.Y), split.gathered(split.Y).astype(np.float64))
+    assert d <= 2 ** -7, d
+
+
+def test_fused_forward_feeds_the_backward(tp):
+    """The backward after a fused forward equals the backward after the
+    two-kernel forward (it reads pre and A, which are bit-identical)."""
+    M, H, F, T = 384, 256, 1024, 2
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    outs = []
+    for mode in ("on", "off"):
+        run, _ = _fwd(tp, lay, t, mode)
+        run.bwd()
+        assert tp.sync_status() == 0
+        outs.append(run)
+    a, b = outs
+    for x, y in zip(a.dW1 + a.dW2 + [a.db2] + a.db1 + a.dX, b.dW1 + b.dW2 + [b.db2] + b.db1 + b.dX):
+        assert torch.equal(x, y)
+
+
+def test_fused_forward_not_taken_outside_its_shapes(tp):
+    tp.set_fused_fwd("on")
+    for kw in (dict(H=320, F=1024), dict(H=256, F=1024, act="swiglu"), dict(H=256, F=96 * 2)):
+        act = kw.pop("act", "gelu_tanh")
+        lay = tp.TPMLP(S=64, B=2, T=2, act=act, dtype="bf16", **kw)
+        t = mlp_inputs(128, lay.H, lay.F, 2, act, "bf16", has_bias=False)
+        run = MlpRun(lay, t)
+        n0 = tp.launch_count()
+        run.fwd()
+        assert tp.launch_count() - n0 == 2, kw
+    assert tp.sync_status() == 0
+    tp.set_fused_fwd("auto")
+
+
+def test_fused_layer_forward_with_dropout(tp):
+    """The sub-block's forward on the fused kernel (dropout in its output
+    epilogue) against the layer oracle."""
+    from test_gpu_layer import LayerRun, layer_inputs, SEED, _p32
+    M, H, F, T, p = 300, 256, 1024, 2, 0.1
+    lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, dropout_p=p)
+    t = layer_inputs(M, H, F, T, "gelu_tanh", "bf16", True)
+    tp.set_fused_fwd("on")
+    run = LayerRun(lay, t)
+    n0 = tp.launch_count()
+    run.fwd(SEED)
+    assert tp.launch_count() - n0 == 2  # LayerNorm + fused MLP
+    run.bwd(SEED)
+    assert tp.sync_status() == 0
+    f = olayer.layer_fwd(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], "gelu_tanh",
+                         _p32(p), SEED)
+    gr = olayer.layer_bwd(t["dY"], t["X"], t["gamma"], t["W1s"], t["W2s"], f, "gelu_tanh", _p32(p))
+    errs = {"Y": rel_err(run.gathered(run.Y), f["Y"]), "dX": rel_err(run.gathered(run.dX), gr["dX"]),
+            "dgamma": rel_err(host(run.dgamma), gr["dgamma"]), "db2": rel_err(host(run.db2), gr["db2"])}
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
+    tp.set_fused_fwd("auto")
