@@ -118,8 +118,11 @@ TP_API void tp_mlp_destroy(tp_mlp *h);
 
 /* Bytes of device workspace tp_mlp_bwd (and, for TP_DT_FP8, tp_mlp_fwd_ws)
  * needs (256-byte aligned start).  It holds dPre_i (M x g*Fs per shard, bf16
- * or fp32), fp32 partial column sums for the bias gradients and, for FP8, the
- * per-tensor amax values and the quantised operands. */
+ * or fp32), fp32 partial column sums for the bias gradients, fp32 split-K
+ * partial sums of the weight gradients when their outputs have few tiles and
+ * many tokens (bf16 and FP8: up to 16 token splits, added in split order by a
+ * reduction kernel) and, for FP8, the per-tensor amax values and the
+ * quantised operands.  A function of the descriptor alone. */
 TP_API size_t tp_mlp_workspace_bytes(const tp_mlp *h);
 
 /* ---- MLP forward ("Megatron-LM 源码精读" s3.3 figure) ------------------------
@@ -182,7 +185,8 @@ TP_API tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X,
                         const void *const *W, const void *b,
                         const void *const *R, void *const *Y, void *stream);
 
-/* Workspace bytes for tp_linear_col_bwd / tp_linear_row_bwd (bias partials). */
+/* Workspace bytes for tp_linear_col_bwd / tp_linear_row_bwd: bias partials,
+ * then split-K partials of the weight gradient (as for tp_mlp_bwd). */
 TP_API size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc);
 
 /* tp_linear_col_bwd: gradients of tp_linear_col with act = TP_ACT_NONE
@@ -210,7 +214,9 @@ TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *d
  *   only the op's tensors and has no allocator of its own, a process whose
  *   device memory is fully reserved by another (caching) allocator, or a
  *   latency-critical loop that cannot take cudaMalloc's implicit device
- *   synchronisation.  It computes exactly what tp_linear_row_bwd computes and
+ *   synchronisation.  It computes the gradients tp_linear_row_bwd computes
+ *   (the weight gradient always without token splitting, so where
+ *   tp_linear_row_bwd splits K the two differ by fp32 summation order) and
  *   allocates nothing: the bias-gradient partial sums go to a 4 MiB array
  *   compiled into the library (held on every GPU that loads the library until
  *   the process exits).  Arguments are those of tp_linear_row_bwd minus the

@@ -322,11 +322,36 @@ static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY,
     return run_gemm(g, d->dtype, st);
 }
 
+// Split-K of a weight gradient (P outputs [Mo x No], K = M tokens): when its
+// 256 x 256 output tiles would occupy fewer than half of about 74 CTA pairs,
+// split the tokens so that the tiles fill them (at most 16 ways, at least 8
+// K blocks of 64 tokens per split).  A fixed pair count keeps the workspace
+// size a function of the shapes alone.
+constexpr int kSplitTargetPairs = 74;
+
+static int wgrad_ksplit(int Mo, int No, int P, int K) {
+    const long long tiles = static_cast<long long>((Mo + 255) / 256) * ((No + 255) / 256) * P;
+    if (tiles == 0 || tiles * 2 > kSplitTargetPairs) return 1;
+    int ks = static_cast<int>(kSplitTargetPairs / tiles);
+    ks = std::min(ks, std::min(16, ((K + 63) / 64) / 8));
+    return std::max(ks, 1);
+}
+
+static size_t split_bytes(const tp_mlp_desc *d, int Mo, int No) {
+    const Dims x = dims_of(d);
+    if (d->dtype == TP_DT_F32) return 0;  // the fp32 engine does not split
+    const int ks = wgrad_ksplit(Mo, No, x.T, x.M);
+    if (ks <= 1) return 0;
+    return align256(sizeof(float) * ks * x.T * static_cast<size_t>((Mo + 255) / 256 * 256) * No);
+}
+
 // Weight gradient dW_i = G_i^T Act_i over all tokens (fp32).  G has width
 // gw (the output side of the layer), Act width aw; either may be token-sharded
-// (1 buffer or nx buffers) or per shard (T buffers).
+// (1 buffer or nx buffers) or per shard (T buffers).  split_ws (or null):
+// workspace for split-K partial sums, split_bytes(d, gw, aw) bytes.
 static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const *G, int g_per_shard, int gw,
-                       const void *const *Act, int a_per_shard, int aw, void *const *dW, cudaStream_t st) {
+                       const void *const *Act, int a_per_shard, int aw, void *const *dW, cudaStream_t st,
+                       float *split_ws) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = name;
@@ -346,6 +371,10 @@ static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const
         set_operand(g.B, Act, x.nx, x.rs ? x.rs : x.M, aw, true, 0, 0, x.rs);
     set_out(g.out, reinterpret_cast<const void *const *>(dW), x.T, 1, 0, aw);
     g.accumulate = d->wgrad_accumulate != 0;
+    if (split_ws && split_bytes(d, gw, aw)) {
+        g.ksplit = wgrad_ksplit(gw, aw, x.T, x.M);
+        g.split_ws = split_ws;
+    }
     return run_gemm(g, d->dtype, st);
 }
 
@@ -401,19 +430,24 @@ static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
     return align256(sizeof(float) * static_cast<size_t>(P) * colsum_chunks(x.M) * N);
 }
 
-// Workspace of the backward: dPre_i (bf16/fp32) then the bias partials.
-static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
+// Workspace of the backward: dPre_i (bf16/fp32), the bias partials, then
+// the split-K partials of the weight gradients.
+static size_t bias_part_bytes(const tp_mlp_desc *d) {
+    const Dims x = dims_of(d);
+    if (!d->has_bias) return 0;
+    // db1: colsum partials, or the fused epilogue's per-32-row-block sums
+    const size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
+    const size_t c = align256(sizeof(float) * size_t(x.T) * ((x.M + 31) / 32) * x.g * x.Fs);
+    return std::max(a, std::max(b, c));
+}
+
+static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes, size_t *split_off = nullptr) {
     const Dims x = dims_of(d);
     const size_t shard = align256(static_cast<size_t>(x.M) * x.g * x.Fs * x.es);
     if (dpre_shard_bytes) *dpre_shard_bytes = shard;
-    size_t part = 0;
-    if (d->has_bias) {
-        // db1: colsum partials, or the fused epilogue's per-32-row-block sums
-        const size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
-        const size_t c = align256(sizeof(float) * size_t(x.T) * ((x.M + 31) / 32) * x.g * x.Fs);
-        part = std::max(a, std::max(b, c));
-    }
-    return shard * x.T + part;
+    const size_t off = shard * x.T + bias_part_bytes(d);
+    if (split_off) *split_off = off;
+    return off + std::max(split_bytes(d, x.H, x.Fs), split_bytes(d, x.g * x.Fs, x.H));
 }
 
 // FP8 region (after the backward region): amax slots, then the quantised
@@ -559,11 +593,12 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
-    size_t shard_bytes = 0;
-    bwd_ws_bytes(d, &shard_bytes);
+    size_t shard_bytes = 0, split_off = 0;
+    bwd_ws_bytes(d, &shard_bytes, &split_off);
     char *base = static_cast<char *>(ws);
     float *amax = reinterpret_cast<float *>(base + L.amax);
     float *partials = reinterpret_cast<float *>(base + x.T * shard_bytes);
+    float *split = reinterpret_cast<float *>(base + split_off);
     void *xq = base + L.xq, *dyq = base + L.dyq;
     void *w1q[kMaxShards], *w2q[kMaxShards], *aq[kMaxShards], *dpq[kMaxShards], *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) {
@@ -625,6 +660,10 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_operand(g.B, aq, x.T, x.M, x.Fs, true, 1, 0, 0);
         set_out(g.out, reinterpret_cast<const void *const *>(dW2), x.T, 1, 0, x.Fs);
         g.accumulate = d->wgrad_accumulate != 0;
+        if (split_bytes(d, x.H, x.Fs)) {
+            g.ksplit = wgrad_ksplit(x.H, x.Fs, x.T, x.M);
+            g.split_ws = split;
+        }
         set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_A);
         TRY(launch_tc_gemm(g, st));
     }
@@ -641,6 +680,10 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_operand(g.B, xa, 1, x.M, x.H, true, 0, 0, 0);
         set_out(g.out, reinterpret_cast<const void *const *>(dW1), x.T, 1, 0, x.H);
         g.accumulate = d->wgrad_accumulate != 0;
+        if (split_bytes(d, gw, x.H)) {
+            g.ksplit = wgrad_ksplit(gw, x.H, x.T, x.M);
+            g.split_ws = split;
+        }
         set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DP, AMAX_X);
         TRY(launch_tc_gemm(g, st));
     }
@@ -783,12 +826,15 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     void *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
+    size_t split_off = 0;
+    bwd_ws_bytes(d, nullptr, &split_off);
+    float *split = reinterpret_cast<float *>(static_cast<char *>(workspace) + split_off);
     // row layer: dPre_i = (dY W2_i) * act'(pre_i), dW2_i = dY^T A_i
     bool db1_fused = false;
     TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st, d->has_bias ? partials : nullptr, &db1_fused));
-    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st));
+    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st, split));
     // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY)
-    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st));
+    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st, split));
     TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st));
     if (d->has_bias) {
         if (db1_fused)
@@ -902,11 +948,18 @@ tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X, const voi
                    static_cast<cudaStream_t>(stream));
 }
 
-size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
-    if (validate_desc(desc) != TP_OK || !desc->has_bias) return 0;
+// single-layer workspace: [bias partials | split-K partials of the weight gradient]
+static size_t linear_part_bytes(const tp_mlp_desc *desc) {
+    if (!desc->has_bias) return 0;
     const Dims x = dims_of(desc);
     size_t a = partials_bytes(desc, x.T, x.g * x.Fs), b = partials_bytes(desc, 1, x.H);
     return a > b ? a : b;
+}
+
+size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
+    if (validate_desc(desc) != TP_OK) return 0;
+    const Dims x = dims_of(desc);
+    return linear_part_bytes(desc) + std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs));
 }
 
 static tp_status check_ws(const tp_mlp_desc *d, void *ws, size_t bytes) {
@@ -939,7 +992,8 @@ tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, co
         return zero_grads(desc, dW, x.T, sizeof(float) * x.Fs * x.H, desc->has_bias ? db : nullptr, x.T,
                           sizeof(float) * x.Fs, st);
     TRY(column_dgrad(desc, dOut, x.Fs, W, nullptr, dX, st));
-    TRY(wgrad(desc, "wgrad_col", dOut, 1, x.Fs, X, 0, x.H, dW, st));
+    TRY(wgrad(desc, "wgrad_col", dOut, 1, x.Fs, X, 0, x.H, dW, st,
+              reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc))));
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_col", dOut, x.T, 1, 0, x.T, x.Fs, db, static_cast<float *>(workspace), st));
     return TP_OK;
@@ -948,6 +1002,22 @@ tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, co
 tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
                             const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
                             size_t workspace_bytes, void *stream) {
+    return linear_row_bwd_impl(desc, dY, X, W, dX, dW, db, workspace, workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+namespace tpmlp {
+
+size_t linear_bias_workspace_bytes(const tp_mlp_desc *desc) {
+    return validate_desc(desc) == TP_OK ? linear_part_bytes(desc) : 0;
+}
+
+// tp_linear_row_bwd; without allow_split the weight gradient is never split
+// over tokens and the workspace need only hold the bias partials.
+tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
+                              const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
+                              size_t workspace_bytes, void *stream, bool allow_split) {
     TRY(validate_desc(desc));
     if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     const Dims x = dims_of(desc);
@@ -959,18 +1029,32 @@ tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, cons
     TRY(check_array(W, x.T, "W"));
     TRY(check_array(reinterpret_cast<const void *const *>(dW), x.T, "dW"));
     if (desc->has_bias) TRY(check_one(db, "db"));
-    TRY(check_ws(desc, workspace, workspace_bytes));
+    if (allow_split) {
+        TRY(check_ws(desc, workspace, workspace_bytes));
+    } else {
+        const size_t need = linear_part_bytes(desc);
+        if (workspace_bytes < need)
+            return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+            return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *const *dba = reinterpret_cast<void *const *>(&db);
     if (x.M == 0)
         return zero_grads(desc, dW, x.T, sizeof(float) * x.H * x.Fs, desc->has_bias ? dba : nullptr, 1,
                           sizeof(float) * x.H, st);
     TRY(row_dgrad(desc, TP_ACT_NONE, dY, W, nullptr, dX, x.Fs, st));
-    TRY(wgrad(desc, "wgrad_row", dY, 0, x.H, X, 1, x.Fs, dW, st));
+    float *split = allow_split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc))
+                               : nullptr;
+    TRY(wgrad(desc, "wgrad_row", dY, 0, x.H, X, 1, x.Fs, dW, st, split));
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
     return TP_OK;
 }
+
+}  // namespace tpmlp
+
+extern "C" {
 
 // ---------------------------------------------------------------------------
 // TransformerLayer MLP sub-block: Y = X + dropout(MLP(LayerNorm(X)))

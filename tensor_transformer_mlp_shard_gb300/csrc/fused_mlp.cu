@@ -15,10 +15,13 @@
 // fit on chip and the two-kernel path (tc_gemm) runs instead.
 //
 // Warp roles (320 threads): warp 0 issues TMA (the X tile once per token
-// tile, then W1 and W2 boxes in consumption order through an 8-slot ring),
+// tile, then W1 and W2 boxes in consumption order through a 16-slot ring),
 // warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of chunk
-// c - 1, so that the tensor core works while the epilogue turns chunk c - 1
-// into A), warps 2-9 run the epilogues.  Every wait is bounded.
+// c - 2, so that the tensor core works while two epilogue groups turn chunks
+// c - 1 and c - 2 into A), warps 2-9 run the epilogues in two groups that
+// take alternate chunks and write pre, A and Y with direct 16-byte stores
+// (no staging: a chunk's epilogue is short, and waiting for bulk stores to
+// release staging buffers stretched it).  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -45,26 +48,28 @@ constexpr int kRows = 128;      // token rows per tile (tcgen05 M)
 constexpr int kChunk = 64;      // hidden units per chunk: column GEMM N, row GEMM K
 constexpr int kMaxH = 256;      // output tile [128 x H] + 2 x 64 accumulator columns <= 512 TMEM columns
 constexpr int kBox = 64 * 128;  // one [64 rows x 64] bf16 box (128-byte rows): 8 KB
-constexpr int kSlots = 8;
+constexpr int kSlots = 16;
+constexpr int kLag = 2;         // the row GEMM of chunk c is issued after the column GEMM of chunk c + 2
 constexpr int kXBytes = kMaxH / 64 * (kRows * 128);  // X tile: H/64 boxes of [128 x 64]
 constexpr int kABytes = kRows * 128;                 // A chunk [128 x 64] bf16
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kOffX = kSlots * kBox;
 constexpr int kOffA = kOffX + kXBytes;
-constexpr int kOffEpi = kOffA + 2 * kABytes;
-constexpr int kOffBar = kOffEpi + kEpiWarps * EPI_STAGE_BYTES;
+constexpr int kOffBar = kOffA + 2 * kABytes;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment slack
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 320
+static_assert(2 * kSlots + 13 <= 64, "barriers overlap the TMEM address slot");
+static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB a block may use");
 
 struct FusedParams {
     CUtensorMap mapX[kMaxShards];    // X token shards, boxes [128 rows x 64], 128-byte swizzle
     CUtensorMap mapW1[kMaxShards];   // W1_i [Fs, H], boxes [64 x 64]
     CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [64 x 64]
-    CUtensorMap mapPre[kMaxShards];  // pre_i [M, Fs], store boxes [32 x 32], 64-byte swizzle
-    CUtensorMap mapA[kMaxShards];    // A_i [M, Fs]
-    CUtensorMap mapY[kMaxShards];    // Y token shards
+    __nv_bfloat16 *pre[kMaxShards];  // pre_i [M, Fs] (or null)
+    __nv_bfloat16 *A[kMaxShards];    // A_i [M, Fs]
+    __nv_bfloat16 *Y[kMaxShards];    // Y token shards [rows_split or M, H]
     const __nv_bfloat16 *b1[kMaxShards];
     const __nv_bfloat16 *b2;
     const __nv_bfloat16 *res[kMaxShards];
@@ -94,6 +99,16 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, const Fused
     }
 }
 
+// Chunk at position c of token tile t.  Every tile walks all nc chunks, but
+// starting at chunk t mod nc, so that the CTAs (which start together) stream
+// different weight chunks at any moment instead of all asking the same L2
+// lines for the same boxes.  The order changes only the fp32 order of the
+// additions into the output tile.
+__device__ __forceinline__ int chunk_at(const FusedParams &p, int t, int c) {
+    const int ch = c + t % p.nc;
+    return ch < p.nc ? ch : ch - p.nc;
+}
+
 // token shard and local row of global row `row0`
 __device__ __forceinline__ void tok_index(const FusedParams &p, int row0, int &j, int &lrow) {
     j = 0;
@@ -104,12 +119,18 @@ __device__ __forceinline__ void tok_index(const FusedParams &p, int row0, int &j
     }
 }
 
+// 32 bf16 of one row: four 16-byte stores (the row's 64 bytes are contiguous)
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint4 (&w)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) reinterpret_cast<uint4 *>(dst)[j] = w[j];
+}
+
 __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid_constant__ FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 32);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 64);  // after the 2 * kSlots + 13 barriers
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * kSlots;
     const uint32_t xfull = empty0 + 8 * kSlots, xempty = xfull + 8;
@@ -128,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         mbar_init(xempty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
-            mbar_init(acce0 + 8 * b, kEpiThreads);
-            mbar_init(af0 + 8 * b, kEpiThreads);
+            mbar_init(acce0 + 8 * b, kEpiThreads / 2);  // one epilogue group per buffer
+            mbar_init(af0 + 8 * b, kEpiThreads / 2);
             mbar_init(ae0 + 8 * b, 1);
         }
         mbar_init(yfull, 1);
@@ -176,14 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 x_par = it & 1;
                 for (int kb = 0; kb < p.kb; ++kb)
                     tma_load_2d(sbase + kOffX + kb * kRows * 128, &p.mapX[tj], xfull, kb * 64, tl);
-                // boxes in the order the MMA warp consumes them
-                for (int c = 0; ok && c <= p.nc; ++c) {
+                // boxes in the order the MMA warp consumes them; position c of
+                // tile t holds chunk (c + t) mod nc
+                for (int c = 0; ok && c < p.nc + kLag; ++c) {
                     if (c < p.nc) {
-                        const int i = c / p.cps, u0 = (c % p.cps) * kChunk;
+                        const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                         for (int kb = 0; ok && kb < p.kb; ++kb) ok = load_box(&p.mapW1[i], kb * 64, u0);
                     }
-                    if (ok && c >= 1) {
-                        const int i = (c - 1) / p.cps, u0 = ((c - 1) % p.cps) * kChunk;
+                    if (ok && c >= kLag) {
+                        const int ch = chunk_at(p, t, c - kLag), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                         for (int g = 0; ok && g < p.kb; ++g) ok = load_box(&p.mapW2[i], u0, g * 64);
                     }
                 }
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             bool ok = true;
             int it = 0, cgb = 0;
             for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it, cgb += p.nc) {
-                for (int c = 0; ok && c <= p.nc; ++c) {
+                for (int c = 0; ok && c < p.nc + kLag; ++c) {
                     if (c < p.nc) {
                         // column GEMM of chunk c: acc1[b] = X_tile W1 chunk^T (K = H)
                         const int cg = cgb + c, b = cg & 1;
@@ -237,15 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         umma_commit(accf0 + 8 * b);
                         if (c == p.nc - 1) umma_commit(xempty);  // the tile's last read of X
                     }
-                    if (c >= 1) {
-                        // row GEMM of chunk c - 1: Y[:, 64g..] += A W2 chunk^T (K = 64)
-                        const int cg = cgb + c - 1, b = cg & 1;
+                    if (c >= kLag) {
+                        // row GEMM of chunk c - kLag: Y[:, 64g..] += A W2 chunk^T (K = 64)
+                        const int cg = cgb + c - kLag, b = cg & 1;
                         const uint32_t use = static_cast<uint32_t>(cg) >> 1;
                         if (!fwait(af0 + 8 * b, use & 1u, p)) {
                             ok = false;
                             break;
                         }
-                        if (c == 1 && !fwait(yempty, (it & 1) ^ 1u, p)) {
+                        if (c == kLag && !fwait(yempty, (it & 1) ^ 1u, p)) {
                             ok = false;
                             break;
                         }
@@ -261,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 umma_bf16(tmem_base + 64 * g, smem_desc(sa + kk * 32, 16, 1024),
-                                          smem_desc(sw + kk * 32, 16, 1024), p.idesc, (c > 1 || kk > 0) ? 1u : 0u);
+                                          smem_desc(sw + kk * 32, 16, 1024), p.idesc,
+                                          (c > kLag || kk > 0) ? 1u : 0u);
                             umma_commit(empty0 + 8 * slot);
                             if (++slot == kSlots) {
                                 slot = 0;
@@ -282,9 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         __syncwarp();
     } else {
         // ---------------- epilogues (warps 2..9) ----------------
+        // Two groups of four warps take alternate chunks (group g: the chunks
+        // whose accumulator / A buffer is g), so one group turns a chunk into A
+        // while the other waits for the next accumulator; within a group warp
+        // w owns TMEM lane quarter w & 3 (32 token rows) and all 64 columns.
         const int q = warp & 3;            // TMEM lane quarter: rows q*32 .. q*32+31 of the tile
-        const int h = (warp - 2) >> 2;     // column half: chunk columns 32h.., output columns 128h..
-        Stager stg{sbase + kOffEpi + (warp - 2) * EPI_STAGE_BYTES, 0u};
+        const int h = (warp - 2) >> 2;     // group: chunks with buffer h; output columns 128h..
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t r_tile = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
         int it = 0, cgb = 0;
@@ -294,46 +320,57 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             const int row = row0 + lane;
             const bool block_ok = row0 < p.M;  // warp-uniform
             const bool row_ok = row < p.M;
-            for (int c = 0; c < p.nc; ++c) {
-                const int cg = cgb + c, b = cg & 1;
+            for (int c = (cgb & 1) == h ? 0 : 1; c < p.nc; c += 2) {
+                const int cg = cgb + c, b = h;
                 const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
+                uint4 bias[8];  // the chunk's 64 b1 values, fetched while the accumulator fills
+                if (p.has_bias) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) bias[k] = *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 8 * k);
+                }
                 ok = fwait(accf0 + 8 * b, use & 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[32];
-                tmem_ld32(tmem_base + kAccCol + kChunk * b + h * 32 + lane_off, r);
+                uint32_t r[2][32];
+                tmem_ld32(tmem_base + kAccCol + kChunk * b + lane_off, r[0]);
+                tmem_ld32(tmem_base + kAccCol + kChunk * b + 32 + lane_off, r[1]);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(acce0 + 8 * b);
-                const int i = c / p.cps, u = (c % p.cps) * kChunk + h * 32;
-                float v[32];
+                mbar_arrive(acce0 + 8 * b);  // the column GEMM may reuse the accumulator
+                uint4 wa[2][4];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (p.has_bias) {
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int u = u0 + 32 * hh;
+                    float v[32];
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        float bb[8];
-                        load_bf16x8(p.b1[i] + u + 8 * g8, bb);
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[hh][j]);
+                    if (p.has_bias) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += bb[j];
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            const uint4 bw = bias[4 * hh + g8];
+                            v[8 * g8 + 0] += bf16_lo(bw.x); v[8 * g8 + 1] += bf16_hi(bw.x);
+                            v[8 * g8 + 2] += bf16_lo(bw.y); v[8 * g8 + 3] += bf16_hi(bw.y);
+                            v[8 * g8 + 4] += bf16_lo(bw.z); v[8 * g8 + 5] += bf16_hi(bw.z);
+                            v[8 * g8 + 6] += bf16_lo(bw.w); v[8 * g8 + 7] += bf16_hi(bw.w);
+                        }
                     }
-                }
-                uint4 w[4];
-                if (p.has_pre) {
-                    pack_bf16x32(v, w);
-                    if (block_ok) stage_store(stg, &p.mapPre[i], u, row0, w, lane);
-                }
-                if (p.act == TP_ACT_GELU_TANH) {
+                    if (p.has_pre) {
+                        pack_bf16x32(v, wa[hh]);
+                        if (row_ok) store_row32(p.pre[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
+                    }
+                    if (p.act == TP_ACT_GELU_TANH) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
+                        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
+                    }
+                    pack_bf16x32(v, wa[hh]);
+                    if (row_ok) store_row32(p.A[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
                 }
-                pack_bf16x32(v, w);
-                if (block_ok) stage_store(stg, &p.mapA[i], u, row0, w, lane);
-                // A into the row GEMM's operand buffer: row r_tile, 16-byte chunks
-                // 4h..4h+3 of its 128-byte line, 128-byte swizzle (chunk ^ (row & 7))
+                // A into the row GEMM's operand buffer: row r_tile, the eight
+                // 16-byte chunks of its 128-byte line, 128-byte swizzle (chunk ^ (row & 7))
                 ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -341,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 }
                 const uint32_t rowa = sbase + kOffA + b * kABytes + r_tile * 128u;
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    st_shared_v4(rowa + ((static_cast<uint32_t>(4 * h + jj) ^ (r_tile & 7u)) << 4), w[jj]);
+                for (int jj = 0; jj < 8; ++jj)
+                    st_shared_v4(rowa + ((static_cast<uint32_t>(jj) ^ (r_tile & 7u)) << 4), wa[jj >> 2][jj & 3]);
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
             }
@@ -389,13 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 }
                 uint4 w[4];
                 pack_bf16x32(v, w);
-                stage_store(stg, &p.mapY[tj], col, tl, w, lane);
+                if (row_ok) store_row32(p.Y[tj] + static_cast<long long>(tl + lane) * p.H + col, w);
             }
             tc_fence_before();
             mbar_arrive(yempty);
         }
-        if (lane == 0) bulk_wait<0>();  // bulk stores done before the CTA leaves
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -425,24 +460,19 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
                          f.act);
     FusedParams prm;
     memset(&prm, 0, sizeof(prm));
-    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int tok_rows = f.rows_split ? f.rows_split : f.M;
     for (int j = 0; j < f.n_tok; ++j) {
         tp_status s = tc::encode_map(&prm.mapX[j], f.X[j], tok_rows, f.H, 64, kRows, false);
-        if (s == TP_OK)
-            s = tc::encode_map_ex(&prm.mapY[j], f.Y[j], tok_rows, f.H, f.H, 32, 32, bf, 2, CU_TENSOR_MAP_SWIZZLE_64B);
         if (s != TP_OK) return s;
+        prm.Y[j] = static_cast<__nv_bfloat16 *>(f.Y[j]);
         prm.res[j] = f.has_res ? static_cast<const __nv_bfloat16 *>(f.R[j]) : nullptr;
     }
     for (int i = 0; i < f.T; ++i) {
         tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, 64, false);
         if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 64, false);
-        if (s == TP_OK)
-            s = tc::encode_map_ex(&prm.mapA[i], f.A[i], f.M, f.Fs, f.Fs, 32, 32, bf, 2, CU_TENSOR_MAP_SWIZZLE_64B);
-        if (s == TP_OK && f.has_pre)
-            s = tc::encode_map_ex(&prm.mapPre[i], f.pre[i], f.M, f.Fs, f.Fs, 32, 32, bf, 2,
-                                  CU_TENSOR_MAP_SWIZZLE_64B);
         if (s != TP_OK) return s;
+        prm.A[i] = static_cast<__nv_bfloat16 *>(f.A[i]);
+        prm.pre[i] = f.has_pre ? static_cast<__nv_bfloat16 *>(f.pre[i]) : nullptr;
         prm.b1[i] = f.has_bias ? static_cast<const __nv_bfloat16 *>(f.b1[i]) : nullptr;
     }
     prm.b2 = f.has_bias ? static_cast<const __nv_bfloat16 *>(f.b2) : nullptr;

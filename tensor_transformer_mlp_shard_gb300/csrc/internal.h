@@ -73,12 +73,23 @@ struct GemmPlan {
     // col_partials[P][ceil(M/32)][out.ld] (the db1 partials).
     float *amax_out = nullptr;
     float *col_partials = nullptr;
+    // EPI_F32 split-K (S == 1): the token (K) range is split `ksplit` ways,
+    // every split writes fp32 partial tiles into split_ws
+    // ([ksplit][P][roundup(M, 256)][N]) and a reduction adds them in split
+    // order into out (= or += with accumulate); ksplit = 1 or no split_ws: none
+    int ksplit = 1;
+    float *split_ws = nullptr;
     // EPI_PLAIN: out = residual + dropout(acc + bias) (TransformerLayer bias-dropout-add)
     bool dropout = false;
     uint32_t drop_threshold = 0;
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
 };
+
+// out_p[m][n] (=, or += with accumulate) sum_{k < ksplit} part[k][p][m][n],
+// part rows padded to split_rows per (k, p); fixed k order
+tp_status launch_splitk_reduce(const float *part, int ksplit, int P, int M, int split_rows, int N,
+                               float *const *out, bool accumulate, cudaStream_t st);
 
 // Column sums over token rows: out_p[c] = sum_m in_p[m, c] for c < N, fp32.
 struct ColsumPlan {
@@ -171,6 +182,14 @@ bool ln_supported(int H, int dtype);  // H within the LayerNorm kernels' row cap
 tp_status launch_ln_fwd(const LnPlan &p, int dtype, cudaStream_t st);
 tp_status launch_ln_bwd(const LnPlan &p, int dtype, cudaStream_t st);
 tp_status launch_dropout_bwd(const LnPlan &p, int dtype, cudaStream_t st);
+
+// tp_linear_row_bwd with split-K optional (the allocation-free entry point
+// runs it on a fixed scratch array that may not hold split partials), and the
+// workspace it needs without splitting (the bias partials).
+tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
+                              const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
+                              size_t workspace_bytes, void *stream, bool allow_split);
+size_t linear_bias_workspace_bytes(const tp_mlp_desc *desc);
 
 // Device status words (per device), the wait limit and the launch counter.
 struct DeviceWords {

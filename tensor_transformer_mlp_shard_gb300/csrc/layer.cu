@@ -416,7 +416,11 @@ static int ln_vpt(int H, int dtype) {
 
 bool ln_supported(int H, int dtype) { return H % (dtype == TP_DT_F32 ? 4 : 8) == 0 && ln_vpt(H, dtype) > 0; }
 
-constexpr int kLnWarpMaxVpw = 16;  // warp-per-row forward up to 512 vectors per row
+// Rows of up to 128 vectors (1024 bf16 / 512 fp32) take one warp each; wider
+// rows one block each (a 256-thread block per row keeps more rows' loads in
+// flight per SM at widths like 4096 than a 98-register warp per row does:
+// 26 us against 30 us for 8192 x 4096 bf16 under ncu).
+constexpr int kLnWarpMaxVpw = 4;
 
 template <typename T>
 static void ln_fwd_dispatch(const LnPlan &p, int vpt, cudaStream_t st) {
@@ -427,16 +431,16 @@ static void ln_fwd_dispatch(const LnPlan &p, int vpt, cudaStream_t st) {
             ln_fwd_warp_kernel<T, 1><<<grid, kLnThreads, 0, st>>>(p);
         else if (nv <= 64)
             ln_fwd_warp_kernel<T, 2><<<grid, kLnThreads, 0, st>>>(p);
-        else if (nv <= 128)
-            ln_fwd_warp_kernel<T, 4><<<grid, kLnThreads, 0, st>>>(p);
-        else if (nv <= 256)
-            ln_fwd_warp_kernel<T, 8><<<grid, kLnThreads, 0, st>>>(p);
         else
-            ln_fwd_warp_kernel<T, 16><<<grid, kLnThreads, 0, st>>>(p);
+            ln_fwd_warp_kernel<T, 4><<<grid, kLnThreads, 0, st>>>(p);
         return;
     }
-    (void)vpt;  // rows above the warp kernel's capacity take four vectors per thread
-    ln_fwd_kernel<T, kLnMaxVpt><<<p.M, kLnThreads, 0, st>>>(p);
+    if (vpt == 1)
+        ln_fwd_kernel<T, 1><<<p.M, kLnThreads, 0, st>>>(p);
+    else if (vpt == 2)
+        ln_fwd_kernel<T, 2><<<p.M, kLnThreads, 0, st>>>(p);
+    else
+        ln_fwd_kernel<T, 4><<<p.M, kLnThreads, 0, st>>>(p);
 }
 
 template <typename T, int VPT>

@@ -60,22 +60,25 @@ extern "C" {
 tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
                                     const void *const *W, void *const *dX, void *const *dW, void *db,
                                     void *stream) {
-    // 0 for an invalid descriptor too: tp_linear_row_bwd then reports the error.
-    const size_t need = tp_linear_workspace_bytes(desc);
+    // 0 for an invalid descriptor too: the row backward then reports the error.
+    const size_t need = tpmlp::linear_bias_workspace_bytes(desc);
     if (need > kScratchBytes)
         return tpmlp::set_error(TP_ERR_UNSUPPORTED,
                                 "bias gradient needs %zu bytes of scratch; the built-in scratch holds %zu "
                                 "(use tp_linear_row_bwd with a caller workspace)",
                                 need, kScratchBytes);
+    // split-K partials of the weight gradient only when they fit as well
+    const size_t full = tp_linear_workspace_bytes(desc);
+    const bool split = full <= kScratchBytes;
     void *ws = nullptr;
-    if (need) {
+    if (split ? full : need) {
         tp_status s = scratch_address(&ws);
         if (s != TP_OK) return s;
     }
     // The partial sums are written in full before they are read, so nothing
     // in the array has to start at zero and stale contents of a previous call
     // are never observed.
-    return tp_linear_row_bwd(desc, dY, X, W, dX, dW, db, ws, need ? kScratchBytes : 0, stream);
+    return tpmlp::linear_row_bwd_impl(desc, dY, X, W, dX, dW, db, ws, ws ? kScratchBytes : 0, stream, split);
 }
 
 }  // extern "C"

@@ -204,6 +204,68 @@ tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t s
     return cuda_check(e, "colsum_finalize");
 }
 
+// ---------------------------------------------------------------------------
+// split-K reduction of the weight gradients: four fp32 per thread, splits
+// added in index order (deterministic)
+// ---------------------------------------------------------------------------
+struct SplitkParams {
+    const float *part;
+    float *out[kMaxShards];
+    int ksplit, P, M, split_rows, N, accumulate;
+};
+
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SplitkParams p) {
+    const int z = blockIdx.y;
+    const long long nq = static_cast<long long>(p.M) * p.N / 4;  // float4 groups of one problem
+    const long long plane = static_cast<long long>(p.split_rows) * p.N;
+    for (long long q = blockIdx.x * 256ll + threadIdx.x; q < nq; q += static_cast<long long>(gridDim.x) * 256) {
+        const long long e = q * 4;
+        const float *src = p.part + static_cast<long long>(z) * plane + e;
+        float4 s = *reinterpret_cast<const float4 *>(src);
+        for (int k = 1; k < p.ksplit; ++k) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + static_cast<long long>(k) * p.P * plane);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(p.out[z] + e);
+        if (p.accumulate) {
+            const float4 o = *dst;
+            s.x += o.x;
+            s.y += o.y;
+            s.z += o.z;
+            s.w += o.w;
+        }
+        *dst = s;
+    }
+}
+
+tp_status launch_splitk_reduce(const float *part, int ksplit, int P, int M, int split_rows, int N,
+                               float *const *out, bool accumulate, cudaStream_t st) {
+    if (N % 4) return set_error(TP_ERR_SHAPE, "split-K reduction needs N %% 4 == 0 (N=%d)", N);
+    SplitkParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.part = part;
+    for (int i = 0; i < kMaxShards; ++i) prm.out[i] = i < P ? out[i] : nullptr;
+    prm.ksplit = ksplit;
+    prm.P = P;
+    prm.M = M;
+    prm.split_rows = split_rows;
+    prm.N = N;
+    prm.accumulate = accumulate ? 1 : 0;
+    const long long nq = static_cast<long long>(M) * N / 4;
+    if (nq == 0 || P == 0) return TP_OK;
+    long long blocks = (nq + 255) / 256;
+    const long long cap = 4ll * num_sms();
+    if (blocks > cap) blocks = cap;
+    launch_begin("splitk_reduce", st);
+    splitk_reduce_kernel<<<dim3(static_cast<unsigned>(blocks), P), 256, 0, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end("splitk_reduce", st);
+    return cuda_check(e, "splitk_reduce");
+}
+
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st) {
     ColsumParams prm;
     memset(&prm, 0, sizeof(prm));

@@ -167,11 +167,17 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.m_tiles = (g.M + tile_m - 1) / tile_m;
     const int n_per_tile = g.b_dual_off ? BN / 2 : BN;
     prm.n_tiles = (g.N + n_per_tile - 1) / n_per_tile;
-    prm.total_tiles = prm.m_tiles * prm.n_tiles * g.P;
+    prm.tiles_per_split = prm.m_tiles * prm.n_tiles * g.P;
+    // split-K: every split gets at least one K block
+    const bool split = g.kind == EPI_F32 && g.S == 1 && g.ksplit > 1 && g.split_ws && prm.num_kb > 1;
+    prm.kb_split = split ? (prm.num_kb + g.ksplit - 1) / g.ksplit : prm.num_kb;
+    const int ksplit = split ? (prm.num_kb + prm.kb_split - 1) / prm.kb_split : 1;
+    prm.split_rows = split ? prm.m_tiles * tile_m : 0;
+    prm.total_tiles = prm.tiles_per_split * ksplit;
     prm.group_m = use_pair ? 8 : 16;
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
-    prm.accumulate = g.accumulate ? 1 : 0;
+    prm.accumulate = (g.accumulate && !split) ? 1 : 0;  // split-K: the reduction accumulates
     // instruction descriptor: fp32 accumulator (bit 4), A/B formats (bits 7-9,
     // 10-12: bf16 = 1 for kind::f16; E4M3 = 0, E5M2 = 1 for kind::f8f6f4),
     // A/B MN-major (bits 15, 16), N/8 at bit 17, M/16 at bit 24
@@ -183,8 +189,18 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     // count that is not a multiple of 32 (a 32-column gate block would reach
     // into the up half of pre / dPre, which a store clipped at the buffer's
     // width cannot prevent).
-    prm.out_tma = tc_fused_epilogue(g) ? 1 : 0;
-    if (prm.out_tma) {
+    prm.out_tma = (tc_fused_epilogue(g) || split) ? 1 : 0;
+    if (split) {
+        // partial sums [ksplit][P][split_rows][N] fp32 in the caller's workspace
+        Out &o = prm.out;
+        memset(&o, 0, sizeof(o));
+        o.ptr[0] = g.split_ws;
+        o.nsplit = 1;
+        o.ld = g.N;
+        tp_status s = encode_map_ex(&prm.mapO[0], g.split_ws, ksplit * g.P * prm.split_rows, g.N, g.N, 16, 32,
+                                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B);
+        if (s != TP_OK) return s;
+    } else if (prm.out_tma) {
         const bool f32 = g.kind == EPI_F32;
         // columns of a whole output row: pre / dPre hold both SwiGLU halves
         const int ocols = static_cast<int>(g.out.ld);
@@ -280,7 +296,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
         e = cudaGetLastError();
     }
     launch_end(g.name, st);
-    return cuda_check(e, g.name);
+    if (e != cudaSuccess || !split) return cuda_check(e, g.name);
+    float *outs[kMaxShards];
+    for (int i = 0; i < kMaxShards; ++i) outs[i] = i < g.P ? static_cast<float *>(g.out.ptr[i * g.out.p_stride]) : nullptr;
+    return launch_splitk_reduce(g.split_ws, ksplit, g.P, g.M, prm.split_rows, g.N, outs, g.accumulate, st);
 }
 
 }  // namespace tpmlp

@@ -73,6 +73,11 @@ struct Params {
     int bias_p_stride, has_bias, has_out2, has_aux;
     int M, N, P, S, Kseg, num_kb;
     int m_tiles, n_tiles, total_tiles, group_m;
+    // split-K (weight gradients): tile t covers K blocks [ks * kb_split, ...) of
+    // split ks = t / tiles_per_split and writes fp32 partial sums at row
+    // (ks * P + p) * split_rows of the single partial buffer (split_rows = 0:
+    // no split, the plain output addressing)
+    int tiles_per_split, kb_split, split_rows;
     int act, b_dual_off, accumulate;
     uint32_t idesc;                  // tcgen05 instruction descriptor (formats, majors, M, N)
     DropoutParams drop;              // EPI_PLAIN: out = residual + dropout(acc + bias)
@@ -233,6 +238,7 @@ __device__ __forceinline__ float dequant_factor(const Params &p) {
 // side by side (problem p owns column tiles [p*n_tiles, (p+1)*n_tiles)).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tile_coords(const Params &p, int t, int &pi, int &mt, int &nt) {
+    t %= p.tiles_per_split;
     const int n_tot = p.P * p.n_tiles;
     const int per_group = p.group_m * n_tot;
     const int g = t / per_group;
@@ -243,6 +249,12 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &pi, int
     const int n = r / gm;
     pi = n / p.n_tiles;
     nt = n - pi * p.n_tiles;
+}
+
+// K blocks [kb0, kb1) of tile t (its split-K range)
+__device__ __forceinline__ void tile_kblocks(const Params &p, int t, int &kb0, int &kb1) {
+    kb0 = (t / p.tiles_per_split) * p.kb_split;
+    kb1 = min(p.num_kb, kb0 + p.kb_split);
 }
 
 // Tensor map and local row for buffer row `row`.  A row past the last token
@@ -452,12 +464,16 @@ __device__ __forceinline__ void flush_amax(const Params &p, float amx) {
 
 template <int EPI>
 __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int row, int nt, uint32_t taddr, int half,
-                                                 float dq, Stager &stg, int lane) {
+                                                 float dq, Stager &stg, int lane, int t) {
     const int row0 = row - lane;             // first row of this warp's block
     const bool block_ok = row0 < p.M;        // warp-uniform
     const bool row_ok = row < p.M;
     int oi, oy, oi2 = 0, oy2 = 0;
     out_index(p.out, pi, row0, oi, oy);
+    if (EPI == EPI_F32 && p.split_rows) {  // split-K partial of split t / tiles_per_split
+        oi = 0;
+        oy = ((t / p.tiles_per_split) * p.P + pi) * p.split_rows + row0;
+    }
     if (p.has_out2) out_index(p.out2, pi, row0, oi2, oy2);
     const __nv_bfloat16 *bias =
         p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
@@ -834,8 +850,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 tile_coords(p, t, pi, mt, nt);
                 const int m0 = mt * BM;
                 const int n0 = p.b_dual_off ? nt * (BN / 2) : nt * BN;
+                int kb0, kb1;
+                tile_kblocks(p, t, kb0, kb1);
                 for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
                             ok = false;
                             break;
@@ -898,8 +916,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * BN;
                 uint32_t accumulate = 0;
+                int kb0, kb1;
+                tile_kblocks(p, t, kb0, kb1);
                 for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(full0 + 8 * stage, phase, p)) {
                             ok = false;
                             break;
@@ -951,7 +971,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             const int row = mt * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
             if (p.out_tma)
-                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane);
+                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane, t);
             else
                 run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
             tc_fence_before();
@@ -1125,8 +1145,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 // B rows of this CTA: its half of the 256 tile columns, or for
                 // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
                 const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
+                int kb0, kb1;
+                tile_kblocks(p, t, kb0, kb1);
                 for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
                             ok = false;
                             break;
@@ -1187,8 +1209,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * BN;
                 uint32_t accumulate = 0;
+                int kb0, kb1;
+                tile_kblocks(p, t, kb0, kb1);
                 for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(full0 + 8 * stage, phase, p)) {
                             ok = false;
                             break;
@@ -1238,7 +1262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             const int row = mt * P_TILE_M + 128 * rank + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
             if (p.out_tma)
-                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane);
+                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane, t);
             else
                 run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
             tc_fence_before();

@@ -77,6 +77,7 @@ CASES = [
     (512, 256, 1024, 4, "gelu_tanh", False, False, True),
     (256, 256, 1024, 4, "swiglu", True, True, False),
     (2048, 1024, 8192, 8, "gelu_tanh", True, True, False),
+    (4096, 256, 512, 2, "gelu_tanh", True, False, False),  # split-K weight gradients
 ]
 
 

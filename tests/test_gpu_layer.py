@@ -7,8 +7,9 @@ add) against oracle/layer.py, through the C ABI (tp_layer_fwd / tp_layer_bwd).
   with the MLP's weights zeroed, so that Y - X = keep * b2 / (1 - p)).
 * Everything else is compared element by element with the fp64 oracle on
   ragged multi-tile sizes, the LayerNorm row widths of every kernel variant
-  (up to 8192 bf16 / 4096 fp32 columns), sequence parallelism and both GEMM
-  tilings: tolerance 1e-2 * max|ref| for bf16 (2^-8 relative storage
+  (a warp per row up to 1024 bf16 / 512 fp32 columns, then a block per row
+  with 1, 2 or 4 vectors per thread up to 8192 bf16 / 4096 fp32 columns),
+  sequence parallelism and both GEMM tilings: tolerance 1e-2 * max|ref| for bf16 (2^-8 relative storage
   rounding of Xn, pre, A, dPre, dXn plus fp32 sums), 1e-5 for fp32 and, for
   the FP8 MLP inside, 3e-2 against the FP8 oracle (the FP8 MLP's own bound).
 """
@@ -107,6 +108,8 @@ CASES = [
     (256, 256, 1024, 2, "gelu_tanh", "bf16", True, False, 0.0),
     (130, 4096, 512, 2, "gelu_tanh", "bf16", True, False, 0.25),
     (130, 8192, 256, 2, "swiglu", "bf16", False, False, 0.1),
+    (136, 2048, 256, 2, "gelu_tanh", "bf16", True, False, 0.1),
+    (72, 1024, 256, 2, "gelu_tanh", "f32", False, False, 0.2),
     (300, 272, 832, 4, "gelu_tanh", "f32", True, False, 0.1),
     (64, 4096, 256, 2, "gelu_tanh", "f32", True, False, 0.5),
     (96, 264, 512, 4, "swiglu", "f32", True, True, 0.1),

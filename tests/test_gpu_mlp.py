@@ -53,6 +53,9 @@ CASES = [
     (256, 256, 1024, 2, "gelu_tanh", "f32", True, False, False),
     (300, 264, 800, 4, "swiglu", "f32", True, True, False),
     (120, 72, 240, 3, "gelu_tanh", "f32", True, True, True),
+    # few weight-gradient tiles and many tokens: split-K weight gradients
+    (4100, 256, 512, 2, "gelu_tanh", "bf16", True, True, False),
+    (4096, 192, 640, 2, "swiglu", "bf16", False, False, True),
 ]
 
 
@@ -172,6 +175,26 @@ def test_deterministic_and_accumulate(tp, tile_mode):
     acc.bwd(run.dY, run.X, run.W1, run.W2, run.pre, run.A, run.dX, run.dW1, run.db1, run.dW2, run.db2, run.ws)
     assert tp.sync_status() == 0
     for a, b in zip(dW10, run.dW1):
+        assert torch.equal(2 * a, b)
+
+
+def test_split_k_weight_gradients_deterministic_and_accumulate(tp, tile_mode):
+    """dW through split-K (8 token splits of a 4100-token K; the reduction adds
+    the splits in order): run-to-run identical, and += with accumulation."""
+    lay = tp.TPMLP(S=2050, B=2, H=256, F=512, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    t = mlp_inputs(4100, 256, 512, 2, "gelu_tanh", "bf16")
+    run = MlpRun(lay, t)
+    run.fwd()
+    run.bwd()
+    dW10, dW20 = [d.clone() for d in run.dW1], [d.clone() for d in run.dW2]
+    run.bwd()
+    for a, b in zip(dW10 + dW20, run.dW1 + run.dW2):
+        assert torch.equal(a, b)
+    acc = tp.TPMLP(S=2050, B=2, H=256, F=512, T=2, act="gelu_tanh", dtype="bf16", has_bias=True,
+                   wgrad_accumulate=True)
+    acc.bwd(run.dY, run.X, run.W1, run.W2, run.pre, run.A, run.dX, run.dW1, run.db1, run.dW2, run.db2, run.ws)
+    assert tp.sync_status() == 0
+    for a, b in zip(dW10 + dW20, run.dW1 + run.dW2):
         assert torch.equal(2 * a, b)
 
 
