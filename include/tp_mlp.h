@@ -340,11 +340,13 @@ TP_API tp_status tp_set_tile_mode(int mode);
  * straight into the row GEMM, so A is never read back from HBM.  It takes
  * bf16 with act = none or GeLU-tanh, H a multiple of 64 up to 256 and F/T a
  * multiple of 64; other problems always use the two-kernel path.
- * Its parallelism is the token tiles, so TP_FUSED_AUTO (default) uses it for
- * those problems when M >= 64 x (SM count) (at least half the SMs get a
- * tile); TP_FUSED_ON uses it for every problem it takes, TP_FUSED_OFF never.
- * Both paths accumulate every output in fp32 over the same products; the
- * order of the additions differs.  Returns TP_ERR_ARG for an unknown mode. */
+ * Streaming all of W1 and W2 through shared memory once per 128-token tile
+ * keeps it slower than the two GEMM kernels (206 us against 136 us for 65536
+ * tokens at H = 256, F = 1024, T = 2 on GB300), so TP_FUSED_AUTO (default)
+ * and TP_FUSED_OFF run the two GEMM kernels and TP_FUSED_ON runs the fused
+ * kernel for every problem it takes.  pre and A are bit-identical between the
+ * paths; Y accumulates the same fp32 products in another order.  Returns
+ * TP_ERR_ARG for an unknown mode. */
 typedef enum { TP_FUSED_AUTO = 0, TP_FUSED_OFF = 1, TP_FUSED_ON = 2 } tp_fused_mode;
 TP_API tp_status tp_set_fused_fwd(int mode);
 

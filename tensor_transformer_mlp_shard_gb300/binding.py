@@ -470,9 +470,9 @@ FUSED_MODES = {"auto": 0, "off": 1, "on": 2}
 
 
 def set_fused_fwd(mode: str):
-    """Forward as one fused kernel for narrow bf16 MLPs (H <= 256): "auto"
-    (when the token tiles fill at least half the GPU), "on" (whenever the
-    shape allows it) or "off" (always the column and row GEMM kernels)."""
+    """Forward as one fused kernel for narrow bf16 MLPs (H <= 256): "on"
+    (whenever the shape allows it); "auto" and "off" run the column and row
+    GEMM kernels, which measure faster (see include/tp_mlp.h)."""
     _check(lib().tp_set_fused_fwd(FUSED_MODES[mode]))
 
 

@@ -765,9 +765,8 @@ static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const 
     if (d->dtype == TP_DT_FP8)
         return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop);
     const Dims x = dims_of(d);
-    const int mode = fused_fwd_mode();
-    if (mode != TP_FUSED_OFF && fused_fwd_supported(x.H, x.Fs, d->act, d->dtype) &&
-        (mode == TP_FUSED_ON || x.M >= 64ll * num_sms())) {
+    // the fused kernel only on request: measured slower than the two GEMMs
+    if (fused_fwd_mode() == TP_FUSED_ON && fused_fwd_supported(x.H, x.Fs, d->act, d->dtype)) {
         FusedPlan f;
         for (int j = 0; j < kMaxShards; ++j) {
             f.X[j] = j < x.nx ? X[j] : nullptr;

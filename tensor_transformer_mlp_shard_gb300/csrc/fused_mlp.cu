@@ -1,5 +1,5 @@
-// Fused MLP forward for narrow layers (the FlashFusedMLP idea of Megatron's
-// fusions/ package, "Megatron-LM 源码精读" s2 code map): one persistent
+// Fused MLP forward for narrow layers (Megatron's FlashFusedMLP,
+// "Megatron-LM 源码精读" s7, the fusions/ entry): one persistent
 // kernel per 128-token tile runs
 //   for every shard i and every 64-unit chunk c of shard i:
 //     acc1  = X_tile W1_i[c]^T                    (tcgen05, TMEM, N = 64)

@@ -1,6 +1,7 @@
 """GPU parity of the fused MLP forward (one kernel: column GEMM, bias,
 activation, row GEMM with A passed through shared memory; Megatron's
-FlashFusedMLP idea, "Megatron-LM 源码精读" s2 code map) through the C ABI.
+FlashFusedMLP, "Megatron-LM 源码精读" s7, the fusions/ entry) through the
+C ABI.
 
 * Against the fp64 oracle, element by element, on ragged multi-tile sizes,
   sequence parallelism, odd T, every H the kernel takes (64..256) and more
