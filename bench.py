@@ -268,13 +268,13 @@ def run_gpu(args, w, dist, rank, local, ws):
         dgamma = torch.empty(H, dtype=f32, device=dev)
         dbeta = torch.empty(H, dtype=f32, device=dev)
 
-        def step():
+        def step(X=X, dY=dY, Y=Y):
             lay.fwd(X, gamma, beta, W1, b1, W2, b2, LAYER_SEED, Y, Xn, mean, rstd, pre, A, workspace=wsp,
                     stream=stream)
             lay.bwd(dY, X, gamma, Xn, mean, rstd, W1, W2, pre, A, LAYER_SEED, dX, dgamma, dbeta, dW1, db1, dW2,
                     db2, wsp, stream=stream)
     else:
-        def step():
+        def step(X=X, dY=dY, Y=Y):
             lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp if w.dtype == "fp8" else None)
             lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
 
@@ -311,29 +311,57 @@ def run_gpu(args, w, dist, rank, local, ws):
     value = job_throughput(ws, flops_step, args.steps, ms_max)
 
     # ---- end to end through the C ABI with host buffers ---------------------
+    # Every step copies its X and dY from pinned host memory and its Y back.
+    # The copies run on a second stream into two alternating device buffer
+    # sets, so that step i's compute overlaps step i+1's inputs and step i-1's
+    # output (events order each copy against the compute that uses the set).
     hX = [x.cpu().pin_memory() for x in X]
     hdY = [d.cpu().pin_memory() for d in dY]
     hY = [torch.empty(rows, H, dtype=td).pin_memory() for _ in range(lay.nx)]
     h2d = sum(t.numel() * t.element_size() for t in hX + hdY)
     d2h = sum(t.numel() * t.element_size() for t in hY)
+    sets = [(X, dY, Y), ([torch.empty_like(x) for x in X], [torch.empty_like(d) for d in dY],
+                         [torch.empty_like(y) for y in Y])]
+    copy_stream = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for d, h in zip(X, hX):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(dY, hdY):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(hY, Y):
-            h.copy_(d, non_blocking=True)
+    def e2e_run(n):
+        """n steps; returns after enqueueing everything (compute stream last)."""
+        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        out_done = torch.cuda.Event()
+        copy_stream.wait_stream(stream)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+        def upload(k):
+            Xs, dYs, _ = sets[k % 2]
+            with torch.cuda.stream(copy_stream):
+                for d, h in zip(Xs, hX):
+                    d.copy_(h, non_blocking=True)
+                for d, h in zip(dYs, hdY):
+                    d.copy_(h, non_blocking=True)
+                in_ready[k % 2].record(copy_stream)
+
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                if i >= 1:
+                    copy_stream.wait_event(done[(i + 1) % 2])  # set (i+1)%2 last used by step i-1
+                upload(i + 1)
+            stream.wait_event(in_ready[i % 2])
+            step(*sets[i % 2])
+            done[i % 2].record(stream)
+            copy_stream.wait_event(done[i % 2])
+            with torch.cuda.stream(copy_stream):
+                for h, d in zip(hY, sets[i % 2][2]):
+                    h.copy_(d, non_blocking=True)
+                out_done.record(copy_stream)
+        stream.wait_event(out_done)
+
+    e2e_run(max(1, args.warmup))
     torch.cuda.synchronize()
     barrier(dist, local)
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e3.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(dist, e2.elapsed_time(e3), dev)
@@ -454,11 +482,18 @@ def run_reference(args, w, rank, block="mlp"):
 
 
 def cpu_baseline(w, block="mlp"):
-    tokens = 1024
-    full = synth.mlp_tensors(w, M=tokens)
+    """The oracle on host cores over a token sample sized to about 15 s of
+    work (a 512-token probe sets the size; at most the whole step)."""
+    probe = 512
+    full = synth.mlp_tensors(w)
+    dt, fl = oracle_sample(w, probe, full, block)
+    rate = fl / dt
+    per_token = fl / probe
+    tokens = int(min(w.M, max(probe, 15.0 * rate / per_token)) // 512 * 512)
     dt, fl = oracle_sample(w, tokens, full, block)
+    what = "the whole step" if tokens == w.M else f"the first {tokens} of {w.M} tokens"
     return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle fwd+bwd on the first {tokens} of {w.M} tokens with the full weights "
+            "sample": f"fp64 numpy oracle fwd+bwd on {what} with the full weights "
                       f"({fl / 1e9:.0f} GFLOP, {dt:.1f} s)"}
 
 

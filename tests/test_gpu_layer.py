@@ -223,3 +223,58 @@ def test_layer_empty_tokens_zero_the_gradients(tp):
     assert tp.sync_status() == 0
     for b in [run.dgamma, run.dbeta, run.db2, *run.dW1, *run.dW2, *run.db1]:
         assert torch.count_nonzero(b).item() == 0
+
+
+def test_layer_gpt_full_size_sampled(tp):
+    """The GPT workload (S=2048, B=4, H=4096, F=16384, T=8, GeLU, bias) in the
+    sub-block, in the launch configuration `bench.py --block layer` times
+    (dropout 0.1, the same seed), against the layer oracle evaluated where it
+    is exact on samples: token rows (Y, dX, pre, A through a per-row
+    LayerNorm, the row's dropout flags and the MLP rows), hidden units (dW1,
+    dW2, db1 over all tokens, from the full LayerNorm output and dZ) and db2
+    in full.  dgamma and dbeta need every row's dXn and are checked at the
+    mid sizes above."""
+    from test_gpu_full_size import sample_rows, sample_units, shard_inputs
+    w = synth.WORKLOADS["gpt"]
+    p, seed = 0.1, 0x5EED_0000_0001
+    lay = tp.TPLayer(S=w.S, B=w.B, H=w.H, F=w.F, T=w.T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
+                     dropout_p=p)
+    t = shard_inputs(w, synth.mlp_tensors(w))
+    lnp = synth.layer_tensors(1, w.H, w.dtype)
+    t["gamma"], t["beta"] = lnp["gamma"], lnp["beta"]
+    run = LayerRun(lay, t)
+    run.fwd(seed)
+    run.bwd(seed)
+    assert tp.sync_status() == 0
+    p = _p32(p)
+    M, H, T, Fs = w.M, w.H, w.T, w.F // w.T
+    X = np.asarray(t["X"], np.float64)
+    dY = np.asarray(t["dY"], np.float64)
+    # token rows
+    rows = sample_rows(M, T, False)
+    Xn_r, mean_r, rstd_r = olayer.layernorm_fwd(X[rows], t["gamma"], t["beta"])
+    keep_r = olayer.dropout_keep(seed, rows, H, p)
+    dZ_r = np.where(keep_r, dY[rows] / (1.0 - p), 0.0)
+    r = oracle.mlp_rows(np.arange(len(rows)), Xn_r, t["W1s"], t["b1s"], t["W2s"], t["b2"], dZ_r, w.act, False)
+    Y_r = X[rows] + np.where(keep_r, r["Y"] / (1.0 - p), 0.0)
+    dX_r = dY[rows] + olayer.layernorm_bwd(r["dX"], X[rows], t["gamma"], mean_r, rstd_r)[0]
+    errs = {"Y": rel_err(run.gathered(run.Y)[rows], Y_r), "dX": rel_err(run.gathered(run.dX)[rows], dX_r),
+            "Xn": rel_err(host(run.Xn)[rows], Xn_r)}
+    for i in range(T):
+        errs[f"pre{i}"] = rel_err(host(run.pre[i])[rows], r["pre"][i])
+        errs[f"A{i}"] = rel_err(host(run.A[i])[rows], r["A"][i])
+    # hidden units over all tokens
+    Xn = olayer.layernorm_fwd(X, t["gamma"], t["beta"])[0]
+    dZ = np.empty_like(dY)
+    for r0 in range(0, M, 1024):
+        rr = np.arange(r0, min(M, r0 + 1024))
+        dZ[rr] = np.where(olayer.dropout_keep(seed, rr, H, p), dY[rr] / (1.0 - p), 0.0)
+    units = sample_units(Fs, T)
+    u = oracle.mlp_units(units, Xn, t["W1s"], t["b1s"], t["W2s"], dZ, w.act)
+    for i in range(T):
+        errs[f"dW1_{i}"] = rel_err(host(run.dW1[i])[units[i]], u["dW1"][i])
+        errs[f"dW2_{i}"] = rel_err(host(run.dW2[i])[:, units[i]], u["dW2"][i])
+        errs[f"db1_{i}"] = rel_err(host(run.db1[i])[units[i]], u["db1"][i])
+    errs["db2"] = rel_err(host(run.db2), dZ.sum(axis=0))
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
