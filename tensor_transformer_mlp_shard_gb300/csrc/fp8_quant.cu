@@ -18,30 +18,59 @@
 
 namespace tpmlp {
 
+// Work split: every segment is cut into chunks of kChunkVec 16-byte vectors
+// and every block takes one chunk (block_start[k] = first block of segment
+// k), so the big segments (X, dY) and the small ones (weight shards) load
+// the GPU evenly; a thread keeps kUnroll loads in flight.
+constexpr int kQuantThreads = 256;
+constexpr int kUnroll = 8;
+constexpr long long kChunkVec = static_cast<long long>(kQuantThreads) * kUnroll * 4;  // 8192 vectors, 128 KB
+
 struct QuantParams {
     QuantSeg seg[kMaxQuantSegs];
+    int block_start[kMaxQuantSegs + 1];
+    int nseg;
     float *amax;
 };
 
-__global__ void __launch_bounds__(256) amax_kernel(const __grid_constant__ QuantParams p) {
-    const QuantSeg &sg = p.seg[blockIdx.y];
+// segment of block b and the block's index within it
+__device__ __forceinline__ int seg_of_block(const QuantParams &p, int b, int *lb) {
+    int k = 0;
+    while (k + 1 < p.nseg && b >= p.block_start[k + 1]) ++k;
+    *lb = b - p.block_start[k];
+    return k;
+}
+
+__device__ __forceinline__ float absmax8(const uint4 &w) {
+    const float a = fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))), fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y))));
+    const float b = fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))), fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w))));
+    return fmaxf(a, b);
+}
+
+__global__ void __launch_bounds__(kQuantThreads) amax_kernel(const __grid_constant__ QuantParams p) {
+    int lb;
+    const QuantSeg &sg = p.seg[seg_of_block(p, blockIdx.x, &lb)];
     const uint4 *in = static_cast<const uint4 *>(sg.in);
     const long long nv = sg.n / 8;
+    const long long v0 = lb * kChunkVec, v1 = min(nv, v0 + kChunkVec);
     float m = 0.0f;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
-        const uint4 w = in[i];
-        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))));
-        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y))));
-        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))));
-        m = fmaxf(m, fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w))));
+    for (long long base = v0 + threadIdx.x; base < v1; base += static_cast<long long>(kQuantThreads) * kUnroll) {
+        uint4 w[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long i = base + static_cast<long long>(u) * kQuantThreads;
+            w[u] = i < v1 ? in[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) m = fmaxf(m, absmax8(w[u]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[8];
+    __shared__ float red[kQuantThreads / 32];
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+        for (int w = 1; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
         atomicMax(reinterpret_cast<unsigned *>(p.amax + sg.slot), __float_as_uint(m));
     }
 }
@@ -52,21 +81,36 @@ __device__ __forceinline__ uint16_t to_fp8x2(float a, float b, int fmt) {
                            : __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
 }
 
-__global__ void __launch_bounds__(256) quant_kernel(const __grid_constant__ QuantParams p) {
-    const QuantSeg &sg = p.seg[blockIdx.y];
+__device__ __forceinline__ uint2 quant8(const uint4 &w, float s, int fmt) {
+    // x * scale is rounded to fp32 first, then to FP8
+    const float x0 = bf16_lo(w.x) * s, x1 = bf16_hi(w.x) * s, x2 = bf16_lo(w.y) * s, x3 = bf16_hi(w.y) * s;
+    const float x4 = bf16_lo(w.z) * s, x5 = bf16_hi(w.z) * s, x6 = bf16_lo(w.w) * s, x7 = bf16_hi(w.w) * s;
+    uint2 o;
+    o.x = uint32_t(to_fp8x2(x0, x1, fmt)) | (uint32_t(to_fp8x2(x2, x3, fmt)) << 16);
+    o.y = uint32_t(to_fp8x2(x4, x5, fmt)) | (uint32_t(to_fp8x2(x6, x7, fmt)) << 16);
+    return o;
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_kernel(const __grid_constant__ QuantParams p) {
+    int lb;
+    const QuantSeg &sg = p.seg[seg_of_block(p, blockIdx.x, &lb)];
     const float s = fp8_scale(p.amax[sg.slot], sg.fmt == FP8_E5M2 ? 57344.0f : 448.0f);
     const uint4 *in = static_cast<const uint4 *>(sg.in);
     uint2 *out = static_cast<uint2 *>(sg.out);
     const long long nv = sg.n / 8;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
-        const uint4 w = in[i];
-        // x * scale is rounded to fp32 first, then to FP8
-        const float x0 = bf16_lo(w.x) * s, x1 = bf16_hi(w.x) * s, x2 = bf16_lo(w.y) * s, x3 = bf16_hi(w.y) * s;
-        const float x4 = bf16_lo(w.z) * s, x5 = bf16_hi(w.z) * s, x6 = bf16_lo(w.w) * s, x7 = bf16_hi(w.w) * s;
-        uint2 o;
-        o.x = uint32_t(to_fp8x2(x0, x1, sg.fmt)) | (uint32_t(to_fp8x2(x2, x3, sg.fmt)) << 16);
-        o.y = uint32_t(to_fp8x2(x4, x5, sg.fmt)) | (uint32_t(to_fp8x2(x6, x7, sg.fmt)) << 16);
-        out[i] = o;
+    const long long v0 = lb * kChunkVec, v1 = min(nv, v0 + kChunkVec);
+    for (long long base = v0 + threadIdx.x; base < v1; base += static_cast<long long>(kQuantThreads) * kUnroll) {
+        uint4 w[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long i = base + static_cast<long long>(u) * kQuantThreads;
+            if (i < v1) w[u] = in[i];
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long i = base + static_cast<long long>(u) * kQuantThreads;
+            if (i < v1) out[i] = quant8(w[u], s, sg.fmt);
+        }
     }
 }
 
@@ -75,23 +119,24 @@ static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, flo
     if (nseg > kMaxQuantSegs) return set_error(TP_ERR_UNSUPPORTED, "too many quantisation segments (%d)", nseg);
     QuantParams prm;
     memset(&prm, 0, sizeof(prm));
-    long long maxn = 0;
+    long long blocks = 0;
     for (int i = 0; i < nseg; ++i) {
         if (segs[i].n % 8) return set_error(TP_ERR_SHAPE, "quantised buffer length %lld not a multiple of 8", segs[i].n);
         prm.seg[i] = segs[i];
-        maxn = segs[i].n > maxn ? segs[i].n : maxn;
+        prm.block_start[i] = static_cast<int>(blocks);
+        blocks += (segs[i].n / 8 + kChunkVec - 1) / kChunkVec;
     }
+    prm.block_start[nseg] = static_cast<int>(blocks);
+    prm.nseg = nseg;
     prm.amax = amax;
-    if (maxn == 0) return TP_OK;
-    const long long blocks = (maxn / 8 + 255) / 256;
-    const int gx = static_cast<int>(blocks < 1024 ? blocks : 1024);
-    dim3 grid(gx, nseg);
+    if (blocks == 0) return TP_OK;
+    if (blocks > (1ll << 31) - 1) return set_error(TP_ERR_SHAPE, "quantised tensor too large");
     const char *name = amax_pass ? "fp8_amax" : "fp8_quant";
     launch_begin(name, st);
     if (amax_pass)
-        amax_kernel<<<grid, 256, 0, st>>>(prm);
+        amax_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, st>>>(prm);
     else
-        quant_kernel<<<grid, 256, 0, st>>>(prm);
+        quant_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, st>>>(prm);
     cudaError_t e = cudaGetLastError();
     launch_end(name, st);
     return cuda_check(e, name);

@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from harness import TOL, dev, host, mlp_inputs, rel_err, split_tokens
 from oracle import layer as olayer
