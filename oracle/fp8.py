@@ -19,6 +19,11 @@ data-parallel group.  Readings (also in the design doc):
      pre, A, dPre, Y and dX are stored in bf16 (round-to-nearest-even), as in
      the bf16 variant, and act' uses the stored bf16 pre;
   F5 bias gradients sum the unquantised bf16 dPre and dY.
+  F6 delayed scaling (the pages' "amax history"): a tensor's scale may come
+     from the maximum of the amaxes its last n quantisations recorded (n = 1
+     is the previous step's amax) instead of from its own amax; while its
+     history is empty (the first step) it uses its own amax.  Every
+     quantisation records the tensor's own amax.  No margin.
 
 FP8 formats (OCP 8-bit floating point): E4M3 -- 1 sign, 4 exponent bits
 (bias 7), 3 mantissa bits, largest finite 448, smallest normal 2^-6, smallest
@@ -80,11 +85,37 @@ def amax_of(parts) -> np.float32:
                           for p in parts))
 
 
-def quantize(parts, fmt: str):
-    """Quantise every shard of one tensor with the tensor's scale.  Returns
-    (list of quantised values as fp64, scale)."""
-    s = scale_of(amax_of(parts), fmt)
+class AmaxHistory:
+    """Delayed scaling (F6): per tensor name, the amaxes of its last n
+    quantisations."""
+
+    def __init__(self, n: int):
+        if n < 1:
+            raise ValueError("history length must be >= 1")
+        self.n = n
+        self.hist = {}
+
+    def amax_for(self, name: str, amax):
+        """The amax the scale derives from: the history's maximum, or the
+        tensor's own amax while the history is empty."""
+        h = self.hist.get(name)
+        return np.float32(max(h)) if h else np.float32(amax)
+
+    def record(self, name: str, amax):
+        h = self.hist.setdefault(name, [])
+        h.append(np.float32(amax))
+        del h[:-self.n]
+
+
+def quantize(parts, fmt: str, name: str = None, history: "AmaxHistory" = None):
+    """Quantise every shard of one tensor with the tensor's scale (F1, F2),
+    or with the scale its amax history gives (F6) when ``history`` is set.
+    Returns (list of quantised values as fp64, scale)."""
+    a = amax_of(parts)
+    s = scale_of(history.amax_for(name, a) if history is not None else a, fmt)
     out = [round_fp8((np.asarray(p, np.float32) * s).astype(np.float32), fmt) for p in parts]
+    if history is not None:
+        history.record(name, a)
     return out, s
 
 
@@ -93,14 +124,15 @@ def dequant(sa, sb) -> float:
     return float(np.float32(1.0) / np.float32(np.float32(sa) * np.float32(sb)))
 
 
-def mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act: str, residual: bool):
+def mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act: str, residual: bool, history: AmaxHistory = None):
     """Forward of the FP8 variant.  X is the full [M, H] input (bf16 values).
     Returns a dict with pre, A (bf16-rounded, per shard), Y (fp64, before the
-    bf16 store), and the quantised operands and scales the backward reuses."""
+    bf16 store), and the quantised operands and scales the backward reuses.
+    ``history``: delayed scaling (F6) with this state, updated in place."""
     T = len(W1s)
-    (Xq,), sx = quantize([X], "e4m3")
-    W1q, sw1 = quantize(W1s, "e4m3")
-    W2q, sw2 = quantize(W2s, "e4m3")
+    (Xq,), sx = quantize([X], "e4m3", "X", history)
+    W1q, sw1 = quantize(W1s, "e4m3", "W1", history)
+    W2q, sw2 = quantize(W2s, "e4m3", "W2", history)
     d1 = dequant(sx, sw1)
     pre, A = [], []
     for i in range(T):
@@ -109,7 +141,7 @@ def mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act: str, residual: bool):
             p = p + np.asarray(b1s[i], np.float64)
         pre.append(round_bf16(p))
         A.append(round_bf16(_mlp.act_fwd(p, act)))
-    Aq, sa = quantize(A, "e4m3")
+    Aq, sa = quantize(A, "e4m3", "A", history)
     d2 = dequant(sa, sw2)
     Y = None
     for i in range(T):
@@ -124,16 +156,17 @@ def mlp_fwd_fp8(X, W1s, b1s, W2s, b2, act: str, residual: bool):
             "sx": sx, "sw1": sw1, "sw2": sw2, "sa": sa}
 
 
-def mlp_bwd_fp8(dY, f, act: str, residual: bool):
-    """Backward of the FP8 variant given the forward's dict ``f``."""
+def mlp_bwd_fp8(dY, f, act: str, residual: bool, history: AmaxHistory = None):
+    """Backward of the FP8 variant given the forward's dict ``f``
+    (``history`` as in mlp_fwd_fp8)."""
     T = len(f["W1q"])
-    (dYq,), sdy = quantize([dY], "e5m2")
+    (dYq,), sdy = quantize([dY], "e5m2", "dY", history)
     d = dequant(sdy, f["sw2"])
     dPre = []
     for i in range(T):
         dA = (dYq @ f["W2q"][i]) * d
         dPre.append(round_bf16(_mlp.act_bwd(f["pre"][i], dA, act)))
-    dPq, sdp = quantize(dPre, "e5m2")
+    dPq, sdp = quantize(dPre, "e5m2", "dPre", history)
     dW2 = [(dYq.T @ f["Aq"][i]) * dequant(sdy, f["sa"]) for i in range(T)]
     dW1 = [(dPq[i].T @ f["Xq"]) * dequant(sdp, f["sx"]) for i in range(T)]
     dX = None

@@ -119,3 +119,62 @@ def test_sampled_fp8_agrees_with_full(act):
         assert np.allclose(s["dW1"][i], gr["dW1"][i][sel], rtol=0, atol=1e-12)
         assert np.allclose(s["dW2"][i], gr["dW2"][i][:, units[i]], rtol=0, atol=1e-12)
         assert np.allclose(s["db1"][i], gr["db1"][i][sel], rtol=0, atol=1e-12)
+
+
+# ---- delayed scaling (F6: the pages' amax history) -------------------------
+
+def test_amax_history_window_and_empty_history():
+    h = fp8.AmaxHistory(3)
+    assert h.amax_for("X", 7.0) == np.float32(7.0)  # empty history: the tensor's own amax
+    for a in (1.0, 4.0, 2.0):
+        h.record("X", a)
+    assert h.amax_for("X", 100.0) == np.float32(4.0)  # max over the window, not the current amax
+    h.record("X", 0.5)  # 1.0 leaves the window of 3
+    assert h.hist["X"] == [np.float32(4.0), np.float32(2.0), np.float32(0.5)]
+    h.record("X", 0.25)
+    h.record("X", 0.125)  # 4.0 and 2.0 leave
+    assert h.amax_for("X", 9.0) == np.float32(0.5)
+    assert h.amax_for("W1", 3.0) == np.float32(3.0)  # tensors keep separate histories
+    with pytest.raises(ValueError):
+        fp8.AmaxHistory(0)
+
+
+def test_history_of_one_scales_by_the_previous_step_and_saturates():
+    rng = np.random.default_rng(3)
+    x1 = rng.normal(size=(64, 32)).astype(np.float32)
+    x2 = 2.0 * x1  # the tensor doubles between steps
+    h = fp8.AmaxHistory(1)
+    (q1,), s1 = fp8.quantize([x1], "e4m3", "X", h)
+    (q2,), s2 = fp8.quantize([x2], "e4m3", "X", h)
+    assert s1 == fp8.scale_of(fp8.amax_of([x1]), "e4m3")  # first step: current scaling
+    assert s2 == s1  # second step: the first step's amax
+    v = (x2 * s2).astype(np.float32)
+    assert np.array_equal(q2, fp8.round_fp8(v, "e4m3"))
+    # everything beyond fmax saturates to +-448; a current scale would have none
+    assert np.count_nonzero(np.abs(q2) == 448.0) >= np.count_nonzero(np.abs(v) > 448.0) > 0
+    assert h.hist["X"] == [fp8.amax_of([x2])]
+
+
+def test_delayed_scaling_on_repeated_inputs_equals_current_scaling():
+    """With the same tensors every step, the history's maximum is each
+    tensor's own amax, so from the first step on delayed scaling reproduces
+    current scaling exactly (and the first step always does)."""
+    rng = np.random.default_rng(5)
+    M, H, F, T = 48, 32, 64, 2
+    X = fp8.round_bf16(rng.normal(size=(M, H)))
+    W1s = [fp8.round_bf16(0.1 * rng.normal(size=(F // T, H))) for _ in range(T)]
+    W2s = [fp8.round_bf16(0.1 * rng.normal(size=(H, F // T))) for _ in range(T)]
+    b1s = [fp8.round_bf16(0.02 * rng.normal(size=F // T)) for _ in range(T)]
+    b2 = fp8.round_bf16(0.02 * rng.normal(size=H))
+    dY = fp8.round_bf16(rng.normal(size=(M, H)))
+    ref = fp8.mlp_fwd_fp8(X, W1s, b1s, W2s, b2, "gelu_tanh", True)
+    gref = fp8.mlp_bwd_fp8(dY, ref, "gelu_tanh", True)
+    h = fp8.AmaxHistory(2)
+    for _ in range(3):
+        f = fp8.mlp_fwd_fp8(X, W1s, b1s, W2s, b2, "gelu_tanh", True, h)
+        g = fp8.mlp_bwd_fp8(dY, f, "gelu_tanh", True, h)
+        assert np.array_equal(f["Y"], ref["Y"]) and np.array_equal(g["dX"], gref["dX"])
+        for a, b in zip(g["dW1"] + g["dW2"], gref["dW1"] + gref["dW2"]):
+            assert np.array_equal(a, b)
+    assert sorted(h.hist) == ["A", "W1", "W2", "X", "dPre", "dY"]
+    assert all(len(v) == 2 for v in h.hist.values())
