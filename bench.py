@@ -224,6 +224,8 @@ def run_gpu(args, w, dist, rank, local, ws):
     else:
         lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
                        residual=w.residual, seq_parallel=w.seq_parallel)
+    if w.dtype == "fp8" and not layer and args.fp8_history:
+        lay.set_fp8_history(args.fp8_history)
     full = synth.mlp_tensors(w)
     td = torch.float32 if w.dtype == "f32" else bf
 
@@ -511,6 +513,8 @@ def main():
     ap.add_argument("--block", default="mlp", choices=["mlp", "layer"],
                     help="layer: the TransformerLayer MLP sub-block, Y = X + dropout(MLP(LayerNorm(X))), "
                          f"p = {LAYER_DROPOUT_P}")
+    ap.add_argument("--fp8-history", type=int, default=0,
+                    help="FP8 delayed scaling over the last N amaxes of every operand (0: current scaling)")
     ap.add_argument("--fused", default="auto", choices=["auto", "on", "off"],
                     help="forward as one fused kernel for narrow MLPs (H <= 256): auto / on / off")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
@@ -532,6 +536,9 @@ def main():
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
               "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
               "tile_mode": args.tile_mode, "fused_fwd": args.fused}
+    if w.dtype == "fp8":
+        config["fp8_scaling"] = (f"delayed, amax history {args.fp8_history}" if args.fp8_history
+                                 else "current (each tensor's own amax)")
     if args.block == "layer":
         config["workload"] += f"; TransformerLayer MLP sub-block: LayerNorm -> MLP -> dropout(p={LAYER_DROPOUT_P})" \
                               " + residual"

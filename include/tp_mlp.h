@@ -149,6 +149,20 @@ TP_API tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *cons
                                void *const *Y, void *const *pre, void *const *A, void *workspace,
                                size_t workspace_bytes, void *stream);
 
+/* FP8 scaling recipe of a TP_DT_FP8 handle ("Megatron-LM 源码精读" s2, the
+ * fp8_utils.py entry: per-tensor scaling with an amax history).  n = 0
+ * (default): current scaling -- every tensor is scaled from its own amax, one
+ * extra read pass per tensor.  n = 1..64: delayed scaling -- each of X, W1,
+ * W2, A, dY, dPre is scaled from the maximum amax its last n quantisations
+ * recorded (n = 1: the previous call's), so the cast needs no amax pass (the
+ * cast reduces the amax it records as it goes); the first call after this one
+ * has no history and scales each tensor from its own amax.  Values beyond the
+ * range a stale scale covers saturate to +-fmax.  The history lives in the
+ * workspace: under delayed scaling every tp_mlp_fwd_ws / tp_mlp_bwd call of
+ * the handle must get the same workspace, untouched in between.  Calling this
+ * again clears the history.  Host only.  TP_ERR_ARG for n outside 0..64. */
+TP_API tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n);
+
 /* ---- MLP backward ------------------------------------------------------------
  * dY  : like Y;  X, W1, W2, pre, A: as passed to / produced by tp_mlp_fwd
  * dX  : like X (bf16/f32 per dtype)

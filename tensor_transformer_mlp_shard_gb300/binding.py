@@ -59,6 +59,7 @@ SIGNATURES = {
     "tp_mlp_workspace_bytes": (ctypes.c_size_t, [VP]),
     "tp_mlp_fwd": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP]),
     "tp_mlp_fwd_ws": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
+    "tp_mlp_set_fp8_history": (ctypes.c_int, [VP, ctypes.c_int]),
     "tp_mlp_bwd": (ctypes.c_int, [VP, PP, PP, PP, PP, PP, PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_col": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP]),
     "tp_linear_row": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP]),
@@ -209,6 +210,12 @@ class TPMLP(Layout):
 
     def workspace_bytes(self) -> int:
         return int(lib().tp_mlp_workspace_bytes(self._h))
+
+    def set_fp8_history(self, n: int):
+        """FP8 delayed scaling over the last n amaxes of every operand (0:
+        current scaling).  Clears the history; pass the same workspace to
+        every later fwd / bwd."""
+        _check(lib().tp_mlp_set_fp8_history(self._h, int(n)))
 
     def fwd(self, X, W1, b1, W2, b2, Y, pre, A, stream=None, workspace=None):
         """Forward; `workspace` (required for dtype "fp8") must then be passed,

@@ -29,6 +29,8 @@
 
 struct tp_mlp {
     tp_mlp_desc d;
+    int fp8_history = 0;  // 0: current scaling; n: delayed scaling over the last n amaxes
+    long long fp8_fwd_steps = 0, fp8_bwd_steps = 0;  // quantisations since the history was set
 };
 
 struct tp_layer {
@@ -454,8 +456,18 @@ static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes, size_
 // operands.  The forward fills Xq, W1q, W2q, Aq and their amax slots; the
 // backward reads them and fills dYq, dPq.
 enum { AMAX_X = 0, AMAX_W1, AMAX_W2, AMAX_A, AMAX_DY, AMAX_DP, AMAX_SLOTS = 8 };
+constexpr int kMaxFp8History = 64;
+// amax region: this step's amax per slot at +0, the amax each scale derives
+// from at +128 (delayed scaling; equal to the first under current scaling)
+constexpr size_t kScaleAmaxOff = 128;
 struct Fp8Layout {
-    size_t amax, xq, w1q, w1q_shard, w2q, w2q_shard, aq, aq_shard, dyq, dpq, dpq_shard, end;
+    size_t amax, hist, xq, w1q, w1q_shard, w2q, w2q_shard, aq, aq_shard, dyq, dpq, dpq_shard, end;
+};
+
+// Delayed scaling of one call: history length n (0: current scaling), the
+// valid history entries and the column this call's amaxes go to.
+struct Fp8Recipe {
+    int n = 0, fill = 0, pos = 0;
 };
 
 static Fp8Layout fp8_layout(const tp_mlp_desc *d) {
@@ -464,6 +476,8 @@ static Fp8Layout fp8_layout(const tp_mlp_desc *d) {
     size_t o = align256(bwd_ws_bytes(d, nullptr));
     L.amax = o;
     o += 256;
+    L.hist = o;  // [AMAX_SLOTS][kMaxFp8History] floats, kept between calls under delayed scaling
+    o += align256(sizeof(float) * AMAX_SLOTS * kMaxFp8History);
     L.xq = o;
     o += align256(size_t(x.M) * x.H);
     L.w1q_shard = align256(size_t(x.g) * x.Fs * x.H);
@@ -515,7 +529,8 @@ static void set_fp8(GemmPlan &g, int fa, int fb, const float *amax, int slot_a, 
 
 static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W1, const void *const *b1,
                          const void *const *W2, const void *b2, const void *const *R, void *const *Y,
-                         void *const *pre, void *const *A, void *ws, cudaStream_t st, const DropCfg *drop) {
+                         void *const *pre, void *const *A, void *ws, cudaStream_t st, const DropCfg *drop,
+                         const Fp8Recipe &rc) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
@@ -528,6 +543,13 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
         w2q[i] = base + L.w2q + i * L.w2q_shard;
         aq[i] = base + L.aq + i * L.aq_shard;
     }
+    // scales: under delayed scaling every GEMM dequantises with the amax its
+    // operand's scale came from (samax); under current scaling that is the
+    // tensor's own amax
+    const bool delayed = rc.n > 0;
+    float *samax = reinterpret_cast<float *>(base + L.amax + kScaleAmaxOff);
+    float *hist = reinterpret_cast<float *>(base + L.hist);
+    const float *sa = delayed ? samax : amax;
     // quantise X (E4M3; sequence shards are gathered into one buffer), W1, W2
     QuantSeg segs[kMaxQuantSegs];
     int n = 0;
@@ -536,7 +558,16 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
         segs[n++] = {X[j], static_cast<char *>(xq) + j * rows * x.H, (long long)(rows * x.H), AMAX_X, FP8_E4M3};
     for (int i = 0; i < x.T; ++i) segs[n++] = {W1[i], w1q[i], (long long)gw * x.H, AMAX_W1, FP8_E4M3};
     for (int i = 0; i < x.T; ++i) segs[n++] = {W2[i], w2q[i], (long long)x.H * x.Fs, AMAX_W2, FP8_E4M3};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    const int xw_slots[3] = {AMAX_X, AMAX_W1, AMAX_W2};
+    if (!delayed || rc.fill == 0) {
+        TRY(launch_fp8_quantize(segs, n, amax, true, st));  // amax pass, then the cast
+        if (delayed) TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, xw_slots, 3, 0, 0, false, st));
+    } else {
+        // one pass: scale from the history, this step's amax reduced on the way
+        TRY(cuda_check(cudaMemsetAsync(amax + AMAX_X, 0, 3 * sizeof(float), st), "cudaMemsetAsync(amax)"));
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, xw_slots, 3, rc.fill, 0, false, st));
+        TRY(launch_fp8_cast(segs, n, amax, samax, true, st));
+    }
     // column GEMM: pre_i = Xq W1q_i^T / (s_x s_w1) + b1_i, A_i = act(pre_i)
     bool a_fused = false;
     {
@@ -556,7 +587,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
         set_out(g.out, reinterpret_cast<const void *const *>(A), x.T, 1, 0, x.Fs);
         if (pre) set_out(g.out2, reinterpret_cast<const void *const *>(pre), x.T, 1, 0, gw);
         set_bias(g, d->has_bias ? b1 : nullptr, x.T, 1);
-        set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_X, AMAX_W1);
+        set_fp8(g, FP8_E4M3, FP8_E4M3, sa, AMAX_X, AMAX_W1);
         a_fused = tc_fused_epilogue(g);
         if (a_fused) {  // the epilogue reduces amax(A) as it stores A
             TRY(cuda_check(cudaMemsetAsync(amax + AMAX_A, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
@@ -567,7 +598,18 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     // quantise A (E4M3, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {A[i], aq[i], (long long)x.M * x.Fs, AMAX_A, FP8_E4M3};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st, a_fused));
+    const int a_slot[1] = {AMAX_A};
+    if (!delayed) {
+        TRY(launch_fp8_quantize(segs, n, amax, true, st, a_fused));
+    } else if (rc.fill == 0) {
+        if (!a_fused) TRY(launch_fp8_quantize(segs, n, amax, true, st));  // amax, then a cast from it
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, a_slot, 1, 0, 0, false, st));
+        if (a_fused) TRY(launch_fp8_cast(segs, n, amax, samax, false, st));
+    } else {
+        if (!a_fused) TRY(cuda_check(cudaMemsetAsync(amax + AMAX_A, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, a_slot, 1, rc.fill, 0, false, st));
+        TRY(launch_fp8_cast(segs, n, amax, samax, !a_fused, st));
+    }
     // row GEMM: Y = sum_i Aq_i W2q_i^T / (s_a s_w2) + b2 (+ R), optionally through dropout
     GemmPlan g;
     g.name = "row_fwd";
@@ -583,13 +625,19 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
     const void *bb[1] = {b2};
     set_bias(g, d->has_bias ? bb : nullptr, 1, 0);
-    set_fp8(g, FP8_E4M3, FP8_E4M3, amax, AMAX_A, AMAX_W2);
+    set_fp8(g, FP8_E4M3, FP8_E4M3, sa, AMAX_A, AMAX_W2);
     set_drop(g, drop);
-    return launch_tc_gemm(g, st);
+    TRY(launch_tc_gemm(g, st));
+    if (delayed) {  // this step's amaxes join the history
+        const int fwd_slots[4] = {AMAX_X, AMAX_W1, AMAX_W2, AMAX_A};
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, fwd_slots, 4, 0, rc.pos, true, st));
+    }
+    return TP_OK;
 }
 
 static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void *const *pre, void *const *dX,
-                         void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *ws, cudaStream_t st) {
+                         void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *ws, cudaStream_t st,
+                         const Fp8Recipe &rc) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
@@ -608,13 +656,25 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         dpq[i] = base + L.dpq + i * L.dpq_shard;
         dpre[i] = base + i * shard_bytes;
     }
+    const bool delayed = rc.n > 0;
+    float *samax = reinterpret_cast<float *>(base + L.amax + kScaleAmaxOff);
+    float *hist = reinterpret_cast<float *>(base + L.hist);
+    const float *sa = delayed ? samax : amax;  // the forward left samax for X, W1, W2, A
     // quantise dY (E5M2; sequence shards gathered)
     QuantSeg segs[kMaxQuantSegs];
     int n = 0;
     const size_t rows = x.rs ? x.rs : x.M;
     for (int j = 0; j < x.nx; ++j)
         segs[n++] = {dY[j], static_cast<char *>(dyq) + j * rows * x.H, (long long)(rows * x.H), AMAX_DY, FP8_E5M2};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st));
+    const int dy_slot[1] = {AMAX_DY}, dp_slot[1] = {AMAX_DP};
+    if (!delayed || rc.fill == 0) {
+        TRY(launch_fp8_quantize(segs, n, amax, true, st));
+        if (delayed) TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, dy_slot, 1, 0, 0, false, st));
+    } else {
+        TRY(cuda_check(cudaMemsetAsync(amax + AMAX_DY, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, dy_slot, 1, rc.fill, 0, false, st));
+        TRY(launch_fp8_cast(segs, n, amax, samax, true, st));
+    }
     const void *dya[1] = {dyq};
     const void *xa[1] = {xq};
     // row layer dgrad: dPre_i = (dYq W2q_i) / (s_dy s_w2) * act'(pre_i)
@@ -633,7 +693,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_operand(g.B, w2q, x.T, x.H, x.Fs, true, 1, 0, 0);
         set_out(g.out, dpre, x.T, 1, 0, gw);
         if (d->act != TP_ACT_NONE) set_out(g.aux, pre, x.T, 1, 0, gw);
-        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_W2);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DY, AMAX_W2);
         dp_fused = d->act != TP_ACT_NONE && tc_fused_epilogue(g);
         if (dp_fused) {  // the epilogue reduces amax(dPre) and the db1 partials
             TRY(cuda_check(cudaMemsetAsync(amax + AMAX_DP, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
@@ -645,7 +705,21 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
     // quantise dPre (E5M2, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {dpre[i], dpq[i], (long long)x.M * gw, AMAX_DP, FP8_E5M2};
-    TRY(launch_fp8_quantize(segs, n, amax, true, st, dp_fused));
+    if (!delayed) {
+        TRY(launch_fp8_quantize(segs, n, amax, true, st, dp_fused));
+    } else if (rc.fill == 0) {
+        if (!dp_fused) TRY(launch_fp8_quantize(segs, n, amax, true, st));
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, dp_slot, 1, 0, 0, false, st));
+        if (dp_fused) TRY(launch_fp8_cast(segs, n, amax, samax, false, st));
+    } else {
+        if (!dp_fused) TRY(cuda_check(cudaMemsetAsync(amax + AMAX_DP, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, dp_slot, 1, rc.fill, 0, false, st));
+        TRY(launch_fp8_cast(segs, n, amax, samax, !dp_fused, st));
+    }
+    if (delayed) {  // this step's amaxes join the history
+        const int bwd_slots[2] = {AMAX_DY, AMAX_DP};
+        TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, bwd_slots, 2, 0, rc.pos, true, st));
+    }
     // weight gradients (both operands MN-major over the tokens)
     {
         GemmPlan g;
@@ -664,7 +738,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             g.ksplit = wgrad_ksplit(x.H, x.Fs, x.T, x.M);
             g.split_ws = split;
         }
-        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DY, AMAX_A);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DY, AMAX_A);
         TRY(launch_tc_gemm(g, st));
     }
     {
@@ -684,7 +758,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             g.ksplit = wgrad_ksplit(gw, x.H, x.T, x.M);
             g.split_ws = split;
         }
-        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DP, AMAX_X);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DP, AMAX_X);
         TRY(launch_tc_gemm(g, st));
     }
     // column layer dgrad: dX = sum_i dPq_i W1q_i / (s_dp s_w1) (+ dY)
@@ -702,7 +776,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
         if (d->residual) set_out(g.aux, dY, x.nx, 0, x.rs, x.H);
         set_bias(g, nullptr, 0, 0);
-        set_fp8(g, FP8_E5M2, FP8_E4M3, amax, AMAX_DP, AMAX_W1);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DP, AMAX_W1);
         TRY(launch_tc_gemm(g, st));
     }
     if (d->has_bias) {
@@ -761,9 +835,9 @@ size_t tp_mlp_workspace_bytes(const tp_mlp *h) { return h ? mlp_ws_layout(&h->d,
 static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const void *const *W1,
                               const void *const *b1, const void *const *W2, const void *b2, const void *const *R,
                               void *const *Y, void *const *pre, void *const *A, void *workspace, const DropCfg *drop,
-                              cudaStream_t st) {
+                              cudaStream_t st, const Fp8Recipe &rc = Fp8Recipe()) {
     if (d->dtype == TP_DT_FP8)
-        return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop);
+        return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop, rc);
     const Dims x = dims_of(d);
     // the fused kernel only on request: measured slower than the two GEMMs
     if (fused_fwd_mode() == TP_FUSED_ON && fused_fwd_supported(x.H, x.Fs, d->act, d->dtype)) {
@@ -808,7 +882,7 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
                               const void *const *W1, const void *const *W2, const void *const *pre,
                               const void *const *A, void *const *dX, void *const *dW1, void *const *db1,
                               void *const *dW2, void *db2, void *workspace, cudaStream_t st,
-                              bool db2_done = false) {
+                              bool db2_done = false, const Fp8Recipe &rc = Fp8Recipe()) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     size_t shard_bytes = 0;
@@ -821,7 +895,7 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     }
     if (d->dtype == TP_DT_FP8)
         return fp8_bwd(d, dY, pre, dX, dW1, d->has_bias ? db1 : nullptr, dW2,
-                       (d->has_bias && !db2_done) ? db2 : nullptr, workspace, st);
+                       (d->has_bias && !db2_done) ? db2 : nullptr, workspace, st, rc);
     void *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
@@ -843,6 +917,16 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
         if (!db2_done) TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
+}
+
+// delayed-scaling state of the next call of a handle (steps: its quantisations so far)
+static Fp8Recipe fp8_recipe(const tp_mlp *h, long long steps) {
+    Fp8Recipe rc;
+    if (h->d.dtype != TP_DT_FP8 || h->fp8_history <= 0) return rc;
+    rc.n = h->fp8_history;
+    rc.fill = static_cast<int>(steps < rc.n ? steps : rc.n);
+    rc.pos = static_cast<int>(steps % rc.n);
+    return rc;
 }
 
 static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
@@ -870,8 +954,11 @@ static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const
     TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
     TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
     if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
-    return mlp_fwd_core(d, X, W1, b1, W2, b2, d->residual ? X : nullptr, Y, pre, A, workspace, nullptr,
-                        static_cast<cudaStream_t>(stream));
+    const Fp8Recipe rc = fp8_recipe(h, h->fp8_fwd_steps);
+    TRY(mlp_fwd_core(d, X, W1, b1, W2, b2, d->residual ? X : nullptr, Y, pre, A, workspace, nullptr,
+                     static_cast<cudaStream_t>(stream), rc));
+    if (d->dtype == TP_DT_FP8 && rc.n) ++h->fp8_fwd_steps;
+    return TP_OK;
 }
 
 tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *W1, const void *const *b1,
@@ -913,8 +1000,11 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
         return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
     if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
-    return mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace,
-                        static_cast<cudaStream_t>(stream));
+    const Fp8Recipe rc = fp8_recipe(h, h->fp8_bwd_steps);
+    TRY(mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace, static_cast<cudaStream_t>(stream),
+                     false, rc));
+    if (d->dtype == TP_DT_FP8 && rc.n && x.M > 0) ++h->fp8_bwd_steps;
+    return TP_OK;
 }
 
 tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
@@ -1284,6 +1374,14 @@ tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
 }
 
 uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    if (n < 0 || n > kMaxFp8History) return set_error(TP_ERR_ARG, "history length %d outside 0..%d", n, kMaxFp8History);
+    h->fp8_history = n;
+    h->fp8_fwd_steps = h->fp8_bwd_steps = 0;
+    return TP_OK;
+}
 
 tp_status tp_set_fused_fwd(int mode) {
     if (mode != TP_FUSED_AUTO && mode != TP_FUSED_OFF && mode != TP_FUSED_ON)

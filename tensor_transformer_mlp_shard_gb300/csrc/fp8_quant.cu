@@ -31,6 +31,8 @@ struct QuantParams {
     int block_start[kMaxQuantSegs + 1];
     int nseg;
     float *amax;
+    const float *scale_amax;  // cast: the amax the scale derives from (null: amax[slot])
+    int accumulate;           // cast: also reduce |x| into amax[slot] (one pass)
 };
 
 // segment of block b and the block's index within it
@@ -94,27 +96,89 @@ __device__ __forceinline__ uint2 quant8(const uint4 &w, float s, int fmt) {
 __global__ void __launch_bounds__(kQuantThreads) quant_kernel(const __grid_constant__ QuantParams p) {
     int lb;
     const QuantSeg &sg = p.seg[seg_of_block(p, blockIdx.x, &lb)];
-    const float s = fp8_scale(p.amax[sg.slot], sg.fmt == FP8_E5M2 ? 57344.0f : 448.0f);
+    const float s = fp8_scale(p.scale_amax ? p.scale_amax[sg.slot] : p.amax[sg.slot],
+                              sg.fmt == FP8_E5M2 ? 57344.0f : 448.0f);
     const uint4 *in = static_cast<const uint4 *>(sg.in);
     uint2 *out = static_cast<uint2 *>(sg.out);
     const long long nv = sg.n / 8;
     const long long v0 = lb * kChunkVec, v1 = min(nv, v0 + kChunkVec);
+    float m = 0.0f;
     for (long long base = v0 + threadIdx.x; base < v1; base += static_cast<long long>(kQuantThreads) * kUnroll) {
         uint4 w[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const long long i = base + static_cast<long long>(u) * kQuantThreads;
-            if (i < v1) w[u] = in[i];
+            w[u] = i < v1 ? in[i] : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const long long i = base + static_cast<long long>(u) * kQuantThreads;
             if (i < v1) out[i] = quant8(w[u], s, sg.fmt);
+            if (p.accumulate) m = fmaxf(m, absmax8(w[u]));
+        }
+    }
+    if (p.accumulate) {  // block-uniform
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __shared__ float red[kQuantThreads / 32];
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
+            atomicMax(reinterpret_cast<unsigned *>(p.amax + sg.slot), __float_as_uint(m));
         }
     }
 }
 
-static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, float *amax, cudaStream_t st) {
+// Amax history of delayed scaling, one thread per tensor slot: prepare
+// (scale_amax[s] = max of the first `fill` entries of row s of the history,
+// or amax[s] when fill is 0) or push (row s, column pos = amax[s]).
+struct HistParams {
+    float *hist;
+    float *scale_amax;
+    const float *amax;
+    int slots[8];
+    int nslots, fill, pos, push, ld;
+};
+
+__global__ void fp8_history_kernel(const __grid_constant__ HistParams p) {
+    const int k = threadIdx.x;
+    if (k >= p.nslots) return;
+    const int s = p.slots[k];
+    if (p.push) {
+        p.hist[s * p.ld + p.pos] = p.amax[s];
+        return;
+    }
+    float m = p.fill ? 0.0f : p.amax[s];
+    for (int i = 0; i < p.fill; ++i) m = fmaxf(m, p.hist[s * p.ld + i]);
+    p.scale_amax[s] = m;
+}
+
+tp_status launch_fp8_history(float *hist, int ld, float *scale_amax, const float *amax, const int *slots, int nslots,
+                             int fill, int pos, bool push, cudaStream_t st) {
+    if (nslots < 1 || nslots > 8 || fill < 0 || fill > ld || pos < 0 || pos >= ld)
+        return set_error(TP_ERR_ARG, "bad amax-history request");
+    HistParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.hist = hist;
+    prm.scale_amax = scale_amax;
+    prm.amax = amax;
+    for (int i = 0; i < nslots; ++i) prm.slots[i] = slots[i];
+    prm.nslots = nslots;
+    prm.fill = fill;
+    prm.pos = pos;
+    prm.push = push ? 1 : 0;
+    prm.ld = ld;
+    const char *name = push ? "fp8_history_push" : "fp8_history_scale";
+    launch_begin(name, st);
+    fp8_history_kernel<<<1, 32, 0, st>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    launch_end(name, st);
+    return cuda_check(e, name);
+}
+
+static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, float *amax, cudaStream_t st,
+                             const float *scale_amax = nullptr, bool accumulate = false) {
     if (nseg <= 0) return TP_OK;
     if (nseg > kMaxQuantSegs) return set_error(TP_ERR_UNSUPPORTED, "too many quantisation segments (%d)", nseg);
     QuantParams prm;
@@ -129,6 +193,8 @@ static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, flo
     prm.block_start[nseg] = static_cast<int>(blocks);
     prm.nseg = nseg;
     prm.amax = amax;
+    prm.scale_amax = scale_amax;
+    prm.accumulate = accumulate ? 1 : 0;
     if (blocks == 0) return TP_OK;
     if (blocks > (1ll << 31) - 1) return set_error(TP_ERR_SHAPE, "quantised tensor too large");
     const char *name = amax_pass ? "fp8_amax" : "fp8_quant";
@@ -140,6 +206,11 @@ static tp_status launch_pass(bool amax_pass, const QuantSeg *segs, int nseg, flo
     cudaError_t e = cudaGetLastError();
     launch_end(name, st);
     return cuda_check(e, name);
+}
+
+tp_status launch_fp8_cast(const QuantSeg *segs, int nseg, float *amax, const float *scale_amax, bool accumulate,
+                          cudaStream_t st) {
+    return launch_pass(false, segs, nseg, amax, st, scale_amax, accumulate);
 }
 
 tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st,

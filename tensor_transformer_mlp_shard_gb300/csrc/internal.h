@@ -118,6 +118,17 @@ constexpr int kMaxQuantSegs = 40;
 tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st,
                               bool amax_known = false);
 
+// One pass: out = fp8(in * scale), the scale from scale_amax[slot] (delayed
+// scaling) or amax[slot]; with accumulate, |in| is also reduced into
+// amax[slot] (zero it first).
+tp_status launch_fp8_cast(const QuantSeg *segs, int nseg, float *amax, const float *scale_amax, bool accumulate,
+                          cudaStream_t st);
+// Amax history [slot][ld] of delayed scaling: prepare scale_amax for the
+// slots (max of the first `fill` history entries, amax itself when fill is 0)
+// or push amax into column pos.
+tp_status launch_fp8_history(float *hist, int ld, float *scale_amax, const float *amax, const int *slots, int nslots,
+                             int fill, int pos, bool push, cudaStream_t st);
+
 // Launchers (return a tp_status).  They only enqueue work on `st`.
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
 bool tc_fused_epilogue(const GemmPlan &g);  // true when amax_out / col_partials are honoured

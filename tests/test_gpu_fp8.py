@@ -149,3 +149,47 @@ def test_fp8_gpt_full_size_sampled(tp):
         errs[f"db1_{i}"] = rel_err(host(run.db1[i])[units[i]], r["db1"][i])
     bad = {k: v for k, v in errs.items() if not v <= 3e-2}
     assert not bad, bad
+
+
+@pytest.mark.parametrize("n", [1, 3])
+def test_fp8_delayed_scaling_matches_oracle_over_steps(tp, n):
+    """Delayed scaling (amax history of length n) over four steps whose inputs
+    change scale (X x1, x1.6, x0.8, x1.2; dY x1, x0.5, x2, x1): every step's
+    outputs against the FP8 oracle driven by the same history (step 2 of the
+    n = 1 run saturates the X codes that outgrew the first step's scale)."""
+    M, H, F, T, act = 384, 256, 1024, 4, "gelu_tanh"
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act=act, dtype="fp8", has_bias=True, residual=True)
+    lay.set_fp8_history(n)
+    base = mlp_inputs(M, H, F, T, act, "fp8", has_bias=True)
+    hist = fp8.AmaxHistory(n)
+    run = MlpRun(lay, base)
+    for step, (sx, sdy) in enumerate([(1.0, 1.0), (1.6, 0.5), (0.8, 2.0), (1.2, 1.0)]):
+        t = dict(base)
+        t["X"] = fp8.round_bf16(base["X"] * sx).astype(np.float32)
+        t["dY"] = fp8.round_bf16(base["dY"] * sdy).astype(np.float32)
+        run.X[0].copy_(torch.from_numpy(t["X"]).to(torch.bfloat16))
+        run.dY[0].copy_(torch.from_numpy(t["dY"]).to(torch.bfloat16))
+        run.fwd()
+        run.bwd()
+        assert tp.sync_status() == 0
+        f = fp8.mlp_fwd_fp8(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, True, hist)
+        gr = fp8.mlp_bwd_fp8(t["dY"], f, act, True, hist)
+        errs = {"Y": rel_err(run.gathered(run.Y), f["Y"]), "dX": rel_err(run.gathered(run.dX), gr["dX"]),
+                "db2": rel_err(host(run.db2), gr["db2"])}
+        for i in range(T):
+            errs[f"A{i}"] = rel_err(host(run.A[i]), f["A"][i])
+            errs[f"dW1_{i}"] = rel_err(host(run.dW1[i]), gr["dW1"][i])
+            errs[f"dW2_{i}"] = rel_err(host(run.dW2[i]), gr["dW2"][i])
+            errs[f"db1_{i}"] = rel_err(host(run.db1[i]), gr["db1"][i])
+        bad = {k: v for k, v in errs.items() if not v <= 3e-2}
+        assert not bad, (step, bad)
+
+
+def test_fp8_history_setter_validates(tp):
+    lay = tp.TPMLP(S=64, B=2, H=256, F=1024, T=4, act="gelu_tanh", dtype="fp8")
+    for bad in (-1, 65):
+        with pytest.raises(tp.TpError) as e:
+            lay.set_fp8_history(bad)
+        assert e.value.status == 1
+    lay.set_fp8_history(0)
+    lay.set_fp8_history(64)
