@@ -569,7 +569,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
         TRY(launch_fp8_cast(segs, n, amax, samax, true, st));
     }
     // column GEMM: pre_i = Xq W1q_i^T / (s_x s_w1) + b1_i, A_i = act(pre_i)
-    bool a_fused = false;
+    bool a_fused = false, a_direct = false;
     {
         GemmPlan g;
         g.name = "col_fwd";
@@ -593,13 +593,25 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
             TRY(cuda_check(cudaMemsetAsync(amax + AMAX_A, 0, sizeof(float), st), "cudaMemsetAsync(amax)"));
             g.amax_out = amax + AMAX_A;
         }
+        if (delayed && rc.fill > 0 && a_fused && tc_writes_fp8(g)) {
+            // A's scale is known before A exists: the epilogue writes its codes too
+            const int a_slot[1] = {AMAX_A};
+            TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, a_slot, 1, rc.fill, 0, false, st));
+            g.q = true;
+            for (int i = 0; i < x.T; ++i) g.q_out[i] = aq[i];
+            g.q_fmt = FP8_E4M3;
+            g.q_scale_amax = samax + AMAX_A;
+            a_direct = true;
+        }
         TRY(launch_tc_gemm(g, st));
     }
     // quantise A (E4M3, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {A[i], aq[i], (long long)x.M * x.Fs, AMAX_A, FP8_E4M3};
     const int a_slot[1] = {AMAX_A};
-    if (!delayed) {
+    if (a_direct) {
+        // codes written by the column GEMM
+    } else if (!delayed) {
         TRY(launch_fp8_quantize(segs, n, amax, true, st, a_fused));
     } else if (rc.fill == 0) {
         if (!a_fused) TRY(launch_fp8_quantize(segs, n, amax, true, st));  // amax, then a cast from it
@@ -678,7 +690,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
     const void *dya[1] = {dyq};
     const void *xa[1] = {xq};
     // row layer dgrad: dPre_i = (dYq W2q_i) / (s_dy s_w2) * act'(pre_i)
-    bool dp_fused = false;
+    bool dp_fused = false, dp_direct = false;
     {
         GemmPlan g;
         g.name = d->act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
@@ -700,12 +712,23 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             g.amax_out = amax + AMAX_DP;
             if (d->has_bias) g.col_partials = partials;
         }
+        if (delayed && rc.fill > 0 && dp_fused && tc_writes_fp8(g)) {
+            // dPre's scale is known before dPre exists: the epilogue writes its codes too
+            TRY(launch_fp8_history(hist, kMaxFp8History, samax, amax, dp_slot, 1, rc.fill, 0, false, st));
+            g.q = true;
+            for (int i = 0; i < x.T; ++i) g.q_out[i] = dpq[i];
+            g.q_fmt = FP8_E5M2;
+            g.q_scale_amax = samax + AMAX_DP;
+            dp_direct = true;
+        }
         TRY(launch_tc_gemm(g, st));
     }
     // quantise dPre (E5M2, one scale over all shards)
     n = 0;
     for (int i = 0; i < x.T; ++i) segs[n++] = {dpre[i], dpq[i], (long long)x.M * gw, AMAX_DP, FP8_E5M2};
-    if (!delayed) {
+    if (dp_direct) {
+        // codes written by the row-layer dgrad
+    } else if (!delayed) {
         TRY(launch_fp8_quantize(segs, n, amax, true, st, dp_fused));
     } else if (rc.fill == 0) {
         if (!dp_fused) TRY(launch_fp8_quantize(segs, n, amax, true, st));

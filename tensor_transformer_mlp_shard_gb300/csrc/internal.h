@@ -73,6 +73,12 @@ struct GemmPlan {
     // col_partials[P][ceil(M/32)][out.ld] (the db1 partials).
     float *amax_out = nullptr;
     float *col_partials = nullptr;
+    // FP8 codes of the output written by the epilogue (tc_writes_fp8(g)):
+    // q_out[p] [M, out.ld] bytes, scale fmax(q_fmt) / *q_scale_amax
+    bool q = false;
+    void *q_out[kMaxShards];
+    int q_fmt = 0;
+    const float *q_scale_amax = nullptr;
     // EPI_F32 split-K (S == 1): the token (K) range is split `ksplit` ways,
     // every split writes fp32 partial tiles into split_ws
     // ([ksplit][P][roundup(M, 256)][N]) and a reduction adds them in split
@@ -132,6 +138,7 @@ tp_status launch_fp8_history(float *hist, int ld, float *scale_amax, const float
 // Launchers (return a tp_status).  They only enqueue work on `st`.
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
 bool tc_fused_epilogue(const GemmPlan &g);  // true when amax_out / col_partials are honoured
+bool tc_writes_fp8(const GemmPlan &g);      // true when q / q_out are honoured
 void set_tile_mode(int mode);  // TP_TILE_*
 tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);

@@ -119,6 +119,13 @@ void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
 
 bool tc_fused_epilogue(const GemmPlan &g) { return !g.accumulate && !(g.act == TP_ACT_SWIGLU && g.N % 32); }
 
+// FP8 codes from the epilogue: the column forward and the GeLU dgrad on the
+// bulk-store path (not SwiGLU, whose epilogues produce two halves per tile)
+bool tc_writes_fp8(const GemmPlan &g) {
+    return tc_fused_epilogue(g) && g.act != TP_ACT_SWIGLU &&
+           (g.kind == EPI_COL || (g.kind == EPI_DACT && g.act == TP_ACT_GELU_TANH));
+}
+
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     using namespace tc;
     const int ki = kernel_index(g.kind, g.A.mn_major, g.B.mn_major);
@@ -211,6 +218,16 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
             s = encode_out_maps(prm.mapO2, g.out2, g.out2.rows_split ? g.out2.rows_split : g.M,
                                 static_cast<int>(g.out2.ld), false);
             if (s != TP_OK) return s;
+        }
+        if (g.q && tc_writes_fp8(g)) {
+            for (int i = 0; i < g.out.n; ++i) {
+                s = encode_map_ex(&prm.mapQ[i], g.q_out[i], orows, ocols, g.out.ld, 32, 32,
+                                  CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+                if (s != TP_OK) return s;
+            }
+            prm.q_out = 1;
+            prm.q_fmt = g.q_fmt;
+            prm.q_scale_amax = g.q_scale_amax;
         }
     }
     prm.drop.on = g.dropout ? 1 : 0;

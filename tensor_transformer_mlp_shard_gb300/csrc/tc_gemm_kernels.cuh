@@ -18,6 +18,7 @@
 // the next tile accumulates into the other.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -81,6 +82,12 @@ struct Params {
     int act, b_dual_off, accumulate;
     uint32_t idesc;                  // tcgen05 instruction descriptor (formats, majors, M, N)
     DropoutParams drop;              // EPI_PLAIN: out = residual + dropout(acc + bias)
+    // FP8 codes of the bf16 output (A of the column forward, dPre of the act'
+    // dgrad) written by the epilogue when the scale is known in advance (FP8
+    // delayed scaling): codes = fp8(bf16(out) * fmax / *q_scale_amax)
+    CUtensorMap mapQ[kMaxShards];    // [rows, cols] bytes, boxes of 32 rows x 32 bytes
+    int q_out, q_fmt;
+    const float *q_scale_amax;
     float *amax_out;                 // bulk-store epilogue: atomic max |bf16 output| (A / dPre), or null
     float *col_partials;             // DACT bulk-store epilogue: per-32-row-block column sums, or null
     int partial_ld;                  //   [P][ceil(M/32)][partial_ld] floats
@@ -372,6 +379,54 @@ __device__ __forceinline__ void stage_store(Stager &st, const CUtensorMap *map, 
     }
 }
 
+// 32 FP8 codes of one row (32 bytes) staged as a 32-row x 32-byte block in
+// one of the warp's two 2 KB halves and written with one bulk tensor store
+__device__ __forceinline__ void stage_store_q(Stager &st, const CUtensorMap *map, int x, int y,
+                                              const uint4 (&wq)[2], int lane) {
+    const uint32_t buf = st.base + st.toggle * 2048u;
+    st.toggle ^= 1u;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t rowa = buf + static_cast<uint32_t>(lane) * 32u;
+    st_shared_v4(rowa, wq[0]);
+    st_shared_v4(rowa + 16u, wq[1]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, buf, x, y);
+        bulk_commit();
+    }
+}
+
+// FP8 codes of 32 bf16 values (packed in w) at scale s: fp32 product, then
+// round-to-nearest-even with saturation, as the quantiser does
+__device__ __forceinline__ void fp8_codes32(const uint4 (&w)[4], float s, int fmt, uint4 (&wq)[2]) {
+    uint32_t c[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t ws[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float2 a = make_float2(bf16_lo(ws[k]) * s, bf16_hi(ws[k]) * s);
+            const uint32_t v = fmt == FP8_E5M2 ? __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E5M2)
+                                               : __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+            lo |= v << (16 * k);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float2 a = make_float2(bf16_lo(ws[2 + k]) * s, bf16_hi(ws[2 + k]) * s);
+            const uint32_t v = fmt == FP8_E5M2 ? __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E5M2)
+                                               : __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+            hi |= v << (16 * k);
+        }
+        c[2 * j] = lo;
+        c[2 * j + 1] = hi;
+    }
+    wq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    wq[1] = make_uint4(c[4], c[5], c[6], c[7]);
+}
+
 __device__ __forceinline__ void pack_bf16x32(const float *v, uint4 (&w)[4]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -570,6 +625,11 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
             if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
             pack_bf16x32(v, w);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+            if (p.q_out) {
+                uint4 wq[2];
+                fp8_codes32(w, fp8_scale(*p.q_scale_amax, p.q_fmt == FP8_E5M2 ? 57344.0f : 448.0f), p.q_fmt, wq);
+                stage_store_q(stg, &p.mapQ[oi], col0, oy, wq, lane);
+            }
         } else if (EPI == EPI_PLAIN) {
             if (p.drop.on) {
                 const long long e0 = static_cast<long long>(row) * p.drop.ld + col0;
@@ -628,6 +688,12 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
                 pack_bf16x32(v, w);
                 stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+                if (p.q_out) {
+                    uint4 wq[2];
+                    fp8_codes32(w, fp8_scale(*p.q_scale_amax, p.q_fmt == FP8_E5M2 ? 57344.0f : 448.0f), p.q_fmt,
+                                wq);
+                    stage_store_q(stg, &p.mapQ[oi], col0, oy, wq, lane);
+                }
             }
         }
     }
