@@ -283,6 +283,11 @@ TP_API void tp_layer_destroy(tp_layer *h);
  * MLP's workspace, dZ and dXn ([M, H] each). */
 TP_API size_t tp_layer_workspace_bytes(const tp_layer *h);
 
+/* FP8 scaling recipe of a TP_DT_FP8 sub-block: as tp_mlp_set_fp8_history
+ * (the history lives in the sub-block's workspace, which every
+ * tp_layer_fwd / tp_layer_bwd call must then get, untouched in between). */
+TP_API tp_status tp_layer_set_fp8_history(tp_layer *h, int n);
+
 /* Forward.  X, Y: like tp_mlp_fwd's X and Y; gamma, beta: [H] (bf16, fp32 for
  * TP_DT_F32); W1, b1, W2, b2, pre, A: as in tp_mlp_fwd; seed: dropout key.
  * Outputs kept for the backward: Xn [M, H] (activation dtype), mean and rstd

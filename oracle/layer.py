@@ -125,13 +125,14 @@ def layer_bwd(dY, X, gamma, W1s, W2s, f, act: str, p: float):
     return g
 
 
-def layer_fwd_fp8(X, gamma, beta, W1s, b1s, W2s, b2, act: str, p: float, seed: int, eps: float = LN_EPS):
+def layer_fwd_fp8(X, gamma, beta, W1s, b1s, W2s, b2, act: str, p: float, seed: int, eps: float = LN_EPS,
+                  history=None):
     """The sub-block with the MLP in the FP8 variant (fp8.py): the LayerNorm
     output is stored in bf16 and that bf16 tensor is the MLP's input (reading
-    F4 of fp8.py applied to Xn)."""
+    F4 of fp8.py applied to Xn).  ``history``: delayed scaling (fp8.py F6)."""
     Xn, mean, rstd = layernorm_fwd(X, gamma, beta, eps)
     Xn_b = _fp8.round_bf16(Xn)
-    f = _fp8.mlp_fwd_fp8(Xn_b, W1s, b1s, W2s, b2, act, False)
+    f = _fp8.mlp_fwd_fp8(Xn_b, W1s, b1s, W2s, b2, act, False, history)
     Z = f["Y"]
     keep = dropout_keep(seed, np.arange(Z.shape[0]), Z.shape[1], p)
     Y = np.asarray(X, np.float64) + np.where(keep, Z / (1.0 - p), 0.0)
@@ -139,12 +140,12 @@ def layer_fwd_fp8(X, gamma, beta, W1s, b1s, W2s, b2, act: str, p: float, seed: i
             "mlp": f}
 
 
-def layer_bwd_fp8(dY, X, gamma, act: str, p: float, f):
+def layer_bwd_fp8(dY, X, gamma, act: str, p: float, f, history=None):
     """Backward of layer_fwd_fp8: dZ and dXn are stored in bf16 (F4), the MLP
     backward is fp8.mlp_bwd_fp8 on dZ."""
     dY = np.asarray(dY, np.float64)
     dZ = _fp8.round_bf16(np.where(f["keep"], dY / (1.0 - p), 0.0))
-    g = _fp8.mlp_bwd_fp8(dZ, f["mlp"], act, False)
+    g = _fp8.mlp_bwd_fp8(dZ, f["mlp"], act, False, history)
     dXn = _fp8.round_bf16(g["dX"])
     dXln, dgamma, dbeta = layernorm_bwd(dXn, X, gamma, f["mean"], f["rstd"])
     g.update(dZ=dZ, dXn=dXn, dX=dY + dXln, dgamma=dgamma, dbeta=dbeta)

@@ -70,6 +70,7 @@ SIGNATURES = {
     "tp_layer_create": (ctypes.c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(VP)]),
     "tp_layer_destroy": (None, [VP]),
     "tp_layer_workspace_bytes": (ctypes.c_size_t, [VP]),
+    "tp_layer_set_fp8_history": (ctypes.c_int, [VP, ctypes.c_int]),
     "tp_layer_fwd": (ctypes.c_int, [VP, PP, VP, VP, PP, PP, PP, VP, ctypes.c_uint64, PP, VP, VP, VP, PP, PP, VP,
                                     ctypes.c_size_t, VP]),
     "tp_layer_bwd": (ctypes.c_int, [VP, PP, PP, VP, VP, VP, VP, PP, PP, PP, PP, ctypes.c_uint64, PP, VP, VP, PP,
@@ -280,6 +281,11 @@ class TPLayer(Layout):
 
     def workspace_bytes(self) -> int:
         return int(lib().tp_layer_workspace_bytes(self._h))
+
+    def set_fp8_history(self, n: int):
+        """FP8 delayed scaling over the last n amaxes (0: current scaling); as
+        TPMLP.set_fp8_history."""
+        _check(lib().tp_layer_set_fp8_history(self._h, int(n)))
 
     def fwd(self, X, gamma, beta, W1, b1, W2, b2, seed, Y, Xn, mean, rstd, pre, A, workspace=None, stream=None):
         c, T, H, Fs, g, M = self._c, self.T, self.H, self.Fs, self.g, self.M

@@ -38,6 +38,8 @@ struct tp_layer {
     tp_mlp_desc inner;  // the MLP inside the sub-block: d.mlp with the residual handled by the block
     uint32_t drop_threshold;
     float drop_scale;
+    int fp8_history = 0;  // as tp_mlp
+    long long fp8_fwd_steps = 0, fp8_bwd_steps = 0;
 };
 
 namespace tpmlp {
@@ -942,11 +944,11 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     return TP_OK;
 }
 
-// delayed-scaling state of the next call of a handle (steps: its quantisations so far)
-static Fp8Recipe fp8_recipe(const tp_mlp *h, long long steps) {
+// delayed-scaling state of a handle's next call (steps: its quantisations so far)
+static Fp8Recipe fp8_recipe(int dtype, int history, long long steps) {
     Fp8Recipe rc;
-    if (h->d.dtype != TP_DT_FP8 || h->fp8_history <= 0) return rc;
-    rc.n = h->fp8_history;
+    if (dtype != TP_DT_FP8 || history <= 0) return rc;
+    rc.n = history;
     rc.fill = static_cast<int>(steps < rc.n ? steps : rc.n);
     rc.pos = static_cast<int>(steps % rc.n);
     return rc;
@@ -977,7 +979,7 @@ static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const
     TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
     TRY(check_array(reinterpret_cast<const void *const *>(A), x.T, "A"));
     if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
-    const Fp8Recipe rc = fp8_recipe(h, h->fp8_fwd_steps);
+    const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_fwd_steps);
     TRY(mlp_fwd_core(d, X, W1, b1, W2, b2, d->residual ? X : nullptr, Y, pre, A, workspace, nullptr,
                      static_cast<cudaStream_t>(stream), rc));
     if (d->dtype == TP_DT_FP8 && rc.n) ++h->fp8_fwd_steps;
@@ -1023,7 +1025,7 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
         return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
     if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
-    const Fp8Recipe rc = fp8_recipe(h, h->fp8_bwd_steps);
+    const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_bwd_steps);
     TRY(mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace, static_cast<cudaStream_t>(stream),
                      false, rc));
     if (d->dtype == TP_DT_FP8 && rc.n && x.M > 0) ++h->fp8_bwd_steps;
@@ -1289,7 +1291,10 @@ tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, con
     dc.threshold = h->drop_threshold;
     dc.scale = h->drop_scale;
     dc.seed = seed;
-    return mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st);
+    const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_fwd_steps);
+    TRY(mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st, rc));
+    if (rc.n) ++h->fp8_fwd_steps;
+    return TP_OK;
 }
 
 tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X, const void *gamma, const void *Xn,
@@ -1359,7 +1364,9 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
     void *xn[kMaxShards], *dxn[kMaxShards];
     split_rows(const_cast<void *>(Xn), x, xn);
     split_rows(base + L.dxn, x, dxn);
-    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st, dropout));
+    const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_bwd_steps);
+    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st, dropout, rc));
+    if (rc.n) ++h->fp8_bwd_steps;
     // LayerNorm backward plus the residual branch: dX = dY + LN'(dXn); partials reuse the dZ region
     lp.dxn = base + L.dxn;
     lp.mean = const_cast<float *>(mean);
@@ -1399,6 +1406,14 @@ tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
 uint64_t tp_launch_count(void) { return g_launches.load(); }
 
 tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    if (n < 0 || n > kMaxFp8History) return set_error(TP_ERR_ARG, "history length %d outside 0..%d", n, kMaxFp8History);
+    h->fp8_history = n;
+    h->fp8_fwd_steps = h->fp8_bwd_steps = 0;
+    return TP_OK;
+}
+
+tp_status tp_layer_set_fp8_history(tp_layer *h, int n) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
     if (n < 0 || n > kMaxFp8History) return set_error(TP_ERR_ARG, "history length %d outside 0..%d", n, kMaxFp8History);
     h->fp8_history = n;

@@ -279,3 +279,33 @@ def test_layer_gpt_full_size_sampled(tp):
     errs["db2"] = rel_err(host(run.db2), dZ.sum(axis=0))
     bad = {k: v for k, v in errs.items() if not v <= 1e-2}
     assert not bad, bad
+
+
+def test_layer_fp8_delayed_scaling_over_steps(tp):
+    """The FP8 sub-block with an amax history of 2 over three steps whose
+    input grows (x1, x1.5, x0.75) against the FP8 layer oracle driven by the
+    same history."""
+    from oracle import fp8
+    M, H, F, T, act, p = 384, 256, 1024, 4, "gelu_tanh", 0.1
+    lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act=act, dtype="fp8", has_bias=True, dropout_p=p)
+    lay.set_fp8_history(2)
+    base = layer_inputs(M, H, F, T, act, "fp8", True, seed_off=9)
+    hist = fp8.AmaxHistory(2)
+    run = LayerRun(lay, base)
+    for step, sx in enumerate((1.0, 1.5, 0.75)):
+        t = dict(base)
+        t["X"] = fp8.round_bf16(base["X"] * sx).astype(np.float32)
+        run.X[0].copy_(torch.from_numpy(t["X"]).to(torch.bfloat16))
+        run.fwd(SEED + step)
+        run.bwd(SEED + step)
+        assert tp.sync_status() == 0
+        f = olayer.layer_fwd_fp8(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act,
+                                 _p32(p), SEED + step, history=hist)
+        gr = olayer.layer_bwd_fp8(t["dY"], t["X"], t["gamma"], act, _p32(p), f, history=hist)
+        errs = {"Y": rel_err(run.gathered(run.Y), f["Y"]), "dX": rel_err(run.gathered(run.dX), gr["dX"]),
+                "dgamma": rel_err(host(run.dgamma), gr["dgamma"]), "db2": rel_err(host(run.db2), gr["db2"])}
+        for i in range(T):
+            errs[f"dW1_{i}"] = rel_err(host(run.dW1[i]), gr["dW1"][i])
+            errs[f"dW2_{i}"] = rel_err(host(run.dW2[i]), gr["dW2"][i])
+        bad = {k: v for k, v in errs.items() if not v <= 3e-2}
+        assert not bad, (step, bad)
