@@ -6,7 +6,7 @@ code with the CUDA path.
 Source: "Megatron-LM 源码精读——大模型并行训练全景" (roger-lv.github.io), s8.2
 (mixed precision / FP8): E4M3 in the forward, E5M2 in the backward, per-tensor
 scaling from the tensor's amax, with the amax reduced across the tensor- and
-data-parallel group.  Readings (also in the design doc):
+data-parallel group.  Readings:
   F1 one scale per logical tensor: the amax is the maximum over all T shards
      (the cross-shard amax all-reduce), scale = fmax / amax computed in fp32
      (1 when amax is 0), fmax = 448 (E4M3) or 57344 (E5M2);

@@ -15,7 +15,7 @@ MLP half of that layer:
                                               inside the dropout, the residual
                                               is the block's input X
 
-Readings (also in DESIGN.md):
+Readings:
   L1 LayerNorm with the population variance, eps = 1e-5, affine gamma/beta;
   L2 dropout keeps an element when its 24-bit uniform draw u24 satisfies
      u24 >= floor(p * 2^24) and scales kept elements by 1/(1-p);

@@ -18,7 +18,7 @@ Sources (page titles; sections / figures on them):
        add), s06 Sequence Parallel.
   [P4] "megatron-docs" table of contents: "f-g 共轭算子", "SwiGLU MLP".
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
   R1 weights use the PyTorch [out, in] layout and Y = X W^T ([P1] s3.1 note on
      the stored shape; s3.2's W_i in R^{out x in/T} is only consistent with it).
   R2 GeLU is the tanh form 0.5x(1+tanh(sqrt(2/pi)(x+0.044715x^3))).

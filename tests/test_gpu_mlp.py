@@ -233,3 +233,45 @@ def test_binding_rejects_wrong_shapes(tp):
         lay.fwd(run.X, run.W1[:1], run.b1, run.W2, run.b2, run.Y, run.pre, run.A)
     with pytest.raises(ValueError):
         lay.fwd([run.X[0][:100]], run.W1, run.b1, run.W2, run.b2, run.Y, run.pre, run.A)
+
+
+@pytest.mark.parametrize("bias", [False, True])
+def test_single_layer_backward_with_split_k(tp, bias):
+    """tp_linear_col_bwd / tp_linear_row_bwd where the weight gradient splits
+    its 4100 tokens (2 output tiles per layer): the caller workspace carries
+    the bias partials and the split partials side by side."""
+    M, H, F, T = 4100, 256, 512, 2
+    Fs = F // T
+    g = torch.Generator().manual_seed(21)
+    bf, f32 = torch.bfloat16, torch.float32
+    rnd = lambda *s, sc=1.0: (torch.randn(*s, generator=g) * sc).to(bf)
+    X, dOut, W = rnd(M, H), [rnd(M, Fs) for _ in range(T)], [rnd(Fs, H, sc=0.05) for _ in range(T)]
+    colL = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="bf16", has_bias=bias)
+    ws = tp.alloc_workspace(tp.linear_workspace_bytes(colL))
+    dX = torch.empty(M, H, dtype=bf, device="cuda")
+    dW = [torch.empty(Fs, H, dtype=f32, device="cuda") for _ in range(T)]
+    db = [torch.empty(Fs, dtype=f32, device="cuda") for _ in range(T)] if bias else None
+    tp.linear_col_bwd(colL, [d.cuda() for d in dOut], [X.cuda()], [w.cuda() for w in W], [dX], dW, db, ws)
+    rowL = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="bf16", has_bias=bias)
+    dY, Xr, W2 = rnd(M, H), [rnd(M, Fs) for _ in range(T)], [rnd(H, Fs, sc=0.05) for _ in range(T)]
+    ws2 = tp.alloc_workspace(tp.linear_workspace_bytes(rowL))
+    dXr = [torch.empty(M, Fs, dtype=bf, device="cuda") for _ in range(T)]
+    dW2 = [torch.empty(H, Fs, dtype=f32, device="cuda") for _ in range(T)]
+    db2 = torch.empty(H, dtype=f32, device="cuda") if bias else None
+    tp.linear_row_bwd(rowL, [dY.cuda()], [x.cuda() for x in Xr], [w.cuda() for w in W2], dXr, dW2, db2, ws2)
+    assert tp.sync_status() == 0
+    n = lambda t: t.float().numpy()
+    rdX, rdW, rdb = oracle.column_bwd([n(d) for d in dOut], n(X), [n(w) for w in W])
+    errs = {"dX": rel_err(host(dX), rdX)}
+    for i in range(T):
+        errs[f"dW{i}"] = rel_err(host(dW[i]), rdW[i])
+        if bias:
+            errs[f"db{i}"] = rel_err(host(db[i]), rdb[i])
+    qdX, qdW, qdb = oracle.row_bwd(n(dY), [n(x) for x in Xr], [n(w) for w in W2])
+    for i in range(T):
+        errs[f"row_dX{i}"] = rel_err(host(dXr[i]), qdX[i])
+        errs[f"row_dW{i}"] = rel_err(host(dW2[i]), qdW[i])
+    if bias:
+        errs["row_db"] = rel_err(host(db2), qdb)
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
