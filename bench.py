@@ -260,7 +260,12 @@ def run_gpu(args, w, dist, rank, local, ws):
     db1 = [torch.empty(g * Fs, dtype=f32, device=dev) for _ in range(T)] if w.has_bias else None
     db2 = torch.empty(H, dtype=f32, device=dev) if w.has_bias else None
     wsp = tp.alloc_workspace(lay.workspace_bytes(), device=dev)
-    stream = torch.cuda.current_stream(dev)
+    # all work on one non-default stream (a CUDA graph cannot capture the legacy stream)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    # the end-to-end loop alternates two device buffer sets for X, dY, Y
+    e2e_sets = [(X, dY, Y), ([torch.empty_like(x) for x in X], [torch.empty_like(d) for d in dY],
+                             [torch.empty_like(y) for y in Y])]
     if layer:
         lnp = synth.layer_tensors(1, H, w.dtype)
         gamma, beta = up(lnp["gamma"]), up(lnp["beta"])
@@ -286,6 +291,21 @@ def run_gpu(args, w, dist, rank, local, ws):
     torch.cuda.synchronize()
     if tp.sync_status(stream) != 0:
         raise RuntimeError("device status not OK after warm-up")
+    graph_launches = 0
+    if args.graph:
+        # one step per graph and input set (the e2e loop alternates two sets)
+        eager_step = step
+        graphs = []
+        n_before = tp.launch_count()
+        for k in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                eager_step() if k == 0 else eager_step(*e2e_sets[1])
+            graphs.append(g)
+        graph_launches = (tp.launch_count() - n_before) // 2
+
+        def step(X_=None, dY_=None, Y_=None):
+            graphs[0 if X_ is None or X_ is X else 1].replay()
     clocks = ClockSampler(local)
     clocks.start()
     tp.prof_enable(True)
@@ -301,7 +321,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     torch.cuda.synchronize()
     barrier(dist, local)
     ms = e0.elapsed_time(e1)
-    launches = tp.launch_count() - n0
+    launches = tp.launch_count() - n0 if not args.graph else graph_launches * args.steps
     kernels = tp.prof_collect()
     tp.prof_enable(False)
     clk = clocks.stop()
@@ -322,8 +342,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     hY = [torch.empty(rows, H, dtype=td).pin_memory() for _ in range(lay.nx)]
     h2d = sum(t.numel() * t.element_size() for t in hX + hdY)
     d2h = sum(t.numel() * t.element_size() for t in hY)
-    sets = [(X, dY, Y), ([torch.empty_like(x) for x in X], [torch.empty_like(d) for d in dY],
-                         [torch.empty_like(y) for y in Y])]
+    sets = e2e_sets
     copy_stream = torch.cuda.Stream(dev)
 
     def e2e_run(n):
@@ -513,6 +532,8 @@ def main():
     ap.add_argument("--block", default="mlp", choices=["mlp", "layer"],
                     help="layer: the TransformerLayer MLP sub-block, Y = X + dropout(MLP(LayerNorm(X))), "
                          f"p = {LAYER_DROPOUT_P}")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step from a CUDA graph captured after the warm-up (no host launch cost)")
     ap.add_argument("--fp8-history", type=int, default=0,
                     help="FP8 delayed scaling over the last N amaxes of every operand (0: current scaling)")
     ap.add_argument("--fused", default="auto", choices=["auto", "on", "off"],
@@ -535,7 +556,8 @@ def main():
               "S": w.S, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "act": w.act, "global_batch": w.B * ws,
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
               "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
-              "tile_mode": args.tile_mode, "fused_fwd": args.fused}
+              "tile_mode": args.tile_mode, "fused_fwd": args.fused,
+              "launch": "CUDA graph replay per step" if args.graph else "eager C-ABI calls per step"}
     if w.dtype == "fp8":
         config["fp8_scaling"] = (f"delayed, amax history {args.fp8_history}" if args.fp8_history
                                  else "current (each tensor's own amax)")
