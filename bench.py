@@ -147,6 +147,10 @@ class ClockSampler:
 def kernel_flops(w):
     """Algorithmic FLOP of one launch of each GEMM kernel for workload w."""
     M, H, F, g = w.M, w.H, w.F, w.g
+    if w.kind == "attn_proj":  # QKV column layer (F = 3H) and output row layer (F_o -> H)
+        Fo = w.F_o
+        return {"col_fwd": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F, "col_dgrad": 2.0 * M * F * H,
+                "row_fwd": 2.0 * M * Fo * H, "row_dgrad": 2.0 * M * H * Fo, "wgrad_row": 2.0 * M * H * Fo}
     return {"col_fwd": 2.0 * M * H * F * g, "row_fwd": 2.0 * M * F * H, "row_dgrad_act": 2.0 * M * H * F,
             "wgrad_row": 2.0 * M * H * F, "wgrad_col": 2.0 * M * H * F * g, "col_dgrad": 2.0 * M * F * g * H,
             "fused_mlp_fwd": 2.0 * M * H * F * g + 2.0 * M * F * H}
@@ -159,6 +163,11 @@ def gemm_bytes(w):
     decides which roof bounds the kernel."""
     M, H, F, g = w.M, w.H, w.F, w.g
     e = 2
+    if w.kind == "attn_proj":
+        Fo = w.F_o
+        return {"col_fwd": e * (M * H + F * H + M * F), "wgrad_col": e * (M * F + M * H) + 4 * F * H,
+                "col_dgrad": e * (M * F + F * H + M * H), "row_fwd": e * (M * Fo + H * Fo + M * H),
+                "row_dgrad": e * (M * H + H * Fo + M * Fo), "wgrad_row": e * (M * H + M * Fo) + 4 * H * Fo}
     res = M * H * e if w.residual else 0
     return {"col_fwd": e * (M * H + g * F * H + M * g * F + M * F),
             "row_fwd": e * (M * F + H * F + M * H) + res,
@@ -167,6 +176,17 @@ def gemm_bytes(w):
             "wgrad_col": e * (M * g * F + M * H) + 4 * g * F * H,
             "col_dgrad": e * (M * g * F + g * F * H + M * H) + res,
             "fused_mlp_fwd": e * (M * H + g * F * H + H * F + M * g * F + M * F + M * H) + res}
+
+
+def step_bytes(w):
+    """Bytes of the device tensors one step reads or writes (operands,
+    activations, outputs, fp32 weight gradients), each counted once."""
+    M, H, F, g = w.M, w.H, w.F, w.g
+    e = 4 if w.dtype == "f32" else 2
+    if w.kind == "attn_proj":
+        Fo = w.F_o
+        return e * (4 * M * H + 2 * M * F + 2 * M * Fo + F * H + H * Fo) + 4 * (F * H + H * Fo)
+    return e * (4 * M * H + M * g * F + M * F + (g + 1) * F * H) + 4 * (g + 1) * F * H
 
 
 LAYER_DROPOUT_P = 0.1  # Megatron's default hidden dropout
@@ -204,16 +224,10 @@ def recorded_traffic(w, tile_mode, kernel):
     return rec.get("bytes_per_launch", {}).get(kernel)
 
 
-def run_gpu(args, w, dist, rank, local, ws):
-    import torch
-
-    import tensor_transformer_mlp_shard_gb300 as tp
-    from tensor_transformer_mlp_shard_gb300 import build
-    build.build()
-    torch.cuda.set_device(local)
-    tp.set_tile_mode(args.tile_mode)
-    tp.set_fused_fwd(args.fused)
-    dev = torch.device("cuda", local)
+def mlp_step(args, w, tp, torch, dev, stream):
+    """The MLP (or sub-block) step on device-resident shards.  Returns
+    step(k) -- one fwd+bwd on buffer set k -- and the two buffer sets, each
+    (inputs uploaded per step, outputs read back per step)."""
     bf = torch.bfloat16
     T, M, H, F, g = w.T, w.M, w.H, w.F, w.g
     Fs = F // T
@@ -260,12 +274,9 @@ def run_gpu(args, w, dist, rank, local, ws):
     db1 = [torch.empty(g * Fs, dtype=f32, device=dev) for _ in range(T)] if w.has_bias else None
     db2 = torch.empty(H, dtype=f32, device=dev) if w.has_bias else None
     wsp = tp.alloc_workspace(lay.workspace_bytes(), device=dev)
-    # all work on one non-default stream (a CUDA graph cannot capture the legacy stream)
-    stream = torch.cuda.Stream(dev)
-    torch.cuda.set_stream(stream)
     # the end-to-end loop alternates two device buffer sets for X, dY, Y
-    e2e_sets = [(X, dY, Y), ([torch.empty_like(x) for x in X], [torch.empty_like(d) for d in dY],
-                             [torch.empty_like(y) for y in Y])]
+    bufs = [(X, dY, Y), ([torch.empty_like(x) for x in X], [torch.empty_like(d) for d in dY],
+                         [torch.empty_like(y) for y in Y])]
     if layer:
         lnp = synth.layer_tensors(1, H, w.dtype)
         gamma, beta = up(lnp["gamma"]), up(lnp["beta"])
@@ -275,15 +286,79 @@ def run_gpu(args, w, dist, rank, local, ws):
         dgamma = torch.empty(H, dtype=f32, device=dev)
         dbeta = torch.empty(H, dtype=f32, device=dev)
 
-        def step(X=X, dY=dY, Y=Y):
+        def step(k=0):
+            X, dY, Y = bufs[k]
             lay.fwd(X, gamma, beta, W1, b1, W2, b2, LAYER_SEED, Y, Xn, mean, rstd, pre, A, workspace=wsp,
                     stream=stream)
             lay.bwd(dY, X, gamma, Xn, mean, rstd, W1, W2, pre, A, LAYER_SEED, dX, dgamma, dbeta, dW1, db1, dW2,
                     db2, wsp, stream=stream)
     else:
-        def step(X=X, dY=dY, Y=Y):
-            lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp if w.dtype == "fp8" else None)
+        def step(k=0):
+            X, dY, Y = bufs[k]
+            lay.fwd(X, W1, b1, W2, b2, Y, pre, A, stream=stream, workspace=wsp)
             lay.bwd(dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, wsp, stream=stream)
+    return step, [(x + d, y) for x, d, y in bufs]
+
+
+def attn_step(args, w, tp, torch, dev, stream):
+    """The attention projections' step: the QKV ColumnParallelLinear
+    (H -> F = 3H, no activation) and the output RowParallelLinear (F_o -> H),
+    forward and backward through the single-layer entry points.  Returns
+    step(k) and the two buffer sets (inputs X, Z, dYqkv, dYo; output Yo)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    T, M, H, F, Fo = w.T, w.M, w.H, w.F, w.F_o
+    Fs, Fos = F // T, Fo // T
+    full = synth.attn_tensors(w)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=bf)
+
+    colL = tp.Layout(S=w.S, B=w.B, H=H, F=F, T=T, act="none", dtype="bf16")
+    rowL = tp.Layout(S=w.S, B=w.B, H=H, F=Fo, T=T, act="none", dtype="bf16")
+    Wq = [up(full["Wqkv"][i * Fs:(i + 1) * Fs]) for i in range(T)]
+    Wo = [up(full["Wo"][:, i * Fos:(i + 1) * Fos]) for i in range(T)]
+    X = up(full["X"])
+    Z = [up(full["Z"][:, i * Fos:(i + 1) * Fos]) for i in range(T)]
+    dYq = [up(full["dYqkv"][:, i * Fs:(i + 1) * Fs]) for i in range(T)]
+    dYo = up(full["dYo"])
+    Yq = [torch.empty(M, Fs, dtype=bf, device=dev) for _ in range(T)]
+    Yo = torch.empty(M, H, dtype=bf, device=dev)
+    dX = torch.empty(M, H, dtype=bf, device=dev)
+    dZ = [torch.empty(M, Fos, dtype=bf, device=dev) for _ in range(T)]
+    dWq = [torch.empty(Fs, H, dtype=f32, device=dev) for _ in range(T)]
+    dWo = [torch.empty(H, Fos, dtype=f32, device=dev) for _ in range(T)]
+    wsc = tp.alloc_workspace(tp.linear_workspace_bytes(colL), device=dev)
+    wsr = tp.alloc_workspace(tp.linear_workspace_bytes(rowL), device=dev)
+    bufs = [(X, Z, dYq, dYo, Yo), (torch.empty_like(X), [torch.empty_like(z) for z in Z],
+                                    [torch.empty_like(d) for d in dYq], torch.empty_like(dYo),
+                                    torch.empty_like(Yo))]
+
+    def step(k=0):
+        X, Z, dYq, dYo, Yo = bufs[k]
+        tp.linear_col(colL, [X], Wq, None, Yq, stream=stream)
+        tp.linear_row(rowL, Z, Wo, None, None, [Yo], stream=stream)
+        tp.linear_col_bwd(colL, dYq, [X], Wq, [dX], dWq, None, workspace=wsc, stream=stream)
+        tp.linear_row_bwd(rowL, [dYo], Z, Wo, dZ, dWo, None, workspace=wsr, stream=stream)
+    return step, [([X] + Z + dYq + [dYo], [Yo]) for X, Z, dYq, dYo, Yo in bufs]
+
+
+def run_gpu(args, w, dist, rank, local, ws):
+    import torch
+
+    import tensor_transformer_mlp_shard_gb300 as tp
+    from tensor_transformer_mlp_shard_gb300 import build
+    build.build()
+    torch.cuda.set_device(local)
+    tp.set_tile_mode(args.tile_mode)
+    tp.set_fused_fwd(args.fused)
+    tp.set_tail_split(args.tail_split == "on")
+    dev = torch.device("cuda", local)
+    layer = args.block == "layer"
+    # all work on one non-default stream (a CUDA graph cannot capture the legacy stream)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    make = attn_step if w.kind == "attn_proj" else mlp_step
+    step, e2e_sets = make(args, w, tp, torch, dev, stream)
 
     # ---- device-resident timing --------------------------------------------
     for _ in range(args.warmup):
@@ -300,12 +375,12 @@ def run_gpu(args, w, dist, rank, local, ws):
         for k in range(2):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                eager_step() if k == 0 else eager_step(*e2e_sets[1])
+                eager_step(k)
             graphs.append(g)
         graph_launches = (tp.launch_count() - n_before) // 2
 
-        def step(X_=None, dY_=None, Y_=None):
-            graphs[0 if X_ is None or X_ is X else 1].replay()
+        def step(k=0):
+            graphs[k].replay()
     clocks = ClockSampler(local)
     clocks.start()
     tp.prof_enable(True)
@@ -333,15 +408,15 @@ def run_gpu(args, w, dist, rank, local, ws):
     value = job_throughput(ws, flops_step, args.steps, ms_max)
 
     # ---- end to end through the C ABI with host buffers ---------------------
-    # Every step copies its X and dY from pinned host memory and its Y back.
+    # Every step copies its inputs (X and dY; for the projections X, Z and the
+    # two upstream gradients) from pinned host memory and its output Y back.
     # The copies run on a second stream into two alternating device buffer
     # sets, so that step i's compute overlaps step i+1's inputs and step i-1's
     # output (events order each copy against the compute that uses the set).
-    hX = [x.cpu().pin_memory() for x in X]
-    hdY = [d.cpu().pin_memory() for d in dY]
-    hY = [torch.empty(rows, H, dtype=td).pin_memory() for _ in range(lay.nx)]
-    h2d = sum(t.numel() * t.element_size() for t in hX + hdY)
-    d2h = sum(t.numel() * t.element_size() for t in hY)
+    h_in = [x.cpu().pin_memory() for x in e2e_sets[0][0]]
+    h_out = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in e2e_sets[0][1]]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
     sets = e2e_sets
     copy_stream = torch.cuda.Stream(dev)
 
@@ -353,11 +428,8 @@ def run_gpu(args, w, dist, rank, local, ws):
         copy_stream.wait_stream(stream)
 
         def upload(k):
-            Xs, dYs, _ = sets[k % 2]
             with torch.cuda.stream(copy_stream):
-                for d, h in zip(Xs, hX):
-                    d.copy_(h, non_blocking=True)
-                for d, h in zip(dYs, hdY):
+                for d, h in zip(sets[k % 2][0], h_in):
                     d.copy_(h, non_blocking=True)
                 in_ready[k % 2].record(copy_stream)
 
@@ -368,11 +440,11 @@ def run_gpu(args, w, dist, rank, local, ws):
                     copy_stream.wait_event(done[(i + 1) % 2])  # set (i+1)%2 last used by step i-1
                 upload(i + 1)
             stream.wait_event(in_ready[i % 2])
-            step(*sets[i % 2])
+            step(i % 2)
             done[i % 2].record(stream)
             copy_stream.wait_event(done[i % 2])
             with torch.cuda.stream(copy_stream):
-                for h, d in zip(hY, sets[i % 2][2]):
+                for h, d in zip(h_out, sets[i % 2][1]):
                     h.copy_(d, non_blocking=True)
                 out_done.record(copy_stream)
         stream.wait_event(out_done)
@@ -451,6 +523,8 @@ def oracle_sample(w, tokens, full=None, block="mlp"):
     (seconds, algorithmic FLOP)."""
     import oracle
     from oracle import layer as olayer
+    if w.kind == "attn_proj":
+        return oracle_sample_attn(w, tokens, full)
     if full is None:
         full = synth.mlp_tensors(w, M=tokens)
     W1s = oracle.shard_column_weight(full["W1"], w.T, w.act)
@@ -471,6 +545,35 @@ def oracle_sample(w, tokens, full=None, block="mlp"):
     return dt, flops
 
 
+def oracle_sample_attn(w, tokens, full=None):
+    """The fp64 oracle's forward and backward of the QKV column layer and the
+    output row layer on the first `tokens` tokens; (seconds, FLOP)."""
+    import oracle
+    if full is None:
+        full = synth.attn_tensors(w, M=tokens)
+    T = w.T
+    Wq = oracle.shard_column_weight(full["Wqkv"], T)
+    Wo = oracle.shard_row_weight(full["Wo"], T)
+    X, dYo = full["X"][:tokens], full["dYo"][:tokens]
+    Zs = oracle.shard_row_weight(full["Z"][:tokens], T)        # column blocks of Z, one per shard
+    dYq = oracle.shard_row_weight(full["dYqkv"][:tokens], T)   # column blocks of the QKV gradient
+    t0 = time.perf_counter()
+    oracle.column_fwd(X, Wq, None, "none")
+    oracle.row_fwd(Zs, Wo)
+    oracle.column_bwd(dYq, X, Wq)
+    oracle.row_bwd(dYo, Zs, Wo)
+    dt = time.perf_counter() - t0
+    return dt, 3.0 * (2.0 * tokens * w.H * w.F + 2.0 * tokens * w.F_o * w.H)
+
+
+def workload_tensors(w, M=None):
+    return synth.attn_tensors(w, M=M) if w.kind == "attn_proj" else synth.mlp_tensors(w, M=M)
+
+
+def flop_per_token(w):
+    return w.flops() / w.M
+
+
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -481,11 +584,11 @@ def cpu_threads():
 def run_reference(args, w, rank, block="mlp"):
     # per-step sample sized so that warm-up + timed steps take ~2 minutes
     probe_tokens = 64
-    full = synth.mlp_tensors(w, M=2048)
+    full = workload_tensors(w, M=2048)
     dt, fl = oracle_sample(w, probe_tokens, full, block)
     rate = fl / dt
     budget = 120.0 / max(1, args.steps + args.warmup)
-    per_token = 3.0 * (2.0 * w.H * w.F * w.g + 2.0 * w.F * w.H)
+    per_token = flop_per_token(w)
     tokens = int(max(64, min(2048, budget * rate / per_token)))
     for _ in range(args.warmup):
         oracle_sample(w, tokens, full, block)
@@ -506,7 +609,7 @@ def cpu_baseline(w, block="mlp"):
     """The oracle on host cores over a token sample sized to about 15 s of
     work (a 512-token probe sets the size; at most the whole step)."""
     probe = 512
-    full = synth.mlp_tensors(w)
+    full = workload_tensors(w)
     dt, fl = oracle_sample(w, probe, full, block)
     rate = fl / dt
     per_token = fl / probe
@@ -540,6 +643,8 @@ def main():
                     help="forward as one fused kernel for narrow MLPs (H <= 256): auto / on / off")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
+    ap.add_argument("--tail-split", default="on", choices=["on", "off"],
+                    help="cut the persistent GEMMs' part-filled last round of tiles along K over all CTA pairs")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -547,16 +652,22 @@ def main():
     if args.dtype == "fp8":
         import dataclasses
         w = dataclasses.replace(w, dtype="fp8")
-    if w.kind != "mlp":
-        raise SystemExit("bench.py times the MLP workloads (gpt, swiglu, sp, tiny)")
+    if w.kind == "attn_proj" and (w.dtype != "bf16" or args.block != "mlp"):
+        raise SystemExit("the attention projections are timed in bf16 as plain layers")
     ws, rank, local = dist_env()
-    config = {"workload": f"{w.name}: X [S={w.S},B={w.B},H={w.H}] {w.dtype}, F={w.F}, T={w.T}, {w.act}"
-                          f"{', bias' if w.has_bias else ''}{', residual' if w.residual else ''}"
-                          f"{', sequence-parallel' if w.seq_parallel else ''}",
+    if w.kind == "attn_proj":
+        desc = (f"{w.name}: X [S={w.S},B={w.B},H={w.H}] {w.dtype}, QKV column layer H -> {w.F} and output row "
+                f"layer {w.F_o} -> H, T={w.T}, no activation, no bias")
+    else:
+        desc = (f"{w.name}: X [S={w.S},B={w.B},H={w.H}] {w.dtype}, F={w.F}, T={w.T}, {w.act}"
+                f"{', bias' if w.has_bias else ''}{', residual' if w.residual else ''}"
+                f"{', sequence-parallel' if w.seq_parallel else ''}")
+    config = {"workload": desc,
               "S": w.S, "B": w.B, "H": w.H, "F": w.F, "T": w.T, "act": w.act, "global_batch": w.B * ws,
               "seq_len": w.S, "parallelism": f"tp{w.T} shards on one GPU; {ws} replica(s)",
-              "l2": "inputs larger than L2 (weights+activations ~1.8 GB per step)",
-              "tile_mode": args.tile_mode, "fused_fwd": args.fused,
+              "l2": f"inputs larger than L2 (~{step_bytes(w) / 1e9:.1f} GB of operands, activations and "
+                    f"gradients per step)",
+              "tile_mode": args.tile_mode, "fused_fwd": args.fused, "tail_split": args.tail_split,
               "launch": "CUDA graph replay per step" if args.graph else "eager C-ABI calls per step"}
     if w.dtype == "fp8":
         config["fp8_scaling"] = (f"delayed, amax history {args.fp8_history}" if args.fp8_history

@@ -122,7 +122,11 @@ TP_API void tp_mlp_destroy(tp_mlp *h);
  * partial sums of the weight gradients when their outputs have few tiles and
  * many tokens (bf16 and FP8: up to 16 token splits, added in split order by a
  * reduction kernel) and, for FP8, the per-tensor amax values and the
- * quantised operands.  A function of the descriptor alone. */
+ * quantised operands; those parts are a function of the descriptor alone and
+ * are what the calls require.  After them comes the scratch of the GEMMs'
+ * tail split (tp_set_tail_split), sized for the GEMM settings and the current
+ * device's SM count at the time of the query: a workspace without it is
+ * accepted and the split skipped. */
 TP_API size_t tp_mlp_workspace_bytes(const tp_mlp *h);
 
 /* ---- MLP forward ("Megatron-LM 源码精读" s3.3 figure) ------------------------
@@ -142,7 +146,8 @@ TP_API tp_status tp_mlp_fwd(tp_mlp *h, const void *const *X, const void *const *
 /* tp_mlp_fwd with a workspace (>= tp_mlp_workspace_bytes, 256-byte aligned).
  * Required for TP_DT_FP8, where the forward quantises X, W1, W2 and A into the
  * workspace and tp_mlp_bwd must then be given the same workspace, unchanged in
- * between; for the other dtypes the workspace is not touched.  TP_DT_FP8
+ * between; for bf16 it is optional and only the row GEMM's tail-split scratch
+ * is used (a NULL, unaligned or too small workspace is ignored).  TP_DT_FP8
  * through tp_mlp_fwd returns TP_ERR_ARG. */
 TP_API tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *const *W1,
                                const void *const *b1, const void *const *W2, const void *b2,
@@ -200,7 +205,9 @@ TP_API tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X,
                         const void *const *R, void *const *Y, void *stream);
 
 /* Workspace bytes for tp_linear_col_bwd / tp_linear_row_bwd: bias partials,
- * then split-K partials of the weight gradient (as for tp_mlp_bwd). */
+ * then split-K partials of the weight gradient (as for tp_mlp_bwd), then the
+ * tail-split scratch of the bf16 dgrad and weight-gradient GEMMs (optional, as
+ * for tp_mlp_workspace_bytes). */
 TP_API size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc);
 
 /* tp_linear_col_bwd: gradients of tp_linear_col with act = TP_ACT_NONE
@@ -280,7 +287,8 @@ TP_API void tp_layer_destroy(tp_layer *h);
 
 /* Bytes of device workspace for tp_layer_bwd (and, for TP_DT_FP8,
  * tp_layer_fwd, whose quantised operands the backward reads from it): the
- * MLP's workspace, dZ and dXn ([M, H] each). */
+ * MLP's workspace, dZ and dXn ([M, H] each), then the MLP GEMMs' tail-split
+ * scratch (optional, as for tp_mlp_workspace_bytes). */
 TP_API size_t tp_layer_workspace_bytes(const tp_layer *h);
 
 /* FP8 scaling recipe of a TP_DT_FP8 sub-block: as tp_mlp_set_fp8_history
@@ -293,7 +301,8 @@ TP_API tp_status tp_layer_set_fp8_history(tp_layer *h, int n);
  * Outputs kept for the backward: Xn [M, H] (activation dtype), mean and rstd
  * [M] fp32, pre, A.  workspace: required (>= tp_layer_workspace_bytes,
  * 256-byte aligned) for TP_DT_FP8 and then passed unchanged to tp_layer_bwd;
- * ignored otherwise (may be NULL). */
+ * optional otherwise (may be NULL), where only the row GEMM's tail-split
+ * scratch is used. */
 TP_API tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, const void *beta,
                               const void *const *W1, const void *const *b1, const void *const *W2,
                               const void *b2, uint64_t seed, void *const *Y, void *Xn, float *mean,
@@ -351,6 +360,33 @@ TP_API tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream);
 typedef enum { TP_TILE_AUTO = 0, TP_TILE_SINGLE = 1, TP_TILE_PAIR = 2 } tp_tile_mode;
 TP_API tp_status tp_set_tile_mode(int mode);
 
+/* Tail split of the pair-tile GEMMs, for all launches made after the call
+ * (on = 1, the default; 0 turns it off).  The pair kernels are persistent:
+ * P CTA pairs take the tiles round-robin, so when the tile count is not a
+ * multiple of P the last round runs part-filled (GPT-size weight gradients:
+ * 1024 tiles on 76 pairs, 13.5 rounds in the time of 14).  When that round
+ * holds rem <= P/2 tiles, the split cuts each of them along K into
+ * s = min(P / rem, 4) units that run side by side in one round; every unit
+ * parks its fp32 partial sum in the workspace and the last unit of each
+ * 32 x 128 slice to finish adds the slices in unit order and runs the tile's
+ * epilogue.  No unit waits for another.  Only whole-tile output GEMMs that
+ * run after at least one full round split (row forward, column dgrad, weight
+ * gradients, single-layer dgrads), and only when the call has the scratch:
+ * tp_mlp_workspace_bytes,
+ * tp_linear_workspace_bytes and tp_layer_workspace_bytes include it at the
+ * end of the workspace, sized for the settings and device current at the
+ * query; a workspace without it (or the plain tp_mlp_fwd) skips the split.
+ * Split tiles sum K in another grouping, so they differ from unsplit ones by
+ * fp32 rounding; a given configuration is run-to-run deterministic.
+ * TP_ERR_ARG unless on is 0 or 1. */
+TP_API tp_status tp_set_tail_split(int on);
+
+/* Upper bound on the CTA pairs of the persistent pair-tile GEMMs, for all
+ * launches made after the call (0, the default: as many as fit on the
+ * device).  Leaves SMs free for concurrent work and sets the round structure
+ * the tail split sees.  TP_ERR_ARG for n < 0. */
+TP_API tp_status tp_set_max_gemm_pairs(int n);
+
 /* Forward of the MLP (and of the sub-block) as one fused kernel, for all
  * calls made after this one.  The fused kernel keeps a 128-token tile's
  * output [128 x H] in tensor memory and streams the F dimension through it
@@ -371,6 +407,10 @@ TP_API tp_status tp_set_fused_fwd(int mode);
 
 /* Number of kernels this library has launched since load. */
 TP_API uint64_t tp_launch_count(void);
+
+/* Number of pair-tile GEMM launches since load that split their last round's
+ * tiles (tp_set_tail_split). */
+TP_API uint64_t tp_tail_split_count(void);
 
 /* Per-kernel timing ("timers"): when enabled, every launch is bracketed by
  * CUDA events recorded on its own stream.  tp_prof_collect synchronises the

@@ -80,6 +80,9 @@ SIGNATURES = {
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
     "tp_launch_count": (ctypes.c_uint64, []),
+    "tp_tail_split_count": (ctypes.c_uint64, []),
+    "tp_set_tail_split": (ctypes.c_int, [ctypes.c_int]),
+    "tp_set_max_gemm_pairs": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_fused_fwd": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
@@ -335,17 +338,15 @@ class TPLayer(Layout):
                                   _arr(pdw2), pdb2, ws_ptr, ws_bytes, _stream(stream)))
 
 
-def _workspace(workspace, need):
-    if need == 0:
-        return None, 0
+def _workspace(workspace, need=None):
+    """(pointer, bytes) of a workspace tensor, (None, 0) for None.  The library
+    checks the size: the part a call requires can be smaller than the queried
+    size `need`, whose end is the optional tail-split scratch."""
     if workspace is None:
-        raise ValueError(f"workspace of {need} bytes required")
+        return None, 0
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    nbytes = workspace.numel() * workspace.element_size()
-    if nbytes < need:
-        raise ValueError(f"workspace has {nbytes} bytes, {need} required")
-    return workspace.data_ptr(), nbytes
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
 
 def alloc_workspace(nbytes: int, device="cuda"):
@@ -477,6 +478,22 @@ def set_tile_mode(mode: str):
     """GEMM tiling of the bf16 engine: "auto", "single" (128-row tiles, one
     CTA) or "pair" (256-row tiles on a CTA pair)."""
     _check(lib().tp_set_tile_mode(TILE_MODES[mode]))
+
+
+def set_tail_split(on: bool):
+    """Tail split of the pair-tile GEMMs (on by default): the last,
+    part-filled round of tiles is cut along K over all CTA pairs."""
+    _check(lib().tp_set_tail_split(1 if on else 0))
+
+
+def set_max_gemm_pairs(n: int):
+    """Upper bound on the CTA pairs of the pair-tile GEMMs (0: all that fit)."""
+    _check(lib().tp_set_max_gemm_pairs(int(n)))
+
+
+def tail_split_count() -> int:
+    """GEMM launches since load that split their last round's tiles."""
+    return int(lib().tp_tail_split_count())
 
 
 FUSED_MODES = {"auto": 0, "off": 1, "on": 2}

@@ -209,6 +209,16 @@ static Dims dims_of(const tp_mlp_desc *d) {
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Scratch of a GEMM's tail split (null: the GEMM does not split its tail)
+struct Scratch {
+    void *p = nullptr;
+    size_t n = 0;
+};
+static void set_tail(GemmPlan &g, Scratch t) {
+    g.tail_ws = t.p;
+    g.tail_bytes = t.p ? t.n : 0;
+}
+
 static tp_status run_gemm(const GemmPlan &g, int dtype, cudaStream_t st) {
     return dtype == TP_DT_F32 ? launch_simt_gemm(g, st) : launch_tc_gemm(g, st);
 }
@@ -281,7 +291,8 @@ static void set_drop(GemmPlan &g, const DropCfg *dc) {
 
 // Row forward: Y = sum_i X_i W_i^T + b (+R); the K loop runs over shards.
 static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void *const *W, const void *b,
-                         const void *const *R, void *const *Y, cudaStream_t st, const DropCfg *drop = nullptr) {
+                         const void *const *R, void *const *Y, cudaStream_t st, const DropCfg *drop = nullptr,
+                         Scratch tail = {}) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = "row_fwd";
@@ -298,13 +309,14 @@ static tp_status row_fwd(const tp_mlp_desc *d, const void *const *Xs, const void
     const void *bb[1] = {b};
     set_bias(g, (d->has_bias && b) ? bb : nullptr, 1, 0);
     set_drop(g, drop);
+    set_tail(g, tail);
     return run_gemm(g, d->dtype, st);
 }
 
 // Row-layer dgrad: dOut_i = (dY W_i) [* act'(pre_i)], i < T (no reduction).
 static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY, const void *const *W,
                            const void *const *pre, void *const *dOut, long long ld_out, cudaStream_t st,
-                           float *col_partials = nullptr, bool *fused = nullptr) {
+                           float *col_partials = nullptr, bool *fused = nullptr, Scratch tail = {}) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = act == TP_ACT_NONE ? "row_dgrad" : "row_dgrad_act";
@@ -323,6 +335,7 @@ static tp_status row_dgrad(const tp_mlp_desc *d, int act, const void *const *dY,
     const bool fuse = col_partials && act != TP_ACT_NONE && d->dtype != TP_DT_F32 && tc_fused_epilogue(g);
     if (fuse) g.col_partials = col_partials;
     if (fused) *fused = fuse;
+    set_tail(g, tail);
     return run_gemm(g, d->dtype, st);
 }
 
@@ -355,7 +368,7 @@ static size_t split_bytes(const tp_mlp_desc *d, int Mo, int No) {
 // workspace for split-K partial sums, split_bytes(d, gw, aw) bytes.
 static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const *G, int g_per_shard, int gw,
                        const void *const *Act, int a_per_shard, int aw, void *const *dW, cudaStream_t st,
-                       float *split_ws) {
+                       float *split_ws, Scratch tail = {}) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = name;
@@ -379,12 +392,13 @@ static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const
         g.ksplit = wgrad_ksplit(gw, aw, x.T, x.M);
         g.split_ws = split_ws;
     }
+    set_tail(g, tail);
     return run_gemm(g, d->dtype, st);
 }
 
 // Column-layer dgrad: dX = sum_i dOut_i W_i (+R); the K loop runs over shards.
 static tp_status column_dgrad(const tp_mlp_desc *d, const void *const *dOut, int kw, const void *const *W,
-                              const void *const *R, void *const *dX, cudaStream_t st) {
+                              const void *const *R, void *const *dX, cudaStream_t st, Scratch tail = {}) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = "col_dgrad";
@@ -399,6 +413,7 @@ static tp_status column_dgrad(const tp_mlp_desc *d, const void *const *dOut, int
     set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
     if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
     set_bias(g, nullptr, 0, 0);
+    set_tail(g, tail);
     return run_gemm(g, d->dtype, st);
 }
 
@@ -500,9 +515,37 @@ static Fp8Layout fp8_layout(const tp_mlp_desc *d) {
     return L;
 }
 
+// Tail-split scratch of the MLP's pair GEMMs (row forward, column dgrad,
+// both weight gradients): the largest any of them may use.  It depends on
+// the GEMM settings and the device, so it comes after everything else in a
+// workspace: validation asks only for the part before it, and a GEMM splits
+// its tail only when the scratch a caller's workspace leaves is large enough.
+static size_t tail_scratch_bytes(const tp_mlp_desc *d) {
+    if (d->dtype == TP_DT_F32) return 0;  // the fp32 engine does not split
+    const Dims x = dims_of(d);
+    const bool f8 = d->dtype == TP_DT_FP8;
+    const int gw = x.g * x.Fs;
+    size_t r = tc_tail_bytes(x.M, x.H, 1, x.T, x.Fs, f8);
+    r = std::max(r, tc_tail_bytes(x.M, x.H, 1, x.T, gw, f8));
+    r = std::max(r, tc_tail_bytes(x.H, x.Fs, x.T, 1, x.M, f8));
+    r = std::max(r, tc_tail_bytes(gw, x.H, x.T, 1, x.M, f8));
+    return align256(r);
+}
+
+// the MLP workspace without its tail-split scratch (what a call requires)
 static size_t mlp_ws_layout(const tp_mlp_desc *d, size_t *dpre_shard_bytes) {
     const size_t b = bwd_ws_bytes(d, dpre_shard_bytes);
-    return d->dtype == TP_DT_FP8 ? fp8_layout(d).end : b;
+    return align256(d->dtype == TP_DT_FP8 ? fp8_layout(d).end : b);
+}
+
+// the scratch a workspace of `bytes` leaves after its first `used` bytes
+static Scratch scratch_after(void *workspace, size_t bytes, size_t used) {
+    Scratch t;
+    if (workspace && bytes > used) {
+        t.p = static_cast<char *>(workspace) + used;
+        t.n = bytes - used;
+    }
+    return t;
 }
 
 static tp_status zero_grads(const tp_mlp_desc *d, void *const *dW, int nW, size_t wbytes, void *const *db, int ndb,
@@ -532,7 +575,7 @@ static void set_fp8(GemmPlan &g, int fa, int fb, const float *amax, int slot_a, 
 static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W1, const void *const *b1,
                          const void *const *W2, const void *b2, const void *const *R, void *const *Y,
                          void *const *pre, void *const *A, void *ws, cudaStream_t st, const DropCfg *drop,
-                         const Fp8Recipe &rc) {
+                         const Fp8Recipe &rc, Scratch tail) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
@@ -641,6 +684,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
     set_bias(g, d->has_bias ? bb : nullptr, 1, 0);
     set_fp8(g, FP8_E4M3, FP8_E4M3, sa, AMAX_A, AMAX_W2);
     set_drop(g, drop);
+    set_tail(g, tail);
     TRY(launch_tc_gemm(g, st));
     if (delayed) {  // this step's amaxes join the history
         const int fwd_slots[4] = {AMAX_X, AMAX_W1, AMAX_W2, AMAX_A};
@@ -651,7 +695,7 @@ static tp_status fp8_fwd(const tp_mlp_desc *d, const void *const *X, const void 
 
 static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void *const *pre, void *const *dX,
                          void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *ws, cudaStream_t st,
-                         const Fp8Recipe &rc) {
+                         const Fp8Recipe &rc, Scratch tail) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     const Fp8Layout L = fp8_layout(d);
@@ -721,6 +765,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             for (int i = 0; i < x.T; ++i) g.q_out[i] = dpq[i];
             g.q_fmt = FP8_E5M2;
             g.q_scale_amax = samax + AMAX_DP;
+            g.q_only = true;  // nothing reads the bf16 dPre: db1 comes from the fused partials
             dp_direct = true;
         }
         TRY(launch_tc_gemm(g, st));
@@ -764,6 +809,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             g.split_ws = split;
         }
         set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DY, AMAX_A);
+        set_tail(g, tail);
         TRY(launch_tc_gemm(g, st));
     }
     {
@@ -784,6 +830,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
             g.split_ws = split;
         }
         set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DP, AMAX_X);
+        set_tail(g, tail);
         TRY(launch_tc_gemm(g, st));
     }
     // column layer dgrad: dX = sum_i dPq_i W1q_i / (s_dp s_w1) (+ dY)
@@ -802,6 +849,7 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         if (d->residual) set_out(g.aux, dY, x.nx, 0, x.rs, x.H);
         set_bias(g, nullptr, 0, 0);
         set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DP, AMAX_W1);
+        set_tail(g, tail);
         TRY(launch_tc_gemm(g, st));
     }
     if (d->has_bias) {
@@ -853,16 +901,18 @@ tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out) {
 
 void tp_mlp_destroy(tp_mlp *h) { delete h; }
 
-size_t tp_mlp_workspace_bytes(const tp_mlp *h) { return h ? mlp_ws_layout(&h->d, nullptr) : 0; }
+size_t tp_mlp_workspace_bytes(const tp_mlp *h) {
+    return h ? mlp_ws_layout(&h->d, nullptr) + tail_scratch_bytes(&h->d) : 0;
+}
 
 // MLP forward on validated arguments: Y = R + dropout(MLP(X)) with R and the
 // dropout optional (the plain MLP passes R = X iff residual, no dropout).
 static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const void *const *W1,
                               const void *const *b1, const void *const *W2, const void *b2, const void *const *R,
                               void *const *Y, void *const *pre, void *const *A, void *workspace, const DropCfg *drop,
-                              cudaStream_t st, const Fp8Recipe &rc = Fp8Recipe()) {
+                              cudaStream_t st, const Fp8Recipe &rc = Fp8Recipe(), Scratch tail = {}) {
     if (d->dtype == TP_DT_FP8)
-        return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop, rc);
+        return fp8_fwd(d, X, W1, d->has_bias ? b1 : nullptr, W2, b2, R, Y, pre, A, workspace, st, drop, rc, tail);
     const Dims x = dims_of(d);
     // the fused kernel only on request: measured slower than the two GEMMs
     if (fused_fwd_mode() == TP_FUSED_ON && fused_fwd_supported(x.H, x.Fs, d->act, d->dtype)) {
@@ -897,7 +947,8 @@ static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const 
         return launch_fused_mlp_fwd(f, st);
     }
     TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));
-    return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr, R, Y, st, drop);
+    return row_fwd(d, reinterpret_cast<const void *const *>(A), W2, d->has_bias ? b2 : nullptr, R, Y, st, drop,
+                   tail);
 }
 
 // MLP backward on validated arguments (workspace checked by the caller).
@@ -907,7 +958,7 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
                               const void *const *W1, const void *const *W2, const void *const *pre,
                               const void *const *A, void *const *dX, void *const *dW1, void *const *db1,
                               void *const *dW2, void *db2, void *workspace, cudaStream_t st,
-                              bool db2_done = false, const Fp8Recipe &rc = Fp8Recipe()) {
+                              bool db2_done = false, const Fp8Recipe &rc = Fp8Recipe(), Scratch tail = {}) {
     const Dims x = dims_of(d);
     const int gw = x.g * x.Fs;
     size_t shard_bytes = 0;
@@ -920,7 +971,7 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     }
     if (d->dtype == TP_DT_FP8)
         return fp8_bwd(d, dY, pre, dX, dW1, d->has_bias ? db1 : nullptr, dW2,
-                       (d->has_bias && !db2_done) ? db2 : nullptr, workspace, st, rc);
+                       (d->has_bias && !db2_done) ? db2 : nullptr, workspace, st, rc, tail);
     void *dpre[kMaxShards];
     for (int i = 0; i < x.T; ++i) dpre[i] = static_cast<char *>(workspace) + i * shard_bytes;
     float *partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + x.T * shard_bytes);
@@ -930,10 +981,10 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     // row layer: dPre_i = (dY W2_i) * act'(pre_i), dW2_i = dY^T A_i
     bool db1_fused = false;
     TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st, d->has_bias ? partials : nullptr, &db1_fused));
-    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st, split));
+    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st, split, tail));
     // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY)
-    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st, split));
-    TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st));
+    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st, split, tail));
+    TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st, tail));
     if (d->has_bias) {
         if (db1_fused)
             TRY(db1_finalize(d, gw, db1, partials, st));
@@ -973,6 +1024,10 @@ static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const
             return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
             return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
+    } else if (!has_ws || !workspace || workspace_bytes < mlp_ws_layout(d, nullptr) ||
+               (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        workspace = nullptr;  // optional for bf16 / fp32: used only when it is large enough
+        workspace_bytes = 0;
     }
     if (x.M == 0) return TP_OK;  // no tokens: activation buffers may be empty (NULL)
     TRY(check_array(X, x.nx, "X"));
@@ -981,7 +1036,8 @@ static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const
     if (d->act != TP_ACT_NONE || pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
     const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_fwd_steps);
     TRY(mlp_fwd_core(d, X, W1, b1, W2, b2, d->residual ? X : nullptr, Y, pre, A, workspace, nullptr,
-                     static_cast<cudaStream_t>(stream), rc));
+                     static_cast<cudaStream_t>(stream), rc,
+                     scratch_after(workspace, workspace_bytes, mlp_ws_layout(d, nullptr))));
     if (d->dtype == TP_DT_FP8 && rc.n) ++h->fp8_fwd_steps;
     return TP_OK;
 }
@@ -1027,7 +1083,7 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
         return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
     const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_bwd_steps);
     TRY(mlp_bwd_core(d, dY, X, W1, W2, pre, A, dX, dW1, db1, dW2, db2, workspace, static_cast<cudaStream_t>(stream),
-                     false, rc));
+                     false, rc, scratch_after(workspace, workspace_bytes, need)));
     if (d->dtype == TP_DT_FP8 && rc.n && x.M > 0) ++h->fp8_bwd_steps;
     return TP_OK;
 }
@@ -1070,14 +1126,36 @@ static size_t linear_part_bytes(const tp_mlp_desc *desc) {
     return a > b ? a : b;
 }
 
-size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
-    if (validate_desc(desc) != TP_OK) return 0;
+// ... then the tail-split scratch of its pair GEMMs (column layer: dgrad and
+// weight gradient; row layer: dgrad and weight gradient), at the end
+static size_t linear_tail_off(const tp_mlp_desc *desc) {
+    const Dims x = dims_of(desc);
+    return align256(linear_part_bytes(desc) + std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs)));
+}
+
+static size_t linear_tail_bytes(const tp_mlp_desc *desc) {
+    if (desc->dtype != TP_DT_BF16) return 0;
+    const Dims x = dims_of(desc);
+    size_t r = tc_tail_bytes(x.M, x.H, 1, x.T, x.Fs, false);
+    r = std::max(r, tc_tail_bytes(x.Fs, x.H, x.T, 1, x.M, false));
+    r = std::max(r, tc_tail_bytes(x.M, x.Fs, x.T, 1, x.H, false));
+    r = std::max(r, tc_tail_bytes(x.H, x.Fs, x.T, 1, x.M, false));
+    return align256(r);
+}
+
+static size_t linear_need(const tp_mlp_desc *desc) {
     const Dims x = dims_of(desc);
     return linear_part_bytes(desc) + std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs));
 }
 
+size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
+    if (validate_desc(desc) != TP_OK) return 0;
+    const size_t t = linear_tail_bytes(desc);
+    return t ? linear_tail_off(desc) + t : linear_need(desc);
+}
+
 static tp_status check_ws(const tp_mlp_desc *d, void *ws, size_t bytes) {
-    const size_t need = tp_linear_workspace_bytes(d);
+    const size_t need = linear_need(d);
     if (bytes < need) return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", bytes, need);
     if (need && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return set_error(TP_ERR_ARG, "workspace must be non-NULL and 256-byte aligned");
@@ -1105,9 +1183,10 @@ tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, co
     if (x.M == 0)
         return zero_grads(desc, dW, x.T, sizeof(float) * x.Fs * x.H, desc->has_bias ? db : nullptr, x.T,
                           sizeof(float) * x.Fs, st);
-    TRY(column_dgrad(desc, dOut, x.Fs, W, nullptr, dX, st));
+    const Scratch tail = scratch_after(workspace, workspace_bytes, linear_tail_off(desc));
+    TRY(column_dgrad(desc, dOut, x.Fs, W, nullptr, dX, st, tail));
     TRY(wgrad(desc, "wgrad_col", dOut, 1, x.Fs, X, 0, x.H, dW, st,
-              reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc))));
+              reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc)), tail));
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_col", dOut, x.T, 1, 0, x.T, x.Fs, db, static_cast<float *>(workspace), st));
     return TP_OK;
@@ -1157,10 +1236,11 @@ tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, co
     if (x.M == 0)
         return zero_grads(desc, dW, x.T, sizeof(float) * x.H * x.Fs, desc->has_bias ? dba : nullptr, 1,
                           sizeof(float) * x.H, st);
-    TRY(row_dgrad(desc, TP_ACT_NONE, dY, W, nullptr, dX, x.Fs, st));
+    const Scratch tail = allow_split ? scratch_after(workspace, workspace_bytes, linear_tail_off(desc)) : Scratch();
+    TRY(row_dgrad(desc, TP_ACT_NONE, dY, W, nullptr, dX, x.Fs, st, nullptr, nullptr, tail));
     float *split = allow_split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc))
                                : nullptr;
-    TRY(wgrad(desc, "wgrad_row", dY, 0, x.H, X, 1, x.Fs, dW, st, split));
+    TRY(wgrad(desc, "wgrad_row", dY, 0, x.H, X, 1, x.Fs, dW, st, split, tail));
     if (desc->has_bias)
         TRY(colsum(desc, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
     return TP_OK;
@@ -1219,7 +1299,14 @@ static LayerWs layer_ws(const tp_layer *h) {
     return L;
 }
 
-size_t tp_layer_workspace_bytes(const tp_layer *h) { return h ? layer_ws(h).end : 0; }
+// ... and after them the MLP's tail-split scratch
+size_t tp_layer_workspace_bytes(const tp_layer *h) {
+    return h ? align256(layer_ws(h).end) + tail_scratch_bytes(&h->inner) : 0;
+}
+
+static Scratch layer_tail(const tp_layer *h, void *ws, size_t bytes) {
+    return scratch_after(ws, bytes, align256(layer_ws(h).end));
+}
 
 static tp_status check_layer_ws(const tp_layer *h, void *ws, size_t bytes) {
     const size_t need = layer_ws(h).end;
@@ -1265,7 +1352,10 @@ tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, con
         TRY(check_array(b1, x.T, "b1"));
         TRY(check_one(b2, "b2"));
     }
-    if (d->dtype == TP_DT_FP8) TRY(check_layer_ws(h, workspace, workspace_bytes));
+    if (d->dtype == TP_DT_FP8)
+        TRY(check_layer_ws(h, workspace, workspace_bytes));
+    else if (!workspace || workspace_bytes < layer_ws(h).end || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        workspace = nullptr;  // optional for bf16 / fp32: used only when it is a full one
     if (x.M == 0) return TP_OK;
     TRY(check_array(X, x.nx, "X"));
     TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
@@ -1292,7 +1382,8 @@ tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, con
     dc.scale = h->drop_scale;
     dc.seed = seed;
     const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_fwd_steps);
-    TRY(mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st, rc));
+    TRY(mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st, rc,
+                     layer_tail(h, workspace, workspace ? workspace_bytes : 0)));
     if (rc.n) ++h->fp8_fwd_steps;
     return TP_OK;
 }
@@ -1365,7 +1456,8 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
     split_rows(const_cast<void *>(Xn), x, xn);
     split_rows(base + L.dxn, x, dxn);
     const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_bwd_steps);
-    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st, dropout, rc));
+    TRY(mlp_bwd_core(d, dz, xn, W1, W2, pre, A, dxn, dW1, db1, dW2, db2, base + L.mlp, st, dropout, rc,
+                     layer_tail(h, workspace, workspace_bytes)));
     if (rc.n) ++h->fp8_bwd_steps;
     // LayerNorm backward plus the residual branch: dX = dY + LN'(dXn); partials reuse the dZ region
     lp.dxn = base + L.dxn;
@@ -1405,6 +1497,8 @@ tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
 
 uint64_t tp_launch_count(void) { return g_launches.load(); }
 
+uint64_t tp_tail_split_count(void) { return tail_split_launches(); }
+
 tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
     if (n < 0 || n > kMaxFp8History) return set_error(TP_ERR_ARG, "history length %d outside 0..%d", n, kMaxFp8History);
@@ -1432,6 +1526,18 @@ tp_status tp_set_tile_mode(int mode) {
     if (mode != TP_TILE_AUTO && mode != TP_TILE_SINGLE && mode != TP_TILE_PAIR)
         return set_error(TP_ERR_ARG, "unknown tile mode %d", mode);
     set_tile_mode(mode);
+    return TP_OK;
+}
+
+tp_status tp_set_tail_split(int on) {
+    if (on != 0 && on != 1) return set_error(TP_ERR_ARG, "tail split flag must be 0 or 1, got %d", on);
+    set_tail_split(on != 0);
+    return TP_OK;
+}
+
+tp_status tp_set_max_gemm_pairs(int n) {
+    if (n < 0) return set_error(TP_ERR_ARG, "pair limit must be >= 0, got %d", n);
+    set_max_gemm_pairs(n);
     return TP_OK;
 }
 

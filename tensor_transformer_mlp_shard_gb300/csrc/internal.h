@@ -79,12 +79,20 @@ struct GemmPlan {
     void *q_out[kMaxShards];
     int q_fmt = 0;
     const float *q_scale_amax = nullptr;
+    // with q on an EPI_DACT plan: the codes are all that is kept, the bf16 out
+    // is not stored (out's maps are still encoded and must be valid)
+    bool q_only = false;
     // EPI_F32 split-K (S == 1): the token (K) range is split `ksplit` ways,
     // every split writes fp32 partial tiles into split_ws
     // ([ksplit][P][roundup(M, 256)][N]) and a reduction adds them in split
     // order into out (= or += with accumulate); ksplit = 1 or no split_ws: none
     int ksplit = 1;
     float *split_ws = nullptr;
+    // Tail split of the CTA-pair kernel (EPI_PLAIN / EPI_F32 on the bulk-store
+    // path, no split-K): scratch of tail_bytes at tail_ws (null: no split);
+    // tc_tail_bytes gives what a shape may use
+    void *tail_ws = nullptr;
+    size_t tail_bytes = 0;
     // EPI_PLAIN: out = residual + dropout(acc + bias) (TransformerLayer bias-dropout-add)
     bool dropout = false;
     uint32_t drop_threshold = 0;
@@ -140,6 +148,15 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st);
 bool tc_fused_epilogue(const GemmPlan &g);  // true when amax_out / col_partials are honoured
 bool tc_writes_fp8(const GemmPlan &g);      // true when q / q_out are honoured
 void set_tile_mode(int mode);  // TP_TILE_*
+// Tail split of the pair GEMMs on (default) or off, and an upper bound on the
+// CTA pairs of their persistent grid (0: as many as fit)
+void set_tail_split(bool on);
+void set_max_gemm_pairs(int n);
+uint64_t tail_split_launches();  // pair GEMM launches that split their tail
+// Scratch bytes a pair GEMM of this shape (out M x N per problem, P problems,
+// K = S segments of Kseg) may use for its tail split at the current settings;
+// 0 when it would not split
+size_t tc_tail_bytes(int M, int N, int P, int S, int Kseg, bool fp8);
 tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st);
 tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st);
 // second pass only: out_p[c] = sum_{k < chunks} partials[p][k][c]

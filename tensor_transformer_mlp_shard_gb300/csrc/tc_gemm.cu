@@ -112,10 +112,63 @@ static void copy_out(Out &o, const OutPlan &src) {
 }
 
 static std::atomic<int> g_tile_mode{0};
+static std::atomic<bool> g_tail_split{true};
+static std::atomic<int> g_max_pairs{0};
+static std::atomic<uint64_t> g_tail_launches{0};
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Persistent round structure: `total` tiles over `pairs` CTA pairs leave
+// rem = total % pairs tiles for a last, part-filled round.  When rem is at
+// most half the pairs, each of those tiles is cut along K into
+// s = min(pairs / rem, 4) units (each at least 4 of the nk K steps), which
+// all run in one round of 1/s of a tile's time.  Measured on GB300: with a
+// single round of units the split pays (the GPT-size weight gradients, 36
+// tiles over 76 pairs, 1.3% faster); spreading a fuller last round over
+// several rounds of units does not (56 tiles as 3 rounds of quarter tiles:
+// 1.3% slower, the units of a round sharing fewer operand panels in L2 than
+// whole tiles do).  Only grids with at least one full round split (smaller
+// problems keep their results bit for bit with the whole-tile path).
+struct TailPlan {
+    int s = 0, rem = 0;
+    size_t slices = 0, bytes = 0;
+};
+static TailPlan tail_plan(int total, int pairs, int nk) {
+    TailPlan r;
+    if (!g_tail_split.load() || pairs <= 0 || total <= pairs) return r;
+    const int rem = total % pairs;
+    if (rem == 0) return r;
+    const int s = std::min(std::min(pairs / rem, 4), nk / 4);
+    if (s < 2) return r;
+    r.s = s;
+    r.rem = rem;
+    r.slices = sizeof(float) * static_cast<size_t>(rem) * s * P_TILE_M * BN;
+    r.bytes = r.slices + align256(sizeof(unsigned) * 16 * static_cast<size_t>(rem));
+    return r;
+}
+
+static int pair_limit(int fit) {
+    const int lim = g_max_pairs.load();
+    return lim > 0 && lim < fit ? lim : fit;
+}
 
 }  // namespace tc
 
 void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
+void set_tail_split(bool on) { tc::g_tail_split.store(on); }
+void set_max_gemm_pairs(int n) { tc::g_max_pairs.store(n > 0 ? n : 0); }
+uint64_t tail_split_launches() { return tc::g_tail_launches.load(); }
+
+size_t tc_tail_bytes(int M, int N, int P, int S, int Kseg, bool fp8) {
+    using namespace tc;
+    const int mode = g_tile_mode.load();
+    if (M <= BM || mode == TP_TILE_SINGLE || M <= 0 || N <= 0 || P <= 0 || S <= 0 || Kseg <= 0) return 0;
+    const int bke = fp8 ? Elem<true>::BKE : Elem<false>::BKE;
+    const long long total = static_cast<long long>((M + P_TILE_M - 1) / P_TILE_M) * ((N + BN - 1) / BN) * P;
+    if (total > (1LL << 30)) return 0;
+    const int nk = S * ((Kseg + bke - 1) / bke);
+    return tail_plan(static_cast<int>(total), pair_limit(num_sms() / 2), nk).bytes;
+}
 
 bool tc_fused_epilogue(const GemmPlan &g) { return !g.accumulate && !(g.act == TP_ACT_SWIGLU && g.N % 32); }
 
@@ -181,6 +234,8 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     const int ksplit = split ? (prm.num_kb + prm.kb_split - 1) / prm.kb_split : 1;
     prm.split_rows = split ? prm.m_tiles * tile_m : 0;
     prm.total_tiles = prm.tiles_per_split * ksplit;
+    prm.total_work = prm.total_tiles;
+    prm.tail_first = prm.total_tiles;
     prm.group_m = use_pair ? 8 : 16;
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
@@ -228,6 +283,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
             prm.q_out = 1;
             prm.q_fmt = g.q_fmt;
             prm.q_scale_amax = g.q_scale_amax;
+            prm.q_only = g.q_only && g.kind == EPI_DACT ? 1 : 0;
         }
     }
     prm.drop.on = g.dropout ? 1 : 0;
@@ -291,9 +347,22 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
         }
     }
     cudaError_t e;
+    const int pairs = std::min(prm.total_tiles, pair_limit(max_pairs[dev % 64][fp8][ki]));
+    if (use_pair && prm.out_tma && !split && (g.kind == EPI_PLAIN || g.kind == EPI_F32) && g.tail_ws) {
+        const TailPlan tp = tail_plan(prm.total_tiles, pairs, g.S * prm.num_kb);
+        if (tp.s > 1 && tp.bytes <= g.tail_bytes && (reinterpret_cast<uintptr_t>(g.tail_ws) & 255u) == 0) {
+            prm.tail_s = tp.s;
+            prm.tail_first = prm.total_tiles - tp.rem;
+            prm.total_work = prm.tail_first + tp.rem * tp.s;
+            prm.tail_ws = static_cast<float *>(g.tail_ws);
+            prm.tail_cnt = reinterpret_cast<unsigned *>(static_cast<char *>(g.tail_ws) + tp.slices);
+            e = cudaMemsetAsync(prm.tail_cnt, 0, sizeof(unsigned) * 16 * static_cast<size_t>(tp.rem), st);
+            if (e != cudaSuccess) return cuda_check(e, "cudaMemsetAsync(tail counters)");
+            g_tail_launches.fetch_add(1);
+        }
+    }
     launch_begin(g.name, st);
     if (use_pair) {
-        const int pairs = std::min(prm.total_tiles, max_pairs[dev % 64][fp8][ki]);
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -79,6 +79,17 @@ struct Params {
     // (ks * P + p) * split_rows of the single partial buffer (split_rows = 0:
     // no split, the plain output addressing)
     int tiles_per_split, kb_split, split_rows;
+    // Tail split (CTA-pair kernel): when the tiles leave the last round of the
+    // persistent grid part-filled, each tile from tail_first on is cut along
+    // its flattened (segment, K block) range into tail_s units, so that the
+    // last round's work spreads over more pairs.  The work items are the
+    // tiles below tail_first, then the units; total_work counts them.  A unit
+    // writes its raw fp32 accumulator to tail_ws; the warp that completes a
+    // 32-row x 128-column slice (counted in tail_cnt, zeroed before the
+    // launch) sums the units' slices in unit order and runs the epilogue.
+    int total_work, tail_first, tail_s;
+    float *tail_ws;                  // [tail tile][tail_s][256 rows][BN] fp32
+    unsigned *tail_cnt;              // [tail tile][16 warp slices]
     int act, b_dual_off, accumulate;
     uint32_t idesc;                  // tcgen05 instruction descriptor (formats, majors, M, N)
     DropoutParams drop;              // EPI_PLAIN: out = residual + dropout(acc + bias)
@@ -86,7 +97,7 @@ struct Params {
     // dgrad) written by the epilogue when the scale is known in advance (FP8
     // delayed scaling): codes = fp8(bf16(out) * fmax / *q_scale_amax)
     CUtensorMap mapQ[kMaxShards];    // [rows, cols] bytes, boxes of 32 rows x 32 bytes
-    int q_out, q_fmt;
+    int q_out, q_fmt, q_only;        // q_only (EPI_DACT): store the codes, not the bf16 out
     const float *q_scale_amax;
     float *amax_out;                 // bulk-store epilogue: atomic max |bf16 output| (A / dPre), or null
     float *col_partials;             // DACT bulk-store epilogue: per-32-row-block column sums, or null
@@ -262,6 +273,32 @@ __device__ __forceinline__ void tile_coords(const Params &p, int t, int &pi, int
 __device__ __forceinline__ void tile_kblocks(const Params &p, int t, int &kb0, int &kb1) {
     kb0 = (t / p.tiles_per_split) * p.kb_split;
     kb1 = min(p.num_kb, kb0 + p.kb_split);
+}
+
+// Work item w of the CTA-pair kernel: tile t, its steps [f0, f1) of the
+// flattened K loop (step f = segment f / num_kb, K block f % num_kb), and
+// for a tail unit its index j within the tile (-1 for a whole tile).
+struct Work {
+    int t, f0, f1, j;
+};
+__device__ __forceinline__ Work work_item(const Params &p, int w) {
+    Work r;
+    if (w < p.tail_first) {
+        int kb0, kb1;
+        tile_kblocks(p, w, kb0, kb1);  // split-K tiles have S == 1
+        r.t = w;
+        r.f0 = kb0;
+        r.f1 = (p.S - 1) * p.num_kb + kb1;
+        r.j = -1;
+    } else {
+        const int u = w - p.tail_first;
+        const int nk = p.S * p.num_kb;
+        r.t = p.tail_first + u / p.tail_s;
+        r.j = u % p.tail_s;
+        r.f0 = static_cast<int>(static_cast<long long>(r.j) * nk / p.tail_s);
+        r.f1 = static_cast<int>(static_cast<long long>(r.j + 1) * nk / p.tail_s);
+    }
+    return r;
 }
 
 // Tensor map and local row for buffer row `row`.  A row past the last token
@@ -517,9 +554,60 @@ __device__ __forceinline__ void flush_amax(const Params &p, float amx) {
     if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned *>(p.amax_out), __float_as_uint(bf16_round(amx)));
 }
 
+// Tail-split slices: one unit's raw fp32 accumulator (256 x BN) is stored as
+// 16 warp slices of 32 rows x 128 columns (16 KB each, slice = CTA rank * 8 +
+// lane quarter * 2 + column half).  Inside a slice, float4 k (0..7) of chunk
+// c (0..3) of lane l sits at float4 index (c * 8 + k) * 32 + l, so that every
+// warp-wide access covers 512 contiguous bytes.  Accesses go through L2.
+constexpr size_t TAIL_SLICE_FLOATS = 32 * 128;
+constexpr size_t TAIL_UNIT_FLOATS = 16 * TAIL_SLICE_FLOATS;
+
+__device__ __forceinline__ void tail_store32(float *slice, int c, int lane, const uint32_t (&r)[32]) {
+    float4 *d4 = reinterpret_cast<float4 *>(slice) + c * 256 + lane;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        __stcg(d4 + 32 * k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                        __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
+}
+
+// chunk c of the tile's accumulator as the sum of its units' slices, added
+// in unit order
+__device__ __forceinline__ void tail_sum32(const float *slice, int c, int lane, int units, uint32_t (&r)[32]) {
+    float acc[32];
+    const float *src = slice + (c * 256 + lane) * 4;
+    {
+        const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 x = __ldcg(s4 + 32 * k);
+            acc[4 * k] = x.x;
+            acc[4 * k + 1] = x.y;
+            acc[4 * k + 2] = x.z;
+            acc[4 * k + 3] = x.w;
+        }
+    }
+    for (int i = 1; i < units; ++i) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(src + i * TAIL_UNIT_FLOATS);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 x = __ldcg(s4 + 32 * k);
+            acc[4 * k] += x.x;
+            acc[4 * k + 1] += x.y;
+            acc[4 * k + 2] += x.z;
+            acc[4 * k + 3] += x.w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(acc[k]);
+}
+
+// Bulk-store epilogue of one warp's 32 rows x 128 columns.  The accumulator
+// comes from TMEM at taddr, or, for a tail-split tile (ws_slice non-null),
+// from the sum of the ws_units slices from ws_slice (this warp's in unit 0).
 template <int EPI>
 __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int row, int nt, uint32_t taddr, int half,
-                                                 float dq, Stager &stg, int lane, int t) {
+                                                 float dq, Stager &stg, int lane, int t,
+                                                 const float *ws_slice = nullptr, int ws_units = 0) {
     const int row0 = row - lane;             // first row of this warp's block
     const bool block_ok = row0 < p.M;        // warp-uniform
     const bool row_ok = row < p.M;
@@ -586,10 +674,15 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
     for (int c = 4 * half; c < 4 * half + 4; ++c) {
         uint32_t r[32];
         __syncwarp();
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
         const int col0 = n0 + c * 32;
-        if (!block_ok || col0 >= p.N) continue;
+        if (ws_slice) {
+            if (!block_ok || col0 >= p.N) continue;
+            tail_sum32(ws_slice, c - 4 * half, lane, ws_units, r);
+        } else {
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+            if (!block_ok || col0 >= p.N) continue;
+        }
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * dq;
@@ -687,7 +780,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 }
                 if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
                 pack_bf16x32(v, w);
-                stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+                if (!p.q_only) stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
                 if (p.q_out) {
                     uint4 wq[2];
                     fp8_codes32(w, fp8_scale(*p.q_scale_amax, p.q_fmt == FP8_E5M2 ? 57344.0f : 448.0f), p.q_fmt,
@@ -1073,6 +1166,8 @@ constexpr int P_B_BYTES = 128 * ROW_BYTES;  // 16 KB: this CTA's 128 rows of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + BAR_BYTES + EPI_SMEM;
 constexpr int P_TILE_M = 256;
+static_assert(TAIL_UNIT_FLOATS == static_cast<size_t>(P_TILE_M) * BN, "tail slices hold one pair tile");
+static_assert(EPI_WARPS == 8, "16 tail slices: 2 CTAs x 4 lane quarters x 2 column halves");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -1204,17 +1299,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             uint32_t phase = 0;
             uint32_t armed = 0, armed_par = 0;
             bool ok = true;
-            for (int t = pair_id; ok && t < p.total_tiles; t += npairs) {
+            for (int w = pair_id; ok && w < p.total_work; w += npairs) {
+                const Work wk = work_item(p, w);
                 int pi, mt, nt;
-                tile_coords(p, t, pi, mt, nt);
+                tile_coords(p, wk.t, pi, mt, nt);
                 const int m0 = mt * P_TILE_M + 128 * rank;
                 // B rows of this CTA: its half of the 256 tile columns, or for
                 // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
                 const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
-                int kb0, kb1;
-                tile_kblocks(p, t, kb0, kb1);
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = kb0; kb < kb1; ++kb) {
+                int s = wk.f0 / p.num_kb, kb = wk.f0 - s * p.num_kb;
+                {
+                    for (int f = wk.f0; f < wk.f1; ++f) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
                             ok = false;
                             break;
@@ -1252,6 +1347,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             stage = 0;
                             phase ^= 1u;
                         }
+                        if (++kb == p.num_kb) {
+                            kb = 0;
+                            ++s;
+                        }
                     }
                 }
             }
@@ -1268,17 +1367,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             uint32_t phase = 0;
             bool ok = true;
             int it = 0;
-            for (int t = pair_id; ok && t < p.total_tiles; t += npairs, ++it) {
+            for (int w = pair_id; ok && w < p.total_work; w += npairs, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_par = (it >> 1) & 1;
                 if (!mbar_wait(tempty0 + 8 * acc, acc_par ^ 1u, p)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * BN;
                 uint32_t accumulate = 0;
-                int kb0, kb1;
-                tile_kblocks(p, t, kb0, kb1);
-                for (int s = 0; ok && s < p.S; ++s) {
-                    for (int kb = kb0; kb < kb1; ++kb) {
+                const Work wk = work_item(p, w);
+                {
+                    for (int f = wk.f0; f < wk.f1; ++f) {
                         if (!mbar_wait(full0 + 8 * stage, phase, p)) {
                             ok = false;
                             break;
@@ -1317,22 +1415,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         Stager stg{smem_base + P_STAGES * P_STAGE_BYTES + BAR_BYTES + (warp - 2) * EPI_STAGE_BYTES, 0u};
         const uint32_t tempty_leader = map_to_cta(tempty0, 0);
         int it = 0;
-        for (int t = pair_id; t < p.total_tiles; t += npairs, ++it) {
+        for (int w = pair_id; w < p.total_work; w += npairs, ++it) {
             const int acc = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             const bool ok = mbar_wait(tfull0 + 8 * acc, acc_par, p);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            const Work wk = work_item(p, w);
             int pi, mt, nt;
-            tile_coords(p, t, pi, mt, nt);
+            tile_coords(p, wk.t, pi, mt, nt);
             const int row = mt * P_TILE_M + 128 * rank + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            if (p.out_tma)
-                run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane, t);
-            else
-                run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
-            tc_fence_before();
-            mbar_arrive_cluster(tempty_leader + 8 * acc);
+            if (EPI == EPI_COL || EPI == EPI_DACT || wk.j < 0) {  // the split is planned for PLAIN / F32 only
+                if (p.out_tma)
+                    run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane, wk.t);
+                else
+                    run_epilogue<EPI>(p, pi, row, nt, taddr, half, dq);
+                tc_fence_before();
+                mbar_arrive_cluster(tempty_leader + 8 * acc);
+            } else if constexpr (EPI == EPI_PLAIN || EPI == EPI_F32) {
+                // tail unit: park this warp's raw accumulator slice, free the
+                // accumulator, and finish the slice if it is the last to arrive
+                const int tt = wk.t - p.tail_first;
+                const int slot = static_cast<int>(rank) * 8 + q * 2 + half;
+                float *ws_slice = p.tail_ws + (static_cast<size_t>(tt) * p.tail_s * 16 + slot) * TAIL_SLICE_FLOATS;
+                float *mine = ws_slice + static_cast<size_t>(wk.j) * TAIL_UNIT_FLOATS;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + (4 * half + c) * 32, r);
+                    tmem_ld_wait();
+                    tail_store32(mine, c, lane, r);
+                }
+                tc_fence_before();
+                mbar_arrive_cluster(tempty_leader + 8 * acc);
+                __threadfence();  // this thread's slice is visible before the warp's arrival counts
+                __syncwarp();
+                unsigned prev = 0;
+                if (lane == 0) prev = atomicAdd(p.tail_cnt + tt * 16 + slot, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == static_cast<unsigned>(p.tail_s - 1)) {
+                    __threadfence();  // and the other units' slices are visible to this warp
+                    run_epilogue_tma<EPI>(p, pi, row, nt, taddr, half, dq, stg, lane, wk.t, ws_slice, p.tail_s);
+                }
+            }
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();

@@ -84,8 +84,10 @@ class MlpRun:
         self.db2 = torch.full((H,), float("nan"), dtype=f32, device=device) if lay.has_bias else None
         self.ws = tp.alloc_workspace(lay.workspace_bytes()) if isinstance(lay, tp.TPMLP) else None
 
-    def fwd(self):
-        ws = self.ws if self.lay.dtype == "fp8" else None
+    def fwd(self, with_workspace=True):
+        """tp_mlp_fwd_ws with the run's workspace (for bf16 it holds only the
+        row GEMM's tail-split scratch), or plain tp_mlp_fwd."""
+        ws = self.ws if with_workspace or self.lay.dtype == "fp8" else None
         self.lay.fwd(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.pre, self.A, workspace=ws)
 
     def bwd(self):

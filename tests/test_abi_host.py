@@ -49,6 +49,15 @@ def test_abi_version_and_status_strings(tp):
     assert L.tp_status_str(5) == b"TP_ERR_TIMEOUT"
 
 
+def test_gemm_setting_validation(tp):
+    L = tp.lib()
+    assert L.tp_set_tail_split(2) == 1 and L.tp_set_tail_split(-1) == 1
+    assert L.tp_set_max_gemm_pairs(-1) == 1
+    assert L.tp_set_tail_split(0) == 0 and L.tp_set_tail_split(1) == 0
+    assert L.tp_set_max_gemm_pairs(4) == 0 and L.tp_set_max_gemm_pairs(0) == 0
+    assert L.tp_tail_split_count() == 0  # nothing launched on a host without a GPU
+
+
 def _create(tp, **kw):
     base = dict(S=128, B=2, H=256, F=1024, T=2, act="gelu_tanh", dtype="bf16")
     base.update(kw)
@@ -129,11 +138,15 @@ def test_workspace_sizes(tp):
     h = ctypes.c_void_p()
     L = tp.lib()
     assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    tp.set_tail_split(False)
     ws = L.tp_mlp_workspace_bytes(h)
+    tp.set_tail_split(True)
     dpre = 8 * 8192 * 2048 * 2
     # db1 partials: one fp32 row of column sums per 32-token block and shard
     partials = 4 * 8 * (8192 // 32) * 2048
     assert ws == dpre + partials
+    # the tail-split scratch (sized from the device's SM count) only adds at the end
+    assert L.tp_mlp_workspace_bytes(h) >= ws
     L.tp_mlp_destroy(h)
     lay2 = tp.Layout(S=2048, B=4, H=4096, F=16384, T=8, act="none", has_bias=False)
     assert tp.linear_workspace_bytes(lay2) == 0
