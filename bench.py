@@ -502,7 +502,8 @@ def run_gpu(args, w, dist, rank, local, ws):
             roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                         "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
-    if roofline is not None and w.dtype == "bf16" and not layer and roofline["bound"] == "tensor":
+    if roofline is not None and w.dtype == "bf16" and not layer and roofline["bound"] == "tensor" \
+            and not args.seq_len:
         roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
     step_frac = value / ws / (peaks["bf16_tflops_sustained"] * (2.0 if w.dtype == "fp8" else 1.0))
     return {
@@ -629,6 +630,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's sequence length S (a smaller case of the same kernels, for "
+                         "profiling); the printed config names the changed workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", default="workload", choices=["workload", "fp8"],
                     help="fp8: the FP8 variant (E4M3 forward, E5M2 backward, bf16 buffers) of the workload")
@@ -649,9 +653,11 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     w = synth.WORKLOADS[args.workload]
+    import dataclasses
     if args.dtype == "fp8":
-        import dataclasses
         w = dataclasses.replace(w, dtype="fp8")
+    if args.seq_len > 0:
+        w = dataclasses.replace(w, S=args.seq_len)
     if w.kind == "attn_proj" and (w.dtype != "bf16" or args.block != "mlp"):
         raise SystemExit("the attention projections are timed in bf16 as plain layers")
     ws, rank, local = dist_env()
