@@ -237,7 +237,7 @@ def mlp_step(args, w, tp, torch, dev, stream):
                          seq_parallel=w.seq_parallel, dropout_p=LAYER_DROPOUT_P)
     else:
         lay = tp.TPMLP(S=w.S, B=w.B, H=H, F=F, T=T, act=w.act, dtype=w.dtype, has_bias=w.has_bias,
-                       residual=w.residual, seq_parallel=w.seq_parallel)
+                       residual=w.residual, seq_parallel=w.seq_parallel, wgrad_accumulate=args.wgrad_accumulate)
     if w.dtype == "fp8" and not layer and args.fp8_history:
         lay.set_fp8_history(args.fp8_history)
     full = synth.mlp_tensors(w)
@@ -647,6 +647,8 @@ def main():
                     help="forward as one fused kernel for narrow MLPs (H <= 256): auto / on / off")
     ap.add_argument("--tile-mode", default="auto", choices=["auto", "single", "pair"],
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
+    ap.add_argument("--wgrad-accumulate", action="store_true",
+                    help="micro-batch step: the weight gradients are added into persistent fp32 buffers")
     ap.add_argument("--tail-split", default="on", choices=["on", "off"],
                     help="cut the persistent GEMMs' part-filled last round of tiles along K over all CTA pairs")
     args = ap.parse_args()
@@ -674,6 +676,7 @@ def main():
               "l2": f"inputs larger than L2 (~{step_bytes(w) / 1e9:.1f} GB of operands, activations and "
                     f"gradients per step)",
               "tile_mode": args.tile_mode, "fused_fwd": args.fused, "tail_split": args.tail_split,
+              "wgrad_accumulate": args.wgrad_accumulate,
               "launch": "CUDA graph replay per step" if args.graph else "eager C-ABI calls per step"}
     if w.dtype == "fp8":
         config["fp8_scaling"] = (f"delayed, amax history {args.fp8_history}" if args.fp8_history

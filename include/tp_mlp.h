@@ -179,7 +179,8 @@ TP_API tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n);
  * the row layer's backward has no communication, s3.2), dW2_i = dY^T A_i,
  * db2 = sum_m dY, dW1_i = dPre_i^T X, db1_i = sum_m dPre_i and
  * dX = sum_i dPre_i W1_i (+ dY if residual) in fp32 inside one kernel.
- * With wgrad_accumulate the weight gradients are added to dW1/dW2 (bias
+ * With wgrad_accumulate the weight gradients are added to dW1/dW2 (one fp32
+ * add per element and call, done by bulk reduce-add stores; bias
  * gradients are always overwritten). */
 TP_API tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X,
                      const void *const *W1, const void *const *W2,

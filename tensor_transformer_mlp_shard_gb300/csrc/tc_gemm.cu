@@ -246,12 +246,12 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     const uint32_t fa = fp8 ? uint32_t(g.fmt_a) : 1u, fb = fp8 ? uint32_t(g.fmt_b) : 1u;
     prm.idesc = (1u << 4) | (fa << 7) | (fb << 10) | (uint32_t(g.A.mn_major) << 15) |
                 (uint32_t(g.B.mn_major) << 16) | (uint32_t(BN >> 3) << 17) | (uint32_t(tile_m >> 4) << 24);
-    // Epilogue outputs go through shared memory and bulk tensor stores, except
-    // when accumulating into dW (read-modify-write) or for SwiGLU with a unit
+    // Epilogue outputs go through shared memory and bulk tensor stores (for
+    // dW accumulation, bulk reduce-add stores), except for SwiGLU with a unit
     // count that is not a multiple of 32 (a 32-column gate block would reach
     // into the up half of pre / dPre, which a store clipped at the buffer's
     // width cannot prevent).
-    prm.out_tma = (tc_fused_epilogue(g) || split) ? 1 : 0;
+    prm.out_tma = (tc_fused_epilogue(g) || split || (g.kind == EPI_F32 && g.accumulate)) ? 1 : 0;
     if (split) {
         // partial sums [ksplit][P][split_rows][N] fp32 in the caller's workspace
         Out &o = prm.out;

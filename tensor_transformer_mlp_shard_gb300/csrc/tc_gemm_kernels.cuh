@@ -378,6 +378,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  "r"(src), "r"(c0), "r"(c1)
                  : "memory");
 }
+// element-wise add of the staged block into the tensor (the L2 performs the adds)
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -399,7 +406,7 @@ struct Stager {
 };
 
 __device__ __forceinline__ void stage_store(Stager &st, const CUtensorMap *map, int x, int y, const uint4 (&w)[4],
-                                            int lane) {
+                                            int lane, bool add = false) {
     const uint32_t buf = st.base + st.toggle * 2048u;
     st.toggle ^= 1u;
     if (lane == 0) bulk_wait_read<1>();  // the store that last used this half has read it
@@ -411,7 +418,10 @@ __device__ __forceinline__ void stage_store(Stager &st, const CUtensorMap *map, 
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-        tma_store_2d(map, buf, x, y);
+        if (add)
+            tma_reduce_add_2d(map, buf, x, y);
+        else
+            tma_store_2d(map, buf, x, y);
         bulk_commit();
     }
 }
@@ -686,12 +696,13 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * dq;
-        if (EPI == EPI_F32) {
+        if (EPI == EPI_F32) {  // with accumulate: dW += through bulk reduce-add stores
+            const bool add = p.accumulate != 0;
             pack_f32x16(v, w);
-            stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
+            stage_store(stg, &p.mapO[oi], col0, oy, w, lane, add);
             if (col0 + 16 < p.N) {
                 pack_f32x16(v + 16, w);
-                stage_store(stg, &p.mapO[oi], col0 + 16, oy, w, lane);
+                stage_store(stg, &p.mapO[oi], col0 + 16, oy, w, lane, add);
             }
             continue;
         }

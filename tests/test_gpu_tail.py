@@ -219,3 +219,32 @@ def test_tail_split_needs_its_scratch(tp):
     assert rel_err(run.gathered(run.Y), ref["Y"]) <= 1e-2
     assert rel_err(run.gathered(run.dX), ref["dX"]) <= 1e-2
     tp.set_max_gemm_pairs(0)
+
+
+def test_tail_split_weight_gradient_accumulation(tp):
+    """wgrad_accumulate through the split weight gradients: the fixup adds the
+    units' sum into dW once (bulk reduce-add), so two accumulating backward
+    calls from zero give exactly twice one call."""
+    M, H, F, T = 1024, 768, 4096, 8
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    tp.set_tail_split(True)
+    tp.set_max_gemm_pairs(11)
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True,
+                   wgrad_accumulate=True)
+    run = MlpRun(lay, t)
+    run.fwd()
+    for d in run.dW1 + run.dW2:
+        d.zero_()
+    n0 = tp.tail_split_count()
+    run.bwd()
+    once = [d.clone() for d in run.dW1 + run.dW2]
+    run.bwd()
+    assert tp.sync_status() == 0
+    assert tp.tail_split_count() - n0 >= 4
+    for a, b in zip(once, run.dW1 + run.dW2):
+        assert torch.equal(2 * a, b)
+    ref = oracle_full(lay, t)
+    for i in range(T):
+        assert rel_err(host(once[i]), ref["dW1"][i]) <= 1e-2
+        assert rel_err(host(once[T + i]), ref["dW2"][i]) <= 1e-2
+    tp.set_max_gemm_pairs(0)
