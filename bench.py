@@ -606,20 +606,51 @@ def run_reference(args, w, rank, block="mlp"):
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def single_core_rate(w, block="mlp"):
+    """The oracle's rate on the whole (small) step with one BLAS thread, in a
+    child process whose thread counts are fixed before numpy loads."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys; sys.path.insert(0, %r); import bench, synth; w = synth.WORKLOADS[%r]; "
+            "dt, fl = bench.oracle_sample(w, w.M, None, %r); print(fl / dt)" % (ROOT, w.name, block))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        return float(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+
+
 def cpu_baseline(w, block="mlp"):
     """The oracle on host cores over a token sample sized to about 15 s of
-    work (a 512-token probe sets the size; at most the whole step)."""
-    probe = 512
+    work (a probe of up to 512 tokens sets the size; at most the whole step),
+    with the full step's time extrapolated from the sample's rate; for the
+    tiny workload also the whole step on one core."""
+    probe = min(512, w.M)
     full = workload_tensors(w)
     dt, fl = oracle_sample(w, probe, full, block)
     rate = fl / dt
     per_token = fl / probe
-    tokens = int(min(w.M, max(probe, 15.0 * rate / per_token)) // 512 * 512)
+    tokens = min(w.M, max(probe, int(15.0 * rate / per_token)))
+    if tokens < w.M:
+        tokens = tokens // probe * probe
     dt, fl = oracle_sample(w, tokens, full, block)
+    reps = 1
+    while dt < 5.0 and reps < 10000:  # a small whole step: repeat it for a stable rate
+        d2, f2 = oracle_sample(w, tokens, full, block)
+        dt, fl, reps = dt + d2, fl + f2, reps + 1
     what = "the whole step" if tokens == w.M else f"the first {tokens} of {w.M} tokens"
-    return {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle fwd+bwd on {what} with the full weights "
-                      f"({fl / 1e9:.0f} GFLOP, {dt:.1f} s)"}
+    if reps > 1:
+        what += f", {reps} times"
+    out = {"value": round(fl / dt / 1e12, 5), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+           "sample": f"fp64 numpy oracle fwd+bwd on {what} with the full weights "
+                     f"({fl / 1e9:.0f} GFLOP, {dt:.1f} s)",
+           "step_s": round(w.flops() * dt / fl, 4),
+           "step_s_kind": "measured" if tokens == w.M else "extrapolated from the sample's rate"}
+    if w.name == "tiny":
+        one = single_core_rate(w, block)
+        if one:
+            out["single_core"] = {"value": round(one / 1e12, 6), "unit": UNIT, "cores": 1,
+                                  "sample": "the whole step, one BLAS thread"}
+    return out
 
 
 # ---------------------------------------------------------------------------
