@@ -288,8 +288,10 @@ TP_API void tp_layer_destroy(tp_layer *h);
 
 /* Bytes of device workspace for tp_layer_bwd (and, for TP_DT_FP8,
  * tp_layer_fwd, whose quantised operands the backward reads from it): the
- * MLP's workspace, dZ and dXn ([M, H] each), then the MLP GEMMs' tail-split
- * scratch (optional, as for tp_mlp_workspace_bytes). */
+ * MLP's workspace, dZ and dXn ([M, H] each), the dropout keep-mask (bf16 and
+ * FP8 with dropout: one bit per element, ceil(H/32) 32-bit words per row),
+ * then the MLP GEMMs' tail-split scratch (optional, as for
+ * tp_mlp_workspace_bytes). */
 TP_API size_t tp_layer_workspace_bytes(const tp_layer *h);
 
 /* FP8 scaling recipe of a TP_DT_FP8 sub-block: as tp_mlp_set_fp8_history
@@ -302,8 +304,11 @@ TP_API tp_status tp_layer_set_fp8_history(tp_layer *h, int n);
  * Outputs kept for the backward: Xn [M, H] (activation dtype), mean and rstd
  * [M] fp32, pre, A.  workspace: required (>= tp_layer_workspace_bytes,
  * 256-byte aligned) for TP_DT_FP8 and then passed unchanged to tp_layer_bwd;
- * optional otherwise (may be NULL), where only the row GEMM's tail-split
- * scratch is used. */
+ * optional otherwise (may be NULL).  With dropout (bf16, FP8) the forward
+ * stores its keep flags in the workspace, and a tp_layer_bwd of the same
+ * handle given the same workspace (untouched in between) and the same seed
+ * reads them instead of redrawing them from the Philox stream (the same
+ * flags either way; the backward of the dropout becomes a pure HBM pass). */
 TP_API tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, const void *beta,
                               const void *const *W1, const void *const *b1, const void *const *W2,
                               const void *b2, uint64_t seed, void *const *Y, void *Xn, float *mean,

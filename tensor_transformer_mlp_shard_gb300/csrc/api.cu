@@ -40,6 +40,9 @@ struct tp_layer {
     float drop_scale;
     int fp8_history = 0;  // as tp_mlp
     long long fp8_fwd_steps = 0, fp8_bwd_steps = 0;
+    // workspaces whose keep-mask region a forward of this handle filled, with
+    // the seed it used (the mask is a function of the seed, p and the shape)
+    std::map<const void *, uint64_t> masks;
 };
 
 namespace tpmlp {
@@ -279,6 +282,7 @@ struct DropCfg {
     uint32_t threshold = 0;  // floor(p * 2^24)
     float scale = 1.0f;      // 1 / (1 - p)
     uint64_t seed = 0;
+    uint32_t *mask = nullptr;  // keep-mask output (ceil(H/32) words per token row), or null
 };
 
 static void set_drop(GemmPlan &g, const DropCfg *dc) {
@@ -287,6 +291,7 @@ static void set_drop(GemmPlan &g, const DropCfg *dc) {
     g.drop_threshold = dc->threshold;
     g.drop_scale = dc->scale;
     g.drop_seed = dc->seed;
+    g.drop_mask = dc->mask;
 }
 
 // Row forward: Y = sum_i X_i W_i^T + b (+R); the K loop runs over shards.
@@ -943,6 +948,7 @@ static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const 
             f.drop_threshold = drop->threshold;
             f.drop_scale = drop->scale;
             f.drop_seed = drop->seed;
+            f.drop_mask = drop->mask;
         }
         return launch_fused_mlp_fwd(f, st);
     }
@@ -1281,9 +1287,10 @@ tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out) {
 void tp_layer_destroy(tp_layer *h) { delete h; }
 
 // Workspace: [MLP workspace | dZ, later the LayerNorm partials | dXn, before
-// that the db2 partials of the dropout backward]
+// that the db2 partials of the dropout backward | the dropout keep-mask the
+// forward stores for the backward (bf16 / FP8 with dropout)]
 struct LayerWs {
-    size_t mlp, dz, dxn, end;
+    size_t mlp, dz, dxn, mask, end;
 };
 
 static LayerWs layer_ws(const tp_layer *h) {
@@ -1295,7 +1302,9 @@ static LayerWs layer_ws(const tp_layer *h) {
     L.mlp = 0;
     L.dz = align256(mlp_ws_layout(&h->inner, nullptr));
     L.dxn = L.dz + std::max(act, ln_part);
-    L.end = L.dxn + std::max(act, drop_part);
+    L.mask = L.dxn + std::max(act, drop_part);
+    const bool mask = h->d.dropout_p > 0.0f && h->inner.dtype != TP_DT_F32;
+    L.end = L.mask + (mask ? align256(sizeof(uint32_t) * static_cast<size_t>(x.M) * ((x.H + 31) / 32)) : 0);
     return L;
 }
 
@@ -1381,9 +1390,14 @@ tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, con
     dc.threshold = h->drop_threshold;
     dc.scale = h->drop_scale;
     dc.seed = seed;
+    const LayerWs L = layer_ws(h);
+    const bool store_mask = dc.on && workspace && L.end > L.mask;  // a full workspace: keep the flags
+    if (store_mask) dc.mask = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.mask);
     const Fp8Recipe rc = fp8_recipe(d->dtype, h->fp8_history, h->fp8_fwd_steps);
+    if (workspace) h->masks.erase(workspace);  // rewritten below, or no longer a pure function of its seed
     TRY(mlp_fwd_core(d, xn, W1, b1, W2, b2, X, Y, pre, A, workspace, &dc, st, rc,
                      layer_tail(h, workspace, workspace ? workspace_bytes : 0)));
+    if (store_mask) h->masks[workspace] = seed;
     if (rc.n) ++h->fp8_fwd_steps;
     return TP_OK;
 }
@@ -1445,6 +1459,11 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
         dp.drop_seed = seed;
         dp.partials = reinterpret_cast<float *>(base + L.dxn);  // free until the MLP writes dXn
         dp.db2 = d->has_bias ? static_cast<float *>(db2) : nullptr;
+        // the keep flags from the mask this handle's forward stored in this
+        // workspace with this seed; otherwise redrawn from the seed
+        const auto it = h->masks.find(workspace);
+        if (L.end > L.mask && it != h->masks.end() && it->second == seed)
+            dp.drop_mask = reinterpret_cast<const uint32_t *>(base + L.mask);
         TRY(launch_dropout_bwd(dp, ln_dtype, st));
         split_rows(dp.dz, x, dzs);
         for (int j = 0; j < x.nx; ++j) dz[j] = dzs[j];

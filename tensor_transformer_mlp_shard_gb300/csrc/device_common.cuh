@@ -56,6 +56,10 @@ struct DropoutParams {
     float scale;  // 1 / (1 - p)
     uint32_t seed_lo, seed_hi;
     long long ld;  // columns of the whole tensor (element index = row * ld + col)
+    // keep-mask output (or null): bit c % 32 of word row * mask_ld + c / 32 is
+    // the keep flag of element (row, c)
+    uint32_t *mask;
+    long long mask_ld;
 };
 
 // keep flags of the 4 elements starting at e (e % 4 == 0), applied to v[0..3]
@@ -67,6 +71,35 @@ __device__ __forceinline__ void dropout4(const DropoutParams &d, long long e, fl
     v[1] = (r.y >> 8) >= d.threshold ? v[1] * d.scale : 0.0f;
     v[2] = (r.z >> 8) >= d.threshold ? v[2] * d.scale : 0.0f;
     v[3] = (r.w >> 8) >= d.threshold ? v[3] * d.scale : 0.0f;
+}
+
+// dropout4 that also returns the 4 keep flags (bit k: element e + k kept)
+__device__ __forceinline__ uint32_t dropout4_bits(const DropoutParams &d, long long e, float *v) {
+    const unsigned long long q = static_cast<unsigned long long>(e) >> 2;
+    const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), 0u, 0u),
+                                  d.seed_lo, d.seed_hi);
+    const uint32_t k0 = (r.x >> 8) >= d.threshold, k1 = (r.y >> 8) >= d.threshold;
+    const uint32_t k2 = (r.z >> 8) >= d.threshold, k3 = (r.w >> 8) >= d.threshold;
+    v[0] = k0 ? v[0] * d.scale : 0.0f;
+    v[1] = k1 ? v[1] * d.scale : 0.0f;
+    v[2] = k2 ? v[2] * d.scale : 0.0f;
+    v[3] = k3 ? v[3] * d.scale : 0.0f;
+    return k0 | (k1 << 1) | (k2 << 2) | (k3 << 3);
+}
+
+// dropout of 32 consecutive elements of one row from column col0 (a multiple
+// of 32), storing their keep word when the mask is requested and the row exists
+__device__ __forceinline__ void dropout32(const DropoutParams &d, int row, int col0, bool row_ok, float *v) {
+    const long long e0 = static_cast<long long>(row) * d.ld + col0;
+    if (!d.mask) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dropout4(d, e0 + 4 * k, v + 4 * k);
+        return;
+    }
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bits |= dropout4_bits(d, e0 + 4 * k, v + 4 * k) << (4 * k);
+    if (row_ok) d.mask[static_cast<long long>(row) * d.mask_ld + col0 / 32] = bits;
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

@@ -408,11 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         for (int j = 0; j < 8; ++j) v[8 * g8 + j] += bb[j];
                     }
                 }
-                if (p.drop.on) {
-                    const long long e0 = static_cast<long long>(row) * p.H + col;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) dropout4(p.drop, e0 + 4 * k, v + 4 * k);
-                }
+                if (p.drop.on) dropout32(p.drop, row, col, row_ok, v);
                 if (p.has_res) {
                     const __nv_bfloat16 *res =
                         p.res[tj] + static_cast<long long>(row_ok ? tl + lane : tl) * p.H + col;
@@ -482,6 +478,8 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     prm.drop.seed_lo = static_cast<uint32_t>(f.drop_seed);
     prm.drop.seed_hi = static_cast<uint32_t>(f.drop_seed >> 32);
     prm.drop.ld = f.H;
+    prm.drop.mask = f.dropout ? f.drop_mask : nullptr;
+    prm.drop.mask_ld = (f.H + 31) / 32;
     prm.rows_split = f.rows_split;
     prm.n_tok = f.n_tok;
     prm.M = f.M;

@@ -93,11 +93,13 @@ struct GemmPlan {
     // tc_tail_bytes gives what a shape may use
     void *tail_ws = nullptr;
     size_t tail_bytes = 0;
-    // EPI_PLAIN: out = residual + dropout(acc + bias) (TransformerLayer bias-dropout-add)
+    // EPI_PLAIN: out = residual + dropout(acc + bias) (TransformerLayer bias-dropout-add);
+    // drop_mask (or null): the keep flags, bit c % 32 of word row * ceil(N/32) + c / 32
     bool dropout = false;
     uint32_t drop_threshold = 0;
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
+    uint32_t *drop_mask = nullptr;
 };
 
 // out_p[m][n] (=, or += with accumulate) sum_{k < ksplit} part[k][p][m][n],
@@ -182,6 +184,7 @@ struct FusedPlan {
     uint32_t drop_threshold = 0;
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
+    uint32_t *drop_mask = nullptr;  // as GemmPlan's drop_mask (ceil(H/32) words per row)
 };
 void set_fused_fwd_mode(int mode);  // TP_FUSED_*
 int fused_fwd_mode();
@@ -209,6 +212,9 @@ struct LnPlan {
     uint32_t drop_threshold = 0;
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
+    // dropout backward: the forward's keep-mask (ceil(H/32) words per row), or
+    // null to recompute the keep flags from the seed
+    const uint32_t *drop_mask = nullptr;
 };
 
 int ln_bwd_chunks(int M);  // upper bound on the LayerNorm backward's blocks

@@ -339,8 +339,9 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(const __grid_constan
 
 // ---------------------------------------------------------------------------
 // Dropout backward fused with the column sums of its output:
-//   dZ = dY * keep / (1 - p)   (keep flags redrawn from the forward's Philox
-//                               stream, element m*H + h),
+//   dZ = dY * keep / (1 - p)   (keep flags read from the forward's keep-mask,
+//                               or redrawn from its Philox stream, element
+//                               m*H + h, when there is none),
 //   partials[blockIdx.y][c] = sum over the block's kDropRows rows of dZ[:, c]
 // (db2 = the sum of the partial rows).  A block covers kDropRows token rows
 // and 8 * kDropThreads (bf16) or 4 * kDropThreads (fp32) columns; each thread
@@ -361,8 +362,13 @@ __global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_
     d.seed_lo = static_cast<uint32_t>(p.drop_seed);
     d.seed_hi = static_cast<uint32_t>(p.drop_seed >> 32);
     d.ld = p.H;
+    d.mask = nullptr;
+    d.mask_ld = 0;
     const int col = (blockIdx.x * kDropThreads + threadIdx.x) * V::N;
     if (col >= p.H) return;
+    // with the forward's keep-mask: V::N bits of one word per row, no Philox
+    const uint32_t *mask = p.drop_mask;
+    const long long mask_ld = (p.H + 31) / 32;
     const int r0 = blockIdx.y * kDropRows;
     const int r1 = min(p.M, r0 + kDropRows);
     float acc[V::N];
@@ -371,6 +377,7 @@ __global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_
 #pragma unroll 1
     for (int rb = r0; rb < r1; rb += kDropUnroll) {
         typename V::Raw raw[kDropUnroll];
+        uint32_t keep[kDropUnroll];
 #pragma unroll
         for (int u = 0; u < kDropUnroll; ++u) {
             const int row = rb + u;
@@ -378,6 +385,7 @@ __global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_
                 int js;
                 const long long off = shard_offset(p.rows_split, row, p.H, &js);
                 raw[u] = V::load_raw(static_cast<const T *>(p.dy[js]) + off + col);
+                if (mask) keep[u] = __ldg(mask + row * mask_ld + col / 32) >> (col % 32);
             }
         }
 #pragma unroll
@@ -387,8 +395,13 @@ __global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_
                 float v[V::N];
                 V::unpack(raw[u], v);
                 const long long e = static_cast<long long>(row) * p.H + col;
+                if (mask) {
 #pragma unroll
-                for (int j = 0; j < V::N; j += 4) dropout4(d, e + j, v + j);
+                    for (int j = 0; j < V::N; ++j) v[j] = (keep[u] >> j) & 1u ? v[j] * d.scale : 0.0f;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < V::N; j += 4) dropout4(d, e + j, v + j);
+                }
                 V::store(static_cast<T *>(p.dz) + e, v);
                 // the column sums take the stored (rounded) values: db2 = sum_m dZ as the MLP sees it
                 V::unpack(V::pack(v), v);

@@ -209,6 +209,10 @@ tp_status launch_simt_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.drop.seed_lo = static_cast<uint32_t>(g.drop_seed);
     prm.drop.seed_hi = static_cast<uint32_t>(g.drop_seed >> 32);
     prm.drop.ld = g.N;
+    prm.drop.mask = nullptr;  // the fp32 engine recomputes keep flags in the backward
+    prm.drop.mask_ld = 0;
+    if (g.dropout && g.drop_mask)
+        return set_error(TP_ERR_UNSUPPORTED, "the fp32 engine does not write a dropout keep-mask");
     if (g.M == 0 || g.N == 0 || g.P == 0) return TP_OK;
     dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, g.P);
     launch_begin(g.name, st);

@@ -292,6 +292,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.drop.seed_lo = static_cast<uint32_t>(g.drop_seed);
     prm.drop.seed_hi = static_cast<uint32_t>(g.drop_seed >> 32);
     prm.drop.ld = g.N;
+    prm.drop.mask = g.dropout ? g.drop_mask : nullptr;
+    prm.drop.mask_ld = (g.N + 31) / 32;
+    if (prm.drop.mask && !prm.out_tma)
+        return set_error(TP_ERR_UNSUPPORTED, "dropout keep-mask output needs the bulk-store epilogue");
     prm.amax_out = prm.out_tma ? g.amax_out : nullptr;
     prm.col_partials = prm.out_tma && g.kind == EPI_DACT ? g.col_partials : nullptr;
     prm.partial_ld = static_cast<int>(g.out.ld);

@@ -735,11 +735,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 stage_store_q(stg, &p.mapQ[oi], col0, oy, wq, lane);
             }
         } else if (EPI == EPI_PLAIN) {
-            if (p.drop.on) {
-                const long long e0 = static_cast<long long>(row) * p.drop.ld + col0;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) dropout4(p.drop, e0 + 4 * k, v + 4 * k);
-            }
+            if (p.drop.on) dropout32(p.drop, row, col0, row_ok, v);
             if (p.has_aux) {
                 const __nv_bfloat16 *res = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
 #pragma unroll

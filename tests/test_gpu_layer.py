@@ -192,6 +192,36 @@ def test_layer_is_deterministic(tp):
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("fused", ["off", "on"])
+def test_dropout_backward_mask_equals_redrawn_flags(tp, fused):
+    """The backward reads the keep-mask its forward stored in the workspace
+    when it gets that workspace and seed back, and redraws the flags from the
+    seed otherwise: both give the same bits (also when the fused forward
+    kernel wrote the mask), and a different seed gives other flags."""
+    M, H, F, T = 300, 256, 1024, 2
+    lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, dropout_p=0.25)
+    t = layer_inputs(M, H, F, T, "gelu_tanh", "bf16", True, seed_off=7)
+    tp.set_fused_fwd(fused)
+    run = LayerRun(lay, t)
+    run.fwd(SEED)
+    other_ws = tp.alloc_workspace(lay.workspace_bytes())
+    outs = []
+    for ws in (run.ws, other_ws):  # stored mask, then redrawn flags
+        run.ws = ws
+        run.bwd(SEED)
+        outs.append([run.gathered(run.dX), host(run.dgamma), host(run.dbeta), host(run.db2),
+                     host(run.dW1[0]), host(run.dW2[1])])
+    assert tp.sync_status() == 0
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    tp.set_fused_fwd("auto")
+    f = olayer.layer_fwd(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], "gelu_tanh",
+                         _p32(0.25), SEED)
+    gr = olayer.layer_bwd(t["dY"], t["X"], t["gamma"], t["W1s"], t["W2s"], f, "gelu_tanh", _p32(0.25))
+    assert rel_err(outs[0][0], gr["dX"]) <= 1e-2
+    assert rel_err(outs[0][3], gr["db2"]) <= 1e-2
+
+
 def test_layer_fp8_matches_fp8_oracle(tp, tile_mode):
     M, H, F, T, act, p = 512, 256, 1024, 4, "gelu_tanh", 0.1
     lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act=act, dtype="fp8", has_bias=True, dropout_p=p)
