@@ -56,6 +56,10 @@ CASES = [
     # few weight-gradient tiles and many tokens: split-K weight gradients
     (4100, 256, 512, 2, "gelu_tanh", "bf16", True, True, False),
     (4096, 192, 640, 2, "swiglu", "bf16", False, False, True),
+    # the largest shard count (TP_MAX_SHARDS = 16): 16 buffers per operand, 16 K segments
+    (2048, 264, 2048, 16, "gelu_tanh", "bf16", True, True, True),
+    (300, 136, 512, 16, "swiglu", "bf16", True, False, False),
+    (96, 72, 256, 16, "gelu_tanh", "f32", True, True, False),
 ]
 
 
