@@ -306,9 +306,12 @@ TP_API tp_status tp_layer_set_fp8_history(tp_layer *h, int n);
  * 256-byte aligned) for TP_DT_FP8 and then passed unchanged to tp_layer_bwd;
  * optional otherwise (may be NULL).  With dropout (bf16, FP8) the forward
  * stores its keep flags in the workspace, and a tp_layer_bwd of the same
- * handle given the same workspace (untouched in between) and the same seed
- * reads them instead of redrawing them from the Philox stream (the same
- * flags either way; the backward of the dropout becomes a pure HBM pass). */
+ * handle given the same workspace and the same seed reads them instead of
+ * redrawing them from the Philox stream (the same flags either way; the
+ * backward of the dropout becomes a pure HBM pass).  The backward checks
+ * each block's first row of the mask against the Philox stream and redraws
+ * the flags where it does not match, so a workspace changed in between costs
+ * time, not correctness. */
 TP_API tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, const void *beta,
                               const void *const *W1, const void *const *b1, const void *const *W2,
                               const void *b2, uint64_t seed, void *const *Y, void *Xn, float *mean,

@@ -365,12 +365,31 @@ __global__ void __launch_bounds__(kDropThreads) dropout_bwd_kernel(const __grid_
     d.mask = nullptr;
     d.mask_ld = 0;
     const int col = (blockIdx.x * kDropThreads + threadIdx.x) * V::N;
-    if (col >= p.H) return;
-    // with the forward's keep-mask: V::N bits of one word per row, no Philox
-    const uint32_t *mask = p.drop_mask;
-    const long long mask_ld = (p.H + 31) / 32;
+    const bool active = col < p.H;
     const int r0 = blockIdx.y * kDropRows;
     const int r1 = min(p.M, r0 + kDropRows);
+    // With the forward's keep-mask: V::N bits of one word per row, no Philox.
+    // The block first checks the mask's bits of its first row against the
+    // Philox stream and redraws every flag itself if any differs (a mask the
+    // workspace no longer holds is caught here, whatever the host believed).
+    const long long mask_ld = (p.H + 31) / 32;
+    const uint32_t *mask = p.drop_mask;
+    if (mask) {
+        bool bad = false;
+        if (active && r0 < r1) {
+            float probe[V::N];
+#pragma unroll
+            for (int j = 0; j < V::N; ++j) probe[j] = 1.0f;
+            const long long e = static_cast<long long>(r0) * p.H + col;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int j = 0; j < V::N; j += 4) bits |= dropout4_bits(d, e + j, probe + j) << j;
+            const uint32_t want = (mask[r0 * mask_ld + col / 32] >> (col % 32)) & ((1u << V::N) - 1u);
+            bad = bits != want;
+        }
+        if (__syncthreads_or(bad)) mask = nullptr;
+    }
+    if (!active) return;
     float acc[V::N];
 #pragma unroll
     for (int j = 0; j < V::N; ++j) acc[j] = 0.0f;

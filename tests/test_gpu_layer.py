@@ -196,24 +196,30 @@ def test_layer_is_deterministic(tp):
 def test_dropout_backward_mask_equals_redrawn_flags(tp, fused):
     """The backward reads the keep-mask its forward stored in the workspace
     when it gets that workspace and seed back, and redraws the flags from the
-    seed otherwise: both give the same bits (also when the fused forward
-    kernel wrote the mask), and a different seed gives other flags."""
+    seed otherwise or when the mask fails the kernel's check: all give the
+    same bits (also when the fused forward kernel wrote the mask)."""
     M, H, F, T = 300, 256, 1024, 2
     lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, dropout_p=0.25)
     t = layer_inputs(M, H, F, T, "gelu_tanh", "bf16", True, seed_off=7)
     tp.set_fused_fwd(fused)
     run = LayerRun(lay, t)
     run.fwd(SEED)
+    fwd_ws = run.ws
     other_ws = tp.alloc_workspace(lay.workspace_bytes())
     outs = []
-    for ws in (run.ws, other_ws):  # stored mask, then redrawn flags
+    for ws, scribble in ((fwd_ws, False), (other_ws, False), (fwd_ws, True)):
+        # stored mask; redrawn flags; a mask the workspace no longer holds (the
+        # kernel's check of each block's first row catches it and redraws)
+        if scribble:
+            ws.random_(0, 256)
         run.ws = ws
         run.bwd(SEED)
         outs.append([run.gathered(run.dX), host(run.dgamma), host(run.dbeta), host(run.db2),
                      host(run.dW1[0]), host(run.dW2[1])])
     assert tp.sync_status() == 0
-    for a, b in zip(*outs):
-        assert np.array_equal(a, b)
+    for later in outs[1:]:
+        for a, b in zip(outs[0], later):
+            assert np.array_equal(a, b)
     tp.set_fused_fwd("auto")
     f = olayer.layer_fwd(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], "gelu_tanh",
                          _p32(0.25), SEED)
