@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, times, out):
 def test_max_over_ranks_and_job_throughput_gloo():
     world = 2
     times = [40.0, 55.0]  # ms for 10 steps on each rank
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (threaded) process
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, _free_port(), times, out), nprocs=world, join=True)
     for r in range(world):
