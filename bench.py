@@ -737,7 +737,7 @@ def main():
     if rank == 0:
         out = dict(base)
         out.update(res)
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and ws == 1:  # the CPU baseline is an N = 1 measurement
             out["cpu_baseline"] = cpu_baseline(w, args.block)
         print(json.dumps(out))
     if dist is not None:
