@@ -82,8 +82,10 @@ typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act
  * tensor -- E4M3 (fmax 448) for X, W1, W2 and the activation A in the forward,
  * E5M2 (fmax 57344) for dY and dPre in the backward -- the products run on
  * tcgen05 kind::f8f6f4 in fp32 and are dequantised by 1/(scale_a*scale_b)
- * before the epilogue.  pre, A, dPre, Y, dX stay bf16; bias gradients sum the
- * unquantised bf16 dPre and dY.  Needs H and F/T multiples of 16, the forward
+ * before the epilogue.  pre, A, Y, dX stay bf16 (and dPre, except under
+ * delayed scaling, where the act' dgrad stores only its codes); bias
+ * gradients sum dPre and dY before quantisation.  Needs H and F/T multiples
+ * of 16, the forward
  * through tp_mlp_fwd_ws, and the same workspace for the following backward
  * (it carries the quantised forward operands).  MLP entry points only. */
 typedef enum { TP_DT_F32 = 0, TP_DT_BF16 = 1, TP_DT_FP8 = 2 } tp_dtype;
