@@ -54,6 +54,17 @@ __device__ __forceinline__ float *out_at(const Out &o, int pi, int row) {
     return o.ptr[idx] + static_cast<long long>(row) * o.ld;
 }
 
+// Base pointer of an operand for problem pi and K segment s when it is not
+// token-sharded (then every element comes from one buffer), else null.
+__device__ __forceinline__ const float *op_base(const Op &o, int pi, int s) {
+    return o.rows_split ? nullptr : o.ptr[pi * o.p_stride + s * o.s_stride];
+}
+
+__device__ __forceinline__ float op_at(const Op &o, const float *base, int pi, int s, int mn, int k) {
+    if (base) return base[static_cast<long long>(o.mn_major ? k : mn) * o.ld + (o.mn_major ? mn : k)];
+    return op_get(o, pi, s, mn, k);
+}
+
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ Params p) {
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs[TK][TN + 4];
@@ -64,21 +75,22 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
     const bool dual = p.b_dual_off != 0;
     float acc[4][4] = {}, acc2[4][4] = {};
     for (int s = 0; s < p.S; ++s) {
+        const float *abase = op_base(p.A, pi, s), *bbase = op_base(p.B, pi, s);
         for (int k0 = 0; k0 < p.Kseg; k0 += TK) {
             for (int e = threadIdx.x; e < TK * TM; e += blockDim.x) {
                 // consecutive threads walk the operand's contiguous dimension
                 int kk, mm;
                 if (p.A.mn_major) { mm = e % TM; kk = e / TM; } else { kk = e % TK; mm = e / TK; }
                 const int m = m0 + mm, k = k0 + kk;
-                As[kk][mm] = (m < p.M && k < p.Kseg) ? op_get(p.A, pi, s, m, k) : 0.0f;
+                As[kk][mm] = (m < p.M && k < p.Kseg) ? op_at(p.A, abase, pi, s, m, k) : 0.0f;
             }
             for (int e = threadIdx.x; e < TK * TN; e += blockDim.x) {
                 int kk, nn;
                 if (p.B.mn_major) { nn = e % TN; kk = e / TN; } else { kk = e % TK; nn = e / TK; }
                 const int n = n0 + nn, k = k0 + kk;
                 const bool ok = n < p.N && k < p.Kseg;
-                Bs[kk][nn] = ok ? op_get(p.B, pi, s, n, k) : 0.0f;
-                if (dual) Bs2[kk][nn] = ok ? op_get(p.B, pi, s, n + p.b_dual_off, k) : 0.0f;
+                Bs[kk][nn] = ok ? op_at(p.B, bbase, pi, s, n, k) : 0.0f;
+                if (dual) Bs2[kk][nn] = ok ? op_at(p.B, bbase, pi, s, n + p.b_dual_off, k) : 0.0f;
             }
             __syncthreads();
 #pragma unroll
