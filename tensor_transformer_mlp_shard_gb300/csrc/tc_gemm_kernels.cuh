@@ -88,6 +88,12 @@ struct Params {
     // 32-row x 128-column slice (counted in tail_cnt, zeroed before the
     // launch) sums the units' slices in unit order and runs the epilogue.
     int total_work, tail_first, tail_s;
+    // CTA-pair kernel, bf16: an MN-major operand whose MN extent is a multiple
+    // of 64 is loaded as one 3D box {64 elements, 64 K rows, 2 groups of 64}
+    // (its map views [K, MN] as {64, K, MN / 64} with strides {row pitch, 128
+    // bytes}), landing as the two 8 KB swizzle atoms of the 128-wide tile that
+    // two 2D boxes would write
+    int a3d, b3d;
     float *tail_ws;                  // [tail tile][tail_s][256 rows][BN] fp32
     unsigned *tail_cnt;              // [tail tile][16 warp slices]
     int act, b_dual_off, accumulate;
@@ -1207,6 +1213,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int c0,
+                                                 int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
 }
@@ -1337,18 +1351,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             tma_load_2d_pair(sa, &p.mapA[idx], fb, k0, lrow);
                         } else {
                             select(p.selA, pi, s, k0, idx, lrow);
+                            if (!F8 && p.a3d) {
+                                tma_load_3d_pair(sa, &p.mapA[idx], fb, 0, lrow, m0 / 64);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < 128 / E::MNB; ++j)
-                                tma_load_2d_pair(sa + j * E::MNB_BYTES, &p.mapA[idx], fb, m0 + j * E::MNB, lrow);
+                                for (int j = 0; j < 128 / E::MNB; ++j)
+                                    tma_load_2d_pair(sa + j * E::MNB_BYTES, &p.mapA[idx], fb, m0 + j * E::MNB, lrow);
+                            }
                         }
                         if (!B_MN) {
                             select(p.selB, pi, s, n0, idx, lrow);
                             tma_load_2d_pair(sb, &p.mapB[idx], fb, k0, lrow);
                         } else {
                             select(p.selB, pi, s, k0, idx, lrow);
+                            if (!F8 && p.b3d) {
+                                tma_load_3d_pair(sb, &p.mapB[idx], fb, 0, lrow, n0 / 64);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < 128 / E::MNB; ++j)
-                                tma_load_2d_pair(sb + j * E::MNB_BYTES, &p.mapB[idx], fb, n0 + j * E::MNB, lrow);
+                                for (int j = 0; j < 128 / E::MNB; ++j)
+                                    tma_load_2d_pair(sb + j * E::MNB_BYTES, &p.mapB[idx], fb, n0 + j * E::MNB, lrow);
+                            }
                         }
                         if (++stage == P_STAGES) {
                             stage = 0;
