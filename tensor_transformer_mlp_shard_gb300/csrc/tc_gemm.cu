@@ -345,7 +345,8 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     static int max_pairs[64][2][kNumKernels] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int smem_bytes = use_pair ? P_SMEM_BYTES : SMEM_BYTES;
+    const int smem_bytes = use_pair ? pair_smem_bytes(g.kind == EPI_DACT ? pair_stages<EPI_DACT>() : P_STAGES)
+                                    : SMEM_BYTES;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev % 64][fp8][use_pair][ki]) {
