@@ -403,7 +403,8 @@ static tp_status wgrad(const tp_mlp_desc *d, const char *name, const void *const
 
 // Column-layer dgrad: dX = sum_i dOut_i W_i (+R); the K loop runs over shards.
 static tp_status column_dgrad(const tp_mlp_desc *d, const void *const *dOut, int kw, const void *const *W,
-                              const void *const *R, void *const *dX, cudaStream_t st, Scratch tail = {}) {
+                              const void *const *R, void *const *dX, cudaStream_t st, Scratch tail = {},
+                              float *res_partials = nullptr) {
     const Dims x = dims_of(d);
     GemmPlan g;
     g.name = "col_dgrad";
@@ -417,6 +418,8 @@ static tp_status column_dgrad(const tp_mlp_desc *d, const void *const *dOut, int
     set_operand(g.B, W, x.T, kw, x.H, true, 0, 1, 0);
     set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
     if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
+    // the residual's per-32-row column sums (db2 partials), tcgen05 engine only
+    if (R && d->dtype != TP_DT_F32) g.col_partials = res_partials;
     set_bias(g, nullptr, 0, 0);
     set_tail(g, tail);
     return run_gemm(g, d->dtype, st);
@@ -449,6 +452,19 @@ static tp_status db1_finalize(const tp_mlp_desc *d, int gw, void *const *db1, fl
     return launch_colsum_finalize(c, (x.M + 31) / 32, st);
 }
 
+// db2 from the column dgrad epilogue's per-32-row-block sums of its residual dY
+static tp_status db2_finalize(const tp_mlp_desc *d, void *db2, float *partials, cudaStream_t st) {
+    const Dims x = dims_of(d);
+    ColsumPlan c;
+    c.name = "bias_grad_row";
+    c.P = 1;
+    c.M = x.M;
+    c.N = x.H;
+    for (int i = 0; i < kMaxShards; ++i) c.out[i] = i == 0 ? static_cast<float *>(db2) : nullptr;
+    c.partials = partials;
+    return launch_colsum_finalize(c, (x.M + 31) / 32, st);
+}
+
 static size_t partials_bytes(const tp_mlp_desc *d, int P, int N) {
     const Dims x = dims_of(d);
     return align256(sizeof(float) * static_cast<size_t>(P) * colsum_chunks(x.M) * N);
@@ -462,7 +478,8 @@ static size_t bias_part_bytes(const tp_mlp_desc *d) {
     // db1: colsum partials, or the fused epilogue's per-32-row-block sums
     const size_t a = partials_bytes(d, x.T, x.g * x.Fs), b = partials_bytes(d, 1, x.H);
     const size_t c = align256(sizeof(float) * size_t(x.T) * ((x.M + 31) / 32) * x.g * x.Fs);
-    return std::max(a, std::max(b, c));
+    const size_t e = align256(sizeof(float) * size_t((x.M + 31) / 32) * x.H);  // db2 from the column dgrad
+    return std::max(std::max(a, e), std::max(b, c));
 }
 
 static size_t bwd_ws_bytes(const tp_mlp_desc *d, size_t *dpre_shard_bytes, size_t *split_off = nullptr) {
@@ -838,7 +855,15 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_tail(g, tail);
         TRY(launch_tc_gemm(g, st));
     }
-    // column layer dgrad: dX = sum_i dPq_i W1q_i / (s_dp s_w1) (+ dY)
+    if (d->has_bias) {  // db1 now: the partials region then takes the db2 partials
+        if (dp_fused)
+            TRY(db1_finalize(d, gw, db1, partials, st));
+        else
+            TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
+    }
+    // column layer dgrad: dX = sum_i dPq_i W1q_i / (s_dp s_w1) (+ dY); with the
+    // residual its epilogue also sums dY per 32-row block (db2 = sum_m dY)
+    const bool db2_fused = db2 && d->residual;
     {
         GemmPlan g;
         g.name = "col_dgrad";
@@ -852,18 +877,18 @@ static tp_status fp8_bwd(const tp_mlp_desc *d, const void *const *dY, const void
         set_operand(g.B, w1q, x.T, gw, x.H, true, 0, 1, 0);
         set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
         if (d->residual) set_out(g.aux, dY, x.nx, 0, x.rs, x.H);
+        if (db2_fused) g.col_partials = partials;
         set_bias(g, nullptr, 0, 0);
         set_fp8(g, FP8_E5M2, FP8_E4M3, sa, AMAX_DP, AMAX_W1);
         set_tail(g, tail);
         TRY(launch_tc_gemm(g, st));
     }
-    if (d->has_bias) {
+    if (db2) {
         void *const *db2a = reinterpret_cast<void *const *>(&db2);
-        if (dp_fused)
-            TRY(db1_finalize(d, gw, db1, partials, st));
+        if (db2_fused)
+            TRY(db2_finalize(d, db2, partials, st));
         else
-            TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
-        if (db2) TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+            TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
 }
@@ -987,16 +1012,23 @@ static tp_status mlp_bwd_core(const tp_mlp_desc *d, const void *const *dY, const
     // row layer: dPre_i = (dY W2_i) * act'(pre_i), dW2_i = dY^T A_i
     bool db1_fused = false;
     TRY(row_dgrad(d, d->act, dY, W2, pre, dpre, gw, st, d->has_bias ? partials : nullptr, &db1_fused));
-    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st, split, tail));
-    // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY)
-    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st, split, tail));
-    TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st, tail));
-    if (d->has_bias) {
+    if (d->has_bias) {  // db1 now: the partials region then takes the db2 partials
         if (db1_fused)
             TRY(db1_finalize(d, gw, db1, partials, st));
         else
             TRY(colsum(d, "bias_grad_col", dpre, x.T, 1, 0, x.T, gw, db1, partials, st));
-        if (!db2_done) TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
+    }
+    TRY(wgrad(d, "wgrad_row", dY, 0, x.H, A, 1, x.Fs, dW2, st, split, tail));
+    // column layer: dW1_i = dPre_i^T X, dX = sum_i dPre_i W1_i (+ dY); with the
+    // residual its epilogue also sums dY per 32-row block (db2 = sum_m dY)
+    TRY(wgrad(d, "wgrad_col", dpre, 1, gw, X, 0, x.H, dW1, st, split, tail));
+    const bool db2_fused = d->has_bias && !db2_done && d->residual && d->dtype != TP_DT_F32;
+    TRY(column_dgrad(d, dpre, gw, W1, d->residual ? dY : nullptr, dX, st, tail, db2_fused ? partials : nullptr));
+    if (d->has_bias && !db2_done) {
+        if (db2_fused)
+            TRY(db2_finalize(d, db2, partials, st));
+        else
+            TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, db2a, partials, st));
     }
     return TP_OK;
 }

@@ -70,7 +70,8 @@ struct GemmPlan {
     // Reductions fused into the bulk-store epilogue (tc_fused_epilogue(g)):
     // atomic max of |out| as bf16 (the FP8 amax of A / dPre; zero it first) and,
     // for EPI_DACT, column sums of out per 32-row block into
-    // col_partials[P][ceil(M/32)][out.ld] (the db1 partials).
+    // col_partials[P][ceil(M/32)][out.ld] (the db1 partials); for EPI_PLAIN
+    // with aux, the same column sums of the residual (db2 from dY).
     float *amax_out = nullptr;
     float *col_partials = nullptr;
     // FP8 codes of the output written by the epilogue (tc_writes_fp8(g)):

@@ -323,7 +323,8 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     if (prm.drop.mask && !prm.out_tma)
         return set_error(TP_ERR_UNSUPPORTED, "dropout keep-mask output needs the bulk-store epilogue");
     prm.amax_out = prm.out_tma ? g.amax_out : nullptr;
-    prm.col_partials = prm.out_tma && g.kind == EPI_DACT ? g.col_partials : nullptr;
+    prm.col_partials =
+        prm.out_tma && (g.kind == EPI_DACT || (g.kind == EPI_PLAIN && g.aux.n > 0)) ? g.col_partials : nullptr;
     prm.partial_ld = static_cast<int>(g.out.ld);
     prm.amax_a = fp8 ? g.amax_a : nullptr;
     prm.amax_b = fp8 ? g.amax_b : nullptr;

@@ -744,13 +744,16 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
             if (p.drop.on) dropout32(p.drop, row, col0, row_ok, v);
             if (p.has_aux) {
                 const __nv_bfloat16 *res = row_ptr<const __nv_bfloat16>(p.aux, pi, row_ok ? row : row0);
+                float r32[32];
 #pragma unroll
                 for (int g8 = 0; g8 < 4; ++g8) {
-                    float rr[8];
-                    load_bf16x8_guarded(res + col0 + 8 * g8, row_ok && col0 + 8 * g8 < p.N, rr);
+                    load_bf16x8_guarded(res + col0 + 8 * g8, row_ok && col0 + 8 * g8 < p.N, r32 + 8 * g8);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[8 * g8 + j] += rr[j];
+                    for (int j = 0; j < 8; ++j) v[8 * g8 + j] += r32[8 * g8 + j];
                 }
+                // column sums of the residual per 32-row block (the row layer's
+                // bias gradient, sum_m dY, when the residual is dY)
+                if (p.col_partials) fused_reductions(p, pi, row0, col0, r32, row_ok, lane, amx);
             }
             pack_bf16x32(v, w);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
