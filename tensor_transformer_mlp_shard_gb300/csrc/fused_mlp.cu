@@ -362,10 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         pack_bf16x32(v, wa[hh]);
                         if (row_ok) store_row32(p.pre[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
                     }
-                    if (p.act == TP_ACT_GELU_TANH) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_fast(v[j]);
-                    }
+                    if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
                     pack_bf16x32(v, wa[hh]);
                     if (row_ok) store_row32(p.A[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
                 }
