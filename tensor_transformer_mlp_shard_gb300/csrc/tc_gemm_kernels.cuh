@@ -540,14 +540,14 @@ __device__ __forceinline__ void fp8_codes32(const uint4 (&w)[4], float s, int fm
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const float2 a = make_float2(bf16_lo(ws[k]) * s, bf16_hi(ws[k]) * s);
+            const float2 a = __fmul2_rn(make_float2(bf16_lo(ws[k]), bf16_hi(ws[k])), f2(s));
             const uint32_t v = fmt == FP8_E5M2 ? __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E5M2)
                                                : __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
             lo |= v << (16 * k);
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const float2 a = make_float2(bf16_lo(ws[2 + k]) * s, bf16_hi(ws[2 + k]) * s);
+            const float2 a = __fmul2_rn(make_float2(bf16_lo(ws[2 + k]), bf16_hi(ws[2 + k])), f2(s));
             const uint32_t v = fmt == FP8_E5M2 ? __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E5M2)
                                                : __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
             hi |= v << (16 * k);
@@ -602,26 +602,31 @@ __device__ __forceinline__ void load_bf16x8_guarded(const __nv_bfloat16 *src, bo
 // `lane` in v[0] after 31 shuffles.
 __device__ __forceinline__ float warp_column_sum32(float (&v)[32], int lane) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 16; o >= 2; o >>= 1) {  // adds on fp32 pairs
         const bool upper = (lane & o) != 0;
 #pragma unroll
-        for (int j = 0; j < o; ++j) {
-            const float send = upper ? v[j] : v[j + o];
-            const float keep = upper ? v[j + o] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int j = 0; j < o; j += 2) {
+            const float2 lo = ld2(v + j), hi = ld2(v + j + o);
+            const float2 send = upper ? lo : hi;
+            const float2 keep = upper ? hi : lo;
+            const float2 got = make_float2(__shfl_xor_sync(0xffffffffu, send.x, o),
+                                           __shfl_xor_sync(0xffffffffu, send.y, o));
+            st2(v + j, __fadd2_rn(keep, got));
         }
     }
-    return v[0];
+    const bool upper = (lane & 1) != 0;
+    const float send = upper ? v[0] : v[1];
+    const float keep = upper ? v[1] : v[0];
+    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// db1 partials and amax of one 32-column block of outputs: rows past M and
-// columns past N contribute nothing.  The partial sums add the fp32 values the
-// epilogue rounds to bf16; the amax is rounded once when flushed (rounding is
-// monotone, so max |bf16(v)| = bf16(max |v|)).
-__device__ __forceinline__ void fused_reductions(const Params &p, int pi, int row0, int col0, const float *vals,
-                                                 bool row_ok, int lane, float &amx, int part_off = 0) {
+// Column sums (bias-gradient partials) of one 32-column block of fp32 values,
+// one row per lane: rows past M and columns past N contribute nothing.
+__device__ __forceinline__ void col_partial_sums(const Params &p, int pi, int row0, int col0, const float *vals,
+                                                 bool row_ok, int lane, int part_off = 0) {
+    if (!p.col_partials) return;
     float v[32];
     if (row_ok && col0 + 32 <= p.N) {
 #pragma unroll
@@ -630,23 +635,41 @@ __device__ __forceinline__ void fused_reductions(const Params &p, int pi, int ro
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = (row_ok && col0 + j < p.N) ? vals[j] : 0.0f;
     }
-    if (p.amax_out) {
+    const float sum = warp_column_sum32(v, lane);
+    if (col0 + lane < p.N)
+        p.col_partials[(static_cast<long long>(pi) * ((p.M + 31) / 32) + row0 / 32) * p.partial_ld + part_off + col0 +
+                       lane] = sum;
+}
+
+// Running max |x| over the bf16 outputs (the FP8 scale of A or dPre), taken on
+// the packed pairs the epilogue stores: max.xorsign.abs keeps max(|a|, |b|) in
+// each half (its sign bits are ignored).  Max |bf16(v)| is the same as the
+// rounded max |v| (rounding is monotone).  Rows past M and column pairs past N
+// contribute nothing (N % 8 == 0, so a pair is inside or outside).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void amax_bf16x32(const Params &p, const uint4 (&w)[4], bool row_ok, int col0,
+                                             uint32_t &amx) {
+    if (!p.amax_out || !row_ok) return;
+    const bool full = col0 + 32 <= p.N;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) amx = fmaxf(amx, fabsf(v[j]));
-    }
-    if (p.col_partials) {
-        const float sum = warp_column_sum32(v, lane);
-        if (col0 + lane < p.N)
-            p.col_partials[(static_cast<long long>(pi) * ((p.M + 31) / 32) + row0 / 32) * p.partial_ld + part_off + col0 +
-                           lane] = sum;
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t q[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (full || col0 + 8 * k + 2 * i < p.N) amx = absmax_bf16x2(amx, q[i]);
     }
 }
 
-__device__ __forceinline__ void flush_amax(const Params &p, float amx) {
+__device__ __forceinline__ void flush_amax(const Params &p, uint32_t amx2) {
     if (!p.amax_out) return;
+    float amx = fmaxf(fabsf(bf16_lo(amx2)), fabsf(bf16_hi(amx2)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amx = fmaxf(amx, __shfl_xor_sync(0xffffffffu, amx, o));
-    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned *>(p.amax_out), __float_as_uint(bf16_round(amx)));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned *>(p.amax_out), __float_as_uint(amx));
 }
 
 // Tail-split slices: one unit's raw fp32 accumulator (256 x BN) is stored as
@@ -715,8 +738,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
     if (p.has_out2) out_index(p.out2, pi, row0, oi2, oy2);
     const __nv_bfloat16 *bias =
         p.has_bias ? reinterpret_cast<const __nv_bfloat16 *>(p.bias[pi * p.bias_p_stride]) : nullptr;
-    const bool fuse = p.amax_out != nullptr || p.col_partials != nullptr;
-    float amx = 0.0f;  // max |bf16 output| of this thread (FP8 scale of A / dPre)
+    uint32_t amx = 0;  // max |bf16 output| of this thread, as a bf16 pair (FP8 scale of A / dPre)
     uint4 w[4];
     if (EPI == EPI_COL && p.act == TP_ACT_SWIGLU) {
         // accumulator columns [0,128) = gate units, [128,256) = up units (N % 32 == 0 here)
@@ -750,11 +772,11 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 stage_store(stg, &p.mapO2[oi2], p.N + u0, oy2, w, lane);
             }
             swiglu_n<32>(G, U);
-            if (fuse) fused_reductions(p, pi, row0, u0, G, row_ok, lane, amx);
             pack_bf16x32(G, w);
+            amax_bf16x32(p, w, row_ok, u0, amx);
             stage_store(stg, &p.mapO[oi], u0, oy, w, lane);
         }
-        if (fuse) flush_amax(p, amx);
+        flush_amax(p, amx);
         return;
     }
     const int n0 = nt * BN;
@@ -799,8 +821,8 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 stage_store(stg, &p.mapO2[oi2], col0, oy2, w, lane);
             }
             if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
-            if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
             pack_bf16x32(v, w);
+            amax_bf16x32(p, w, row_ok, col0, amx);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
             if (p.q_out) {
                 uint4 wq[2];
@@ -819,7 +841,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                 }
                 // column sums of the residual per 32-row block (the row layer's
                 // bias gradient, sum_m dY, when the residual is dY)
-                if (p.col_partials) fused_reductions(p, pi, row0, col0, r32, row_ok, lane, amx);
+                col_partial_sums(p, pi, row0, col0, r32, row_ok, lane);
             }
             pack_bf16x32(v, w);
             stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
@@ -835,14 +857,14 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                     load_bf16x8_guarded(pre + p.N + col0 + 8 * g8, ok, U);
                     swiglu_grad_n<8>(v + 8 * g8, dU + 8 * g8, G, U);
                 }
-                if (fuse) {
-                    // dG feeds db1 columns [0, N), dU columns [N, 2N)
-                    fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
-                    fused_reductions(p, pi, row0, col0, dU, row_ok, lane, amx, p.N);
-                }
+                // dG feeds db1 columns [0, N), dU columns [N, 2N)
+                col_partial_sums(p, pi, row0, col0, v, row_ok, lane);
+                col_partial_sums(p, pi, row0, col0, dU, row_ok, lane, p.N);
                 pack_bf16x32(v, w);
+                amax_bf16x32(p, w, row_ok, col0, amx);
                 stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
                 pack_bf16x32(dU, w);
+                amax_bf16x32(p, w, row_ok, col0, amx);
                 stage_store(stg, &p.mapO[oi], p.N + col0, oy, w, lane);
             } else {
                 if (p.act == TP_ACT_GELU_TANH) {
@@ -853,8 +875,9 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
                         mul_gelu_tanh_grad_n<8>(v + 8 * g8, x);
                     }
                 }
-                if (fuse) fused_reductions(p, pi, row0, col0, v, row_ok, lane, amx);
+                col_partial_sums(p, pi, row0, col0, v, row_ok, lane);
                 pack_bf16x32(v, w);
+                amax_bf16x32(p, w, row_ok, col0, amx);
                 if (!p.q_only) stage_store(stg, &p.mapO[oi], col0, oy, w, lane);
                 if (p.q_out) {
                     uint4 wq[2];
@@ -865,7 +888,7 @@ __device__ __forceinline__ void run_epilogue_tma(const Params &p, int pi, int ro
             }
         }
     }
-    if (fuse) flush_amax(p, amx);
+    flush_amax(p, amx);
 }
 
 template <int EPI>
