@@ -170,6 +170,21 @@ TP_API tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *cons
  * again clears the history.  Host only.  TP_ERR_ARG for n outside 0..64. */
 TP_API tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n);
 
+/* The per-tensor amaxes (max |x| over all shards, fp32) the last calls of a
+ * TP_DT_FP8 handle recorded in `workspace` (the one passed to them), in the
+ * order X, W1, W2, A (set by tp_mlp_fwd_ws), dY, dPre (set by tp_mlp_bwd):
+ * the values that enter the scales of the next call (delayed scaling) or
+ * gave this call's (current scaling).  A's and dPre's come from the GEMM
+ * epilogues that produce them when their scale is known beforehand, and are
+ * the max over the bf16 values they round to.  out: TP_FP8_AMAX_COUNT floats
+ * in device or host memory (copied with cudaMemcpyDefault on `stream`;
+ * pageable host memory makes the copy synchronous).  TP_ERR_ARG for a NULL
+ * handle or out, a handle that is not TP_DT_FP8, or a workspace that is
+ * NULL, unaligned or smaller than the FP8 region. */
+#define TP_FP8_AMAX_COUNT 6
+TP_API tp_status tp_mlp_fp8_amax(const tp_mlp *h, const void *workspace, size_t workspace_bytes, float *out,
+                                 void *stream);
+
 /* ---- MLP backward ------------------------------------------------------------
  * dY  : like Y;  X, W1, W2, pre, A: as passed to / produced by tp_mlp_fwd
  * dX  : like X (bf16/f32 per dtype)

@@ -60,6 +60,7 @@ SIGNATURES = {
     "tp_mlp_fwd": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP]),
     "tp_mlp_fwd_ws": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_mlp_set_fp8_history": (ctypes.c_int, [VP, ctypes.c_int]),
+    "tp_mlp_fp8_amax": (ctypes.c_int, [VP, VP, ctypes.c_size_t, VP, VP]),
     "tp_mlp_bwd": (ctypes.c_int, [VP, PP, PP, PP, PP, PP, PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_col": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP]),
     "tp_linear_row": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP]),
@@ -220,6 +221,16 @@ class TPMLP(Layout):
         current scaling).  Clears the history; pass the same workspace to
         every later fwd / bwd."""
         _check(lib().tp_mlp_set_fp8_history(self._h, int(n)))
+
+    FP8_AMAX_NAMES = ("X", "W1", "W2", "A", "dY", "dPre")
+
+    def fp8_amax(self, workspace, stream=None):
+        """The per-tensor amaxes the last fwd / bwd recorded in `workspace`, as
+        a CUDA float32 tensor in the order of FP8_AMAX_NAMES (dtype "fp8")."""
+        ws_ptr, ws_bytes = _workspace(workspace)
+        out = torch.empty(len(self.FP8_AMAX_NAMES), dtype=torch.float32, device=workspace.device)
+        _check(lib().tp_mlp_fp8_amax(self._h, ws_ptr, ws_bytes, out.data_ptr(), _stream(stream)))
+        return out
 
     def fwd(self, X, W1, b1, W2, b2, Y, pre, A, stream=None, workspace=None):
         """Forward; `workspace` (required for dtype "fp8") must then be passed,

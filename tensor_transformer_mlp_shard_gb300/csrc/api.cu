@@ -1558,6 +1558,18 @@ tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n) {
     return TP_OK;
 }
 
+tp_status tp_mlp_fp8_amax(const tp_mlp *h, const void *workspace, size_t workspace_bytes, float *out, void *stream) {
+    if (!h || !out) return set_error(TP_ERR_ARG, "handle or out is NULL");
+    if (h->d.dtype != TP_DT_FP8) return set_error(TP_ERR_ARG, "the handle is not TP_DT_FP8");
+    const Fp8Layout L = fp8_layout(&h->d);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.end)
+        return set_error(TP_ERR_ARG, "workspace must be the handle's (non-NULL, 256-byte aligned, %zu bytes)", L.end);
+    const char *src = static_cast<const char *>(workspace) + L.amax;
+    return cuda_check(cudaMemcpyAsync(out, src, sizeof(float) * TP_FP8_AMAX_COUNT, cudaMemcpyDefault,
+                                      static_cast<cudaStream_t>(stream)),
+                      "cudaMemcpyAsync(amax)");
+}
+
 tp_status tp_layer_set_fp8_history(tp_layer *h, int n) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
     if (n < 0 || n > kMaxFp8History) return set_error(TP_ERR_ARG, "history length %d outside 0..%d", n, kMaxFp8History);

@@ -122,6 +122,22 @@ def test_null_and_misaligned_pointers_rejected_before_launch(tp):
     L.tp_mlp_destroy(h)
 
 
+def test_fp8_amax_validation(tp):
+    """tp_mlp_fp8_amax rejects a NULL handle or out, a non-FP8 handle and a
+    workspace too small for the FP8 region, before any copy."""
+    L = tp.lib()
+    out = ctypes.c_void_p(0x10000)
+    assert L.tp_mlp_fp8_amax(None, ctypes.c_void_p(0x100000), 1 << 30, out, None) == 1
+    for dtype, expect_msg in (("bf16", b"TP_DT_FP8"), ("fp8", b"workspace")):
+        d = tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh", dtype=dtype)
+        h = ctypes.c_void_p()
+        assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+        assert L.tp_mlp_fp8_amax(h, ctypes.c_void_p(0x100000), 256, None, None) == 1
+        assert L.tp_mlp_fp8_amax(h, ctypes.c_void_p(0x100000), 256, out, None) == 1
+        assert expect_msg in L.tp_last_error()
+        L.tp_mlp_destroy(h)
+
+
 def test_linear_col_bwd_rejects_activation(tp):
     from tensor_transformer_mlp_shard_gb300.binding import _arr
     L = tp.lib()

@@ -193,3 +193,38 @@ def test_fp8_history_setter_validates(tp):
         assert e.value.status == 1
     lay.set_fp8_history(0)
     lay.set_fp8_history(64)
+
+
+@pytest.mark.parametrize("n", [0, 1])
+@pytest.mark.parametrize("act,F", [("gelu_tanh", 1024), ("gelu_tanh", 320), ("swiglu", 1024)])
+def test_fp8_amax_of_every_operand(tp, n, act, F):
+    """The amaxes a step records (tp_mlp_fp8_amax; "Megatron-LM 源码精读" s8.2,
+    the amax reduced over all shards of a tensor) equal max |x| of X, W1, W2,
+    dY and of the bf16 A the forward stored, exactly.  Under delayed scaling
+    (n = 1) the second step takes A's amax from the column GEMM's epilogue (a
+    max over the packed bf16 pairs it stores) and dPre's from the act' dgrad's;
+    under current scaling both come from separate passes.  F = 320 (F/T = 80)
+    leaves a part-filled 32-column block in every tile row.  dPre is formed
+    with different rounding on the two sides (see the module docstring), so
+    its amax is compared with the FP8 oracle's to 2^-5."""
+    M, H, T = 384, 256, 4
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act=act, dtype="fp8", has_bias=True, residual=True)
+    lay.set_fp8_history(n)
+    t = mlp_inputs(M, H, F, T, act, "fp8", has_bias=True)
+    run = MlpRun(lay, t)
+    hist = fp8.AmaxHistory(n) if n else None
+    for _ in range(2):
+        run.fwd()
+        run.bwd()
+        f = fp8.mlp_fwd_fp8(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, True, hist)
+        gr = fp8.mlp_bwd_fp8(t["dY"], f, act, True, hist)
+    assert tp.sync_status() == 0
+    got = host(lay.fp8_amax(run.ws)).astype(np.float64)
+
+    def amax(bufs):
+        return max(float(b.float().abs().max()) for b in bufs)
+
+    want = [amax(run.X), amax(run.W1), amax(run.W2), amax(run.A), amax(run.dY)]
+    assert list(got[:5]) == want, dict(zip(lay.FP8_AMAX_NAMES, zip(got, want)))
+    ref_dp = float(fp8.amax_of(gr["dPre"]))
+    assert abs(got[5] - ref_dp) <= 2 ** -5 * ref_dp, (got[5], ref_dp)
