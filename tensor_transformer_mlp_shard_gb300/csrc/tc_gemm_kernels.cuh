@@ -1405,6 +1405,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
                 const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
                 int s = wk.f0 / p.num_kb, kb = wk.f0 - s * p.num_kb;
+                // K-major operands select their map and row by the tile row,
+                // once per K segment (under sequence parallelism a division
+                // per K step here cost the SP GEMMs 6-9%); MN-major ones
+                // select by the K block, every step
+                int ia = 0, ra = 0, ib = 0, rb = 0;
+                if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
+                if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
                 {
                     for (int f = wk.f0; f < wk.f1; ++f) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
@@ -1421,11 +1428,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
                         const uint32_t sb = sa + P_A_BYTES;
                         const int k0 = kb * E::BKE;
-                        int idx, lrow;
                         if (!A_MN) {
-                            select(p.selA, pi, s, m0, idx, lrow);
-                            tma_load_2d_pair(sa, &p.mapA[idx], fb, k0, lrow);
+                            tma_load_2d_pair(sa, &p.mapA[ia], fb, k0, ra);
                         } else {
+                            int idx, lrow;
                             select(p.selA, pi, s, k0, idx, lrow);
                             if (!F8 && p.a3d) {
                                 tma_load_3d_pair(sa, &p.mapA[idx], fb, 0, lrow, m0 / 64);
@@ -1436,9 +1442,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             }
                         }
                         if (!B_MN) {
-                            select(p.selB, pi, s, n0, idx, lrow);
-                            tma_load_2d_pair(sb, &p.mapB[idx], fb, k0, lrow);
+                            tma_load_2d_pair(sb, &p.mapB[ib], fb, k0, rb);
                         } else {
+                            int idx, lrow;
                             select(p.selB, pi, s, k0, idx, lrow);
                             if (!F8 && p.b3d) {
                                 tma_load_3d_pair(sb, &p.mapB[idx], fb, 0, lrow, n0 / 64);
@@ -1455,6 +1461,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         if (++kb == p.num_kb) {
                             kb = 0;
                             ++s;
+                            if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
+                            if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
                         }
                     }
                 }
