@@ -27,16 +27,20 @@ namespace tpmlp {
 namespace tc {
 
 typedef void (*KernelFn)(Params);
-constexpr int kNumKernels = 5;
+constexpr int kNumKernels = 6;
 KernelFn fp8_kernel_at(int i, bool pair);  // tc_gemm_fp8.cu
 
-// The five (epilogue, A major, B major) combinations the MLP uses.
-static int kernel_index(int kind, bool amn, bool bmn) {
+// The five (epilogue, A major, B major) combinations the MLP uses, the
+// weight gradient twice: plain, and with token-sharded operands (sequence
+// parallelism), whose K loop crosses shards.
+static int kernel_index(const GemmPlan &g) {
+    const int kind = g.kind;
+    const bool amn = g.A.mn_major, bmn = g.B.mn_major;
     if (kind == EPI_COL && !amn && !bmn) return 0;
     if (kind == EPI_PLAIN && !amn && !bmn) return 1;
     if (kind == EPI_PLAIN && !amn && bmn) return 2;
     if (kind == EPI_DACT && !amn && bmn) return 3;
-    if (kind == EPI_F32 && amn && bmn) return 4;
+    if (kind == EPI_F32 && amn && bmn) return g.A.rows_split || g.B.rows_split ? 5 : 4;
     return -1;
 }
 
@@ -48,6 +52,7 @@ static KernelFn kernel_at(int i, bool pair, bool fp8) {
         case 2: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, true, false> : tc_gemm_kernel<EPI_PLAIN, false, true, false>;
         case 3: return pair ? tc_gemm_pair_kernel<EPI_DACT, false, true, false> : tc_gemm_kernel<EPI_DACT, false, true, false>;
         case 4: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true, false> : tc_gemm_kernel<EPI_F32, true, true, false>;
+        case 5: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true, false, true> : tc_gemm_kernel<EPI_F32, true, true, false>;
     }
     return nullptr;
 }
@@ -201,7 +206,7 @@ bool tc_writes_fp8(const GemmPlan &g) {
 
 tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     using namespace tc;
-    const int ki = kernel_index(g.kind, g.A.mn_major, g.B.mn_major);
+    const int ki = kernel_index(g);
     if (ki < 0)
         return set_error(TP_ERR_UNSUPPORTED, "no tcgen05 kernel for epilogue %d / majors %d%d", g.kind,
                          int(g.A.mn_major), int(g.B.mn_major));

@@ -16,6 +16,7 @@ KernelFn fp8_kernel_at(int i, bool pair) {
         case 2: return pair ? tc_gemm_pair_kernel<EPI_PLAIN, false, true, true> : tc_gemm_kernel<EPI_PLAIN, false, true, true>;
         case 3: return pair ? tc_gemm_pair_kernel<EPI_DACT, false, true, true> : tc_gemm_kernel<EPI_DACT, false, true, true>;
         case 4: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true, true> : tc_gemm_kernel<EPI_F32, true, true, true>;
+        case 5: return pair ? tc_gemm_pair_kernel<EPI_F32, true, true, true, true> : tc_gemm_kernel<EPI_F32, true, true, true>;
     }
     return nullptr;
 }

@@ -320,6 +320,32 @@ __device__ __forceinline__ void select(const Sel &s, int pi, int seg, int row, i
     }
 }
 
+// select() carried along a K loop for an MN-major operand split into token
+// shards: the map and local row of the current K block, advanced without a
+// division per step (shards are multiples of the K block, so a step never
+// straddles two of them).
+struct SelCursor {
+    int idx, lrow, j;
+    __device__ __forceinline__ void init(const Sel &s, int pi, int seg, int row) {
+        idx = pi * s.p_stride + seg * s.s_stride;
+        lrow = row;
+        j = 0;
+        if (s.rows_split) {
+            j = min(row / s.rows_split, s.nsplit - 1);
+            idx += j;
+            lrow = row - j * s.rows_split;
+        }
+    }
+    __device__ __forceinline__ void advance(const Sel &s, int step) {
+        lrow += step;
+        if (s.rows_split && lrow >= s.rows_split && j < s.nsplit - 1) {
+            lrow -= s.rows_split;
+            ++j;
+            ++idx;
+        }
+    }
+};
+
 template <typename T>
 __device__ __forceinline__ T *row_ptr(const Out &o, int pi, int row) {
     int idx = pi * o.p_stride;
@@ -1347,7 +1373,9 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool F8>
+// TS: the MN-major operands are split into token shards (the weight
+// gradients under sequence parallelism); their maps follow a SelCursor.
+template <int EPI, bool A_MN, bool B_MN, bool F8, bool TS = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ Params p) {
     constexpr int NST = pair_stages<EPI>();
     extern __shared__ uint8_t smem_raw[];
@@ -1412,6 +1440,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 int ia = 0, ra = 0, ib = 0, rb = 0;
                 if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
                 if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
+                SelCursor ca, cb;
+                if constexpr (TS) {
+                    if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
+                    if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
+                }
                 {
                     for (int f = wk.f0; f < wk.f1; ++f) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
@@ -1432,7 +1465,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             tma_load_2d_pair(sa, &p.mapA[ia], fb, k0, ra);
                         } else {
                             int idx, lrow;
-                            select(p.selA, pi, s, k0, idx, lrow);
+                            if constexpr (TS) {
+                                idx = ca.idx;
+                                lrow = ca.lrow;
+                            } else {
+                                select(p.selA, pi, s, k0, idx, lrow);
+                            }
                             if (!F8 && p.a3d) {
                                 tma_load_3d_pair(sa, &p.mapA[idx], fb, 0, lrow, m0 / 64);
                             } else {
@@ -1445,7 +1483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             tma_load_2d_pair(sb, &p.mapB[ib], fb, k0, rb);
                         } else {
                             int idx, lrow;
-                            select(p.selB, pi, s, k0, idx, lrow);
+                            if constexpr (TS) {
+                                idx = cb.idx;
+                                lrow = cb.lrow;
+                            } else {
+                                select(p.selB, pi, s, k0, idx, lrow);
+                            }
                             if (!F8 && p.b3d) {
                                 tma_load_3d_pair(sb, &p.mapB[idx], fb, 0, lrow, n0 / 64);
                             } else {
@@ -1463,6 +1506,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             ++s;
                             if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
                             if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
+                            if constexpr (TS) {
+                                if (A_MN) ca.init(p.selA, pi, s, 0);
+                                if (B_MN) cb.init(p.selB, pi, s, 0);
+                            }
+                        } else if constexpr (TS) {
+                            if (A_MN) ca.advance(p.selA, E::BKE);
+                            if (B_MN) cb.advance(p.selB, E::BKE);
                         }
                     }
                 }
