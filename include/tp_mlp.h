@@ -316,6 +316,14 @@ TP_API size_t tp_layer_workspace_bytes(const tp_layer *h);
  * tp_layer_fwd / tp_layer_bwd call must then get, untouched in between). */
 TP_API tp_status tp_layer_set_fp8_history(tp_layer *h, int n);
 
+/* The per-tensor amaxes a TP_DT_FP8 sub-block's last calls recorded in
+ * `workspace`, as tp_mlp_fp8_amax returns them for the MLP inside: X is the
+ * LayerNorm output that enters the MLP and dY the gradient at the MLP's
+ * output (after the dropout backward).  Same arguments and errors as
+ * tp_mlp_fp8_amax. */
+TP_API tp_status tp_layer_fp8_amax(const tp_layer *h, const void *workspace, size_t workspace_bytes, float *out,
+                                   void *stream);
+
 /* Forward.  X, Y: like tp_mlp_fwd's X and Y; gamma, beta: [H] (bf16, fp32 for
  * TP_DT_F32); W1, b1, W2, b2, pre, A: as in tp_mlp_fwd; seed: dropout key.
  * Outputs kept for the backward: Xn [M, H] (activation dtype), mean and rstd

@@ -61,6 +61,7 @@ SIGNATURES = {
     "tp_mlp_fwd_ws": (ctypes.c_int, [VP, PP, PP, PP, PP, VP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_mlp_set_fp8_history": (ctypes.c_int, [VP, ctypes.c_int]),
     "tp_mlp_fp8_amax": (ctypes.c_int, [VP, VP, ctypes.c_size_t, VP, VP]),
+    "tp_layer_fp8_amax": (ctypes.c_int, [VP, VP, ctypes.c_size_t, VP, VP]),
     "tp_mlp_bwd": (ctypes.c_int, [VP, PP, PP, PP, PP, PP, PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_col": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP]),
     "tp_linear_row": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP]),
@@ -295,6 +296,16 @@ class TPLayer(Layout):
 
     def workspace_bytes(self) -> int:
         return int(lib().tp_layer_workspace_bytes(self._h))
+
+    FP8_AMAX_NAMES = ("X", "W1", "W2", "A", "dY", "dPre")
+
+    def fp8_amax(self, workspace, stream=None):
+        """The per-tensor amaxes of the MLP inside the block, as TPMLP.fp8_amax
+        (X: the LayerNorm output, dY: the gradient at the MLP's output)."""
+        ws_ptr, ws_bytes = _workspace(workspace)
+        out = torch.empty(len(self.FP8_AMAX_NAMES), dtype=torch.float32, device=workspace.device)
+        _check(lib().tp_layer_fp8_amax(self._h, ws_ptr, ws_bytes, out.data_ptr(), _stream(stream)))
+        return out
 
     def set_fp8_history(self, n: int):
         """FP8 delayed scaling over the last n amaxes (0: current scaling); as

@@ -1558,16 +1558,30 @@ tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n) {
     return TP_OK;
 }
 
-tp_status tp_mlp_fp8_amax(const tp_mlp *h, const void *workspace, size_t workspace_bytes, float *out, void *stream) {
-    if (!h || !out) return set_error(TP_ERR_ARG, "handle or out is NULL");
-    if (h->d.dtype != TP_DT_FP8) return set_error(TP_ERR_ARG, "the handle is not TP_DT_FP8");
-    const Fp8Layout L = fp8_layout(&h->d);
+// the amax slots of an FP8 MLP workspace (the MLP's part of a sub-block's
+// workspace starts at offset 0)
+static tp_status fp8_amax_copy(const tp_mlp_desc *d, const void *workspace, size_t workspace_bytes, float *out,
+                               void *stream) {
+    if (!out) return set_error(TP_ERR_ARG, "out is NULL");
+    if (d->dtype != TP_DT_FP8) return set_error(TP_ERR_ARG, "the handle is not TP_DT_FP8");
+    const Fp8Layout L = fp8_layout(d);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.end)
         return set_error(TP_ERR_ARG, "workspace must be the handle's (non-NULL, 256-byte aligned, %zu bytes)", L.end);
     const char *src = static_cast<const char *>(workspace) + L.amax;
     return cuda_check(cudaMemcpyAsync(out, src, sizeof(float) * TP_FP8_AMAX_COUNT, cudaMemcpyDefault,
                                       static_cast<cudaStream_t>(stream)),
                       "cudaMemcpyAsync(amax)");
+}
+
+tp_status tp_mlp_fp8_amax(const tp_mlp *h, const void *workspace, size_t workspace_bytes, float *out, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    return fp8_amax_copy(&h->d, workspace, workspace_bytes, out, stream);
+}
+
+tp_status tp_layer_fp8_amax(const tp_layer *h, const void *workspace, size_t workspace_bytes, float *out,
+                            void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    return fp8_amax_copy(&h->inner, workspace, workspace_bytes, out, stream);
 }
 
 tp_status tp_layer_set_fp8_history(tp_layer *h, int n) {

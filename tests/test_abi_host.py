@@ -128,6 +128,7 @@ def test_fp8_amax_validation(tp):
     L = tp.lib()
     out = ctypes.c_void_p(0x10000)
     assert L.tp_mlp_fp8_amax(None, ctypes.c_void_p(0x100000), 1 << 30, out, None) == 1
+    assert L.tp_layer_fp8_amax(None, ctypes.c_void_p(0x100000), 1 << 30, out, None) == 1
     for dtype, expect_msg in (("bf16", b"TP_DT_FP8"), ("fp8", b"workspace")):
         d = tp.make_desc(128, 2, 256, 1024, 2, act="gelu_tanh", dtype=dtype)
         h = ctypes.c_void_p()

@@ -251,6 +251,30 @@ def test_layer_fp8_matches_fp8_oracle(tp, tile_mode):
     assert not bad, bad
 
 
+def test_layer_fp8_amax(tp):
+    """tp_layer_fp8_amax: the amaxes of the MLP inside the block equal max |x|
+    of the LayerNorm output Xn, W1, W2, the stored bf16 A and (dropout off, so
+    the gradient at the MLP's output is the block's dY) dY, exactly; dPre's is
+    positive and finite (its exact value is pinned for the MLP entry points)."""
+    M, H, F, T, act = 512, 256, 1024, 4, "gelu_tanh"
+    lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act=act, dtype="fp8", has_bias=True, dropout_p=0.0)
+    lay.set_fp8_history(1)
+    t = layer_inputs(M, H, F, T, act, "fp8", True, seed_off=11)
+    run = LayerRun(lay, t)
+    for _ in range(2):
+        run.fwd(SEED)
+        run.bwd(SEED)
+    assert tp.sync_status() == 0
+    got = host(lay.fp8_amax(run.ws)).astype(np.float64)
+
+    def amax(bufs):
+        return max(float(b.float().abs().max()) for b in bufs)
+
+    want = [amax([run.Xn]), amax(run.W1), amax(run.W2), amax(run.A), amax(run.dY)]
+    assert list(got[:5]) == want, dict(zip(lay.FP8_AMAX_NAMES, zip(got, want)))
+    assert 0.0 < got[5] < float("inf")
+
+
 def test_layer_empty_tokens_zero_the_gradients(tp):
     lay = tp.TPLayer(S=0, B=2, H=256, F=1024, T=4, act="gelu_tanh", dtype="bf16", has_bias=True, dropout_p=0.1)
     t = layer_inputs(0, 256, 1024, 4, "gelu_tanh", "bf16", True)
