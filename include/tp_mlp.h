@@ -170,7 +170,9 @@ TP_API tp_status tp_mlp_fwd_ws(tp_mlp *h, const void *const *X, const void *cons
  * again clears the history.  Host only.  TP_ERR_ARG for n outside 0..64. */
 TP_API tp_status tp_mlp_set_fp8_history(tp_mlp *h, int n);
 
-/* The per-tensor amaxes (max |x| over all shards, fp32) the last calls of a
+/* The per-tensor amaxes (max |x| over all shards, fp32: the cross-shard amax
+ * reduction of "Megatron-LM 源码精读" s8.2, the values the amax history of s2,
+ * the fp8_utils.py entry, records) the last calls of a
  * TP_DT_FP8 handle recorded in `workspace` (the one passed to them), in the
  * order X, W1, W2, A (set by tp_mlp_fwd_ws), dY, dPre (set by tp_mlp_bwd):
  * the values that enter the scales of the next call (delayed scaling) or
