@@ -43,7 +43,10 @@
  *   Errors.  Argument and shape errors return before anything is enqueued.
  *     Launch failures return TP_ERR_CUDA.  A kernel whose internal wait
  *     exceeds the wait limit records TP_ERR_TIMEOUT in a device status word
- *     and returns early; tp_sync_status() reports (and clears) it.
+ *     and returns early.  Every MLP and sub-block handle owns a status word
+ *     of its own, which tp_mlp_sync_status() / tp_layer_sync_status() report
+ *     (and clear); the calls without a handle (single layers, FP8 quantiser)
+ *     share one word, which tp_sync_status() reports (and clears).
  *     tp_last_error() gives a message for the last failing call of the
  *     calling thread.
  */
@@ -110,11 +113,15 @@ typedef struct tp_mlp tp_mlp; /* opaque handle: validated descriptor */
 
 /* ---- handle ------------------------------------------------------------ */
 
-/* Validate `desc` and create a handle.  Host only: no CUDA call.
+/* Validate `desc` and create a handle.  Host only: no CUDA call.  The handle
+ * takes one of 1023 device status words (the walk-through s02's layer object
+ * is one unit of state; here its state includes where its kernels report a
+ * timeout), released by tp_mlp_destroy.
  * Returns TP_ERR_SHAPE for F % T != 0, T outside 1..TP_MAX_SHARDS, widths not
  * multiples of 8, S % T != 0 under sequence parallelism (bf16 additionally
  * needs M/T % 128 == 0 under sequence parallelism); TP_ERR_ARG for bad
- * enums, flags other than 0/1 or a null pointer. */
+ * enums, flags other than 0/1 or a null pointer; TP_ERR_UNSUPPORTED when
+ * 1023 MLP and sub-block handles are already live. */
 TP_API tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out);
 TP_API void tp_mlp_destroy(tp_mlp *h);
 
@@ -255,19 +262,26 @@ TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *d
  *   only the op's tensors and has no allocator of its own, a process whose
  *   device memory is fully reserved by another (caching) allocator, or a
  *   latency-critical loop that cannot take cudaMalloc's implicit device
- *   synchronisation.  It computes the gradients tp_linear_row_bwd computes
- *   (the weight gradient always without token splitting, so where
- *   tp_linear_row_bwd splits K the two differ by fp32 summation order) and
- *   allocates nothing: the bias-gradient partial sums go to a 4 MiB array
+ *   synchronisation.  It allocates nothing: its scratch is a 4 MiB array
  *   compiled into the library (held on every GPU that loads the library until
  *   the process exits).  Arguments are those of tp_linear_row_bwd minus the
- *   workspace.  A problem whose partials exceed 4 MiB (4 * ceil(M/256) * H
- *   bytes, rounded up to 256, when has_bias) returns TP_ERR_UNSUPPORTED.
- *   The first call on a device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture.
- *   All calls share the one array and each call overwrites the part it reads
- *   (nothing needs to start at zero), so calls that overlap on the GPU -- on
- *   different streams, or from several host threads -- race. */
+ *   workspace.  Two regimes:
+ *   - tp_linear_workspace_bytes(desc) <= 4 MiB: the array serves as that
+ *     workspace, and the call runs exactly the plan of tp_linear_row_bwd
+ *     (split-K and tail split of the weight gradient included), with the
+ *     same results bit for bit;
+ *   - otherwise the weight gradient runs without token splitting and without
+ *     the tail split, and the array holds only the bias-gradient partials
+ *     (results differ from tp_linear_row_bwd by fp32 summation order where
+ *     that call splits).
+ *   A problem whose bias partials exceed 4 MiB (4 * ceil(M/256) * H bytes,
+ *   rounded up to 256, when has_bias) returns TP_ERR_UNSUPPORTED.
+ *   The device address of the array is looked up on the first call per
+ *   device and CUDA context (with that device current); make that first call
+ *   before any stream capture.  All calls share the one array and each call
+ *   overwrites the part it reads (nothing needs to start at zero), so calls
+ *   that overlap on the GPU -- on different streams, or from several host
+ *   threads -- race. */
 TP_API tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *const *dY,
                                            const void *const *X, const void *const *W,
                                            void *const *dX, void *const *dW, void *db,
@@ -298,7 +312,8 @@ typedef struct {
 
 typedef struct tp_layer tp_layer;
 
-/* Validate and create (host only).  Besides tp_mlp_create's checks: TP_ERR_ARG
+/* Validate and create (host only; takes a status word like tp_mlp_create).
+ * Besides tp_mlp_create's checks: TP_ERR_ARG
  * for mlp.residual != 0, p outside [0, 1) or ln_eps <= 0; TP_ERR_UNSUPPORTED
  * for H above 8192 (bf16, FP8) or 4096 (fp32), the LayerNorm kernels' row
  * capacity. */
@@ -374,9 +389,20 @@ TP_API tp_status tp_fp8_quantize(const void *const *in, void *const *out, const 
 
 /* ---- status, limits, diagnostics ---------------------------------------- */
 
-/* Synchronise `stream`, then read and clear the device status word.  Returns
- * TP_OK, TP_ERR_TIMEOUT (a bounded wait ran out) or TP_ERR_CUDA. */
+/* Synchronise `stream`, then read and clear the status word shared by the
+ * calls without a handle (tp_linear_*, tp_fp8_quantize,
+ * tp_debug_wait_timeout).  Returns TP_OK, TP_ERR_TIMEOUT (a bounded wait ran
+ * out) or TP_ERR_CUDA. */
 TP_API tp_status tp_sync_status(void *stream);
+
+/* Synchronise `stream`, then read and clear the status word of handle h:
+ * TP_ERR_TIMEOUT iff a kernel launched by one of h's calls (tp_mlp_fwd,
+ * tp_mlp_fwd_ws, tp_mlp_bwd; tp_layer_fwd, tp_layer_bwd) ran out of its wait
+ * limit since the last read.  Launches of other handles, on this or other
+ * streams, neither set nor clear it.  TP_ERR_ARG for a NULL handle,
+ * TP_ERR_CUDA when the synchronisation or the read fails. */
+TP_API tp_status tp_mlp_sync_status(tp_mlp *h, void *stream);
+TP_API tp_status tp_layer_sync_status(tp_layer *h, void *stream);
 
 /* Wall-clock bound of every in-kernel wait, in nanoseconds (default 4e9).
  * Applies to launches made after the call. */
@@ -386,6 +412,10 @@ TP_API void tp_set_wait_limit_ns(uint64_t ns);
  * limit_ns; it records TP_ERR_TIMEOUT in the status word and returns.  Used
  * to test the failure path without faulting or hanging the GPU. */
 TP_API tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* As tp_debug_wait_timeout, reporting to the status word of handle h (read
+ * with tp_mlp_sync_status): tests that a timeout reaches only its handle. */
+TP_API tp_status tp_mlp_debug_wait_timeout(tp_mlp *h, uint64_t limit_ns, void *stream);
 
 /* GEMM tiling of the bf16 engine, for all launches made after the call:
  * TP_TILE_AUTO (default) uses 256-row tiles computed by a pair of CTAs on two
@@ -460,6 +490,14 @@ typedef struct {
 } tp_prof_entry;
 TP_API void tp_prof_enable(int on);
 TP_API int tp_prof_collect(tp_prof_entry *entries, int max_entries);
+
+/* SM clock of the GEMM kernels launched while the per-kernel timer was on:
+ * one thread of every CTA reads the SM cycle counter (clock64) and the
+ * wall-clock timer (%globaltimer, ns) when the CTA starts and ends, and the
+ * differences are summed over all CTAs.  cycles / ns * 1000 is the average
+ * SM clock in MHz under that load.  Synchronises the device, then returns
+ * the two sums and clears them.  TP_ERR_ARG for NULL outputs. */
+TP_API tp_status tp_prof_clock(uint64_t *cycles, uint64_t *ns);
 
 TP_API const char *tp_status_str(tp_status s);
 TP_API const char *tp_last_error(void);

@@ -79,6 +79,10 @@ SIGNATURES = {
                                     PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_fp8_quantize": (ctypes.c_int, [PP, PP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int, VP, VP]),
     "tp_sync_status": (ctypes.c_int, [VP]),
+    "tp_mlp_sync_status": (ctypes.c_int, [VP, VP]),
+    "tp_layer_sync_status": (ctypes.c_int, [VP, VP]),
+    "tp_mlp_debug_wait_timeout": (ctypes.c_int, [VP, ctypes.c_uint64, VP]),
+    "tp_prof_clock": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
     "tp_launch_count": (ctypes.c_uint64, []),
@@ -217,6 +221,16 @@ class TPMLP(Layout):
     def workspace_bytes(self) -> int:
         return int(lib().tp_mlp_workspace_bytes(self._h))
 
+    def sync_status(self, stream=None) -> int:
+        """Synchronise the stream and return (and clear) this handle's device
+        status word (TP_ERR_TIMEOUT when one of its kernels' waits ran out)."""
+        return int(lib().tp_mlp_sync_status(self._h, _stream(stream)))
+
+    def debug_wait_timeout(self, limit_ns: int, stream=None):
+        """A kernel that waits on a flag nothing sets, reporting its timeout to
+        this handle's status word."""
+        _check(lib().tp_mlp_debug_wait_timeout(self._h, int(limit_ns), _stream(stream)))
+
     def set_fp8_history(self, n: int):
         """FP8 delayed scaling over the last n amaxes of every operand (0:
         current scaling).  Clears the history; pass the same workspace to
@@ -296,6 +310,11 @@ class TPLayer(Layout):
 
     def workspace_bytes(self) -> int:
         return int(lib().tp_layer_workspace_bytes(self._h))
+
+    def sync_status(self, stream=None) -> int:
+        """Synchronise the stream and return (and clear) this handle's device
+        status word."""
+        return int(lib().tp_layer_sync_status(self._h, _stream(stream)))
 
     FP8_AMAX_NAMES = ("X", "W1", "W2", "A", "dY", "dPre")
 
@@ -481,7 +500,9 @@ def fp8_quantize(inputs, outputs, fmt: str, amax, stream=None):
 # status / diagnostics
 # ---------------------------------------------------------------------------
 def sync_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device status word."""
+    """Synchronise the stream and return (and clear) the status word of the
+    calls without a handle (single layers, FP8 quantiser); MLP and sub-block
+    handles report through their own sync_status()."""
     return int(lib().tp_sync_status(_stream(stream)))
 
 
@@ -543,6 +564,15 @@ def prof_collect():
     if n < 0:
         raise TpError(4, lib().tp_last_error().decode(errors="replace"))
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n)}
+
+
+def prof_clock():
+    """(SM cycles, ns) summed over the CTAs of the GEMM launches made while the
+    per-kernel timer was on, then cleared: cycles / ns * 1e3 is their SM clock
+    in MHz."""
+    c, t = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().tp_prof_clock(ctypes.byref(c), ctypes.byref(t)))
+    return int(c.value), int(t.value)
 
 
 def status_str(s: int) -> str:

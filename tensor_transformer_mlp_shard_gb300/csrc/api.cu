@@ -29,12 +29,14 @@
 
 struct tp_mlp {
     tp_mlp_desc d;
+    int status_slot = 0;  // this handle's device status word (see StatusScope)
     int fp8_history = 0;  // 0: current scaling; n: delayed scaling over the last n amaxes
     long long fp8_fwd_steps = 0, fp8_bwd_steps = 0;  // quantisations since the history was set
 };
 
 struct tp_layer {
     tp_layer_desc d;
+    int status_slot = 0;  // as tp_mlp
     tp_mlp_desc inner;  // the MLP inside the sub-block: d.mlp with the residual handled by the block
     uint32_t drop_threshold;
     float drop_scale;
@@ -46,9 +48,6 @@ struct tp_layer {
 };
 
 namespace tpmlp {
-
-tp_status read_and_clear_status(cudaStream_t st, int *out);
-tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // errors
@@ -106,6 +105,11 @@ static bool g_prof_on = false;
 static std::vector<ProfRec> g_prof_recs;
 static std::vector<cudaEvent_t> g_event_pool;
 static thread_local cudaEvent_t g_pending = nullptr;
+
+bool prof_enabled() {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    return g_prof_on;
+}
 
 static cudaEvent_t get_event() {
     if (!g_event_pool.empty()) {
@@ -925,11 +929,21 @@ tp_status tp_mlp_create(const tp_mlp_desc *desc, tp_mlp **out) {
     tp_mlp *h = new (std::nothrow) tp_mlp;
     if (!h) return set_error(TP_ERR_ARG, "out of host memory");
     h->d = *desc;
+    h->status_slot = alloc_status_slot();
+    if (h->status_slot < 0) {
+        delete h;
+        return set_error(TP_ERR_UNSUPPORTED, "more than %d live handles (each owns a device status word)",
+                         kStatusSlots - 1);
+    }
     *out = h;
     return TP_OK;
 }
 
-void tp_mlp_destroy(tp_mlp *h) { delete h; }
+void tp_mlp_destroy(tp_mlp *h) {
+    if (!h) return;
+    free_status_slot(h->status_slot);
+    delete h;
+}
 
 size_t tp_mlp_workspace_bytes(const tp_mlp *h) {
     return h ? mlp_ws_layout(&h->d, nullptr) + tail_scratch_bytes(&h->d) : 0;
@@ -1047,6 +1061,7 @@ static tp_status mlp_fwd_impl(tp_mlp *h, const void *const *X, const void *const
                               const void *const *W2, const void *b2, void *const *Y, void *const *pre,
                               void *const *A, void *workspace, size_t workspace_bytes, bool has_ws, void *stream) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const StatusScope scope(h->status_slot);
     const tp_mlp_desc *d = &h->d;
     const Dims x = dims_of(d);
     TRY(check_array(W1, x.T, "W1"));
@@ -1097,6 +1112,7 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
                      void *const *dW1, void *const *db1, void *const *dW2, void *db2, void *workspace,
                      size_t workspace_bytes, void *stream) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const StatusScope scope(h->status_slot);
     const tp_mlp_desc *d = &h->d;
     const Dims x = dims_of(d);
     TRY(check_array(W1, x.T, "W1"));
@@ -1240,8 +1256,9 @@ tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY, cons
 
 namespace tpmlp {
 
-size_t linear_bias_workspace_bytes(const tp_mlp_desc *desc) {
-    return validate_desc(desc) == TP_OK ? linear_part_bytes(desc) : 0;
+size_t linear_row_bias_bytes(const tp_mlp_desc *desc) {
+    if (validate_desc(desc) != TP_OK || !desc->has_bias) return 0;
+    return partials_bytes(desc, 1, desc->H);
 }
 
 // tp_linear_row_bwd; without allow_split the weight gradient is never split
@@ -1263,7 +1280,7 @@ tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, co
     if (allow_split) {
         TRY(check_ws(desc, workspace, workspace_bytes));
     } else {
-        const size_t need = linear_part_bytes(desc);
+        const size_t need = linear_row_bias_bytes(desc);
         if (workspace_bytes < need)
             return set_error(TP_ERR_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
         if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -1309,6 +1326,12 @@ tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out) {
     if (!h) return set_error(TP_ERR_ARG, "out of host memory");
     h->d = *desc;
     h->inner = desc->mlp;
+    h->status_slot = alloc_status_slot();
+    if (h->status_slot < 0) {
+        delete h;
+        return set_error(TP_ERR_UNSUPPORTED, "more than %d live handles (each owns a device status word)",
+                         kStatusSlots - 1);
+    }
     // keep iff the draw's top 24 bits >= floor(p * 2^24); kept values scaled by 1/(1-p)
     h->drop_threshold = static_cast<uint32_t>(p * 16777216.0);
     h->drop_scale = static_cast<float>(1.0 / (1.0 - p));
@@ -1316,7 +1339,11 @@ tp_status tp_layer_create(const tp_layer_desc *desc, tp_layer **out) {
     return TP_OK;
 }
 
-void tp_layer_destroy(tp_layer *h) { delete h; }
+void tp_layer_destroy(tp_layer *h) {
+    if (!h) return;
+    free_status_slot(h->status_slot);
+    delete h;
+}
 
 // Workspace: [MLP workspace | dZ, later the LayerNorm partials | dXn, before
 // that the db2 partials of the dropout backward | the dropout keep-mask the
@@ -1383,6 +1410,7 @@ tp_status tp_layer_fwd(tp_layer *h, const void *const *X, const void *gamma, con
                        uint64_t seed, void *const *Y, void *Xn, float *mean, float *rstd, void *const *pre,
                        void *const *A, void *workspace, size_t workspace_bytes, void *stream) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const StatusScope scope(h->status_slot);
     const tp_mlp_desc *d = &h->inner;
     const Dims x = dims_of(d);
     TRY(check_one(gamma, "gamma"));
@@ -1440,6 +1468,7 @@ tp_status tp_layer_bwd(tp_layer *h, const void *const *dY, const void *const *X,
                        float *dbeta, void *const *dW1, void *const *db1, void *const *dW2, void *db2,
                        void *workspace, size_t workspace_bytes, void *stream) {
     if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const StatusScope scope(h->status_slot);
     const tp_mlp_desc *d = &h->inner;
     const Dims x = dims_of(d);
     TRY(check_one(gamma, "gamma"));
@@ -1533,16 +1562,44 @@ tp_status tp_fp8_quantize(const void *const *in, void *const *out, const int64_t
     return launch_fp8_quantize(segs, nbuf, amax, true, static_cast<cudaStream_t>(stream));
 }
 
-tp_status tp_sync_status(void *stream) {
+static tp_status sync_slot(int slot, void *stream) {
     int v = 0;
-    TRY(read_and_clear_status(static_cast<cudaStream_t>(stream), &v));
+    TRY(read_and_clear_status(static_cast<cudaStream_t>(stream), slot, &v));
     if (v == TP_OK) return TP_OK;
     return set_error(static_cast<tp_status>(v), "device reported %s", tp_status_str(static_cast<tp_status>(v)));
+}
+
+tp_status tp_sync_status(void *stream) { return sync_slot(0, stream); }
+
+tp_status tp_mlp_sync_status(tp_mlp *h, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    return sync_slot(h->status_slot, stream);
+}
+
+tp_status tp_layer_sync_status(tp_layer *h, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    return sync_slot(h->status_slot, stream);
+}
+
+tp_status tp_mlp_debug_wait_timeout(tp_mlp *h, uint64_t limit_ns, void *stream) {
+    if (!h) return set_error(TP_ERR_ARG, "handle is NULL");
+    const StatusScope scope(h->status_slot);
+    return launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_prof_clock(uint64_t *cycles, uint64_t *ns) {
+    if (!cycles || !ns) return set_error(TP_ERR_ARG, "cycles or ns is NULL");
+    unsigned long long c = 0, t = 0;
+    TRY(read_and_clear_clock(&c, &t));
+    *cycles = c;
+    *ns = t;
+    return TP_OK;
 }
 
 void tp_set_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns ? ns : 1); }
 
 tp_status tp_debug_wait_timeout(uint64_t limit_ns, void *stream) {
+    const StatusScope scope(0);
     return launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
 }
 

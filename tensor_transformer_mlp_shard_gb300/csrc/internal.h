@@ -227,18 +227,42 @@ tp_status launch_dropout_bwd(const LnPlan &p, int dtype, cudaStream_t st);
 
 // tp_linear_row_bwd with split-K optional (the allocation-free entry point
 // runs it on a fixed scratch array that may not hold split partials), and the
-// workspace it needs without splitting (the bias partials).
+// workspace it needs without splitting: the row layer's bias partials,
+// 4 * ceil(M/256) * H bytes rounded up to 256 (0 without a bias or for an
+// invalid descriptor).
 tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
                               const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
                               size_t workspace_bytes, void *stream, bool allow_split);
-size_t linear_bias_workspace_bytes(const tp_mlp_desc *desc);
+size_t linear_row_bias_bytes(const tp_mlp_desc *desc);
 
-// Device status words (per device), the wait limit and the launch counter.
+// Device status words, the wait limit and the launch counter.  Status and
+// abort words come in slots: slot 0 for the calls without a handle, one slot
+// per live MLP / sub-block handle.  The entry points of a handle run under a
+// StatusScope naming its slot, and every launch made on that thread in the
+// meantime reports to that slot.
+constexpr int kStatusSlots = 1024;
 struct DeviceWords {
     int *status = nullptr;
     unsigned *abort_word = nullptr;
+    unsigned long long *clk = nullptr;  // kernel clock counters (per-kernel timer on), or null
 };
-tp_status device_words(DeviceWords *w);
+tp_status device_words(DeviceWords *w);  // words of the calling thread's current slot
+int alloc_status_slot();                  // 1..kStatusSlots-1, or -1 when all are taken
+void free_status_slot(int slot);
+class StatusScope {
+   public:
+    explicit StatusScope(int slot);
+    ~StatusScope();
+    StatusScope(const StatusScope &) = delete;
+    StatusScope &operator=(const StatusScope &) = delete;
+
+   private:
+    int prev_;
+};
+tp_status read_and_clear_status(cudaStream_t st, int slot, int *out);
+tp_status read_and_clear_clock(unsigned long long *cycles, unsigned long long *ns);
+tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st);
+bool prof_enabled();
 uint64_t wait_limit_ns();
 unsigned next_launch_id();
 int num_sms();

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -18,54 +19,107 @@ namespace tpmlp {
 // ---------------------------------------------------------------------------
 // status words
 // ---------------------------------------------------------------------------
-__device__ int g_tp_status = 0;  // first device-side error of any launch
-__device__ unsigned g_tp_abort = 0;
+// One status word and one abort word per slot.  Slot 0 belongs to the calls
+// without a handle (the single-layer entry points, the FP8 quantiser and the
+// wait self-test); every MLP or sub-block handle owns a slot of its own for
+// its lifetime, so that a timeout is reported to, and cleared by, the handle
+// whose launch raised it.
+__device__ int g_tp_status[kStatusSlots];  // first device-side error per slot
+__device__ unsigned g_tp_abort[kStatusSlots];
 __device__ unsigned g_tp_never_set = 0;
+// SM cycles and wall-clock nanoseconds summed over the CTAs of the GEMM
+// launches made while the per-kernel timer is on (clock64 and %globaltimer
+// read by one thread at the start and end of each CTA): their ratio is the
+// SM clock those kernels actually ran at.
+__device__ unsigned long long g_tp_clk[2];
+
+static std::mutex g_slot_mu;
+static bool g_slot_used[kStatusSlots] = {true};  // slot 0 is never handed out
+static thread_local int g_cur_slot = 0;
+
+int alloc_status_slot() {
+    std::lock_guard<std::mutex> lock(g_slot_mu);
+    for (int i = 1; i < kStatusSlots; ++i)
+        if (!g_slot_used[i]) {
+            g_slot_used[i] = true;
+            return i;
+        }
+    return -1;
+}
+
+void free_status_slot(int slot) {
+    if (slot <= 0 || slot >= kStatusSlots) return;
+    std::lock_guard<std::mutex> lock(g_slot_mu);
+    g_slot_used[slot] = false;
+}
+
+StatusScope::StatusScope(int slot) : prev_(g_cur_slot) { g_cur_slot = slot; }
+StatusScope::~StatusScope() { g_cur_slot = prev_; }
 
 tp_status device_words(DeviceWords *w) {
-    static DeviceWords cached[64];
-    static bool have[64] = {};
+    static int *st_base[64] = {};
+    static unsigned *ab_base[64] = {};
+    static unsigned long long *clk_base[64] = {};
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
-    if (dev < 64 && have[dev]) {
-        *w = cached[dev];
-        return TP_OK;
+    if (dev < 0 || dev >= 64) return set_error(TP_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!st_base[dev]) {
+        void *ps = nullptr, *pa = nullptr, *pc = nullptr;
+        e = cudaGetSymbolAddress(&ps, g_tp_status);
+        if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(status)");
+        e = cudaGetSymbolAddress(&pa, g_tp_abort);
+        if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(abort)");
+        e = cudaGetSymbolAddress(&pc, g_tp_clk);
+        if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(clock)");
+        st_base[dev] = static_cast<int *>(ps);
+        ab_base[dev] = static_cast<unsigned *>(pa);
+        clk_base[dev] = static_cast<unsigned long long *>(pc);
     }
-    void *ps = nullptr, *pa = nullptr;
-    e = cudaGetSymbolAddress(&ps, g_tp_status);
-    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(status)");
-    e = cudaGetSymbolAddress(&pa, g_tp_abort);
-    if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(abort)");
-    w->status = static_cast<int *>(ps);
-    w->abort_word = static_cast<unsigned *>(pa);
-    if (dev < 64) {
-        cached[dev] = *w;
-        have[dev] = true;
-    }
+    w->status = st_base[dev] + g_cur_slot;
+    w->abort_word = ab_base[dev] + g_cur_slot;
+    w->clk = prof_enabled() ? clk_base[dev] : nullptr;
     return TP_OK;
 }
 
-tp_status read_and_clear_status(cudaStream_t st, int *out) {
+tp_status read_and_clear_status(cudaStream_t st, int slot, int *out) {
+    if (slot < 0 || slot >= kStatusSlots) return set_error(TP_ERR_ARG, "bad status slot %d", slot);
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_check(e, "cudaStreamSynchronize");
+    const size_t off = sizeof(int) * static_cast<size_t>(slot);
     int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_tp_status, sizeof(int));
+    e = cudaMemcpyFromSymbol(&v, g_tp_status, sizeof(int), off);
     if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyFromSymbol(status)");
     const int zero = 0;
-    e = cudaMemcpyToSymbol(g_tp_status, &zero, sizeof(int));
+    e = cudaMemcpyToSymbol(g_tp_status, &zero, sizeof(int), off);
     if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyToSymbol(status)");
     *out = v;
     return TP_OK;
 }
 
+tp_status read_and_clear_clock(unsigned long long *cycles, unsigned long long *ns) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_check(e, "cudaDeviceSynchronize");
+    unsigned long long v[2] = {0, 0};
+    e = cudaMemcpyFromSymbol(v, g_tp_clk, sizeof(v));
+    if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyFromSymbol(clock)");
+    const unsigned long long zero[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_tp_clk, zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyToSymbol(clock)");
+    *cycles = v[0];
+    *ns = v[1];
+    return TP_OK;
+}
+
 // Waits for a flag that nothing sets; the wall-clock bound ends the wait and
 // the kernel records TP_ERR_TIMEOUT, like any of the GEMM kernels' waits.
-__global__ void wait_timeout_kernel(unsigned long long limit_ns) {
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, int *status) {
     const uint64_t t0 = global_timer_ns();
     while (*reinterpret_cast<volatile unsigned *>(&g_tp_never_set) == 0) {
         if (global_timer_ns() - t0 > limit_ns) {
-            atomicCAS(&g_tp_status, 0, TP_ERR_TIMEOUT);
+            atomicCAS(status, 0, TP_ERR_TIMEOUT);
             return;
         }
         __nanosleep(1000);
@@ -73,8 +127,11 @@ __global__ void wait_timeout_kernel(unsigned long long limit_ns) {
 }
 
 tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st) {
+    DeviceWords w;
+    tp_status s = device_words(&w);
+    if (s != TP_OK) return s;
     launch_begin("wait_timeout", st);
-    wait_timeout_kernel<<<1, 1, 0, st>>>(limit_ns);
+    wait_timeout_kernel<<<1, 1, 0, st>>>(limit_ns, w.status);
     cudaError_t e = cudaGetLastError();
     launch_end("wait_timeout", st);
     return cuda_check(e, "wait_timeout_kernel");

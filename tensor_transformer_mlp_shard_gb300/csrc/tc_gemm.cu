@@ -340,6 +340,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     if (s != TP_OK) return s;
     prm.status = w.status;
     prm.abort_word = w.abort_word;
+    prm.clk = w.clk;
     prm.launch_id = next_launch_id();
     prm.wait_limit_ns = wait_limit_ns();
     if (prm.total_tiles == 0 || prm.num_kb == 0) return TP_OK;

@@ -114,6 +114,27 @@ struct Params {
     unsigned *abort_word;
     unsigned launch_id;
     unsigned long long wait_limit_ns;
+    // when non-null: thread 0 of every CTA adds the SM cycles (clock64) and
+    // nanoseconds (%globaltimer) between the CTA's start and end to clk[0]
+    // and clk[1] -- the SM clock the kernel ran at, for the per-kernel timer
+    unsigned long long *clk;
+};
+
+// Start and end of a CTA's clock record (see Params::clk).
+struct ClockMark {
+    unsigned long long c0 = 0, t0 = 0;
+    __device__ __forceinline__ void start(const unsigned long long *clk) {
+        if (clk && threadIdx.x == 0) {
+            c0 = clock64();
+            t0 = global_timer_ns();
+        }
+    }
+    __device__ __forceinline__ void stop(unsigned long long *clk) const {
+        if (clk && threadIdx.x == 0) {
+            atomicAdd(clk, static_cast<unsigned long long>(clock64()) - c0);
+            atomicAdd(clk + 1, global_timer_ns() - t0);
+        }
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -1065,6 +1086,8 @@ __device__ __forceinline__ void run_epilogue(const Params &p, int pi, int row, i
 // ---------------------------------------------------------------------------
 template <int EPI, bool A_MN, bool B_MN, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Params p) {
+    ClockMark clk_mark;
+    clk_mark.start(p.clk);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
@@ -1248,6 +1271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    clk_mark.stop(p.clk);
 }
 
 // ---------------------------------------------------------------------------
@@ -1377,6 +1401,8 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 // gradients under sequence parallelism); their maps follow a SelCursor.
 template <int EPI, bool A_MN, bool B_MN, bool F8, bool TS = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ Params p) {
+    ClockMark clk_mark;
+    clk_mark.start(p.clk);
     constexpr int NST = pair_stages<EPI>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1632,6 +1658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     cluster_sync();
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    clk_mark.stop(p.clk);
 }
 
 }  // namespace tc

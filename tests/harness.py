@@ -12,6 +12,16 @@ import synth
 TOL = {"f32": 1e-5, "bf16": 1e-2}
 
 
+def status_ok(tp, *handles) -> bool:
+    """Synchronise and read (clearing them) the status word of the calls
+    without a handle and the words of the given MLP / sub-block handles:
+    True when none of them recorded a device-side error."""
+    ok = tp.sync_status() == 0
+    for h in handles:
+        ok = (h.sync_status() == 0) and ok
+    return ok
+
+
 def rel_err(gpu, ref) -> float:
     """max |gpu - ref| / max |ref| over all elements (fp64)."""
     g = np.asarray(gpu, dtype=np.float64)

@@ -46,3 +46,16 @@ def test_step_bytes_counts_each_tensor_once():
     M, H, F = w.M, w.H, w.F
     expect = 2 * (4 * M * H + 2 * M * F + 2 * F * H) + 4 * 2 * F * H
     assert bench.step_bytes(w) == expect
+
+
+def test_peak_follows_the_timed_region():
+    """A timed region shorter than the sustained measurement's 4 s is
+    compared against the burst peak, a longer one against the sustained
+    peak; FP8 takes twice the bf16 figure."""
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "measured"}
+    p, kind = bench.pick_peak(peaks, 0.074, "bf16")
+    assert p == 1900.0 and "burst" in kind and "0.07 s" in kind
+    p, kind = bench.pick_peak(peaks, 12.0, "bf16")
+    assert p == 1700.0 and "sustained" in kind
+    p, kind = bench.pick_peak(peaks, 1.0, "fp8")
+    assert p == 3800.0 and kind.startswith("fp8")

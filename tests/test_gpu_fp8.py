@@ -21,7 +21,7 @@ import torch
 
 import oracle
 import synth
-from harness import MlpRun, host, mlp_inputs, rel_err
+from harness import MlpRun, host, mlp_inputs, rel_err, status_ok
 from oracle import fp8
 
 pytestmark = pytest.mark.gpu
@@ -89,7 +89,7 @@ def test_fp8_mlp_matches_fp8_oracle(tp, tile_mode, M, H, F, T, act, bias, residu
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     f = fp8.mlp_fwd_fp8(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, residual)
     gr = fp8.mlp_bwd_fp8(t["dY"], f, act, residual)
     errs = {"Y": rel_err(run.gathered(run.Y), f["Y"]), "dX": rel_err(run.gathered(run.dX), gr["dX"])}
@@ -117,7 +117,7 @@ def test_fp8_needs_workspace_and_mlp_entry_points(tp):
     with pytest.raises(tp.TpError) as e:
         tp.linear_col(L, run.X, run.W1, None, run.A)
     assert e.value.status == 3
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
 
 
 def test_fp8_gpt_full_size_sampled(tp):
@@ -135,7 +135,7 @@ def test_fp8_gpt_full_size_sampled(tp):
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     rows = np.array(sorted({0, 1, 777, 4095, 4096, 8190, 8191} | set(np.random.default_rng(5).integers(0, w.M, 25))))
     Fs = w.F // w.T
     units = [np.array([0, 100, Fs - 1]) for _ in range(w.T)]
@@ -171,7 +171,7 @@ def test_fp8_delayed_scaling_matches_oracle_over_steps(tp, n):
         run.dY[0].copy_(torch.from_numpy(t["dY"]).to(torch.bfloat16))
         run.fwd()
         run.bwd()
-        assert tp.sync_status() == 0
+        assert status_ok(tp, lay)
         f = fp8.mlp_fwd_fp8(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, True, hist)
         gr = fp8.mlp_bwd_fp8(t["dY"], f, act, True, hist)
         errs = {"Y": rel_err(run.gathered(run.Y), f["Y"]), "dX": rel_err(run.gathered(run.dX), gr["dX"]),
@@ -218,7 +218,7 @@ def test_fp8_amax_of_every_operand(tp, n, act, F):
         run.bwd()
         f = fp8.mlp_fwd_fp8(t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, True, hist)
         gr = fp8.mlp_bwd_fp8(t["dY"], f, act, True, hist)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     got = host(lay.fp8_amax(run.ws)).astype(np.float64)
 
     def amax(bufs):

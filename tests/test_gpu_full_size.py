@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from harness import MlpRun, host, rel_err
+from harness import MlpRun, host, rel_err, status_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +72,7 @@ def test_mlp_workload_sampled(tp, name):
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     M, T, Fs = w.M, w.T, w.F // w.T
     rows = sample_rows(M, T, w.seq_parallel)
     r = oracle.mlp_rows(rows, t["X"], t["W1s"], t["b1s"], t["W2s"], t["b2"], t["dY"], w.act, w.residual)
@@ -165,7 +165,7 @@ def test_tiny_workload_through_linear_layers(tp):
     Y = torch.empty_like(run.Y[0])
     tp.linear_col(colL, run.X, run.W1, run.b1, A, pre)
     tp.linear_row(rowL, A, run.W2, run.b2, None, [Y])
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     assert torch.equal(Y, run.Y[0])
     for a, b in zip(A + pre, run.A + run.pre):
         assert torch.equal(a, b)

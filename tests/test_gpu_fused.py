@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from harness import MlpRun, host, mlp_inputs, rel_err
+from harness import MlpRun, host, mlp_inputs, rel_err, status_ok
 from oracle import layer as olayer
 
 pytestmark = pytest.mark.gpu
@@ -48,7 +48,7 @@ def _fwd(tp, lay, t, mode):
     n0 = tp.launch_count()
     run.fwd()
     launches = tp.launch_count() - n0
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     return run, launches
 
 
@@ -85,7 +85,7 @@ def test_fused_forward_feeds_the_backward(tp):
     for mode in ("on", "off"):
         run, _ = _fwd(tp, lay, t, mode)
         run.bwd()
-        assert tp.sync_status() == 0
+        assert status_ok(tp, lay)
         outs.append(run)
     a, b = outs
     for x, y in zip(a.dW1 + a.dW2 + [a.db2] + a.db1 + a.dX, b.dW1 + b.dW2 + [b.db2] + b.db1 + b.dX):
@@ -102,7 +102,7 @@ def test_fused_forward_not_taken_outside_its_shapes(tp):
         n0 = tp.launch_count()
         run.fwd()
         assert tp.launch_count() - n0 == 2, kw
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     tp.set_fused_fwd("auto")
 
 
@@ -119,7 +119,7 @@ def test_fused_layer_forward_with_dropout(tp):
     run.fwd(SEED)
     assert tp.launch_count() - n0 == 2  # LayerNorm + fused MLP
     run.bwd(SEED)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     f = olayer.layer_fwd(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], "gelu_tanh",
                          _p32(p), SEED)
     gr = olayer.layer_bwd(t["dY"], t["X"], t["gamma"], t["W1s"], t["W2s"], f, "gelu_tanh", _p32(p))

@@ -8,7 +8,7 @@ call is captured; the test uses current scaling there.)"""
 import pytest
 import torch
 
-from harness import MlpRun, mlp_inputs
+from harness import MlpRun, mlp_inputs, status_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def test_mlp_step_replays_bitwise(tp, dtype, act, sp):
         run.fwd()  # eager warm-up call
         run.bwd()
     s.synchronize()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     ref = [x.clone() for x in run.Y + run.dX + run.pre + run.A + run.dW1 + run.dW2 + run.db1 + [run.db2]]
     for x in run.Y + run.dX + run.dW1 + run.dW2:
         x.fill_(float("nan"))
@@ -45,7 +45,7 @@ def test_mlp_step_replays_bitwise(tp, dtype, act, sp):
     for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     out = run.Y + run.dX + run.pre + run.A + run.dW1 + run.dW2 + run.db1 + [run.db2]
     for a, b in zip(ref, out):
         assert torch.equal(a, b)
@@ -69,6 +69,6 @@ def test_layer_step_replays_bitwise(tp):
         run.bwd(SEED)
     g.replay()
     torch.cuda.synchronize()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for a, b in zip(ref, run.Y + run.dX + [run.Xn, run.dgamma, run.dbeta, run.db2] + run.dW1):
         assert torch.equal(a, b)

@@ -19,7 +19,7 @@ import torch
 
 import oracle
 import synth
-from harness import TOL, dev, host, mlp_inputs, rel_err, split_tokens
+from harness import TOL, dev, host, mlp_inputs, rel_err, split_tokens, status_ok
 from oracle import layer as olayer
 
 pytestmark = pytest.mark.gpu
@@ -127,7 +127,7 @@ def test_layer_matches_oracle(tp, tile_mode, M, H, F, T, act, dtype, bias, sp, p
     run = LayerRun(lay, t)
     run.fwd(SEED)
     run.bwd(SEED)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     p = _p32(p)
     f = olayer.layer_fwd(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, p, SEED)
     gr = olayer.layer_bwd(t["dY"], t["X"], t["gamma"], t["W1s"], t["W2s"], f, act, p)
@@ -165,7 +165,7 @@ def test_dropout_keep_flags_bit_exact(tp, dtype, sp, p):
     run = LayerRun(lay, t)
     seed = 987654321987
     run.fwd(seed)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     jump = run.gathered(run.Y) - run.gathered(run.X)
     keep = jump > 0.5 / (1.0 - _p32(p))
     ref = olayer.dropout_keep(seed, np.arange(M), H, _p32(p))
@@ -187,7 +187,7 @@ def test_layer_is_deterministic(tp):
         run.bwd(SEED)
         outs.append([run.gathered(run.Y), run.gathered(run.dX), host(run.dgamma), host(run.dbeta),
                      host(run.dW1[0]), host(run.db2)])
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
 
@@ -216,7 +216,7 @@ def test_dropout_backward_mask_equals_redrawn_flags(tp, fused):
         run.bwd(SEED)
         outs.append([run.gathered(run.dX), host(run.dgamma), host(run.dbeta), host(run.db2),
                      host(run.dW1[0]), host(run.dW2[1])])
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for later in outs[1:]:
         for a, b in zip(outs[0], later):
             assert np.array_equal(a, b)
@@ -235,7 +235,7 @@ def test_layer_fp8_matches_fp8_oracle(tp, tile_mode):
     run = LayerRun(lay, t)
     run.fwd(SEED)
     run.bwd(SEED)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     p = _p32(p)
     f = olayer.layer_fwd_fp8(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act, p, SEED)
     gr = olayer.layer_bwd_fp8(t["dY"], t["X"], t["gamma"], act, p, f)
@@ -264,7 +264,7 @@ def test_layer_fp8_amax(tp):
     for _ in range(2):
         run.fwd(SEED)
         run.bwd(SEED)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     got = host(lay.fp8_amax(run.ws)).astype(np.float64)
 
     def amax(bufs):
@@ -281,7 +281,7 @@ def test_layer_empty_tokens_zero_the_gradients(tp):
     run = LayerRun(lay, t)
     run.fwd(SEED)
     run.bwd(SEED)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for b in [run.dgamma, run.dbeta, run.db2, *run.dW1, *run.dW2, *run.db1]:
         assert torch.count_nonzero(b).item() == 0
 
@@ -306,7 +306,7 @@ def test_layer_gpt_full_size_sampled(tp):
     run = LayerRun(lay, t)
     run.fwd(seed)
     run.bwd(seed)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     p = _p32(p)
     M, H, T, Fs = w.M, w.H, w.T, w.F // w.T
     X = np.asarray(t["X"], np.float64)
@@ -358,7 +358,7 @@ def test_layer_fp8_delayed_scaling_over_steps(tp):
         run.X[0].copy_(torch.from_numpy(t["X"]).to(torch.bfloat16))
         run.fwd(SEED + step)
         run.bwd(SEED + step)
-        assert tp.sync_status() == 0
+        assert status_ok(tp, lay)
         f = olayer.layer_fwd_fp8(t["X"], t["gamma"], t["beta"], t["W1s"], t["b1s"], t["W2s"], t["b2"], act,
                                  _p32(p), SEED + step, history=hist)
         gr = olayer.layer_bwd_fp8(t["dY"], t["X"], t["gamma"], act, _p32(p), f, history=hist)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from harness import TOL, MlpRun, host, mlp_inputs, oracle_full, rel_err
+from harness import TOL, MlpRun, host, mlp_inputs, oracle_full, rel_err, status_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,7 @@ def test_mlp_matches_oracle(tp, tile_mode, M, H, F, T, act, dtype, bias, residua
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     ref = oracle_full(lay, t)
     _check_all(run, ref, lay, TOL[dtype])
 
@@ -103,7 +103,7 @@ def test_tiny_workload_full(tp):
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     _check_all(run, oracle_full(lay, t), lay, 1e-5)
 
 
@@ -118,7 +118,7 @@ def test_column_shards_are_independent_bitwise(tp, tile_mode):
     run.W1[2].mul_(-1.5)
     run.b1[2].add_(1.0)
     run.fwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for i in range(4):
         same = torch.equal(run.pre[i], pre0[i]) and torch.equal(run.A[i], A0[i])
         assert same == (i != 2)
@@ -136,7 +136,7 @@ def test_row_backward_needs_no_reduction_bitwise(tp, tile_mode):
     dW1 = [d.clone() for d in run.dW1]
     run.W2[1].mul_(0.5)
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for i in range(4):
         assert torch.equal(run.dW2[i], dW2[i])
         assert torch.equal(run.dW1[i], dW1[i]) == (i != 1)
@@ -153,7 +153,7 @@ def test_sharded_equals_unsharded_on_gpu(tp):
         run = MlpRun(lay, t)
         run.fwd()
         run.bwd()
-        assert tp.sync_status() == 0
+        assert status_ok(tp, lay)
         outs[T] = (run.gathered(run.Y), run.gathered(run.dX),
                    oracle.unshard_column([host(d) for d in run.dW1]))
     for T in (2, 4, 8):
@@ -177,7 +177,7 @@ def test_deterministic_and_accumulate(tp, tile_mode):
     acc = tp.TPMLP(S=150, B=2, H=264, F=800, T=4, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True,
                    wgrad_accumulate=True)
     acc.bwd(run.dY, run.X, run.W1, run.W2, run.pre, run.A, run.dX, run.dW1, run.db1, run.dW2, run.db2, run.ws)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay, acc)
     for a, b in zip(dW10, run.dW1):
         assert torch.equal(2 * a, b)
 
@@ -197,7 +197,7 @@ def test_split_k_weight_gradients_deterministic_and_accumulate(tp, tile_mode):
     acc = tp.TPMLP(S=2050, B=2, H=256, F=512, T=2, act="gelu_tanh", dtype="bf16", has_bias=True,
                    wgrad_accumulate=True)
     acc.bwd(run.dY, run.X, run.W1, run.W2, run.pre, run.A, run.dX, run.dW1, run.db1, run.dW2, run.db2, run.ws)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay, acc)
     for a, b in zip(dW10 + dW20, run.dW1 + run.dW2):
         assert torch.equal(2 * a, b)
 
@@ -208,7 +208,7 @@ def test_empty_tokens(tp):
     run = MlpRun(lay, t)
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     for d in run.dW1 + run.dW2 + run.db1 + [run.db2]:
         assert torch.count_nonzero(d).item() == 0
 
@@ -225,8 +225,32 @@ def test_bounded_wait_reports_timeout(tp):
     t = mlp_inputs(128, 64, 256, 2, "gelu_tanh", "bf16")
     run = MlpRun(lay, t)
     run.fwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     assert rel_err(run.gathered(run.Y), oracle_full(lay, t)["Y"]) < 1e-2
+
+
+def test_timeout_reaches_only_its_handle(tp):
+    """Two MLP handles used on two streams: a bounded wait that runs out under
+    handle A is reported by A's status word only.  Handle B's calls in the
+    meantime neither see nor clear it, and the word of the calls without a
+    handle stays clean."""
+    assert tp.sync_status() == 0
+    a = tp.TPMLP(S=64, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    b = tp.TPMLP(S=64, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
+    assert a.sync_status() == 0 and b.sync_status() == 0
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    t = mlp_inputs(128, 64, 256, 2, "gelu_tanh", "bf16")
+    run = MlpRun(b, t)
+    torch.cuda.synchronize()  # inputs uploaded before the two streams start
+    a.debug_wait_timeout(2_000_000, stream=sa)  # 2 ms, on A's stream
+    with torch.cuda.stream(sb):
+        run.fwd()
+        run.bwd()
+    assert b.sync_status(sb) == 0
+    assert tp.sync_status(sb) == 0
+    assert a.sync_status(sa) == 5
+    assert a.sync_status(sa) == 0  # read clears it
+    assert rel_err(run.gathered(run.Y), oracle_full(b, t)["Y"]) < 1e-2
 
 
 def test_binding_rejects_wrong_shapes(tp):

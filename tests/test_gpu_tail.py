@@ -23,7 +23,7 @@ import pytest
 import torch
 
 import oracle
-from harness import MlpRun, host, mlp_inputs, oracle_full, rel_err
+from harness import MlpRun, host, mlp_inputs, oracle_full, rel_err, status_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +57,7 @@ def _step(tp, lay, t, split, pairs):
     n0 = tp.tail_split_count()
     run.fwd()
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     return run, tp.tail_split_count() - n0
 
 
@@ -162,7 +162,7 @@ def test_layer_tail_split_with_dropout(tp):
         n0 = tp.tail_split_count()
         run.fwd(SEED)
         run.bwd(SEED)
-        assert tp.sync_status() == 0
+        assert status_ok(tp, lay)
         runs.append((run, tp.tail_split_count() - n0))
     (a, na), (b, nb) = runs
     assert na >= 4 and nb == 0, (na, nb)
@@ -213,7 +213,7 @@ def test_tail_split_needs_its_scratch(tp):
     run.fwd()
     run.bwd()
     run.fwd(with_workspace=False)
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     assert tp.tail_split_count() == n0
     ref = oracle_full(lay, t)
     assert rel_err(run.gathered(run.Y), ref["Y"]) <= 1e-2
@@ -239,7 +239,7 @@ def test_tail_split_weight_gradient_accumulation(tp):
     run.bwd()
     once = [d.clone() for d in run.dW1 + run.dW2]
     run.bwd()
-    assert tp.sync_status() == 0
+    assert status_ok(tp, lay)
     assert tp.tail_split_count() - n0 >= 4
     for a, b in zip(once, run.dW1 + run.dW2):
         assert torch.equal(2 * a, b)
