@@ -227,3 +227,74 @@ def mlp_sampled_fp8(rows, units, X, W1s, b1s, W2s, b2, dY, act: str, residual: b
         out["dW2"].append((dYq.T @ Aq[i][:, u]) * dequant(sdy, sa))
         out["db1"].append(dPre[i][:, sel].sum(axis=0))
     return out
+
+
+# ----------------------------------------------------------------------------
+# the single layers in FP8 (the same readings F1-F5 applied to one
+# ColumnParallelLinear or RowParallelLinear): the layer's input activation and
+# weight are quantised E4M3 in the forward, its upstream gradient E5M2 in the
+# backward, each with one scale over all its shards; current scaling.
+# ----------------------------------------------------------------------------
+def column_fwd_fp8(X, W_shards, b_shards, act: str):
+    """ColumnParallelLinear + activation: pre_i = Xq Wq_i^T / (s_x s_w) + b_i,
+    out_i = act(pre_i); pre and out stored in bf16.  X is the full [M, H]
+    input.  Returns (pre list, out list), bf16 values as fp64."""
+    (Xq,), sx = quantize([X], "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    d = dequant(sx, sw)
+    pre, out = [], []
+    for i in range(len(Wq)):
+        p = (Xq @ Wq[i].T) * d
+        if b_shards is not None and b_shards[i] is not None:
+            p = p + np.asarray(b_shards[i], np.float64)
+        pre.append(round_bf16(p))
+        out.append(round_bf16(_mlp.act_fwd(p, act)))
+    return pre, out
+
+
+def row_fwd_fp8(X_shards, W_shards, b=None, R=None):
+    """RowParallelLinear: Y = (sum_i Xq_i Wq_i^T) / (s_x s_w) + b (+ R), the
+    shard sum explicit in shard order, one scale over all shards of X and of
+    W.  Returns Y in fp64 (before the bf16 store)."""
+    Xq, sx = quantize(X_shards, "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    Y = None
+    for i in range(len(Wq)):
+        part = Xq[i] @ Wq[i].T
+        Y = part if Y is None else Y + part
+    Y = Y * dequant(sx, sw)
+    if b is not None:
+        Y = Y + np.asarray(b, np.float64)
+    if R is not None:
+        Y = Y + np.asarray(R, np.float64)
+    return Y
+
+
+def column_bwd_fp8(dOut_shards, X, W_shards):
+    """Backward of ColumnParallelLinear (no activation): dOut quantised E5M2
+    over all shards, X and W as in the forward (E4M3):
+    dX = (sum_i dOq_i Wq_i) / (s_do s_w), dW_i = dOq_i^T Xq / (s_do s_x),
+    db_i = sum over tokens of the unquantised dOut_i (F5)."""
+    (Xq,), sx = quantize([X], "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    dOq, sdo = quantize(dOut_shards, "e5m2")
+    dX = None
+    for i in range(len(Wq)):
+        part = dOq[i] @ Wq[i]
+        dX = part if dX is None else dX + part
+    dX = dX * dequant(sdo, sw)
+    dW = [(dOq[i].T @ Xq) * dequant(sdo, sx) for i in range(len(Wq))]
+    db = [np.asarray(d, np.float64).sum(axis=0) for d in dOut_shards]
+    return dX, dW, db
+
+
+def row_bwd_fp8(dY, X_shards, W_shards):
+    """Backward of RowParallelLinear: dY quantised E5M2, X and W as in the
+    forward (E4M3): dX_i = dYq Wq_i / (s_dy s_w), dW_i = dYq^T Xq_i /
+    (s_dy s_x), db = sum over tokens of the unquantised dY (F5)."""
+    Xq, sx = quantize(X_shards, "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    (dYq,), sdy = quantize([dY], "e5m2")
+    dX = [(dYq @ Wq[i]) * dequant(sdy, sw) for i in range(len(Wq))]
+    dW = [(dYq.T @ Xq[i]) * dequant(sdy, sx) for i in range(len(Wq))]
+    return dX, dW, np.asarray(dY, np.float64).sum(axis=0)

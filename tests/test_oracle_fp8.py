@@ -178,3 +178,70 @@ def test_delayed_scaling_on_repeated_inputs_equals_current_scaling():
             assert np.array_equal(a, b)
     assert sorted(h.hist) == ["A", "W1", "W2", "X", "dPre", "dY"]
     assert all(len(v) == 2 for v in h.hist.values())
+
+
+def _layer_inputs(seed, M=48, H=96, F=128, T=4):
+    rng = np.random.default_rng(seed)
+    r = lambda *s, sc=1.0: fp8.round_bf16(rng.standard_normal(s) * sc)
+    return rng, r, M, H, F, T
+
+
+def test_fp8_layers_close_to_exact_layers():
+    """Each FP8 single layer approximates the exact fp64 layer within the
+    formats' relative precision; a transposed operand, an inverted scale or a
+    dropped term would be off by orders of magnitude."""
+    _, r, M, H, F, T = _layer_inputs(5)
+    Fs = F // T
+    X, W, b = r(M, H), [r(Fs, H, sc=0.1) for _ in range(T)], [r(Fs, sc=0.1) for _ in range(T)]
+    dO = [r(M, Fs) for _ in range(T)]
+    Xr, W2, b2, R, dY = [r(M, Fs) for _ in range(T)], [r(H, Fs, sc=0.1) for _ in range(T)], r(H, sc=0.1), \
+        r(M, H), r(M, H)
+
+    def rel(a, b):
+        return np.max(np.abs(np.asarray(a) - np.asarray(b))) / np.max(np.abs(b))
+
+    for act in ("none", "gelu_tanh"):
+        pre8, out8 = fp8.column_fwd_fp8(X, W, b, act)
+        pre, out = oracle.column_fwd(X, W, b, act)
+        for i in range(T):
+            assert rel(pre8[i], pre[i]) < 0.05 and rel(out8[i], out[i]) < 0.05
+    assert rel(fp8.row_fwd_fp8(Xr, W2, b2, R), oracle.row_fwd(Xr, W2, b2, R)) < 0.05
+    dX8, dW8, db8 = fp8.column_bwd_fp8(dO, X, W)
+    dX, dW, db = oracle.column_bwd(dO, X, W)
+    assert rel(dX8, dX) < 0.1
+    for i in range(T):
+        assert rel(dW8[i], dW[i]) < 0.15 and rel(db8[i], db[i]) == 0.0
+    rX8, rW8, rdb8 = fp8.row_bwd_fp8(dY, Xr, W2)
+    rX, rW, rdb = oracle.row_bwd(dY, Xr, W2)
+    for i in range(T):
+        assert rel(rX8[i], rX[i]) < 0.1 and rel(rW8[i], rW[i]) < 0.15
+    assert rel(rdb8, rdb) == 0.0
+
+
+def test_fp8_layers_compose_to_the_fp8_mlp():
+    """Column layer, activation and row layer in FP8, chained the way the MLP
+    chains them (the row layer's input is the stored bf16 activation), give
+    the FP8 MLP's outputs exactly; the row backward's dX_i is the MLP's dA_i
+    before act', and its dW the MLP's dW2."""
+    _, r, M, H, F, T = _layer_inputs(6)
+    Fs = F // T
+    X, dY = r(M, H), r(M, H)
+    W1s = [r(Fs, H, sc=0.1) for _ in range(T)]
+    b1s = [r(Fs, sc=0.1) for _ in range(T)]
+    W2s = [r(H, Fs, sc=0.1) for _ in range(T)]
+    b2 = r(H, sc=0.1)
+    f = fp8.mlp_fwd_fp8(X, W1s, b1s, W2s, b2, "gelu_tanh", True)
+    g = fp8.mlp_bwd_fp8(dY, f, "gelu_tanh", True)
+    pre, A = fp8.column_fwd_fp8(X, W1s, b1s, "gelu_tanh")
+    for i in range(T):
+        assert np.array_equal(pre[i], f["pre"][i]) and np.array_equal(A[i], f["A"][i])
+    assert np.array_equal(fp8.row_fwd_fp8(A, W2s, b2, X), f["Y"])
+    dA, dW2, db2 = fp8.row_bwd_fp8(dY, A, W2s)
+    for i in range(T):
+        assert np.array_equal(dW2[i], g["dW2"][i])
+        assert np.array_equal(fp8.round_bf16(oracle.act_bwd(f["pre"][i], dA[i], "gelu_tanh")), g["dPre"][i])
+    assert np.array_equal(db2, g["db2"])
+    dX, dW1, db1 = fp8.column_bwd_fp8(g["dPre"], X, W1s)
+    assert np.array_equal(dX + dY, g["dX"])
+    for i in range(T):
+        assert np.array_equal(dW1[i], g["dW1"][i]) and np.array_equal(db1[i], g["db1"][i])
