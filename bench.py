@@ -336,8 +336,8 @@ def attn_step(args, w, tp, torch, dev, stream):
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=bf)
 
-    colL = tp.Layout(S=w.S, B=w.B, H=H, F=F, T=T, act="none", dtype="bf16")
-    rowL = tp.Layout(S=w.S, B=w.B, H=H, F=Fo, T=T, act="none", dtype="bf16")
+    colL = tp.Layout(S=w.S, B=w.B, H=H, F=F, T=T, act="none", dtype=w.dtype)
+    rowL = tp.Layout(S=w.S, B=w.B, H=H, F=Fo, T=T, act="none", dtype=w.dtype)
     Wq = [up(full["Wqkv"][i * Fs:(i + 1) * Fs]) for i in range(T)]
     Wo = [up(full["Wo"][:, i * Fos:(i + 1) * Fos]) for i in range(T)]
     X = up(full["X"])
@@ -352,8 +352,10 @@ def attn_step(args, w, tp, torch, dev, stream):
     dWo = [torch.empty(H, Fos, dtype=f32, device=dev) for _ in range(T)]
     wsc = tp.alloc_workspace(tp.linear_workspace_bytes(colL), device=dev)
     wsr = tp.alloc_workspace(tp.linear_workspace_bytes(rowL), device=dev)
-    # inputs (X, Z, the two upstream gradients) and activation results (the
-    # QKV projection, the output projection, dX, dZ) per buffer set
+    # inputs (X, Z, the two upstream gradients) and outputs per buffer set;
+    # the e2e leg reads back the results at the block's boundary -- the output
+    # projection and the input gradient dX, as for the MLP -- while the QKV
+    # projection and dZ stay on the device for the attention core
     bufs = [(X, Z, dYq, dYo, (Yq, Yo, dX, dZ)),
             (torch.empty_like(X), [torch.empty_like(z) for z in Z], [torch.empty_like(d) for d in dYq],
              torch.empty_like(dYo), ([torch.empty_like(y) for y in Yq], torch.empty_like(Yo), torch.empty_like(dX),
@@ -361,11 +363,13 @@ def attn_step(args, w, tp, torch, dev, stream):
 
     def step(k=0):
         X, Z, dYq, dYo, (Yq, Yo, dX, dZ) = bufs[k]
-        tp.linear_col(colL, [X], Wq, None, Yq, stream=stream)
-        tp.linear_row(rowL, Z, Wo, None, None, [Yo], stream=stream)
+        # the forward's workspace goes, unchanged, to the backward (FP8: the
+        # forward's quantised X and W; bf16: the row GEMM's tail-split scratch)
+        tp.linear_col(colL, [X], Wq, None, Yq, stream=stream, workspace=wsc)
+        tp.linear_row(rowL, Z, Wo, None, None, [Yo], stream=stream, workspace=wsr)
         tp.linear_col_bwd(colL, dYq, [X], Wq, [dX], dWq, None, workspace=wsc, stream=stream)
         tp.linear_row_bwd(rowL, [dYo], Z, Wo, dZ, dWo, None, workspace=wsr, stream=stream)
-    return step, [([X] + Z + dYq + [dYo], Yq + [Yo, dX] + dZ) for X, Z, dYq, dYo, (Yq, Yo, dX, dZ) in bufs], None
+    return step, [([X] + Z + dYq + [dYo], [Yo, dX]) for X, Z, dYq, dYo, (Yq, Yo, dX, dZ) in bufs], None
 
 
 def run_gpu(args, w, dist, rank, local, ws):
@@ -378,6 +382,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     tp.set_tile_mode(args.tile_mode)
     tp.set_fused_fwd(args.fused)
     tp.set_tail_split(args.tail_split == "on")
+    tp.set_k_order(args.k_order == "alternate")
     dev = torch.device("cuda", local)
     layer = args.block == "layer"
     # all work on one non-default stream (a CUDA graph cannot capture the legacy stream)
@@ -446,7 +451,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     # ---- end to end through the C ABI with host buffers ---------------------
     # Every step copies its inputs (X and dY; for the projections X, Z and the
     # two upstream gradients) from pinned host memory and its activation
-    # results (Y and dX; for the projections both outputs, dX and dZ) back.
+    # results (Y and dX; for the projections the output projection and dX) back.
     # The copies run on a second stream into two alternating device buffer
     # sets, so that step i's compute overlaps step i+1's inputs and step i-1's
     # output (events order each copy against the compute that uses the set).
@@ -723,6 +728,9 @@ def main():
                     help="bf16 GEMM tiling: CTA-pair 256-row tiles (auto) or single-CTA 128-row tiles")
     ap.add_argument("--wgrad-accumulate", action="store_true",
                     help="micro-batch step: the weight gradients are added into persistent fp32 buffers")
+    ap.add_argument("--k-order", default="alternate", choices=["alternate", "forward"],
+                    help="K order of the pair GEMMs' whole tiles: every other persistent round backwards "
+                         "(alternate, fewer operand re-reads from HBM) or always forwards")
     ap.add_argument("--tail-split", default="on", choices=["on", "off"],
                     help="cut the persistent GEMMs' part-filled last round of tiles along K over all CTA pairs")
     args = ap.parse_args()
@@ -734,8 +742,10 @@ def main():
         w = dataclasses.replace(w, dtype="fp8")
     if args.seq_len > 0:
         w = dataclasses.replace(w, S=args.seq_len)
-    if w.kind == "attn_proj" and (w.dtype != "bf16" or args.block != "mlp"):
-        raise SystemExit("the attention projections are timed in bf16 as plain layers")
+    if w.kind == "attn_proj" and (w.dtype not in ("bf16", "fp8") or args.block != "mlp"):
+        raise SystemExit("the attention projections are timed in bf16 or FP8 as plain layers")
+    if w.kind == "attn_proj" and args.fp8_history:
+        raise SystemExit("the single layers quantise with current scaling (no amax history)")
     ws, rank, local = dist_env()
     if w.kind == "attn_proj":
         desc = (f"{w.name}: X [S={w.S},B={w.B},H={w.H}] {w.dtype}, QKV column layer H -> {w.F} and output row "
@@ -750,6 +760,7 @@ def main():
               "l2": f"inputs larger than L2 (~{step_bytes(w) / 1e9:.1f} GB of operands, activations and "
                     f"gradients per step)",
               "tile_mode": args.tile_mode, "fused_fwd": args.fused, "tail_split": args.tail_split,
+              "k_order": args.k_order,
               "wgrad_accumulate": args.wgrad_accumulate,
               "launch": "CUDA graph replay per step" if args.graph else "eager C-ABI calls per step"}
     if w.dtype == "fp8":

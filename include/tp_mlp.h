@@ -88,9 +88,13 @@ typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act
  * before the epilogue.  pre, A, Y, dX stay bf16 (and dPre, except under
  * delayed scaling, where the act' dgrad stores only its codes); bias
  * gradients sum dPre and dY before quantisation.  Needs H and F/T multiples
- * of 16, the forward
- * through tp_mlp_fwd_ws, and the same workspace for the following backward
- * (it carries the quantised forward operands).  MLP entry points only. */
+ * of 16, the forward through tp_mlp_fwd_ws, and the same workspace for the
+ * following backward (it carries the quantised forward operands).  The single
+ * layers take the same recipe per layer (current scaling): the forward
+ * (tp_linear_col_ws / tp_linear_row_ws) quantises the layer's input
+ * activation and weight E4M3 into the workspace, and the backward given that
+ * workspace, unchanged, quantises the upstream gradient E5M2 and reuses the
+ * forward's codes. */
 typedef enum { TP_DT_F32 = 0, TP_DT_BF16 = 1, TP_DT_FP8 = 2 } tp_dtype;
 
 /* Problem description shared by the MLP and the single-layer entry points.
@@ -218,30 +222,60 @@ TP_API tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const 
 /* ---- single layers ("Megatron-LM 源码精读" s3.1, s3.2; walk-through s02) ------
  * tp_linear_col: out_i = act(X W_i^T + b_i) for every shard, no reduction.
  *   X: like tp_mlp_fwd's X; W: T x [g*Fs, H]; b: T x [g*Fs] or NULL;
- *   out: T x [M, Fs]; pre: T x [M, g*Fs] or NULL (not stored). */
+ *   out: T x [M, Fs]; pre: T x [M, g*Fs] or NULL (not stored).
+ *   TP_DT_FP8 needs tp_linear_col_ws (TP_ERR_ARG here). */
 TP_API tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X,
                         const void *const *W, const void *const *b,
                         void *const *out, void *const *pre, void *stream);
 
+/* tp_linear_col with a workspace (>= tp_linear_workspace_bytes, 256-byte
+ *   aligned).  Required for TP_DT_FP8 ("Megatron-LM 源码精读" s8.2): X and the
+ *   W shards are quantised E4M3, each with one scale over all its shards,
+ *   into the workspace, and out_i = act(Xq Wq_i^T / (s_x s_w) + b_i) with pre
+ *   and out stored bf16; tp_linear_col_bwd must then get the same workspace,
+ *   unchanged.  For bf16 / fp32 the workspace is not used. */
+TP_API tp_status tp_linear_col_ws(const tp_mlp_desc *desc, const void *const *X,
+                                  const void *const *W, const void *const *b,
+                                  void *const *out, void *const *pre, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
 /* tp_linear_row: Y = sum_i X_i W_i^T + b (+ R), the sum over shards in fp32
  *   inside one kernel.  X: T x [M, Fs]; W: T x [H, Fs]; b: [H] or NULL;
  *   R: like Y, or NULL (required iff desc->residual); Y: 1 x [M, H] or T token
- *   shards under seq_parallel.  desc->act is ignored. */
+ *   shards under seq_parallel.  desc->act is ignored.  TP_DT_FP8 needs
+ *   tp_linear_row_ws (TP_ERR_ARG here). */
 TP_API tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X,
                         const void *const *W, const void *b,
                         const void *const *R, void *const *Y, void *stream);
 
-/* Workspace bytes for tp_linear_col_bwd / tp_linear_row_bwd: bias partials,
- * then split-K partials of the weight gradient (as for tp_mlp_bwd), then the
- * tail-split scratch of the bf16 dgrad and weight-gradient GEMMs (optional, as
- * for tp_mlp_workspace_bytes). */
+/* tp_linear_row with a workspace (>= tp_linear_workspace_bytes, 256-byte
+ *   aligned).  Required for TP_DT_FP8: the X and W shards are quantised E4M3
+ *   (one scale per tensor over its shards) into the workspace and
+ *   Y = sum_i Xq_i Wq_i^T / (s_x s_w) + b (+ R); tp_linear_row_bwd must then
+ *   get the same workspace, unchanged.  For bf16 the workspace's tail-split
+ *   scratch lets the row GEMM split its last round (tp_set_tail_split); a
+ *   workspace smaller than what tp_linear_row_bwd requires is ignored. */
+TP_API tp_status tp_linear_row_ws(const tp_mlp_desc *desc, const void *const *X,
+                                  const void *const *W, const void *b,
+                                  const void *const *R, void *const *Y, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Workspace bytes for the single layers: bias partials, then split-K partials
+ * of the weight gradient (as for tp_mlp_bwd), then for TP_DT_FP8 the amax
+ * slots and the codes of the layer's input activation, weight and upstream
+ * gradient, then the tail-split scratch of the bf16 / FP8 pair GEMMs
+ * (optional, as for tp_mlp_workspace_bytes).  One size serves a column and a
+ * row layer of the descriptor. */
 TP_API size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc);
 
 /* tp_linear_col_bwd: gradients of tp_linear_col with act = TP_ACT_NONE
  *   (TP_ERR_UNSUPPORTED otherwise; the fused activation backward belongs to
  *   tp_mlp_bwd).  dOut: T x [M, Fs]; X, W as in the forward;
  *   dX = sum_i dOut_i W_i (fp32 sum over shards in one kernel), stored like X;
- *   dW_i = dOut_i^T X (fp32, T x [Fs, H]); db_i = sum_m dOut_i (fp32) or NULL. */
+ *   dW_i = dOut_i^T X (fp32, T x [Fs, H]); db_i = sum_m dOut_i (fp32) or NULL.
+ *   TP_DT_FP8: the workspace of the tp_linear_col_ws call, unchanged; dOut is
+ *   quantised E5M2 (one scale over its shards) and the products use the
+ *   forward's codes of X and W; db sums the unquantised dOut. */
 TP_API tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut,
                             const void *const *X, const void *const *W,
                             void *const *dX, void *const *dW, void *const *db,
@@ -250,7 +284,10 @@ TP_API tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *d
 /* tp_linear_row_bwd: gradients of tp_linear_row (no reduction over shards).
  *   dY: like Y; X, W as in the forward; dX_i = dY W_i (T x [M, Fs]);
  *   dW_i = dY^T X_i (fp32, T x [H, Fs]); db = sum_m dY (fp32 [H]) or NULL.
- *   The residual's gradient is dY itself and is not materialised. */
+ *   The residual's gradient is dY itself and is not materialised.
+ *   TP_DT_FP8: the workspace of the tp_linear_row_ws call, unchanged; dY is
+ *   quantised E5M2 and the products use the forward's codes of X and W; db
+ *   sums the unquantised dY. */
 TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *dY,
                             const void *const *X, const void *const *W,
                             void *const *dX, void *const *dW, void *db,
@@ -275,7 +312,8 @@ TP_API tp_status tp_linear_row_bwd(const tp_mlp_desc *desc, const void *const *d
  *     (results differ from tp_linear_row_bwd by fp32 summation order where
  *     that call splits).
  *   A problem whose bias partials exceed 4 MiB (4 * ceil(M/256) * H bytes,
- *   rounded up to 256, when has_bias) returns TP_ERR_UNSUPPORTED.
+ *   rounded up to 256, when has_bias) returns TP_ERR_UNSUPPORTED, and so does
+ *   TP_DT_FP8 (its backward needs the forward's workspace).
  *   The device address of the array is looked up on the first call per
  *   device and CUDA context (with that device current); make that first call
  *   before any stream capture.  All calls share the one array and each call
@@ -446,6 +484,19 @@ TP_API tp_status tp_set_tile_mode(int mode);
  * fp32 rounding; a given configuration is run-to-run deterministic.
  * TP_ERR_ARG unless on is 0 or 1. */
 TP_API tp_status tp_set_tail_split(int on);
+
+/* K order of the pair-tile GEMMs' whole tiles, for all launches made after
+ * the call.  The persistent CTA pairs take their tiles round by round, and
+ * consecutive rounds share operand panels (the same band of row tiles and a
+ * column tile).  With alternate = 1 (the default) the row forward, the
+ * column dgrads and the weight gradients walk the K loop of every other
+ * round from its last block down, so that a round starts on the K blocks
+ * the previous round loaded last, which are still in L2, instead of on the
+ * ones L2 has already evicted: fewer operand re-reads from HBM.  Such tiles
+ * add the same products over K in the reverse order (fp32 rounding differs;
+ * a given configuration is run-to-run deterministic).  alternate = 0 walks
+ * every tile forwards.  TP_ERR_ARG unless alternate is 0 or 1. */
+TP_API tp_status tp_set_k_order(int alternate);
 
 /* Upper bound on the CTA pairs of the persistent pair-tile GEMMs, for all
  * launches made after the call (0, the default: as many as fit on the

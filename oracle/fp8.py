@@ -298,3 +298,34 @@ def row_bwd_fp8(dY, X_shards, W_shards):
     dX = [(dYq @ Wq[i]) * dequant(sdy, sw) for i in range(len(Wq))]
     dW = [(dYq.T @ Xq[i]) * dequant(sdy, sx) for i in range(len(Wq))]
     return dX, dW, np.asarray(dY, np.float64).sum(axis=0)
+
+
+def column_sampled_fp8(rows, units, X, W_shards, dOut_shards):
+    """column_fwd_fp8 (act none) and column_bwd_fp8 evaluated only at the
+    given token rows (pre and dX) and at the given output units of every
+    shard (``units[i]`` indexes [0, Fs): rows of dW_i); the per-tensor scales
+    still come from the full tensors.  Returns {"pre": [...], "dX", "dW"}."""
+    rows = np.asarray(rows)
+    (Xq,), sx = quantize([X], "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    dOq, sdo = quantize(dOut_shards, "e5m2")
+    d = dequant(sx, sw)
+    pre = [round_bf16((Xq[rows] @ Wq[i].T) * d) for i in range(len(Wq))]
+    dX = sum(dOq[i][rows] @ Wq[i] for i in range(len(Wq))) * dequant(sdo, sw)
+    dW = [(dOq[i][:, np.asarray(units[i])].T @ Xq) * dequant(sdo, sx) for i in range(len(Wq))]
+    return {"pre": pre, "dX": dX, "dW": dW}
+
+
+def row_sampled_fp8(rows, units, X_shards, W_shards, dY):
+    """row_fwd_fp8 (no bias or residual) and row_bwd_fp8 evaluated only at
+    the given token rows (Y and dX_i) and at the given input units of every
+    shard (``units[i]`` indexes [0, Fs): columns of dW_i); the scales come
+    from the full tensors.  Returns {"Y", "dX": [...], "dW": [...]}."""
+    rows = np.asarray(rows)
+    Xq, sx = quantize(X_shards, "e4m3")
+    Wq, sw = quantize(W_shards, "e4m3")
+    (dYq,), sdy = quantize([dY], "e5m2")
+    Y = sum(Xq[i][rows] @ Wq[i].T for i in range(len(Wq))) * dequant(sx, sw)
+    dX = [(dYq[rows] @ Wq[i]) * dequant(sdy, sw) for i in range(len(Wq))]
+    dW = [(dYq.T @ Xq[i][:, np.asarray(units[i])]) * dequant(sdy, sx) for i in range(len(Wq))]
+    return {"Y": Y, "dX": dX, "dW": dW}

@@ -65,6 +65,8 @@ SIGNATURES = {
     "tp_mlp_bwd": (ctypes.c_int, [VP, PP, PP, PP, PP, PP, PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
     "tp_linear_col": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP]),
     "tp_linear_row": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP]),
+    "tp_linear_col_ws": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
+    "tp_linear_row_ws": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, VP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_linear_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Desc)]),
     "tp_linear_col_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, PP, VP, ctypes.c_size_t, VP]),
     "tp_linear_row_bwd": (ctypes.c_int, [ctypes.POINTER(Desc), PP, PP, PP, PP, PP, VP, VP, ctypes.c_size_t, VP]),
@@ -89,6 +91,7 @@ SIGNATURES = {
     "tp_tail_split_count": (ctypes.c_uint64, []),
     "tp_set_tail_split": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_max_gemm_pairs": (ctypes.c_int, [ctypes.c_int]),
+    "tp_set_k_order": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_fused_fwd": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
@@ -398,7 +401,9 @@ def alloc_workspace(nbytes: int, device="cuda"):
 # ---------------------------------------------------------------------------
 # single layers
 # ---------------------------------------------------------------------------
-def linear_col(layout: Layout, X, W, b, out, pre=None, stream=None):
+def linear_col(layout: Layout, X, W, b, out, pre=None, stream=None, workspace=None):
+    """Column layer forward; with `workspace` (required for dtype "fp8",
+    which then needs it, unchanged, in linear_col_bwd) tp_linear_col_ws."""
     c, T, H, Fs, g = _Checker(layout.dtype), layout.T, layout.H, layout.Fs, layout.g
     d = layout.desc()
     px = c.tensors("X", X, layout.nx, (layout.xrows, H))
@@ -406,11 +411,18 @@ def linear_col(layout: Layout, X, W, b, out, pre=None, stream=None):
     pb = c.tensors("b", b, T, (g * Fs,)) if layout.has_bias else None
     po = c.tensors("out", out, T, (layout.M, Fs))
     pp = c.optional("pre", pre, T, (layout.M, g * Fs))
-    _check(lib().tp_linear_col(ctypes.byref(d), _arr(px), _arr(pw), _arr(pb), _arr(po), _arr(pp),
-                               _stream(stream)))
+    if workspace is None:
+        _check(lib().tp_linear_col(ctypes.byref(d), _arr(px), _arr(pw), _arr(pb), _arr(po), _arr(pp),
+                                   _stream(stream)))
+    else:
+        ws, nws = _workspace(workspace)
+        _check(lib().tp_linear_col_ws(ctypes.byref(d), _arr(px), _arr(pw), _arr(pb), _arr(po), _arr(pp), ws, nws,
+                                      _stream(stream)))
 
 
-def linear_row(layout: Layout, X, W, b, R, Y, stream=None):
+def linear_row(layout: Layout, X, W, b, R, Y, stream=None, workspace=None):
+    """Row layer forward; with `workspace` (required for dtype "fp8", which
+    then needs it, unchanged, in linear_row_bwd) tp_linear_row_ws."""
     c, T, H, Fs = _Checker(layout.dtype), layout.T, layout.H, layout.Fs
     d = layout.desc()
     px = c.tensors("X", X, T, (layout.M, Fs))
@@ -418,7 +430,12 @@ def linear_row(layout: Layout, X, W, b, R, Y, stream=None):
     pb = c.tensors("b", b, 1, (H,))[0] if layout.has_bias else None
     pr = c.tensors("R", R, layout.nx, (layout.xrows, H)) if layout.residual else None
     py = c.tensors("Y", Y, layout.nx, (layout.xrows, H))
-    _check(lib().tp_linear_row(ctypes.byref(d), _arr(px), _arr(pw), pb, _arr(pr), _arr(py), _stream(stream)))
+    if workspace is None:
+        _check(lib().tp_linear_row(ctypes.byref(d), _arr(px), _arr(pw), pb, _arr(pr), _arr(py), _stream(stream)))
+    else:
+        ws, nws = _workspace(workspace)
+        _check(lib().tp_linear_row_ws(ctypes.byref(d), _arr(px), _arr(pw), pb, _arr(pr), _arr(py), ws, nws,
+                                      _stream(stream)))
 
 
 def linear_workspace_bytes(layout: Layout) -> int:
@@ -527,6 +544,13 @@ def set_tail_split(on: bool):
     """Tail split of the pair-tile GEMMs (on by default): the last,
     part-filled round of tiles is cut along K over all CTA pairs."""
     _check(lib().tp_set_tail_split(1 if on else 0))
+
+
+def set_k_order(alternate: bool):
+    """Every other persistent round of the pair GEMMs (row forward, column
+    dgrad, weight gradients) walks K backwards (True, the default) so that
+    it starts on what the previous round left in L2; False: always forwards."""
+    _check(lib().tp_set_k_order(1 if alternate else 0))
 
 
 def set_max_gemm_pairs(n: int):

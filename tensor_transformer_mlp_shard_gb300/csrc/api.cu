@@ -1142,37 +1142,8 @@ tp_status tp_mlp_bwd(tp_mlp *h, const void *const *dY, const void *const *X, con
     return TP_OK;
 }
 
-tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
-                        void *const *out, void *const *pre, void *stream) {
-    TRY(validate_desc(desc));
-    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
-    const Dims x = dims_of(desc);
-    TRY(check_array(W, x.T, "W"));
-    if (desc->has_bias) TRY(check_array(b, x.T, "b"));
-    if (x.M == 0) return TP_OK;
-    TRY(check_array(X, x.nx, "X"));
-    TRY(check_array(reinterpret_cast<const void *const *>(out), x.T, "out"));
-    if (pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
-    return column_fwd(desc, X, W, desc->has_bias ? b : nullptr, out, pre, static_cast<cudaStream_t>(stream));
-}
-
-tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
-                        const void *const *R, void *const *Y, void *stream) {
-    TRY(validate_desc(desc));
-    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
-    const Dims x = dims_of(desc);
-    TRY(check_array(W, x.T, "W"));
-    if (desc->has_bias) TRY(check_one(b, "b"));
-    if (!desc->residual && R) return set_error(TP_ERR_ARG, "R given but desc->residual is 0");
-    if (x.M == 0) return TP_OK;
-    TRY(check_array(X, x.T, "X"));
-    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
-    if (desc->residual) TRY(check_array(R, x.nx, "R"));
-    return row_fwd(desc, X, W, desc->has_bias ? b : nullptr, desc->residual ? R : nullptr, Y,
-                   static_cast<cudaStream_t>(stream));
-}
-
-// single-layer workspace: [bias partials | split-K partials of the weight gradient]
+// single-layer workspace: [bias partials | split-K partials of the weight
+// gradient | (FP8) amax slots and operand codes | tail-split scratch]
 static size_t linear_part_bytes(const tp_mlp_desc *desc) {
     if (!desc->has_bias) return 0;
     const Dims x = dims_of(desc);
@@ -1180,32 +1151,62 @@ static size_t linear_part_bytes(const tp_mlp_desc *desc) {
     return a > b ? a : b;
 }
 
-// ... then the tail-split scratch of its pair GEMMs (column layer: dgrad and
-// weight gradient; row layer: dgrad and weight gradient), at the end
-static size_t linear_tail_off(const tp_mlp_desc *desc) {
+static size_t linear_split_bytes(const tp_mlp_desc *desc) {
     const Dims x = dims_of(desc);
-    return align256(linear_part_bytes(desc) + std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs)));
+    return std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs));
 }
+
+// FP8 region of a single-layer workspace ("Megatron-LM 源码精读" s8.2 applied
+// to one layer): the amax of the layer's input activation (X), its weight (W)
+// and its upstream gradient (G), then their codes.  The forward fills X and W
+// (E4M3), the backward reads them and fills G (E5M2).  A column layer's X is
+// one [M, H] buffer (token shards gathered), its W shards [g*Fs, H] and its G
+// shards [M, Fs]; a row layer's X shards are [M, Fs], its W shards [H, Fs]
+// and its G one [M, H] buffer.
+enum { LAMAX_X = 0, LAMAX_W = 1, LAMAX_G = 2 };
+struct LinFp8Layout {
+    size_t amax, xq, xq_shard, wq, wq_shard, gq, gq_shard, end;
+};
+
+static LinFp8Layout linear_fp8_layout(const tp_mlp_desc *d) {
+    const Dims x = dims_of(d);
+    LinFp8Layout L;
+    size_t o = align256(linear_part_bytes(d) + linear_split_bytes(d));
+    L.amax = o;
+    o += 256;
+    const size_t full = align256(size_t(x.M) * x.H);
+    L.xq_shard = align256(size_t(x.M) * x.Fs);
+    L.xq = o;
+    o += std::max(full, L.xq_shard * x.T);
+    L.wq_shard = align256(size_t(x.g) * x.Fs * x.H);
+    L.wq = o;
+    o += L.wq_shard * x.T;
+    L.gq_shard = align256(size_t(x.M) * x.Fs);
+    L.gq = o;
+    o += std::max(full, L.gq_shard * x.T);
+    L.end = o;
+    return L;
+}
+
+// what a single-layer call requires (the part before the tail-split scratch)
+static size_t linear_need(const tp_mlp_desc *desc) {
+    if (desc->dtype == TP_DT_FP8) return linear_fp8_layout(desc).end;
+    return linear_part_bytes(desc) + linear_split_bytes(desc);
+}
+
+// ... then the tail-split scratch of its pair GEMMs (column layer: dgrad and
+// weight gradient; row layer: forward, dgrad and weight gradient), at the end
+static size_t linear_tail_off(const tp_mlp_desc *desc) { return align256(linear_need(desc)); }
 
 static size_t linear_tail_bytes(const tp_mlp_desc *desc) {
-    if (desc->dtype != TP_DT_BF16) return 0;
+    if (desc->dtype == TP_DT_F32) return 0;  // the fp32 engine does not split
     const Dims x = dims_of(desc);
-    size_t r = tc_tail_bytes(x.M, x.H, 1, x.T, x.Fs, false);
-    r = std::max(r, tc_tail_bytes(x.Fs, x.H, x.T, 1, x.M, false));
-    r = std::max(r, tc_tail_bytes(x.M, x.Fs, x.T, 1, x.H, false));
-    r = std::max(r, tc_tail_bytes(x.H, x.Fs, x.T, 1, x.M, false));
+    const bool f8 = desc->dtype == TP_DT_FP8;
+    size_t r = tc_tail_bytes(x.M, x.H, 1, x.T, x.Fs, f8);
+    r = std::max(r, tc_tail_bytes(x.Fs, x.H, x.T, 1, x.M, f8));
+    r = std::max(r, tc_tail_bytes(x.M, x.Fs, x.T, 1, x.H, f8));
+    r = std::max(r, tc_tail_bytes(x.H, x.Fs, x.T, 1, x.M, f8));
     return align256(r);
-}
-
-static size_t linear_need(const tp_mlp_desc *desc) {
-    const Dims x = dims_of(desc);
-    return linear_part_bytes(desc) + std::max(split_bytes(desc, x.Fs, x.H), split_bytes(desc, x.H, x.Fs));
-}
-
-size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
-    if (validate_desc(desc) != TP_OK) return 0;
-    const size_t t = linear_tail_bytes(desc);
-    return t ? linear_tail_off(desc) + t : linear_need(desc);
 }
 
 static tp_status check_ws(const tp_mlp_desc *d, void *ws, size_t bytes) {
@@ -1216,11 +1217,307 @@ static tp_status check_ws(const tp_mlp_desc *d, void *ws, size_t bytes) {
     return TP_OK;
 }
 
+// FP8 single layers: the codes and amax slots inside a checked workspace
+struct LinFp8 {
+    float *amax;
+    char *xq, *wq, *gq;
+    size_t xs, ws, gs;  // shard strides
+    void *x_at(int i) const { return xq + i * xs; }
+    void *w_at(int i) const { return wq + i * ws; }
+    void *g_at(int i) const { return gq + i * gs; }
+};
+
+static LinFp8 lin_fp8(const tp_mlp_desc *d, void *workspace) {
+    const LinFp8Layout L = linear_fp8_layout(d);
+    char *b = static_cast<char *>(workspace);
+    return {reinterpret_cast<float *>(b + L.amax), b + L.xq, b + L.wq, b + L.gq, L.xq_shard, L.wq_shard, L.gq_shard};
+}
+
+// one tensor of `nbuf` buffers of `elems` elements each, quantised into
+// consecutive slots `dst_stride` bytes apart, all with the tensor's one scale
+static void add_segs(QuantSeg *segs, int &n, const void *const *src, int nbuf, long long elems, char *dst,
+                     size_t dst_stride, int slot, int fmt) {
+    for (int j = 0; j < nbuf; ++j) segs[n++] = {src[j], dst + j * dst_stride, elems, slot, fmt};
+}
+
+// column layer forward: out_i = act(Xq Wq_i^T / (s_x s_w) + b_i)
+static tp_status fp8_linear_col_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W,
+                                    const void *const *b, void *const *out, void *const *pre, void *workspace,
+                                    cudaStream_t st) {
+    const Dims x = dims_of(d);
+    const int gw = x.g * x.Fs;
+    const LinFp8 q = lin_fp8(d, workspace);
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    const size_t rows = x.rs ? x.rs : x.M;
+    add_segs(segs, n, X, x.nx, (long long)(rows * x.H), q.xq, rows * x.H, LAMAX_X, FP8_E4M3);
+    add_segs(segs, n, W, x.T, (long long)gw * x.H, q.wq, q.ws, LAMAX_W, FP8_E4M3);
+    TRY(launch_fp8_quantize(segs, n, q.amax, true, st));
+    GemmPlan g;
+    g.name = "col_fwd";
+    g.kind = EPI_COL;
+    g.act = d->act;
+    g.M = x.M;
+    g.N = x.Fs;
+    g.P = x.T;
+    g.S = 1;
+    g.Kseg = x.H;
+    const void *xa[1] = {q.xq};
+    const void *wq[kMaxShards];
+    for (int i = 0; i < x.T; ++i) wq[i] = q.w_at(i);
+    set_operand(g.A, xa, 1, x.M, x.H, false, 0, 0, 0);
+    set_operand(g.B, wq, x.T, gw, x.H, false, 1, 0, 0);
+    g.b_dual_off = d->act == TP_ACT_SWIGLU ? x.Fs : 0;
+    set_out(g.out, reinterpret_cast<const void *const *>(out), x.T, 1, 0, x.Fs);
+    if (pre) set_out(g.out2, reinterpret_cast<const void *const *>(pre), x.T, 1, 0, gw);
+    set_bias(g, b, x.T, 1);
+    set_fp8(g, FP8_E4M3, FP8_E4M3, q.amax, LAMAX_X, LAMAX_W);
+    return launch_tc_gemm(g, st);
+}
+
+// row layer forward: Y = sum_i Xq_i Wq_i^T / (s_x s_w) + b (+R)
+static tp_status fp8_linear_row_fwd(const tp_mlp_desc *d, const void *const *X, const void *const *W, const void *b,
+                                    const void *const *R, void *const *Y, void *workspace, cudaStream_t st,
+                                    Scratch tail) {
+    const Dims x = dims_of(d);
+    const LinFp8 q = lin_fp8(d, workspace);
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    add_segs(segs, n, X, x.T, (long long)x.M * x.Fs, q.xq, q.xs, LAMAX_X, FP8_E4M3);
+    add_segs(segs, n, W, x.T, (long long)x.H * x.Fs, q.wq, q.ws, LAMAX_W, FP8_E4M3);
+    TRY(launch_fp8_quantize(segs, n, q.amax, true, st));
+    GemmPlan g;
+    g.name = "row_fwd";
+    g.kind = EPI_PLAIN;
+    g.M = x.M;
+    g.N = x.H;
+    g.P = 1;
+    g.S = x.T;
+    g.Kseg = x.Fs;
+    const void *xq[kMaxShards], *wq[kMaxShards];
+    for (int i = 0; i < x.T; ++i) {
+        xq[i] = q.x_at(i);
+        wq[i] = q.w_at(i);
+    }
+    set_operand(g.A, xq, x.T, x.M, x.Fs, false, 0, 1, 0);
+    set_operand(g.B, wq, x.T, x.H, x.Fs, false, 0, 1, 0);
+    set_out(g.out, reinterpret_cast<const void *const *>(Y), x.nx, 0, x.rs, x.H);
+    if (R) set_out(g.aux, R, x.nx, 0, x.rs, x.H);
+    const void *bb[1] = {b};
+    set_bias(g, b ? bb : nullptr, 1, 0);
+    set_fp8(g, FP8_E4M3, FP8_E4M3, q.amax, LAMAX_X, LAMAX_W);
+    set_tail(g, tail);
+    return launch_tc_gemm(g, st);
+}
+
+// column layer backward (no activation): dX = sum_i dOq_i Wq_i / (s_g s_w),
+// dW_i = dOq_i^T Xq / (s_g s_x), db_i = sum_m dOut_i
+static tp_status fp8_linear_col_bwd(const tp_mlp_desc *d, const void *const *dOut, void *const *dX,
+                                    void *const *dW, void *const *db, void *workspace, cudaStream_t st,
+                                    Scratch tail) {
+    const Dims x = dims_of(d);
+    const LinFp8 q = lin_fp8(d, workspace);
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    add_segs(segs, n, dOut, x.T, (long long)x.M * x.Fs, q.gq, q.gs, LAMAX_G, FP8_E5M2);
+    TRY(launch_fp8_quantize(segs, n, q.amax, true, st));
+    const void *gq[kMaxShards], *wq[kMaxShards];
+    for (int i = 0; i < x.T; ++i) {
+        gq[i] = q.g_at(i);
+        wq[i] = q.w_at(i);
+    }
+    {
+        GemmPlan g;
+        g.name = "col_dgrad";
+        g.kind = EPI_PLAIN;
+        g.M = x.M;
+        g.N = x.H;
+        g.P = 1;
+        g.S = x.T;
+        g.Kseg = x.Fs;
+        set_operand(g.A, gq, x.T, x.M, x.Fs, false, 0, 1, 0);
+        set_operand(g.B, wq, x.T, x.Fs, x.H, true, 0, 1, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dX), x.nx, 0, x.rs, x.H);
+        set_bias(g, nullptr, 0, 0);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, q.amax, LAMAX_G, LAMAX_W);
+        set_tail(g, tail);
+        TRY(launch_tc_gemm(g, st));
+    }
+    {
+        GemmPlan g;
+        g.name = "wgrad_col";
+        g.kind = EPI_F32;
+        g.M = x.Fs;
+        g.N = x.H;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.M;
+        const void *xa[1] = {q.xq};
+        set_operand(g.A, gq, x.T, x.M, x.Fs, true, 1, 0, 0);
+        set_operand(g.B, xa, 1, x.M, x.H, true, 0, 0, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dW), x.T, 1, 0, x.H);
+        g.accumulate = d->wgrad_accumulate != 0;
+        if (split_bytes(d, x.Fs, x.H)) {
+            g.ksplit = wgrad_ksplit(x.Fs, x.H, x.T, x.M);
+            g.split_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(d));
+        }
+        set_fp8(g, FP8_E5M2, FP8_E4M3, q.amax, LAMAX_G, LAMAX_X);
+        set_tail(g, tail);
+        TRY(launch_tc_gemm(g, st));
+    }
+    if (db) TRY(colsum(d, "bias_grad_col", dOut, x.T, 1, 0, x.T, x.Fs, db, static_cast<float *>(workspace), st));
+    return TP_OK;
+}
+
+// row layer backward: dX_i = dYq Wq_i / (s_g s_w), dW_i = dYq^T Xq_i /
+// (s_g s_x), db = sum_m dY
+static tp_status fp8_linear_row_bwd(const tp_mlp_desc *d, const void *const *dY, void *const *dX, void *const *dW,
+                                    void *db, void *workspace, cudaStream_t st, Scratch tail) {
+    const Dims x = dims_of(d);
+    const LinFp8 q = lin_fp8(d, workspace);
+    QuantSeg segs[kMaxQuantSegs];
+    int n = 0;
+    const size_t rows = x.rs ? x.rs : x.M;
+    add_segs(segs, n, dY, x.nx, (long long)(rows * x.H), q.gq, rows * x.H, LAMAX_G, FP8_E5M2);
+    TRY(launch_fp8_quantize(segs, n, q.amax, true, st));
+    const void *ga[1] = {q.gq};
+    const void *xq[kMaxShards], *wq[kMaxShards];
+    for (int i = 0; i < x.T; ++i) {
+        xq[i] = q.x_at(i);
+        wq[i] = q.w_at(i);
+    }
+    {
+        GemmPlan g;
+        g.name = "row_dgrad";
+        g.kind = EPI_PLAIN;
+        g.M = x.M;
+        g.N = x.Fs;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.H;
+        set_operand(g.A, ga, 1, x.M, x.H, false, 0, 0, 0);
+        set_operand(g.B, wq, x.T, x.H, x.Fs, true, 1, 0, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dX), x.T, 1, 0, x.Fs);
+        set_bias(g, nullptr, 0, 0);
+        set_fp8(g, FP8_E5M2, FP8_E4M3, q.amax, LAMAX_G, LAMAX_W);
+        set_tail(g, tail);
+        TRY(launch_tc_gemm(g, st));
+    }
+    {
+        GemmPlan g;
+        g.name = "wgrad_row";
+        g.kind = EPI_F32;
+        g.M = x.H;
+        g.N = x.Fs;
+        g.P = x.T;
+        g.S = 1;
+        g.Kseg = x.M;
+        set_operand(g.A, ga, 1, x.M, x.H, true, 0, 0, 0);
+        set_operand(g.B, xq, x.T, x.M, x.Fs, true, 1, 0, 0);
+        set_out(g.out, reinterpret_cast<const void *const *>(dW), x.T, 1, 0, x.Fs);
+        g.accumulate = d->wgrad_accumulate != 0;
+        if (split_bytes(d, x.H, x.Fs)) {
+            g.ksplit = wgrad_ksplit(x.H, x.Fs, x.T, x.M);
+            g.split_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(d));
+        }
+        set_fp8(g, FP8_E5M2, FP8_E4M3, q.amax, LAMAX_G, LAMAX_X);
+        set_tail(g, tail);
+        TRY(launch_tc_gemm(g, st));
+    }
+    if (db) {
+        void *const *dba = reinterpret_cast<void *const *>(&db);
+        TRY(colsum(d, "bias_grad_row", dY, x.nx, 0, x.rs, 1, x.H, dba, static_cast<float *>(workspace), st));
+    }
+    return TP_OK;
+}
+
+// workspace of a single-layer forward: required (checked) for FP8, optional
+// otherwise (then used only for the row forward's tail split, and only when
+// it holds at least what a backward call requires)
+static tp_status linear_fwd_ws(const tp_mlp_desc *d, bool has_ws, void *&workspace, size_t &workspace_bytes) {
+    if (d->dtype == TP_DT_FP8) {
+        if (!has_ws)
+            return set_error(TP_ERR_ARG, "the FP8 single-layer forward needs a workspace: call the _ws variant");
+        return check_ws(d, workspace, workspace_bytes);
+    }
+    if (!has_ws || !workspace || workspace_bytes < linear_need(d) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        workspace = nullptr;
+        workspace_bytes = 0;
+    }
+    return TP_OK;
+}
+
+static tp_status linear_col_impl(const tp_mlp_desc *desc, const void *const *X, const void *const *W,
+                                 const void *const *b, void *const *out, void *const *pre, void *workspace,
+                                 size_t workspace_bytes, bool has_ws, void *stream) {
+    TRY(validate_desc(desc));
+    const Dims x = dims_of(desc);
+    TRY(check_array(W, x.T, "W"));
+    if (desc->has_bias) TRY(check_array(b, x.T, "b"));
+    TRY(linear_fwd_ws(desc, has_ws, workspace, workspace_bytes));
+    if (x.M == 0) return TP_OK;
+    TRY(check_array(X, x.nx, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(out), x.T, "out"));
+    if (pre) TRY(check_array(reinterpret_cast<const void *const *>(pre), x.T, "pre"));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (desc->dtype == TP_DT_FP8)
+        return fp8_linear_col_fwd(desc, X, W, desc->has_bias ? b : nullptr, out, pre, workspace, st);
+    return column_fwd(desc, X, W, desc->has_bias ? b : nullptr, out, pre, st);
+}
+
+static tp_status linear_row_impl(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
+                                 const void *const *R, void *const *Y, void *workspace, size_t workspace_bytes,
+                                 bool has_ws, void *stream) {
+    TRY(validate_desc(desc));
+    const Dims x = dims_of(desc);
+    TRY(check_array(W, x.T, "W"));
+    if (desc->has_bias) TRY(check_one(b, "b"));
+    if (!desc->residual && R) return set_error(TP_ERR_ARG, "R given but desc->residual is 0");
+    TRY(linear_fwd_ws(desc, has_ws, workspace, workspace_bytes));
+    if (x.M == 0) return TP_OK;
+    TRY(check_array(X, x.T, "X"));
+    TRY(check_array(reinterpret_cast<const void *const *>(Y), x.nx, "Y"));
+    if (desc->residual) TRY(check_array(R, x.nx, "R"));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Scratch tail = scratch_after(workspace, workspace_bytes, linear_tail_off(desc));
+    if (desc->dtype == TP_DT_FP8)
+        return fp8_linear_row_fwd(desc, X, W, desc->has_bias ? b : nullptr, desc->residual ? R : nullptr, Y,
+                                  workspace, st, tail);
+    return row_fwd(desc, X, W, desc->has_bias ? b : nullptr, desc->residual ? R : nullptr, Y, st, nullptr, tail);
+}
+
+tp_status tp_linear_col(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *const *b,
+                        void *const *out, void *const *pre, void *stream) {
+    return linear_col_impl(desc, X, W, b, out, pre, nullptr, 0, false, stream);
+}
+
+tp_status tp_linear_col_ws(const tp_mlp_desc *desc, const void *const *X, const void *const *W,
+                           const void *const *b, void *const *out, void *const *pre, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    return linear_col_impl(desc, X, W, b, out, pre, workspace, workspace_bytes, true, stream);
+}
+
+tp_status tp_linear_row(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
+                        const void *const *R, void *const *Y, void *stream) {
+    return linear_row_impl(desc, X, W, b, R, Y, nullptr, 0, false, stream);
+}
+
+tp_status tp_linear_row_ws(const tp_mlp_desc *desc, const void *const *X, const void *const *W, const void *b,
+                           const void *const *R, void *const *Y, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    return linear_row_impl(desc, X, W, b, R, Y, workspace, workspace_bytes, true, stream);
+}
+
+size_t tp_linear_workspace_bytes(const tp_mlp_desc *desc) {
+    if (validate_desc(desc) != TP_OK) return 0;
+    const size_t t = linear_tail_bytes(desc);
+    return t ? linear_tail_off(desc) + t : linear_need(desc);
+}
+
 tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, const void *const *X,
                             const void *const *W, void *const *dX, void *const *dW, void *const *db, void *workspace,
                             size_t workspace_bytes, void *stream) {
     TRY(validate_desc(desc));
-    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
     if (desc->act != TP_ACT_NONE)
         return set_error(TP_ERR_UNSUPPORTED, "tp_linear_col_bwd takes act = TP_ACT_NONE (use tp_mlp_bwd)");
     const Dims x = dims_of(desc);
@@ -1238,6 +1535,8 @@ tp_status tp_linear_col_bwd(const tp_mlp_desc *desc, const void *const *dOut, co
         return zero_grads(desc, dW, x.T, sizeof(float) * x.Fs * x.H, desc->has_bias ? db : nullptr, x.T,
                           sizeof(float) * x.Fs, st);
     const Scratch tail = scratch_after(workspace, workspace_bytes, linear_tail_off(desc));
+    if (desc->dtype == TP_DT_FP8)
+        return fp8_linear_col_bwd(desc, dOut, dX, dW, desc->has_bias ? db : nullptr, workspace, st, tail);
     TRY(column_dgrad(desc, dOut, x.Fs, W, nullptr, dX, st, tail));
     TRY(wgrad(desc, "wgrad_col", dOut, 1, x.Fs, X, 0, x.H, dW, st,
               reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc)), tail));
@@ -1267,7 +1566,8 @@ tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, co
                               const void *const *W, void *const *dX, void *const *dW, void *db, void *workspace,
                               size_t workspace_bytes, void *stream, bool allow_split) {
     TRY(validate_desc(desc));
-    if (desc->dtype == TP_DT_FP8) return set_error(TP_ERR_UNSUPPORTED, "FP8 runs through tp_mlp_fwd_ws/tp_mlp_bwd");
+    if (desc->dtype == TP_DT_FP8 && !allow_split)
+        return set_error(TP_ERR_UNSUPPORTED, "FP8 needs the workspace of the forward (tp_linear_row_bwd)");
     const Dims x = dims_of(desc);
     if (x.M > 0) {
         TRY(check_array(dY, x.nx, "dY"));
@@ -1292,6 +1592,8 @@ tp_status linear_row_bwd_impl(const tp_mlp_desc *desc, const void *const *dY, co
         return zero_grads(desc, dW, x.T, sizeof(float) * x.H * x.Fs, desc->has_bias ? dba : nullptr, 1,
                           sizeof(float) * x.H, st);
     const Scratch tail = allow_split ? scratch_after(workspace, workspace_bytes, linear_tail_off(desc)) : Scratch();
+    if (desc->dtype == TP_DT_FP8)
+        return fp8_linear_row_bwd(desc, dY, dX, dW, desc->has_bias ? db : nullptr, workspace, st, tail);
     TRY(row_dgrad(desc, TP_ACT_NONE, dY, W, nullptr, dX, x.Fs, st, nullptr, nullptr, tail));
     float *split = allow_split ? reinterpret_cast<float *>(static_cast<char *>(workspace) + linear_part_bytes(desc))
                                : nullptr;
@@ -1666,6 +1968,13 @@ tp_status tp_set_tile_mode(int mode) {
 tp_status tp_set_tail_split(int on) {
     if (on != 0 && on != 1) return set_error(TP_ERR_ARG, "tail split flag must be 0 or 1, got %d", on);
     set_tail_split(on != 0);
+    return TP_OK;
+}
+
+tp_status tp_set_k_order(int alternate) {
+    if (alternate != 0 && alternate != 1)
+        return set_error(TP_ERR_ARG, "K-order flag must be 0 or 1, got %d", alternate);
+    set_k_reverse(alternate != 0);
     return TP_OK;
 }
 

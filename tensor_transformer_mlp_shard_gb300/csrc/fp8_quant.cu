@@ -216,9 +216,13 @@ tp_status launch_fp8_cast(const QuantSeg *segs, int nseg, float *amax, const flo
 tp_status launch_fp8_quantize(const QuantSeg *segs, int nseg, float *amax, bool zero_slots, cudaStream_t st,
                               bool amax_known) {
     if (amax_known) return launch_pass(false, segs, nseg, amax, st);  // amax already reduced by the producer
-    if (zero_slots) {
+    if (zero_slots) {  // one memset per distinct slot (the buffers of a tensor share one)
+        uint64_t done = 0;
         for (int i = 0; i < nseg; ++i) {
-            cudaError_t e = cudaMemsetAsync(amax + segs[i].slot, 0, sizeof(float), st);
+            const int sl = segs[i].slot;
+            if (sl >= 0 && sl < 64 && (done >> sl) & 1u) continue;
+            if (sl >= 0 && sl < 64) done |= uint64_t(1) << sl;
+            cudaError_t e = cudaMemsetAsync(amax + sl, 0, sizeof(float), st);
             if (e != cudaSuccess) return cuda_check(e, "cudaMemsetAsync(amax)");
         }
     }

@@ -154,6 +154,9 @@ void set_tile_mode(int mode);  // TP_TILE_*
 // Tail split of the pair GEMMs on (default) or off, and an upper bound on the
 // CTA pairs of their persistent grid (0: as many as fit)
 void set_tail_split(bool on);
+// K order of the pair GEMMs' whole tiles: every other persistent round walks
+// K backwards (default) or every round forwards
+void set_k_reverse(bool on);
 void set_max_gemm_pairs(int n);
 uint64_t tail_split_launches();  // pair GEMM launches that split their tail
 // Scratch bytes a pair GEMM of this shape (out M x N per problem, P problems,

@@ -106,6 +106,10 @@ extern "C" {
 tp_status tp_linear_row_bwd_noalloc(const tp_mlp_desc *desc, const void *const *dY, const void *const *X,
                                     const void *const *W, void *const *dX, void *const *dW, void *db,
                                     void *stream) {
+    // FP8 reads the quantised forward operands from the forward's workspace
+    if (desc && desc->dtype == TP_DT_FP8)
+        return tpmlp::set_error(TP_ERR_UNSUPPORTED,
+                                "the FP8 backward reads the forward's codes from its workspace (tp_linear_row_bwd)");
     // the row layer's own bias partials (0 without a bias, or for an invalid
     // descriptor: the row backward then reports the error)
     const size_t need = tpmlp::linear_row_bias_bytes(desc);

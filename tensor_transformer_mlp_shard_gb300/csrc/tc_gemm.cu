@@ -138,6 +138,7 @@ static void copy_out(Out &o, const OutPlan &src) {
 
 static std::atomic<int> g_tile_mode{0};
 static std::atomic<bool> g_tail_split{true};
+static std::atomic<bool> g_k_reverse{true};
 static std::atomic<int> g_max_pairs{0};
 static std::atomic<uint64_t> g_tail_launches{0};
 
@@ -181,6 +182,7 @@ static int pair_limit(int fit) {
 
 void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
 void set_tail_split(bool on) { tc::g_tail_split.store(on); }
+void set_k_reverse(bool on) { tc::g_k_reverse.store(on); }
 void set_max_gemm_pairs(int n) { tc::g_max_pairs.store(n > 0 ? n : 0); }
 uint64_t tail_split_launches() { return tc::g_tail_launches.load(); }
 
@@ -268,6 +270,11 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.total_work = prm.total_tiles;
     prm.tail_first = prm.total_tiles;
     prm.group_m = use_pair ? 8 : 16;
+    // alternate-round K order for the GEMMs whose operands are re-read most
+    // (row forward, column dgrad, weight gradients); the column forward and
+    // the act' dgrad keep one order (their results are compared bit for bit
+    // with the fused forward kernel and across calls of different shapes)
+    prm.k_reverse = use_pair && g_k_reverse.load() && (g.kind == EPI_PLAIN || g.kind == EPI_F32) ? 1 : 0;
     prm.act = g.act;
     prm.b_dual_off = g.b_dual_off;
     prm.accumulate = (g.accumulate && !split) ? 1 : 0;  // split-K: the reduction accumulates

@@ -94,6 +94,12 @@ struct Params {
     // bytes}), landing as the two 8 KB swizzle atoms of the 128-wide tile that
     // two 2D boxes would write
     int a3d, b3d;
+    // CTA-pair kernel: the producer walks the K loop of a whole tile
+    // backwards in every other round of the persistent loop.  Consecutive
+    // rounds share operand panels (the same band of row tiles, a column
+    // tile), and a round that starts where the previous one ended re-reads
+    // from L2 the K blocks that round loaded last instead of from HBM.
+    int k_reverse;
     float *tail_ws;                  // [tail tile][tail_s][256 rows][BN] fp32
     unsigned *tail_cnt;              // [tail tile][16 warp slices]
     int act, b_dual_off, accumulate;
@@ -363,6 +369,15 @@ struct SelCursor {
             lrow -= s.rows_split;
             ++j;
             ++idx;
+        }
+    }
+    // the K block before the current one (a K loop walked backwards)
+    __device__ __forceinline__ void retreat(const Sel &s, int step) {
+        lrow -= step;
+        if (s.rows_split && lrow < 0 && j > 0) {
+            lrow += s.rows_split;
+            --j;
+            --idx;
         }
     }
 };
@@ -1450,7 +1465,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             uint32_t phase = 0;
             uint32_t armed = 0, armed_par = 0;
             bool ok = true;
-            for (int w = pair_id; ok && w < p.total_work; w += npairs) {
+            int it = 0;
+            for (int w = pair_id; ok && w < p.total_work; w += npairs, ++it) {
                 const Work wk = work_item(p, w);
                 int pi, mt, nt;
                 tile_coords(p, wk.t, pi, mt, nt);
@@ -1458,7 +1474,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 // B rows of this CTA: its half of the 256 tile columns, or for
                 // SwiGLU the gate (rank 0) / up (rank 1) rows of 128 units
                 const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
-                int s = wk.f0 / p.num_kb, kb = wk.f0 - s * p.num_kb;
+                // odd rounds walk a whole tile's K steps from the last one down
+                const bool rev = p.k_reverse && wk.j < 0 && (it & 1);
+                const int f_first = rev ? wk.f1 - 1 : wk.f0;
+                int s = f_first / p.num_kb, kb = f_first - s * p.num_kb;
                 // K-major operands select their map and row by the tile row,
                 // once per K segment (under sequence parallelism a division
                 // per K step here cost the SP GEMMs 6-9%); MN-major ones
@@ -1527,7 +1546,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             stage = 0;
                             phase ^= 1u;
                         }
-                        if (++kb == p.num_kb) {
+                        if (rev) {
+                            if (kb == 0) {
+                                kb = p.num_kb - 1;
+                                if (--s >= 0) {
+                                    if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
+                                    if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
+                                    if constexpr (TS) {
+                                        if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
+                                        if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
+                                    }
+                                }
+                            } else {
+                                --kb;
+                                if constexpr (TS) {
+                                    if (A_MN) ca.retreat(p.selA, E::BKE);
+                                    if (B_MN) cb.retreat(p.selB, E::BKE);
+                                }
+                            }
+                        } else if (++kb == p.num_kb) {
                             kb = 0;
                             ++s;
                             if (!A_MN) select(p.selA, pi, s, m0, ia, ra);

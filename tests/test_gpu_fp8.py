@@ -106,7 +106,7 @@ def test_fp8_mlp_matches_fp8_oracle(tp, tile_mode, M, H, F, T, act, bias, residu
     assert not bad, bad
 
 
-def test_fp8_needs_workspace_and_mlp_entry_points(tp):
+def test_fp8_forward_needs_a_workspace(tp):
     lay = tp.TPMLP(S=64, B=2, H=256, F=1024, T=4, act="gelu_tanh", dtype="fp8")
     t = mlp_inputs(128, 256, 1024, 4, "gelu_tanh", "fp8", has_bias=False)
     run = MlpRun(lay, t)
@@ -115,8 +115,8 @@ def test_fp8_needs_workspace_and_mlp_entry_points(tp):
     assert e.value.status == 1
     L = tp.Layout(S=64, B=2, H=256, F=1024, T=4, act="none", dtype="fp8")
     with pytest.raises(tp.TpError) as e:
-        tp.linear_col(L, run.X, run.W1, None, run.A)
-    assert e.value.status == 3
+        tp.linear_col(L, run.X, run.W1, None, run.A)  # no workspace
+    assert e.value.status == 1
     assert status_ok(tp, lay)
 
 
@@ -228,3 +228,147 @@ def test_fp8_amax_of_every_operand(tp, n, act, F):
     assert list(got[:5]) == want, dict(zip(lay.FP8_AMAX_NAMES, zip(got, want)))
     ref_dp = float(fp8.amax_of(gr["dPre"]))
     assert abs(got[5] - ref_dp) <= 2 ** -5 * ref_dp, (got[5], ref_dp)
+
+
+# ---------------------------------------------------------------------------
+# single layers in FP8 (tp_linear_*_ws and the backward with the same
+# workspace).  The quantiser inputs are the bf16 inputs themselves, so both
+# sides quantise identical values with identical scales; the outputs differ
+# by the fp32 summation and the bf16 store only: the bf16 tolerance applies.
+# ---------------------------------------------------------------------------
+LAYER_CASES = [
+    # M, H, F, T, bias, sp
+    (300, 272, 832, 4, True, False),
+    (512, 256, 1024, 4, False, True),
+    (4096, 256, 512, 2, True, False),  # split-K weight gradients
+    (2048, 1024, 8192, 8, False, False),
+]
+
+
+def _layer_tensors(M, H, F, T, seed):
+    base = synth.SEED_BASE + 7000 + 10 * seed
+    Fs = F // T
+    r = lambda k, shape, std=1.0: synth.round_bf16(synth.normal(base + k, shape, std))
+    return {"X": r(0, (M, H)), "W": [r(1 + i, (Fs, H), 0.02) for i in range(T)],
+            "b": [r(20 + i, (Fs,), 0.02) for i in range(T)], "dO": [r(40 + i, (M, Fs)) for i in range(T)],
+            "Xr": [r(60 + i, (M, Fs)) for i in range(T)], "W2": [r(80 + i, (H, Fs), 0.02) for i in range(T)],
+            "b2": r(100, (H,), 0.02), "R": r(101, (M, H)), "dY": r(102, (M, H))}
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,H,F,T,bias,sp", LAYER_CASES)
+def test_fp8_linear_layers_match_fp8_oracle(tp, tile_mode, M, H, F, T, bias, sp):
+    t = _layer_tensors(M, H, F, T, 1)
+    Fs = F // T
+    bf, f32 = dict(dtype=torch.bfloat16, device="cuda"), dict(dtype=torch.float32, device="cuda")
+    split = (lambda a: [np.ascontiguousarray(x) for x in oracle.sp_split(a, T)]) if sp else (lambda a: [a])
+    # column layer (no activation) forward and backward, one workspace
+    col = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="fp8", has_bias=bias, seq_parallel=sp)
+    ws = tp.alloc_workspace(tp.linear_workspace_bytes(col))
+    X = [_dev(x) for x in split(t["X"])]
+    W = [_dev(w) for w in t["W"]]
+    b = [_dev(x) for x in t["b"]] if bias else None
+    out = [torch.empty(M, Fs, **bf) for _ in range(T)]
+    tp.linear_col(col, X, W, b, out, workspace=ws)
+    dX = [torch.empty(col.xrows, H, **bf) for _ in range(col.nx)]
+    dW = [torch.empty(Fs, H, **f32) for _ in range(T)]
+    db = [torch.empty(Fs, **f32) for _ in range(T)] if bias else None
+    tp.linear_col_bwd(col, [_dev(d) for d in t["dO"]], X, W, dX, dW, db, workspace=ws)
+    # row layer (bias, residual) forward and backward
+    row = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="fp8", has_bias=bias, residual=bias,
+                    seq_parallel=sp)
+    ws2 = tp.alloc_workspace(tp.linear_workspace_bytes(row))
+    Xr, W2 = [_dev(x) for x in t["Xr"]], [_dev(w) for w in t["W2"]]
+    Y = [torch.empty(row.xrows, H, **bf) for _ in range(row.nx)]
+    tp.linear_row(row, Xr, W2, _dev(t["b2"]) if bias else None, [_dev(x) for x in split(t["R"])] if bias else None,
+                  Y, workspace=ws2)
+    dXr = [torch.empty(M, Fs, **bf) for _ in range(T)]
+    dWr = [torch.empty(H, Fs, **f32) for _ in range(T)]
+    dbr = torch.empty(H, **f32) if bias else None
+    tp.linear_row_bwd(row, [_dev(x) for x in split(t["dY"])], Xr, W2, dXr, dWr, dbr, workspace=ws2)
+    assert tp.sync_status() == 0
+
+    gather = lambda bufs: np.concatenate([host(x) for x in bufs], axis=0)
+    pre, o = fp8.column_fwd_fp8(t["X"], t["W"], t["b"] if bias else None, "none")
+    cdX, cdW, cdb = fp8.column_bwd_fp8(t["dO"], t["X"], t["W"])
+    Yr = fp8.row_fwd_fp8(t["Xr"], t["W2"], t["b2"] if bias else None, t["R"] if bias else None)
+    rdX, rdW, rdb = fp8.row_bwd_fp8(t["dY"], t["Xr"], t["W2"])
+    errs = {"col_dX": rel_err(gather(dX), cdX), "row_Y": rel_err(gather(Y), Yr)}
+    for i in range(T):
+        errs[f"col_out{i}"] = rel_err(host(out[i]), o[i])
+        errs[f"col_dW{i}"] = rel_err(host(dW[i]), cdW[i])
+        errs[f"row_dX{i}"] = rel_err(host(dXr[i]), rdX[i])
+        errs[f"row_dW{i}"] = rel_err(host(dWr[i]), rdW[i])
+        if bias:
+            errs[f"col_db{i}"] = rel_err(host(db[i]), cdb[i])
+    if bias:
+        errs["row_db"] = rel_err(host(dbr), rdb)
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
+
+
+def test_fp8_column_layer_with_activation(tp):
+    """The FP8 column forward with its GeLU epilogue: pre and the activation
+    against the oracle."""
+    M, H, F, T = 300, 272, 832, 4
+    t = _layer_tensors(M, H, F, T, 2)
+    Fs = F // T
+    col = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="fp8", has_bias=True)
+    ws = tp.alloc_workspace(tp.linear_workspace_bytes(col))
+    out = [torch.empty(M, Fs, dtype=torch.bfloat16, device="cuda") for _ in range(T)]
+    pre = [torch.empty(M, Fs, dtype=torch.bfloat16, device="cuda") for _ in range(T)]
+    tp.linear_col(col, [_dev(t["X"])], [_dev(w) for w in t["W"]], [_dev(b) for b in t["b"]], out, pre,
+                  workspace=ws)
+    assert tp.sync_status() == 0
+    rp, ro = fp8.column_fwd_fp8(t["X"], t["W"], t["b"], "gelu_tanh")
+    for i in range(T):
+        assert rel_err(host(pre[i]), rp[i]) <= 1e-2
+        assert rel_err(host(out[i]), ro[i]) <= 1e-2
+
+
+def test_fp8_attention_projections_sampled(tp):
+    """The attention projections' workload (QKV column layer 4096 -> 3 x 4096
+    and output row layer 4096 -> 4096 over T = 8, X [4096, 2, 4096]) in FP8,
+    in the launch configuration bench.py times, against the FP8 oracle on
+    sampled token rows and units."""
+    from test_gpu_full_size import sample_rows, sample_units
+    w = synth.WORKLOADS["attn_proj"]
+    T, M, H, F, Fo = w.T, w.M, w.H, w.F, w.F_o
+    Fs, Fos = F // T, Fo // T
+    full = synth.attn_tensors(w)
+    Wq = [np.ascontiguousarray(x) for x in oracle.shard_column_weight(full["Wqkv"], T)]
+    Wo = [np.ascontiguousarray(x) for x in oracle.shard_row_weight(full["Wo"], T)]
+    Zs = [np.ascontiguousarray(x) for x in oracle.shard_row_weight(full["Z"], T)]
+    dYq = [np.ascontiguousarray(x) for x in oracle.shard_row_weight(full["dYqkv"], T)]
+    colL = tp.Layout(S=w.S, B=w.B, H=H, F=F, T=T, act="none", dtype="fp8")
+    rowL = tp.Layout(S=w.S, B=w.B, H=H, F=Fo, T=T, act="none", dtype="fp8")
+    wsc = tp.alloc_workspace(tp.linear_workspace_bytes(colL))
+    wsr = tp.alloc_workspace(tp.linear_workspace_bytes(rowL))
+    bf, f32 = dict(dtype=torch.bfloat16, device="cuda"), dict(dtype=torch.float32, device="cuda")
+    X, Wqd, Wod, Zd = _dev(full["X"]), [_dev(x) for x in Wq], [_dev(x) for x in Wo], [_dev(x) for x in Zs]
+    Yq = [torch.empty(M, Fs, **bf) for _ in range(T)]
+    Yo = torch.empty(M, H, **bf)
+    dX = torch.empty(M, H, **bf)
+    dWq = [torch.empty(Fs, H, **f32) for _ in range(T)]
+    dZ = [torch.empty(M, Fos, **bf) for _ in range(T)]
+    dWo = [torch.empty(H, Fos, **f32) for _ in range(T)]
+    tp.linear_col(colL, [X], Wqd, None, Yq, workspace=wsc)
+    tp.linear_row(rowL, Zd, Wod, None, None, [Yo], workspace=wsr)
+    tp.linear_col_bwd(colL, [_dev(x) for x in dYq], [X], Wqd, [dX], dWq, None, workspace=wsc)
+    tp.linear_row_bwd(rowL, [_dev(full["dYo"])], Zd, Wod, dZ, dWo, None, workspace=wsr)
+    assert tp.sync_status() == 0
+    rows = sample_rows(M, T, False)
+    us, uo = sample_units(Fs, T), sample_units(Fos, T)
+    c = fp8.column_sampled_fp8(rows, us, full["X"], Wq, dYq)
+    r = fp8.row_sampled_fp8(rows, uo, Zs, Wo, full["dYo"])
+    errs = {"dX": rel_err(host(dX)[rows], c["dX"]), "Yo": rel_err(host(Yo)[rows], r["Y"])}
+    for i in range(T):
+        errs[f"Yq{i}"] = rel_err(host(Yq[i])[rows], c["pre"][i])
+        errs[f"dWq{i}"] = rel_err(host(dWq[i])[us[i]], c["dW"][i])
+        errs[f"dZ{i}"] = rel_err(host(dZ[i])[rows], r["dX"][i])
+        errs[f"dWo{i}"] = rel_err(host(dWo[i])[:, uo[i]], r["dW"][i])
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad

@@ -248,3 +248,39 @@ def test_tail_split_weight_gradient_accumulation(tp):
         assert rel_err(host(once[i]), ref["dW1"][i]) <= 1e-2
         assert rel_err(host(once[T + i]), ref["dW2"][i]) <= 1e-2
     tp.set_max_gemm_pairs(0)
+
+
+@pytest.mark.parametrize("sp", [False, True])
+def test_alternate_k_order_matches_oracle_and_forward_order(tp, sp):
+    """The pair GEMMs walk K backwards in every other persistent round
+    (tp_set_k_order): with the grid cut to 7 pairs the row forward, column
+    dgrad and both weight gradients run several rounds, so odd rounds take
+    the reversed order.  Against the oracle, against the forward-only order
+    (fp32 reassociation: 1e-5 for fp32 outputs, one bf16 step for bf16
+    ones), and run to run bit for bit; under sequence parallelism the
+    weight gradients' token-shard cursor walks backwards across shards."""
+    M, H, F, T = 1024, 512, 2048, 4
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=not sp,
+                   seq_parallel=sp)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    outs = []
+    try:
+        for alternate in (True, False, True):
+            tp.set_k_order(alternate)
+            run, _ = _step(tp, lay, t, False, 7)
+            outs.append(_outputs(run))
+    finally:
+        tp.set_k_order(True)
+    a, b, c = outs
+    far = [k for k in a if not _close(a[k], b[k], k)]
+    assert not far, far
+    for k in a:
+        assert np.array_equal(a[k], c[k]), k
+    assert any(not np.array_equal(a[k], b[k]) for k in a)  # the reversed rounds did run
+    ref = oracle_full(lay, t)
+    errs = {"Y": rel_err(a["Y"], ref["Y"]), "dX": rel_err(a["dX"], ref["dX"])}
+    for i in range(T):
+        errs[f"dW1_{i}"] = rel_err(a[f"dW1_{i}"], ref["dW1"][i])
+        errs[f"dW2_{i}"] = rel_err(a[f"dW2_{i}"], ref["dW2"][i])
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad

@@ -245,3 +245,26 @@ def test_fp8_layers_compose_to_the_fp8_mlp():
     assert np.array_equal(dX + dY, g["dX"])
     for i in range(T):
         assert np.array_equal(dW1[i], g["dW1"][i]) and np.array_equal(db1[i], g["db1"][i])
+
+
+def test_sampled_fp8_layers_agree_with_full():
+    """The sampled FP8 layer evaluators give the full functions' values at
+    the sampled rows and units."""
+    _, r, M, H, F, T = _layer_inputs(8, M=40, H=32, F=64, T=2)
+    Fs = F // T
+    X, W, dO = r(M, H), [r(Fs, H, sc=0.1) for _ in range(T)], [r(M, Fs) for _ in range(T)]
+    rows, units = [0, 7, 39], [[0, 5, Fs - 1], [3, Fs - 1]]
+    s = fp8.column_sampled_fp8(rows, units, X, W, dO)
+    pre, _ = fp8.column_fwd_fp8(X, W, None, "none")
+    dX, dW, _ = fp8.column_bwd_fp8(dO, X, W)
+    assert np.allclose(s["dX"], dX[rows], rtol=1e-12, atol=1e-12)
+    for i in range(T):
+        assert np.array_equal(s["pre"][i], pre[i][rows])
+        assert np.allclose(s["dW"][i], dW[i][units[i]], rtol=1e-12, atol=1e-12)
+    Xs, W2, dY = [r(M, Fs) for _ in range(T)], [r(H, Fs, sc=0.1) for _ in range(T)], r(M, H)
+    s = fp8.row_sampled_fp8(rows, units, Xs, W2, dY)
+    assert np.allclose(s["Y"], fp8.row_fwd_fp8(Xs, W2)[rows], rtol=1e-12, atol=1e-12)
+    rdX, rdW, _ = fp8.row_bwd_fp8(dY, Xs, W2)
+    for i in range(T):
+        assert np.allclose(s["dX"][i], rdX[i][rows], rtol=1e-12, atol=1e-12)
+        assert np.allclose(s["dW"][i], rdW[i][:, units[i]], rtol=1e-12, atol=1e-12)
