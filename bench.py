@@ -383,6 +383,7 @@ def run_gpu(args, w, dist, rank, local, ws):
     tp.set_fused_fwd(args.fused)
     tp.set_tail_split(args.tail_split == "on")
     tp.set_k_order(args.k_order == "alternate")
+    tp.set_band_rows(args.band_rows)
     dev = torch.device("cuda", local)
     layer = args.block == "layer"
     # all work on one non-default stream (a CUDA graph cannot capture the legacy stream)
@@ -422,7 +423,6 @@ def run_gpu(args, w, dist, rank, local, ws):
     clocks.start()
     tp.prof_enable(True)
     tp.prof_collect()  # drop warm-up records
-    tp.prof_clock()
     n0 = tp.launch_count()
     barrier(dist, local)
     torch.cuda.synchronize()
@@ -435,11 +435,12 @@ def run_gpu(args, w, dist, rank, local, ws):
     barrier(dist, local)
     ms = e0.elapsed_time(e1)
     launches = tp.launch_count() - n0 if not args.graph else graph_launches * args.steps
-    kernels = tp.prof_collect()
-    cyc, ns = tp.prof_clock()
+    kclk = tp.prof_collect(clocks=True)
+    kernels = {k: v[:2] for k, v in kclk.items()}
     tp.prof_enable(False)
     clk = clocks.stop()
     # the SM clock the GEMMs ran at (clock64 against %globaltimer in every CTA)
+    cyc, ns = sum(v[2] for v in kclk.values()), sum(v[3] for v in kclk.values())
     clk["kernel_mhz"] = round(cyc / ns * 1e3, 1) if ns else None
     st = status()
     if st != 0:
@@ -521,6 +522,8 @@ def run_gpu(args, w, dist, rank, local, ws):
         ent = {"launches": n, "avg_ms": round(avg, 4), "share": None}
         if name in kf and avg > 0:
             ent["tflops"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+        if kclk[name][3]:
+            ent["sm_mhz"] = round(kclk[name][2] / kclk[name][3] * 1e3, 1)
         if name in kb and avg > 0:
             gbs = kb[name] / (avg * 1e-3) / 1e9
             ent["gbs"] = round(gbs, 1)
@@ -550,7 +553,7 @@ def run_gpu(args, w, dist, rank, local, ws):
                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                         "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
     if roofline is not None and w.dtype == "bf16" and not layer and roofline["bound"] == "tensor" \
-            and not args.seq_len:
+            and not args.seq_len and not args.ffn:
         roofline["traffic"] = recorded_traffic(w, args.tile_mode, dom)
     step_frac = value / ws / peak_t
     return {
@@ -712,6 +715,9 @@ def main():
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's sequence length S (a smaller case of the same kernels, for "
                          "profiling); the printed config names the changed workload")
+    ap.add_argument("--ffn", type=int, default=0,
+                    help="override the workload's FFN width F (a smaller case of the same kernels with the same K "
+                         "of the weight gradients, for profiling); the printed config names the changed workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", default="workload", choices=["workload", "fp8"],
                     help="fp8: the FP8 variant (E4M3 forward, E5M2 backward, bf16 buffers) of the workload")
@@ -731,6 +737,8 @@ def main():
     ap.add_argument("--k-order", default="alternate", choices=["alternate", "forward"],
                     help="K order of the pair GEMMs' whole tiles: every other persistent round backwards "
                          "(alternate, fewer operand re-reads from HBM) or always forwards")
+    ap.add_argument("--band-rows", type=int, default=0,
+                    help="rows of 256-row tiles per raster band of the pair GEMMs' tile order (0: library choice)")
     ap.add_argument("--tail-split", default="on", choices=["on", "off"],
                     help="cut the persistent GEMMs' part-filled last round of tiles along K over all CTA pairs")
     args = ap.parse_args()
@@ -742,6 +750,8 @@ def main():
         w = dataclasses.replace(w, dtype="fp8")
     if args.seq_len > 0:
         w = dataclasses.replace(w, S=args.seq_len)
+    if args.ffn > 0:
+        w = dataclasses.replace(w, F=args.ffn)
     if w.kind == "attn_proj" and (w.dtype not in ("bf16", "fp8") or args.block != "mlp"):
         raise SystemExit("the attention projections are timed in bf16 or FP8 as plain layers")
     if w.kind == "attn_proj" and args.fp8_history:
@@ -760,7 +770,7 @@ def main():
               "l2": f"inputs larger than L2 (~{step_bytes(w) / 1e9:.1f} GB of operands, activations and "
                     f"gradients per step)",
               "tile_mode": args.tile_mode, "fused_fwd": args.fused, "tail_split": args.tail_split,
-              "k_order": args.k_order,
+              "k_order": args.k_order, "band_rows": args.band_rows or "library choice",
               "wgrad_accumulate": args.wgrad_accumulate,
               "launch": "CUDA graph replay per step" if args.graph else "eager C-ABI calls per step"}
     if w.dtype == "fp8":

@@ -498,6 +498,15 @@ TP_API tp_status tp_set_tail_split(int on);
  * every tile forwards.  TP_ERR_ARG unless alternate is 0 or 1. */
 TP_API tp_status tp_set_k_order(int alternate);
 
+/* Tile order of the pair-tile GEMMs, for all launches made after the call:
+ * output tiles are taken in bands of `rows` rows of 256-row tiles, the row
+ * fastest within a band and the columns of all problems side by side.  A
+ * band's operand panels are what a round of the persistent grid shares in
+ * L2, so the band height trades re-reads of the A panels (one per band)
+ * against re-reads of the B panels (once per band).  0 (the default) picks
+ * the library's choice.  TP_ERR_ARG for rows outside 0..4096. */
+TP_API tp_status tp_set_band_rows(int rows);
+
 /* Upper bound on the CTA pairs of the persistent pair-tile GEMMs, for all
  * launches made after the call (0, the default: as many as fit on the
  * device).  Leaves SMs free for concurrent work and sets the round structure
@@ -530,25 +539,25 @@ TP_API uint64_t tp_launch_count(void);
 TP_API uint64_t tp_tail_split_count(void);
 
 /* Per-kernel timing ("timers"): when enabled, every launch is bracketed by
- * CUDA events recorded on its own stream.  tp_prof_collect synchronises the
- * recorded events and returns, per kernel name, launches and total device
- * milliseconds; it then clears the records.  Returns the number of entries
+ * CUDA events recorded on its own stream, and the GEMM kernels count their
+ * CTAs' SM cycles and nanoseconds.  tp_prof_collect synchronises the
+ * recorded events (and, when there are clock counts, the device) and
+ * returns, per kernel name, launches, total device milliseconds and the
+ * clock counts; it then clears the records.  Returns the number of entries
  * written (<= max_entries) or -1 on error. */
 typedef struct {
     char name[48];
     int launches;
     double total_ms;
+    /* GEMM kernels: SM cycles (clock64) and nanoseconds (%globaltimer)
+     * between the start and the end of every CTA, summed over the CTAs of
+     * the recorded launches: sm_cycles / sm_ns * 1000 is the SM clock in
+     * MHz they ran at; 0 for kernels without the counter. */
+    uint64_t sm_cycles;
+    uint64_t sm_ns;
 } tp_prof_entry;
 TP_API void tp_prof_enable(int on);
 TP_API int tp_prof_collect(tp_prof_entry *entries, int max_entries);
-
-/* SM clock of the GEMM kernels launched while the per-kernel timer was on:
- * one thread of every CTA reads the SM cycle counter (clock64) and the
- * wall-clock timer (%globaltimer, ns) when the CTA starts and ends, and the
- * differences are summed over all CTAs.  cycles / ns * 1000 is the average
- * SM clock in MHz under that load.  Synchronises the device, then returns
- * the two sums and clears them.  TP_ERR_ARG for NULL outputs. */
-TP_API tp_status tp_prof_clock(uint64_t *cycles, uint64_t *ns);
 
 TP_API const char *tp_status_str(tp_status s);
 TP_API const char *tp_last_error(void);

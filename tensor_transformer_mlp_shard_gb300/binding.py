@@ -42,7 +42,8 @@ class LayerDesc(ctypes.Structure):
 
 
 class ProfEntry(ctypes.Structure):
-    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double),
+                ("sm_cycles", ctypes.c_uint64), ("sm_ns", ctypes.c_uint64)]
 
 
 _lib = None
@@ -84,7 +85,6 @@ SIGNATURES = {
     "tp_mlp_sync_status": (ctypes.c_int, [VP, VP]),
     "tp_layer_sync_status": (ctypes.c_int, [VP, VP]),
     "tp_mlp_debug_wait_timeout": (ctypes.c_int, [VP, ctypes.c_uint64, VP]),
-    "tp_prof_clock": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "tp_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "tp_debug_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, VP]),
     "tp_launch_count": (ctypes.c_uint64, []),
@@ -92,6 +92,7 @@ SIGNATURES = {
     "tp_set_tail_split": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_max_gemm_pairs": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_k_order": (ctypes.c_int, [ctypes.c_int]),
+    "tp_set_band_rows": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_fused_fwd": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
@@ -553,6 +554,12 @@ def set_k_order(alternate: bool):
     _check(lib().tp_set_k_order(1 if alternate else 0))
 
 
+def set_band_rows(rows: int):
+    """Rows of 256-row tiles per raster band of the pair GEMMs' tile order
+    (0: the library's choice)."""
+    _check(lib().tp_set_band_rows(int(rows)))
+
+
 def set_max_gemm_pairs(n: int):
     """Upper bound on the CTA pairs of the pair-tile GEMMs (0: all that fit)."""
     _check(lib().tp_set_max_gemm_pairs(int(n)))
@@ -581,22 +588,18 @@ def prof_enable(on: bool = True):
     lib().tp_prof_enable(1 if on else 0)
 
 
-def prof_collect():
-    """{kernel name: (launches, total device ms)} since the last collect."""
+def prof_collect(clocks: bool = False):
+    """{kernel name: (launches, total device ms)} since the last collect;
+    with clocks=True {name: (launches, total ms, SM cycles, SM ns)}, the last
+    two summed over the CTAs of GEMM launches (0 for other kernels)."""
     buf = (ProfEntry * 64)()
     n = lib().tp_prof_collect(buf, 64)
     if n < 0:
         raise TpError(4, lib().tp_last_error().decode(errors="replace"))
+    if clocks:
+        return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms, buf[i].sm_cycles, buf[i].sm_ns)
+                for i in range(n)}
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n)}
-
-
-def prof_clock():
-    """(SM cycles, ns) summed over the CTAs of the GEMM launches made while the
-    per-kernel timer was on, then cleared: cycles / ns * 1e3 is their SM clock
-    in MHz."""
-    c, t = ctypes.c_uint64(0), ctypes.c_uint64(0)
-    _check(lib().tp_prof_clock(ctypes.byref(c), ctypes.byref(t)))
-    return int(c.value), int(t.value)
 
 
 def status_str(s: int) -> str:

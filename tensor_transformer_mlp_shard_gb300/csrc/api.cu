@@ -111,6 +111,22 @@ bool prof_enabled() {
     return g_prof_on;
 }
 
+// clock counter slot per kernel name (the last slot is shared by any names
+// beyond the first kClockSlots - 1)
+static std::vector<std::string> g_clock_names;
+
+int prof_clock_slot(const char *kernel) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof_on) return -1;
+    for (size_t i = 0; i < g_clock_names.size(); ++i)
+        if (g_clock_names[i] == kernel) return static_cast<int>(i);
+    if (static_cast<int>(g_clock_names.size()) < kClockSlots - 1) {
+        g_clock_names.push_back(kernel);
+        return static_cast<int>(g_clock_names.size()) - 1;
+    }
+    return kClockSlots - 1;
+}
+
 static cudaEvent_t get_event() {
     if (!g_event_pool.empty()) {
         cudaEvent_t e = g_event_pool.back();
@@ -1889,14 +1905,6 @@ tp_status tp_mlp_debug_wait_timeout(tp_mlp *h, uint64_t limit_ns, void *stream) 
     return launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
 }
 
-tp_status tp_prof_clock(uint64_t *cycles, uint64_t *ns) {
-    if (!cycles || !ns) return set_error(TP_ERR_ARG, "cycles or ns is NULL");
-    unsigned long long c = 0, t = 0;
-    TRY(read_and_clear_clock(&c, &t));
-    *cycles = c;
-    *ns = t;
-    return TP_OK;
-}
 
 void tp_set_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns ? ns : 1); }
 
@@ -1971,6 +1979,12 @@ tp_status tp_set_tail_split(int on) {
     return TP_OK;
 }
 
+tp_status tp_set_band_rows(int rows) {
+    if (rows < 0 || rows > 4096) return set_error(TP_ERR_ARG, "band rows %d outside 0..4096", rows);
+    set_band_rows(rows);
+    return TP_OK;
+}
+
 tp_status tp_set_k_order(int alternate) {
     if (alternate != 0 && alternate != 1)
         return set_error(TP_ERR_ARG, "K-order flag must be 0 or 1, got %d", alternate);
@@ -1991,9 +2005,11 @@ void tp_prof_enable(int on) {
 
 int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
     std::vector<ProfRec> recs;
+    std::vector<std::string> clock_names;
     {
         std::lock_guard<std::mutex> lock(g_prof_mu);
         recs.swap(g_prof_recs);
+        clock_names = g_clock_names;
     }
     std::map<std::string, std::pair<int, double>> agg;
     std::vector<std::string> order;
@@ -2017,6 +2033,10 @@ int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
         set_error(TP_ERR_CUDA, "event timing failed");
         return -1;
     }
+    // the kernels' clock counters (only kernels launched with the timer on
+    // have a slot; reading them also clears them)
+    unsigned long long clk[2 * kClockSlots] = {};
+    if (!clock_names.empty() && read_and_clear_clocks(clk) != TP_OK) return -1;
     int n = 0;
     for (auto &name : order) {
         if (!entries || n >= max_entries) break;
@@ -2025,6 +2045,11 @@ int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
         snprintf(e.name, sizeof(e.name), "%s", name.c_str());
         e.launches = agg[name].first;
         e.total_ms = agg[name].second;
+        for (size_t s = 0; s < clock_names.size(); ++s)
+            if (clock_names[s] == name) {
+                e.sm_cycles = clk[2 * s];
+                e.sm_ns = clk[2 * s + 1];
+            }
     }
     return n;
 }

@@ -157,6 +157,8 @@ void set_tail_split(bool on);
 // K order of the pair GEMMs' whole tiles: every other persistent round walks
 // K backwards (default) or every round forwards
 void set_k_reverse(bool on);
+// rows of pair tiles per raster band of the pair GEMMs' tile order (0: default)
+void set_band_rows(int g);
 void set_max_gemm_pairs(int n);
 uint64_t tail_split_launches();  // pair GEMM launches that split their tail
 // Scratch bytes a pair GEMM of this shape (out M x N per problem, P problems,
@@ -244,12 +246,15 @@ size_t linear_row_bias_bytes(const tp_mlp_desc *desc);
 // StatusScope naming its slot, and every launch made on that thread in the
 // meantime reports to that slot.
 constexpr int kStatusSlots = 1024;
+constexpr int kClockSlots = 32;  // kernel names with clock counters of their own
 struct DeviceWords {
     int *status = nullptr;
     unsigned *abort_word = nullptr;
-    unsigned long long *clk = nullptr;  // kernel clock counters (per-kernel timer on), or null
+    unsigned long long *clk = nullptr;  // the kernel's clock counters (per-kernel timer on), or null
 };
-tp_status device_words(DeviceWords *w);  // words of the calling thread's current slot
+// words of the calling thread's current slot, and, with the per-kernel timer
+// on and a kernel name given, that kernel's clock counters
+tp_status device_words(DeviceWords *w, const char *kernel = nullptr);
 int alloc_status_slot();                  // 1..kStatusSlots-1, or -1 when all are taken
 void free_status_slot(int slot);
 class StatusScope {
@@ -263,7 +268,9 @@ class StatusScope {
     int prev_;
 };
 tp_status read_and_clear_status(cudaStream_t st, int slot, int *out);
-tp_status read_and_clear_clock(unsigned long long *cycles, unsigned long long *ns);
+// all kernels' clock counters (2 * kClockSlots values: cycles, ns per slot), then zeroed
+tp_status read_and_clear_clocks(unsigned long long *v);
+int prof_clock_slot(const char *kernel);  // clock slot of a kernel name, -1 with the timer off
 tp_status launch_wait_timeout(unsigned long long limit_ns, cudaStream_t st);
 bool prof_enabled();
 uint64_t wait_limit_ns();

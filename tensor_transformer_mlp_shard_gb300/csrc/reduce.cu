@@ -29,9 +29,9 @@ __device__ unsigned g_tp_abort[kStatusSlots];
 __device__ unsigned g_tp_never_set = 0;
 // SM cycles and wall-clock nanoseconds summed over the CTAs of the GEMM
 // launches made while the per-kernel timer is on (clock64 and %globaltimer
-// read by one thread at the start and end of each CTA): their ratio is the
-// SM clock those kernels actually ran at.
-__device__ unsigned long long g_tp_clk[2];
+// read by one thread at the start and end of each CTA), one pair per kernel
+// name: their ratio is the SM clock those kernels actually ran at.
+__device__ unsigned long long g_tp_clk[2 * kClockSlots];
 
 static std::mutex g_slot_mu;
 static bool g_slot_used[kStatusSlots] = {true};  // slot 0 is never handed out
@@ -56,7 +56,7 @@ void free_status_slot(int slot) {
 StatusScope::StatusScope(int slot) : prev_(g_cur_slot) { g_cur_slot = slot; }
 StatusScope::~StatusScope() { g_cur_slot = prev_; }
 
-tp_status device_words(DeviceWords *w) {
+tp_status device_words(DeviceWords *w, const char *kernel) {
     static int *st_base[64] = {};
     static unsigned *ab_base[64] = {};
     static unsigned long long *clk_base[64] = {};
@@ -80,7 +80,8 @@ tp_status device_words(DeviceWords *w) {
     }
     w->status = st_base[dev] + g_cur_slot;
     w->abort_word = ab_base[dev] + g_cur_slot;
-    w->clk = prof_enabled() ? clk_base[dev] : nullptr;
+    const int slot = kernel ? prof_clock_slot(kernel) : -1;
+    w->clk = slot >= 0 ? clk_base[dev] + 2 * slot : nullptr;
     return TP_OK;
 }
 
@@ -99,17 +100,14 @@ tp_status read_and_clear_status(cudaStream_t st, int slot, int *out) {
     return TP_OK;
 }
 
-tp_status read_and_clear_clock(unsigned long long *cycles, unsigned long long *ns) {
+tp_status read_and_clear_clocks(unsigned long long *v) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_check(e, "cudaDeviceSynchronize");
-    unsigned long long v[2] = {0, 0};
-    e = cudaMemcpyFromSymbol(v, g_tp_clk, sizeof(v));
+    e = cudaMemcpyFromSymbol(v, g_tp_clk, sizeof(unsigned long long) * 2 * kClockSlots);
     if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyFromSymbol(clock)");
-    const unsigned long long zero[2] = {0, 0};
+    static const unsigned long long zero[2 * kClockSlots] = {};
     e = cudaMemcpyToSymbol(g_tp_clk, zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_check(e, "cudaMemcpyToSymbol(clock)");
-    *cycles = v[0];
-    *ns = v[1];
     return TP_OK;
 }
 

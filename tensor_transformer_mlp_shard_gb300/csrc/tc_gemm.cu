@@ -139,6 +139,7 @@ static void copy_out(Out &o, const OutPlan &src) {
 static std::atomic<int> g_tile_mode{0};
 static std::atomic<bool> g_tail_split{true};
 static std::atomic<bool> g_k_reverse{true};
+static std::atomic<int> g_band_rows{0};
 static std::atomic<int> g_max_pairs{0};
 static std::atomic<uint64_t> g_tail_launches{0};
 
@@ -183,6 +184,7 @@ static int pair_limit(int fit) {
 void set_tile_mode(int mode) { tc::g_tile_mode.store(mode); }
 void set_tail_split(bool on) { tc::g_tail_split.store(on); }
 void set_k_reverse(bool on) { tc::g_k_reverse.store(on); }
+void set_band_rows(int g) { tc::g_band_rows.store(g > 0 ? g : 0); }
 void set_max_gemm_pairs(int n) { tc::g_max_pairs.store(n > 0 ? n : 0); }
 uint64_t tail_split_launches() { return tc::g_tail_launches.load(); }
 
@@ -269,7 +271,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.total_tiles = prm.tiles_per_split * ksplit;
     prm.total_work = prm.total_tiles;
     prm.tail_first = prm.total_tiles;
-    prm.group_m = use_pair ? 8 : 16;
+    // bands of 16 pair-tile rows: measured on GB300 against 2, 4, 8, 32 and
+    // 64 (GPT, SwiGLU and sequence-parallel workloads), the fastest or
+    // within 0.5% of it for every GEMM, with the least DRAM traffic overall
+    prm.group_m = use_pair ? (g_band_rows.load() > 0 ? g_band_rows.load() : 16) : 16;
     // alternate-round K order for the GEMMs whose operands are re-read most
     // (row forward, column dgrad, weight gradients); the column forward and
     // the act' dgrad keep one order (their results are compared bit for bit
@@ -343,7 +348,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.fmax_a = g.fmt_a == FP8_E5M2 ? 57344.0f : 448.0f;
     prm.fmax_b = g.fmt_b == FP8_E5M2 ? 57344.0f : 448.0f;
     DeviceWords w;
-    tp_status s = device_words(&w);
+    tp_status s = device_words(&w, g.name);
     if (s != TP_OK) return s;
     prm.status = w.status;
     prm.abort_word = w.abort_word;
