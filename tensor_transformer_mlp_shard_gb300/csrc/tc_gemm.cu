@@ -219,6 +219,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     const int mode = g_tile_mode.load();
     const bool use_pair = mode == TP_TILE_PAIR || (mode == TP_TILE_AUTO && g.M > BM);
     const bool fp8 = g.fp8;
+    // the pair kernels take an MN-major operand's K rows as the row itself
+    // except in the token-sharded instance (index 5)
+    if (use_pair && ki != 5 && ((g.A.mn_major && g.A.rows_split) || (g.B.mn_major && g.B.rows_split)))
+        return set_error(TP_ERR_UNSUPPORTED, "token-sharded MN-major operand outside the token-sharded GEMM instance");
     KernelFn fn = kernel_at(ki, use_pair, fp8);
     const int bke = fp8 ? Elem<true>::BKE : Elem<false>::BKE;  // K elements per stage
     const int mnb = fp8 ? Elem<true>::MNB : Elem<false>::MNB;  // MN elements per MN-major box

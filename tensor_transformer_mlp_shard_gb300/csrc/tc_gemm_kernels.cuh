@@ -1461,11 +1461,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs) ----------------
+            // One thread issues both operands' loads of every stage.  In the
+            // weight gradients (both operands MN-major) its instruction path
+            // per K step is what the MMAs wait on, so everything that does not
+            // change within a K segment is computed once per segment.
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_par = 0;
             bool ok = true;
             int it = 0;
+            const uint32_t full0_c = map_to_cta(full0, 0);  // CTA 0's full barriers, cluster window
             for (int w = pair_id; ok && w < p.total_work; w += npairs, ++it) {
                 const Work wk = work_item(p, w);
                 int pi, mt, nt;
@@ -1476,104 +1481,108 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 const int n0 = p.b_dual_off ? nt * (BN / 2) + (rank ? p.b_dual_off : 0) : nt * BN + 128 * rank;
                 // odd rounds walk a whole tile's K steps from the last one down
                 const bool rev = p.k_reverse && wk.j < 0 && (it & 1);
+                const int dkb = rev ? -1 : 1;
                 const int f_first = rev ? wk.f1 - 1 : wk.f0;
                 int s = f_first / p.num_kb, kb = f_first - s * p.num_kb;
-                // K-major operands select their map and row by the tile row,
-                // once per K segment (under sequence parallelism a division
-                // per K step here cost the SP GEMMs 6-9%); MN-major ones
-                // select by the K block, every step
-                int ia = 0, ra = 0, ib = 0, rb = 0;
-                if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
-                if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
+                // Maps and rows for the current K segment.  K-major operands
+                // select by the tile row (under sequence parallelism a division
+                // per K step cost the SP GEMMs 6-9%).  MN-major operands outside
+                // the token-sharded instance are never split into token shards:
+                // their map depends on the problem and the segment only and
+                // their row is the K offset; in that instance a cursor follows
+                // the token shards along the K loop.
+                const CUtensorMap *ma = nullptr, *mb = nullptr;
+                int ra = 0, rb = 0;
+                auto segment_maps = [&]() {
+                    int idx = 0;
+                    if (!A_MN) {
+                        select(p.selA, pi, s, m0, idx, ra);
+                        ma = &p.mapA[idx];
+                    } else if (!TS) {
+                        ma = &p.mapA[pi * p.selA.p_stride + s * p.selA.s_stride];
+                    }
+                    if (!B_MN) {
+                        select(p.selB, pi, s, n0, idx, rb);
+                        mb = &p.mapB[idx];
+                    } else if (!TS) {
+                        mb = &p.mapB[pi * p.selB.p_stride + s * p.selB.s_stride];
+                    }
+                };
+                segment_maps();
                 SelCursor ca, cb;
                 if constexpr (TS) {
                     if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
                     if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
                 }
-                {
-                    for (int f = wk.f0; f < wk.f1; ++f) {
-                        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
-                            ok = false;
-                            break;
+                const int a_grp = m0 / 64, b_grp = n0 / 64;  // 3D boxes: 64-wide group of the MN origin
+                for (int f = wk.f0; f < wk.f1; ++f) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0_c + 8 * stage;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(full0 + 8 * stage, 2 * P_STAGE_BYTES);
+                        armed |= 1u << stage;
+                        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    }
+                    const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
+                    const uint32_t sb = sa + P_A_BYTES;
+                    const int k0 = kb * E::BKE;
+                    if (!A_MN) {
+                        tma_load_2d_pair(sa, ma, fb, k0, ra);
+                    } else {
+                        const CUtensorMap *m = ma;
+                        int lrow = k0;
+                        if constexpr (TS) {
+                            m = &p.mapA[ca.idx];
+                            lrow = ca.lrow;
                         }
-                        const uint32_t fb_local = full0 + 8 * stage;
-                        const uint32_t fb = map_to_cta(fb_local, 0);
-                        if (rank == 0) {
-                            mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
-                            armed |= 1u << stage;
-                            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-                        }
-                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                        const uint32_t sb = sa + P_A_BYTES;
-                        const int k0 = kb * E::BKE;
-                        if (!A_MN) {
-                            tma_load_2d_pair(sa, &p.mapA[ia], fb, k0, ra);
+                        if (!F8 && p.a3d) {
+                            tma_load_3d_pair(sa, m, fb, 0, lrow, a_grp);
                         } else {
-                            int idx, lrow;
-                            if constexpr (TS) {
-                                idx = ca.idx;
-                                lrow = ca.lrow;
-                            } else {
-                                select(p.selA, pi, s, k0, idx, lrow);
-                            }
-                            if (!F8 && p.a3d) {
-                                tma_load_3d_pair(sa, &p.mapA[idx], fb, 0, lrow, m0 / 64);
-                            } else {
 #pragma unroll
-                                for (int j = 0; j < 128 / E::MNB; ++j)
-                                    tma_load_2d_pair(sa + j * E::MNB_BYTES, &p.mapA[idx], fb, m0 + j * E::MNB, lrow);
-                            }
+                            for (int j = 0; j < 128 / E::MNB; ++j)
+                                tma_load_2d_pair(sa + j * E::MNB_BYTES, m, fb, m0 + j * E::MNB, lrow);
                         }
-                        if (!B_MN) {
-                            tma_load_2d_pair(sb, &p.mapB[ib], fb, k0, rb);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d_pair(sb, mb, fb, k0, rb);
+                    } else {
+                        const CUtensorMap *m = mb;
+                        int lrow = k0;
+                        if constexpr (TS) {
+                            m = &p.mapB[cb.idx];
+                            lrow = cb.lrow;
+                        }
+                        if (!F8 && p.b3d) {
+                            tma_load_3d_pair(sb, m, fb, 0, lrow, b_grp);
                         } else {
-                            int idx, lrow;
-                            if constexpr (TS) {
-                                idx = cb.idx;
-                                lrow = cb.lrow;
-                            } else {
-                                select(p.selB, pi, s, k0, idx, lrow);
-                            }
-                            if (!F8 && p.b3d) {
-                                tma_load_3d_pair(sb, &p.mapB[idx], fb, 0, lrow, n0 / 64);
-                            } else {
 #pragma unroll
-                                for (int j = 0; j < 128 / E::MNB; ++j)
-                                    tma_load_2d_pair(sb + j * E::MNB_BYTES, &p.mapB[idx], fb, n0 + j * E::MNB, lrow);
+                            for (int j = 0; j < 128 / E::MNB; ++j)
+                                tma_load_2d_pair(sb + j * E::MNB_BYTES, m, fb, n0 + j * E::MNB, lrow);
+                        }
+                    }
+                    if (++stage == NST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    kb += dkb;
+                    if (kb == p.num_kb || kb < 0) {  // next (or, walking backwards, previous) K segment
+                        s += dkb;
+                        kb = rev ? p.num_kb - 1 : 0;
+                        if (s >= 0 && s < p.S) {
+                            segment_maps();
+                            if constexpr (TS) {
+                                if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
+                                if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
                             }
                         }
-                        if (++stage == NST) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    } else if constexpr (TS) {
                         if (rev) {
-                            if (kb == 0) {
-                                kb = p.num_kb - 1;
-                                if (--s >= 0) {
-                                    if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
-                                    if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
-                                    if constexpr (TS) {
-                                        if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
-                                        if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
-                                    }
-                                }
-                            } else {
-                                --kb;
-                                if constexpr (TS) {
-                                    if (A_MN) ca.retreat(p.selA, E::BKE);
-                                    if (B_MN) cb.retreat(p.selB, E::BKE);
-                                }
-                            }
-                        } else if (++kb == p.num_kb) {
-                            kb = 0;
-                            ++s;
-                            if (!A_MN) select(p.selA, pi, s, m0, ia, ra);
-                            if (!B_MN) select(p.selB, pi, s, n0, ib, rb);
-                            if constexpr (TS) {
-                                if (A_MN) ca.init(p.selA, pi, s, 0);
-                                if (B_MN) cb.init(p.selB, pi, s, 0);
-                            }
-                        } else if constexpr (TS) {
+                            if (A_MN) ca.retreat(p.selA, E::BKE);
+                            if (B_MN) cb.retreat(p.selB, E::BKE);
+                        } else {
                             if (A_MN) ca.advance(p.selA, E::BKE);
                             if (B_MN) cb.advance(p.selB, E::BKE);
                         }
