@@ -98,14 +98,15 @@ tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int bo
 
 // MN-major bf16 operand [rows (K) x cols (MN)], cols % 64 == 0, as the 3D
 // tensor {64 elements, rows, cols / 64 groups} with strides {row pitch, 128
-// bytes}: a box {64, 64, 2} is the two [64 K rows x 128 bytes] swizzle atoms
-// of a 128-wide MN tile, one after the other (the CTA-pair kernel's a3d/b3d)
-static tp_status encode_map_mn3d(CUtensorMap *m, const void *ptr, int rows, int cols) {
+// bytes}: a box {64, box_rows, 2} is the two [box_rows K rows x 128 bytes]
+// swizzle atoms of a 128-wide MN tile, one after the other (the CTA-pair
+// kernel's a3d/b3d; box_rows = the K elements of one stage)
+static tp_status encode_map_mn3d(CUtensorMap *m, const void *ptr, int rows, int cols, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
-    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -224,7 +225,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     if (use_pair && ki != 5 && ((g.A.mn_major && g.A.rows_split) || (g.B.mn_major && g.B.rows_split)))
         return set_error(TP_ERR_UNSUPPORTED, "token-sharded MN-major operand outside the token-sharded GEMM instance");
     KernelFn fn = kernel_at(ki, use_pair, fp8);
-    const int bke = fp8 ? Elem<true>::BKE : Elem<false>::BKE;  // K elements per stage
+    // K elements per stage: one 128-byte row of each operand, two for the
+    // pair kernel's bf16 weight gradients (both operands MN-major, tc_gemm_pair_kernel's KB2)
+    const int kb2 = (use_pair && !fp8 && g.A.mn_major && g.B.mn_major) ? 2 : 1;
+    const int bke = (fp8 ? Elem<true>::BKE : Elem<false>::BKE) * kb2;
     const int mnb = fp8 ? Elem<true>::MNB : Elem<false>::MNB;  // MN elements per MN-major box
     const int tile_m = use_pair ? P_TILE_M : BM;
     // rows of the B tile that one CTA loads per box
@@ -236,13 +240,13 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     prm.a3d = use_pair && !fp8 && g.A.mn_major && g.A.cols % 64 == 0;
     prm.b3d = use_pair && !fp8 && g.B.mn_major && g.B.cols % 64 == 0 && !g.b_dual_off;
     for (int i = 0; i < g.A.n; ++i) {
-        tp_status s = prm.a3d        ? encode_map_mn3d(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols)
+        tp_status s = prm.a3d        ? encode_map_mn3d(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke)
                       : g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, mnb, bke, fp8)
                                      : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke, BM, fp8);
         if (s != TP_OK) return s;
     }
     for (int i = 0; i < g.B.n; ++i) {
-        tp_status s = prm.b3d        ? encode_map_mn3d(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols)
+        tp_status s = prm.b3d        ? encode_map_mn3d(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke)
                       : g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
                                      : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke, b_box_rows, fp8);
         if (s != TP_OK) return s;

@@ -1418,10 +1418,20 @@ template <int EPI, bool A_MN, bool B_MN, bool F8, bool TS = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ Params p) {
     ClockMark clk_mark;
     clk_mark.start(p.clk);
-    constexpr int NST = pair_stages<EPI>();
+    using E = Elem<F8>;
+    // K blocks per stage: two for the bf16 weight gradients (both operands
+    // MN-major), whose producer issues one 3D box of {64, 128 K rows, 2
+    // atoms} per operand and stage instead of one of 64 rows -- half the
+    // loads and barrier operations per K for the thread whose issue path
+    // limits these GEMMs -- in half as many stages of twice the size (the
+    // same shared memory)
+    constexpr int KB2 = (A_MN && B_MN && !F8) ? 2 : 1;
+    constexpr int NST = pair_stages<EPI>() / KB2;
+    constexpr int STG = P_STAGE_BYTES * KB2;  // bytes of one stage in this CTA
+    constexpr int BKS = E::BKE * KB2;         // K elements of one stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NST * P_STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NST * STG);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 5);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * NST;
@@ -1432,7 +1442,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    using E = Elem<F8>;
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
@@ -1511,8 +1520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 segment_maps();
                 SelCursor ca, cb;
                 if constexpr (TS) {
-                    if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
-                    if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
+                    if (A_MN) ca.init(p.selA, pi, s, kb * BKS);
+                    if (B_MN) cb.init(p.selB, pi, s, kb * BKS);
                 }
                 const int a_grp = m0 / 64, b_grp = n0 / 64;  // 3D boxes: 64-wide group of the MN origin
                 for (int f = wk.f0; f < wk.f1; ++f) {
@@ -1522,13 +1531,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                     }
                     const uint32_t fb = full0_c + 8 * stage;
                     if (rank == 0) {
-                        mbar_arrive_expect_tx(full0 + 8 * stage, 2 * P_STAGE_BYTES);
+                        mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STG);
                         armed |= 1u << stage;
                         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     }
-                    const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                    const uint32_t sb = sa + P_A_BYTES;
-                    const int k0 = kb * E::BKE;
+                    const uint32_t sa = smem_base + stage * STG;
+                    const uint32_t sb = sa + P_A_BYTES * KB2;
+                    const int k0 = kb * BKS;
                     if (!A_MN) {
                         tma_load_2d_pair(sa, ma, fb, k0, ra);
                     } else {
@@ -1543,7 +1552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         } else {
 #pragma unroll
                             for (int j = 0; j < 128 / E::MNB; ++j)
-                                tma_load_2d_pair(sa + j * E::MNB_BYTES, m, fb, m0 + j * E::MNB, lrow);
+                                tma_load_2d_pair(sa + j * E::MNB_BYTES * KB2, m, fb, m0 + j * E::MNB, lrow);
                         }
                     }
                     if (!B_MN) {
@@ -1560,7 +1569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         } else {
 #pragma unroll
                             for (int j = 0; j < 128 / E::MNB; ++j)
-                                tma_load_2d_pair(sb + j * E::MNB_BYTES, m, fb, n0 + j * E::MNB, lrow);
+                                tma_load_2d_pair(sb + j * E::MNB_BYTES * KB2, m, fb, n0 + j * E::MNB, lrow);
                         }
                     }
                     if (++stage == NST) {
@@ -1574,17 +1583,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         if (s >= 0 && s < p.S) {
                             segment_maps();
                             if constexpr (TS) {
-                                if (A_MN) ca.init(p.selA, pi, s, kb * E::BKE);
-                                if (B_MN) cb.init(p.selB, pi, s, kb * E::BKE);
+                                if (A_MN) ca.init(p.selA, pi, s, kb * BKS);
+                                if (B_MN) cb.init(p.selB, pi, s, kb * BKS);
                             }
                         }
                     } else if constexpr (TS) {
                         if (rev) {
-                            if (A_MN) ca.retreat(p.selA, E::BKE);
-                            if (B_MN) cb.retreat(p.selB, E::BKE);
+                            if (A_MN) ca.retreat(p.selA, BKS);
+                            if (B_MN) cb.retreat(p.selB, BKS);
                         } else {
-                            if (A_MN) ca.advance(p.selA, E::BKE);
-                            if (B_MN) cb.advance(p.selB, E::BKE);
+                            if (A_MN) ca.advance(p.selA, BKS);
+                            if (B_MN) cb.advance(p.selB, BKS);
                         }
                     }
                 }
@@ -1617,13 +1626,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                        const uint32_t sb = sa + P_A_BYTES;
+                        const uint32_t sa = smem_base + stage * STG;
+                        const uint32_t sb = sa + P_A_BYTES * KB2;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = A_MN ? smem_desc(sa + kk * E::KADV_MN, E::MNB_BYTES, 1024)
+                        for (int kk = 0; kk < 4 * KB2; ++kk) {
+                            const uint64_t ad = A_MN ? smem_desc(sa + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
                                                      : smem_desc(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? smem_desc(sb + kk * E::KADV_MN, E::MNB_BYTES, 1024)
+                            const uint64_t bd = B_MN ? smem_desc(sb + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
                                                      : smem_desc(sb + kk * 32, 16, 1024);
                             umma_op_pair<F8>(d, ad, bd, idesc, accumulate);
                             accumulate = 1;
@@ -1647,7 +1656,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         const float dq = dequant_factor(p);
-        Stager stg{smem_base + NST * P_STAGE_BYTES + BAR_BYTES + (warp - 2) * EPI_STAGE_BYTES, 0u};
+        Stager stg{smem_base + NST * STG + BAR_BYTES + (warp - 2) * EPI_STAGE_BYTES, 0u};
         const uint32_t tempty_leader = map_to_cta(tempty0, 0);
         int it = 0;
         for (int w = pair_id; w < p.total_work; w += npairs, ++it) {
