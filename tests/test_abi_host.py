@@ -244,3 +244,53 @@ def test_layer_null_pointers_rejected_before_launch(tp):
                           ctypes.c_void_p(0x100000), 16, None) == 1
     assert b"workspace" in L.tp_last_error()
     L.tp_layer_destroy(h)
+
+
+def test_handles_take_status_slots_until_exhausted(tp):
+    """Every MLP / sub-block handle owns one of 1023 device status words; the
+    1024th live handle is refused (TP_ERR_UNSUPPORTED) before any CUDA call,
+    and destroying a handle returns its word."""
+    L = tp.lib()
+    d = tp.make_desc(128, 2, 256, 1024, 2)
+    hs = []
+    try:
+        while True:
+            h = ctypes.c_void_p()
+            s = L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h))
+            if s != 0:
+                break
+            hs.append(h)
+            assert len(hs) <= 1023
+        assert s == 3 and 1000 <= len(hs) <= 1023  # other live handles of this process hold the rest
+        assert b"live handles" in L.tp_last_error()
+        L.tp_mlp_destroy(hs.pop())
+        h = ctypes.c_void_p()
+        assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+        hs.append(h)
+    finally:
+        for h in hs:
+            L.tp_mlp_destroy(h)
+    h = ctypes.c_void_p()
+    assert L.tp_mlp_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    L.tp_mlp_destroy(h)
+    assert L.tp_mlp_sync_status(None, None) == 1 and L.tp_layer_sync_status(None, None) == 1
+
+
+def test_fp8_single_layers_need_a_workspace_and_no_alloc_refuses_fp8(tp):
+    """The FP8 single-layer forward without a workspace is TP_ERR_ARG, and the
+    allocation-free row backward refuses FP8 (its backward reads the
+    forward's codes from the forward's workspace): both before any launch."""
+    L = tp.lib()
+    from tensor_transformer_mlp_shard_gb300.binding import _arr
+    d = tp.make_desc(128, 2, 256, 1024, 2, act="none", dtype="fp8")
+    p = [0x10000 * (i + 1) for i in range(2)]
+    assert L.tp_linear_col(ctypes.byref(d), _arr(p[:1]), _arr(p), None, _arr(p), None, None) == 1
+    assert L.tp_linear_row(ctypes.byref(d), _arr(p), _arr(p), None, None, _arr(p[:1]), None) == 1
+    assert L.tp_linear_row_bwd_noalloc(ctypes.byref(d), _arr(p[:1]), _arr(p), _arr(p), _arr(p), _arr(p), None,
+                                       None) == 3
+    need = L.tp_linear_workspace_bytes(ctypes.byref(d))
+    nb = tp.make_desc(128, 2, 256, 1024, 2, act="none", dtype="bf16")
+    assert need > L.tp_linear_workspace_bytes(ctypes.byref(nb))  # the FP8 region: amax slots and codes
+    # a workspace smaller than that is refused
+    assert L.tp_linear_col_ws(ctypes.byref(d), _arr(p[:1]), _arr(p), None, _arr(p), None,
+                              ctypes.c_void_p(0x100000), need - 256, None) == 1

@@ -372,3 +372,44 @@ def test_fp8_attention_projections_sampled(tp):
         errs[f"dWo{i}"] = rel_err(host(dWo[i])[:, uo[i]], r["dW"][i])
     bad = {k: v for k, v in errs.items() if not v <= 1e-2}
     assert not bad, bad
+
+
+def test_fp8_column_layer_swiglu_and_accumulated_weight_gradients(tp):
+    """The FP8 column forward with the SwiGLU epilogue (gate and up rows of a
+    shard in one tile) against the oracle, and the FP8 single-layer
+    backward with wgrad_accumulate: two calls from zero give exactly twice
+    one call's weight gradients (one fp32 add per element and call)."""
+    M, H, F, T = 300, 272, 832, 4
+    Fs = F // T
+    t = _layer_tensors(M, H, 2 * F, T, 3)  # W shards of 2 * F/T rows: gate rows, then up rows
+    Wg = t["W"]
+    col = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="swiglu", dtype="fp8")
+    ws = tp.alloc_workspace(tp.linear_workspace_bytes(col))
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    out = [torch.empty(M, Fs, **bf) for _ in range(T)]
+    pre = [torch.empty(M, 2 * Fs, **bf) for _ in range(T)]
+    tp.linear_col(col, [_dev(t["X"])], [_dev(w) for w in Wg], None, out, pre, workspace=ws)
+    assert tp.sync_status() == 0
+    rp, ro = fp8.column_fwd_fp8(t["X"], Wg, None, "swiglu")
+    for i in range(T):
+        assert rel_err(host(pre[i]), rp[i]) <= 1e-2
+        assert rel_err(host(out[i]), ro[i]) <= 1e-2
+    # accumulated weight gradients of the row layer
+    acc = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="fp8", wgrad_accumulate=True)
+    one = tp.Layout(S=M // 2, B=2, H=H, F=F, T=T, act="none", dtype="fp8")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    r = _layer_tensors(M, H, F, T, 4)
+    Xr, W2, dY = [_dev(x) for x in r["Xr"]], [_dev(w) for w in r["W2"]], [_dev(r["dY"])]
+    res = []
+    for lay, calls in ((one, 1), (acc, 2)):
+        w2 = tp.alloc_workspace(tp.linear_workspace_bytes(lay))
+        Y = [torch.empty(M, H, **bf)]
+        tp.linear_row(lay, Xr, W2, None, None, Y, workspace=w2)
+        dX = [torch.empty(M, Fs, **bf) for _ in range(T)]
+        dW = [torch.zeros(H, Fs, **f32) for _ in range(T)]
+        for _ in range(calls):
+            tp.linear_row_bwd(lay, dY, Xr, W2, dX, dW, None, workspace=w2)
+        assert tp.sync_status() == 0
+        res.append(dW)
+    for a, b in zip(*res):
+        assert torch.equal(2 * a, b)
