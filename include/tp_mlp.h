@@ -507,6 +507,16 @@ TP_API tp_status tp_set_k_order(int alternate);
  * the library's choice.  TP_ERR_ARG for rows outside 0..4096. */
 TP_API tp_status tp_set_band_rows(int rows);
 
+/* Programmatic dependent launch of the pair-tile GEMMs, for all launches
+ * made after the call.  With on = 1 (the default) each pair-tile GEMM is
+ * launched with programmatic stream serialization: its CTAs may start on
+ * SMs the previous kernel in the stream has left, set up their barriers and
+ * tensor memory there, and wait in griddepcontrol.wait until that kernel
+ * has completed and its writes are visible before they read an operand or
+ * write an output, so stream order and results are unchanged.  on = 0
+ * launches them in plain stream order.  TP_ERR_ARG unless on is 0 or 1. */
+TP_API tp_status tp_set_launch_overlap(int on);
+
 /* Upper bound on the CTA pairs of the persistent pair-tile GEMMs, for all
  * launches made after the call (0, the default: as many as fit on the
  * device).  Leaves SMs free for concurrent work and sets the round structure
@@ -558,6 +568,13 @@ typedef struct {
 } tp_prof_entry;
 TP_API void tp_prof_enable(int on);
 TP_API int tp_prof_collect(tp_prof_entry *entries, int max_entries);
+/* Restrict the timers' events to the launches of one kernel (its name as
+ * tp_prof_collect reports it); NULL or "" times every launch again.  The
+ * other launches then carry no events in their stream (each event pair
+ * costs the stream a few microseconds between kernels), while the GEMMs'
+ * clock counters keep counting: tp_prof_collect lists such kernels after the
+ * timed ones with launches = 0 and total_ms = 0.  The string is copied. */
+TP_API void tp_prof_select(const char *kernel);
 
 TP_API const char *tp_status_str(tp_status s);
 TP_API const char *tp_last_error(void);

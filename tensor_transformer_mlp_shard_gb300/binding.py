@@ -93,10 +93,12 @@ SIGNATURES = {
     "tp_set_max_gemm_pairs": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_k_order": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_band_rows": (ctypes.c_int, [ctypes.c_int]),
+    "tp_set_launch_overlap": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_tile_mode": (ctypes.c_int, [ctypes.c_int]),
     "tp_set_fused_fwd": (ctypes.c_int, [ctypes.c_int]),
     "tp_prof_enable": (None, [ctypes.c_int]),
     "tp_prof_collect": (ctypes.c_int, [ctypes.POINTER(ProfEntry), ctypes.c_int]),
+    "tp_prof_select": (None, [ctypes.c_char_p]),
 }
 
 
@@ -554,6 +556,13 @@ def set_k_order(alternate: bool):
     _check(lib().tp_set_k_order(1 if alternate else 0))
 
 
+def set_launch_overlap(on: bool):
+    """Programmatic dependent launch of the pair GEMMs (on by default): a
+    GEMM's CTAs set up while the previous kernel finishes and wait for it
+    before touching memory; False: plain stream order."""
+    _check(lib().tp_set_launch_overlap(1 if on else 0))
+
+
 def set_band_rows(rows: int):
     """Rows of 256-row tiles per raster band of the pair GEMMs' tile order
     (0: the library's choice)."""
@@ -586,6 +595,12 @@ def launch_count() -> int:
 
 def prof_enable(on: bool = True):
     lib().tp_prof_enable(1 if on else 0)
+
+
+def prof_select(kernel=None):
+    """Time only the launches of `kernel` with events (None: every launch);
+    the GEMMs' clock counters keep counting for all kernels."""
+    lib().tp_prof_select(kernel.encode() if kernel else None)
 
 
 def prof_collect(clocks: bool = False):

@@ -102,6 +102,7 @@ struct ProfRec {
 };
 static std::mutex g_prof_mu;
 static bool g_prof_on = false;
+static std::string g_prof_only;  // non-empty: only launches of this kernel get events
 static std::vector<ProfRec> g_prof_recs;
 static std::vector<cudaEvent_t> g_event_pool;
 static thread_local cudaEvent_t g_pending = nullptr;
@@ -139,11 +140,10 @@ static cudaEvent_t get_event() {
 }
 
 void launch_begin(const char *name, cudaStream_t st) {
-    (void)name;
     g_launches.fetch_add(1);
     std::lock_guard<std::mutex> lock(g_prof_mu);
     g_pending = nullptr;
-    if (!g_prof_on) return;
+    if (!g_prof_on || (!g_prof_only.empty() && g_prof_only != name)) return;
     cudaEvent_t e = get_event();
     if (e && cudaEventRecord(e, st) == cudaSuccess) g_pending = e;
 }
@@ -1992,6 +1992,12 @@ tp_status tp_set_k_order(int alternate) {
     return TP_OK;
 }
 
+tp_status tp_set_launch_overlap(int on) {
+    if (on != 0 && on != 1) return set_error(TP_ERR_ARG, "launch-overlap flag must be 0 or 1, got %d", on);
+    set_pdl(on != 0);
+    return TP_OK;
+}
+
 tp_status tp_set_max_gemm_pairs(int n) {
     if (n < 0) return set_error(TP_ERR_ARG, "pair limit must be >= 0, got %d", n);
     set_max_gemm_pairs(n);
@@ -2001,6 +2007,11 @@ tp_status tp_set_max_gemm_pairs(int n) {
 void tp_prof_enable(int on) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     g_prof_on = on != 0;
+}
+
+void tp_prof_select(const char *kernel) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_only = kernel ? kernel : "";
 }
 
 int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
@@ -2037,6 +2048,13 @@ int tp_prof_collect(tp_prof_entry *entries, int max_entries) {
     // have a slot; reading them also clears them)
     unsigned long long clk[2 * kClockSlots] = {};
     if (!clock_names.empty() && read_and_clear_clocks(clk) != TP_OK) return -1;
+    // kernels counted by the clock counters but not timed by events (a
+    // selection is in force) are listed after the timed ones, launches 0
+    for (size_t s = 0; s < clock_names.size(); ++s)
+        if (!agg.count(clock_names[s]) && (clk[2 * s] || clk[2 * s + 1])) {
+            order.push_back(clock_names[s]);
+            agg[clock_names[s]] = {0, 0.0};
+        }
     int n = 0;
     for (auto &name : order) {
         if (!entries || n >= max_entries) break;

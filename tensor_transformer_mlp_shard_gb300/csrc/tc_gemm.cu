@@ -142,6 +142,7 @@ static std::atomic<bool> g_tail_split{true};
 static std::atomic<bool> g_k_reverse{true};
 static std::atomic<int> g_band_rows{0};
 static std::atomic<int> g_max_pairs{0};
+static std::atomic<bool> g_pdl{true};
 static std::atomic<uint64_t> g_tail_launches{0};
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -187,6 +188,7 @@ void set_tail_split(bool on) { tc::g_tail_split.store(on); }
 void set_k_reverse(bool on) { tc::g_k_reverse.store(on); }
 void set_band_rows(int g) { tc::g_band_rows.store(g > 0 ? g : 0); }
 void set_max_gemm_pairs(int n) { tc::g_max_pairs.store(n > 0 ? n : 0); }
+void set_pdl(bool on) { tc::g_pdl.store(on); }
 uint64_t tail_split_launches() { return tc::g_tail_launches.load(); }
 
 size_t tc_tail_bytes(int M, int N, int P, int S, int Kseg, bool fp8) {
@@ -422,17 +424,22 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     launch_begin(g.name, st);
     if (use_pair) {
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        // programmatic dependent launch: the pairs' set-up (barriers, TMEM)
+        // overlaps the previous kernel, and the kernel waits for it in
+        // griddepcontrol.wait before it touches global memory
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
         cfg.blockDim = dim3(NUM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = smem_bytes;
         cfg.stream = st;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = g_pdl.load() ? 2 : 1;
         e = cudaLaunchKernelEx(&cfg, fn, prm);
     } else {
         const int grid = prm.total_tiles < num_sms() ? prm.total_tiles : num_sms();

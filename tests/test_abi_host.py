@@ -57,6 +57,8 @@ def test_gemm_setting_validation(tp):
     assert L.tp_set_k_order(0) == 0 and L.tp_set_k_order(1) == 0
     assert L.tp_set_band_rows(-1) == 1 and L.tp_set_band_rows(5000) == 1
     assert L.tp_set_band_rows(16) == 0 and L.tp_set_band_rows(0) == 0
+    assert L.tp_set_launch_overlap(2) == 1 and L.tp_set_launch_overlap(-1) == 1
+    assert L.tp_set_launch_overlap(0) == 0 and L.tp_set_launch_overlap(1) == 0
     assert L.tp_set_tail_split(0) == 0 and L.tp_set_tail_split(1) == 0
     assert L.tp_set_max_gemm_pairs(4) == 0 and L.tp_set_max_gemm_pairs(0) == 0
     assert L.tp_tail_split_count() == 0  # nothing launched on a host without a GPU

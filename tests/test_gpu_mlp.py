@@ -253,6 +253,46 @@ def test_timeout_reaches_only_its_handle(tp):
     assert rel_err(run.gathered(run.Y), oracle_full(b, t)["Y"]) < 1e-2
 
 
+def test_kernel_timers_and_selection(tp):
+    """The per-kernel timers (tp_prof_enable / tp_prof_collect): every
+    launch of a forward+backward step is timed by events and the pair GEMMs
+    report their SM clock; with tp_prof_select only the chosen kernel's
+    launches carry events, while the other GEMMs are still listed through
+    their clock counters (launches 0).  The results do not change."""
+    M, H, F, T = 1024, 512, 2048, 4
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    run = MlpRun(lay, t)
+    gemms = {"col_fwd", "row_fwd", "row_dgrad_act", "wgrad_row", "wgrad_col", "col_dgrad"}
+    outs = []
+    try:
+        for sel in (None, "row_fwd"):
+            tp.prof_select(sel)
+            tp.prof_enable(True)
+            tp.prof_collect()
+            run.fwd()
+            run.bwd()
+            got = tp.prof_collect(clocks=True)
+            tp.prof_enable(False)
+            assert status_ok(tp, lay)
+            outs.append([host(x) for x in run.Y + run.dX + run.dW1 + run.dW2])
+            assert gemms <= set(got), got
+            for name in gemms:
+                n, ms, cyc, ns = got[name]
+                assert cyc > 0 and ns > 0 and 500 < cyc / ns * 1e3 < 2500, (name, got[name])  # MHz
+                if sel is None or name == sel:
+                    assert n == 1 and ms > 0, (name, got[name])
+                else:
+                    assert n == 0 and ms == 0, (name, got[name])
+            if sel is not None:
+                assert all(v[0] == 0 for k, v in got.items() if k != sel), got
+    finally:
+        tp.prof_select(None)
+        tp.prof_enable(False)
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
 def test_binding_rejects_wrong_shapes(tp):
     lay = tp.TPMLP(S=64, B=2, H=64, F=256, T=2, act="gelu_tanh", dtype="bf16", has_bias=True)
     t = mlp_inputs(128, 64, 256, 2, "gelu_tanh", "bf16")

@@ -36,6 +36,7 @@ def tp():
     yield tp
     tp.set_max_gemm_pairs(0)
     tp.set_tail_split(True)
+    tp.set_launch_overlap(True)
 
 
 def _outputs(run):
@@ -309,3 +310,50 @@ def test_band_rows_match_oracle(tp, band):
         errs[f"db1_{i}"] = rel_err(a[f"db1_{i}"], ref["db1"][i])
     bad = {k: v for k, v in errs.items() if not v <= 1e-2}
     assert not bad, bad
+
+
+@pytest.mark.parametrize("sp", [False, True])
+def test_launch_overlap_keeps_stream_order(tp, sp):
+    """Programmatic dependent launch of the pair GEMMs (tp_set_launch_overlap):
+    two forward+backward steps on different inputs, issued back to back with
+    no host synchronisation and sharing the pre, A and workspace buffers, so
+    that a GEMM reading an operand before the kernel producing it finished
+    (the row forward's A, the dgrads' dPre) or overwriting a buffer a GEMM
+    before it still reads (the second column forward's pre and A under the
+    first backward) would change the results.  Both steps give the bits of
+    plain stream order and match the oracle; the grid cut to 7 pairs gives
+    several persistent rounds and a tail split."""
+    M, H, F, T = 1024, 512, 2048, 4
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=not sp,
+                   seq_parallel=sp)
+    ins = [mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True, seed_off=k) for k in (0, 1)]
+    res = {}
+    try:
+        for on in (False, True, True):
+            tp.set_launch_overlap(on)
+            tp.set_max_gemm_pairs(7)
+            runs = [MlpRun(lay, t) for t in ins]
+            runs[1].pre, runs[1].A, runs[1].ws = runs[0].pre, runs[0].A, runs[0].ws
+            torch.cuda.synchronize()
+            for r in runs:
+                r.fwd()
+                r.bwd()
+            assert status_ok(tp, lay)
+            res.setdefault(on, []).append([_outputs(r) for r in runs])
+    finally:
+        tp.set_launch_overlap(True)
+        tp.set_max_gemm_pairs(0)
+    plain = res[False][0]
+    for got in res[True]:
+        for k in (0, 1):
+            for name in plain[k]:
+                assert np.array_equal(plain[k][name], got[k][name]), (k, name)
+    for k in (0, 1):
+        ref = oracle_full(lay, ins[k])
+        a = plain[k]
+        errs = {"Y": rel_err(a["Y"], ref["Y"]), "dX": rel_err(a["dX"], ref["dX"])}
+        for i in range(T):
+            errs[f"dW1_{i}"] = rel_err(a[f"dW1_{i}"], ref["dW1"][i])
+            errs[f"dW2_{i}"] = rel_err(a[f"dW2_{i}"], ref["dW2"][i])
+        bad = {n: v for n, v in errs.items() if not v <= 1e-2}
+        assert not bad, (k, bad)
