@@ -96,11 +96,12 @@ tp_status encode_map(CUtensorMap *m, const void *ptr, int rows, int cols, int bo
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// MN-major bf16 operand [rows (K) x cols (MN)], cols % 64 == 0, as the 3D
-// tensor {64 elements, rows, cols / 64 groups} with strides {row pitch, 128
-// bytes}: a box {64, box_rows, 2} is the two [box_rows K rows x 128 bytes]
-// swizzle atoms of a 128-wide MN tile, one after the other (the CTA-pair
-// kernel's a3d/b3d; box_rows = the K elements of one stage)
+// bf16 operand [rows x cols], cols % 64 == 0, as the 3D tensor {64
+// elements, rows, cols / 64 groups} with strides {row pitch, 128 bytes}: a
+// box {64, box_rows, 2} lands as two [box_rows x 128 bytes] swizzle atoms,
+// one after the other (the CTA-pair kernel's a3d/b3d).  MN-major [K x MN]:
+// the two 64-wide MN atoms of a 128-wide tile, box_rows = the K elements of
+// one stage; K-major [rows x K]: two consecutive K blocks of 128 rows.
 static tp_status encode_map_mn3d(CUtensorMap *m, const void *ptr, int rows, int cols, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return set_error(TP_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -228,29 +229,39 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
         return set_error(TP_ERR_UNSUPPORTED, "token-sharded MN-major operand outside the token-sharded GEMM instance");
     KernelFn fn = kernel_at(ki, use_pair, fp8);
     // K elements per stage: one 128-byte row of each operand, two for the
-    // pair kernel's bf16 weight gradients (both operands MN-major, tc_gemm_pair_kernel's KB2)
-    const int kb2 = (use_pair && !fp8 && g.A.mn_major && g.B.mn_major) ? 2 : 1;
-    const int bke = (fp8 ? Elem<true>::BKE : Elem<false>::BKE) * kb2;
+    // pair kernel's bf16 GEMMs (tc_gemm_pair_kernel's KB2)
+    static_assert(pair_kb2<EPI_COL, false>() == 2 && pair_kb2<EPI_PLAIN, false>() == 2 &&
+                      pair_kb2<EPI_DACT, false>() == 2 && pair_kb2<EPI_F32, false>() == 2 &&
+                      pair_kb2<EPI_COL, true>() == 1 && pair_kb2<EPI_PLAIN, true>() == 1 &&
+                      pair_kb2<EPI_DACT, true>() == 1 && pair_kb2<EPI_F32, true>() == 1,
+                  "the host's K blocks per stage match the kernels'");
+    const int kb2 = use_pair && !fp8 ? 2 : 1;
+    const int bke1 = fp8 ? Elem<true>::BKE : Elem<false>::BKE;  // K elements of one 128-byte row
+    const int bke = bke1 * kb2;
     const int mnb = fp8 ? Elem<true>::MNB : Elem<false>::MNB;  // MN elements per MN-major box
     const int tile_m = use_pair ? P_TILE_M : BM;
     // rows of the B tile that one CTA loads per box
     const int b_box_rows = (use_pair || g.b_dual_off) ? BN / 2 : BN;
     Params prm;
     memset(&prm, 0, sizeof(prm));
-    // one 3D box instead of two 2D boxes per MN-major bf16 operand and stage
-    // (pair kernel): the weight gradients run 11% faster (GB300, GPT sizes)
-    prm.a3d = use_pair && !fp8 && g.A.mn_major && g.A.cols % 64 == 0;
-    prm.b3d = use_pair && !fp8 && g.B.mn_major && g.B.cols % 64 == 0 && !g.b_dual_off;
+    // one 3D box instead of two 2D boxes per operand and stage (pair kernel,
+    // bf16): an MN-major operand's two 64-wide atoms (the weight gradients
+    // run 11% faster, GB300, GPT sizes), or a K-major operand's two K blocks
+    // when a stage holds two (both need the extent along the box groups to
+    // be a multiple of 64)
+    prm.a3d = use_pair && !fp8 && g.A.cols % 64 == 0 && (g.A.mn_major || kb2 == 2);
+    prm.b3d = use_pair && !fp8 && g.B.cols % 64 == 0 && (g.B.mn_major ? !g.b_dual_off : kb2 == 2);
     for (int i = 0; i < g.A.n; ++i) {
-        tp_status s = prm.a3d        ? encode_map_mn3d(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke)
+        tp_status s = prm.a3d ? encode_map_mn3d(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, g.A.mn_major ? bke : BM)
                       : g.A.mn_major ? encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, mnb, bke, fp8)
-                                     : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke, BM, fp8);
+                                     : encode_map(&prm.mapA[i], g.A.ptr[i], g.A.rows, g.A.cols, bke1, BM, fp8);
         if (s != TP_OK) return s;
     }
     for (int i = 0; i < g.B.n; ++i) {
-        tp_status s = prm.b3d        ? encode_map_mn3d(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke)
-                      : g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
-                                     : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke, b_box_rows, fp8);
+        tp_status s =
+            prm.b3d ? encode_map_mn3d(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, g.B.mn_major ? bke : b_box_rows)
+            : g.B.mn_major ? encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, mnb, bke, fp8)
+                           : encode_map(&prm.mapB[i], g.B.ptr[i], g.B.rows, g.B.cols, bke1, b_box_rows, fp8);
         if (s != TP_OK) return s;
     }
     prm.selA = {g.A.p_stride, g.A.s_stride, g.A.rows_split, g.A.n};
@@ -374,8 +385,10 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     static int max_pairs[64][2][kNumKernels] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int smem_bytes = use_pair ? pair_smem_bytes(g.kind == EPI_DACT ? pair_stages<EPI_DACT>() : P_STAGES)
-                                    : SMEM_BYTES;
+    const int smem_bytes = !use_pair              ? SMEM_BYTES
+                           : g.kind != EPI_DACT ? (fp8 ? pair_smem_total<EPI_PLAIN, true>() : pair_smem_total<EPI_PLAIN, false>())
+                           : fp8                ? pair_smem_total<EPI_DACT, true>()
+                                                : pair_smem_total<EPI_DACT, false>();
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev % 64][fp8][use_pair][ki]) {

@@ -1307,16 +1307,29 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * ROW_BYTES;  // 16 KB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = 128 * ROW_BYTES;  // 16 KB: this CTA's 128 rows of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-// Ring depth per epilogue: the act' dgrad reads pre through L1, which gets the
-// shared memory a block does not claim, so it runs a 5-stage ring (L1 about
-// 60 KB instead of 28 KB): 2% fewer SM cycles in bf16 and 5% in FP8 (one
-// stage less costs the other GEMMs up to 1%); in time, under the power cap,
-// the FP8 act' dgrad gains 1% and the bf16 one stays level.
-template <int EPI>
+// Ring depth, in 32 KB units: six everywhere (three stages of two K blocks in
+// bf16) except the FP8 act' dgrad, which reads pre through L1 (the shared
+// memory a block does not claim) and runs five stages of one K block (L1
+// about 60 KB instead of 28 KB: 5% fewer SM cycles, 1% in time under the
+// power cap).  The bf16 act' dgrad gained the same way with one K block per
+// stage, but with two it is 3% faster still at six units, level with the
+// column forward; two stages of two K blocks (more L1) made it 27% slower.
+template <int EPI, bool F8>
 constexpr int pair_stages() {
-    return EPI == EPI_DACT ? 5 : P_STAGES;
+    return (EPI == EPI_DACT && F8) ? 5 : P_STAGES;
+}
+// K blocks per stage (see tc_gemm_pair_kernel): two for bf16
+template <int EPI, bool F8>
+constexpr int pair_kb2() {
+    return F8 ? 1 : 2;
 }
 constexpr int pair_smem_bytes(int stages) { return stages * P_STAGE_BYTES + 1024 + BAR_BYTES + EPI_SMEM; }
+// dynamic shared memory of a pair-kernel instance: the ring as the kernel
+// lays it out (whole stages of KB2 K blocks) and the rest
+template <int EPI, bool F8>
+constexpr int pair_smem_total() {
+    return pair_smem_bytes(pair_stages<EPI, F8>() / pair_kb2<EPI, F8>() * pair_kb2<EPI, F8>());
+}
 constexpr int P_SMEM_BYTES = pair_smem_bytes(P_STAGES);
 constexpr int P_TILE_M = 256;
 static_assert(TAIL_UNIT_FLOATS == static_cast<size_t>(P_TILE_M) * BN, "tail slices hold one pair tile");
@@ -1430,14 +1443,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     ClockMark clk_mark;
     clk_mark.start(p.clk);
     using E = Elem<F8>;
-    // K blocks per stage: two for the bf16 weight gradients (both operands
-    // MN-major), whose producer issues one 3D box of {64, 128 K rows, 2
-    // atoms} per operand and stage instead of one of 64 rows -- half the
-    // loads and barrier operations per K for the thread whose issue path
-    // limits these GEMMs -- in half as many stages of twice the size (the
-    // same shared memory)
-    constexpr int KB2 = (A_MN && B_MN && !F8) ? 2 : 1;
-    constexpr int NST = pair_stages<EPI>() / KB2;
+    // K blocks per stage: two for bf16, in half as many stages of twice the
+    // size (the same shared memory).  An MN-major operand comes as
+    // one 3D box of {64, 128 K rows, 2 atoms}, a K-major one as one 3D box
+    // {64, 128 rows, 2 K blocks} (or two 2D boxes when its K extent is not a
+    // multiple of 64): half the loads and barrier operations per K for the
+    // producer thread, and eight MMAs per full barrier instead of four.
+    constexpr int KB2 = pair_kb2<EPI, F8>();
+    constexpr int NST = pair_stages<EPI, F8>() / KB2;
     constexpr int STG = P_STAGE_BYTES * KB2;  // bytes of one stage in this CTA
     constexpr int BKS = E::BKE * KB2;         // K elements of one stage
     extern __shared__ uint8_t smem_raw[];
@@ -1553,7 +1566,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                     const uint32_t sb = sa + P_A_BYTES * KB2;
                     const int k0 = kb * BKS;
                     if (!A_MN) {
-                        tma_load_2d_pair(sa, ma, fb, k0, ra);
+                        if (KB2 == 1) {
+                            tma_load_2d_pair(sa, ma, fb, k0, ra);
+                        } else if (p.a3d) {
+                            tma_load_3d_pair(sa, ma, fb, 0, ra, k0 / E::BKE);
+                        } else {
+                            tma_load_2d_pair(sa, ma, fb, k0, ra);
+                            tma_load_2d_pair(sa + P_A_BYTES, ma, fb, k0 + E::BKE, ra);
+                        }
                     } else {
                         const CUtensorMap *m = ma;
                         int lrow = k0;
@@ -1570,7 +1590,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         }
                     }
                     if (!B_MN) {
-                        tma_load_2d_pair(sb, mb, fb, k0, rb);
+                        if (KB2 == 1) {
+                            tma_load_2d_pair(sb, mb, fb, k0, rb);
+                        } else if (p.b3d) {
+                            tma_load_3d_pair(sb, mb, fb, 0, rb, k0 / E::BKE);
+                        } else {
+                            tma_load_2d_pair(sb, mb, fb, k0, rb);
+                            tma_load_2d_pair(sb + P_B_BYTES, mb, fb, k0 + E::BKE, rb);
+                        }
                     } else {
                         const CUtensorMap *m = mb;
                         int lrow = k0;
@@ -1644,10 +1671,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         const uint32_t sb = sa + P_A_BYTES * KB2;
 #pragma unroll
                         for (int kk = 0; kk < 4 * KB2; ++kk) {
-                            const uint64_t ad = A_MN ? smem_desc(sa + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
-                                                     : smem_desc(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? smem_desc(sb + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
-                                                     : smem_desc(sb + kk * 32, 16, 1024);
+                            // K-major: K block kk / 4 is its own 16 KB slab
+                            const uint64_t ad =
+                                A_MN ? smem_desc(sa + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
+                                     : smem_desc(sa + (kk >> 2) * P_A_BYTES + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd =
+                                B_MN ? smem_desc(sb + kk * E::KADV_MN, E::MNB_BYTES * KB2, 1024)
+                                     : smem_desc(sb + (kk >> 2) * P_B_BYTES + (kk & 3) * 32, 16, 1024);
                             umma_op_pair<F8>(d, ad, bd, idesc, accumulate);
                             accumulate = 1;
                         }
