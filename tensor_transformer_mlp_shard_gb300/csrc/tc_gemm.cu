@@ -151,7 +151,8 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Persistent round structure: `total` tiles over `pairs` CTA pairs leave
 // rem = total % pairs tiles for a last, part-filled round.  When rem is at
 // most half the pairs, each of those tiles is cut along K into
-// s = min(pairs / rem, 4) units (each at least 4 of the nk K steps), which
+// s = min(pairs / rem, 4) units (each at least 4 of the nk K blocks of
+// 128-byte rows; a stage may hold two), which
 // all run in one round of 1/s of a tile's time.  Measured on GB300: with a
 // single round of units the split pays (the GPT-size weight gradients, 36
 // tiles over 76 pairs, 1.3% faster); spreading a fuller last round over
@@ -422,7 +423,7 @@ tp_status launch_tc_gemm(const GemmPlan &g, cudaStream_t st) {
     cudaError_t e;
     const int pairs = std::min(prm.total_tiles, pair_limit(max_pairs[dev % 64][fp8][ki]));
     if (use_pair && prm.out_tma && !split && (g.kind == EPI_PLAIN || g.kind == EPI_F32) && g.tail_ws) {
-        const TailPlan tp = tail_plan(prm.total_tiles, pairs, g.S * prm.num_kb);
+        const TailPlan tp = tail_plan(prm.total_tiles, pairs, g.S * prm.num_kb * kb2);
         if (tp.s > 1 && tp.bytes <= g.tail_bytes && (reinterpret_cast<uintptr_t>(g.tail_ws) & 255u) == 0) {
             prm.tail_s = tp.s;
             prm.tail_first = prm.total_tiles - tp.rem;
