@@ -64,9 +64,19 @@ def load_peaks():
         with open(path) as f:
             p = json.load(f)
         return {"bf16_tflops": float(p["bf16_tflops"]), "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]),
-                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+                "hbm_gbs": float(p["hbm_gbs"]), "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
     except Exception:
-        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "sm_max_mhz": 2070.0,
+                "source": "fallback"}
+
+
+def fp32_alu_peak(sms, peaks):
+    """(TFLOP/s, description) of the fp32 FFMA rate the fp32 engine is bound
+    by: SMs x 128 FP32 lanes x 2 FLOP per FMA x the maximum SM clock."""
+    mhz = peaks["sm_max_mhz"]
+    return (sms * 128 * 2 * mhz * 1e6 / 1e12,
+            f"fp32 FFMA, nominal: {sms} SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz (maximum SM clock)")
 
 
 # ---------------------------------------------------------------------------
@@ -179,11 +189,12 @@ def kernel_flops(w):
 
 def gemm_bytes(w):
     """Algorithmic HBM bytes of one launch of each GEMM kernel (bf16 operands
-    and activations, fp32 weight gradients; every operand read once, every
+    and activations, or fp32 ones for the fp32 workloads, fp32 weight
+    gradients; every operand read once, every
     output written once) -- with kernel_flops, the arithmetic intensity that
     decides which roof bounds the kernel."""
     M, H, F, g = w.M, w.H, w.F, w.g
-    e = 2
+    e = 4 if w.dtype == "f32" else 2
     if w.kind == "attn_proj":
         Fo = w.F_o
         return {"col_fwd": e * (M * H + F * H + M * F), "wgrad_col": e * (M * F + M * H) + 4 * F * H,
@@ -558,7 +569,10 @@ def run_gpu(args, w, dist, rank, local, ws):
     if dom and dom in kclk and kclk[dom][0] > 0:
         n, tot = kclk[dom][:2]
         avg_s = (tot / n) * 1e-3
-        peak, peak_kind = peak_t, peak_kind_t
+        peak, peak_kind, bound = peak_t, peak_kind_t, "tensor"
+        if w.dtype == "f32":  # the fp32 engine runs on the CUDA cores' FFMA
+            peak, peak_kind = fp32_alu_peak(torch.cuda.get_device_properties(dev).multi_processor_count, peaks)
+            bound = "alu"
         gb = gemm_bytes(w)[dom]
         # below the ridge point (peak FLOP/s / peak B/s) the kernel is bound by HBM
         if kf[dom] / gb < peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
@@ -569,7 +583,7 @@ def run_gpu(args, w, dist, rank, local, ws):
                         "tflops": round(kf[dom] / avg_s / 1e12, 1)}
         else:
             achieved = kf[dom] / avg_s / 1e12
-            roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+            roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                         "peak_kind": peak_kind, "algorithmic_flop_per_launch": kf[dom]}
     if roofline is not None and w.dtype == "bf16" and not layer and roofline["bound"] == "tensor" \

@@ -59,3 +59,12 @@ def test_peak_follows_the_timed_region():
     assert p == 1700.0 and "sustained" in kind
     p, kind = bench.pick_peak(peaks, 1.0, "fp8")
     assert p == 3800.0 and kind.startswith("fp8")
+
+
+def test_fp32_engine_peak_from_unit_counts():
+    """The fp32 engine's roof: SMs x 128 FP32 lanes x 2 FLOP x the maximum
+    SM clock (GB300: 152 SMs at 2070 MHz, 80.6 TFLOP/s)."""
+    import bench
+    peak, kind = bench.fp32_alu_peak(152, {"sm_max_mhz": 2070.0})
+    assert abs(peak - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+    assert abs(peak - 80.55) < 0.01 and "FFMA" in kind
