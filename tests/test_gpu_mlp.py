@@ -53,6 +53,9 @@ CASES = [
     (256, 256, 1024, 2, "gelu_tanh", "f32", True, False, False),
     (300, 264, 800, 4, "swiglu", "f32", True, True, False),
     (120, 72, 240, 3, "gelu_tanh", "f32", True, True, True),
+    # enough 64 x 64 tiles that the fp32 engine splits no K range (the other
+    # fp32 cases split theirs over clusters of 2 to 8 blocks)
+    (1024, 512, 2048, 2, "gelu_tanh", "f32", True, True, False),
     # few weight-gradient tiles and many tokens: split-K weight gradients
     (4100, 256, 512, 2, "gelu_tanh", "bf16", True, True, False),
     (4096, 192, 640, 2, "swiglu", "bf16", False, False, True),
