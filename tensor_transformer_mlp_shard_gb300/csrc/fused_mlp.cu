@@ -10,15 +10,16 @@
 //   Y = (X +) dropout(Y + b2) -> HBM   (dropout only in the TransformerLayer)
 // so A never makes the round trip HBM -> row GEMM, and the cross-shard sum of
 // the row layer (the forward all-reduce) is the Y accumulation over (i, c).
-// The output tile [128 x H] lives in TMEM next to two 64-column accumulators
+// The output tile [128 x H] lives in TMEM next to four 64-column accumulators
 // of the column GEMM, so H <= 256: at wider layers the output row does not
 // fit on chip and the two-kernel path (tc_gemm) runs instead.
 //
 // Warp roles (320 threads): warp 0 issues TMA (the X tile once per token
-// tile, then W1 and W2 boxes in consumption order through a 16-slot ring),
+// tile, then W1 and W2 boxes in consumption order through an 8-slot ring),
 // warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of chunk
-// c - 2, so that the tensor core works while two epilogue groups turn chunks
-// c - 1 and c - 2 into A), warps 2-9 run the epilogues in two groups that
+// c - 3, so that the tensor core works while two epilogue groups turn the
+// chunks in between into A; four accumulators and four A buffers), warps 2-9
+// run the epilogues in two groups that
 // take alternate chunks and write pre, A and Y with direct 16-byte stores
 // (no staging: a chunk's epilogue is short, and waiting for bulk stores to
 // release staging buffers stretched it).  Every wait is bounded.
@@ -48,19 +49,22 @@ constexpr int kRows = 128;      // token rows per tile (tcgen05 M)
 constexpr int kChunk = 64;      // hidden units per chunk: column GEMM N, row GEMM K
 constexpr int kMaxH = 256;      // output tile [128 x H] + 2 x 64 accumulator columns <= 512 TMEM columns
 constexpr int kBox = 64 * 128;  // one [64 rows x 64] bf16 box (128-byte rows): 8 KB
-constexpr int kSlots = 16;
-constexpr int kLag = 2;         // the row GEMM of chunk c is issued after the column GEMM of chunk c + 2
+constexpr int kSlots = 8;
+constexpr int kNB = 4;          // column-GEMM accumulators and A buffers
+constexpr int kLag = 3;         // the row GEMM of chunk c is issued after the column GEMM of chunk c + 3
 constexpr int kXBytes = kMaxH / 64 * (kRows * 128);  // X tile: H/64 boxes of [128 x 64]
 constexpr int kABytes = kRows * 128;                 // A chunk [128 x 64] bf16
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kOffX = kSlots * kBox;
 constexpr int kOffA = kOffX + kXBytes;
-constexpr int kOffBar = kOffA + 2 * kABytes;
+constexpr int kOffBar = kOffA + kNB * kABytes;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment slack
 constexpr int kTmemCols = 512;
-constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 320
-static_assert(2 * kSlots + 13 <= 64, "barriers overlap the TMEM address slot");
+constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256, 320, 384, 448
+static_assert(2 * kSlots + 5 + 4 * kNB <= 64, "barriers overlap the TMEM address slot");
+static_assert(kAccCol + kNB * kChunk <= kTmemCols, "column accumulators beyond TMEM");
+static_assert(kLag < kNB, "the row GEMM must not lag the column GEMM by a whole buffer cycle");
 static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB a block may use");
 
 struct FusedParams {
@@ -130,13 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 64);  // after the 2 * kSlots + 13 barriers
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 64);  // after the 2 * kSlots + 5 + 4 * kNB barriers
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * kSlots;
     const uint32_t xfull = empty0 + 8 * kSlots, xempty = xfull + 8;
-    const uint32_t accf0 = xempty + 8, acce0 = accf0 + 16;  // column-GEMM accumulator full / drained
-    const uint32_t af0 = acce0 + 16, ae0 = af0 + 16;        // A buffer written / consumed
-    const uint32_t yfull = ae0 + 16, yempty = yfull + 8, drain = yempty + 8;
+    const uint32_t accf0 = xempty + 8, acce0 = accf0 + 8 * kNB;  // column-GEMM accumulator full / drained
+    const uint32_t af0 = acce0 + 8 * kNB, ae0 = af0 + 8 * kNB;    // A buffer written / consumed
+    const uint32_t yfull = ae0 + 8 * kNB, yempty = yfull + 8, drain = yempty + 8;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr uint32_t kEpiThreads = 32 * kEpiWarps;
 
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         }
         mbar_init(xfull, 1);
         mbar_init(xempty, 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNB; ++b) {
             mbar_init(accf0 + 8 * b, 1);
             mbar_init(acce0 + 8 * b, kEpiThreads / 2);  // one epilogue group per buffer
             mbar_init(af0 + 8 * b, kEpiThreads / 2);
@@ -226,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 for (int c = 0; ok && c < p.nc + kLag; ++c) {
                     if (c < p.nc) {
                         // column GEMM of chunk c: acc1[b] = X_tile W1 chunk^T (K = H)
-                        const int cg = cgb + c, b = cg & 1;
-                        const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                        const int cg = cgb + c, b = cg % kNB;
+                        const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                         if (!fwait(acce0 + 8 * b, (use & 1u) ^ 1u, p)) {
                             ok = false;
                             break;
@@ -261,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     if (c >= kLag) {
                         // row GEMM of chunk c - kLag: Y[:, 64g..] += A W2 chunk^T (K = 64)
-                        const int cg = cgb + c - kLag, b = cg & 1;
-                        const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                        const int cg = cgb + c - kLag, b = cg % kNB;
+                        const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                         if (!fwait(af0 + 8 * b, use & 1u, p)) {
                             ok = false;
                             break;
@@ -321,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             const bool block_ok = row0 < p.M;  // warp-uniform
             const bool row_ok = row < p.M;
             for (int c = (cgb & 1) == h ? 0 : 1; c < p.nc; c += 2) {
-                const int cg = cgb + c, b = h;
-                const uint32_t use = static_cast<uint32_t>(cg) >> 1;
+                const int cg = cgb + c, b = cg % kNB;
+                const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                 const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                 uint4 bias[8];  // the chunk's 64 b1 values, fetched while the accumulator fills
                 if (p.has_bias) {
