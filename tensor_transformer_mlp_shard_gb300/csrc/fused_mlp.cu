@@ -1,28 +1,27 @@
 // Fused MLP forward for narrow layers (Megatron's FlashFusedMLP,
 // "Megatron-LM 源码精读" s7, the fusions/ entry): one persistent
 // kernel per 128-token tile runs
-//   for every shard i and every 64-unit chunk c of shard i:
-//     acc1  = X_tile W1_i[c]^T                    (tcgen05, TMEM, N = 64)
+//   for every shard i and every 128-unit chunk c of shard i:
+//     acc1  = X_tile W1_i[c]^T                    (tcgen05, TMEM, N = 128)
 //     pre   = acc1 + b1_i[c]  -> HBM (kept for the backward)
 //     A     = act(pre)        -> HBM (kept for the backward)
-//                             -> shared memory, 128-byte swizzled K-major
-//     Y    += A W2_i[:, c]^T                      (tcgen05, TMEM, K = 64)
+//                             -> shared memory, two 128-byte swizzled K-major atoms
+//     Y    += A W2_i[:, c]^T                      (tcgen05, TMEM, K = 128)
 //   Y = (X +) dropout(Y + b2) -> HBM   (dropout only in the TransformerLayer)
 // so A never makes the round trip HBM -> row GEMM, and the cross-shard sum of
 // the row layer (the forward all-reduce) is the Y accumulation over (i, c).
-// The output tile [128 x H] lives in TMEM next to four 64-column accumulators
-// of the column GEMM, so H <= 256: at wider layers the output row does not
-// fit on chip and the two-kernel path (tc_gemm) runs instead.
+// The output tile [128 x H] lives in TMEM next to two 128-column
+// accumulators of the column GEMM, so H <= 256: at wider layers the output
+// row does not fit on chip and the two-kernel path (tc_gemm) runs instead.
 //
 // Warp roles (320 threads): warp 0 issues TMA (the X tile once per token
-// tile, then W1 and W2 boxes in consumption order through an 8-slot ring),
-// warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of chunk
-// c - 3, so that the tensor core works while two epilogue groups turn the
-// chunks in between into A; four accumulators and four A buffers), warps 2-9
-// run the epilogues in two groups that
-// take alternate chunks and write pre, A and Y with direct 16-byte stores
-// (no staging: a chunk's epilogue is short, and waiting for bulk stores to
-// release staging buffers stretched it).  Every wait is bounded.
+// tile, then W1 and W2 boxes of 16 KB in consumption order through a 6-slot
+// ring), warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of
+// chunk c - 2, so that the tensor core works while two epilogue groups turn
+// chunks c - 1 and c - 2 into A), warps 2-9 run the epilogues in two groups
+// that take alternate chunks and write pre, A and Y with direct 16-byte
+// stores (no staging: a chunk's epilogue is short, and waiting for bulk
+// stores to release staging buffers stretched it).  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -46,14 +45,15 @@ namespace fm {
 using namespace tc;
 
 constexpr int kRows = 128;      // token rows per tile (tcgen05 M)
-constexpr int kChunk = 64;      // hidden units per chunk: column GEMM N, row GEMM K
-constexpr int kMaxH = 256;      // output tile [128 x H] + 2 x 64 accumulator columns <= 512 TMEM columns
-constexpr int kBox = 64 * 128;  // one [64 rows x 64] bf16 box (128-byte rows): 8 KB
-constexpr int kSlots = 8;
-constexpr int kNB = 4;          // column-GEMM accumulators and A buffers
-constexpr int kLag = 3;         // the row GEMM of chunk c is issued after the column GEMM of chunk c + 3
+constexpr int kChunk = 128;     // hidden units per chunk: column GEMM N, row GEMM K
+constexpr int kMaxH = 256;      // output tile [128 x H] + 2 x 128 accumulator columns <= 512 TMEM columns
+constexpr int kBox = 128 * 128; // one [128 rows x 64] bf16 box (128-byte rows): 16 KB
+constexpr int kSlots = 6;
+constexpr int kNB = 2;          // column-GEMM accumulators and A buffers
+constexpr int kLag = 2;         // the row GEMM of chunk c is issued after the column GEMM of chunk c + 2
 constexpr int kXBytes = kMaxH / 64 * (kRows * 128);  // X tile: H/64 boxes of [128 x 64]
-constexpr int kABytes = kRows * 128;                 // A chunk [128 x 64] bf16
+constexpr int kAtom = kRows * 128;                   // [128 rows x 64] bf16, one 128-byte swizzle atom
+constexpr int kABytes = kChunk / 64 * kAtom;         // A chunk [128 x 128] bf16: two K-major atoms
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kOffX = kSlots * kBox;
@@ -61,16 +61,16 @@ constexpr int kOffA = kOffX + kXBytes;
 constexpr int kOffBar = kOffA + kNB * kABytes;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment slack
 constexpr int kTmemCols = 512;
-constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256, 320, 384, 448
+constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 384
 static_assert(2 * kSlots + 5 + 4 * kNB <= 64, "barriers overlap the TMEM address slot");
 static_assert(kAccCol + kNB * kChunk <= kTmemCols, "column accumulators beyond TMEM");
-static_assert(kLag < kNB, "the row GEMM must not lag the column GEMM by a whole buffer cycle");
+static_assert(kLag <= kNB, "the row GEMM must not lag the column GEMM by more than a buffer cycle");
 static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB a block may use");
 
 struct FusedParams {
     CUtensorMap mapX[kMaxShards];    // X token shards, boxes [128 rows x 64], 128-byte swizzle
-    CUtensorMap mapW1[kMaxShards];   // W1_i [Fs, H], boxes [64 x 64]
-    CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [64 x 64]
+    CUtensorMap mapW1[kMaxShards];   // W1_i [Fs, H], boxes [128 units x 64]
+    CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [128 rows of H x 64 units]
     __nv_bfloat16 *pre[kMaxShards];  // pre_i [M, Fs] (or null)
     __nv_bfloat16 *A[kMaxShards];    // A_i [M, Fs]
     __nv_bfloat16 *Y[kMaxShards];    // Y token shards [rows_split or M, H]
@@ -81,6 +81,7 @@ struct FusedParams {
     int rows_split, n_tok;
     int M, H, Fs, T, act, has_bias, has_res, has_pre;
     int m_tiles, cps, nc, kb;  // chunks per shard, chunks per tile (T * cps), H / 64
+    int nh;                    // 128-column halves of the output (H / 128 rounded up)
     uint32_t idesc;            // bf16 x bf16 -> fp32, both K-major, M = 128, N = 64
     int *status;
     unsigned *abort_word;
@@ -210,7 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     if (ok && c >= kLag) {
                         const int ch = chunk_at(p, t, c - kLag), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
-                        for (int g = 0; ok && g < p.kb; ++g) ok = load_box(&p.mapW2[i], u0, g * 64);
+                        for (int h = 0; ok && h < p.nh; ++h)
+                            for (int k2 = 0; ok && k2 < kChunk / 64; ++k2)
+                                ok = load_box(&p.mapW2[i], u0 + 64 * k2, h * 128);
                     }
                 }
             }
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         if (c == p.nc - 1) umma_commit(xempty);  // the tile's last read of X
                     }
                     if (c >= kLag) {
-                        // row GEMM of chunk c - kLag: Y[:, 64g..] += A W2 chunk^T (K = 64)
+                        // row GEMM of chunk c - kLag: Y[:, 128h..] += A W2 chunk^T (K = 128)
                         const int cg = cgb + c - kLag, b = cg % kNB;
                         const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                         if (!fwait(af0 + 8 * b, use & 1u, p)) {
@@ -277,22 +280,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         }
                         tc_fence_after();
                         const uint32_t sa = sbase + kOffA + b * kABytes;
-                        for (int g = 0; g < p.kb; ++g) {
-                            if (!fwait(full0 + 8 * slot, phase, p)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t sw = sbase + slot * kBox;
+                        for (int h = 0; ok && h < p.nh; ++h) {
+                            for (int k2 = 0; k2 < kChunk / 64; ++k2) {
+                                if (!fwait(full0 + 8 * slot, phase, p)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint32_t sw = sbase + slot * kBox;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_bf16(tmem_base + 64 * g, smem_desc(sa + kk * 32, 16, 1024),
-                                          smem_desc(sw + kk * 32, 16, 1024), p.idesc,
-                                          (c > kLag || kk > 0) ? 1u : 0u);
-                            umma_commit(empty0 + 8 * slot);
-                            if (++slot == kSlots) {
-                                slot = 0;
-                                phase ^= 1u;
+                                for (int kk = 0; kk < 4; ++kk)
+                                    umma_bf16(tmem_base + 128 * h, smem_desc(sa + k2 * kAtom + kk * 32, 16, 1024),
+                                              smem_desc(sw + kk * 32, 16, 1024), p.idesc,
+                                              (c > kLag || k2 > 0 || kk > 0) ? 1u : 0u);
+                                umma_commit(empty0 + 8 * slot);
+                                if (++slot == kSlots) {
+                                    slot = 0;
+                                    phase ^= 1u;
+                                }
                             }
                         }
                         if (!ok) break;
@@ -328,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 const int cg = cgb + c, b = cg % kNB;
                 const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                 const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
-                uint4 bias[8];  // the chunk's 64 b1 values, fetched while the accumulator fills
+                uint4 bias[kChunk / 8];  // the chunk's b1 values, fetched while the accumulator fills
                 if (p.has_bias) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) bias[k] = *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 8 * k);
+                    for (int k = 0; k < kChunk / 8; ++k) bias[k] = *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 8 * k);
                 }
                 ok = fwait(accf0 + 8 * b, use & 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
@@ -339,19 +344,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[2][32];
-                tmem_ld32(tmem_base + kAccCol + kChunk * b + lane_off, r[0]);
-                tmem_ld32(tmem_base + kAccCol + kChunk * b + 32 + lane_off, r[1]);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(acce0 + 8 * b);  // the column GEMM may reuse the accumulator
-                uint4 wa[2][4];
+                // the A buffer is free once the row GEMM of chunk cg - kNB is done
+                ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rowa = sbase + kOffA + b * kABytes + r_tile * 128u;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                for (int hh = 0; hh < kChunk / 32; ++hh) {  // 32 units at a time
                     const int u = u0 + 32 * hh;
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + kAccCol + kChunk * b + 32 * hh + lane_off, r);
+                    tmem_ld_wait();
+                    if (hh == kChunk / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(acce0 + 8 * b);  // the column GEMM may reuse the accumulator
+                    }
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[hh][j]);
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                     if (p.has_bias) {
 #pragma unroll
                         for (int g8 = 0; g8 < 4; ++g8) {
@@ -362,68 +374,84 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                             v[8 * g8 + 6] += bf16_lo(bw.w); v[8 * g8 + 7] += bf16_hi(bw.w);
                         }
                     }
+                    uint4 wa[4];
                     if (p.has_pre) {
-                        pack_bf16x32(v, wa[hh]);
-                        if (row_ok) store_row32(p.pre[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
+                        pack_bf16x32(v, wa);
+                        if (row_ok) store_row32(p.pre[i] + static_cast<long long>(row) * p.Fs + u, wa);
                     }
                     if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
-                    pack_bf16x32(v, wa[hh]);
-                    if (row_ok) store_row32(p.A[i] + static_cast<long long>(row) * p.Fs + u, wa[hh]);
-                }
-                // A into the row GEMM's operand buffer: row r_tile, the eight
-                // 16-byte chunks of its 128-byte line, 128-byte swizzle (chunk ^ (row & 7))
-                ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t rowa = sbase + kOffA + b * kABytes + r_tile * 128u;
+                    pack_bf16x32(v, wa);
+                    if (row_ok) store_row32(p.A[i] + static_cast<long long>(row) * p.Fs + u, wa);
+                    // A into the row GEMM's operand buffer: K-major atom hh / 2, row
+                    // r_tile, 16-byte chunks 4 (hh % 2) .. + 3 of its 128-byte line,
+                    // 128-byte swizzle (chunk ^ (row & 7))
+                    const uint32_t atom = rowa + static_cast<uint32_t>(hh >> 1) * kAtom;
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    st_shared_v4(rowa + ((static_cast<uint32_t>(jj) ^ (r_tile & 7u)) << 4), wa[jj >> 2][jj & 3]);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t c16 = 4u * static_cast<uint32_t>(hh & 1) + static_cast<uint32_t>(jj);
+                        st_shared_v4(atom + ((c16 ^ (r_tile & 7u)) << 4), wa[jj]);
+                    }
+                }
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
             }
             if (!ok) break;
+            int tj, tl;
+            tok_index(p, row0, tj, tl);
+            const __nv_bfloat16 *res_row =
+                p.has_res ? p.res[tj] + static_cast<long long>(row_ok ? tl + lane : tl) * p.H : nullptr;
+            // b2 and the residual of 32 output columns (the first piece's while Y accumulates,
+            // each later piece's alongside its TMEM load)
+            auto fetch = [&](int cb, uint4 (&bb)[4], uint4 (&rr)[4]) {
+                const int col = h * 128 + cb * 32;
+                const bool in = col < p.H;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    bb[k] = p.has_bias && in ? *reinterpret_cast<const uint4 *>(p.b2 + col + 8 * k) : make_uint4(0, 0, 0, 0);
+                    rr[k] = res_row && in && row_ok ? *reinterpret_cast<const uint4 *>(res_row + col + 8 * k)
+                                                    : make_uint4(0, 0, 0, 0);
+                }
+            };
+            uint4 bb[4], rr[4];
+            fetch(0, bb, rr);  // while the last row GEMMs run
             ok = fwait(yfull, it & 1, p);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            int tj, tl;
-            tok_index(p, row0, tj, tl);
+#pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 const int col = h * 128 + cb * 32;
                 if (col >= p.H) break;
+                if (cb > 0) fetch(cb, bb, rr);  // in flight with the TMEM load
                 uint32_t r[32];
                 tmem_ld32(tmem_base + col + lane_off, r);
                 tmem_ld_wait();
-                if (!block_ok) continue;
-                float v[32];
+                if (block_ok) {
+                    float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (p.has_bias) {
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (p.has_bias) {
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        float bb[8];
-                        load_bf16x8(p.b2 + col + 8 * g8, bb);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += bb[j];
+                        for (int k = 0; k < 4; ++k) {
+                            v[8 * k + 0] += bf16_lo(bb[k].x); v[8 * k + 1] += bf16_hi(bb[k].x);
+                            v[8 * k + 2] += bf16_lo(bb[k].y); v[8 * k + 3] += bf16_hi(bb[k].y);
+                            v[8 * k + 4] += bf16_lo(bb[k].z); v[8 * k + 5] += bf16_hi(bb[k].z);
+                            v[8 * k + 6] += bf16_lo(bb[k].w); v[8 * k + 7] += bf16_hi(bb[k].w);
+                        }
                     }
-                }
-                if (p.drop.on) dropout32(p.drop, row, col, row_ok, v);
-                if (p.has_res) {
-                    const __nv_bfloat16 *res =
-                        p.res[tj] + static_cast<long long>(row_ok ? tl + lane : tl) * p.H + col;
+                    if (p.drop.on) dropout32(p.drop, row, col, row_ok, v);
+                    if (res_row) {
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        float rr[8];
-                        load_bf16x8_guarded(res + 8 * g8, row_ok, rr);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[8 * g8 + j] += rr[j];
+                        for (int k = 0; k < 4; ++k) {
+                            v[8 * k + 0] += bf16_lo(rr[k].x); v[8 * k + 1] += bf16_hi(rr[k].x);
+                            v[8 * k + 2] += bf16_lo(rr[k].y); v[8 * k + 3] += bf16_hi(rr[k].y);
+                            v[8 * k + 4] += bf16_lo(rr[k].z); v[8 * k + 5] += bf16_hi(rr[k].z);
+                            v[8 * k + 6] += bf16_lo(rr[k].w); v[8 * k + 7] += bf16_hi(rr[k].w);
+                        }
                     }
+                    uint4 w[4];
+                    pack_bf16x32(v, w);
+                    if (row_ok) store_row32(p.Y[tj] + static_cast<long long>(tl + lane) * p.H + col, w);
                 }
-                uint4 w[4];
-                pack_bf16x32(v, w);
-                if (row_ok) store_row32(p.Y[tj] + static_cast<long long>(tl + lane) * p.H + col, w);
             }
             tc_fence_before();
             mbar_arrive(yempty);
@@ -443,8 +471,8 @@ void set_fused_fwd_mode(int mode) { g_fused_mode.store(mode); }
 int fused_fwd_mode() { return g_fused_mode.load(); }
 
 bool fused_fwd_supported(int H, int Fs, int act, int dtype) {
-    return dtype == TP_DT_BF16 && act != TP_ACT_SWIGLU && H >= 64 && H <= fm::kMaxH && H % 64 == 0 && Fs >= 64 &&
-           Fs % 64 == 0;
+    return dtype == TP_DT_BF16 && act != TP_ACT_SWIGLU && H >= 64 && H <= fm::kMaxH && H % 64 == 0 &&
+           Fs >= fm::kChunk && Fs % fm::kChunk == 0;
 }
 
 tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
@@ -465,8 +493,8 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
         prm.res[j] = f.has_res ? static_cast<const __nv_bfloat16 *>(f.R[j]) : nullptr;
     }
     for (int i = 0; i < f.T; ++i) {
-        tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, 64, false);
-        if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 64, false);
+        tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, kChunk, false);
+        if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 128, false);
         if (s != TP_OK) return s;
         prm.A[i] = static_cast<__nv_bfloat16 *>(f.A[i]);
         prm.pre[i] = f.has_pre ? static_cast<__nv_bfloat16 *>(f.pre[i]) : nullptr;
@@ -495,6 +523,7 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     prm.cps = f.Fs / kChunk;
     prm.nc = f.T * prm.cps;
     prm.kb = f.H / 64;
+    prm.nh = (f.H + 127) / 128;
     // fp32 accumulator (bit 4), bf16 A and B (bits 7-9, 10-12), both K-major,
     // N/8 at bit 17, M/16 at bit 24
     prm.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kChunk >> 3) << 17) | (uint32_t(kRows >> 4) << 24);
