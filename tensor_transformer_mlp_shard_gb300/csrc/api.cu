@@ -558,10 +558,11 @@ static Fp8Layout fp8_layout(const tp_mlp_desc *d) {
 }
 
 // Tail-split scratch of the MLP's pair GEMMs (row forward, column dgrad,
-// both weight gradients): the largest any of them may use.  It depends on
-// the GEMM settings and the device, so it comes after everything else in a
-// workspace: validation asks only for the part before it, and a GEMM splits
-// its tail only when the scratch a caller's workspace leaves is large enough.
+// both weight gradients) and of the fused forward's even split: the largest
+// any of them may use.  It depends on the GEMM settings and the device, so it
+// comes after everything else in a workspace: validation asks only for the
+// part before it, and a kernel uses it only when the scratch a caller's
+// workspace leaves is large enough.
 static size_t tail_scratch_bytes(const tp_mlp_desc *d) {
     if (d->dtype == TP_DT_F32) return 0;  // the fp32 engine does not split
     const Dims x = dims_of(d);
@@ -571,6 +572,7 @@ static size_t tail_scratch_bytes(const tp_mlp_desc *d) {
     r = std::max(r, tc_tail_bytes(x.M, x.H, 1, x.T, gw, f8));
     r = std::max(r, tc_tail_bytes(x.H, x.Fs, x.T, 1, x.M, f8));
     r = std::max(r, tc_tail_bytes(gw, x.H, x.T, 1, x.M, f8));
+    if (fused_fwd_supported(x.H, x.Fs, d->act, d->dtype)) r = std::max(r, fused_fwd_scratch_bytes(x.M));
     return align256(r);
 }
 
@@ -1005,6 +1007,8 @@ static tp_status mlp_fwd_core(const tp_mlp_desc *d, const void *const *X, const 
             f.drop_seed = drop->seed;
             f.drop_mask = drop->mask;
         }
+        f.scratch = tail.p;
+        f.scratch_bytes = tail.n;
         return launch_fused_mlp_fwd(f, st);
     }
     TRY(column_fwd(d, X, W1, d->has_bias ? b1 : nullptr, A, pre, st));

@@ -62,6 +62,7 @@ constexpr int kOffBar = kOffA + kNB * kABytes;
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment slack
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 384
+constexpr int kPartF4 = 4 * 8 * 32;  // one warp's parked sums: 32 rows x 128 columns fp32, in float4
 static_assert(2 * kSlots + 5 + 4 * kNB <= 64, "barriers overlap the TMEM address slot");
 static_assert(kAccCol + kNB * kChunk <= kTmemCols, "column accumulators beyond TMEM");
 static_assert(kLag <= kNB, "the row GEMM must not lag the column GEMM by more than a buffer cycle");
@@ -82,6 +83,14 @@ struct FusedParams {
     int M, H, Fs, T, act, has_bias, has_res, has_pre;
     int m_tiles, cps, nc, kb;  // chunks per shard, chunks per tile (T * cps), H / 64
     int nh;                    // 128-column halves of the output (H / 128 rounded up)
+    // Even split: CTA b takes the (tile, chunk position) units
+    // [b W / G, (b + 1) W / G) of the W = m_tiles * nc in tile-major order
+    // (0: CTA b takes whole tiles b, b + G, ...).  A tile cut at a range
+    // boundary is finished by whichever of its two CTAs gets there second.
+    int split;
+    long long work;
+    float *part;         // [G][8 warps][4096] fp32 output slices of the cut tiles
+    unsigned *part_cnt;  // [G][8] arrivals per cut tile and warp, then [G][8] ready flags (zeroed)
     uint32_t idesc;            // bf16 x bf16 -> fp32, both K-major, M = 128, N = 64
     int *status;
     unsigned *abort_word;
@@ -112,6 +121,53 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, const Fused
 __device__ __forceinline__ int chunk_at(const FusedParams &p, int t, int c) {
     const int ch = c + t % p.nc;
     return ch < p.nc ? ch : ch - p.nc;
+}
+
+// The k-th run of this CTA's work: chunk positions [c0, c1) of token tile t.
+// With the even split a CTA's range holds at least nc units (the host takes
+// it only with more tiles than CTAs), so a tile is cut at most once: the
+// first run of CTA b may start inside a tile (c0 > 0) and the last run of
+// CTA b - 1 then ends at the same position (c1 < nc).
+__device__ __forceinline__ bool segment(const FusedParams &p, int k, int &t, int &c0, int &c1) {
+    if (!p.split) {
+        t = blockIdx.x + k * gridDim.x;
+        c0 = 0;
+        c1 = p.nc;
+        return t < p.m_tiles;
+    }
+    const long long s = p.work * blockIdx.x / gridDim.x, e = p.work * (blockIdx.x + 1) / gridDim.x;
+    const long long u = k == 0 ? s : (s / p.nc + k) * p.nc;
+    if (u >= e) return false;
+    t = static_cast<int>(u / p.nc);
+    const long long base = static_cast<long long>(t) * p.nc;
+    c0 = static_cast<int>(u - base);
+    c1 = static_cast<int>(e - base < p.nc ? e - base : p.nc);
+    return true;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *a) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned *a, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// bounded wait for a flag another CTA of this launch sets
+__device__ __forceinline__ bool flag_wait(const unsigned *f, const FusedParams &p) {
+    if (ld_acquire_u32(f) != 0u) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ld_acquire_u32(f) != 0u) return true;
+        if ((n & 63u) == 0) {
+            if (*reinterpret_cast<volatile unsigned *>(p.abort_word) == p.launch_id) return false;
+            if (global_timer_ns() - t0 > p.wait_limit_ns) {
+                raise_device_error(p.status, p.abort_word, p.launch_id, TP_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
 }
 
 // token shard and local row of global row `row0`
@@ -192,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 }
                 return true;
             };
-            int it = 0;
-            for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it) {
+            int t, c0, c1;
+            for (int it = 0; ok && segment(p, it, t, c0, c1); ++it) {
                 int tj, tl;
                 tok_index(p, t * kRows, tj, tl);
                 if (!fwait(xempty, (it & 1) ^ 1u, p)) break;
@@ -204,12 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     tma_load_2d(sbase + kOffX + kb * kRows * 128, &p.mapX[tj], xfull, kb * 64, tl);
                 // boxes in the order the MMA warp consumes them; position c of
                 // tile t holds chunk (c + t) mod nc
-                for (int c = 0; ok && c < p.nc + kLag; ++c) {
-                    if (c < p.nc) {
+                for (int c = c0; ok && c < c1 + kLag; ++c) {
+                    if (c < c1) {
                         const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                         for (int kb = 0; ok && kb < p.kb; ++kb) ok = load_box(&p.mapW1[i], kb * 64, u0);
                     }
-                    if (ok && c >= kLag) {
+                    if (ok && c - kLag >= c0) {
                         const int ch = chunk_at(p, t, c - kLag), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                         for (int h = 0; ok && h < p.nh; ++h)
                             for (int k2 = 0; ok && k2 < kChunk / 64; ++k2)
@@ -228,18 +284,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             int slot = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int it = 0, cgb = 0;
-            for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it, cgb += p.nc) {
-                for (int c = 0; ok && c < p.nc + kLag; ++c) {
-                    if (c < p.nc) {
+            int cgb = 0, t, c0, c1;  // cgb: chunks of earlier runs (accumulator and A buffer turns)
+            for (int it = 0; ok && segment(p, it, t, c0, c1); ++it, cgb += c1 - c0) {
+                for (int c = c0; ok && c < c1 + kLag; ++c) {
+                    if (c < c1) {
                         // column GEMM of chunk c: acc1[b] = X_tile W1 chunk^T (K = H)
-                        const int cg = cgb + c, b = cg % kNB;
+                        const int cg = cgb + c - c0, b = cg % kNB;
                         const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                         if (!fwait(acce0 + 8 * b, (use & 1u) ^ 1u, p)) {
                             ok = false;
                             break;
                         }
-                        if (c == 0 && !fwait(xfull, it & 1, p)) {
+                        if (c == c0 && !fwait(xfull, it & 1, p)) {
                             ok = false;
                             break;
                         }
@@ -264,17 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         }
                         if (!ok) break;
                         umma_commit(accf0 + 8 * b);
-                        if (c == p.nc - 1) umma_commit(xempty);  // the tile's last read of X
+                        if (c == c1 - 1) umma_commit(xempty);  // the run's last read of X
                     }
-                    if (c >= kLag) {
+                    if (c - kLag >= c0) {
                         // row GEMM of chunk c - kLag: Y[:, 128h..] += A W2 chunk^T (K = 128)
-                        const int cg = cgb + c - kLag, b = cg % kNB;
+                        const int cg = cgb + c - kLag - c0, b = cg % kNB;
                         const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                         if (!fwait(af0 + 8 * b, use & 1u, p)) {
                             ok = false;
                             break;
                         }
-                        if (c == kLag && !fwait(yempty, (it & 1) ^ 1u, p)) {
+                        if (c == c0 + kLag && !fwait(yempty, (it & 1) ^ 1u, p)) {
                             ok = false;
                             break;
                         }
@@ -292,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                                 for (int kk = 0; kk < 4; ++kk)
                                     umma_bf16(tmem_base + 128 * h, smem_desc(sa + k2 * kAtom + kk * 32, 16, 1024),
                                               smem_desc(sw + kk * 32, 16, 1024), p.idesc,
-                                              (c > kLag || k2 > 0 || kk > 0) ? 1u : 0u);
+                                              (c > c0 + kLag || k2 > 0 || kk > 0) ? 1u : 0u);
                                 umma_commit(empty0 + 8 * slot);
                                 if (++slot == kSlots) {
                                     slot = 0;
@@ -322,15 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         const int h = (warp - 2) >> 2;     // group: chunks with buffer h; output columns 128h..
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t r_tile = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
-        int it = 0, cgb = 0;
+        int cgb = 0, t, c0, c1;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.m_tiles; t += gridDim.x, ++it, cgb += p.nc) {
+        for (int it = 0; ok && segment(p, it, t, c0, c1); ++it, cgb += c1 - c0) {
             const int row0 = t * kRows + q * 32;
             const int row = row0 + lane;
             const bool block_ok = row0 < p.M;  // warp-uniform
             const bool row_ok = row < p.M;
-            for (int c = (cgb & 1) == h ? 0 : 1; c < p.nc; c += 2) {
-                const int cg = cgb + c, b = cg % kNB;
+            for (int c = c0 + ((cgb & 1) == h ? 0 : 1); c < c1; c += 2) {
+                const int cg = cgb + c - c0, b = cg % kNB;
                 const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                 const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
                 uint4 bias[kChunk / 8];  // the chunk's b1 values, fetched while the accumulator fills
@@ -417,6 +473,44 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             ok = fwait(yfull, it & 1, p);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            // A tile cut between two CTAs: the first of them to get here parks
+            // its raw sums (this warp's 32 rows x 128 columns) and moves on; the
+            // second adds them to its own and runs the epilogue.  The sum of the
+            // two parts is the same whichever arrives first.
+            int other = -1;  // the parked slot to add, if this warp arrived second
+            if (p.split && (c0 > 0 || c1 < p.nc)) {
+                const int slot = (c0 > 0 ? blockIdx.x : blockIdx.x + 1) * kEpiWarps + (warp - 2);
+                float4 *mine = reinterpret_cast<float4 *>(p.part) + static_cast<size_t>(slot) * kPartF4;
+                unsigned *ready = p.part_cnt + gridDim.x * kEpiWarps + slot;
+                unsigned prev = 0;
+                if (lane == 0) prev = atomicAdd(p.part_cnt + slot, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == 0) {
+#pragma unroll 1
+                    for (int cb = 0; cb < 4; ++cb) {
+                        if (h * 128 + cb * 32 >= p.H) break;
+                        uint32_t r[32];
+                        tmem_ld32(tmem_base + h * 128 + cb * 32 + lane_off, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            mine[(cb * 8 + k) * 32 + lane] =
+                                make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                            __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                    }
+                    tc_fence_before();
+                    mbar_arrive(yempty);
+                    __threadfence();  // every lane's slice is visible before the flag
+                    __syncwarp();
+                    if (lane == 0) st_release_u32(ready, 1u);
+                    continue;
+                }
+                // the first CTA claimed its arrival before this one, so it is
+                // running and its flag comes without waiting on anything else
+                ok = flag_wait(ready, p);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                other = slot;
+            }
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 const int col = h * 128 + cb * 32;
@@ -429,6 +523,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (other >= 0) {  // the other CTA's part: plain loads, ordered after the flag's acquire
+                        const float4 *src = reinterpret_cast<const float4 *>(p.part) +
+                                            static_cast<size_t>(other) * kPartF4 + cb * 8 * 32 + lane;
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; k4 += 4) {
+                            float4 o[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) o[k] = src[(k4 + k) * 32];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                v[4 * (k4 + k) + 0] += o[k].x; v[4 * (k4 + k) + 1] += o[k].y;
+                                v[4 * (k4 + k) + 2] += o[k].z; v[4 * (k4 + k) + 3] += o[k].w;
+                            }
+                        }
+                    }
                     if (p.has_bias) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -473,6 +582,17 @@ int fused_fwd_mode() { return g_fused_mode.load(); }
 bool fused_fwd_supported(int H, int Fs, int act, int dtype) {
     return dtype == TP_DT_BF16 && act != TP_ACT_SWIGLU && H >= 64 && H <= fm::kMaxH && H % 64 == 0 &&
            Fs >= fm::kChunk && Fs % fm::kChunk == 0;
+}
+
+// Bytes of scratch the even split of an M-token forward takes (0: it keeps
+// whole tiles per CTA, because the tiles fill a whole number of rounds or
+// fewer than one): the parked sums of one cut tile per CTA and two words per
+// cut tile and warp.
+size_t fused_fwd_scratch_bytes(long long M) {
+    using namespace fm;
+    const long long tiles = (M + kRows - 1) / kRows, g = num_sms();
+    if (tiles <= g || tiles % g == 0) return 0;
+    return static_cast<size_t>(g) * kEpiWarps * (kPartF4 * sizeof(float4) + 2 * sizeof(unsigned));
 }
 
 tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
@@ -550,6 +670,17 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
         }
     }
     const int grid = prm.m_tiles < num_sms() ? prm.m_tiles : num_sms();
+    const size_t need = fused_fwd_scratch_bytes(f.M);
+    if (need > 0 && f.scratch && f.scratch_bytes >= need && (reinterpret_cast<uintptr_t>(f.scratch) & 15u) == 0) {
+        prm.split = 1;
+        prm.work = static_cast<long long>(prm.m_tiles) * prm.nc;
+        prm.part = static_cast<float *>(f.scratch);
+        prm.part_cnt = reinterpret_cast<unsigned *>(static_cast<char *>(f.scratch) +
+                                                    static_cast<size_t>(grid) * kEpiWarps * kPartF4 * sizeof(float4));
+        s = cuda_check(cudaMemsetAsync(prm.part_cnt, 0, static_cast<size_t>(grid) * kEpiWarps * 2 * sizeof(unsigned), st),
+                       "cudaMemsetAsync(fused split flags)");
+        if (s != TP_OK) return s;
+    }
     launch_begin("fused_mlp_fwd", st);
     fused_mlp_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(prm);
     cudaError_t e = cudaGetLastError();

@@ -192,7 +192,10 @@ struct FusedPlan {
     float drop_scale = 1.0f;
     uint64_t drop_seed = 0;
     uint32_t *drop_mask = nullptr;  // as GemmPlan's drop_mask (ceil(H/32) words per row)
+    void *scratch = nullptr;        // the workspace's scratch: the even split of the work over the SMs
+    size_t scratch_bytes = 0;       // runs only when it holds fused_fwd_scratch_bytes(M)
 };
+size_t fused_fwd_scratch_bytes(long long M);
 void set_fused_fwd_mode(int mode);  // TP_FUSED_*
 int fused_fwd_mode();
 bool fused_fwd_supported(int H, int Fs, int act, int dtype);  // shapes the fused kernel takes

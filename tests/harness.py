@@ -96,7 +96,8 @@ class MlpRun:
 
     def fwd(self, with_workspace=True):
         """tp_mlp_fwd_ws with the run's workspace (for bf16 it holds only the
-        row GEMM's tail-split scratch), or plain tp_mlp_fwd."""
+        scratch of the row GEMM's tail split and of the fused forward's even
+        split), or plain tp_mlp_fwd."""
         ws = self.ws if with_workspace or self.lay.dtype == "fp8" else None
         self.lay.fwd(self.X, self.W1, self.b1, self.W2, self.b2, self.Y, self.pre, self.A, workspace=ws)
 

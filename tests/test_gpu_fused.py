@@ -10,6 +10,9 @@ C ABI.
 * Against the two-kernel path on the same inputs: both accumulate the same
   products in fp32 in 64-element K steps, so pre and A agree bit for bit and
   Y to within fp32 reassociation of the chunk sums.
+* The even split of the work over the SMs (taken with more token tiles than
+  SMs, not a whole number of rounds, and the workspace's scratch) against the
+  whole-tile schedule of the same kernel (no workspace).
 """
 import numpy as np
 import pytest
@@ -39,6 +42,10 @@ CASES = [
     (1024, 192, 1024, 4, "gelu_tanh", True, True, True),
     (128, 256, 256, 1, "gelu_tanh", False, True, False),
     (40000, 256, 1024, 2, "gelu_tanh", True, True, False),
+    # more token tiles than SMs, not a whole number of rounds: the work is cut
+    # evenly over the CTAs and a cut tile is finished by the second of its two
+    (20736, 128, 768, 3, "gelu_tanh", True, True, True),
+    (20485, 64, 512, 4, "none", False, False, False),
 ]
 
 
@@ -75,6 +82,30 @@ def test_fused_forward_matches_oracle_and_two_kernel_path(tp, M, H, F, T, act, b
     assert d <= 2 ** -7, d
 
 
+@pytest.mark.parametrize("M,H,F,T,sp", [(40000, 256, 1024, 2, False), (20736, 128, 768, 3, True)])
+def test_fused_even_split_matches_whole_tiles(tp, M, H, F, T, sp):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = (M + 127) // 128
+    assert tiles > sms and tiles % sms, "the case must cut tiles"
+    lay = tp.TPMLP(S=M // T if sp else M, B=T if sp else 1, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16",
+                   has_bias=True, residual=True, seq_parallel=sp)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    tp.set_fused_fwd("on")
+    runs = []
+    for ws in (True, False):
+        run = MlpRun(lay, t)
+        run.fwd(with_workspace=ws)
+        assert status_ok(tp, lay)
+        runs.append(run)
+    split, whole = runs
+    for i in range(T):
+        assert torch.equal(split.pre[i], whole.pre[i]), i
+        assert torch.equal(split.A[i], whole.A[i]), i
+    d = rel_err(split.gathered(split.Y), whole.gathered(whole.Y).astype(np.float64))
+    assert d <= 2 ** -7, d
+    tp.set_fused_fwd("auto")
+
+
 def test_fused_forward_feeds_the_backward(tp):
     """The backward after a fused forward equals the backward after the
     two-kernel forward (it reads pre and A, which are bit-identical)."""
@@ -106,11 +137,14 @@ def test_fused_forward_not_taken_outside_its_shapes(tp):
     tp.set_fused_fwd("auto")
 
 
-def test_fused_layer_forward_with_dropout(tp):
+@pytest.mark.parametrize("M", [300, 20000])
+def test_fused_layer_forward_with_dropout(tp, M):
     """The sub-block's forward on the fused kernel (dropout in its output
-    epilogue) against the layer oracle."""
+    epilogue) against the layer oracle; at 20000 tokens the work is cut
+    evenly over the SMs, so the cut tiles' dropout runs in the CTA that
+    finishes them."""
     from test_gpu_layer import LayerRun, layer_inputs, SEED, _p32
-    M, H, F, T, p = 300, 256, 1024, 2, 0.1
+    H, F, T, p = 256, 1024, 2, 0.1
     lay = tp.TPLayer(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, dropout_p=p)
     t = layer_inputs(M, H, F, T, "gelu_tanh", "bf16", True)
     tp.set_fused_fwd("on")
