@@ -72,8 +72,8 @@ struct FusedParams {
     CUtensorMap mapX[kMaxShards];    // X token shards, boxes [128 rows x 64], 128-byte swizzle
     CUtensorMap mapW1[kMaxShards];   // W1_i [Fs, H], boxes [128 units x 64]
     CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [128 rows of H x 64 units]
+    CUtensorMap mapA[kMaxShards];    // A_i [M, Fs], boxes [128 tokens x 64 units] stored from shared memory
     __nv_bfloat16 *pre[kMaxShards];  // pre_i [M, Fs] (or null)
-    __nv_bfloat16 *A[kMaxShards];    // A_i [M, Fs]
     __nv_bfloat16 *Y[kMaxShards];    // Y token shards [rows_split or M, H]
     const __nv_bfloat16 *b1[kMaxShards];
     const __nv_bfloat16 *b2;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             mbar_init(accf0 + 8 * b, 1);
             mbar_init(acce0 + 8 * b, kEpiThreads / 2);  // one epilogue group per buffer
             mbar_init(af0 + 8 * b, kEpiThreads / 2);
-            mbar_init(ae0 + 8 * b, 1);
+            mbar_init(ae0 + 8 * b, 2);  // the row GEMM and the bulk store of A have read it
         }
         mbar_init(yfull, 1);
         mbar_init(yempty, kEpiThreads);
@@ -378,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         const int h = (warp - 2) >> 2;     // group: chunks with buffer h; output columns 128h..
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t r_tile = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
+        const bool elect = lane == 0 && ((warp - 2) & 3) == 0;          // issues the group's bulk stores
         int cgb = 0, t, c0, c1;
         bool ok = true;
         for (int it = 0; ok && segment(p, it, t, c0, c1); ++it, cgb += c1 - c0) {
@@ -400,7 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     break;
                 }
                 tc_fence_after();
-                // the A buffer is free once the row GEMM of chunk cg - kNB is done
+                // the A buffer is free once the row GEMM of chunk cg - kNB is done and
+                // the bulk store of that chunk's A has read it
+                if (elect && use > 0) {
+                    bulk_wait_read<0>();
+                    mbar_arrive(ae0 + 8 * b);
+                }
                 ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -437,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
                     pack_bf16x32(v, wa);
-                    if (row_ok) store_row32(p.A[i] + static_cast<long long>(row) * p.Fs + u, wa);
-                    // A into the row GEMM's operand buffer: K-major atom hh / 2, row
+                    // A into the row GEMM's operand buffer (which a bulk store then copies
+                    // to A_i, clipping rows past M): K-major atom hh / 2, row
                     // r_tile, 16-byte chunks 4 (hh % 2) .. + 3 of its 128-byte line,
                     // 128-byte swizzle (chunk ^ (row & 7))
                     const uint32_t atom = rowa + static_cast<uint32_t>(hh >> 1) * kAtom;
@@ -450,6 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 }
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
+                if (elect) {  // once the group's 128 rows are in, A goes to HBM in two boxes
+                    ok = fwait(af0 + 8 * b, use & 1u, p);
+                    if (ok) {
+                        const uint32_t sa = sbase + kOffA + b * kABytes;
+                        for (int k2 = 0; k2 < kChunk / 64; ++k2) tma_store_2d(&p.mapA[i], sa + k2 * kAtom, u0 + 64 * k2, t * kRows);
+                        bulk_commit();
+                    }
+                }
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
             }
             if (!ok) break;
             int tj, tl;
@@ -567,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         }
     }
 
+    if (warp >= 2 && lane == 0 && ((warp - 2) & 3) == 0) bulk_wait<0>();  // the group's A stores are done
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -615,8 +634,8 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     for (int i = 0; i < f.T; ++i) {
         tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, kChunk, false);
         if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 128, false);
+        if (s == TP_OK) s = tc::encode_map(&prm.mapA[i], f.A[i], f.M, f.Fs, 64, kRows, false);
         if (s != TP_OK) return s;
-        prm.A[i] = static_cast<__nv_bfloat16 *>(f.A[i]);
         prm.pre[i] = f.has_pre ? static_cast<__nv_bfloat16 *>(f.pre[i]) : nullptr;
         prm.b1[i] = f.has_bias ? static_cast<const __nv_bfloat16 *>(f.b1[i]) : nullptr;
     }
