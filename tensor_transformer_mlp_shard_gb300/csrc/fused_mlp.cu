@@ -63,7 +63,7 @@ constexpr int kSmemBytes = kOffBar + 1024 + 1024;  // + barriers, + alignment sl
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 256;  // column-GEMM accumulators at TMEM columns 256 and 384
 constexpr int kPartF4 = 4 * 8 * 32;  // one warp's parked sums: 32 rows x 128 columns fp32, in float4
-static_assert(2 * kSlots + 5 + 4 * kNB <= 64, "barriers overlap the TMEM address slot");
+static_assert(2 * kSlots + 5 + 5 * kNB <= 64, "barriers overlap the TMEM address slot");
 static_assert(kAccCol + kNB * kChunk <= kTmemCols, "column accumulators beyond TMEM");
 static_assert(kLag <= kNB, "the row GEMM must not lag the column GEMM by more than a buffer cycle");
 static_assert(kSmemBytes <= 232448, "shared memory above the 227 KB a block may use");
@@ -74,7 +74,7 @@ struct FusedParams {
     CUtensorMap mapW2[kMaxShards];   // W2_i [H, Fs], boxes [128 rows of H x 64 units]
     CUtensorMap mapA[kMaxShards];    // A_i [M, Fs], boxes [128 tokens x 64 units] stored from shared memory
     __nv_bfloat16 *pre[kMaxShards];  // pre_i [M, Fs] (or null)
-    __nv_bfloat16 *Y[kMaxShards];    // Y token shards [rows_split or M, H]
+    CUtensorMap mapY[kMaxShards];    // Y token shards [rows_split or M, H], boxes [32 tokens x 64], stored
     const __nv_bfloat16 *b1[kMaxShards];
     const __nv_bfloat16 *b2;
     const __nv_bfloat16 *res[kMaxShards];
@@ -191,13 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 64);  // after the 2 * kSlots + 5 + 4 * kNB barriers
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 64);  // after the 2 * kSlots + 5 + 5 * kNB barriers
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * kSlots;
     const uint32_t xfull = empty0 + 8 * kSlots, xempty = xfull + 8;
     const uint32_t accf0 = xempty + 8, acce0 = accf0 + 8 * kNB;  // column-GEMM accumulator full / drained
     const uint32_t af0 = acce0 + 8 * kNB, ae0 = af0 + 8 * kNB;    // A buffer written / consumed
     const uint32_t yfull = ae0 + 8 * kNB, yempty = yfull + 8, drain = yempty + 8;
+    const uint32_t bufr0 = drain + 8;  // per epilogue group: the bulk stores from its buffer have read it
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr uint32_t kEpiThreads = 32 * kEpiWarps;
 
@@ -212,11 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             mbar_init(accf0 + 8 * b, 1);
             mbar_init(acce0 + 8 * b, kEpiThreads / 2);  // one epilogue group per buffer
             mbar_init(af0 + 8 * b, kEpiThreads / 2);
-            mbar_init(ae0 + 8 * b, 2);  // the row GEMM and the bulk store of A have read it
+            mbar_init(ae0 + 8 * b, 1);
         }
         mbar_init(yfull, 1);
         mbar_init(yempty, kEpiThreads);
         mbar_init(drain, 1);
+        for (int g = 0; g < kNB; ++g) mbar_init(bufr0 + 8 * g, kEpiThreads / 2);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -379,6 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t r_tile = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
         const bool elect = lane == 0 && ((warp - 2) & 3) == 0;          // issues the group's bulk stores
+        const uint32_t buf = sbase + kOffA + h * kABytes;  // the group's A buffer (= buffer h), Y staging too
+        uint32_t nrel = 0;
+        // Before the group writes its buffer: the bulk stores issued from it have
+        // read it.  A warp's lane 0 waits for its own (each warp stages and stores
+        // its 32 rows of Y; the elected thread also the whole buffer's A), then
+        // the group's 128 threads meet on its barrier.
+        auto release = [&]() -> bool {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            mbar_arrive(bufr0 + 8 * h);
+            return fwait(bufr0 + 8 * h, nrel++ & 1u, p);
+        };
         int cgb = 0, t, c0, c1;
         bool ok = true;
         for (int it = 0; ok && segment(p, it, t, c0, c1); ++it, cgb += c1 - c0) {
@@ -390,35 +404,37 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 const int cg = cgb + c - c0, b = cg % kNB;
                 const uint32_t use = static_cast<uint32_t>(cg) / kNB;
                 const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
-                uint4 bias[kChunk / 8];  // the chunk's b1 values, fetched while the accumulator fills
-                if (p.has_bias) {
+                // b1 of one 32-unit piece: the first piece's while the accumulator
+                // fills, each next piece's while the current one is computed
+                auto fetch_b1 = [&](int hh, uint4 (&bw)[4]) {
 #pragma unroll
-                    for (int k = 0; k < kChunk / 8; ++k) bias[k] = *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 8 * k);
-                }
+                    for (int k = 0; k < 4; ++k)
+                        bw[k] = p.has_bias ? *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 32 * hh + 8 * k)
+                                           : make_uint4(0, 0, 0, 0);
+                };
+                uint4 bcur[4], bnext[4];
+                fetch_b1(0, bcur);
                 ok = fwait(accf0 + 8 * b, use & 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // the A buffer is free once the row GEMM of chunk cg - kNB is done and
-                // the bulk store of that chunk's A has read it
-                if (elect && use > 0) {
-                    bulk_wait_read<0>();
-                    mbar_arrive(ae0 + 8 * b);
-                }
-                ok = fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
+                // the A buffer is free once the bulk stores from it have read it and
+                // the row GEMM of chunk cg - kNB is done
+                ok = release() && fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
-                const uint32_t rowa = sbase + kOffA + b * kABytes + r_tile * 128u;
+                const uint32_t rowa = buf + r_tile * 128u;
 #pragma unroll
                 for (int hh = 0; hh < kChunk / 32; ++hh) {  // 32 units at a time
                     const int u = u0 + 32 * hh;
                     uint32_t r[32];
                     tmem_ld32(tmem_base + kAccCol + kChunk * b + 32 * hh + lane_off, r);
                     tmem_ld_wait();
+                    if (hh + 1 < kChunk / 32) fetch_b1(hh + 1, bnext);
                     if (hh == kChunk / 32 - 1) {
                         tc_fence_before();
                         mbar_arrive(acce0 + 8 * b);  // the column GEMM may reuse the accumulator
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     if (p.has_bias) {
 #pragma unroll
                         for (int g8 = 0; g8 < 4; ++g8) {
-                            const uint4 bw = bias[4 * hh + g8];
+                            const uint4 bw = bcur[g8];
                             v[8 * g8 + 0] += bf16_lo(bw.x); v[8 * g8 + 1] += bf16_hi(bw.x);
                             v[8 * g8 + 2] += bf16_lo(bw.y); v[8 * g8 + 3] += bf16_hi(bw.y);
                             v[8 * g8 + 4] += bf16_lo(bw.z); v[8 * g8 + 5] += bf16_hi(bw.z);
@@ -453,14 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         const uint32_t c16 = 4u * static_cast<uint32_t>(hh & 1) + static_cast<uint32_t>(jj);
                         st_shared_v4(atom + ((c16 ^ (r_tile & 7u)) << 4), wa[jj]);
                     }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) bcur[k] = bnext[k];
                 }
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
                 if (elect) {  // once the group's 128 rows are in, A goes to HBM in two boxes
                     ok = fwait(af0 + 8 * b, use & 1u, p);
                     if (ok) {
-                        const uint32_t sa = sbase + kOffA + b * kABytes;
-                        for (int k2 = 0; k2 < kChunk / 64; ++k2) tma_store_2d(&p.mapA[i], sa + k2 * kAtom, u0 + 64 * k2, t * kRows);
+                        for (int k2 = 0; k2 < kChunk / 64; ++k2) tma_store_2d(&p.mapA[i], buf + k2 * kAtom, u0 + 64 * k2, t * kRows);
                         bulk_commit();
                     }
                 }
@@ -491,6 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             ok = fwait(yfull, it & 1, p);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            // The group's output columns are staged in its buffer, free once the last
+            // row GEMM is done (which yfull says) and the bulk stores from it have
+            // read it; every warp of the group takes part, whatever it does next.
+            const int ycols = min(128, p.H - h * 128);
+            if (ycols > 0) {
+                ok = release();
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
             // A tile cut between two CTAs: the first of them to get here parks
             // its raw sums (this warp's 32 rows x 128 columns) and moves on; the
             // second adds them to its own and runs the epilogue.  The sum of the
@@ -577,15 +602,30 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     uint4 w[4];
                     pack_bf16x32(v, w);
-                    if (row_ok) store_row32(p.Y[tj] + static_cast<long long>(tl + lane) * p.H + col, w);
+                    const uint32_t atom = buf + r_tile * 128u + static_cast<uint32_t>(cb >> 1) * kAtom;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t c16 = 4u * static_cast<uint32_t>(cb & 1) + static_cast<uint32_t>(jj);
+                        st_shared_v4(atom + ((c16 ^ (r_tile & 7u)) << 4), w[jj]);
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(yempty);
+            if (ycols > 0 && block_ok) {  // this warp's 32 rows, staged: one bulk store per 64 columns
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int k2 = 0; k2 < ycols / 64; ++k2)
+                        tma_store_2d(&p.mapY[tj], buf + static_cast<uint32_t>(q * 32 * 128 + k2 * kAtom),
+                                     h * 128 + 64 * k2, tl);
+                    bulk_commit();
+                }
+            }
         }
     }
 
-    if (warp >= 2 && lane == 0 && ((warp - 2) & 3) == 0) bulk_wait<0>();  // the group's A stores are done
+    if (warp >= 2 && lane == 0) bulk_wait<0>();  // the epilogue warps' bulk stores are done
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -627,8 +667,8 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     const int tok_rows = f.rows_split ? f.rows_split : f.M;
     for (int j = 0; j < f.n_tok; ++j) {
         tp_status s = tc::encode_map(&prm.mapX[j], f.X[j], tok_rows, f.H, 64, kRows, false);
+        if (s == TP_OK) s = tc::encode_map(&prm.mapY[j], f.Y[j], tok_rows, f.H, 64, 32, false);
         if (s != TP_OK) return s;
-        prm.Y[j] = static_cast<__nv_bfloat16 *>(f.Y[j]);
         prm.res[j] = f.has_res ? static_cast<const __nv_bfloat16 *>(f.R[j]) : nullptr;
     }
     for (int i = 0; i < f.T; ++i) {
