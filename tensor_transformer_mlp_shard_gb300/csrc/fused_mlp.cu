@@ -420,13 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     break;
                 }
                 tc_fence_after();
-                // the A buffer is free once the bulk stores from it have read it and
-                // the row GEMM of chunk cg - kNB is done
-                ok = release() && fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
                 const uint32_t rowa = buf + r_tile * 128u;
 #pragma unroll
                 for (int hh = 0; hh < kChunk / 32; ++hh) {  // 32 units at a time
@@ -459,6 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
                     pack_bf16x32(v, wa);
+                    if (hh == 0) {
+                        // the A buffer is free once the bulk stores from it have read it and
+                        // the row GEMM of chunk cg - kNB is done (waited for only now, so
+                        // that the first piece is computed meanwhile)
+                        ok = release() && fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
+                        if (!__all_sync(0xffffffffu, ok)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     // A into the row GEMM's operand buffer (which a bulk store then copies
                     // to A_i, clipping rows past M): K-major atom hh / 2, row
                     // r_tile, 16-byte chunks 4 (hh % 2) .. + 3 of its 128-byte line,
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
 #pragma unroll
                     for (int k = 0; k < 4; ++k) bcur[k] = bnext[k];
                 }
+                if (!ok) break;
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
                 if (elect) {  // once the group's 128 rows are in, A goes to HBM in two boxes
