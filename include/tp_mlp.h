@@ -526,18 +526,21 @@ TP_API tp_status tp_set_max_gemm_pairs(int n);
 /* Forward of the MLP (and of the sub-block) as one fused kernel, for all
  * calls made after this one.  The fused kernel keeps a 128-token tile's
  * output [128 x H] in tensor memory and streams the F dimension through it
- * in 64-unit chunks: per chunk the column GEMM, bias and activation (pre and
+ * in 128-unit chunks: per chunk the column GEMM, bias and activation (pre and
  * A are still stored for the backward), then A goes from shared memory
  * straight into the row GEMM, so A is never read back from HBM.  It takes
  * bf16 with act = none or GeLU-tanh, H a multiple of 64 up to 256 and F/T a
- * multiple of 64; other problems always use the two-kernel path.
- * Streaming all of W1 and W2 through shared memory once per 128-token tile
- * keeps it slower than the two GEMM kernels (206 us against 136 us for 65536
- * tokens at H = 256, F = 1024, T = 2 on GB300), so TP_FUSED_AUTO (default)
- * and TP_FUSED_OFF run the two GEMM kernels and TP_FUSED_ON runs the fused
- * kernel for every problem it takes.  pre and A are bit-identical between the
- * paths; Y accumulates the same fp32 products in another order.  Returns
- * TP_ERR_ARG for an unknown mode. */
+ * multiple of 128; other problems always use the two-kernel path.  With a
+ * workspace (tp_mlp_fwd_ws, tp_layer_fwd) of the size the handle reports,
+ * the work is split evenly over the SMs when the token tiles spill over a
+ * whole number of rounds of the SMs by at most a quarter of a round.
+ * TP_FUSED_AUTO (default) runs the fused kernel for the problems it takes
+ * with at most ten 128-token tiles per SM, where it measured faster than the
+ * two GEMMs on GB300 (132 us against 155 us for 65536 tokens at H = 256,
+ * F = 1024, T = 2; 1.04x at 1536 tiles), and the two GEMM kernels otherwise;
+ * TP_FUSED_ON runs it for every problem it takes, TP_FUSED_OFF never.  pre and A are bit-identical between the paths; Y accumulates the
+ * same fp32 products in another order.  Returns TP_ERR_ARG for an unknown
+ * mode. */
 typedef enum { TP_FUSED_AUTO = 0, TP_FUSED_OFF = 1, TP_FUSED_ON = 2 } tp_fused_mode;
 TP_API tp_status tp_set_fused_fwd(int mode);
 

@@ -19,9 +19,12 @@
 // ring), warp 1 issues the MMAs (column GEMM of chunk c, then row GEMM of
 // chunk c - 2, so that the tensor core works while two epilogue groups turn
 // chunks c - 1 and c - 2 into A), warps 2-9 run the epilogues in two groups
-// that take alternate chunks and write pre, A and Y with direct 16-byte
-// stores (no staging: a chunk's epilogue is short, and waiting for bulk
-// stores to release staging buffers stretched it).  Every wait is bounded.
+// that take alternate chunks.  A group writes A into its shared-memory
+// operand buffer, from which one bulk tensor store per 64 units copies it to
+// HBM; the group's output columns of Y are staged in the same buffer at the
+// end of a tile and stored the same way, 32 rows per warp; pre goes out with
+// direct 16-byte stores (staging it too measured slower).  Every wait is
+// bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -229,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched with programmatic dependent launch: the set-up above overlaps the
+    // previous kernel, and nothing in global memory is touched before it is done
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -647,14 +654,17 @@ bool fused_fwd_supported(int H, int Fs, int act, int dtype) {
            Fs >= fm::kChunk && Fs % fm::kChunk == 0;
 }
 
-// Bytes of scratch the even split of an M-token forward takes (0: it keeps
-// whole tiles per CTA, because the tiles fill a whole number of rounds or
-// fewer than one): the parked sums of one cut tile per CTA and two words per
-// cut tile and warp.
+// Bytes of scratch the even split of an M-token forward takes: the parked
+// sums of one cut tile per CTA and two words per cut tile and warp.  0 (whole
+// tiles per CTA) unless the tiles spill over whole rounds of the SMs by at
+// most a quarter of a round: measured on GB300, the split won there (54
+// against 68 us at 1.09 rounds) and lost to whole tiles from about a third of
+// a round on (142 against 133 us at 3.37 rounds), because the even split
+// gives most CTAs one more run of chunks to start and drain.
 size_t fused_fwd_scratch_bytes(long long M) {
     using namespace fm;
     const long long tiles = (M + kRows - 1) / kRows, g = num_sms();
-    if (tiles <= g || tiles % g == 0) return 0;
+    if (tiles <= g || tiles % g == 0 || tiles % g > g / 4) return 0;
     return static_cast<size_t>(g) * kEpiWarps * (kPartF4 * sizeof(float4) + 2 * sizeof(unsigned));
 }
 
@@ -744,9 +754,18 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
                        "cudaMemsetAsync(fused split flags)");
         if (s != TP_OK) return s;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_on() ? 1 : 0;
     launch_begin("fused_mlp_fwd", st);
-    fused_mlp_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_mlp_fwd_kernel, prm);
     launch_end("fused_mlp_fwd", st);
     return cuda_check(e, "fused_mlp_fwd");
 }

@@ -160,6 +160,7 @@ void set_k_reverse(bool on);
 // rows of pair tiles per raster band of the pair GEMMs' tile order (0: default)
 void set_band_rows(int g);
 void set_pdl(bool on);
+bool pdl_on();  // kernels that take it are launched with programmatic dependent launch
 void set_max_gemm_pairs(int n);
 uint64_t tail_split_launches();  // pair GEMM launches that split their tail
 // Scratch bytes a pair GEMM of this shape (out M x N per problem, P problems,

@@ -191,6 +191,7 @@ void set_k_reverse(bool on) { tc::g_k_reverse.store(on); }
 void set_band_rows(int g) { tc::g_band_rows.store(g > 0 ? g : 0); }
 void set_max_gemm_pairs(int n) { tc::g_max_pairs.store(n > 0 ? n : 0); }
 void set_pdl(bool on) { tc::g_pdl.store(on); }
+bool pdl_on() { return tc::g_pdl.load(); }
 uint64_t tail_split_launches() { return tc::g_tail_launches.load(); }
 
 size_t tc_tail_bytes(int M, int N, int P, int S, int Kseg, bool fp8) {

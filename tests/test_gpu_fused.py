@@ -10,9 +10,10 @@ C ABI.
 * Against the two-kernel path on the same inputs: both accumulate the same
   products in fp32 in 64-element K steps, so pre and A agree bit for bit and
   Y to within fp32 reassociation of the chunk sums.
-* The even split of the work over the SMs (taken with more token tiles than
-  SMs, not a whole number of rounds, and the workspace's scratch) against the
-  whole-tile schedule of the same kernel (no workspace).
+* The even split of the work over the SMs (taken when the token tiles spill
+  over whole rounds of the SMs by at most a quarter of a round, and the
+  workspace's scratch is there) against the whole-tile schedule of the same
+  kernel (no workspace).
 """
 import numpy as np
 import pytest
@@ -42,7 +43,7 @@ CASES = [
     (1024, 192, 1024, 4, "gelu_tanh", True, True, True),
     (128, 256, 256, 1, "gelu_tanh", False, True, False),
     (40000, 256, 1024, 2, "gelu_tanh", True, True, False),
-    # more token tiles than SMs, not a whole number of rounds: the work is cut
+    # a few token tiles more than a whole number of rounds: the work is cut
     # evenly over the CTAs and a cut tile is finished by the second of its two
     (20736, 128, 768, 3, "gelu_tanh", True, True, True),
     (20485, 64, 512, 4, "none", False, False, False),
@@ -86,7 +87,7 @@ def test_fused_forward_matches_oracle_and_two_kernel_path(tp, M, H, F, T, act, b
 def test_fused_even_split_matches_whole_tiles(tp, M, H, F, T, sp):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tiles = (M + 127) // 128
-    assert tiles > sms and tiles % sms, "the case must cut tiles"
+    assert tiles > sms and 0 < tiles % sms <= sms // 4, "the case must cut tiles"
     lay = tp.TPMLP(S=M // T if sp else M, B=T if sp else 1, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16",
                    has_bias=True, residual=True, seq_parallel=sp)
     t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
@@ -135,6 +136,23 @@ def test_fused_forward_not_taken_outside_its_shapes(tp):
         assert tp.launch_count() - n0 == 2, kw
     assert status_ok(tp, lay)
     tp.set_fused_fwd("auto")
+
+
+def test_fused_forward_by_default_up_to_ten_tiles_per_sm(tp):
+    """TP_FUSED_AUTO takes the fused kernel for the shapes it takes with at
+    most ten 128-token tiles per SM, the two GEMMs beyond that and for the
+    shapes it does not take."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tp.set_fused_fwd("auto")
+    for M, H, F, fused in ((4096, 256, 1024, True), (128 * 10 * sms, 128, 512, True),
+                           (128 * (10 * sms + 1), 128, 512, False), (4096, 512, 1024, False)):
+        lay = tp.TPMLP(S=M, B=1, H=H, F=F, T=2, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+        t = mlp_inputs(M, H, F, 2, "gelu_tanh", "bf16", has_bias=True)
+        run = MlpRun(lay, t)
+        n0 = tp.launch_count()
+        run.fwd()
+        assert tp.launch_count() - n0 == (1 if fused else 2), (M, H)
+        assert status_ok(tp, lay)
 
 
 @pytest.mark.parametrize("M", [300, 20000])
