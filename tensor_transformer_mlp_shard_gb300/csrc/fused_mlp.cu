@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             const __nv_bfloat16 *res_row =
                 p.has_res ? p.res[tj] + static_cast<long long>(row_ok ? tl + lane : tl) * p.H : nullptr;
             // b2 and the residual of 32 output columns (the first piece's while Y accumulates,
-            // each later piece's alongside its TMEM load)
+            // each later piece's while the one before it is computed)
             auto fetch = [&](int cb, uint4 (&bb)[4], uint4 (&rr)[4]) {
                 const int col = h * 128 + cb * 32;
                 const bool in = col < p.H;
@@ -569,10 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             for (int cb = 0; cb < 4; ++cb) {
                 const int col = h * 128 + cb * 32;
                 if (col >= p.H) break;
-                if (cb > 0) fetch(cb, bb, rr);  // in flight with the TMEM load
                 uint32_t r[32];
                 tmem_ld32(tmem_base + col + lane_off, r);
                 tmem_ld_wait();
+                uint4 bn[4], rn[4];  // the next piece's b2 and residual, in flight while this one is computed
+                if (cb + 1 < 4) fetch(cb + 1, bn, rn);
                 if (block_ok) {
                     float v[32];
 #pragma unroll
@@ -618,6 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     for (int jj = 0; jj < 4; ++jj) {
                         const uint32_t c16 = 4u * static_cast<uint32_t>(cb & 1) + static_cast<uint32_t>(jj);
                         st_shared_v4(atom + ((c16 ^ (r_tile & 7u)) << 4), w[jj]);
+                    }
+                }
+                if (cb + 1 < 4) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        bb[k] = bn[k];
+                        rr[k] = rn[k];
                     }
                 }
             }
