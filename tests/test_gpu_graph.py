@@ -51,6 +51,39 @@ def test_mlp_step_replays_bitwise(tp, dtype, act, sp):
         assert torch.equal(a, b)
 
 
+def test_fused_split_forward_replays_bitwise(tp):
+    """The fused forward with its work split evenly over the SMs (a few token
+    tiles past a whole round): the flag memset and the kernel record into the
+    graph, and every replay gives the eager result bit for bit (a cut tile's
+    two parts are added in either arrival order to the same sum)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, H, F, T = 128 * (sms + 3), 256, 1024, 2
+    lay = tp.TPMLP(S=M, B=1, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    run = MlpRun(lay, t)
+    tp.set_fused_fwd("on")
+    try:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            run.fwd()
+        s.synchronize()
+        assert status_ok(tp, lay)
+        ref = [x.clone() for x in run.Y + run.pre + run.A]
+        for x in run.Y:
+            x.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run.fwd()
+        for _ in range(3):
+            g.replay()
+            torch.cuda.synchronize()
+            assert status_ok(tp, lay)
+            for a, b in zip(ref, run.Y + run.pre + run.A):
+                assert torch.equal(a, b)
+    finally:
+        tp.set_fused_fwd("auto")
+
+
 def test_layer_step_replays_bitwise(tp):
     from test_gpu_layer import LayerRun, layer_inputs, SEED
     M, H, F, T = 384, 256, 1024, 4
