@@ -47,6 +47,9 @@ CASES = [
     # evenly over the CTAs and a cut tile is finished by the second of its two
     (20736, 128, 768, 3, "gelu_tanh", True, True, True),
     (20485, 64, 512, 4, "none", False, False, False),
+    # the most shards the kernel's tensor maps take (16), and 8 token shards
+    (600, 128, 2048, 16, "gelu_tanh", True, True, False),
+    (1024, 64, 1024, 8, "gelu_tanh", True, True, True),
 ]
 
 
