@@ -584,10 +584,9 @@ FUSED_MODES = {"auto": 0, "off": 1, "on": 2}
 
 def set_fused_fwd(mode: str):
     """Forward as one fused kernel for narrow bf16 MLPs (H <= 256): "auto"
-    (default: where the shape allows it and there are at most ten 128-token
-    tiles per SM, where it measures faster than the two GEMMs), "on"
-    (whenever the shape allows it) or "off" (the column and row GEMM
-    kernels); see include/tp_mlp.h."""
+    (default) and "on" run it whenever the shape allows it (it measures faster
+    than the two GEMMs there), "off" runs the column and row GEMM kernels;
+    see include/tp_mlp.h."""
     _check(lib().tp_set_fused_fwd(FUSED_MODES[mode]))
 
 

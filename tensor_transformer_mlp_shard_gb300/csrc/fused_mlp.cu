@@ -84,6 +84,7 @@ struct FusedParams {
     DropoutParams drop;        // Y = R + dropout(sum + b2) (TransformerLayer bias-dropout-add)
     int rows_split, n_tok;
     int M, H, Fs, T, act, has_bias, has_res, has_pre;
+    int pre_v8;  // every pre_i 32-byte aligned: 32-byte stores
     int m_tiles, cps, nc, kb;  // chunks per shard, chunks per tile (T * cps), H / 64
     int nh;                    // 128-column halves of the output (H / 128 rounded up)
     // Even split: CTA b takes the (tile, chunk position) units
@@ -184,6 +185,16 @@ __device__ __forceinline__ void tok_index(const FusedParams &p, int row0, int &j
 }
 
 // 32 bf16 of one row: four 16-byte stores (the row's 64 bytes are contiguous)
+// the same as two 32-byte stores (dst 32-byte aligned): half the store
+// instructions for a warp whose lanes each write a different row
+__device__ __forceinline__ void store_row32_v8(__nv_bfloat16 *dst, const uint4 (&w)[4]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * j),
+                     "r"(w[2 * j].x), "r"(w[2 * j].y), "r"(w[2 * j].z), "r"(w[2 * j].w), "r"(w[2 * j + 1].x),
+                     "r"(w[2 * j + 1].y), "r"(w[2 * j + 1].z), "r"(w[2 * j + 1].w)
+                     : "memory");
+}
 __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint4 (&w)[4]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) reinterpret_cast<uint4 *>(dst)[j] = w[j];
@@ -455,7 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     uint4 wa[4];
                     if (p.has_pre) {
                         pack_bf16x32(v, wa);
-                        if (row_ok) store_row32(p.pre[i] + static_cast<long long>(row) * p.Fs + u, wa);
+                        if (row_ok) {
+                            __nv_bfloat16 *dst = p.pre[i] + static_cast<long long>(row) * p.Fs + u;
+                            if (p.pre_v8)
+                                store_row32_v8(dst, wa);
+                            else
+                                store_row32(dst, wa);
+                        }
                     }
                     if (p.act == TP_ACT_GELU_TANH) gelu_tanh_n<32>(v);
                     pack_bf16x32(v, wa);
@@ -720,6 +737,9 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     prm.has_bias = f.has_bias ? 1 : 0;
     prm.has_res = f.has_res ? 1 : 0;
     prm.has_pre = f.has_pre ? 1 : 0;
+    prm.pre_v8 = 1;
+    for (int i = 0; i < f.T; ++i)
+        if (f.has_pre && (reinterpret_cast<uintptr_t>(f.pre[i]) & 31u)) prm.pre_v8 = 0;
     prm.m_tiles = (f.M + kRows - 1) / kRows;
     prm.cps = f.Fs / kChunk;
     prm.nc = f.T * prm.cps;

@@ -110,6 +110,29 @@ def test_fused_even_split_matches_whole_tiles(tp, M, H, F, T, sp):
     tp.set_fused_fwd("auto")
 
 
+def test_fused_forward_pre_buffers_16_byte_aligned(tp):
+    """pre buffers 16- but not 32-byte aligned take the 16-byte stores instead
+    of the 32-byte ones, with the same results."""
+    M, H, F, T = 1000, 256, 1024, 2
+    lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    tp.set_fused_fwd("on")
+    aligned, _ = _fwd(tp, lay, t, "on")
+    run = MlpRun(lay, t)
+    Fs = F // T
+    backing = [torch.empty(M * Fs + 8, dtype=torch.bfloat16, device="cuda") for _ in range(T)]
+    run.pre = [b[8:].view(M, Fs) for b in backing]  # 16 bytes past a 256-byte boundary
+    assert all(x.data_ptr() % 32 == 16 for x in run.pre)
+    run.fwd()
+    assert status_ok(tp, lay)
+    for i in range(T):
+        assert torch.equal(run.pre[i], aligned.pre[i]), i
+        assert torch.equal(run.A[i], aligned.A[i]), i
+    for a, b in zip(run.Y, aligned.Y):
+        assert torch.equal(a, b)
+    tp.set_fused_fwd("auto")
+
+
 def test_fused_forward_feeds_the_backward(tp):
     """The backward after a fused forward equals the backward after the
     two-kernel forward (it reads pre and A, which are bit-identical)."""
@@ -141,14 +164,13 @@ def test_fused_forward_not_taken_outside_its_shapes(tp):
     tp.set_fused_fwd("auto")
 
 
-def test_fused_forward_by_default_up_to_ten_tiles_per_sm(tp):
-    """TP_FUSED_AUTO takes the fused kernel for the shapes it takes with at
-    most ten 128-token tiles per SM, the two GEMMs beyond that and for the
-    shapes it does not take."""
+def test_fused_forward_by_default(tp):
+    """TP_FUSED_AUTO takes the fused kernel for the shapes it takes, at any
+    token count, and the two GEMMs for the shapes it does not take."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tp.set_fused_fwd("auto")
-    for M, H, F, fused in ((4096, 256, 1024, True), (128 * 10 * sms, 128, 512, True),
-                           (128 * (10 * sms + 1), 128, 512, False), (4096, 512, 1024, False)):
+    for M, H, F, fused in ((4096, 256, 1024, True), (128 * (10 * sms + 1), 128, 512, True),
+                           (4096, 512, 1024, False), (4096, 256, 96 * 2, False)):
         lay = tp.TPMLP(S=M, B=1, H=H, F=F, T=2, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
         t = mlp_inputs(M, H, F, 2, "gelu_tanh", "bf16", has_bias=True)
         run = MlpRun(lay, t)
