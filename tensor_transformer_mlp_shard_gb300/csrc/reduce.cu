@@ -6,6 +6,7 @@
 // into fp32 partials (workspace); pass 2 adds the partials of each column in
 // chunk order.  Both passes use a fixed order, so results are run-to-run
 // deterministic (no atomics).
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -209,37 +210,79 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_partial_kernel(const __gri
     }
 }
 
-// Second pass: out_z[c] = sum_k partials[z][k][c].  A block owns 32 columns;
-// warp w adds the partial rows k = w, w + kWarps, ... in increasing k (four
-// interleaved accumulators for memory-level parallelism, combined in a fixed
-// order), then warp 0 adds the warps' sums in warp order: deterministic.
+// Second pass: out_z[c] = sum_k partials[z][k][c].  A cluster of S blocks owns
+// 32 columns and block s of it the partial rows of slice [s K / S, (s + 1) K / S):
+// its warp w adds the rows lo + w, lo + w + kWarps, ... in increasing order
+// (eight interleaved accumulators for memory-level parallelism, combined in a
+// fixed order) and warp 0 adds the warps' sums in warp order; after a cluster
+// barrier block 0 adds the S slice sums in rank order through distributed
+// shared memory.  Deterministic for a given S, which the host derives from the
+// shape alone (S > 1 spreads tall, narrow sums such as a 65536-token bias
+// gradient over more SMs).
 __global__ void __launch_bounds__(32 * kWarps) colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
     __shared__ float red[kWarps][32];
+    __shared__ float slice[32];
+    const unsigned S = cl.num_blocks(), rank = cl.block_rank();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int z = blockIdx.y;
-    const int c = blockIdx.x * 32 + lane;
-    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    const int c = static_cast<int>(blockIdx.x / S) * 32 + lane;
+    const int lo = static_cast<int>(static_cast<long long>(p.chunks) * rank / S);
+    const int hi = static_cast<int>(static_cast<long long>(p.chunks) * (rank + 1) / S);
+    float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
     if (c < p.N) {
         const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
         const long long step = static_cast<long long>(kWarps) * p.N;
-        int k = warp;
-        for (; k + 3 * kWarps < p.chunks; k += 4 * kWarps) {
+        int k = lo + warp;
+        for (; k + 7 * kWarps < hi; k += 8 * kWarps) {
             const float *q = src + static_cast<long long>(k) * p.N;
-            a0 += q[0];
-            a1 += q[step];
-            a2 += q[2 * step];
-            a3 += q[3 * step];
-        }
-        for (; k < p.chunks; k += kWarps) a0 += src[static_cast<long long>(k) * p.N];
-    }
-    red[warp][lane] = (a0 + a1) + (a2 + a3);
-    __syncthreads();
-    if (warp == 0 && c < p.N) {
-        float s = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w][lane];
-        p.out[z][c] = s;
+            for (int j = 0; j < 8; ++j) a[j] += q[j * step];
+        }
+        for (; k < hi; k += kWarps) a[0] += src[static_cast<long long>(k) * p.N];
     }
+    red[warp][lane] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    __syncthreads();
+    if (warp == 0) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += red[w][lane];
+        slice[lane] = t;
+    }
+    cl.sync();
+    if (rank == 0 && warp == 0 && c < p.N) {
+        float t = slice[lane];
+        for (unsigned r = 1; r < S; ++r) t += cl.map_shared_rank(slice, r)[lane];
+        p.out[z][c] = t;
+    }
+    cl.sync();  // the other blocks' slice sums stay until block 0 has read them
+}
+
+// The finalize over P problems of N columns and K partial rows: S (the
+// cluster size) doubles up to 8 while the grid stays within two blocks per SM
+// and every slice keeps 64 rows.
+static tp_status launch_finalize(const ColsumParams &prm, int P, cudaStream_t st) {
+    const int ncb = (prm.N + 31) / 32;
+    int S = 1;
+    while (S < 8 && static_cast<long long>(ncb) * P * (2 * S) <= 2ll * num_sms() && prm.chunks / (2 * S) >= 64)
+        S *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(ncb * S, P, 1);
+    cfg.blockDim = dim3(32 * kWarps, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    launch_begin("colsum_finalize", st);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, colsum_finalize_kernel, prm);
+    launch_end("colsum_finalize", st);
+    return cuda_check(e, "colsum_finalize");
 }
 
 tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t st) {
@@ -251,12 +294,7 @@ tp_status launch_colsum_finalize(const ColsumPlan &c, int chunks, cudaStream_t s
     prm.chunks = chunks;
     prm.partials = c.partials;
     if (c.N == 0 || c.P == 0) return TP_OK;
-    dim3 g2((c.N + 31) / 32, c.P);
-    launch_begin("colsum_finalize", st);
-    colsum_finalize_kernel<<<g2, 32 * kWarps, 0, st>>>(prm);
-    cudaError_t e = cudaGetLastError();
-    launch_end("colsum_finalize", st);
-    return cuda_check(e, "colsum_finalize");
+    return launch_finalize(prm, c.P, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,12 +391,7 @@ tp_status launch_colsum(const ColsumPlan &c, int dtype, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     launch_end(c.name, st);
     if (e != cudaSuccess) return cuda_check(e, c.name);
-    dim3 g2((c.N + 31) / 32, c.P);
-    launch_begin("colsum_finalize", st);
-    colsum_finalize_kernel<<<g2, 32 * kWarps, 0, st>>>(prm);
-    e = cudaGetLastError();
-    launch_end("colsum_finalize", st);
-    return cuda_check(e, "colsum_finalize");
+    return launch_finalize(prm, c.P, st);
 }
 
 }  // namespace tpmlp
