@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_partial_kernel(const __gri
 // Second pass: out_z[c] = sum_k partials[z][k][c].  A cluster of S blocks owns
 // 32 columns and block s of it the partial rows of slice [s K / S, (s + 1) K / S):
 // its warp w adds the rows lo + w, lo + w + kWarps, ... in increasing order
-// (eight interleaved accumulators for memory-level parallelism, combined in a
+// (four interleaved accumulators for memory-level parallelism, combined in a
 // fixed order) and warp 0 adds the warps' sums in warp order; after a cluster
 // barrier block 0 adds the S slice sums in rank order through distributed
 // shared memory.  Deterministic for a given S, which the host derives from the
@@ -230,19 +230,21 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_finalize_kernel(const __gr
     const int c = static_cast<int>(blockIdx.x / S) * 32 + lane;
     const int lo = static_cast<int>(static_cast<long long>(p.chunks) * rank / S);
     const int hi = static_cast<int>(static_cast<long long>(p.chunks) * (rank + 1) / S);
-    float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
     if (c < p.N) {
         const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
         const long long step = static_cast<long long>(kWarps) * p.N;
         int k = lo + warp;
-        for (; k + 7 * kWarps < hi; k += 8 * kWarps) {
+        for (; k + 3 * kWarps < hi; k += 4 * kWarps) {
             const float *q = src + static_cast<long long>(k) * p.N;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a[j] += q[j * step];
+            a0 += q[0];
+            a1 += q[step];
+            a2 += q[2 * step];
+            a3 += q[3 * step];
         }
-        for (; k < hi; k += kWarps) a[0] += src[static_cast<long long>(k) * p.N];
+        for (; k < hi; k += kWarps) a0 += src[static_cast<long long>(k) * p.N];
     }
-    red[warp][lane] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    red[warp][lane] = (a0 + a1) + (a2 + a3);
     __syncthreads();
     if (warp == 0) {
         float t = 0.0f;
