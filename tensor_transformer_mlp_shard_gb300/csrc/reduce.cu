@@ -317,12 +317,22 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
         const long long e = q * 4;
         const float *src = p.part + static_cast<long long>(z) * plane + e;
         float4 s = *reinterpret_cast<const float4 *>(src);
-        for (int k = 1; k < p.ksplit; ++k) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + static_cast<long long>(k) * p.P * plane);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+        // eight splits' loads in flight at a time, added in split order
+        for (int k0 = 1; k0 < p.ksplit; k0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (k0 + j < p.ksplit)
+                    v[j] = *reinterpret_cast<const float4 *>(src + static_cast<long long>(k0 + j) * p.P * plane);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (k0 + j < p.ksplit) {
+                    s.x += v[j].x;
+                    s.y += v[j].y;
+                    s.z += v[j].z;
+                    s.w += v[j].w;
+                }
+            }
         }
         float4 *dst = reinterpret_cast<float4 *>(p.out[z] + e);
         if (p.accumulate) {
