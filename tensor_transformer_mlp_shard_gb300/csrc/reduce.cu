@@ -212,17 +212,18 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_partial_kernel(const __gri
 
 // Second pass: out_z[c] = sum_k partials[z][k][c].  A cluster of S blocks owns
 // 32 columns and block s of it the partial rows of slice [s K / S, (s + 1) K / S):
-// its warp w adds the rows lo + w, lo + w + kWarps, ... in increasing order
+// its warp w of 16 adds the rows lo + w, lo + w + 16, ... in increasing order
 // (four interleaved accumulators for memory-level parallelism, combined in a
 // fixed order) and warp 0 adds the warps' sums in warp order; after a cluster
 // barrier block 0 adds the S slice sums in rank order through distributed
 // shared memory.  Deterministic for a given S, which the host derives from the
 // shape alone (S > 1 spreads tall, narrow sums such as a 65536-token bias
 // gradient over more SMs).
-__global__ void __launch_bounds__(32 * kWarps) colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
+constexpr int kFinWarps = 16;
+__global__ void __launch_bounds__(32 * kFinWarps) colsum_finalize_kernel(const __grid_constant__ ColsumParams p) {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
-    __shared__ float red[kWarps][32];
+    __shared__ float red[kFinWarps][32];
     __shared__ float slice[32];
     const unsigned S = cl.num_blocks(), rank = cl.block_rank();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -233,23 +234,23 @@ __global__ void __launch_bounds__(32 * kWarps) colsum_finalize_kernel(const __gr
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
     if (c < p.N) {
         const float *src = p.partials + static_cast<long long>(z) * p.chunks * p.N + c;
-        const long long step = static_cast<long long>(kWarps) * p.N;
+        const long long step = static_cast<long long>(kFinWarps) * p.N;
         int k = lo + warp;
-        for (; k + 3 * kWarps < hi; k += 4 * kWarps) {
+        for (; k + 3 * kFinWarps < hi; k += 4 * kFinWarps) {
             const float *q = src + static_cast<long long>(k) * p.N;
             a0 += q[0];
             a1 += q[step];
             a2 += q[2 * step];
             a3 += q[3 * step];
         }
-        for (; k < hi; k += kWarps) a0 += src[static_cast<long long>(k) * p.N];
+        for (; k < hi; k += kFinWarps) a0 += src[static_cast<long long>(k) * p.N];
     }
     red[warp][lane] = (a0 + a1) + (a2 + a3);
     __syncthreads();
     if (warp == 0) {
         float t = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += red[w][lane];
+        for (int w = 0; w < kFinWarps; ++w) t += red[w][lane];
         slice[lane] = t;
     }
     cl.sync();
@@ -276,7 +277,7 @@ static tp_status launch_finalize(const ColsumParams &prm, int P, cudaStream_t st
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(ncb * S, P, 1);
-    cfg.blockDim = dim3(32 * kWarps, 1, 1);
+    cfg.blockDim = dim3(32 * kFinWarps, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;
