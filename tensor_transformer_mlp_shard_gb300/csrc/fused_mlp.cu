@@ -23,7 +23,7 @@
 // operand buffer, from which one bulk tensor store per 64 units copies it to
 // HBM; the group's output columns of Y are staged in the same buffer at the
 // end of a tile and stored the same way, 32 rows per warp; pre goes out with
-// direct 16-byte stores (staging it too measured slower).  Every wait is
+// direct 32-byte stores (staging it too measured slower).  Every wait is
 // bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
