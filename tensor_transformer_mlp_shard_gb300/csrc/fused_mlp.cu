@@ -184,6 +184,13 @@ __device__ __forceinline__ void tok_index(const FusedParams &p, int row0, int &j
     }
 }
 
+// v[0..8) += the 8 bf16 of w, two lanes of fp32 at a time
+__device__ __forceinline__ void add_bf16x8(float *v, const uint4 &w) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st2(v + 2 * k, __fadd2_rn(ld2(v + 2 * k), make_float2(bf16_lo(u[k]), bf16_hi(u[k]))));
+}
+
 // 32 bf16 of one row: four 16-byte stores (the row's 64 bytes are contiguous)
 // the same as two 32-byte stores (dst 32-byte aligned): half the store
 // instructions for a warp whose lanes each write a different row
@@ -455,13 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                     if (p.has_bias) {
 #pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            const uint4 bw = bcur[g8];
-                            v[8 * g8 + 0] += bf16_lo(bw.x); v[8 * g8 + 1] += bf16_hi(bw.x);
-                            v[8 * g8 + 2] += bf16_lo(bw.y); v[8 * g8 + 3] += bf16_hi(bw.y);
-                            v[8 * g8 + 4] += bf16_lo(bw.z); v[8 * g8 + 5] += bf16_hi(bw.z);
-                            v[8 * g8 + 6] += bf16_lo(bw.w); v[8 * g8 + 7] += bf16_hi(bw.w);
-                        }
+                        for (int g8 = 0; g8 < 4; ++g8) add_bf16x8(v + 8 * g8, bcur[g8]);
                     }
                     uint4 wa[4];
                     if (p.has_pre) {
@@ -612,22 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     }
                     if (p.has_bias) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            v[8 * k + 0] += bf16_lo(bb[k].x); v[8 * k + 1] += bf16_hi(bb[k].x);
-                            v[8 * k + 2] += bf16_lo(bb[k].y); v[8 * k + 3] += bf16_hi(bb[k].y);
-                            v[8 * k + 4] += bf16_lo(bb[k].z); v[8 * k + 5] += bf16_hi(bb[k].z);
-                            v[8 * k + 6] += bf16_lo(bb[k].w); v[8 * k + 7] += bf16_hi(bb[k].w);
-                        }
+                        for (int k = 0; k < 4; ++k) add_bf16x8(v + 8 * k, bb[k]);
                     }
                     if (p.drop.on) dropout32(p.drop, row, col, row_ok, v);
                     if (res_row) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            v[8 * k + 0] += bf16_lo(rr[k].x); v[8 * k + 1] += bf16_hi(rr[k].x);
-                            v[8 * k + 2] += bf16_lo(rr[k].y); v[8 * k + 3] += bf16_hi(rr[k].y);
-                            v[8 * k + 4] += bf16_lo(rr[k].z); v[8 * k + 5] += bf16_hi(rr[k].z);
-                            v[8 * k + 6] += bf16_lo(rr[k].w); v[8 * k + 7] += bf16_hi(rr[k].w);
-                        }
+                        for (int k = 0; k < 4; ++k) add_bf16x8(v + 8 * k, rr[k]);
                     }
                     uint4 w[4];
                     pack_bf16x32(v, w);
