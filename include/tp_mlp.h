@@ -536,7 +536,7 @@ TP_API tp_status tp_set_max_gemm_pairs(int n);
  * whole number of rounds of the SMs by at most a quarter of a round.
  * TP_FUSED_AUTO (default) and TP_FUSED_ON run the fused kernel for every
  * problem it takes (on GB300 it measured faster than the two GEMMs from 16 to
- * 2048 128-token tiles: 126 us against 155 us for 65536 tokens at H = 256,
+ * 2048 128-token tiles: 124 us against 155 us for 65536 tokens at H = 256,
  * F = 1024, T = 2), TP_FUSED_OFF never.  pre and A are bit-identical between the paths; Y accumulates the
  * same fp32 products in another order.  Returns TP_ERR_ARG for an unknown
  * mode. */
