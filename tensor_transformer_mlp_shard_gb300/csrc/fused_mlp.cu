@@ -13,6 +13,8 @@
 // The output tile [128 x H] lives in TMEM next to two 128-column
 // accumulators of the column GEMM, so H <= 256: at wider layers the output
 // row does not fit on chip and the two-kernel path (tc_gemm) runs instead.
+// Token tiles go to the CTAs whole, or, when they spill over whole rounds of
+// the SMs by a little, as an even split of (tile, chunk) units (below).
 //
 // Warp roles (320 threads): warp 0 issues TMA (the X tile once per token
 // tile, then W1 and W2 boxes of 16 KB in consumption order through a 6-slot
@@ -95,7 +97,7 @@ struct FusedParams {
     long long work;
     float *part;         // [G][8 warps][4096] fp32 output slices of the cut tiles
     unsigned *part_cnt;  // [G][8] arrivals per cut tile and warp, then [G][8] ready flags (zeroed)
-    uint32_t idesc;            // bf16 x bf16 -> fp32, both K-major, M = 128, N = 64
+    uint32_t idesc;            // bf16 x bf16 -> fp32, both K-major, M = 128, N = 128
     int *status;
     unsigned *abort_word;
     unsigned launch_id;
