@@ -20,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from harness import MlpRun, host, mlp_inputs, rel_err, status_ok
+from harness import MlpRun, host, mlp_inputs, oracle_full, rel_err, status_ok
 from oracle import layer as olayer
 
 pytestmark = pytest.mark.gpu
@@ -131,6 +131,35 @@ def test_fused_forward_pre_buffers_16_byte_aligned(tp):
     for a, b in zip(run.Y, aligned.Y):
         assert torch.equal(a, b)
     tp.set_fused_fwd("auto")
+
+
+def test_narrow_workload_full_size_against_oracle(tp):
+    """The narrow workload as bench.py times it (65536 tokens, H = 256, F = 1024,
+    T = 2, bias, residual; the fused forward by default, whole tiles), forward
+    and backward against the fp64 oracle element by element: the bias
+    gradients' 2048 partial rows go through the finalize's clusters of 8
+    blocks and the weight gradients through the 16-way split-K reduction."""
+    M, H, F, T = 65536, 256, 1024, 2
+    lay = tp.TPMLP(S=4096, B=16, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=True)
+    t = mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True)
+    tp.set_fused_fwd("auto")
+    run = MlpRun(lay, t)
+    n0 = tp.launch_count()
+    run.fwd()
+    assert tp.launch_count() - n0 == 1
+    run.bwd()
+    assert status_ok(tp, lay)
+    ref = oracle_full(lay, t)
+    errs = {"Y": rel_err(run.gathered(run.Y), ref["Y"]), "dX": rel_err(run.gathered(run.dX), ref["dX"]),
+            "db2": rel_err(host(run.db2), ref["db2"])}
+    for i in range(T):
+        errs[f"pre{i}"] = rel_err(host(run.pre[i]), ref["pre"][i])
+        errs[f"A{i}"] = rel_err(host(run.A[i]), ref["A"][i])
+        errs[f"dW1_{i}"] = rel_err(host(run.dW1[i]), ref["dW1"][i])
+        errs[f"dW2_{i}"] = rel_err(host(run.dW2[i]), ref["dW2"][i])
+        errs[f"db1_{i}"] = rel_err(host(run.db1[i]), ref["db1"][i])
+    bad = {k: v for k, v in errs.items() if not v <= 1e-2}
+    assert not bad, bad
 
 
 def test_fused_forward_feeds_the_backward(tp):
