@@ -537,9 +537,10 @@ TP_API tp_status tp_set_max_gemm_pairs(int n);
  * TP_FUSED_AUTO (default) and TP_FUSED_ON run the fused kernel for every
  * problem it takes (on GB300 it measured faster than the two GEMMs from 16 to
  * 2048 128-token tiles: 124 us against 155 us for 65536 tokens at H = 256,
- * F = 1024, T = 2), TP_FUSED_OFF never.  pre and A are bit-identical between the paths; Y accumulates the
- * same fp32 products in another order.  Returns TP_ERR_ARG for an unknown
- * mode. */
+ * F = 1024, T = 2), TP_FUSED_OFF never.  pre and A are bit-identical
+ * between the paths; Y accumulates the same fp32 products in another order.
+ * The pre buffers take 32-byte stores when they are 32-byte aligned (16-byte
+ * ones otherwise).  Returns TP_ERR_ARG for an unknown mode. */
 typedef enum { TP_FUSED_AUTO = 0, TP_FUSED_OFF = 1, TP_FUSED_ON = 2 } tp_fused_mode;
 TP_API tp_status tp_set_fused_fwd(int mode);
 
