@@ -312,8 +312,8 @@ def test_band_rows_match_oracle(tp, band):
     assert not bad, bad
 
 
-@pytest.mark.parametrize("sp", [False, True])
-def test_launch_overlap_keeps_stream_order(tp, sp):
+@pytest.mark.parametrize("sp,H", [(False, 512), (True, 512), (False, 256)])
+def test_launch_overlap_keeps_stream_order(tp, sp, H):
     """Programmatic dependent launch of the pair GEMMs (tp_set_launch_overlap):
     two forward+backward steps on different inputs, issued back to back with
     no host synchronisation and sharing the pre, A and workspace buffers, so
@@ -322,8 +322,9 @@ def test_launch_overlap_keeps_stream_order(tp, sp):
     before it still reads (the second column forward's pre and A under the
     first backward) would change the results.  Both steps give the bits of
     plain stream order and match the oracle; the grid cut to 7 pairs gives
-    several persistent rounds and a tail split."""
-    M, H, F, T = 1024, 512, 2048, 4
+    several persistent rounds and a tail split.  At H = 256 the forward is the
+    fused kernel, also launched with programmatic dependent launch."""
+    M, F, T = 1024, 2048, 4
     lay = tp.TPMLP(S=M // 2, B=2, H=H, F=F, T=T, act="gelu_tanh", dtype="bf16", has_bias=True, residual=not sp,
                    seq_parallel=sp)
     ins = [mlp_inputs(M, H, F, T, "gelu_tanh", "bf16", has_bias=True, seed_off=k) for k in (0, 1)]
