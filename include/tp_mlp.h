@@ -529,8 +529,10 @@ TP_API tp_status tp_set_max_gemm_pairs(int n);
  * in 128-unit chunks: per chunk the column GEMM, bias and activation (pre and
  * A are still stored for the backward), then A goes from shared memory
  * straight into the row GEMM, so A is never read back from HBM.  It takes
- * bf16 with act = none or GeLU-tanh, H a multiple of 64 up to 256 and F/T a
- * multiple of 128; other problems always use the two-kernel path.  With a
+ * bf16 with H a multiple of 64 up to 256 and act = none or GeLU-tanh with F/T
+ * a multiple of 128, or SwiGLU with F/T a multiple of 64 (a chunk is then 64
+ * gate and the 64 matching up units); other problems always use the
+ * two-kernel path.  With a
  * workspace (tp_mlp_fwd_ws, tp_layer_fwd) of the size the handle reports,
  * the work is split evenly over the SMs when the token tiles spill over a
  * whole number of rounds of the SMs by at most a quarter of a round.

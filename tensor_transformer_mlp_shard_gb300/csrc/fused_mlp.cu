@@ -87,6 +87,9 @@ struct FusedParams {
     int rows_split, n_tok;
     int M, H, Fs, T, act, has_bias, has_res, has_pre;
     int pre_v8;  // every pre_i 32-byte aligned: 32-byte stores
+    int swiglu;  // SwiGLU: a chunk is 64 gate and the 64 matching up units
+    int uc;      // units of A per chunk: 128, or 64 under SwiGLU
+    int pre_ld;  // row stride of pre_i: Fs, or 2 Fs (gate | up) under SwiGLU
     int m_tiles, cps, nc, kb;  // chunks per shard, chunks per tile (T * cps), H / 64
     int nh;                    // 128-column halves of the output (H / 128 rounded up)
     // Even split: CTA b takes the (tile, chunk position) units
@@ -209,7 +212,90 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint4 (&w)
     for (int j = 0; j < 4; ++j) reinterpret_cast<uint4 *>(dst)[j] = w[j];
 }
 
+// A SwiGLU chunk's epilogue (one thread = one token row): the accumulator
+// holds the 64 gate units u0.. in columns [0, 64) and the matching up units in
+// [64, 128); pre gets both (gate | up halves of its row), A = silu(gate) * up
+// goes into atom 0 of the group's buffer, in two 32-unit pieces.  The same
+// arithmetic as the two-kernel path's column epilogue.
+template <typename Release>
+__device__ __forceinline__ bool swiglu_chunk(const FusedParams &p, int i, int u0, int b, uint32_t use, int row,
+                                             bool row_ok, uint32_t r_tile, uint32_t lane_off, uint32_t tmem_base,
+                                             uint32_t buf, uint32_t accf0, uint32_t acce0, uint32_t ae0,
+                                             Release &release) {
+    auto fetch = [&](int jp, uint4 (&bg)[4], uint4 (&bu)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            bg[k] = p.has_bias ? *reinterpret_cast<const uint4 *>(p.b1[i] + u0 + 32 * jp + 8 * k) : make_uint4(0, 0, 0, 0);
+            bu[k] = p.has_bias ? *reinterpret_cast<const uint4 *>(p.b1[i] + p.Fs + u0 + 32 * jp + 8 * k)
+                               : make_uint4(0, 0, 0, 0);
+        }
+    };
+    uint4 bg[4], bu[4];
+    fetch(0, bg, bu);
+    bool good = fwait(accf0 + 8 * b, use & 1u, p);
+    if (!__all_sync(0xffffffffu, good)) return false;
+    tc_fence_after();
+    const uint32_t acc = tmem_base + kAccCol + kChunk * b + lane_off;
+#pragma unroll
+    for (int jp = 0; jp < 2; ++jp) {
+        uint32_t rg[32], ru[32];
+        tmem_ld32(acc + 32 * jp, rg);
+        tmem_ld32(acc + 64 + 32 * jp, ru);
+        tmem_ld_wait();
+        if (jp == 1) {
+            tc_fence_before();
+            mbar_arrive(acce0 + 8 * b);  // the column GEMM may reuse the accumulator
+        }
+        float G[32], U[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            G[j] = __uint_as_float(rg[j]);
+            U[j] = __uint_as_float(ru[j]);
+        }
+        if (p.has_bias) {
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                add_bf16x8(G + 8 * g8, bg[g8]);
+                add_bf16x8(U + 8 * g8, bu[g8]);
+            }
+        }
+        if (jp == 0) fetch(1, bg, bu);
+        uint4 wa[4];
+        if (p.has_pre && row_ok) {
+            __nv_bfloat16 *dst = p.pre[i] + static_cast<long long>(row) * p.pre_ld + u0 + 32 * jp;
+            pack_bf16x32(G, wa);
+            if (p.pre_v8)
+                store_row32_v8(dst, wa);
+            else
+                store_row32(dst, wa);
+            pack_bf16x32(U, wa);
+            if (p.pre_v8)
+                store_row32_v8(dst + p.Fs, wa);
+            else
+                store_row32(dst + p.Fs, wa);
+        }
+        swiglu_n<32>(G, U);
+        pack_bf16x32(G, wa);
+        if (jp == 0) {
+            // the A buffer is free once the bulk stores from it have read it and the
+            // row GEMM of chunk cg - kNB is done
+            good = release() && fwait(ae0 + 8 * b, (use & 1u) ^ 1u, p);
+            if (!__all_sync(0xffffffffu, good)) return false;
+        }
+        // atom 0, row r_tile, 16-byte chunks 4 jp .. + 3, 128-byte swizzle
+        const uint32_t rowa = buf + r_tile * 128u;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t c16 = 4u * static_cast<uint32_t>(jp) + static_cast<uint32_t>(jj);
+            st_shared_v4(rowa + ((c16 ^ (r_tile & 7u)) << 4), wa[jj]);
+        }
+    }
+    return true;
+}
+
+template <bool SWIGLU>  // the SwiGLU chunk layout (p.swiglu), compiled apart from the GeLU one
 __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid_constant__ FusedParams p) {
+    constexpr int UC = SWIGLU ? 64 : kChunk;  // units of A per chunk (p.uc)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -264,13 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             uint32_t phase = 0, armed = 0, armed_par = 0;
             bool x_armed = false, ok = true;
             uint32_t x_par = 0;
-            auto load_box = [&](const CUtensorMap *map, int c0, int c1) -> bool {
+            // one 16 KB box [128 rows x 64], or (c1b >= 0) two [64 rows x 64]
+            // boxes stacked in the slot: the gate and up rows of a SwiGLU chunk
+            auto load_box = [&](const CUtensorMap *map, int c0, int c1, int c1b = -1) -> bool {
                 if (!fwait(empty0 + 8 * slot, phase ^ 1u, p)) return false;
                 const uint32_t fb = full0 + 8 * slot;
                 mbar_arrive_expect_tx(fb, kBox);
                 armed |= 1u << slot;
                 armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                 tma_load_2d(sbase + slot * kBox, map, fb, c0, c1);
+                if (c1b >= 0) tma_load_2d(sbase + slot * kBox + kBox / 2, map, fb, c0, c1b);
                 if (++slot == kSlots) {
                     slot = 0;
                     phase ^= 1u;
@@ -291,13 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                 // tile t holds chunk (c + t) mod nc
                 for (int c = c0; ok && c < c1 + kLag; ++c) {
                     if (c < c1) {
-                        const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
-                        for (int kb = 0; ok && kb < p.kb; ++kb) ok = load_box(&p.mapW1[i], kb * 64, u0);
+                        const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * UC;
+                        for (int kb = 0; ok && kb < p.kb; ++kb)
+                            ok = load_box(&p.mapW1[i], kb * 64, u0, SWIGLU ? p.Fs + u0 : -1);
                     }
                     if (ok && c - kLag >= c0) {
-                        const int ch = chunk_at(p, t, c - kLag), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
+                        const int ch = chunk_at(p, t, c - kLag), i = ch / p.cps, u0 = (ch % p.cps) * UC;
                         for (int h = 0; ok && h < p.nh; ++h)
-                            for (int k2 = 0; ok && k2 < kChunk / 64; ++k2)
+                            for (int k2 = 0; ok && k2 < UC / 64; ++k2)
                                 ok = load_box(&p.mapW2[i], u0 + 64 * k2, h * 128);
                     }
                 }
@@ -366,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                         tc_fence_after();
                         const uint32_t sa = sbase + kOffA + b * kABytes;
                         for (int h = 0; ok && h < p.nh; ++h) {
-                            for (int k2 = 0; k2 < kChunk / 64; ++k2) {
+                            for (int k2 = 0; k2 < UC / 64; ++k2) {
                                 if (!fwait(full0 + 8 * slot, phase, p)) {
                                     ok = false;
                                     break;
@@ -430,7 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
             for (int c = c0 + ((cgb & 1) == h ? 0 : 1); c < c1; c += 2) {
                 const int cg = cgb + c - c0, b = cg % kNB;
                 const uint32_t use = static_cast<uint32_t>(cg) / kNB;
-                const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * kChunk;
+                const int ch = chunk_at(p, t, c), i = ch / p.cps, u0 = (ch % p.cps) * UC;
+                if constexpr (SWIGLU) {
+                    ok = swiglu_chunk(p, i, u0, b, use, row, row_ok, r_tile, lane_off, tmem_base, buf, accf0, acce0,
+                                      ae0, release);
+                    if (!ok) break;
+                } else {
                 // b1 of one 32-unit piece: the first piece's while the accumulator
                 // fills, each next piece's while the current one is computed
                 auto fetch_b1 = [&](int hh, uint4 (&bw)[4]) {
@@ -470,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     if (p.has_pre) {
                         pack_bf16x32(v, wa);
                         if (row_ok) {
-                            __nv_bfloat16 *dst = p.pre[i] + static_cast<long long>(row) * p.Fs + u;
+                            __nv_bfloat16 *dst = p.pre[i] + static_cast<long long>(row) * p.pre_ld + u;
                             if (p.pre_v8)
                                 store_row32_v8(dst, wa);
                             else
@@ -503,12 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_mlp_fwd_kernel(const __grid
                     for (int k = 0; k < 4; ++k) bcur[k] = bnext[k];
                 }
                 if (!ok) break;
+                }
                 fence_async_smem();
                 mbar_arrive(af0 + 8 * b);
                 if (elect) {  // once the group's 128 rows are in, A goes to HBM in two boxes
                     ok = fwait(af0 + 8 * b, use & 1u, p);
                     if (ok) {
-                        for (int k2 = 0; k2 < kChunk / 64; ++k2) tma_store_2d(&p.mapA[i], buf + k2 * kAtom, u0 + 64 * k2, t * kRows);
+                        for (int k2 = 0; k2 < UC / 64; ++k2) tma_store_2d(&p.mapA[i], buf + k2 * kAtom, u0 + 64 * k2, t * kRows);
                         bulk_commit();
                     }
                 }
@@ -668,8 +764,8 @@ void set_fused_fwd_mode(int mode) { g_fused_mode.store(mode); }
 int fused_fwd_mode() { return g_fused_mode.load(); }
 
 bool fused_fwd_supported(int H, int Fs, int act, int dtype) {
-    return dtype == TP_DT_BF16 && act != TP_ACT_SWIGLU && H >= 64 && H <= fm::kMaxH && H % 64 == 0 &&
-           Fs >= fm::kChunk && Fs % fm::kChunk == 0;
+    const int uc = act == TP_ACT_SWIGLU ? 64 : fm::kChunk;  // units of A per chunk
+    return dtype == TP_DT_BF16 && H >= 64 && H <= fm::kMaxH && H % 64 == 0 && Fs >= uc && Fs % uc == 0;
 }
 
 // Bytes of scratch the even split of an M-token forward takes: the parked
@@ -704,7 +800,9 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
         prm.res[j] = f.has_res ? static_cast<const __nv_bfloat16 *>(f.R[j]) : nullptr;
     }
     for (int i = 0; i < f.T; ++i) {
-        tp_status s = tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, kChunk, false);
+        // W1_i [g Fs, H]; a SwiGLU chunk loads its gate and up rows as two 64-row boxes
+        tp_status s = f.act == TP_ACT_SWIGLU ? tc::encode_map(&prm.mapW1[i], f.W1[i], 2 * f.Fs, f.H, 64, 64, false)
+                                             : tc::encode_map(&prm.mapW1[i], f.W1[i], f.Fs, f.H, 64, kChunk, false);
         if (s == TP_OK) s = tc::encode_map(&prm.mapW2[i], f.W2[i], f.H, f.Fs, 64, 128, false);
         if (s == TP_OK) s = tc::encode_map(&prm.mapA[i], f.A[i], f.M, f.Fs, 64, kRows, false);
         if (s != TP_OK) return s;
@@ -734,7 +832,10 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     for (int i = 0; i < f.T; ++i)
         if (f.has_pre && (reinterpret_cast<uintptr_t>(f.pre[i]) & 31u)) prm.pre_v8 = 0;
     prm.m_tiles = (f.M + kRows - 1) / kRows;
-    prm.cps = f.Fs / kChunk;
+    prm.swiglu = f.act == TP_ACT_SWIGLU ? 1 : 0;
+    prm.uc = prm.swiglu ? 64 : kChunk;
+    prm.pre_ld = prm.swiglu ? 2 * f.Fs : f.Fs;
+    prm.cps = f.Fs / prm.uc;
     prm.nc = f.T * prm.cps;
     prm.kb = f.H / 64;
     prm.nh = (f.H + 127) / 128;
@@ -757,8 +858,11 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev % 64]) {
-            cudaError_t e =
-                cudaFuncSetAttribute(fused_mlp_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            cudaError_t e = cudaFuncSetAttribute(fused_mlp_fwd_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fused_mlp_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
             if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(fused_mlp_fwd)");
             attr_set[dev % 64] = true;
         }
@@ -786,7 +890,8 @@ tp_status launch_fused_mlp_fwd(const FusedPlan &f, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl_on() ? 1 : 0;
     launch_begin("fused_mlp_fwd", st);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fused_mlp_fwd_kernel, prm);
+    cudaError_t e = prm.swiglu ? cudaLaunchKernelEx(&cfg, fused_mlp_fwd_kernel<true>, prm)
+                               : cudaLaunchKernelEx(&cfg, fused_mlp_fwd_kernel<false>, prm);
     launch_end("fused_mlp_fwd", st);
     return cuda_check(e, "fused_mlp_fwd");
 }

@@ -4,9 +4,10 @@ FlashFusedMLP, "Megatron-LM 源码精读" s7, the fusions/ entry) through the
 C ABI.
 
 * Against the fp64 oracle, element by element, on ragged multi-tile sizes,
-  sequence parallelism, odd T, every H the kernel takes (64..256) and more
-  token tiles than SMs (the persistent loop): tolerance 1e-2 * max|ref|
-  (bf16 storage of pre and A, fp32 sums), the MLP's bf16 bound.
+  sequence parallelism, odd T, every H the kernel takes (64..256), GeLU,
+  no activation and SwiGLU, and more token tiles than SMs (the persistent
+  loop): tolerance 1e-2 * max|ref| (bf16 storage of pre and A, fp32 sums),
+  the MLP's bf16 bound.
 * Against the two-kernel path on the same inputs: both accumulate the same
   products in fp32 in 64-element K steps, so pre and A agree bit for bit and
   Y to within fp32 reassociation of the chunk sums.
@@ -50,6 +51,11 @@ CASES = [
     # the most shards the kernel's tensor maps take (16), and 8 token shards
     (600, 128, 2048, 16, "gelu_tanh", True, True, False),
     (1024, 64, 1024, 8, "gelu_tanh", True, True, True),
+    # SwiGLU: 64 gate and 64 up units per chunk
+    (300, 256, 512, 2, "swiglu", True, True, False),
+    (1024, 128, 768, 2, "swiglu", False, False, True),
+    (517, 192, 320, 5, "swiglu", True, False, False),
+    (20736, 64, 384, 3, "swiglu", True, True, True),
 ]
 
 
@@ -181,7 +187,7 @@ def test_fused_forward_feeds_the_backward(tp):
 
 def test_fused_forward_not_taken_outside_its_shapes(tp):
     tp.set_fused_fwd("on")
-    for kw in (dict(H=320, F=1024), dict(H=256, F=1024, act="swiglu"), dict(H=256, F=96 * 2)):
+    for kw in (dict(H=320, F=1024), dict(H=256, F=96 * 2, act="swiglu"), dict(H=256, F=96 * 2)):
         act = kw.pop("act", "gelu_tanh")
         lay = tp.TPMLP(S=64, B=2, T=2, act=act, dtype="bf16", **kw)
         t = mlp_inputs(128, lay.H, lay.F, 2, act, "bf16", has_bias=False)
