@@ -10,6 +10,9 @@
 //   Y = (X +) dropout(Y + b2) -> HBM   (dropout only in the TransformerLayer)
 // so A never makes the round trip HBM -> row GEMM, and the cross-shard sum of
 // the row layer (the forward all-reduce) is the Y accumulation over (i, c).
+// Under SwiGLU (the kernel's second instance) a chunk is 64 units of A: the
+// column GEMM's 128 columns are 64 gate and the 64 matching up units, and
+// A = silu(gate) * up.
 // The output tile [128 x H] lives in TMEM next to two 128-column
 // accumulators of the column GEMM, so H <= 256: at wider layers the output
 // row does not fit on chip and the two-kernel path (tc_gemm) runs instead.
