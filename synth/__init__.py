@@ -163,6 +163,10 @@ WORKLOADS = {
                        dtype="bf16", has_bias=True, bias_std=0.02, residual=True,
                        seq_parallel=False,
                        notes="the tiny configuration's widths in bf16 with 65536 tokens: a memory-bound MLP"),
+    "narrow_swiglu": Workload("narrow_swiglu", "mlp", S=4096, B=16, H=256, F=1024, T=2, act="swiglu",
+                              dtype="bf16", has_bias=True, bias_std=0.02, residual=True,
+                              seq_parallel=False,
+                              notes="the narrow workload with a SwiGLU activation (gate and up rows in W1)"),
     "sp": Workload("sp", "mlp", S=4096, B=4, H=6144, F=24576, T=8, act="gelu_tanh",
                    dtype="bf16", has_bias=False, bias_std=0.0, residual=False,
                    seq_parallel=True, notes="input/output stored as 8 shards [512,4,6144]"),
